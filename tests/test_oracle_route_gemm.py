@@ -1,0 +1,178 @@
+"""Pins of the oracle's routing, permutation, combine, repack and grouped GEMMs
+against brute force on small inputs, round-trip identities and finite
+differences of the whole forward."""
+import numpy as np
+import pytest
+
+from oracle import moe_oracle as O
+
+
+def _brute_route(idx, expert_begin, E, align):
+    T, k = idx.shape
+    counts = [0] * E
+    rank = {}
+    for t in range(T):
+        for j in range(k):
+            e = int(idx[t, j]) - expert_begin
+            if 0 <= e < E:
+                rank[(t, j)] = counts[e]
+                counts[e] += 1
+    offs = [0]
+    for e in range(E):
+        offs.append(offs[-1] + (counts[e] + align - 1) // align * align)
+    row_of = []
+    for t in range(T):
+        for j in range(k):
+            e = int(idx[t, j]) - expert_begin
+            row_of.append(offs[e] + rank[(t, j)] if 0 <= e < E else -1)
+    return counts, offs, row_of
+
+
+@pytest.mark.parametrize("T,k,E,eb,nexp", [(37, 2, 4, 0, 4), (50, 3, 5, 2, 9), (8, 1, 3, 0, 3), (64, 4, 2, 1, 8)])
+def test_route_matches_brute_force(T, k, E, eb, nexp):
+    rng = np.random.default_rng(T * 31 + k)
+    idx = np.stack([rng.permutation(nexp)[:k] for _ in range(T)])
+    rt = O.route(idx, eb, E)
+    counts, offs, row_of = _brute_route(idx, eb, E, O.ALIGN)
+    assert list(rt.counts) == counts
+    assert list(rt.offsets) == offs
+    assert list(rt.row_of) == row_of
+    # tok_of / slot_of are the inverse map, -1 on pad rows
+    for i, r in enumerate(row_of):
+        if r >= 0:
+            assert rt.tok_of[r] == i // k and rt.slot_of[r] == i
+    assert (rt.tok_of >= 0).sum() == sum(counts)
+
+
+def test_route_empty_expert_and_all_on_one():
+    idx = np.zeros((40, 1), dtype=np.int64) + 2      # every token on expert 2
+    rt = O.route(idx, 0, 4)
+    assert list(rt.counts) == [0, 0, 40, 0]
+    assert list(rt.offsets) == [0, 0, 0, 64, 64]
+    assert list(rt.row_of) == list(range(40))
+
+
+def test_permute_unpermute_identity():
+    rng = np.random.default_rng(11)
+    T, H, E = 45, 16, 5
+    x = rng.normal(size=(T, H))
+    idx = rng.integers(0, E, size=(T, 1))
+    rt = O.route(idx, 0, E)
+    xp = O.permute(x, rt)
+    assert np.all(xp[rt.tok_of < 0] == 0)
+    out = O.unpermute_combine(xp, rt.row_of, np.ones((T, 1)))
+    assert np.array_equal(out, x)
+
+
+def test_combine_weighted_sum_brute_force():
+    rng = np.random.default_rng(12)
+    T, H, k, E = 20, 6, 3, 4
+    idx = np.stack([rng.permutation(6)[:k] for _ in range(T)])   # some experts not local
+    p = rng.random((T, k))
+    rt = O.route(idx, 0, E)
+    y = rng.normal(size=(rt.R_pad, H))
+    out = O.unpermute_combine(y, rt.row_of, p)
+    for t in range(T):
+        ref = np.zeros(H)
+        for j in range(k):
+            e = idx[t, j]
+            if e < E:
+                ref += p[t, j] * y[rt.row_of[t * k + j]]
+        assert np.allclose(out[t], ref, rtol=0, atol=1e-14)
+
+
+def test_repack_hand_order_and_bijection():
+    # F = 4, G = 2: packed rows = in0 in1 gate0 gate1 in2 in3 gate2 gate3
+    assert list(O.packed_to_logical(4, 2)) == [0, 1, 4, 5, 2, 3, 6, 7]
+    W = np.arange(2 * 128 * 3).reshape(2, 128, 3)
+    Wp = O.repack_fc1(W, 32)
+    assert np.array_equal(O.unpack_fc1(Wp, 32), W)
+    assert np.array_equal(Wp[1, 32], W[1, 64])       # first gate row of block 0
+    assert np.array_equal(Wp[1, 64], W[1, 32])       # second input block
+
+
+def test_grouped_gemm_triple_loop_two_experts():
+    rng = np.random.default_rng(13)
+    T, H, N = 10, 4, 3
+    idx = rng.integers(0, 2, size=(T, 1))
+    rt = O.route(idx, 0, 2)
+    A = O.permute(rng.normal(size=(T, H)), rt)
+    B = rng.normal(size=(2, N, H))
+    C = O.grouped_gemm_rows(A, B, rt)
+    for r in range(rt.R_pad):
+        e = rt.expert_of_row[r]
+        for n in range(N):
+            ref = 0.0
+            if rt.tok_of[r] >= 0:
+                for h in range(H):
+                    ref += A[r, h] * B[e, n, h]
+            assert abs(C[r, n] - ref) < 1e-12
+
+
+def _toy(act=O.ACT_SWIGLU, seed=14):
+    rng = np.random.default_rng(seed)
+    T, H, F, E, G = 9, 5, 4, 2, 2
+    idx = rng.integers(0, E, size=(T, 1))
+    rt = O.route(idx, 0, E)
+    x = rng.normal(size=(T, H))
+    W1 = rng.normal(size=(E, 2 * F, H)) * 0.5
+    b1 = rng.normal(size=(E, 2 * F)) * 0.1
+    W2 = rng.normal(size=(E, F, H)) * 0.5
+    dY = rng.normal(size=(rt.R_pad, H))
+    return rng, rt, x, W1, b1, W2, dY, F, G
+
+
+@pytest.mark.parametrize("act", [O.ACT_SWIGLU, O.ACT_GEGLU, O.ACT_SREGLU])
+def test_fc1_and_dglu_against_finite_differences(act):
+    """L = sum(dY * (act(x W1^T + b1) @ W2_e)) over real rows.  dglu_bwd must be
+    dL/dpre in packed order (so W2's orientation, the packing and the
+    activation derivative are all checked at once)."""
+    rng, rt, x, W1, b1, W2, dY, F, G = _toy(act)
+    prm = O.ActParams(act)
+    xp = O.permute(x, rt)
+    W1p = O.repack_fc1(W1, G)
+    b1p = O.repack_fc1(b1[..., None], G)[..., 0]
+    fo = O.fc1_glu_fwd(xp, W1p, b1p, rt, prm, G)
+    # recompute pre in float64 (fo.pre_bf16 is rounded)
+    pre = O.grouped_gemm_rows(xp, W1p, rt)
+    for e in range(rt.E):
+        r0, n = rt.offsets[e], rt.counts[e]
+        pre[r0:r0 + n] += b1p[e]
+    pre[rt.tok_of < 0] = 0
+
+    def loss(P):
+        u, g = O.unpack_glu_cols(P, G)
+        y = O.act_fwd(u, g, prm)
+        y[rt.tok_of < 0] = 0
+        return float(np.sum(dY * O.grouped_gemm_rows(y, np.transpose(W2, (0, 2, 1)), rt)))
+
+    d = O.dglu_bwd(dY, W2, pre, rt, prm, G).astype(np.float64)
+    h = 1e-6
+    for r in np.nonzero(rt.tok_of >= 0)[0][:5]:
+        for c in range(2 * F):
+            P1, P2 = pre.copy(), pre.copy()
+            P1[r, c] += h
+            P2[r, c] -= h
+            fd = (loss(P1) - loss(P2)) / (2 * h)
+            assert abs(d[r, c] - fd) <= 1e-4 * max(1.0, abs(fd)), (r, c, d[r, c], fd)
+    # forward: the activation of the unrounded pre-activation
+    u, g = O.unpack_glu_cols(pre, G)
+    ref = O.act_fwd(u, g, prm)
+    ref[rt.tok_of < 0] = 0
+    assert np.allclose(fo.y, ref.astype(np.float32))
+    assert np.all(fo.pre_bf16[rt.tok_of < 0] == 0)
+
+
+def test_wgrad_triple_loop():
+    rng = np.random.default_rng(15)
+    T, H, M = 12, 3, 4
+    idx = rng.integers(0, 3, size=(T, 1))
+    rt = O.route(idx, 0, 3)
+    A = O.permute(rng.normal(size=(T, M)), rt).T
+    B = O.permute(rng.normal(size=(T, H)), rt).T
+    D = O.grouped_wgrad(A, B, rt)
+    for e in range(3):
+        for m in range(M):
+            for n in range(H):
+                ref = sum(A[m, r] * B[n, r] for r in range(rt.R_pad) if rt.expert_of_row[r] == e)
+                assert abs(D[e, m, n] - ref) < 1e-12
