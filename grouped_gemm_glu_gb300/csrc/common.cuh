@@ -1,0 +1,329 @@
+// Device-side building blocks shared by the kernels of libmoeglu: status
+// plumbing, bounded mbarrier waits, TMA loads, tcgen05 (MMA, tensor-memory
+// allocation, loads, copies) and the MX/NVFP4 number-format helpers.
+// Everything targets sm_103a and is written as inline PTX.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp4.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moeglu.h"
+
+namespace moeglu {
+
+// ---------------------------------------------------------------------------
+// Status and time
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void set_status(int32_t* st, int32_t code) {
+  if (st) atomicOr(st, code);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+}
+__device__ __forceinline__ uint32_t mbar_test(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(b)), "r"(parity)
+      : "memory");
+  return ok;
+}
+
+// A wait that gives up.  Every pipeline wait in the persistent kernels goes
+// through this: after `limit_ns` (or once another role of the CTA has given
+// up) it records MOE_ERR_TIMEOUT in the status word, raises the CTA's abort
+// flag and returns false so that the caller can leave its loop.
+struct WaitGuard {
+  volatile int* abort;
+  int32_t* status;
+  uint64_t limit_ns;
+};
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, const WaitGuard& g) {
+  if (mbar_test(b, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test(b, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*g.abort) return false;
+      if (globaltimer_ns() - t0 > g.limit_ns) {
+        *g.abort = 1;
+        set_status(g.status, MOE_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// TMA (bulk tensor copies global -> shared, completion on an mbarrier)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uint64_t* bar, int32_t c0,
+                                            int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar, int32_t c0,
+                                            int32_t c1, int32_t c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
+      "[%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05: tensor memory, MMA, commit, loads, copies
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Arrives once on `bar` when every tcgen05 operation this thread issued
+// before it has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulator.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Block-scaled E4M3 x E4M3 MMA with E8M0 scales per 32 elements of K read
+// from tensor memory.
+__device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Copies 32 rows x 16 bytes of shared memory into 4 tensor-memory columns of
+// each of the four 32-lane sub-partitions (the same data in each).
+__device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand tile stored as rows of
+// 128 bytes with the 128-byte swizzle (8-row atoms of 1024 bytes).
+__device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(1024u >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Descriptor without swizzle (scale-factor copies): 8-row x 16-byte atoms,
+// `sbo` bytes between atoms.
+__device__ __forceinline__ uint64_t sdesc_noswizzle(uint32_t saddr, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(sbo >> 4) << 32) | (1ull << 46);
+}
+
+// Instruction descriptors (kind::f16 with bf16 operands and fp32 accumulate;
+// kind::mxf8f6f4 with E4M3 operands and E8M0 scales).  Both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_mxf8_e8m0(int M, int N) {
+  return ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ uint32_t idesc_with_sf_ids(uint32_t idesc, uint32_t a_id, uint32_t b_id) {
+  return idesc | (b_id << 4) | (a_id << 29);
+}
+
+// 32 lanes x 32 consecutive 32-bit columns per thread (thread i <- lane
+// base+i), followed by the wait, so the registers are valid on return.
+#define MOEGLU_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : MOEGLU_R8(0), MOEGLU_R8(8), MOEGLU_R8(16), MOEGLU_R8(24)
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+#undef MOEGLU_R8
+
+// ---------------------------------------------------------------------------
+// Number formats
+// ---------------------------------------------------------------------------
+// |x| as ordered unsigned bits (NaN sorts above +Inf).
+__device__ __forceinline__ uint32_t abs_bits(float x) { return __float_as_uint(x) & 0x7FFFFFFFu; }
+
+// E8M0 block scale from the block's amax bits: OCP MX shared exponent
+// floor(log2 amax) - 8 (E4M3 emax), clamped to the E8M0 range; 0xFF (NaN)
+// for a non-finite amax.  floor(log2) of a normal float is its exponent
+// field - 127; subnormal amax clamps to the floor.
+__device__ __forceinline__ uint32_t e8m0_from_amax_bits(uint32_t amax_bits) {
+  const uint32_t ex = amax_bits >> 23;
+  return ex == 0xFFu ? 0xFFu : (ex > 8u ? ex - 8u : 0u);
+}
+// 2^(127 - byte) as a float (the exact multiplier that brings the block
+// into E4M3 range); valid for byte <= 253.
+__device__ __forceinline__ float mx_inv_scale(uint32_t sbyte) { return __uint_as_float((254u - sbyte) << 23); }
+
+// Two floats -> two E4M3 bytes (round to nearest even, saturating), a in
+// the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);  // a -> low half
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Quantises 32 floats of one MX block: returns the scale byte and writes
+// the 32 codes (8 words, element 0 in the low byte of word 0).
+__device__ __forceinline__ uint32_t mx_quant_block32(const float* v, uint32_t* codes) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) m = max(m, abs_bits(v[i]));
+  const uint32_t sb = e8m0_from_amax_bits(m);
+  if (sb == 0xFFu) {
+#pragma unroll
+    for (int w = 0; w < 8; ++w) codes[w] = 0x7F7F7F7Fu;
+    return sb;
+  }
+  const float inv = mx_inv_scale(sb);
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const uint32_t lo = e4m3x2(v[4 * w] * inv, v[4 * w + 1] * inv);
+    const uint32_t hi = e4m3x2(v[4 * w + 2] * inv, v[4 * w + 3] * inv);
+    codes[w] = lo | (hi << 16);
+  }
+  return sb;
+}
+
+// ---------------------------------------------------------------------------
+// Activations (fp32).  Textbook GLU family; see moe_act_t.
+// ---------------------------------------------------------------------------
+struct GluParams {
+  int act;
+  float alpha, up_offset, gate_lo, gate_hi, up_lo, up_hi;
+};
+
+__device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + __expf(-z)); }
+__device__ __forceinline__ float phi_cdf(float z) { return 0.5f * (1.0f + erff(z * 0.70710678118654752f)); }
+__device__ __forceinline__ float phi_pdf(float z) { return 0.39894228040143268f * __expf(-0.5f * z * z); }
+
+// forward: y = act(u, g); sReLU uses u only
+__device__ __forceinline__ float act_fwd(const GluParams& p, float u, float g) {
+  if (p.act == MOE_ACT_SRELU) {
+    const float r = fmaxf(u, 0.0f);
+    return r * r;
+  }
+  const float gc = fminf(fmaxf(g, p.gate_lo), p.gate_hi);
+  const float uc = fminf(fmaxf(u, p.up_lo), p.up_hi) + p.up_offset;
+  float f;
+  if (p.act == MOE_ACT_SWIGLU) {
+    f = gc * sigmoidf_(p.alpha * gc);
+  } else if (p.act == MOE_ACT_GEGLU) {
+    f = gc * phi_cdf(gc);
+  } else if (p.act == MOE_ACT_GEGLU_TANH) {
+    const float k = 0.79788456080286536f;
+    f = 0.5f * gc * (1.0f + tanhf(k * (gc + 0.044715f * gc * gc * gc)));
+  } else {  // sReGLU
+    const float r = fmaxf(gc, 0.0f);
+    f = r * r;
+  }
+  return uc * f;
+}
+
+// backward: (du, dg) for incoming dy
+__device__ __forceinline__ void act_bwd(const GluParams& p, float u, float g, float dy, float& du, float& dg) {
+  if (p.act == MOE_ACT_SRELU) {
+    du = dy * 2.0f * fmaxf(u, 0.0f);
+    dg = 0.0f;
+    return;
+  }
+  const float gc = fminf(fmaxf(g, p.gate_lo), p.gate_hi);
+  const float uc = fminf(fmaxf(u, p.up_lo), p.up_hi) + p.up_offset;
+  const float mg = (g >= p.gate_lo && g <= p.gate_hi) ? 1.0f : 0.0f;
+  const float mu = (u >= p.up_lo && u <= p.up_hi) ? 1.0f : 0.0f;
+  float f, df;
+  if (p.act == MOE_ACT_SWIGLU) {
+    const float s = sigmoidf_(p.alpha * gc);
+    f = gc * s;
+    df = s * (1.0f + p.alpha * gc * (1.0f - s));
+  } else if (p.act == MOE_ACT_GEGLU) {
+    const float c = phi_cdf(gc);
+    f = gc * c;
+    df = c + gc * phi_pdf(gc);
+  } else if (p.act == MOE_ACT_GEGLU_TANH) {
+    const float k = 0.79788456080286536f;
+    const float t = tanhf(k * (gc + 0.044715f * gc * gc * gc));
+    f = 0.5f * gc * (1.0f + t);
+    df = 0.5f * (1.0f + t) + 0.5f * gc * (1.0f - t * t) * k * (1.0f + 3.0f * 0.044715f * gc * gc);
+  } else {
+    const float r = fmaxf(gc, 0.0f);
+    f = r * r;
+    df = 2.0f * r;
+  }
+  du = dy * f * mu;
+  dg = dy * uc * df * mg;
+}
+
+}  // namespace moeglu

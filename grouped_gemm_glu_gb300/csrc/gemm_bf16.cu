@@ -1,0 +1,638 @@
+// Persistent grouped GEMM on the 5th-generation tensor cores (tcgen05) with
+// bf16 operands and the activation fused into the epilogue:
+//   forward  GroupGemm + Activation + Quantize/Transpose
+//   backward GroupGemm + dActivation + Quantize/Transpose
+// ([MoE-Fusion] "Boosting MoE Training Throughput with Advanced Fusion
+// Kernels": the three-kernel family; "Optimizing GLU via fused GEMM
+// epilogues" (Fig. 2): repacked weights put matching input and gate columns
+// in one tile, so the epilogue combines them without a global round trip;
+// "Fusing MXFP8 and NVFP4 quantisation": the MXFP8 output and its transposed
+// copy are produced inside the GEMM kernel; "Eliminating host-device
+// synchronisation": the per-expert row counts are read from device memory by
+// the kernel's own tile scheduler.  [MegaMoE] §4.2: producer / consumer warp
+// specialisation over a multi-stage shared-memory ring; §5.3: tails masked.)
+//
+// CTA = 6 warps, one CTA per SM, persistent over tiles t = blockIdx.x +
+// i*gridDim.x (tiles ordered expert-major, then N, then M so that the CTAs
+// working at one time share weight tiles in L2):
+//   warps 0-3  epilogue: TMEM -> registers (thread = accumulator row),
+//              bias, activation, MXFP8 row + column quantisation, stores
+//   warp  4    TMA producer (one thread): A = activations [rows][K] box
+//              128x64, B = weights [E][N][K] box 256x64, 128-byte swizzle,
+//              STAGES-deep ring of full/empty mbarriers
+//   warp  5    TMEM owner + MMA issuer (one thread): tcgen05.mma kind::f16,
+//              M=128 N=256 K=16, accumulator double-buffered in TMEM
+//              (2 x 256 columns), tcgen05.commit frees smem stages and
+//              hands finished accumulators to the epilogue
+// Every wait is bounded (MOE_ERR_TIMEOUT + early exit, never a trap).
+#include "common.cuh"
+#include "host_common.h"
+
+namespace moeglu {
+namespace g16 {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int EPI_WARPS = 4;
+constexpr int THREADS = (EPI_WARPS + 2) * 32;
+constexpr int PRODUCER_WARP = 4, MMA_WARP = 5;
+constexpr int A_TILE = BM * BK * 2;
+constexpr int B_TILE = BN * BK * 2;
+constexpr int STAGE_BYTES = A_TILE + B_TILE;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int E_MAX = 1024;
+constexpr int SCRATCH_PER_WARP = 1024;
+constexpr int OFF_SCRATCH = STAGES * STAGE_BYTES;
+constexpr int OFF_PREF = OFF_SCRATCH + EPI_WARPS * SCRATCH_PER_WARP;
+constexpr int OFF_BARS = OFF_PREF + (E_MAX + 2) * 4;
+constexpr int NUM_BARS = 2 * STAGES + 5;
+constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
+constexpr int SMEM_BYTES = 1024 + OFF_MISC + 64;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+
+enum Mode { FWD_GLU = 0, FWD_ELT = 1, FWD_PRE = 2, BWD_GLU = 3, BWD_ELT = 4 };
+
+struct Args {
+  const int32_t* counts;
+  const int32_t* offsets;
+  int E, K, N_gemm, F, N1, R_cap, n_tiles_n, out_N;
+  const uint16_t* bias;    // [E][N1] (forward), may be null
+  const float* row_scale;  // [R_cap], may be null
+  const uint16_t* pre_in;  // backward: saved pre-activation [R_cap][N1]
+  GluParams prm;
+  int out_mode;
+  uint8_t* q_row;
+  uint8_t* s_row;
+  uint8_t* q_col;
+  uint8_t* s_col;
+  uint16_t* y;
+  float* amax;
+  uint16_t* pre_out;
+  int32_t* status;
+  uint64_t wait_ns;
+};
+
+struct Tile {
+  int e, m_idx, n_idx, row0, rows_valid, rows_pad;
+};
+
+__device__ __forceinline__ Tile decode_tile(int t, const int32_t* pref, int E, int n_tiles_n,
+                                            const int32_t* counts, const int32_t* offsets, int R_cap) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pref[mid] * n_tiles_n <= t) lo = mid; else hi = mid - 1;
+  }
+  Tile ti;
+  ti.e = lo;
+  const int mt = pref[lo + 1] - pref[lo];
+  const int local = t - pref[lo] * n_tiles_n;
+  ti.n_idx = local / mt;
+  ti.m_idx = local - ti.n_idx * mt;
+  const int cnt = __ldg(counts + lo);
+  ti.row0 = __ldg(offsets + lo) + ti.m_idx * BM;
+  ti.rows_valid = min(BM, cnt - ti.m_idx * BM);
+  ti.rows_pad = min(BM, ((cnt + 31) & ~31) - ti.m_idx * BM);
+  // never touch rows at or past R_cap, whatever counts/offsets hold
+  ti.rows_pad = ti.row0 < 0 ? 0 : max(0, min(ti.rows_pad, R_cap - ti.row0));
+  ti.rows_valid = min(ti.rows_valid, ti.rows_pad);
+  return ti;
+}
+
+// One 32-column block of activation results of one row -> its outputs.
+// y: 32 fp32 values (0 on pad rows).  col0: first output column (multiple
+// of 32).  row_ok: this thread's row lies inside the padded segment.
+// The column-wise MXFP8 path needs the whole warp (the warp's 32 rows are
+// one column block).
+__device__ __forceinline__ void emit_block(const Args& a, const float* y, int col0, int row, int rb, bool row_ok,
+                                           uint8_t* scratch, int lane, uint32_t& amax_bits) {
+  const int N = a.out_N;
+  if (a.out_mode == MOE_OUT_MXFP8) {
+    uint32_t codes[8];
+    const uint32_t sb = mx_quant_block32(y, codes);
+    if (row_ok) {
+      uint4* dst = reinterpret_cast<uint4*>(a.q_row + (size_t)row * N + col0);
+      dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+      dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+      a.s_row[(size_t)row * (N / 32) + col0 / 32] = (uint8_t)sb;
+    }
+    if (a.q_col != nullptr) {
+      uint32_t my_sb = 0;
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        const uint32_t s0 = e8m0_from_amax_bits(__reduce_max_sync(0xFFFFFFFFu, abs_bits(y[i])));
+        const uint32_t s1 = e8m0_from_amax_bits(__reduce_max_sync(0xFFFFFFFFu, abs_bits(y[i + 1])));
+        if (lane == i) my_sb = s0;
+        if (lane == i + 1) my_sb = s1;
+        uint32_t c2 = e4m3x2(y[i] * mx_inv_scale(min(s0, 253u)), y[i + 1] * mx_inv_scale(min(s1, 253u)));
+        if (s0 == 0xFFu) c2 = (c2 & 0xFF00u) | 0x7Fu;
+        if (s1 == 0xFFu) c2 = (c2 & 0x00FFu) | 0x7F00u;
+        scratch[i * 32 + lane] = (uint8_t)(c2 & 0xFFu);
+        scratch[(i + 1) * 32 + lane] = (uint8_t)(c2 >> 8);
+      }
+      __syncwarp();
+      const uint4* src = reinterpret_cast<const uint4*>(scratch + lane * 32);
+      const uint4 w0 = src[0], w1 = src[1];
+      uint4* dst = reinterpret_cast<uint4*>(a.q_col + (size_t)(col0 + lane) * a.R_cap + rb);
+      dst[0] = w0;
+      dst[1] = w1;
+      a.s_col[(size_t)(col0 + lane) * (a.R_cap / 32) + rb / 32] = (uint8_t)my_sb;
+      __syncwarp();
+    }
+  } else {
+    if (row_ok) {
+      uint4* dst = reinterpret_cast<uint4*>(a.y + (size_t)row * N + col0);
+#pragma unroll
+      for (int w = 0; w < 4; ++w)
+        dst[w] = make_uint4(pack_bf16x2(y[8 * w], y[8 * w + 1]), pack_bf16x2(y[8 * w + 2], y[8 * w + 3]),
+                            pack_bf16x2(y[8 * w + 4], y[8 * w + 5]), pack_bf16x2(y[8 * w + 6], y[8 * w + 7]));
+    }
+    if (a.out_mode == MOE_OUT_NVFP4) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) amax_bits = max(amax_bits, abs_bits(y[i]));
+    }
+  }
+}
+
+__device__ __forceinline__ void load_bf16x32(const uint16_t* p, float* v) {
+  const uint4* s = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const uint4 q = __ldg(s + w);
+    v[8 * w + 0] = bf16_lo(q.x);
+    v[8 * w + 1] = bf16_hi(q.x);
+    v[8 * w + 2] = bf16_lo(q.y);
+    v[8 * w + 3] = bf16_hi(q.y);
+    v[8 * w + 4] = bf16_lo(q.z);
+    v[8 * w + 5] = bf16_hi(q.z);
+    v[8 * w + 6] = bf16_lo(q.w);
+    v[8 * w + 7] = bf16_hi(q.w);
+  }
+}
+
+__device__ __forceinline__ void store_bf16x32(uint16_t* p, const float* v, bool zero) {
+  uint4* d = reinterpret_cast<uint4*>(p);
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    if (zero) {
+      d[w] = make_uint4(0, 0, 0, 0);
+    } else {
+      d[w] = make_uint4(pack_bf16x2(v[8 * w], v[8 * w + 1]), pack_bf16x2(v[8 * w + 2], v[8 * w + 3]),
+                        pack_bf16x2(v[8 * w + 4], v[8 * w + 5]), pack_bf16x2(v[8 * w + 6], v[8 * w + 7]));
+    }
+  }
+}
+
+template <int MODE>
+__device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& ti, uint32_t tacc, int q, int lane,
+                                              uint8_t* scratch, uint32_t& amax_bits) {
+  if (q * 32 >= ti.rows_pad) return;  // no row of this warp lies in the padded segment
+  const int r_local = q * 32 + lane;
+  const bool real = r_local < ti.rows_valid;
+  const bool row_ok = r_local < ti.rows_pad;  // always true here, kept for clarity
+  const int row = ti.row0 + r_local;
+  const int rb = ti.row0 + q * 32;
+  const float rs = (a.row_scale != nullptr && real) ? __ldg(a.row_scale + row) : 1.0f;
+
+  if (MODE == FWD_GLU) {
+#pragma unroll 1
+    for (int j = 0; j < BN / 64; ++j) {
+      const int f0 = ti.n_idx * (BN / 2) + j * 32;
+      if (f0 >= a.F) break;
+      const int p0 = ti.n_idx * BN + j * 64;
+      float v[64];
+      tmem_ld32(tacc + j * 64, v);
+      tmem_ld32(tacc + j * 64 + 32, v + 32);
+      if (a.bias != nullptr) {
+        float b[32];
+        const uint16_t* bp = a.bias + (size_t)ti.e * a.N1 + p0;
+        load_bf16x32(bp, b);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] += b[i];
+        load_bf16x32(bp + 32, b);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[32 + i] += b[i];
+      }
+      if (a.pre_out != nullptr && row_ok) {
+        uint16_t* pp = a.pre_out + (size_t)row * a.N1 + p0;
+        store_bf16x32(pp, v, !real);
+        store_bf16x32(pp + 32, v + 32, !real);
+      }
+      float yv[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) yv[i] = real ? act_fwd(a.prm, v[i], v[32 + i]) * rs : 0.0f;
+      emit_block(a, yv, f0, row, rb, row_ok, scratch, lane, amax_bits);
+    }
+  } else if (MODE == FWD_ELT || MODE == FWD_PRE) {
+#pragma unroll 1
+    for (int j = 0; j < BN / 32; ++j) {
+      const int c0 = ti.n_idx * BN + j * 32;
+      if (c0 >= a.N_gemm) break;
+      float v[32];
+      tmem_ld32(tacc + j * 32, v);
+      if (a.bias != nullptr) {
+        float b[32];
+        load_bf16x32(a.bias + (size_t)ti.e * a.N1 + c0, b);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] += b[i];
+      }
+      if (a.pre_out != nullptr && row_ok) store_bf16x32(a.pre_out + (size_t)row * a.N1 + c0, v, !real);
+      if (MODE == FWD_ELT) {
+        float yv[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) yv[i] = real ? act_fwd(a.prm, v[i], 0.0f) * rs : 0.0f;
+        emit_block(a, yv, c0, row, rb, row_ok, scratch, lane, amax_bits);
+      }
+    }
+  } else if (MODE == BWD_GLU) {
+#pragma unroll 1
+    for (int j = 0; j < BN / 32; ++j) {
+      const int f0 = ti.n_idx * BN + j * 32;
+      if (f0 >= a.F) break;
+      const int p0 = (f0 / 32) * 64;
+      float d[32], u[32], g[32];
+      tmem_ld32(tacc + j * 32, d);
+      if (real) {
+        load_bf16x32(a.pre_in + (size_t)row * a.N1 + p0, u);
+        load_bf16x32(a.pre_in + (size_t)row * a.N1 + p0 + 32, g);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float du, dg;
+          act_bwd(a.prm, u[i], g[i], d[i] * rs, du, dg);
+          u[i] = du;
+          g[i] = dg;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) u[i] = g[i] = 0.0f;
+      }
+      emit_block(a, u, p0, row, rb, row_ok, scratch, lane, amax_bits);
+      emit_block(a, g, p0 + 32, row, rb, row_ok, scratch, lane, amax_bits);
+    }
+  } else {  // BWD_ELT
+#pragma unroll 1
+    for (int j = 0; j < BN / 32; ++j) {
+      const int f0 = ti.n_idx * BN + j * 32;
+      if (f0 >= a.F) break;
+      float d[32], x[32];
+      tmem_ld32(tacc + j * 32, d);
+      if (real) {
+        load_bf16x32(a.pre_in + (size_t)row * a.N1 + f0, x);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float du, dg;
+          act_bwd(a.prm, x[i], 0.0f, d[i] * rs, du, dg);
+          x[i] = du;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] = 0.0f;
+      }
+      emit_block(a, x, f0, row, rb, row_ok, scratch, lane, amax_bits);
+    }
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1)
+    k_grouped_bf16(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Args a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* tiles = smem;
+  uint8_t* scratch_all = smem + OFF_SCRATCH;
+  int32_t* pref = reinterpret_cast<int32_t*>(smem + OFF_PREF);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BARS);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* acc_full = bars + 2 * STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* mma_done = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = a.E;
+
+  if (warp == PRODUCER_WARP && lane == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full + b, 1);
+      mbar_init(acc_empty + b, EPI_WARPS);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_async_shared();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  // m-tiles per expert -> exclusive prefix pref[0..E]
+  for (int e = threadIdx.x; e < E; e += THREADS) pref[e + 1] = (__ldg(a.counts + e) + BM - 1) / BM;
+  if (threadIdx.x == 0) pref[0] = 0;
+  __syncthreads();
+  if (warp == 0) {
+    const int per = (E + 31) / 32;
+    const int beg = 1 + lane * per, end = min(E + 1, beg + per);
+    int s = 0;
+    for (int i = beg; i < end; ++i) s += pref[i];
+    int incl = s;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    int run = incl - s;
+    for (int i = beg; i < end; ++i) {
+      run += pref[i];
+      pref[i] = run;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  // capacity guard: a routing that overflowed R_cap produces no tiles
+  const bool over = __ldg(a.offsets + E) > a.R_cap;
+  if (over && threadIdx.x == 0) set_status(a.status, MOE_ERR_CAPACITY);
+  const int total = over ? 0 : pref[E] * a.n_tiles_n;
+  const int num_kb = a.K / BK;
+  WaitGuard guard{abort_flag, a.status, a.wait_ns};
+
+  if (warp == PRODUCER_WARP) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, issued_parity = 0;  // per stage: armed and its parity
+      for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        const Tile ti = decode_tile(t, pref, E, a.n_tiles_n, a.counts, a.offsets, a.R_cap);
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(empty + stage, phase ^ 1u, guard)) {
+            ok = false;
+            break;
+          }
+          uint8_t* a_dst = tiles + stage * STAGE_BYTES;
+          mbar_arrive_expect_tx(full + stage, STAGE_BYTES);
+          tma_load_2d(a_dst, &tmA, full + stage, kb * BK, ti.row0);
+          tma_load_3d(a_dst + A_TILE, &tmB, full + stage, kb * BK, ti.n_idx * BN, ti.e);
+          issued |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+      if (*abort_flag) {
+        // give the copies already in flight a bounded chance to land
+        volatile int never = 0;
+        WaitGuard drain{&never, a.status, 100000000ull};
+        for (int s = 0; s < STAGES; ++s)
+          if (issued & (1u << s)) mbar_wait(full + s, (issued_parity >> s) & 1u, drain);
+      }
+    }
+  } else if (warp == MMA_WARP) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int lt = 0;
+      for (int t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
+        const int buf = lt & 1;
+        const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
+        if (!mbar_wait(acc_empty + buf, aph ^ 1u, guard)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(full + stage, phase, guard)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(tiles + stage * STAGE_BYTES);
+          const uint32_t b_addr = a_addr + A_TILE;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            umma_bf16(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32), sdesc_kmajor_sw128(b_addr + k * 32), idesc,
+                      (kb | k) != 0 ? 1u : 0u);
+          }
+          tc_commit(empty + stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(acc_full + buf);
+      }
+      // all MMAs issued by this thread have completed once this arrives
+      tc_commit(mma_done);
+      volatile int never = 0;
+      WaitGuard drain{&never, a.status, 100000000ull};
+      mbar_wait(mma_done, 0, drain);
+    }
+  } else {
+    // epilogue warps 0..3: warp q reads TMEM lanes 32q..32q+31
+    const int q = warp;
+    uint8_t* scratch = scratch_all + q * SCRATCH_PER_WARP;
+    uint32_t amax_bits = 0;
+    int lt = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
+      const int buf = lt & 1;
+      const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(acc_full + buf, aph, guard) ? 1 : 0;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const Tile ti = decode_tile(t, pref, E, a.n_tiles_n, a.counts, a.offsets, a.R_cap);
+      const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
+      epilogue_tile<MODE>(a, ti, tacc, q, lane, scratch, amax_bits);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty + buf);
+    }
+    if (a.out_mode == MOE_OUT_NVFP4 && a.amax != nullptr) {
+      const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, amax_bits);
+      if (lane == 0 && m != 0) atomicMax(reinterpret_cast<int*>(a.amax), (int)m);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+template <int MODE>
+static moe_status_t launch(const void* A, const void* B, const Args& args, int sm_margin, cudaStream_t stream) {
+  CUtensorMap tmA, tmB;
+  {
+    const uint64_t dims[2] = {(uint64_t)args.K, (uint64_t)args.R_cap};
+    const uint64_t strides[1] = {(uint64_t)args.K * 2};
+    const uint32_t box[2] = {BK, BM};
+    if (!encode_tmap(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+      return MOE_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)args.K, (uint64_t)args.N_gemm, (uint64_t)args.E};
+    const uint64_t strides[2] = {(uint64_t)args.K * 2, (uint64_t)args.N_gemm * args.K * 2};
+    const uint32_t box[3] = {BK, BN, 1};
+    if (!encode_tmap(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, B, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+      return MOE_ERR_CUDA;
+  }
+  const void* kfn = (const void*)k_grouped_bf16<MODE>;
+  if (!set_smem_limit(kfn, SMEM_BYTES)) return MOE_ERR_CUDA;
+  const int sms = sm_count();
+  int grid = sms - sm_margin;
+  const long long tiles_bound = ((long long)args.R_cap / BM + args.E) * args.n_tiles_n;
+  if (grid > tiles_bound) grid = (int)tiles_bound;
+  if (grid < 1) grid = 1;
+  k_grouped_bf16<MODE><<<grid, THREADS, SMEM_BYTES, stream>>>(tmA, tmB, args);
+  count_launch();
+  return launch_status();
+}
+
+static GluParams to_glu(const moe_glu_params_t* p) {
+  GluParams g;
+  g.act = p->act;
+  g.alpha = p->alpha;
+  g.up_offset = p->up_offset;
+  g.gate_lo = p->gate_lo;
+  g.gate_hi = p->gate_hi;
+  g.up_lo = p->up_lo;
+  g.up_hi = p->up_hi;
+  return g;
+}
+
+static bool out_ok(int out_mode, const moe_act_out_t* o) {
+  if (!o) return false;
+  if (out_mode == MOE_OUT_MXFP8) {
+    if (!o->q_row || !o->s_row) return false;
+    if ((o->q_col == nullptr) != (o->s_col == nullptr)) return false;
+    if (!aligned16(o->q_row) || (o->q_col && !aligned16(o->q_col))) return false;
+    return true;
+  }
+  if (out_mode == MOE_OUT_BF16) return o->y && aligned16(o->y);
+  if (out_mode == MOE_OUT_NVFP4) return o->y && aligned16(o->y) && o->amax;
+  return false;
+}
+
+}  // namespace g16
+}  // namespace moeglu
+
+using namespace moeglu;
+
+extern "C" moe_status_t moe_grouped_fc1_glu_quant_fwd(const moe_bf16* x_perm, const moe_bf16* W1p,
+                                                      const moe_bf16* b1p, const float* row_scale,
+                                                      const int32_t* counts, const int32_t* offsets, int E, int H,
+                                                      int F, int R_cap, const moe_glu_params_t* params,
+                                                      int out_mode, const moe_act_out_t* out, int sm_margin,
+                                                      int32_t* status, moe_stream_t stream) {
+  using namespace g16;
+  if (!x_perm || !W1p || !counts || !offsets || !params || !out) return MOE_ERR_ARG;
+  if (E <= 0 || E > E_MAX || H <= 0 || (H % BK) || F <= 0 || (F % 32) || R_cap <= 0 || (R_cap % BM)) return MOE_ERR_ARG;
+  if (!aligned16(x_perm) || !aligned16(W1p) || (b1p && !aligned16(b1p))) return MOE_ERR_ARG;
+  if (sm_margin < 0) return MOE_ERR_ARG;
+  const int act = params->act;
+  if (act < MOE_ACT_SWIGLU || act > MOE_ACT_NONE) return MOE_ERR_ARG;
+  const bool gated = act == MOE_ACT_SWIGLU || act == MOE_ACT_GEGLU || act == MOE_ACT_GEGLU_TANH || act == MOE_ACT_SREGLU;
+  const bool none = act == MOE_ACT_NONE;
+  Args a{};
+  a.counts = counts;
+  a.offsets = offsets;
+  a.E = E;
+  a.K = H;
+  a.F = F;
+  a.R_cap = R_cap;
+  a.bias = b1p;
+  a.row_scale = row_scale;
+  a.prm = to_glu(params);
+  a.out_mode = out_mode;
+  a.status = status;
+  a.wait_ns = g_wait_limit_ns.load();
+  if (none) {
+    // unfused path: the GEMM writes the bf16 pre-activation of all N1 = F columns given
+    if (!out->pre || !aligned16(out->pre)) return MOE_ERR_ARG;
+    a.N1 = F;  // for MOE_ACT_NONE, F is the full GEMM width
+    a.N_gemm = F;
+    a.out_N = F;
+    a.out_mode = MOE_OUT_BF16;
+    a.pre_out = reinterpret_cast<uint16_t*>(out->pre);
+    a.n_tiles_n = (F + BN - 1) / BN;
+    return launch<FWD_PRE>(x_perm, W1p, a, sm_margin, as_stream(stream));
+  }
+  if (!out_ok(out_mode, out)) return MOE_ERR_ARG;
+  if (out->pre && !aligned16(out->pre)) return MOE_ERR_ARG;
+  a.q_row = out->q_row;
+  a.s_row = out->s_row;
+  a.q_col = out->q_col;
+  a.s_col = out->s_col;
+  a.y = reinterpret_cast<uint16_t*>(out->y);
+  a.amax = out->amax;
+  a.pre_out = reinterpret_cast<uint16_t*>(out->pre);
+  a.out_N = F;
+  if (gated) {
+    a.N1 = 2 * F;
+    a.N_gemm = 2 * F;
+    a.n_tiles_n = (2 * F + BN - 1) / BN;
+    return launch<FWD_GLU>(x_perm, W1p, a, sm_margin, as_stream(stream));
+  }
+  a.N1 = F;
+  a.N_gemm = F;
+  a.n_tiles_n = (F + BN - 1) / BN;
+  return launch<FWD_ELT>(x_perm, W1p, a, sm_margin, as_stream(stream));
+}
+
+extern "C" moe_status_t moe_grouped_dglu_quant_bwd(const moe_bf16* dY_perm, const moe_bf16* W2, const moe_bf16* pre,
+                                                   const float* row_scale, const int32_t* counts,
+                                                   const int32_t* offsets, int E, int H, int F, int R_cap,
+                                                   const moe_glu_params_t* params, int out_mode,
+                                                   const moe_act_out_t* dfc1, int sm_margin, int32_t* status,
+                                                   moe_stream_t stream) {
+  using namespace g16;
+  if (!dY_perm || !W2 || !pre || !counts || !offsets || !params || !dfc1) return MOE_ERR_ARG;
+  if (E <= 0 || E > E_MAX || H <= 0 || (H % BK) || F <= 0 || (F % 32) || R_cap <= 0 || (R_cap % BM)) return MOE_ERR_ARG;
+  if (!aligned16(dY_perm) || !aligned16(W2) || !aligned16(pre)) return MOE_ERR_ARG;
+  if (sm_margin < 0) return MOE_ERR_ARG;
+  const int act = params->act;
+  if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SREGLU) return MOE_ERR_ARG;
+  if (out_mode == MOE_OUT_NVFP4) return MOE_ERR_UNSUPPORTED;
+  if (!out_ok(out_mode, dfc1)) return MOE_ERR_ARG;
+  const bool gated = act != MOE_ACT_SRELU;
+  Args a{};
+  a.counts = counts;
+  a.offsets = offsets;
+  a.E = E;
+  a.K = H;
+  a.F = F;
+  a.R_cap = R_cap;
+  a.N_gemm = F;
+  a.N1 = gated ? 2 * F : F;
+  a.n_tiles_n = (F + BN - 1) / BN;
+  a.out_N = a.N1;
+  a.row_scale = row_scale;
+  a.pre_in = reinterpret_cast<const uint16_t*>(pre);
+  a.prm = to_glu(params);
+  a.out_mode = out_mode;
+  a.q_row = dfc1->q_row;
+  a.s_row = dfc1->s_row;
+  a.q_col = dfc1->q_col;
+  a.s_col = dfc1->s_col;
+  a.y = reinterpret_cast<uint16_t*>(dfc1->y);
+  a.status = status;
+  a.wait_ns = g_wait_limit_ns.load();
+  if (gated) return launch<BWD_GLU>(dY_perm, W2, a, sm_margin, as_stream(stream));
+  return launch<BWD_ELT>(dY_perm, W2, a, sm_margin, as_stream(stream));
+}

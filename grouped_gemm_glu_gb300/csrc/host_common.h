@@ -1,0 +1,44 @@
+// Host-side helpers of libmoeglu: TMA descriptor encoding (through the
+// driver entry point, so the library does not link libcuda), device
+// properties, launch accounting and argument checks.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "moeglu.h"
+
+namespace moeglu {
+
+extern std::atomic<uint64_t> g_launches;  // kernels launched by this library
+extern std::atomic<uint64_t> g_wait_limit_ns;
+
+inline void count_launch(int n = 1) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+inline cudaStream_t as_stream(moe_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// Opts a kernel into `bytes` of dynamic shared memory (once per kernel and
+// device; returns false on failure).
+bool set_smem_limit(const void* kernel, int bytes);
+
+// Encodes a tiled TMA descriptor for a row-major tensor with dims[0] the
+// contiguous dimension.  rank 2 or 3; strides_bytes has rank-1 entries.
+bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
+                 const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                 CUtensorMapSwizzle swizzle);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline moe_status_t launch_status() {
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moeglu

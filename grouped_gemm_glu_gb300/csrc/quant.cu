@@ -1,0 +1,260 @@
+// Standalone memory-bound kernels around the fused GEMMs:
+//   k_quant_rows / k_quant_cols  MXFP8 quantisation of a bf16 tensor along its
+//                                rows or (transposed) columns: the weight
+//                                casts, the column-wise copies the weight-
+//                                gradient GEMMs read, and the quantize step
+//                                of the unfused path
+//   k_nvfp4_cast                 NVFP4 cast after the forward's bf16 + amax
+//                                output
+//   k_glu_act                    activation of the unfused path
+// ([MoE-Fusion] "Boosting MoE Training Throughput with Advanced Fusion
+// Kernels", "Fusing MXFP8 and NVFP4 quantisation": MXFP8 = row-wise output
+// plus a transposed copy; NVFP4 = bf16 output plus per-tensor amax.
+// [MegaMoE] §2.3: E4M3 elements with per-block scales.)
+#include "common.cuh"
+#include "host_common.h"
+
+namespace moeglu {
+
+constexpr int QE_MAX = 1024;
+
+// Number of real rows (0..32) of the 32-row block starting at r0, given the
+// expert segment map in shared memory; -1 if r0 >= offsets[E].
+__device__ __forceinline__ int block_real_rows(int r0, const int32_t* s_off, const int32_t* s_cnt, int E) {
+  if (r0 >= s_off[E]) return -1;
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_off[mid] <= r0) lo = mid; else hi = mid - 1;
+  }
+  return max(0, min(32, s_off[lo] + s_cnt[lo] - r0));
+}
+
+__device__ __forceinline__ void load_seg(const int32_t* counts, const int32_t* offsets, int E, int32_t* s_off,
+                                         int32_t* s_cnt) {
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    s_off[e] = offsets[e];
+    if (e < E) s_cnt[e] = counts[e];
+  }
+  __syncthreads();
+}
+
+// Row-wise: one thread per 32-element block.  rows >= offsets[E] untouched,
+// rows of an expert past its count are quantised as zeros.
+__global__ void __launch_bounds__(256) k_quant_rows(const uint16_t* __restrict__ src, int G, int R, int Cc,
+                                                    const int32_t* __restrict__ counts,
+                                                    const int32_t* __restrict__ offsets, int E,
+                                                    uint8_t* __restrict__ q, uint8_t* __restrict__ s) {
+  __shared__ int32_t s_off[QE_MAX + 1];
+  __shared__ int32_t s_cnt[QE_MAX];
+  if (E > 0) load_seg(counts, offsets, E, s_off, s_cnt);
+  const int nb = Cc / 32;
+  const size_t total = (size_t)G * R * nb;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t rowg = i / nb;  // g*R + r
+    const int b = (int)(i - rowg * nb);
+    const int r = (int)(rowg % R);
+    bool zero = false;
+    if (E > 0) {
+      const int real = block_real_rows(r & ~31, s_off, s_cnt, E);
+      if (real < 0) continue;
+      zero = (r & 31) >= real;
+    }
+    float v[32];
+    if (zero) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+    } else {
+      const uint4* p = reinterpret_cast<const uint4*>(src + rowg * Cc + (size_t)b * 32);
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint4 x = __ldg(p + w);
+        v[8 * w + 0] = bf16_lo(x.x);
+        v[8 * w + 1] = bf16_hi(x.x);
+        v[8 * w + 2] = bf16_lo(x.y);
+        v[8 * w + 3] = bf16_hi(x.y);
+        v[8 * w + 4] = bf16_lo(x.z);
+        v[8 * w + 5] = bf16_hi(x.z);
+        v[8 * w + 6] = bf16_lo(x.w);
+        v[8 * w + 7] = bf16_hi(x.w);
+      }
+    }
+    uint32_t codes[8];
+    const uint32_t sb = mx_quant_block32(v, codes);
+    uint4* dq = reinterpret_cast<uint4*>(q + rowg * Cc + (size_t)b * 32);
+    dq[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+    dq[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+    s[rowg * nb + b] = (uint8_t)sb;
+  }
+}
+
+// Column-wise (transposed): a CTA covers 32 rows x 256 columns; lane c of
+// warp w owns column 32w + c and quantises its 32 values (one MX block).
+__global__ void __launch_bounds__(256) k_quant_cols(const uint16_t* __restrict__ src, int G, int R, int Cc,
+                                                    const int32_t* __restrict__ counts,
+                                                    const int32_t* __restrict__ offsets, int E,
+                                                    uint8_t* __restrict__ q, uint8_t* __restrict__ s) {
+  __shared__ int32_t s_off[QE_MAX + 1];
+  __shared__ int32_t s_cnt[QE_MAX];
+  if (E > 0) load_seg(counts, offsets, E, s_off, s_cnt);
+  const int col_tiles = (Cc + 255) / 256;
+  const int row_blocks = R / 32;
+  const size_t total = (size_t)G * row_blocks * col_tiles;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (size_t i = blockIdx.x; i < total; i += gridDim.x) {
+    const int ct = (int)(i % col_tiles);
+    const size_t rest = i / col_tiles;
+    const int rbk = (int)(rest % row_blocks);
+    const int g = (int)(rest / row_blocks);
+    const int r0 = rbk * 32;
+    const int c = ct * 256 + warp * 32 + lane;
+    int real = 32;
+    if (E > 0) {
+      real = block_real_rows(r0, s_off, s_cnt, E);
+      if (real < 0) continue;  // uniform over the CTA
+    }
+    if (c >= Cc) continue;
+    float v[32];
+    const uint16_t* base = src + ((size_t)g * R + r0) * Cc + c;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = j < real ? __uint_as_float((uint32_t)__ldg(base + (size_t)j * Cc) << 16) : 0.0f;
+    uint32_t codes[8];
+    const uint32_t sb = mx_quant_block32(v, codes);
+    uint4* dq = reinterpret_cast<uint4*>(q + ((size_t)g * Cc + c) * R + r0);
+    dq[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+    dq[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+    s[((size_t)g * Cc + c) * (R / 32) + rbk] = (uint8_t)sb;
+  }
+}
+
+// NVFP4: one thread per 16-element block of a row < offsets[E].
+__global__ void __launch_bounds__(256) k_nvfp4_cast(const uint16_t* __restrict__ y, const float* __restrict__ amax,
+                                                    const int32_t* __restrict__ offsets, int E, int N,
+                                                    uint8_t* __restrict__ q, uint8_t* __restrict__ s,
+                                                    float* __restrict__ s_global) {
+  const float am = *amax;
+  const float sg = (am > 0.0f && am <= 3.402823466e38f) ? 2688.0f / am : 1.0f;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *s_global = sg;
+  const int R = __ldg(offsets + E);
+  const int nb = N / 16;
+  const size_t total = (size_t)R * nb;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const uint4* p = reinterpret_cast<const uint4*>(y + i * 16);
+    const uint4 a = __ldg(p), b = __ldg(p + 1);
+    float v[16] = {bf16_lo(a.x), bf16_hi(a.x), bf16_lo(a.y), bf16_hi(a.y), bf16_lo(a.z), bf16_hi(a.z),
+                   bf16_lo(a.w), bf16_hi(a.w), bf16_lo(b.x), bf16_hi(b.x), bf16_lo(b.y), bf16_hi(b.y),
+                   bf16_lo(b.z), bf16_hi(b.z), bf16_lo(b.w), bf16_hi(b.w)};
+    float ab = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) ab = fmaxf(ab, fabsf(v[j]));
+    const float sbf = (ab / 6.0f) * sg;
+    const __nv_fp8_storage_t sc = __nv_cvt_float_to_fp8(sbf, __NV_SATFINITE, __NV_E4M3);
+    const float sbv = __half2float(__half(__nv_cvt_fp8_to_halfraw(sc, __NV_E4M3)));
+    const float inv = sbv > 0.0f ? sg / sbv : 0.0f;
+    uint32_t w[2] = {0, 0};
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) {
+      const uint32_t c2 =
+          (uint32_t)__nv_cvt_float2_to_fp4x2(make_float2(v[j] * inv, v[j + 1] * inv), __NV_E2M1, cudaRoundNearest);
+      w[j / 8] |= (c2 & 0xFFu) << (8 * ((j % 8) / 2));
+    }
+    *reinterpret_cast<uint2*>(q + i * 8) = make_uint2(w[0], w[1]);
+    s[i] = (uint8_t)sc;
+  }
+}
+
+// Unfused activation: pre [R][N1] bf16 -> y [R][F] bf16, one thread per 32
+// output columns of a row < offsets[E].
+__global__ void __launch_bounds__(256) k_glu_act(const uint16_t* __restrict__ pre, const int32_t* __restrict__ offsets,
+                                                 int E, int F, int N1, GluParams prm, uint16_t* __restrict__ y) {
+  const int R = __ldg(offsets + E);
+  const int nb = F / 32;
+  const bool gated = N1 == 2 * F;
+  const size_t total = (size_t)R * nb;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t r = i / nb;
+    const int b = (int)(i - r * nb);
+    float u[32], g[32];
+    const uint16_t* pr = pre + r * N1;
+    const int pu = gated ? b * 64 : b * 32;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      u[j] = __uint_as_float((uint32_t)__ldg(pr + pu + j) << 16);
+      g[j] = gated ? __uint_as_float((uint32_t)__ldg(pr + pu + 32 + j) << 16) : 0.0f;
+    }
+    uint4* d = reinterpret_cast<uint4*>(y + r * F + (size_t)b * 32);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      float o[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) o[j] = act_fwd(prm, u[8 * w + j], g[8 * w + j]);
+      d[w] = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
+                        pack_bf16x2(o[6], o[7]));
+    }
+  }
+}
+
+static int grid_for(size_t items, int per_block) {
+  const size_t g = (items + per_block - 1) / per_block;
+  const size_t cap = (size_t)sm_count() * 16;
+  return (int)(g < 1 ? 1 : (g > cap ? cap : g));
+}
+
+}  // namespace moeglu
+
+using namespace moeglu;
+
+extern "C" moe_status_t moe_quantize_mxfp8(const moe_bf16* src, int G, int R, int Cc, int col, const int32_t* counts,
+                                           const int32_t* offsets, int E, uint8_t* q, uint8_t* s,
+                                           moe_stream_t stream) {
+  if (!src || !q || !s || G <= 0 || R <= 0 || Cc <= 0) return MOE_ERR_ARG;
+  if ((counts == nullptr) != (offsets == nullptr)) return MOE_ERR_ARG;
+  if (counts && (G != 1 || E <= 0 || E > QE_MAX || (R % 32))) return MOE_ERR_ARG;
+  if (!counts) E = 0;
+  if (!aligned16(src) || !aligned16(q)) return MOE_ERR_ARG;
+  cudaStream_t st = as_stream(stream);
+  if (!col) {
+    if (Cc % 32) return MOE_ERR_ARG;
+    k_quant_rows<<<grid_for((size_t)G * R * (Cc / 32), 256), 256, 0, st>>>(src, G, R, Cc, counts, offsets, E, q, s);
+  } else {
+    if (R % 32) return MOE_ERR_ARG;
+    const size_t tiles = (size_t)G * (R / 32) * ((Cc + 255) / 256);
+    k_quant_cols<<<grid_for(tiles, 1), 256, 0, st>>>(src, G, R, Cc, counts, offsets, E, q, s);
+  }
+  count_launch();
+  return launch_status();
+}
+
+extern "C" moe_status_t moe_nvfp4_cast(const moe_bf16* y, const float* amax, const int32_t* counts,
+                                       const int32_t* offsets, int E, int N, int R_cap, uint8_t* q, uint8_t* s,
+                                       float* s_global, moe_stream_t stream) {
+  (void)counts;
+  if (!y || !amax || !offsets || !q || !s || !s_global || E <= 0 || N <= 0 || (N % 16) || R_cap <= 0)
+    return MOE_ERR_ARG;
+  if (!aligned16(y) || (reinterpret_cast<uintptr_t>(q) & 7)) return MOE_ERR_ARG;
+  k_nvfp4_cast<<<grid_for((size_t)R_cap * (N / 16), 256), 256, 0, as_stream(stream)>>>(y, amax, offsets, E, N, q, s,
+                                                                                      s_global);
+  count_launch();
+  return launch_status();
+}
+
+extern "C" moe_status_t moe_glu_act(const moe_bf16* pre, const int32_t* counts, const int32_t* offsets, int E, int F,
+                                    int R_cap, const moe_glu_params_t* params, moe_bf16* y, moe_stream_t stream) {
+  (void)counts;
+  if (!pre || !offsets || !params || !y || E <= 0 || F <= 0 || (F % 32) || R_cap <= 0) return MOE_ERR_ARG;
+  if (!aligned16(y)) return MOE_ERR_ARG;
+  const int act = params->act;
+  if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SREGLU) return MOE_ERR_ARG;
+  GluParams g;
+  g.act = act;
+  g.alpha = params->alpha;
+  g.up_offset = params->up_offset;
+  g.gate_lo = params->gate_lo;
+  g.gate_hi = params->gate_hi;
+  g.up_lo = params->up_lo;
+  g.up_hi = params->up_hi;
+  const int N1 = act == MOE_ACT_SRELU ? F : 2 * F;
+  k_glu_act<<<grid_for((size_t)R_cap * (F / 32), 256), 256, 0, as_stream(stream)>>>(pre, offsets, E, F, N1, g, y);
+  count_launch();
+  return launch_status();
+}

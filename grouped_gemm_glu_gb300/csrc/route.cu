@@ -1,0 +1,324 @@
+// Routing, permutation, unpermute-combine and FC1 weight repack.
+//
+// Sources: [MegaMoE] (hnwysp.cn article on the MegaMoE math model and
+// DeepGEMM) §2.1 — y = sum over the top-k experts of p_i E_i(x) — and §4.3 —
+// each expert's tokens laid out contiguously so its rows form one GEMM
+// problem; [MoE-Fusion] ("Boosting MoE Training Throughput with Advanced
+// Fusion Kernels") "Eliminating host-device synchronisation": the per-group
+// token counts are produced and kept in device memory.
+//
+// Route = four launches, no host synchronisation:
+//   k_route_count   per chunk of assignments, a histogram per local expert
+//   k_route_scan    one CTA: exclusive scan over chunks (stable bases), the
+//                   counts, the padded offsets, capacity check
+//   k_route_scatter per chunk, stable rank of every assignment inside its
+//                   expert (ascending flat index t*k+j) -> row_of, tok_of,
+//                   prob_perm
+//   k_permute_gather one warp per permuted row: 16-byte copies of x rows,
+//                   zero fill of pad rows
+#include "common.cuh"
+#include "host_common.h"
+
+namespace moeglu {
+
+constexpr int ROUTE_THREADS = 256;
+constexpr int ROUTE_WARPS = ROUTE_THREADS / 32;
+constexpr int ROUTE_PER_THREAD = 8;
+constexpr int ROUTE_CHUNK = ROUTE_THREADS * ROUTE_PER_THREAD;  // assignments per CTA
+constexpr int ROUTE_WARP_SPAN = ROUTE_CHUNK / ROUTE_WARPS;     // contiguous assignments per warp
+constexpr int ROUTE_E_MAX = 1024;
+constexpr int ALIGN = 32;
+
+// workspace: chunk_counts [n_chunks][E] int32, then one int32 overflow flag
+static inline int route_chunks(int T, int k) { return (T * k + ROUTE_CHUNK - 1) / ROUTE_CHUNK; }
+
+__global__ void __launch_bounds__(ROUTE_THREADS) k_route_count(const int32_t* __restrict__ idx, int n_assign,
+                                                               int expert_begin, int E,
+                                                               int32_t* __restrict__ chunk_counts) {
+  __shared__ int32_t hist[ROUTE_E_MAX];
+  for (int e = threadIdx.x; e < E; e += ROUTE_THREADS) hist[e] = 0;
+  __syncthreads();
+  const int base = blockIdx.x * ROUTE_CHUNK;
+#pragma unroll
+  for (int i = 0; i < ROUTE_PER_THREAD; ++i) {
+    const int a = base + i * ROUTE_THREADS + threadIdx.x;
+    if (a < n_assign) {
+      const int e = __ldg(idx + a) - expert_begin;
+      if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += ROUTE_THREADS) chunk_counts[(size_t)blockIdx.x * E + e] = hist[e];
+}
+
+// One CTA of 1024 threads.  Thread e turns column e of chunk_counts into its
+// exclusive prefix over chunks (the stable base of each chunk inside the
+// expert) and produces counts[e]; then a block scan gives the padded offsets.
+__global__ void __launch_bounds__(1024) k_route_scan(int32_t* __restrict__ chunk_counts, int n_chunks, int E,
+                                                     int R_cap, int32_t* __restrict__ counts,
+                                                     int32_t* __restrict__ offsets, int32_t* __restrict__ overflow,
+                                                     int32_t* status) {
+  __shared__ int32_t warp_sums[32];
+  const int e = threadIdx.x;
+  int32_t total = 0;
+  if (e < E) {
+    for (int c = 0; c < n_chunks; ++c) {
+      int32_t* p = chunk_counts + (size_t)c * E + e;
+      const int32_t v = *p;
+      *p = total;
+      total += v;
+    }
+    counts[e] = total;
+  }
+  // inclusive scan of padded counts across the block
+  const int32_t padded = e < E ? (total + ALIGN - 1) / ALIGN * ALIGN : 0;
+  int32_t x = padded;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int32_t y = __shfl_up_sync(0xFFFFFFFFu, x, d);
+    if (lane >= d) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t w = warp_sums[lane];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int32_t y = __shfl_up_sync(0xFFFFFFFFu, w, d);
+      if (lane >= d) w += y;
+    }
+    warp_sums[lane] = w;
+  }
+  __syncthreads();
+  const int32_t incl = x + (warp > 0 ? warp_sums[warp - 1] : 0);
+  if (e < E) offsets[e] = incl - padded;
+  if (e == E - 1) {
+    offsets[E] = incl;
+    const int32_t over = incl > R_cap ? 1 : 0;
+    *overflow = over;
+    if (over) set_status(status, MOE_ERR_CAPACITY);
+  }
+}
+
+__global__ void __launch_bounds__(ROUTE_THREADS) k_route_scatter(
+    const int32_t* __restrict__ idx, const float* __restrict__ prob, int n_assign, int k, int expert_begin, int E,
+    const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ offsets,
+    const int32_t* __restrict__ overflow, int32_t* __restrict__ row_of, int32_t* __restrict__ tok_of,
+    float* __restrict__ prob_perm) {
+  // per warp, per expert: running rank base inside this CTA's chunk
+  extern __shared__ int32_t wbase[];  // [ROUTE_WARPS][E]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunk0 = blockIdx.x * ROUTE_CHUNK;
+  const int w0 = chunk0 + warp * ROUTE_WARP_SPAN;
+  const bool over = *overflow != 0;
+  for (int e = threadIdx.x; e < ROUTE_WARPS * E; e += ROUTE_THREADS) wbase[e] = 0;
+  __syncthreads();
+  // pass 1: per-warp histogram of its contiguous span
+  for (int i = 0; i < ROUTE_WARP_SPAN; i += 32) {
+    const int a = w0 + i + lane;
+    if (a < n_assign) {
+      const int e = __ldg(idx + a) - expert_begin;
+      if (e >= 0 && e < E) atomicAdd(&wbase[warp * E + e], 1);
+    }
+  }
+  __syncthreads();
+  // exclusive prefix over warps, plus the chunk's base within the expert
+  for (int e = threadIdx.x; e < E; e += ROUTE_THREADS) {
+    int32_t run = chunk_base[(size_t)blockIdx.x * E + e] + offsets[e];
+    for (int w = 0; w < ROUTE_WARPS; ++w) {
+      const int32_t v = wbase[w * E + e];
+      wbase[w * E + e] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+  // pass 2: stable rank, 32 consecutive assignments at a time
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int i = 0; i < ROUTE_WARP_SPAN; i += 32) {
+    const int a = w0 + i + lane;
+    int e = -1;
+    if (a < n_assign) {
+      e = __ldg(idx + a) - expert_begin;
+      if (e < 0 || e >= E) e = -1;
+    }
+    const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+    if (a < n_assign) {
+      if (e >= 0 && !over) {
+        const int32_t row = wbase[warp * E + e] + __popc(peers & lt_mask);
+        row_of[a] = row;
+        tok_of[row] = a / k;
+        prob_perm[row] = __ldg(prob + a);
+      } else {
+        row_of[a] = -1;
+      }
+    }
+    __syncwarp();
+    if (e >= 0 && (peers & lt_mask) == 0) wbase[warp * E + e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+// One warp per permuted row r < offsets[E]: a real row copies x[tok_of[r]],
+// a pad row is zero-filled and gets tok_of = -1, prob_perm = 0.
+__global__ void __launch_bounds__(256) k_permute_gather(const uint4* __restrict__ x, int H8, int E,
+                                                        const int32_t* __restrict__ counts,
+                                                        const int32_t* __restrict__ offsets,
+                                                        const int32_t* __restrict__ overflow,
+                                                        int32_t* __restrict__ tok_of, float* __restrict__ prob_perm,
+                                                        uint4* __restrict__ x_perm) {
+  __shared__ int32_t s_off[ROUTE_E_MAX + 1];
+  __shared__ int32_t s_cnt[ROUTE_E_MAX];
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    s_off[e] = offsets[e];
+    if (e < E) s_cnt[e] = counts[e];
+  }
+  __syncthreads();
+  if (*overflow) return;
+  const int R = s_off[E];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  for (int r = blockIdx.x * wpb + warp; r < R; r += gridDim.x * wpb) {
+    // expert of row r: last e with s_off[e] <= r
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_off[mid] <= r) lo = mid; else hi = mid - 1;
+    }
+    const bool real = r < s_off[lo] + s_cnt[lo];
+    uint4* dst = x_perm + (size_t)r * H8;
+    if (real) {
+      const int t = tok_of[r];
+      const uint4* src = x + (size_t)t * H8;
+      for (int v = lane; v < H8; v += 32) dst[v] = __ldg(src + v);
+    } else {
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      for (int v = lane; v < H8; v += 32) dst[v] = z;
+      if (lane == 0) {
+        tok_of[r] = -1;
+        prob_perm[r] = 0.0f;
+      }
+    }
+  }
+}
+
+// out[t] = bf16(sum_j p[t][j] * y_perm[row_of[t*k+j]]) in fp32, j ascending.
+// Work items are (token, 8-element vector) pairs, consecutive threads on
+// consecutive vectors of one row.
+__global__ void __launch_bounds__(256) k_unpermute_combine(const uint4* __restrict__ y, const int32_t* __restrict__ row_of,
+                                                           const float* __restrict__ prob, int T, int H8, int k,
+                                                           uint4* __restrict__ out) {
+  const size_t total = (size_t)T * H8;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / H8);
+    const int v = (int)(i - (size_t)t * H8);
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int j = 0; j < k; ++j) {
+      const int32_t r = __ldg(row_of + (size_t)t * k + j);
+      if (r < 0) continue;
+      const float p = __ldg(prob + (size_t)t * k + j);
+      const uint4 w = __ldg(y + (size_t)r * H8 + v);
+      acc[0] = fmaf(p, bf16_lo(w.x), acc[0]);
+      acc[1] = fmaf(p, bf16_hi(w.x), acc[1]);
+      acc[2] = fmaf(p, bf16_lo(w.y), acc[2]);
+      acc[3] = fmaf(p, bf16_hi(w.y), acc[3]);
+      acc[4] = fmaf(p, bf16_lo(w.z), acc[4]);
+      acc[5] = fmaf(p, bf16_hi(w.z), acc[5]);
+      acc[6] = fmaf(p, bf16_lo(w.w), acc[6]);
+      acc[7] = fmaf(p, bf16_hi(w.w), acc[7]);
+    }
+    out[i] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                        pack_bf16x2(acc[6], acc[7]));
+  }
+}
+
+// Repack (or its inverse) of FC1 rows: one CTA per (expert, packed row).
+__global__ void __launch_bounds__(128) k_repack_fc1(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
+                                                    int F, int H, int inverse) {
+  const int e = blockIdx.y;
+  const int p = blockIdx.x;  // packed row
+  const int b = p >> 6, o = p & 63;
+  const int logical = o < 32 ? b * 32 + o : F + b * 32 + (o - 32);
+  const size_t N1 = 2 * (size_t)F;
+  const size_t from = (size_t)e * N1 + (inverse ? p : logical);
+  const size_t to = (size_t)e * N1 + (inverse ? logical : p);
+  if ((H & 7) == 0) {
+    const uint4* s = reinterpret_cast<const uint4*>(src + from * H);
+    uint4* d = reinterpret_cast<uint4*>(dst + to * H);
+    for (int v = threadIdx.x; v < H / 8; v += blockDim.x) d[v] = __ldg(s + v);
+  } else {
+    for (int h = threadIdx.x; h < H; h += blockDim.x) dst[to * H + h] = src[from * H + h];
+  }
+}
+
+}  // namespace moeglu
+
+using namespace moeglu;
+
+extern "C" size_t moe_route_workspace_size(int T, int k, int E) {
+  if (T <= 0 || k <= 0 || E <= 0) return 256;
+  return ((size_t)route_chunks(T, k) * E + 64) * sizeof(int32_t);
+}
+
+extern "C" moe_status_t moe_route_permute(const moe_bf16* x, const int32_t* topk_idx, const float* topk_prob, int T,
+                                          int H, int k, int expert_begin, int E, int R_cap, moe_bf16* x_perm,
+                                          int32_t* row_of, int32_t* tok_of, float* prob_perm, int32_t* counts,
+                                          int32_t* offsets, void* ws, size_t ws_bytes, int32_t* status,
+                                          moe_stream_t stream) {
+  if (!x || !topk_idx || !topk_prob || !x_perm || !row_of || !tok_of || !prob_perm || !counts || !offsets || !ws)
+    return MOE_ERR_ARG;
+  if (T <= 0 || H <= 0 || (H & 7) || k <= 0 || k > 64 || E <= 0 || E > ROUTE_E_MAX || R_cap <= 0 || (R_cap & 31))
+    return MOE_ERR_ARG;
+  if ((int64_t)T * k > (int64_t)INT32_MAX / 2) return MOE_ERR_ARG;
+  if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_ARG;
+  if (ws_bytes < moe_route_workspace_size(T, k, E)) return MOE_ERR_ARG;
+  cudaStream_t s = as_stream(stream);
+  const int n_assign = T * k;
+  const int n_chunks = route_chunks(T, k);
+  int32_t* chunk_counts = static_cast<int32_t*>(ws);
+  int32_t* overflow = chunk_counts + (size_t)n_chunks * E;
+  k_route_count<<<n_chunks, ROUTE_THREADS, 0, s>>>(topk_idx, n_assign, expert_begin, E, chunk_counts);
+  k_route_scan<<<1, 1024, 0, s>>>(chunk_counts, n_chunks, E, R_cap, counts, offsets, overflow, status);
+  const int scatter_smem = ROUTE_WARPS * E * (int)sizeof(int32_t);
+  if (scatter_smem > 48 * 1024 && !set_smem_limit((const void*)k_route_scatter, scatter_smem)) return MOE_ERR_CUDA;
+  k_route_scatter<<<n_chunks, ROUTE_THREADS, scatter_smem, s>>>(topk_idx, topk_prob, n_assign, k, expert_begin, E,
+                                                                 chunk_counts, offsets, overflow, row_of, tok_of,
+                                                                 prob_perm);
+  const int sms = sm_count();
+  const int rows_bound = R_cap;
+  int grid = (rows_bound + 7) / 8;
+  if (grid > sms * 8) grid = sms * 8;
+  if (grid < 1) grid = 1;
+  k_permute_gather<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), H / 8, E, counts, offsets, overflow,
+                                        tok_of, prob_perm, reinterpret_cast<uint4*>(x_perm));
+  count_launch(4);
+  return launch_status();
+}
+
+extern "C" moe_status_t moe_unpermute_combine(const moe_bf16* y_perm, const int32_t* row_of, const float* topk_prob,
+                                              int T, int H, int k, moe_bf16* out, int32_t* status,
+                                              moe_stream_t stream) {
+  (void)status;
+  if (!y_perm || !row_of || !topk_prob || !out) return MOE_ERR_ARG;
+  if (T <= 0 || H <= 0 || (H & 7) || k <= 0) return MOE_ERR_ARG;
+  if (!aligned16(y_perm) || !aligned16(out)) return MOE_ERR_ARG;
+  const size_t items = (size_t)T * (H / 8);
+  int grid = (int)((items + 255) / 256);
+  const int cap = sm_count() * 8;
+  if (grid > cap) grid = cap;
+  k_unpermute_combine<<<grid, 256, 0, as_stream(stream)>>>(reinterpret_cast<const uint4*>(y_perm), row_of,
+                                                           topk_prob, T, H / 8, k, reinterpret_cast<uint4*>(out));
+  count_launch();
+  return launch_status();
+}
+
+extern "C" moe_status_t moe_repack_fc1(const moe_bf16* W1, moe_bf16* W1p, int E, int F, int H, int inverse,
+                                       moe_stream_t stream) {
+  if (!W1 || !W1p || W1 == W1p || E <= 0 || F <= 0 || (F & 31) || H <= 0) return MOE_ERR_ARG;
+  if ((H & 7) == 0 && (!aligned16(W1) || !aligned16(W1p))) return MOE_ERR_ARG;
+  if (E > 65535) return MOE_ERR_ARG;
+  dim3 grid(2 * F, E);
+  k_repack_fc1<<<grid, 128, 0, as_stream(stream)>>>(W1, W1p, F, H, inverse);
+  count_launch();
+  return launch_status();
+}

@@ -1,0 +1,93 @@
+"""ctypes binding of libmoeglu.so (the C ABI declared in include/moeglu.h).
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+``load()`` raises if the shared library has not been built; there is no
+fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import math
+import os
+import re
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libmoeglu.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "moeglu.h")
+
+MOE_OK, MOE_ERR_ARG, MOE_ERR_CUDA, MOE_ERR_CAPACITY, MOE_ERR_TIMEOUT, MOE_ERR_UNSUPPORTED = 0, 1, 2, 4, 8, 16
+ACT = {"swiglu": 0, "geglu": 1, "geglu_tanh": 2, "srelu": 3, "sreglu": 4, "none": 5}
+OUT_BF16, OUT_MXFP8, OUT_NVFP4 = 0, 1, 2
+
+
+class GluParams(C.Structure):
+    _fields_ = [("act", C.c_int32), ("alpha", C.c_float), ("up_offset", C.c_float),
+                ("gate_lo", C.c_float), ("gate_hi", C.c_float), ("up_lo", C.c_float), ("up_hi", C.c_float)]
+
+
+class ActOut(C.Structure):
+    _fields_ = [("q_row", C.c_void_p), ("s_row", C.c_void_p), ("q_col", C.c_void_p), ("s_col", C.c_void_p),
+                ("y", C.c_void_p), ("amax", C.c_void_p), ("pre", C.c_void_p)]
+
+
+def glu_params(act: str = "swiglu", alpha: float = 1.0, up_offset: float = 0.0,
+               gate_lo: float = -math.inf, gate_hi: float = math.inf,
+               up_lo: float = -math.inf, up_hi: float = math.inf) -> GluParams:
+    return GluParams(ACT[act], alpha, up_offset, gate_lo, gate_hi, up_lo, up_hi)
+
+
+P, I, U64, SZ, F32 = C.c_void_p, C.c_int, C.c_uint64, C.c_size_t, C.c_float
+
+_SIGS = {
+    "moe_repack_fc1": [P, P, I, I, I, I, P],
+    "moe_route_workspace_size": ([I, I, I], SZ),
+    "moe_route_permute": [P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P, SZ, P, P],
+    "moe_grouped_fc1_glu_quant_fwd": [P, P, P, P, P, P, I, I, I, I, C.POINTER(GluParams), I, C.POINTER(ActOut), I, P, P],
+    "moe_grouped_dglu_quant_bwd": [P, P, P, P, P, P, I, I, I, I, C.POINTER(GluParams), I, C.POINTER(ActOut), I, P, P],
+    "moe_quantize_mxfp8": [P, I, I, I, I, P, P, I, P, P, P],
+    "moe_grouped_fc2_fwd": [P, P, P, P, P, P, I, I, I, I, P, I, P, P],
+    "moe_grouped_wgrad": [P, P, P, P, P, P, I, I, I, I, P, I, I, P, P],
+    "moe_unpermute_combine": [P, P, P, I, I, I, P, P, P],
+    "moe_nvfp4_cast": [P, P, P, P, I, I, I, P, P, P, P],
+    "moe_glu_act": [P, P, P, I, I, I, C.POINTER(GluParams), P, P],
+    "moe_get_status": [P, P, P],
+    "moe_set_wait_limit_ns": ([U64], None),
+    "moe_launch_count": ([], U64),
+}
+
+_lib = None
+
+
+def header_symbols(path: str = HEADER) -> list[str]:
+    """Function names declared in the public header."""
+    txt = open(path).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(moe_\w+)\s*\(", txt, flags=re.M)))
+
+
+def load():
+    """Loads the library (once) and declares the signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with grouped_gemm_glu_gb300.build.build() "
+                           "(the CUDA library is the only implementation)")
+    lib = C.CDLL(LIB_PATH)
+    for name, sig in _SIGS.items():
+        fn = getattr(lib, name)
+        if isinstance(sig, tuple):
+            fn.argtypes, fn.restype = sig
+        else:
+            fn.argtypes, fn.restype = sig, C.c_int
+    _lib = lib
+    return lib
+
+
+class MoeError(RuntimeError):
+    pass
+
+
+def check(rc: int, what: str):
+    if rc != MOE_OK:
+        raise MoeError(f"{what} failed with status {rc}")

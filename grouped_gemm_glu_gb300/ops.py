@@ -1,0 +1,223 @@
+"""torch-facing wrappers of the C ABI: allocate outputs with torch (device
+memory and streams only) and pass raw pointers to libmoeglu.  No step of the
+method is computed here."""
+from __future__ import annotations
+
+import ctypes as C
+
+import torch
+
+from . import lib as L
+
+
+def _p(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _s(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def _dev(t):
+    if not t.is_cuda:
+        raise ValueError("tensors must live on a CUDA device")
+    return t.device
+
+
+def new_status(device) -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def read_status(status: torch.Tensor) -> int:
+    out = C.c_int32(0)
+    L.check(L.load().moe_get_status(_p(status), C.byref(out), _s()), "moe_get_status")
+    return out.value
+
+
+def repack_fc1(W1: torch.Tensor, inverse: bool = False) -> torch.Tensor:
+    """[E, 2F, H] logical input|gate rows <-> packed rows (bf16)."""
+    lib = L.load()
+    E, N1, H = W1.shape
+    out = torch.empty_like(W1)
+    L.check(lib.moe_repack_fc1(_p(W1), _p(out), E, N1 // 2, H, int(inverse), _s()), "moe_repack_fc1")
+    return out
+
+
+def route_permute(x, topk_idx, topk_prob, E: int, R_cap: int, expert_begin: int = 0, status=None) -> dict:
+    lib = L.load()
+    dev = _dev(x)
+    T, H = x.shape
+    k = topk_idx.shape[1]
+    o = {
+        "x_perm": torch.empty(R_cap, H, dtype=torch.bfloat16, device=dev),
+        "row_of": torch.empty(T * k, dtype=torch.int32, device=dev),
+        "tok_of": torch.empty(R_cap, dtype=torch.int32, device=dev),
+        "prob_perm": torch.empty(R_cap, dtype=torch.float32, device=dev),
+        "counts": torch.empty(E, dtype=torch.int32, device=dev),
+        "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+    }
+    ws_bytes = lib.moe_route_workspace_size(T, k, E)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    st = status if status is not None else new_status(dev)
+    L.check(lib.moe_route_permute(_p(x), _p(topk_idx), _p(topk_prob), T, H, k, expert_begin, E, R_cap,
+                                  _p(o["x_perm"]), _p(o["row_of"]), _p(o["tok_of"]), _p(o["prob_perm"]),
+                                  _p(o["counts"]), _p(o["offsets"]), _p(ws), ws_bytes, _p(st), _s()),
+            "moe_route_permute")
+    o["status"] = st
+    return o
+
+
+def _act_out(q_row=None, s_row=None, q_col=None, s_col=None, y=None, amax=None, pre=None) -> L.ActOut:
+    return L.ActOut(*(None if t is None else t.data_ptr() for t in (q_row, s_row, q_col, s_col, y, amax, pre)))
+
+
+def fc1_fwd(x_perm, W1p, counts, offsets, F: int, params: L.GluParams, out_mode: int = L.OUT_MXFP8,
+            b1p=None, row_scale=None, save_pre: bool = True, with_col: bool = True, sm_margin: int = 0,
+            status=None, out: dict | None = None) -> dict:
+    """GroupGemm + Activation + Quantize/Transpose.  Returns the output tensors
+    ({q_row, s_row, q_col, s_col} | {y[, amax]}, and pre when saved)."""
+    lib = L.load()
+    dev = _dev(x_perm)
+    R_cap, H = x_perm.shape
+    E = counts.shape[0]
+    gated = params.act in (L.ACT["swiglu"], L.ACT["geglu"], L.ACT["geglu_tanh"], L.ACT["sreglu"])
+    N1 = 2 * F if gated else F
+    o = out if out is not None else {}
+    if params.act == L.ACT["none"]:
+        o.setdefault("pre", torch.empty(R_cap, F, dtype=torch.bfloat16, device=dev))
+    else:
+        if out_mode == L.OUT_MXFP8:
+            o.setdefault("q_row", torch.empty(R_cap, F, dtype=torch.uint8, device=dev))
+            o.setdefault("s_row", torch.empty(R_cap, F // 32, dtype=torch.uint8, device=dev))
+            if with_col:
+                o.setdefault("q_col", torch.empty(F, R_cap, dtype=torch.uint8, device=dev))
+                o.setdefault("s_col", torch.empty(F, R_cap // 32, dtype=torch.uint8, device=dev))
+        else:
+            o.setdefault("y", torch.empty(R_cap, F, dtype=torch.bfloat16, device=dev))
+            if out_mode == L.OUT_NVFP4:
+                o.setdefault("amax", torch.zeros(1, dtype=torch.float32, device=dev))
+        if save_pre:
+            o.setdefault("pre", torch.empty(R_cap, N1, dtype=torch.bfloat16, device=dev))
+    st = status if status is not None else new_status(dev)
+    ao = _act_out(o.get("q_row"), o.get("s_row"), o.get("q_col"), o.get("s_col"), o.get("y"), o.get("amax"),
+                  o.get("pre"))
+    L.check(lib.moe_grouped_fc1_glu_quant_fwd(_p(x_perm), _p(W1p), _p(b1p), _p(row_scale), _p(counts),
+                                              _p(offsets), E, H, F, R_cap, C.byref(params), out_mode,
+                                              C.byref(ao), sm_margin, _p(st), _s()),
+            "moe_grouped_fc1_glu_quant_fwd")
+    o["status"] = st
+    return o
+
+
+def dglu_bwd(dY_perm, W2, pre, counts, offsets, F: int, params: L.GluParams, out_mode: int = L.OUT_MXFP8,
+             row_scale=None, with_col: bool = True, sm_margin: int = 0, status=None,
+             out: dict | None = None) -> dict:
+    """GroupGemm + dActivation + Quantize/Transpose.  dFC1 in packed order."""
+    lib = L.load()
+    dev = _dev(dY_perm)
+    R_cap, H = dY_perm.shape
+    E = counts.shape[0]
+    N1 = pre.shape[1]
+    o = out if out is not None else {}
+    if out_mode == L.OUT_MXFP8:
+        o.setdefault("q_row", torch.empty(R_cap, N1, dtype=torch.uint8, device=dev))
+        o.setdefault("s_row", torch.empty(R_cap, N1 // 32, dtype=torch.uint8, device=dev))
+        if with_col:
+            o.setdefault("q_col", torch.empty(N1, R_cap, dtype=torch.uint8, device=dev))
+            o.setdefault("s_col", torch.empty(N1, R_cap // 32, dtype=torch.uint8, device=dev))
+    else:
+        o.setdefault("y", torch.empty(R_cap, N1, dtype=torch.bfloat16, device=dev))
+    st = status if status is not None else new_status(dev)
+    ao = _act_out(o.get("q_row"), o.get("s_row"), o.get("q_col"), o.get("s_col"), o.get("y"))
+    L.check(lib.moe_grouped_dglu_quant_bwd(_p(dY_perm), _p(W2), _p(pre), _p(row_scale), _p(counts), _p(offsets),
+                                           E, H, F, R_cap, C.byref(params), out_mode, C.byref(ao), sm_margin,
+                                           _p(st), _s()),
+            "moe_grouped_dglu_quant_bwd")
+    o["status"] = st
+    return o
+
+
+def quantize_mxfp8(src, col: bool = False, counts=None, offsets=None, out=None):
+    """src [R, C] or [G, R, C] bf16 -> (q, s); col=True gives the transposed
+    column-wise copy."""
+    lib = L.load()
+    dev = _dev(src)
+    s3 = src if src.dim() == 3 else src.unsqueeze(0)
+    G, R, Cc = s3.shape
+    if col:
+        q = torch.empty(G, Cc, R, dtype=torch.uint8, device=dev) if out is None else out[0]
+        s = torch.empty(G, Cc, R // 32, dtype=torch.uint8, device=dev) if out is None else out[1]
+    else:
+        q = torch.empty(G, R, Cc, dtype=torch.uint8, device=dev) if out is None else out[0]
+        s = torch.empty(G, R, Cc // 32, dtype=torch.uint8, device=dev) if out is None else out[1]
+    E = 0 if counts is None else counts.shape[0]
+    L.check(lib.moe_quantize_mxfp8(_p(s3), G, R, Cc, int(col), _p(counts), _p(offsets), E, _p(q), _p(s), _s()),
+            "moe_quantize_mxfp8")
+    if src.dim() == 2 and out is None:
+        return q[0], s[0]
+    return q, s
+
+
+def fc2_fwd(Aq, As, Wq, Ws, counts, offsets, sm_margin: int = 0, status=None, out=None):
+    """y [R_cap, N] bf16 = block-scaled grouped GEMM of MXFP8 A [R_cap, K]
+    and per-expert MXFP8 W [E, N, K]."""
+    lib = L.load()
+    dev = _dev(Aq)
+    R_cap, K = Aq.shape
+    E, N, _ = Wq.shape
+    y = out if out is not None else torch.empty(R_cap, N, dtype=torch.bfloat16, device=dev)
+    st = status if status is not None else new_status(dev)
+    L.check(lib.moe_grouped_fc2_fwd(_p(Aq), _p(As), _p(Wq), _p(Ws), _p(counts), _p(offsets), E, K, N, R_cap,
+                                    _p(y), sm_margin, _p(st), _s()), "moe_grouped_fc2_fwd")
+    return y
+
+
+def wgrad(Aq_col, As_col, Bq_col, Bs_col, counts, offsets, out_f32: bool = False, sm_margin: int = 0,
+          status=None, out=None):
+    """D [E, M, N] = per-expert contraction over the expert's rows of the
+    column-wise MXFP8 copies A [M, R_cap] and B [N, R_cap]."""
+    lib = L.load()
+    dev = _dev(Aq_col)
+    M, R_cap = Aq_col.shape
+    N = Bq_col.shape[0]
+    E = counts.shape[0]
+    D = out if out is not None else torch.empty(E, M, N, dtype=torch.float32 if out_f32 else torch.bfloat16,
+                                                device=dev)
+    st = status if status is not None else new_status(dev)
+    L.check(lib.moe_grouped_wgrad(_p(Aq_col), _p(As_col), _p(Bq_col), _p(Bs_col), _p(counts), _p(offsets), E, M,
+                                  N, R_cap, _p(D), int(out_f32), sm_margin, _p(st), _s()), "moe_grouped_wgrad")
+    return D
+
+
+def unpermute_combine(y_perm, row_of, topk_prob, status=None, out=None):
+    lib = L.load()
+    dev = _dev(y_perm)
+    T, k = topk_prob.shape
+    H = y_perm.shape[1]
+    o = out if out is not None else torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    L.check(lib.moe_unpermute_combine(_p(y_perm), _p(row_of), _p(topk_prob), T, H, k, _p(o), _p(status), _s()),
+            "moe_unpermute_combine")
+    return o
+
+
+def nvfp4_cast(y, amax, counts, offsets):
+    lib = L.load()
+    dev = _dev(y)
+    R_cap, N = y.shape
+    q = torch.empty(R_cap, N // 2, dtype=torch.uint8, device=dev)
+    s = torch.empty(R_cap, N // 16, dtype=torch.uint8, device=dev)
+    sg = torch.empty(1, dtype=torch.float32, device=dev)
+    L.check(lib.moe_nvfp4_cast(_p(y), _p(amax), _p(counts), _p(offsets), counts.shape[0], N, R_cap, _p(q), _p(s),
+                               _p(sg), _s()), "moe_nvfp4_cast")
+    return q, s, sg
+
+
+def glu_act(pre, counts, offsets, F: int, params: L.GluParams):
+    lib = L.load()
+    dev = _dev(pre)
+    R_cap = pre.shape[0]
+    y = torch.empty(R_cap, F, dtype=torch.bfloat16, device=dev)
+    L.check(lib.moe_glu_act(_p(pre), _p(counts), _p(offsets), counts.shape[0], F, R_cap, C.byref(params), _p(y),
+                            _s()), "moe_glu_act")
+    return y

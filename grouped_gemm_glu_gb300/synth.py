@@ -137,11 +137,17 @@ def make_inputs(w: Workload, seed: int = 0) -> dict:
     return out
 
 
-def random_mxfp8(rows: int, cols: int, seed: int, scale_lo: int = 118, scale_hi: int = 131):
-    """Random MXFP8 operand: E4M3 codes (never the NaN codes) and E8M0
-    scales drawn uniformly from [scale_lo, scale_hi]."""
+def random_mxfp8(rows: int, cols: int, seed: int, scale_lo: int = 123, scale_hi: int = 125,
+                 exp_lo: int = 5, exp_hi: int = 9):
+    """Random MXFP8 operand: E4M3 codes with a random sign, exponent field in
+    [exp_lo, exp_hi) (magnitudes 2^(exp_lo-7) .. 2^(exp_hi-7), never the NaN
+    code) and random mantissa, plus E8M0 scales drawn from [scale_lo,
+    scale_hi].  The defaults keep a K ~ 2000 contraction of two such
+    operands near unit magnitude."""
     rng = np.random.default_rng(seed)
-    q = rng.integers(0, 256, size=(rows, cols), dtype=np.uint8)
-    q = np.where((q & 0x7F) == 0x7F, q ^ 0x01, q).astype(np.uint8)
+    sign = rng.integers(0, 2, size=(rows, cols), dtype=np.uint8) << 7
+    ex = rng.integers(exp_lo, exp_hi, size=(rows, cols), dtype=np.uint8) << 3
+    man = rng.integers(0, 8, size=(rows, cols), dtype=np.uint8)
+    q = (sign | ex | man).astype(np.uint8)
     s = rng.integers(scale_lo, scale_hi + 1, size=(rows, cols // 32), dtype=np.uint8)
     return torch.from_numpy(q), torch.from_numpy(s)

@@ -1,0 +1,259 @@
+/*
+ * moeglu.h — C ABI of libmoeglu.so: the sync-free MoE MLP hot path for
+ * GB300 (sm_103a).  Grouped GEMM with the GLU activation fused into its
+ * epilogue and MXFP8 / NVFP4 quantisation (plus the transposed copy) fused
+ * after it, forward and backward, with the permute and combine around it.
+ *
+ * Sources (page titles; sections named on them):
+ *   [MoE-Fusion] "Boosting MoE Training Throughput with Advanced Fusion
+ *                Kernels" (NVIDIA technical blog, 2026-06-15): the
+ *                three-kernel family GroupGemm + Quantize,
+ *                GroupGemm + Activation + Quantize/Transpose,
+ *                GroupGemm + dActivation + Quantize/Transpose; sections
+ *                "Optimizing GLU via fused GEMM epilogues" (Fig. 2),
+ *                "Eliminating host-device synchronisation",
+ *                "Fusing MXFP8 and NVFP4 quantisation", and the list of
+ *                end-to-end features (dynamic scheduling, cluster margin).
+ *   [MegaMoE]    hnwysp.cn article on the MegaMoE math model and DeepGEMM:
+ *                §2.1 (routing, combine), §2.3 (FP8 formats, block scales),
+ *                §4.3 (grouped GEMM over contiguous expert rows), §5.3 (tails).
+ *
+ * Conventions for every call
+ *   - All tensor pointers are caller-owned DEVICE memory, row-major, dense
+ *     (the leading dimension is the row length given).  The library never
+ *     allocates device memory, never synchronises the stream and never reads
+ *     device data on the host: per-expert counts stay on the device, so a
+ *     whole layer can be captured in one CUDA graph.
+ *   - Arguments are validated on the host; a bad argument returns
+ *     MOE_ERR_ARG and launches nothing.  A launch failure returns
+ *     MOE_ERR_CUDA.  Errors found on the device (capacity overflow, a
+ *     pipeline wait that timed out) are OR-ed into the caller's int32
+ *     `status` word (device memory, zero it before use) and read with
+ *     moe_get_status() outside any capture.
+ *   - Shapes: T tokens, H hidden, k top-k, E local experts, F expert FFN
+ *     width, N1 = 2F (gated activations) or F (sReLU).  Permuted buffers
+ *     have R_cap rows (a multiple of 128, >= T*min(k,E) + 31*E is always
+ *     enough).  Rows of one expert are contiguous, start at offsets[e]
+ *     (a multiple of 32) and are followed by pad rows up to the next
+ *     multiple of 32; only rows < offsets[E] are defined.
+ *   - bf16 means IEEE bfloat16 (uint16 storage); MXFP8 tensors are E4M3
+ *     codes (uint8) with one E8M0 scale byte per 32 consecutive elements
+ *     along the contiguous dimension.
+ *   - `stream` is a cudaStream_t (0 = legacy default stream).
+ *   - `sm_margin` leaves that many SMs free for concurrent kernels
+ *     ([MoE-Fusion]: configurable cluster margin); the persistent GEMMs
+ *     launch one CTA per remaining SM.
+ */
+#ifndef MOEGLU_H
+#define MOEGLU_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void* moe_stream_t; /* cudaStream_t */
+typedef uint16_t moe_bf16;  /* bfloat16 storage */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_ARG = 1,         /* invalid argument (host check) */
+  MOE_ERR_CUDA = 2,        /* CUDA runtime / launch error */
+  MOE_ERR_CAPACITY = 4,    /* device: routed rows exceed R_cap */
+  MOE_ERR_TIMEOUT = 8,     /* device: a pipeline wait gave up */
+  MOE_ERR_UNSUPPORTED = 16 /* shape/option this build does not handle */
+} moe_status_t;
+
+/* Activation of the FC1 epilogue.  [MoE-Fusion] names SwiGLU, GeGLU and
+ * sReLU; formulas (textbook readings): SwiGLU (u'+c) g' sigmoid(alpha g');
+ * GeGLU (u'+c) g' Phi(g') (erf form) or its tanh approximation; sReLU
+ * max(x,0)^2 (not gated, N1 = F); sReGLU (u'+c) max(g',0)^2. */
+typedef enum {
+  MOE_ACT_SWIGLU = 0,
+  MOE_ACT_GEGLU = 1,
+  MOE_ACT_GEGLU_TANH = 2,
+  MOE_ACT_SRELU = 3,
+  MOE_ACT_SREGLU = 4,
+  MOE_ACT_NONE = 5 /* FC1 only: plain grouped GEMM writing the bf16 pre-activation (out->pre),
+                      no activation, for the unfused path; here F is the full GEMM width N1 */
+} moe_act_t;
+
+/* Epilogue options ([MoE-Fusion]: clamping, feature scaling, bias).
+ * g' = clamp(gate, gate_lo, gate_hi), u' = clamp(up, up_lo, up_hi); the
+ * clamp's derivative is 1 inside the closed interval and 0 outside.  Use
+ * +-INFINITY to disable a bound.  c = up_offset (GPT-OSS uses 1). */
+typedef struct {
+  int32_t act;       /* moe_act_t */
+  float alpha;       /* SwiGLU sigmoid slope (1 = plain, 1.702 GPT-OSS) */
+  float up_offset;   /* c */
+  float gate_lo, gate_hi;
+  float up_lo, up_hi;
+} moe_glu_params_t;
+
+/* Output quantisation of a fused epilogue. */
+typedef enum {
+  MOE_OUT_BF16 = 0,  /* y bf16 [R_cap][N] */
+  MOE_OUT_MXFP8 = 1, /* q_row/s_row (+ q_col/s_col when non-null) */
+  MOE_OUT_NVFP4 = 2  /* y bf16 + per-tensor amax (cast with moe_nvfp4_cast) */
+} moe_out_mode_t;
+
+/* Outputs of a fused activation epilogue (N = F for the forward, N = N1 for
+ * the backward).  Unused pointers may be NULL. */
+typedef struct {
+  uint8_t* q_row;    /* MXFP8 codes   [R_cap][N]      */
+  uint8_t* s_row;    /* E8M0 scales   [R_cap][N/32]   */
+  uint8_t* q_col;    /* transposed    [N][R_cap]      (column-wise blocks of 32 rows) */
+  uint8_t* s_col;    /*               [N][R_cap/32]   */
+  moe_bf16* y;       /* bf16 output   [R_cap][N]      (BF16 / NVFP4 modes) */
+  float* amax;       /* one float: max |y| over all real rows (NVFP4 mode); caller zeroes it */
+  moe_bf16* pre;     /* forward only: saved pre-activation [R_cap][N1] (bias added), for the backward */
+} moe_act_out_t;
+
+/* ---------------------------------------------------------------------- */
+
+/* FC1 weight repack ([MoE-Fusion], "Optimizing GLU via fused GEMM
+ * epilogues", Fig. 2: input and gate columns repacked so one thread block
+ * owns matching halves; done once at checkpoint load).
+ * W1 [E][2F][H] bf16, rows [0,F) input, [F,2F) gate  ->  W1p [E][2F][H]:
+ * packed row p, block b = p/64, o = p%64: o < 32 -> input row 32b+o,
+ * else gate row F+32b+o-32.  Also repacks a bias [E][2F] when H == 1.
+ * F % 32 == 0.  inverse != 0 performs the inverse permutation. */
+MOE_API moe_status_t moe_repack_fc1(const moe_bf16* W1, moe_bf16* W1p, int E, int F, int H,
+                            int inverse, moe_stream_t stream);
+
+/* Bytes of device workspace moe_route_permute needs. */
+MOE_API size_t moe_route_workspace_size(int T, int k, int E);
+
+/* Routing + permutation ([MegaMoE] §2.1, §4.3; [MoE-Fusion],
+ * "Eliminating host-device synchronisation": counts stay on the device).
+ * In:  x [T][H] bf16, topk_idx [T][k] int32 (global expert ids),
+ *      topk_prob [T][k] f32.  Experts [expert_begin, expert_begin+E) are
+ *      local; other assignments are dropped (row_of = -1).
+ * Out: counts [E], offsets [E+1] (exclusive prefix of counts rounded up to
+ *      32), row_of [T*k] (permuted row of assignment t*k+j, rows of one
+ *      expert in ascending t*k+j), tok_of [R_cap] (token of each row, -1
+ *      on pad rows), prob_perm [R_cap] (0 on pad rows), x_perm [R_cap][H]
+ *      (pad rows zero).  ws: moe_route_workspace_size() bytes.
+ *      offsets[E] > R_cap sets MOE_ERR_CAPACITY in *status and writes no rows. */
+MOE_API moe_status_t moe_route_permute(const moe_bf16* x, const int32_t* topk_idx, const float* topk_prob,
+                               int T, int H, int k, int expert_begin, int E, int R_cap,
+                               moe_bf16* x_perm, int32_t* row_of, int32_t* tok_of, float* prob_perm,
+                               int32_t* counts, int32_t* offsets,
+                               void* ws, size_t ws_bytes, int32_t* status, moe_stream_t stream);
+
+/* GroupGemm + Activation + Quantize/Transpose, forward ([MoE-Fusion]).
+ * pre = x_perm[rows of e] . W1p[e]^T + b1p[e]  (bf16 in, fp32 accumulate in
+ * tensor memory); the epilogue pairs input/gate columns of the packed tile,
+ * applies the activation, multiplies by row_scale[row] when non-NULL
+ * (feature scaling), and writes per out_mode.  Pad rows are written as 0.
+ * x_perm [R_cap][H], W1p [E][N1][H] (packed when gated), b1p [E][N1] or
+ * NULL, row_scale [R_cap] f32 or NULL.  H % 64 == 0, F % 32 == 0. */
+MOE_API moe_status_t moe_grouped_fc1_glu_quant_fwd(const moe_bf16* x_perm, const moe_bf16* W1p,
+                                           const moe_bf16* b1p, const float* row_scale,
+                                           const int32_t* counts, const int32_t* offsets,
+                                           int E, int H, int F, int R_cap,
+                                           const moe_glu_params_t* params, int out_mode,
+                                           const moe_act_out_t* out, int sm_margin,
+                                           int32_t* status, moe_stream_t stream);
+
+/* GroupGemm + dActivation + Quantize/Transpose, backward ([MoE-Fusion]: the
+ * epilogue reads the GEMM output, computes dSwiGLU, quantises and writes).
+ * da = dY_perm[rows of e] . W2[e]^T with W2 [E][F][H] (the forward is
+ * y = a . W2[e]); (du, dg) from the saved bf16 pre [R_cap][N1]; times
+ * row_scale when non-NULL; written as dFC1 [R_cap][N1] in packed column
+ * order per out_mode (MXFP8 row + column-wise, or bf16).  H % 64 == 0. */
+MOE_API moe_status_t moe_grouped_dglu_quant_bwd(const moe_bf16* dY_perm, const moe_bf16* W2,
+                                        const moe_bf16* pre, const float* row_scale,
+                                        const int32_t* counts, const int32_t* offsets,
+                                        int E, int H, int F, int R_cap,
+                                        const moe_glu_params_t* params, int out_mode,
+                                        const moe_act_out_t* dfc1, int sm_margin,
+                                        int32_t* status, moe_stream_t stream);
+
+/* MXFP8 quantisation of a bf16 tensor (the standalone quantize/transpose
+ * kernel of the unfused path, and the weight cast).  src [G][R][C] bf16.
+ * col == 0: q [G][R][C], s [G][R][C/32] (blocks along C).
+ * col != 0: q [G][C][R], s [G][C][R/32] (blocks of 32 rows; transposed).
+ * counts/offsets (G == 1 only, may be NULL): rows of the permuted layout
+ * outside [offsets[e], offsets[e]+counts[e]) are treated as zero and rows
+ * >= offsets[E] are not written. */
+MOE_API moe_status_t moe_quantize_mxfp8(const moe_bf16* src, int G, int R, int C, int col,
+                                const int32_t* counts, const int32_t* offsets, int E,
+                                uint8_t* q, uint8_t* s, moe_stream_t stream);
+
+/* GroupGemm (+ bf16 out), block-scaled MXFP8 ([MoE-Fusion] GroupGemm +
+ * Quantize family; [MegaMoE] §2.3: C ~ (A_q/s_A)(B_q/s_B)).
+ * y[rows of e] = dequant(Aq,As)[rows] . dequant(Wq[e],Ws[e])^T, fp32
+ * accumulate, bf16 out; pad rows 0.  Serves FC2 (K = F, N = H) and the
+ * data-gradient GEMM dX = dFC1 . W1p (K = N1, N = H).
+ * Aq [R_cap][K], As [R_cap][K/32], Wq [E][N][K], Ws [E][N][K/32].
+ * K % 128 == 0, N % 128 == 0. */
+MOE_API moe_status_t moe_grouped_fc2_fwd(const uint8_t* Aq, const uint8_t* As,
+                                 const uint8_t* Wq, const uint8_t* Ws,
+                                 const int32_t* counts, const int32_t* offsets,
+                                 int E, int K, int N, int R_cap,
+                                 moe_bf16* y, int sm_margin, int32_t* status, moe_stream_t stream);
+
+/* Weight-gradient grouped GEMM, contraction over each expert's rows
+ * (variable K = the expert's padded row count).  Inputs are the
+ * column-wise (transposed) MXFP8 copies: Aq [M][R_cap], As [M][R_cap/32],
+ * Bq [N][R_cap], Bs [N][R_cap/32].  D[e] = A[:, seg e] . B[:, seg e]^T,
+ * written as f32 (out_f32 != 0) or bf16 into D [E][M][N].
+ * dW1p = wgrad(dFC1 col, x col); dW2 = wgrad(a col, dY col).
+ * M % 128 == 0, N % 128 == 0. */
+MOE_API moe_status_t moe_grouped_wgrad(const uint8_t* Aq, const uint8_t* As,
+                               const uint8_t* Bq, const uint8_t* Bs,
+                               const int32_t* counts, const int32_t* offsets,
+                               int E, int M, int N, int R_cap,
+                               void* D, int out_f32, int sm_margin, int32_t* status,
+                               moe_stream_t stream);
+
+/* Unpermute + combine ([MegaMoE] §2.1: y = sum_{i in topk} p_i E_i(x)).
+ * out[t] = bf16( sum_j topk_prob[t][j] * y_perm[row_of[t*k+j]] ) over
+ * j with row_of >= 0, summed in fp32 in j order; 0 when none is local. */
+MOE_API moe_status_t moe_unpermute_combine(const moe_bf16* y_perm, const int32_t* row_of,
+                                   const float* topk_prob, int T, int H, int k,
+                                   moe_bf16* out, int32_t* status, moe_stream_t stream);
+
+/* NVFP4 cast of the forward's bf16 output ([MoE-Fusion], "Fusing MXFP8 and
+ * NVFP4 quantisation": the fused kernel emits BF16 + per-tensor amax).
+ * s_g = 2688 / amax (1 if amax == 0) written to *s_global; per 16
+ * elements s_b = E4M3(fp32(amax_b/6) * s_g); q = E2M1(v * fp32(s_g/s_b)).
+ * y [R_cap][N] bf16 -> q [R_cap][N/2] (element 2i low nibble),
+ * s [R_cap][N/16] E4M3.  Rows >= offsets[E] are not written; pad rows
+ * give zeros.  N % 16 == 0. */
+MOE_API moe_status_t moe_nvfp4_cast(const moe_bf16* y, const float* amax,
+                            const int32_t* counts, const int32_t* offsets, int E,
+                            int N, int R_cap, uint8_t* q, uint8_t* s, float* s_global,
+                            moe_stream_t stream);
+
+/* Standalone activation of the unfused path: pre [R][N1] bf16 -> y [R][F]
+ * bf16 (rows >= offsets[E] untouched, pad rows 0). */
+MOE_API moe_status_t moe_glu_act(const moe_bf16* pre, const int32_t* counts, const int32_t* offsets,
+                         int E, int F, int R_cap, const moe_glu_params_t* params,
+                         moe_bf16* y, moe_stream_t stream);
+
+/* Copies the device status word to *host_out (synchronises `stream`; not
+ * for use inside a graph capture). */
+MOE_API moe_status_t moe_get_status(const int32_t* status, int32_t* host_out, moe_stream_t stream);
+
+/* Pipeline wait limit in nanoseconds for the persistent GEMMs (default 2e9);
+ * after it a wait gives up, sets MOE_ERR_TIMEOUT and the kernel returns. */
+MOE_API void moe_set_wait_limit_ns(uint64_t ns);
+
+/* Cumulative number of kernels this library has launched in this process
+ * (launch accounting for benchmarks). */
+MOE_API uint64_t moe_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOEGLU_H */

@@ -1,0 +1,43 @@
+"""The C-ABI library builds, loads without a GPU and exports every function
+the public header declares (no compute call is made)."""
+import ctypes
+
+import pytest
+
+from grouped_gemm_glu_gb300 import build as B
+from grouped_gemm_glu_gb300 import lib as L
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return L.load()
+
+
+def test_header_declares_the_hot_path(lib):
+    names = L.header_symbols()
+    for n in ("moe_route_permute", "moe_grouped_fc1_glu_quant_fwd", "moe_grouped_fc2_fwd",
+              "moe_grouped_dglu_quant_bwd", "moe_unpermute_combine", "moe_grouped_wgrad", "moe_quantize_mxfp8",
+              "moe_nvfp4_cast", "moe_repack_fc1"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    raw = ctypes.CDLL(L.LIB_PATH)
+    missing = [n for n in L.header_symbols() if not hasattr(raw, n)]
+    assert not missing, missing
+    assert set(L.header_symbols()) == set(L._SIGS), "binding signatures out of sync with the header"
+
+
+def test_workspace_size_is_host_only(lib):
+    # pure host arithmetic: callable without a device
+    assert lib.moe_route_workspace_size(8192, 8, 32) >= 4 * 32 * (8192 * 8 // 2048)
+
+
+def test_argument_validation_needs_no_device(lib):
+    # a null pointer is rejected on the host before anything is launched
+    assert lib.moe_unpermute_combine(None, None, None, 1, 8, 1, None, None, None) == L.MOE_ERR_ARG
+    prm = L.glu_params("swiglu")
+    out = L.ActOut()
+    assert lib.moe_grouped_fc1_glu_quant_fwd(None, None, None, None, None, None, 4, 256, 512, 1152,
+                                             ctypes.byref(prm), 1, ctypes.byref(out), 0, None, None) == L.MOE_ERR_ARG
