@@ -1,6 +1,8 @@
 // Host helpers of libmoeglu (see host_common.h) and the small entry points
 // that launch nothing: status read-back, wait limit, launch counter.
 #include <mutex>
+#include <set>
+#include <tuple>
 
 #include "host_common.h"
 
@@ -22,9 +24,18 @@ int sm_count() {
 }
 
 bool set_smem_limit(const void* kernel, int bytes) {
-  // cudaFuncSetAttribute is cheap but not free; it is applied on every call
-  // because the current device may change between calls.
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
+  // applied once per (kernel, device, size): later calls, including calls
+  // made while a stream is being captured, only look it up
+  static std::mutex mu;
+  static std::set<std::tuple<const void*, int, int>> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  const auto key = std::make_tuple(kernel, dev, bytes);
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count(key)) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+  done.insert(key);
+  return true;
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

@@ -1,0 +1,158 @@
+"""One MoE MLP layer step (forward + backward) as a fixed sequence of C-ABI
+calls over preallocated device buffers.  Nothing here reads device data on
+the host, so the whole step captures into one CUDA graph.
+
+Forward:  route+permute -> FC1 GroupGemm+Activation+Quantize/Transpose
+          -> MXFP8 cast of W2 -> FC2 block-scaled GroupGemm -> unpermute+combine
+Backward: FC2-data-grad GroupGemm+dActivation+Quantize/Transpose (dFC1)
+          -> MXFP8 cast of W1p (transposed) -> dX = dFC1 . W1p
+          -> column-wise MXFP8 of x_perm and dY_perm
+          -> weight gradients dW1p = dFC1^T x, dW2 = a^T dY (per expert)
+
+Weight layouts: W1 [E][2F][H] (rows: input | gate; repacked once into W1p),
+W2 [E][F][H] (y = a . W2[e]); gradients come out in the same layouts
+(dW1 in packed row order).
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+import torch
+
+from . import lib as L
+from .ops import _p, _s
+
+
+class MoeLayer:
+    def __init__(self, W1, W2, T: int, k: int, R_cap: int, params: L.GluParams, b1=None,
+                 expert_begin: int = 0, sm_margin: int = 0, gated: bool = True):
+        self.lib = L.load()
+        dev = W1.device
+        self.dev = dev
+        E, N1, H = W1.shape
+        F = W2.shape[1]
+        self.E, self.N1, self.H, self.F, self.T, self.k, self.R_cap = E, N1, H, F, T, k, R_cap
+        self.params = params
+        self.expert_begin = expert_begin
+        self.sm_margin = sm_margin
+        self.gated = gated
+        self.W2 = W2
+        u8, bf = torch.uint8, torch.bfloat16
+        z = lambda *s, dt=bf: torch.empty(*s, dtype=dt, device=dev)
+        if gated:
+            self.W1p = z(E, N1, H)
+            L.check(self.lib.moe_repack_fc1(_p(W1), _p(self.W1p), E, F, H, 0, _s()), "repack")
+            self.b1p = None
+            if b1 is not None:
+                self.b1p = z(E, N1)
+                L.check(self.lib.moe_repack_fc1(_p(b1), _p(self.b1p), E, F, 1, 0, _s()), "repack bias")
+        else:
+            self.W1p, self.b1p = W1, b1
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        # routing
+        self.x_perm = z(R_cap, H)
+        self.row_of = z(T * k, dt=torch.int32)
+        self.tok_of = z(R_cap, dt=torch.int32)
+        self.prob_perm = z(R_cap, dt=torch.float32)
+        self.counts = z(E, dt=torch.int32)
+        self.offsets = z(E + 1, dt=torch.int32)
+        self.ws_bytes = self.lib.moe_route_workspace_size(T, k, E)
+        self.ws = z(self.ws_bytes, dt=u8)
+        # forward
+        self.a_q, self.a_s = z(R_cap, F, dt=u8), z(R_cap, F // 32, dt=u8)
+        self.a_qc, self.a_sc = z(F, R_cap, dt=u8), z(F, R_cap // 32, dt=u8)
+        self.pre = z(R_cap, N1)
+        self.W2q, self.W2s = z(E, H, F, dt=u8), z(E, H, F // 32, dt=u8)
+        self.y_perm = z(R_cap, H)
+        self.out = z(T, H)
+        # backward
+        self.d_q, self.d_s = z(R_cap, N1, dt=u8), z(R_cap, N1 // 32, dt=u8)
+        self.d_qc, self.d_sc = z(N1, R_cap, dt=u8), z(N1, R_cap // 32, dt=u8)
+        self.W1q, self.W1s = z(E, H, N1, dt=u8), z(E, H, N1 // 32, dt=u8)
+        self.dX_perm = z(R_cap, H)
+        self.x_qc, self.x_sc = z(H, R_cap, dt=u8), z(H, R_cap // 32, dt=u8)
+        self.dy_qc, self.dy_sc = z(H, R_cap, dt=u8), z(H, R_cap // 32, dt=u8)
+        self.dW1 = z(E, N1, H)
+        self.dW2 = z(E, F, H)
+        self.fc1_out = L.ActOut(self.a_q.data_ptr(), self.a_s.data_ptr(), self.a_qc.data_ptr(),
+                                self.a_sc.data_ptr(), None, None, self.pre.data_ptr())
+        self.bwd_out = L.ActOut(self.d_q.data_ptr(), self.d_s.data_ptr(), self.d_qc.data_ptr(),
+                                self.d_sc.data_ptr(), None, None, None)
+
+    # each entry: (name, callable issuing exactly one C-ABI call)
+    def forward_calls(self, x, topk_idx, topk_prob):
+        lib, s = self.lib, _s()
+        E, N1, H, F, T, k, R = self.E, self.N1, self.H, self.F, self.T, self.k, self.R_cap
+        st = _p(self.status)
+        return [
+            ("route_permute", lambda: lib.moe_route_permute(
+                _p(x), _p(topk_idx), _p(topk_prob), T, H, k, self.expert_begin, E, R, _p(self.x_perm),
+                _p(self.row_of), _p(self.tok_of), _p(self.prob_perm), _p(self.counts), _p(self.offsets),
+                _p(self.ws), self.ws_bytes, st, s)),
+            ("fc1_glu_quant", lambda: lib.moe_grouped_fc1_glu_quant_fwd(
+                _p(self.x_perm), _p(self.W1p), _p(self.b1p), None, _p(self.counts), _p(self.offsets), E, H, F, R,
+                C.byref(self.params), L.OUT_MXFP8, C.byref(self.fc1_out), self.sm_margin, st, s)),
+            ("quant_w2", lambda: lib.moe_quantize_mxfp8(
+                _p(self.W2), E, F, H, 1, None, None, 0, _p(self.W2q), _p(self.W2s), s)),
+            ("fc2", lambda: lib.moe_grouped_fc2_fwd(
+                _p(self.a_q), _p(self.a_s), _p(self.W2q), _p(self.W2s), _p(self.counts), _p(self.offsets), E, F,
+                H, R, _p(self.y_perm), self.sm_margin, st, s)),
+            ("combine", lambda: lib.moe_unpermute_combine(
+                _p(self.y_perm), _p(self.row_of), _p(topk_prob), T, H, k, _p(self.out), st, s)),
+        ]
+
+    def backward_calls(self, dY_perm):
+        lib, s = self.lib, _s()
+        E, N1, H, F, R = self.E, self.N1, self.H, self.F, self.R_cap
+        st = _p(self.status)
+        return [
+            ("dglu_quant", lambda: lib.moe_grouped_dglu_quant_bwd(
+                _p(dY_perm), _p(self.W2), _p(self.pre), None, _p(self.counts), _p(self.offsets), E, H, F, R,
+                C.byref(self.params), L.OUT_MXFP8, C.byref(self.bwd_out), self.sm_margin, st, s)),
+            ("quant_w1", lambda: lib.moe_quantize_mxfp8(
+                _p(self.W1p), E, N1, H, 1, None, None, 0, _p(self.W1q), _p(self.W1s), s)),
+            ("dx", lambda: lib.moe_grouped_fc2_fwd(
+                _p(self.d_q), _p(self.d_s), _p(self.W1q), _p(self.W1s), _p(self.counts), _p(self.offsets), E, N1,
+                H, R, _p(self.dX_perm), self.sm_margin, st, s)),
+            ("quant_x_col", lambda: lib.moe_quantize_mxfp8(
+                _p(self.x_perm), 1, R, H, 1, _p(self.counts), _p(self.offsets), E, _p(self.x_qc), _p(self.x_sc), s)),
+            ("quant_dy_col", lambda: lib.moe_quantize_mxfp8(
+                _p(dY_perm), 1, R, H, 1, _p(self.counts), _p(self.offsets), E, _p(self.dy_qc), _p(self.dy_sc), s)),
+            ("wgrad_w1", lambda: lib.moe_grouped_wgrad(
+                _p(self.d_qc), _p(self.d_sc), _p(self.x_qc), _p(self.x_sc), _p(self.counts), _p(self.offsets), E,
+                N1, H, R, _p(self.dW1), 0, self.sm_margin, st, s)),
+            ("wgrad_w2", lambda: lib.moe_grouped_wgrad(
+                _p(self.a_qc), _p(self.a_sc), _p(self.dy_qc), _p(self.dy_sc), _p(self.counts), _p(self.offsets),
+                E, F, H, R, _p(self.dW2), 0, self.sm_margin, st, s)),
+        ]
+
+    def step_calls(self, x, topk_idx, topk_prob, dY_perm):
+        return self.forward_calls(x, topk_idx, topk_prob) + self.backward_calls(dY_perm)
+
+    def run(self, calls, events=None):
+        """Issues the calls on the current stream; optional events[i] are
+        recorded before call i and events[-1] after the last one."""
+        for i, (name, fn) in enumerate(calls):
+            if events is not None:
+                events[i].record()
+            L.check(fn(), name)
+        if events is not None:
+            events[len(calls)].record()
+
+    def step(self, x, topk_idx, topk_prob, dY_perm):
+        self.run(self.step_calls(x, topk_idx, topk_prob, dY_perm))
+
+    def capture(self, x, topk_idx, topk_prob, dY_perm) -> torch.cuda.CUDAGraph:
+        """Captures one forward + backward step into a CUDA graph (global
+        capture mode: any host synchronisation inside would fail it)."""
+        calls = self.step_calls(x, topk_idx, topk_prob, dY_perm)
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.run(calls)  # warm-up outside capture (sets kernel attributes)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=s, capture_error_mode="global"):
+                self.run(self.step_calls(x, topk_idx, topk_prob, dY_perm))
+        torch.cuda.current_stream().wait_stream(s)
+        return g

@@ -20,6 +20,8 @@ Weights are N(0, 1/H) (variance) for both FC1 and FC2; x ~ N(0, 1).
 """
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass
 
 import numpy as np
@@ -55,7 +57,15 @@ class Workload:
     def R_cap(self) -> int:
         """Capacity of the permuted buffers: every assignment local plus
         up to 31 pad rows per expert, rounded up to a multiple of 128."""
-        r = self.T * self.k + self.E * 31
+        r = self.T * min(self.k, self.E) + self.E * 31
+        return (r + 127) // 128 * 128
+
+    def capped_R(self, factor: float) -> int:
+        """A smaller capacity for an expert-parallel shard: `factor` times the
+        expected number of local rows plus the padding (routing reports
+        MOE_ERR_CAPACITY if a batch ever exceeds it)."""
+        expect = self.T * self.k * self.E / self.n_experts
+        r = min(int(factor * expect), self.T * min(self.k, self.E)) + self.E * 31
         return (r + 127) // 128 * 128
 
 
@@ -78,6 +88,29 @@ def scaled(w: Workload, **kw) -> Workload:
 
 def _streams(seed: int, n: int):
     return [np.random.default_rng(s) for s in np.random.SeedSequence(seed).spawn(n)]
+
+
+_CHUNK = 1 << 22
+
+
+def _normal(ss: np.random.SeedSequence, shape, scale: float = 1.0) -> np.ndarray:
+    """float32 N(0, scale^2) of the given shape, filled in fixed chunks of 4M
+    values, each from its own child seed (so the values do not depend on the
+    number of threads that fill them)."""
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.float32)
+    nch = (n + _CHUNK - 1) // _CHUNK
+    seeds = ss.spawn(nch)
+
+    def fill(i):
+        seg = out[i * _CHUNK:min(n, (i + 1) * _CHUNK)]
+        np.random.default_rng(seeds[i]).standard_normal(seg.shape[0], dtype=np.float32, out=seg)
+        if scale != 1.0:
+            seg *= np.float32(scale)
+
+    with ThreadPoolExecutor(max_workers=min(32, os.cpu_count() or 1)) as ex:
+        list(ex.map(fill, range(nch)))
+    return out.reshape(shape)
 
 
 def _bf16(a: np.ndarray) -> torch.Tensor:
@@ -115,7 +148,7 @@ def router_inputs(w: Workload, rng: np.random.Generator):
     return idx, p
 
 
-def make_inputs(w: Workload, seed: int = 0) -> dict:
+def make_inputs(w: Workload, seed: int = 0, R_cap: int | None = None) -> dict:
     """All inputs of one forward + backward step as CPU torch tensors.
 
     x bf16 [T, H]; topk_idx int32 [T, k]; topk_prob f32 [T, k];
@@ -123,17 +156,17 @@ def make_inputs(w: Workload, seed: int = 0) -> dict:
     b1 bf16 [E, N1] or None; W2 bf16 [E, F, H] (y = a @ W2_e);
     dY bf16 [R_cap, H] (gradient arriving at the FC2 output, per permuted
     row; rows that turn out to be padding are ignored by the path)."""
-    rs = _streams(seed, 6)
+    ss = np.random.SeedSequence(seed).spawn(6)
     sd = 1.0 / np.sqrt(w.H)
     out = {}
-    out["x"] = _bf16(rs[0].standard_normal((w.T, w.H), dtype=np.float32))
-    idx, p = router_inputs(w, rs[1])
+    out["x"] = _bf16(_normal(ss[0], (w.T, w.H)))
+    idx, p = router_inputs(w, np.random.default_rng(ss[1]))
     out["topk_idx"] = torch.from_numpy(idx)
     out["topk_prob"] = torch.from_numpy(p)
-    out["W1"] = _bf16(rs[2].standard_normal((w.E, w.N1, w.H), dtype=np.float32) * np.float32(sd))
-    out["W2"] = _bf16(rs[3].standard_normal((w.E, w.F, w.H), dtype=np.float32) * np.float32(sd))
-    out["b1"] = _bf16(rs[4].standard_normal((w.E, w.N1), dtype=np.float32) * np.float32(0.02)) if w.bias else None
-    out["dY"] = _bf16(rs[5].standard_normal((w.R_cap, w.H), dtype=np.float32))
+    out["W1"] = _bf16(_normal(ss[2], (w.E, w.N1, w.H), sd))
+    out["W2"] = _bf16(_normal(ss[3], (w.E, w.F, w.H), sd))
+    out["b1"] = _bf16(_normal(ss[4], (w.E, w.N1), 0.02)) if w.bias else None
+    out["dY"] = _bf16(_normal(ss[5], (R_cap or w.R_cap, w.H)))
     return out
 
 

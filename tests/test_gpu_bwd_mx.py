@@ -1,0 +1,188 @@
+"""GPU parity of the fused backward GroupGemm + dActivation + Quantize/Transpose
+and of the block-scaled MXFP8 grouped GEMMs (FC2 forward, data gradient,
+weight gradient) against the oracle, each fed the same synthetic inputs."""
+import numpy as np
+import pytest
+import torch
+
+from grouped_gemm_glu_gb300 import lib as L
+from grouped_gemm_glu_gb300 import ops, synth
+from oracle import moe_oracle as O
+from parity import assert_bf16_close, assert_mx_close, np_
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _routing(w, seed=0, counts=None):
+    if counts is not None:
+        ids = np.concatenate([np.full(c, e) for e, c in enumerate(counts)]).astype(np.int32)
+        np.random.default_rng(seed).shuffle(ids)
+        idx = ids.reshape(-1, 1)
+    else:
+        idx, _ = synth.router_inputs(w, synth._streams(seed, 1)[0])
+    rt = O.route(idx, w.expert_begin, w.E)
+    cnt = torch.from_numpy(rt.counts.astype(np.int32)).to(DEV)
+    off = torch.from_numpy(rt.offsets.astype(np.int32)).to(DEV)
+    return rt, cnt, off
+
+
+def _act(w):
+    if w.gpt_oss:
+        return (L.glu_params("swiglu", alpha=1.702, up_offset=1.0, gate_lo=-7.0, gate_hi=7.0),
+                O.ActParams(O.ACT_SWIGLU, alpha=1.702, up_offset=1.0, gate_lo=-7.0, gate_hi=7.0))
+    m = {"swiglu": O.ACT_SWIGLU, "geglu": O.ACT_GEGLU, "srelu": O.ACT_SRELU}
+    return L.glu_params(w.act), O.ActParams(m[w.act])
+
+
+def _dglu_case(w, rows=None, counts=None, seed=0, out_mode=L.OUT_MXFP8):
+    rt, cnt, off = _routing(w, seed, counts)
+    inp = synth.make_inputs(w, seed)
+    rng = np.random.default_rng(seed + 100)
+    pre = synth._bf16(rng.standard_normal((w.R_cap, w.N1), dtype=np.float32) * 2.0)
+    gp, op = _act(w)
+    o = ops.dglu_bwd(inp["dY"].to(DEV), inp["W2"].to(DEV), pre.to(DEV), cnt, off, w.F, gp, out_mode)
+    torch.cuda.synchronize()
+    assert ops.read_status(o["status"]) == 0
+    dY, W2, pr = inp["dY"], inp["W2"], np_(pre)
+    w2_cache = {}
+    blocks = rows if rows is not None else list(range(0, rt.R_pad, 32))
+    acc = {k: [] for k in ("qg", "sg", "qr", "sr", "v", "qcg", "scg", "qcr", "scr", "vc")}
+    for r0 in blocks:
+        rr = np.arange(r0, r0 + 32)
+        e = int(rt.expert_of_row[r0])
+        real = rt.tok_of[rr] >= 0
+        if e not in w2_cache:
+            w2_cache = {e: np_(W2[e])}
+        da = np_(dY[r0:r0 + 32]) @ w2_cache[e].T
+        if w.gated:
+            u, g = O.unpack_glu_cols(pr[rr])
+            du, dg = O.act_bwd(u, g, da, op)
+            d = O.pack_glu_cols(du, dg)
+        else:
+            d, _ = O.act_bwd(pr[rr], None, da, op)
+        d[~real] = 0
+        d = d.astype(np.float32)
+        if out_mode == L.OUT_BF16:
+            assert_bf16_close(np_(o["y"][r0:r0 + 32]), O.bf16_round(d), f"dFC1 rows {r0}")
+            continue
+        q, s = O.mx_quantize_rows(d)
+        qc, sc = O.mx_quantize_cols(d)
+        acc["qg"].append(np_(o["q_row"][r0:r0 + 32]))
+        acc["sg"].append(np_(o["s_row"][r0:r0 + 32]))
+        acc["qr"].append(q)
+        acc["sr"].append(s)
+        acc["v"].append(d)
+        acc["qcg"].append(np_(o["q_col"][:, r0:r0 + 32]))
+        acc["scg"].append(np_(o["s_col"][:, r0 // 32:r0 // 32 + 1]))
+        acc["qcr"].append(qc)
+        acc["scr"].append(sc)
+        acc["vc"].append(d.T)
+    if out_mode == L.OUT_MXFP8:
+        cat = {k: np.concatenate(v) for k, v in acc.items()}
+        assert_mx_close(cat["qg"], cat["sg"], cat["qr"], cat["sr"], cat["v"], f"{w.name} dFC1 row-wise")
+        assert_mx_close(cat["qcg"], cat["scg"], cat["qcr"], cat["scr"], cat["vc"], f"{w.name} dFC1 col-wise")
+
+
+@pytest.mark.parametrize("out_mode", [L.OUT_MXFP8, L.OUT_BF16])
+def test_dglu_tiny_full(out_mode):
+    _dglu_case(synth.WORKLOADS["tiny"], out_mode=out_mode)
+
+
+def test_dglu_edge_counts():
+    counts = [0, 1, 31, 32, 33, 127, 128, 129, 255, 256, 257, 0]
+    w = synth.Workload("edge", sum(counts), 128, len(counts), len(counts), 1, 96, "swiglu", "mxfp8", "normal")
+    _dglu_case(w, counts=counts)
+
+
+def test_dglu_gptoss_tail():
+    w = synth.scaled(synth.WORKLOADS["gptoss"], T=512)
+    _dglu_case(w)
+
+
+def test_dglu_srelu():
+    w = synth.scaled(synth.WORKLOADS["skew_srelu"], T=512, H=512)
+    _dglu_case(w)
+
+
+def test_dglu_dsv3_full_size_sampled():
+    w = synth.WORKLOADS["dsv3"]
+    rt, _, _ = _routing(w)
+    blocks = sorted({int(rt.offsets[e]) for e in range(w.E) if rt.counts[e]} |
+                    {int(rt.offsets[e + 1]) - 32 for e in range(w.E) if rt.counts[e]})
+    _dglu_case(w, rows=blocks)
+
+
+def _fc2_case(E, K, N, counts, seed, experts=None, n_cols=None):
+    """Block-scaled grouped GEMM on random MXFP8 operands; the oracle
+    dequantises (exact) and multiplies in float64.  experts / n_cols limit
+    the comparison to some experts and a random subset of columns."""
+    w = synth.Workload("fc2", sum(counts), 64, E, E, 1, 64, "swiglu", "mxfp8", "normal")
+    rt, cnt, off = _routing(w, seed, counts)
+    R_cap = w.R_cap
+    Aq, As = synth.random_mxfp8(R_cap, K, seed + 1)
+    Wq, Ws = synth.random_mxfp8(E * N, K, seed + 2)
+    Wq, Ws = Wq.view(E, N, K), Ws.view(E, N, K // 32)
+    y = ops.fc2_fwd(Aq.to(DEV), As.to(DEV), Wq.to(DEV), Ws.to(DEV), cnt, off)
+    torch.cuda.synchronize()
+    yg = np_(y)
+    cols = np.arange(N) if n_cols is None else np.sort(np.random.default_rng(seed).choice(N, n_cols, replace=False))
+    for e in (range(E) if experts is None else experts):
+        r0, n, r1 = int(rt.offsets[e]), int(rt.counts[e]), int(rt.offsets[e + 1])
+        A = O.mx_dequantize(Aq[r0:r0 + n].numpy(), As[r0:r0 + n].numpy())
+        W = O.mx_dequantize(Wq[e][cols].numpy(), Ws[e][cols].numpy())
+        assert_bf16_close(yg[r0:r0 + n][:, cols], O.bf16_round(A @ W.T), f"fc2 expert {e}")
+        assert np.all(yg[r0 + n:r1] == 0), "pad rows must be zero"
+
+
+def test_fc2_block_scaled_edge_counts():
+    _fc2_case(6, 256, 256, [0, 1, 33, 128, 129, 300], 1)
+
+
+def test_fc2_dsv3_shape():
+    # FC2 of the DeepSeek-V3 shard: K = F = 2048, N = H = 7168, ~256 rows per expert
+    _fc2_case(32, 2048, 7168, list(np.random.default_rng(2).integers(200, 320, 32)), 2,
+              experts=(0, 13, 31), n_cols=512)
+
+
+def test_dx_shape():
+    # data gradient dX = dFC1 . W1p: K = 2F = 4096
+    _fc2_case(4, 4096, 1024, [100, 0, 257, 64], 3)
+
+
+@pytest.mark.parametrize("out_f32", [True, False])
+def test_wgrad_edge_counts(out_f32):
+    counts = [0, 1, 31, 32, 33, 127, 128, 129, 200, 0]
+    E, M, N = len(counts), 256, 384
+    w = synth.Workload("wg", sum(counts), 64, E, E, 1, 64, "swiglu", "mxfp8", "normal")
+    rt, cnt, off = _routing(w, 4, counts)
+    R_cap = w.R_cap
+    Aq, As = synth.random_mxfp8(M, R_cap, 5)
+    Bq, Bs = synth.random_mxfp8(N, R_cap, 6)
+    D = ops.wgrad(Aq.to(DEV), As.to(DEV), Bq.to(DEV), Bs.to(DEV), cnt, off, out_f32=out_f32)
+    torch.cuda.synchronize()
+    ref = O.grouped_wgrad(O.mx_dequantize(Aq.numpy(), As.numpy()), O.mx_dequantize(Bq.numpy(), Bs.numpy()), rt)
+    got = np_(D)
+    assert_bf16_close(got, ref if out_f32 else O.bf16_round(ref), "wgrad")
+    for e, c in enumerate(counts):
+        if c == 0:
+            assert np.all(got[e] == 0)
+
+
+def test_wgrad_dsv3_dw2_shape_sampled_experts():
+    # dW2 of the DeepSeek-V3 shard: [E, F=2048, H=7168], K = rows of each expert
+    w = synth.WORKLOADS["dsv3"]
+    rt, cnt, off = _routing(w)
+    F, H = 2048, 7168
+    Aq, As = synth.random_mxfp8(F, w.R_cap, 7)
+    Bq, Bs = synth.random_mxfp8(H, w.R_cap, 8)
+    D = ops.wgrad(Aq.to(DEV), As.to(DEV), Bq.to(DEV), Bs.to(DEV), cnt, off, out_f32=False)
+    torch.cuda.synchronize()
+    Aq, As, Bq, Bs = Aq.numpy(), As.numpy(), Bq.numpy(), Bs.numpy()
+    for e in (0, 7, 31):
+        r0, r1 = int(rt.offsets[e]), int(rt.offsets[e + 1])
+        sl = np.random.default_rng(e).choice(F, 64, replace=False)
+        A = O.mx_dequantize(Aq[sl][:, r0:r1], As[sl][:, r0 // 32:r1 // 32])
+        B = O.mx_dequantize(Bq[:, r0:r1], Bs[:, r0 // 32:r1 // 32])
+        ref = A @ B.T
+        assert_bf16_close(np_(D[e])[sl], O.bf16_round(ref), f"dW2 expert {e}")
