@@ -16,6 +16,8 @@
 //                   prob_perm
 //   k_permute_gather one warp per permuted row: 16-byte copies of x rows,
 //                   zero fill of pad rows
+#include <mutex>
+
 #include "common.cuh"
 #include "host_common.h"
 
@@ -320,5 +322,81 @@ extern "C" moe_status_t moe_repack_fc1(const moe_bf16* W1, moe_bf16* W1p, int E,
   dim3 grid(2 * F, E);
   k_repack_fc1<<<grid, 128, 0, as_stream(stream)>>>(W1, W1p, F, H, inverse);
   count_launch();
+  return launch_status();
+}
+
+// ---------------------------------------------------------------------------
+// Routing without any device allocation.
+//
+// Some callers cannot allocate device memory at the point where they route
+// tokens: an inference or training runtime that reserves all GPU memory up
+// front in its own pool, or code running inside a driver-level callback
+// where cudaMalloc is not allowed.  For them, moe_route_permute_noalloc
+// keeps its per-chunk scratch (the stable rank bases and the overflow flag)
+// in the file-scope array below instead of a caller-provided workspace.
+// The array is part of the library image: every GPU that loads the library
+// holds ROUTE_STATIC_SCRATCH_BYTES of it until the process exits.
+// ---------------------------------------------------------------------------
+namespace moeglu {
+
+constexpr size_t ROUTE_STATIC_SCRATCH_BYTES = 1u << 20;  // 1 MiB
+static __device__ __align__(256) int32_t g_route_scratch[ROUTE_STATIC_SCRATCH_BYTES / sizeof(int32_t)];
+
+// Device address of g_route_scratch, looked up once per device.  On the
+// host the name g_route_scratch is only a stand-in for the device symbol,
+// never a usable address, so the address must come from the runtime.
+static int32_t* route_scratch_ptr() {
+  static std::mutex mu;
+  static int32_t* ptrs[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (ptrs[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int32_t*>(p);
+  }
+  return ptrs[dev];
+}
+
+}  // namespace moeglu
+
+extern "C" size_t moe_route_noalloc_max_scratch_bytes(void) { return moeglu::ROUTE_STATIC_SCRATCH_BYTES; }
+
+extern "C" moe_status_t moe_route_permute_noalloc(const moe_bf16* x, const int32_t* topk_idx, const float* topk_prob,
+                                                  int T, int H, int k, int expert_begin, int E, int R_cap,
+                                                  moe_bf16* x_perm, int32_t* row_of, int32_t* tok_of,
+                                                  float* prob_perm, int32_t* counts, int32_t* offsets,
+                                                  int32_t* status, moe_stream_t stream) {
+  using namespace moeglu;
+  if (!x || !topk_idx || !topk_prob || !x_perm || !row_of || !tok_of || !prob_perm || !counts || !offsets)
+    return MOE_ERR_ARG;
+  if (T <= 0 || H <= 0 || (H & 7) || k <= 0 || k > 64 || E <= 0 || E > ROUTE_E_MAX || R_cap <= 0 || (R_cap & 31))
+    return MOE_ERR_ARG;
+  if ((int64_t)T * k > (int64_t)INT32_MAX / 2) return MOE_ERR_ARG;
+  if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_ARG;
+  // the scratch this routing needs must fit the fixed array
+  if (moe_route_workspace_size(T, k, E) > ROUTE_STATIC_SCRATCH_BYTES) return MOE_ERR_ARG;
+  int32_t* scratch = route_scratch_ptr();
+  if (!scratch) return MOE_ERR_CUDA;
+  cudaStream_t s = as_stream(stream);
+  const int n_assign = T * k;
+  const int n_chunks = route_chunks(T, k);
+  int32_t* chunk_counts = scratch;  // every entry is written by k_route_count before it is read
+  int32_t* overflow = chunk_counts + (size_t)n_chunks * E;  // written by k_route_scan before it is read
+  k_route_count<<<n_chunks, ROUTE_THREADS, 0, s>>>(topk_idx, n_assign, expert_begin, E, chunk_counts);
+  k_route_scan<<<1, 1024, 0, s>>>(chunk_counts, n_chunks, E, R_cap, counts, offsets, overflow, status);
+  const int scatter_smem = ROUTE_WARPS * E * (int)sizeof(int32_t);
+  if (scatter_smem > 48 * 1024 && !set_smem_limit((const void*)k_route_scatter, scatter_smem)) return MOE_ERR_CUDA;
+  k_route_scatter<<<n_chunks, ROUTE_THREADS, scatter_smem, s>>>(topk_idx, topk_prob, n_assign, k, expert_begin, E,
+                                                                 chunk_counts, offsets, overflow, row_of, tok_of,
+                                                                 prob_perm);
+  const int sms = sm_count();
+  int grid = (R_cap + 7) / 8;
+  if (grid > sms * 8) grid = sms * 8;
+  if (grid < 1) grid = 1;
+  k_permute_gather<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), H / 8, E, counts, offsets, overflow,
+                                        tok_of, prob_perm, reinterpret_cast<uint4*>(x_perm));
+  count_launch(4);
   return launch_status();
 }

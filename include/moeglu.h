@@ -241,6 +241,31 @@ MOE_API moe_status_t moe_glu_act(const moe_bf16* pre, const int32_t* counts, con
                          int E, int F, int R_cap, const moe_glu_params_t* params,
                          moe_bf16* y, moe_stream_t stream);
 
+/* moe_route_permute without a workspace argument and without any device
+ * allocation, for callers that cannot allocate device memory when they route
+ * (a runtime that owns all GPU memory in its own pool, or code running where
+ * cudaMalloc is not allowed).  The pages describe no such entry point: it is
+ * a convenience of this library, not part of the method.
+ * Same arguments, results and status semantics as moe_route_permute minus
+ * ws/ws_bytes.  Its scratch is a fixed 1 MiB array inside the library
+ * (moe_route_noalloc_max_scratch_bytes()), present on every GPU that loads
+ * the library until the process exits; a routing whose scratch
+ * (moe_route_workspace_size(T, k, E)) exceeds it returns MOE_ERR_ARG.
+ * The first call on each device looks up that array's device address
+ * (cudaGetSymbolAddress) with the device current; make that first call
+ * before any stream capture.  All calls share the one array: calls that
+ * may run at the same time on the GPU (different streams, or several host
+ * threads) race on it and must be serialised by the caller.  Nothing in the
+ * array needs to start at zero: each call writes every entry it reads. */
+MOE_API moe_status_t moe_route_permute_noalloc(const moe_bf16* x, const int32_t* topk_idx, const float* topk_prob,
+                                               int T, int H, int k, int expert_begin, int E, int R_cap,
+                                               moe_bf16* x_perm, int32_t* row_of, int32_t* tok_of,
+                                               float* prob_perm, int32_t* counts, int32_t* offsets,
+                                               int32_t* status, moe_stream_t stream);
+
+/* Size in bytes of the fixed scratch array used by moe_route_permute_noalloc. */
+MOE_API size_t moe_route_noalloc_max_scratch_bytes(void);
+
 /* Copies the device status word to *host_out (synchronises `stream`; not
  * for use inside a graph capture). */
 MOE_API moe_status_t moe_get_status(const int32_t* status, int32_t* host_out, moe_stream_t stream);
