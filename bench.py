@@ -277,7 +277,8 @@ def main():
 
     if args.experts:
         base = synth.scaled(base, E=args.experts)
-    w = synth.scaled(base, expert_begin=(rank * base.E) % base.n_experts)
+    from grouped_gemm_glu_gb300 import shard
+    w = synth.scaled(base, expert_begin=shard.shard_expert_begin(rank, base.E, base.n_experts))
     R_cap = w.capped_R(CAPACITY_FACTOR)
     inp = synth.make_inputs(w, seed=0, R_cap=R_cap)
     host = {k: inp[k].pin_memory() for k in ("x", "topk_idx", "topk_prob", "dY")}

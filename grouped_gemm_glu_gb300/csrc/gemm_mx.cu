@@ -25,7 +25,7 @@
 namespace moeglu {
 namespace gmx {
 
-constexpr int BM = 128, BN = 128, BK = 128, STAGES = 6;
+constexpr int BM = 128, BN = 128, BK = 128, STAGES = 5;
 constexpr int EPI_WARPS = 4;
 constexpr int PRODUCER_WARP = 4, MMA_WARP = 5, SF_WARP = 6;
 constexpr int THREADS = 7 * 32;
@@ -36,8 +36,12 @@ constexpr int SF_STAGE = 1024;  // 512 bytes of A scales + 512 of B scales
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SFA_COL = 2 * BN, SFB_COL = 2 * BN + 4;
 constexpr int E_MAX = 1024;
+constexpr int SF_PREFETCH = 4;                   // stages the scale loader runs ahead
+constexpr int EPI_ROW_BYTES = 256 + 16;          // staged output row (64 words + pad)
+constexpr int EPI_WARP_BYTES = 32 * EPI_ROW_BYTES;
 constexpr int OFF_SF = STAGES * STAGE_BYTES;
-constexpr int OFF_PREF = OFF_SF + STAGES * SF_STAGE;
+constexpr int OFF_EPI = OFF_SF + STAGES * SF_STAGE;
+constexpr int OFF_PREF = OFF_EPI + EPI_WARPS * EPI_WARP_BYTES;
 constexpr int OFF_BARS = OFF_PREF + (E_MAX + 2) * 4;
 constexpr int NUM_BARS = 2 * STAGES + 5;
 constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
@@ -104,12 +108,82 @@ __device__ __forceinline__ Tile decode(int t, const int32_t* pref, const Args& a
   return ti;
 }
 
+// Walks the (tile, k-block) stages of this CTA in the order the producer and
+// the MMA issuer consume them (tiles without k-blocks contribute none).
+struct StageIter {
+  int t, kb, total;
+  Tile ti;
+  bool valid;
+};
+
+__device__ __forceinline__ void stage_iter_settle(StageIter& it, const int32_t* pref, const Args& a) {
+  while (it.t < it.total) {
+    it.ti = decode(it.t, pref, a);
+    if (it.ti.num_kb > 0) {
+      it.valid = true;
+      return;
+    }
+    it.t += gridDim.x;
+  }
+  it.valid = false;
+}
+
+__device__ __forceinline__ void stage_iter_init(StageIter& it, int total, const int32_t* pref, const Args& a) {
+  it.t = blockIdx.x;
+  it.kb = 0;
+  it.total = total;
+  stage_iter_settle(it, pref, a);
+}
+
+__device__ __forceinline__ void stage_iter_next(StageIter& it, const int32_t* pref, const Args& a) {
+  if (++it.kb < it.ti.num_kb) return;
+  it.kb = 0;
+  it.t += gridDim.x;
+  stage_iter_settle(it, pref, a);
+}
+
+// The 4 scale bytes (k sub-blocks 0..3 of k-block kb) of A rows
+// m0+32j+lane and B rows n0+32j+lane, j = 0..3.
+__device__ __forceinline__ void load_scales(const StageIter& it, const Args& a, int lane, uint32_t* v) {
+  const Tile& ti = it.ti;
+  if (!a.kgrouped) {
+    const int ks = a.K / 32;
+    const int kbyte = it.kb * 4;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int r = ti.m0 + 32 * j + lane;
+      v[j] = (r < a.R_cap) ? __ldg(reinterpret_cast<const uint32_t*>(a.As + (size_t)r * ks + kbyte)) : 0u;
+      const int n = ti.n0 + 32 * j + lane;
+      v[4 + j] = __ldg(reinterpret_cast<const uint32_t*>(a.Bs + ((size_t)ti.e * a.N + n) * ks + kbyte));
+    }
+  } else {
+    const int ks = a.R_cap / 32;
+    const int kbyte = ti.kseg0 / 32 + it.kb * 4;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint8_t* pa = a.As + (size_t)(ti.m0 + 32 * j + lane) * ks;
+      const uint8_t* pb = a.Bs + (size_t)(ti.n0 + 32 * j + lane) * ks;
+      uint32_t x = 0, y = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (kbyte + i < ks) {
+          x |= (uint32_t)__ldg(pa + kbyte + i) << (8 * i);
+          y |= (uint32_t)__ldg(pb + kbyte + i) << (8 * i);
+        }
+      }
+      v[j] = x;
+      v[4 + j] = y;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(THREADS, 1)
     k_grouped_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Args a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* tiles = smem;
   uint8_t* sf = smem + OFF_SF;
+  uint8_t* epi_all = smem + OFF_EPI;
   int32_t* pref = reinterpret_cast<int32_t*>(smem + OFF_PREF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BARS);
   uint64_t* full = bars;
@@ -214,13 +288,26 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
   } else if (warp == SF_WARP) {
+    // Scale loader: global loads run SF_PREFETCH stages ahead of the
+    // shared-memory writes, so their latency overlaps the pipeline.
+    StageIter cs, pf;
+    stage_iter_init(cs, total, pref, a);
+    pf = cs;
+    uint32_t ring[SF_PREFETCH][8];
+#pragma unroll
+    for (int d = 0; d < SF_PREFETCH; ++d) {
+      if (pf.valid) {
+        load_scales(pf, a, lane, ring[d]);
+        stage_iter_next(pf, pref, a);
+      }
+    }
     int stage = 0;
     uint32_t phase = 0;
-    const int ks = a.kgrouped ? a.R_cap / 32 : a.K / 32;  // scale bytes per row
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const Tile ti = decode(t, pref, a);
-      bool ok = true;
-      for (int kb = 0; kb < ti.num_kb; ++kb) {
+    bool ok = true;
+    while (cs.valid && ok) {
+#pragma unroll
+      for (int d = 0; d < SF_PREFETCH; ++d) {
+        if (!cs.valid) break;
         int w = 1;
         if (lane == 0) w = mbar_wait(empty + stage, phase ^ 1u, guard) ? 1 : 0;
         w = __shfl_sync(0xFFFFFFFFu, w, 0);
@@ -228,37 +315,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           ok = false;
           break;
         }
-        uint32_t va[4], vb[4];
-        if (!a.kgrouped) {
-          const int kbyte = kb * 4;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int r = ti.m0 + 32 * j + lane;
-            va[j] = (r < a.R_cap) ? __ldg(reinterpret_cast<const uint32_t*>(a.As + (size_t)r * ks + kbyte)) : 0u;
-            const int n = ti.n0 + 32 * j + lane;
-            vb[j] = __ldg(reinterpret_cast<const uint32_t*>(a.Bs + ((size_t)ti.e * a.N + n) * ks + kbyte));
-          }
-        } else {
-          const int kbyte = ti.kseg0 / 32 + kb * 4;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint8_t* pa = a.As + (size_t)(ti.m0 + 32 * j + lane) * ks;
-            const uint8_t* pb = a.Bs + (size_t)(ti.n0 + 32 * j + lane) * ks;
-            uint32_t x = 0, y = 0;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              if (kbyte + i < ks) {
-                x |= (uint32_t)__ldg(pa + kbyte + i) << (8 * i);
-                y |= (uint32_t)__ldg(pb + kbyte + i) << (8 * i);
-              }
-            }
-            va[j] = x;
-            vb[j] = y;
-          }
-        }
         uint4* dsa = reinterpret_cast<uint4*>(sf + stage * SF_STAGE);
-        dsa[lane] = make_uint4(va[0], va[1], va[2], va[3]);
-        dsa[32 + lane] = make_uint4(vb[0], vb[1], vb[2], vb[3]);
+        dsa[lane] = make_uint4(ring[d][0], ring[d][1], ring[d][2], ring[d][3]);
+        dsa[32 + lane] = make_uint4(ring[d][4], ring[d][5], ring[d][6], ring[d][7]);
         fence_async_shared();
         __syncwarp();
         if (lane == 0) mbar_arrive(full + stage);
@@ -266,8 +325,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           stage = 0;
           phase ^= 1u;
         }
+        stage_iter_next(cs, pref, a);
+        if (pf.valid) {
+          load_scales(pf, a, lane, ring[d]);
+          stage_iter_next(pf, pref, a);
+        }
       }
-      if (!ok) break;
     }
   } else if (warp == MMA_WARP) {
     if (lane == 0) {
@@ -327,39 +390,56 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const Tile ti = decode(t, pref, a);
       const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
-      const int r_local = q * 32 + lane;
       if (q * 32 < ti.rows_pad) {
-        const bool real = r_local < ti.rows_valid;
+        const bool real = q * 32 + lane < ti.rows_valid;
         const bool empty_k = ti.num_kb == 0;
+        uint8_t* stg = epi_all + q * EPI_WARP_BYTES;
+        const int out_es = (a.kgrouped && a.out_f32) ? 4 : 2;      // output element size
+        const int chunk_cols = 256 / out_es;                        // columns per staged pass
+        // each pass stages 32 rows x 256 bytes, then stores them row by row
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          float v[32];
-          if (!empty_k) tmem_ld32(tacc + c * 32, v);
-          if (empty_k || !real) {
+        for (int c0 = 0; c0 < BN; c0 += chunk_cols) {
+#pragma unroll 1
+          for (int c = c0; c < c0 + chunk_cols; c += 32) {
+            float v[32];
+            if (!empty_k) tmem_ld32(tacc + c, v);
+            if (empty_k || !real) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-          }
-          if (!a.kgrouped) {
-            uint16_t* y = reinterpret_cast<uint16_t*>(a.out) + (size_t)(ti.m0 + r_local) * a.N + ti.n0 + c * 32;
-            uint4* d = reinterpret_cast<uint4*>(y);
+              for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+            }
+            uint8_t* dst = stg + lane * EPI_ROW_BYTES + (c - c0) * out_es;
+            if (out_es == 4) {
 #pragma unroll
-            for (int w = 0; w < 4; ++w)
-              d[w] = make_uint4(pack_bf16x2(v[8 * w], v[8 * w + 1]), pack_bf16x2(v[8 * w + 2], v[8 * w + 3]),
-                                pack_bf16x2(v[8 * w + 4], v[8 * w + 5]), pack_bf16x2(v[8 * w + 6], v[8 * w + 7]));
-          } else {
-            const size_t off = ((size_t)ti.e * a.M + ti.m0 + r_local) * a.N + ti.n0 + c * 32;
-            if (a.out_f32) {
-              float4* d = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + off);
-#pragma unroll
-              for (int w = 0; w < 8; ++w) d[w] = make_float4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
+              for (int w = 0; w < 8; ++w)
+                reinterpret_cast<float4*>(dst)[w] = make_float4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
             } else {
-              uint4* d = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + off);
 #pragma unroll
               for (int w = 0; w < 4; ++w)
-                d[w] = make_uint4(pack_bf16x2(v[8 * w], v[8 * w + 1]), pack_bf16x2(v[8 * w + 2], v[8 * w + 3]),
-                                  pack_bf16x2(v[8 * w + 4], v[8 * w + 5]), pack_bf16x2(v[8 * w + 6], v[8 * w + 7]));
+                reinterpret_cast<uint4*>(dst)[w] =
+                    make_uint4(pack_bf16x2(v[8 * w], v[8 * w + 1]), pack_bf16x2(v[8 * w + 2], v[8 * w + 3]),
+                               pack_bf16x2(v[8 * w + 4], v[8 * w + 5]), pack_bf16x2(v[8 * w + 6], v[8 * w + 7]));
             }
           }
+          __syncwarp();
+          // 2 rows per instruction, 16 lanes x 16 bytes each: full 128-byte lines
+          const int half = lane >> 4, ch = lane & 15;
+#pragma unroll 4
+          for (int rr = 0; rr < 32; rr += 2) {
+            const int row = rr + half;
+            const int r_local = q * 32 + row;
+            if (r_local < ti.rows_pad) {
+              const uint4 val = *reinterpret_cast<const uint4*>(stg + row * EPI_ROW_BYTES + ch * 16);
+              uint8_t* g;
+              if (!a.kgrouped)
+                g = reinterpret_cast<uint8_t*>(a.out) +
+                    ((size_t)(ti.m0 + r_local) * a.N + ti.n0 + c0) * 2;
+              else
+                g = reinterpret_cast<uint8_t*>(a.out) +
+                    (((size_t)ti.e * a.M + ti.m0 + r_local) * a.N + ti.n0 + c0) * out_es;
+              *reinterpret_cast<uint4*>(g + ch * 16) = val;
+            }
+          }
+          __syncwarp();
         }
       }
       tc_fence_before();

@@ -88,42 +88,64 @@ __global__ void __launch_bounds__(256) k_quant_rows(const uint16_t* __restrict__
   }
 }
 
-// Column-wise (transposed): a CTA covers 32 rows x 256 columns; lane c of
-// warp w owns column 32w + c and quantises its 32 values (one MX block).
+// Column-wise (transposed).  A CTA owns a tile of 32 rows (one MX block
+// along R) x 256 columns: it reads the tile with coalesced 16-byte loads
+// into shared memory (rows padded by 16 bytes so column reads are free of
+// bank conflicts), then thread c quantises column c's 32 values and writes
+// its 32 codes (one full 32-byte sector) to q[c][r0 .. r0+32).
+constexpr int QC_COLS = 256;
+constexpr int QC_ROW_BYTES = QC_COLS * 2 + 16;
+
 __global__ void __launch_bounds__(256) k_quant_cols(const uint16_t* __restrict__ src, int G, int R, int Cc,
                                                     const int32_t* __restrict__ counts,
                                                     const int32_t* __restrict__ offsets, int E,
                                                     uint8_t* __restrict__ q, uint8_t* __restrict__ s) {
   __shared__ int32_t s_off[QE_MAX + 1];
   __shared__ int32_t s_cnt[QE_MAX];
+  __shared__ __align__(16) uint8_t tile[32 * QC_ROW_BYTES];
   if (E > 0) load_seg(counts, offsets, E, s_off, s_cnt);
-  const int col_tiles = (Cc + 255) / 256;
+  const int col_tiles = (Cc + QC_COLS - 1) / QC_COLS;
   const int row_blocks = R / 32;
   const size_t total = (size_t)G * row_blocks * col_tiles;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = threadIdx.x;
   for (size_t i = blockIdx.x; i < total; i += gridDim.x) {
     const int ct = (int)(i % col_tiles);
     const size_t rest = i / col_tiles;
     const int rbk = (int)(rest % row_blocks);
     const int g = (int)(rest / row_blocks);
     const int r0 = rbk * 32;
-    const int c = ct * 256 + warp * 32 + lane;
     int real = 32;
     if (E > 0) {
       real = block_real_rows(r0, s_off, s_cnt, E);
       if (real < 0) continue;  // uniform over the CTA
     }
-    if (c >= Cc) continue;
-    float v[32];
-    const uint16_t* base = src + ((size_t)g * R + r0) * Cc + c;
+    const int c0 = ct * QC_COLS;
+    // load: 32 rows x 32 chunks of 16 bytes; thread t covers chunk t%32 of rows t/32, t/32+8, ...
+    const int ch = t & 31;
+    const bool ch_ok = c0 + ch * 8 < Cc;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = j < real ? __uint_as_float((uint32_t)__ldg(base + (size_t)j * Cc) << 16) : 0.0f;
-    uint32_t codes[8];
-    const uint32_t sb = mx_quant_block32(v, codes);
-    uint4* dq = reinterpret_cast<uint4*>(q + ((size_t)g * Cc + c) * R + r0);
-    dq[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-    dq[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-    s[((size_t)g * Cc + c) * (R / 32) + rbk] = (uint8_t)sb;
+    for (int rr = 0; rr < 4; ++rr) {
+      const int r = (t >> 5) + rr * 8;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (ch_ok && r < real)
+        v = __ldg(reinterpret_cast<const uint4*>(src + ((size_t)g * R + r0 + r) * Cc + c0 + ch * 8));
+      *reinterpret_cast<uint4*>(tile + r * QC_ROW_BYTES + ch * 16) = v;
+    }
+    __syncthreads();
+    const int c = c0 + t;
+    if (c < Cc) {
+      float v[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        v[j] = __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t*>(tile + j * QC_ROW_BYTES + t * 2)) << 16);
+      uint32_t codes[8];
+      const uint32_t sb = mx_quant_block32(v, codes);
+      uint4* dq = reinterpret_cast<uint4*>(q + ((size_t)g * Cc + c) * R + r0);
+      dq[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+      dq[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+      s[((size_t)g * Cc + c) * (R / 32) + rbk] = (uint8_t)sb;
+    }
+    __syncthreads();
   }
 }
 
@@ -217,8 +239,8 @@ extern "C" moe_status_t moe_quantize_mxfp8(const moe_bf16* src, int G, int R, in
     if (Cc % 32) return MOE_ERR_ARG;
     k_quant_rows<<<grid_for((size_t)G * R * (Cc / 32), 256), 256, 0, st>>>(src, G, R, Cc, counts, offsets, E, q, s);
   } else {
-    if (R % 32) return MOE_ERR_ARG;
-    const size_t tiles = (size_t)G * (R / 32) * ((Cc + 255) / 256);
+    if ((R % 32) || (Cc % 8)) return MOE_ERR_ARG;
+    const size_t tiles = (size_t)G * (R / 32) * ((Cc + QC_COLS - 1) / QC_COLS);
     k_quant_cols<<<grid_for(tiles, 1), 256, 0, st>>>(src, G, R, Cc, counts, offsets, E, q, s);
   }
   count_launch();
