@@ -8,16 +8,22 @@
 // (B_q / s_B) with fine-grained per-block scales folded into the GEMM;
 // §4.3: grouped problems over contiguous expert rows.)
 //
-// CTA = 7 warps, one per SM, persistent over tiles t = blockIdx.x + i*gridDim.x:
-//   warps 0-3  epilogue (thread = accumulator row): fp32 -> bf16 / fp32 stores
-//   warp  4    TMA producer: A and B tiles of 128 x 128 bytes, 128-byte swizzle
-//   warp  5    TMEM owner + MMA issuer: per k-block, tcgen05.cp of the A and
-//              B scale tiles into tensor memory, then 4 MMAs of K = 32
-//              (M=128, N=128) selecting scale byte k of each 32-bit column
-//   warp  6    scale loader: gathers the 4 scale bytes of each of the 128 A
-//              rows and 128 B rows of the k-block into shared memory in the
-//              order tcgen05.cp expects (16-byte row r holds rows r, r+32,
-//              r+64, r+96), fences it to the async proxy and arrives
+// Two launches per call:
+//   k_sf_tile     rewrites the row-major E8M0 scales of the tiles the GEMM
+//                 will visit into the order tcgen05.cp consumes: for every
+//                 (128-row tile, 128-element k-block) 512 contiguous bytes,
+//                 byte 16*l + 4*j + i = scale of row 32*j + l, k sub-block i
+//                 (a gather done by thousands of warps in parallel)
+//   k_grouped_mx  persistent GEMM, 6 warps, one CTA per SM:
+//     warps 0-3  epilogue (thread = accumulator row): one wait for all 128
+//                columns, frees the accumulator, then bf16 / fp32 rows staged
+//                in shared memory and stored as full 128-byte lines
+//     warp  4    TMA producer: A and B tiles of 128 x 128 bytes (128-byte
+//                swizzle) and the two 512-byte scale blocks (1-D bulk
+//                copies), all completing on the stage's mbarrier
+//     warp  5    TMEM owner + MMA issuer: tcgen05.cp of the scale blocks into
+//                tensor memory, then 4 MMAs of K = 32 (M = N = 128) selecting
+//                scale byte k of each 32-bit column
 // Every wait is bounded (MOE_ERR_TIMEOUT + early exit, never a trap).
 #include "common.cuh"
 #include "host_common.h"
@@ -27,17 +33,17 @@ namespace gmx {
 
 constexpr int BM = 128, BN = 128, BK = 128, STAGES = 5;
 constexpr int EPI_WARPS = 4;
-constexpr int PRODUCER_WARP = 4, MMA_WARP = 5, SF_WARP = 6;
-constexpr int THREADS = 7 * 32;
+constexpr int PRODUCER_WARP = 4, MMA_WARP = 5;
+constexpr int THREADS = 6 * 32;
 constexpr int A_TILE = BM * BK;
 constexpr int B_TILE = BN * BK;
 constexpr int STAGE_BYTES = A_TILE + B_TILE;
-constexpr int SF_STAGE = 1024;  // 512 bytes of A scales + 512 of B scales
+constexpr int SF_BLOCK = 512;             // one (128-row tile, k-block) of scales
+constexpr int SF_STAGE = 2 * SF_BLOCK;    // A then B
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SFA_COL = 2 * BN, SFB_COL = 2 * BN + 4;
 constexpr int E_MAX = 1024;
-constexpr int SF_PREFETCH = 4;                   // stages the scale loader runs ahead
-constexpr int EPI_ROW_BYTES = 256 + 16;          // staged output row (64 words + pad)
+constexpr int EPI_ROW_BYTES = 256 + 16;   // staged output row (64 words + pad)
 constexpr int EPI_WARP_BYTES = 32 * EPI_ROW_BYTES;
 constexpr int OFF_SF = STAGES * STAGE_BYTES;
 constexpr int OFF_EPI = OFF_SF + STAGES * SF_STAGE;
@@ -53,20 +59,72 @@ struct Args {
   const int32_t* offsets;
   int E, M, N, K, R_cap;   // K: fixed contraction (M-grouped); M: rows of A (K-grouped)
   int kgrouped;            // 0: FC2 / dX, 1: weight gradient
-  int n_tiles_n, m_tiles;  // tiles along N; along M (K-grouped only)
-  const uint8_t* As;       // A scales
-  const uint8_t* Bs;       // B scales
+  int n_tiles_n, m_tiles;  // tiles along N; along M (K-grouped)
+  int KB;                  // M-grouped: k-blocks per row tile (K / 128)
+  int KG;                  // K-grouped: stride of the k-block axis of the tiled scales
+  const uint8_t* As;       // scales, row-major (input of k_sf_tile)
+  const uint8_t* Bs;
+  uint8_t* sfa_t;          // scales in MMA order (output of k_sf_tile)
+  uint8_t* sfb_t;
   void* out;               // bf16 [R_cap][N] or D [E][M][N] (f32 or bf16)
   int out_f32;
   int32_t* status;
   uint64_t wait_ns;
 };
 
+// Prefix in shared memory: M-grouped -> 128-row tiles per expert (from
+// counts); K-grouped -> 128-row k-blocks per expert (from the padded
+// segment lengths).  pref[0..E], exclusive.  Uses all threads of the CTA.
+__device__ __forceinline__ void build_prefix(const Args& a, int32_t* pref, int nthreads) {
+  const int E = a.E;
+  for (int e = threadIdx.x; e < E; e += nthreads) {
+    int v;
+    if (!a.kgrouped) {
+      v = (__ldg(a.counts + e) + BM - 1) / BM;
+    } else {
+      const int seg = __ldg(a.offsets + e + 1) - __ldg(a.offsets + e);
+      v = seg > 0 ? (seg + BK - 1) / BK : 0;
+    }
+    pref[e + 1] = max(v, 0);
+  }
+  if (threadIdx.x == 0) pref[0] = 0;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int per = (E + 31) / 32;
+    const int beg = 1 + lane * per, end = min(E + 1, beg + per);
+    int s = 0;
+    for (int i = beg; i < end; ++i) s += pref[i];
+    int incl = s;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    int run = incl - s;
+    for (int i = beg; i < end; ++i) {
+      run += pref[i];
+      pref[i] = run;
+    }
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ int find_group(const int32_t* pref, int E, int x) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pref[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 struct Tile {
-  int e, m0, n0;           // expert, first A row (M-grouped: permuted row), first column
+  int e, m0, n0;             // expert, first A row (M-grouped: permuted row), first column
   int rows_valid, rows_pad;  // M-grouped row masks
-  int kseg0, kseg;         // K-grouped: first row of the expert segment and its padded length
+  int kseg0, kseg;           // contraction start (K-grouped: segment's first row) and length
   int num_kb;
+  size_t sfa, sfb;           // byte offsets of the tile's first scale blocks
 };
 
 __device__ __forceinline__ Tile decode(int t, const int32_t* pref, const Args& a) {
@@ -92,91 +150,144 @@ __device__ __forceinline__ Tile decode(int t, const int32_t* pref, const Args& a
     ti.kseg0 = 0;
     ti.kseg = a.K;
     ti.num_kb = a.K / BK;
+    ti.sfa = (size_t)(pref[lo] + m_idx) * a.KB * SF_BLOCK;
+    ti.sfb = ((size_t)lo * a.n_tiles_n + n_idx) * a.KB * SF_BLOCK;
   } else {
     const int per_e = a.m_tiles * a.n_tiles_n;
     ti.e = t / per_e;
     const int local = t - ti.e * per_e;
     const int m_idx = local / a.n_tiles_n;
+    const int n_idx = local - m_idx * a.n_tiles_n;
     ti.m0 = m_idx * BM;
-    ti.n0 = (local - m_idx * a.n_tiles_n) * BN;
+    ti.n0 = n_idx * BN;
     ti.rows_valid = ti.rows_pad = BM;
     const int o0 = __ldg(a.offsets + ti.e), o1 = __ldg(a.offsets + ti.e + 1);
     ti.kseg0 = o0;
     ti.kseg = (o0 < 0 || o1 > a.R_cap || o1 < o0) ? 0 : o1 - o0;
     ti.num_kb = (ti.kseg + BK - 1) / BK;
+    ti.sfa = ((size_t)m_idx * a.KG + pref[ti.e]) * SF_BLOCK;
+    ti.sfb = ((size_t)n_idx * a.KG + pref[ti.e]) * SF_BLOCK;
   }
   return ti;
 }
 
-// Walks the (tile, k-block) stages of this CTA in the order the producer and
-// the MMA issuer consume them (tiles without k-blocks contribute none).
-struct StageIter {
-  int t, kb, total;
-  Tile ti;
-  bool valid;
-};
-
-__device__ __forceinline__ void stage_iter_settle(StageIter& it, const int32_t* pref, const Args& a) {
-  while (it.t < it.total) {
-    it.ti = decode(it.t, pref, a);
-    if (it.ti.num_kb > 0) {
-      it.valid = true;
-      return;
-    }
-    it.t += gridDim.x;
-  }
-  it.valid = false;
+// ---------------------------------------------------------------------------
+// Scale re-tiling.  One warp per 512-byte block; lane l gathers the 4 scale
+// bytes of rows 32j + l (j = 0..3) and writes its 16 bytes.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t load4_unaligned(const uint8_t* row, int kbyte, int ks) {
+  // bytes row[kbyte .. kbyte+3]; bytes at or past ks read as 0.  ks % 4 == 0.
+  const int w0 = kbyte & ~3, sh = (kbyte & 3) * 8;
+  const uint32_t lo = w0 < ks ? __ldg(reinterpret_cast<const uint32_t*>(row + w0)) : 0u;
+  const uint32_t hi = (sh != 0 && w0 + 4 < ks) ? __ldg(reinterpret_cast<const uint32_t*>(row + w0 + 4)) : 0u;
+  return sh == 0 ? lo : __funnelshift_r(lo, hi, sh);
 }
 
-__device__ __forceinline__ void stage_iter_init(StageIter& it, int total, const int32_t* pref, const Args& a) {
-  it.t = blockIdx.x;
-  it.kb = 0;
-  it.total = total;
-  stage_iter_settle(it, pref, a);
-}
-
-__device__ __forceinline__ void stage_iter_next(StageIter& it, const int32_t* pref, const Args& a) {
-  if (++it.kb < it.ti.num_kb) return;
-  it.kb = 0;
-  it.t += gridDim.x;
-  stage_iter_settle(it, pref, a);
-}
-
-// The 4 scale bytes (k sub-blocks 0..3 of k-block kb) of A rows
-// m0+32j+lane and B rows n0+32j+lane, j = 0..3.
-__device__ __forceinline__ void load_scales(const StageIter& it, const Args& a, int lane, uint32_t* v) {
-  const Tile& ti = it.ti;
+__global__ void __launch_bounds__(256) k_sf_tile(const Args a) {
+  __shared__ int32_t pref[E_MAX + 2];
+  build_prefix(a, pref, blockDim.x);
+  if (__ldg(a.offsets + a.E) > a.R_cap) return;
+  const int lane = threadIdx.x & 31;
+  const int warps = blockDim.x >> 5;
+  size_t nA, nB;
+  int ktot = 0;
   if (!a.kgrouped) {
-    const int ks = a.K / 32;
-    const int kbyte = it.kb * 4;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int r = ti.m0 + 32 * j + lane;
-      v[j] = (r < a.R_cap) ? __ldg(reinterpret_cast<const uint32_t*>(a.As + (size_t)r * ks + kbyte)) : 0u;
-      const int n = ti.n0 + 32 * j + lane;
-      v[4 + j] = __ldg(reinterpret_cast<const uint32_t*>(a.Bs + ((size_t)ti.e * a.N + n) * ks + kbyte));
-    }
+    const int mt_cap = a.R_cap / BM + a.E;
+    nA = (size_t)min(pref[a.E], mt_cap) * a.KB;
+    nB = (size_t)a.E * a.n_tiles_n * a.KB;
   } else {
-    const int ks = a.R_cap / 32;
-    const int kbyte = ti.kseg0 / 32 + it.kb * 4;
+    ktot = min(pref[a.E], a.KG);
+    nA = (size_t)a.m_tiles * ktot;
+    nB = (size_t)a.n_tiles_n * ktot;
+  }
+  const size_t total = nA + nB;
+  for (size_t it = (size_t)blockIdx.x * warps + (threadIdx.x >> 5); it < total; it += (size_t)gridDim.x * warps) {
+    uint32_t v[4];
+    uint8_t* dst;
+    if (!a.kgrouped) {
+      const int ks = a.K / 32;
+      if (it < nA) {
+        const int mt = (int)(it / a.KB), kb = (int)(it % a.KB);
+        const int e = find_group(pref, a.E, mt);
+        const int m0 = __ldg(a.offsets + e) + (mt - pref[e]) * BM;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint8_t* pa = a.As + (size_t)(ti.m0 + 32 * j + lane) * ks;
-      const uint8_t* pb = a.Bs + (size_t)(ti.n0 + 32 * j + lane) * ks;
-      uint32_t x = 0, y = 0;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if (kbyte + i < ks) {
-          x |= (uint32_t)__ldg(pa + kbyte + i) << (8 * i);
-          y |= (uint32_t)__ldg(pb + kbyte + i) << (8 * i);
+        for (int j = 0; j < 4; ++j) {
+          const int r = m0 + 32 * j + lane;
+          v[j] = (r >= 0 && r < a.R_cap) ? __ldg(reinterpret_cast<const uint32_t*>(a.As + (size_t)r * ks + kb * 4))
+                                         : 0u;
         }
+        dst = a.sfa_t + it * SF_BLOCK;
+      } else {
+        const size_t jb = it - nA;
+        const int kb = (int)(jb % a.KB);
+        const size_t rest = jb / a.KB;
+        const int nt = (int)(rest % a.n_tiles_n), e = (int)(rest / a.n_tiles_n);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int n = nt * BN + 32 * j + lane;
+          v[j] = __ldg(reinterpret_cast<const uint32_t*>(a.Bs + ((size_t)e * a.N + n) * ks + kb * 4));
+        }
+        dst = a.sfb_t + jb * SF_BLOCK;
       }
-      v[j] = x;
-      v[4 + j] = y;
+    } else {
+      const int ks = a.R_cap / 32;
+      const bool isA = it < nA;
+      const size_t jb = isA ? it : it - nA;
+      const int rt = (int)(jb / ktot), kg = (int)(jb % ktot);
+      const int e = find_group(pref, a.E, kg);
+      const int kbyte = __ldg(a.offsets + e) / 32 + (kg - pref[e]) * 4;
+      const uint8_t* base = isA ? a.As : a.Bs;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = rt * BM + 32 * j + lane;
+        v[j] = load4_unaligned(base + (size_t)r * ks, kbyte, ks);
+      }
+      dst = (isA ? a.sfa_t : a.sfb_t) + ((size_t)rt * a.KG + kg) * SF_BLOCK;
     }
+    reinterpret_cast<uint4*>(dst)[lane] = make_uint4(v[0], v[1], v[2], v[3]);
   }
 }
 
+// Epilogue pass: stages 32 rows x 256 bytes of this warp's accumulator rows
+// (fp32: columns P..P+63; bf16: all 128) in shared memory and stores them as
+// full 128-byte lines, 2 rows per instruction.
+template <bool F32, int P>
+__device__ __forceinline__ void store_pass(const Args& a, const Tile& ti, const float* v, uint8_t* stg, int q,
+                                           int lane) {
+  if (F32) {
+    float4* d = reinterpret_cast<float4*>(stg + lane * EPI_ROW_BYTES);
+#pragma unroll
+    for (int w = 0; w < 16; ++w) d[w] = make_float4(v[P + 4 * w], v[P + 4 * w + 1], v[P + 4 * w + 2], v[P + 4 * w + 3]);
+  } else {
+    uint4* d = reinterpret_cast<uint4*>(stg + lane * EPI_ROW_BYTES);
+#pragma unroll
+    for (int w = 0; w < 16; ++w)
+      d[w] = make_uint4(pack_bf16x2(v[8 * w], v[8 * w + 1]), pack_bf16x2(v[8 * w + 2], v[8 * w + 3]),
+                        pack_bf16x2(v[8 * w + 4], v[8 * w + 5]), pack_bf16x2(v[8 * w + 6], v[8 * w + 7]));
+  }
+  __syncwarp();
+  const int es = F32 ? 4 : 2;
+  const int half = lane >> 4, ch = lane & 15;
+#pragma unroll 4
+  for (int rr = 0; rr < 32; rr += 2) {
+    const int row = rr + half;
+    const int r_local = q * 32 + row;
+    if (r_local < ti.rows_pad) {
+      const uint4 val = *reinterpret_cast<const uint4*>(stg + row * EPI_ROW_BYTES + ch * 16);
+      uint8_t* g;
+      if (!a.kgrouped)
+        g = reinterpret_cast<uint8_t*>(a.out) + ((size_t)(ti.m0 + r_local) * a.N + ti.n0 + P) * es;
+      else
+        g = reinterpret_cast<uint8_t*>(a.out) + (((size_t)ti.e * a.M + ti.m0 + r_local) * a.N + ti.n0 + P) * es;
+      *reinterpret_cast<uint4*>(g + ch * 16) = val;
+    }
+  }
+  __syncwarp();
+}
+
+// ---------------------------------------------------------------------------
+// The GEMM
+// ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(THREADS, 1)
     k_grouped_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Args a) {
   extern __shared__ uint8_t smem_raw[];
@@ -199,7 +310,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == PRODUCER_WARP && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full + s, 2);   // TMA transaction arrival + scale loader
+      mbar_init(full + s, 1);
       mbar_init(empty + s, 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -217,35 +328,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
   }
-  int total = 0;
-  bool over = false;
-  if (!a.kgrouped) {
-    for (int e = threadIdx.x; e < E; e += THREADS) pref[e + 1] = (__ldg(a.counts + e) + BM - 1) / BM;
-    if (threadIdx.x == 0) pref[0] = 0;
-    __syncthreads();
-    if (warp == 0) {
-      const int per = (E + 31) / 32;
-      const int beg = 1 + lane * per, end = min(E + 1, beg + per);
-      int s = 0;
-      for (int i = beg; i < end; ++i) s += pref[i];
-      int incl = s;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-        if (lane >= d) incl += v;
-      }
-      int run = incl - s;
-      for (int i = beg; i < end; ++i) {
-        run += pref[i];
-        pref[i] = run;
-      }
-    }
-  }
+  build_prefix(a, pref, THREADS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  over = __ldg(a.offsets + E) > a.R_cap;
+  const bool over = __ldg(a.offsets + E) > a.R_cap;
   if (over && threadIdx.x == 0) set_status(a.status, MOE_ERR_CAPACITY);
+  int total = 0;
   if (!over) total = a.kgrouped ? E * a.m_tiles * a.n_tiles_n : pref[E] * a.n_tiles_n;
   const uint32_t tmem_base = *tmem_slot;
   WaitGuard guard{abort_flag, a.status, a.wait_ns};
@@ -263,7 +352,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           uint8_t* dst = tiles + stage * STAGE_BYTES;
-          mbar_arrive_expect_tx(full + stage, STAGE_BYTES);
+          uint8_t* sdst = sf + stage * SF_STAGE;
+          mbar_arrive_expect_tx(full + stage, STAGE_BYTES + SF_STAGE);
           if (!a.kgrouped) {
             tma_load_2d(dst, &tmA, full + stage, kb * BK, ti.m0);
             tma_load_3d(dst + A_TILE, &tmB, full + stage, kb * BK, ti.n0, ti.e);
@@ -271,6 +361,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             tma_load_2d(dst, &tmA, full + stage, ti.kseg0 + kb * BK, ti.m0);
             tma_load_2d(dst + A_TILE, &tmB, full + stage, ti.kseg0 + kb * BK, ti.n0);
           }
+          bulk_load(sdst, a.sfa_t + ti.sfa + (size_t)kb * SF_BLOCK, SF_BLOCK, full + stage);
+          bulk_load(sdst + SF_BLOCK, a.sfb_t + ti.sfb + (size_t)kb * SF_BLOCK, SF_BLOCK, full + stage);
           issued |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -285,51 +377,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         WaitGuard drain{&never, a.status, 100000000ull};
         for (int s = 0; s < STAGES; ++s)
           if (issued & (1u << s)) mbar_wait(full + s, (issued_parity >> s) & 1u, drain);
-      }
-    }
-  } else if (warp == SF_WARP) {
-    // Scale loader: global loads run SF_PREFETCH stages ahead of the
-    // shared-memory writes, so their latency overlaps the pipeline.
-    StageIter cs, pf;
-    stage_iter_init(cs, total, pref, a);
-    pf = cs;
-    uint32_t ring[SF_PREFETCH][8];
-#pragma unroll
-    for (int d = 0; d < SF_PREFETCH; ++d) {
-      if (pf.valid) {
-        load_scales(pf, a, lane, ring[d]);
-        stage_iter_next(pf, pref, a);
-      }
-    }
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    while (cs.valid && ok) {
-#pragma unroll
-      for (int d = 0; d < SF_PREFETCH; ++d) {
-        if (!cs.valid) break;
-        int w = 1;
-        if (lane == 0) w = mbar_wait(empty + stage, phase ^ 1u, guard) ? 1 : 0;
-        w = __shfl_sync(0xFFFFFFFFu, w, 0);
-        if (!w) {
-          ok = false;
-          break;
-        }
-        uint4* dsa = reinterpret_cast<uint4*>(sf + stage * SF_STAGE);
-        dsa[lane] = make_uint4(ring[d][0], ring[d][1], ring[d][2], ring[d][3]);
-        dsa[32 + lane] = make_uint4(ring[d][4], ring[d][5], ring[d][6], ring[d][7]);
-        fence_async_shared();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(full + stage);
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
-        stage_iter_next(cs, pref, a);
-        if (pf.valid) {
-          load_scales(pf, a, lane, ring[d]);
-          stage_iter_next(pf, pref, a);
-        }
       }
     }
   } else if (warp == MMA_WARP) {
@@ -356,7 +403,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t b_addr = a_addr + A_TILE;
           const uint32_t sf_addr = smem_u32(sf + stage * SF_STAGE);
           tc_cp_32x128b_x4(tmem_base + SFA_COL, sdesc_noswizzle(sf_addr, 128));
-          tc_cp_32x128b_x4(tmem_base + SFB_COL, sdesc_noswizzle(sf_addr + 512, 128));
+          tc_cp_32x128b_x4(tmem_base + SFB_COL, sdesc_noswizzle(sf_addr + SF_BLOCK, 128));
           const int nsub = min(4, (ti.kseg - kb * BK) / 32);
           for (int k = 0; k < nsub; ++k) {
             umma_mxf8(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32), sdesc_kmajor_sw128(b_addr + k * 32),
@@ -379,6 +426,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     const int q = warp;
+    uint8_t* stg = epi_all + q * EPI_WARP_BYTES;
+    const int out_es = (a.kgrouped && a.out_f32) ? 4 : 2;  // output element size
     int lt = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
       const int buf = lt & 1;
@@ -389,62 +438,25 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       const Tile ti = decode(t, pref, a);
-      const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
-      if (q * 32 < ti.rows_pad) {
-        const bool real = q * 32 + lane < ti.rows_valid;
-        const bool empty_k = ti.num_kb == 0;
-        uint8_t* stg = epi_all + q * EPI_WARP_BYTES;
-        const int out_es = (a.kgrouped && a.out_f32) ? 4 : 2;      // output element size
-        const int chunk_cols = 256 / out_es;                        // columns per staged pass
-        // each pass stages 32 rows x 256 bytes, then stores them row by row
-#pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += chunk_cols) {
-#pragma unroll 1
-          for (int c = c0; c < c0 + chunk_cols; c += 32) {
-            float v[32];
-            if (!empty_k) tmem_ld32(tacc + c, v);
-            if (empty_k || !real) {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-            }
-            uint8_t* dst = stg + lane * EPI_ROW_BYTES + (c - c0) * out_es;
-            if (out_es == 4) {
-#pragma unroll
-              for (int w = 0; w < 8; ++w)
-                reinterpret_cast<float4*>(dst)[w] = make_float4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
-            } else {
-#pragma unroll
-              for (int w = 0; w < 4; ++w)
-                reinterpret_cast<uint4*>(dst)[w] =
-                    make_uint4(pack_bf16x2(v[8 * w], v[8 * w + 1]), pack_bf16x2(v[8 * w + 2], v[8 * w + 3]),
-                               pack_bf16x2(v[8 * w + 4], v[8 * w + 5]), pack_bf16x2(v[8 * w + 6], v[8 * w + 7]));
-            }
-          }
-          __syncwarp();
-          // 2 rows per instruction, 16 lanes x 16 bytes each: full 128-byte lines
-          const int half = lane >> 4, ch = lane & 15;
-#pragma unroll 4
-          for (int rr = 0; rr < 32; rr += 2) {
-            const int row = rr + half;
-            const int r_local = q * 32 + row;
-            if (r_local < ti.rows_pad) {
-              const uint4 val = *reinterpret_cast<const uint4*>(stg + row * EPI_ROW_BYTES + ch * 16);
-              uint8_t* g;
-              if (!a.kgrouped)
-                g = reinterpret_cast<uint8_t*>(a.out) +
-                    ((size_t)(ti.m0 + r_local) * a.N + ti.n0 + c0) * 2;
-              else
-                g = reinterpret_cast<uint8_t*>(a.out) +
-                    (((size_t)ti.e * a.M + ti.m0 + r_local) * a.N + ti.n0 + c0) * out_es;
-              *reinterpret_cast<uint4*>(g + ch * 16) = val;
-            }
-          }
-          __syncwarp();
-        }
-      }
+      const bool live = q * 32 < ti.rows_pad;
+      const bool real = q * 32 + lane < ti.rows_valid;
+      float v[BN];
+      if (live && ti.num_kb > 0) tmem_ld128(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN), v);
+      // the accumulator is in registers: hand the buffer back to the MMA
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty + buf);
+      if (!live) continue;
+      if (ti.num_kb == 0 || !real) {
+#pragma unroll
+        for (int i = 0; i < BN; ++i) v[i] = 0.0f;
+      }
+      if (out_es == 4) {
+        store_pass<true, 0>(a, ti, v, stg, q, lane);
+        store_pass<true, 64>(a, ti, v, stg, q, lane);
+      } else {
+        store_pass<false, 0>(a, ti, v, stg, q, lane);
+      }
     }
   }
   tc_fence_before();
@@ -456,14 +468,33 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 static moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const Args& a, long long tiles_bound,
-                           int sm_margin, cudaStream_t stream) {
+                           long long sf_items, int sm_margin, cudaStream_t stream) {
   if (!set_smem_limit((const void*)k_grouped_mx, SMEM_BYTES)) return MOE_ERR_CUDA;
-  int grid = sm_count() - sm_margin;
+  const int sms = sm_count();
+  long long sgrid = (sf_items + 7) / 8;
+  if (sgrid > (long long)sms * 8) sgrid = (long long)sms * 8;
+  if (sgrid < 1) sgrid = 1;
+  k_sf_tile<<<(int)sgrid, 256, 0, stream>>>(a);
+  int grid = sms - sm_margin;
   if (grid > tiles_bound) grid = (int)tiles_bound;
   if (grid < 1) grid = 1;
   k_grouped_mx<<<grid, THREADS, SMEM_BYTES, stream>>>(tmA, tmB, a);
-  count_launch();
+  count_launch(2);
   return launch_status();
+}
+
+static size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
+
+static void fc2_ws_parts(int E, int K, int N, int R_cap, size_t* a_bytes, size_t* b_bytes) {
+  const size_t KB = (size_t)K / BK;
+  *a_bytes = align_up(((size_t)R_cap / BM + E) * KB * SF_BLOCK);
+  *b_bytes = align_up((size_t)E * (N / BN) * KB * SF_BLOCK);
+}
+
+static void wgrad_ws_parts(int E, int M, int N, int R_cap, size_t* a_bytes, size_t* b_bytes) {
+  const size_t KG = (size_t)R_cap / BK + E;
+  *a_bytes = align_up((size_t)(M / BM) * KG * SF_BLOCK);
+  *b_bytes = align_up((size_t)(N / BN) * KG * SF_BLOCK);
 }
 
 }  // namespace gmx
@@ -471,17 +502,34 @@ static moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const
 
 using namespace moeglu;
 
+extern "C" size_t moe_grouped_fc2_workspace_size(int E, int K, int N, int R_cap) {
+  if (E <= 0 || K <= 0 || N <= 0 || R_cap <= 0) return 0;
+  size_t a, b;
+  gmx::fc2_ws_parts(E, K, N, R_cap, &a, &b);
+  return a + b;
+}
+
+extern "C" size_t moe_grouped_wgrad_workspace_size(int E, int M, int N, int R_cap) {
+  if (E <= 0 || M <= 0 || N <= 0 || R_cap <= 0) return 0;
+  size_t a, b;
+  gmx::wgrad_ws_parts(E, M, N, R_cap, &a, &b);
+  return a + b;
+}
+
 extern "C" moe_status_t moe_grouped_fc2_fwd(const uint8_t* Aq, const uint8_t* As, const uint8_t* Wq,
                                             const uint8_t* Ws, const int32_t* counts, const int32_t* offsets, int E,
-                                            int K, int N, int R_cap, moe_bf16* y, int sm_margin, int32_t* status,
-                                            moe_stream_t stream) {
+                                            int K, int N, int R_cap, moe_bf16* y, void* ws, size_t ws_bytes,
+                                            int sm_margin, int32_t* status, moe_stream_t stream) {
   using namespace gmx;
-  if (!Aq || !As || !Wq || !Ws || !counts || !offsets || !y) return MOE_ERR_ARG;
+  if (!Aq || !As || !Wq || !Ws || !counts || !offsets || !y || !ws) return MOE_ERR_ARG;
   if (E <= 0 || E > E_MAX || K <= 0 || (K % BK) || N <= 0 || (N % BN) || R_cap <= 0 || (R_cap % BM))
     return MOE_ERR_ARG;
   if (!aligned16(Aq) || !aligned16(Wq) || !aligned16(y) || (reinterpret_cast<uintptr_t>(As) & 3) ||
-      (reinterpret_cast<uintptr_t>(Ws) & 3) || sm_margin < 0)
+      (reinterpret_cast<uintptr_t>(Ws) & 3) || (reinterpret_cast<uintptr_t>(ws) & 255) || sm_margin < 0)
     return MOE_ERR_ARG;
+  size_t a_bytes, b_bytes;
+  fc2_ws_parts(E, K, N, R_cap, &a_bytes, &b_bytes);
+  if (ws_bytes < a_bytes + b_bytes) return MOE_ERR_ARG;
   CUtensorMap tmA, tmB;
   {
     const uint64_t dims[2] = {(uint64_t)K, (uint64_t)R_cap};
@@ -508,25 +556,36 @@ extern "C" moe_status_t moe_grouped_fc2_fwd(const uint8_t* Aq, const uint8_t* As
   a.kgrouped = 0;
   a.n_tiles_n = N / BN;
   a.m_tiles = 0;
+  a.KB = K / BK;
+  a.KG = 0;
   a.As = As;
   a.Bs = Ws;
+  a.sfa_t = static_cast<uint8_t*>(ws);
+  a.sfb_t = static_cast<uint8_t*>(ws) + a_bytes;
   a.out = y;
   a.out_f32 = 0;
   a.status = status;
   a.wait_ns = g_wait_limit_ns.load();
-  const long long bound = ((long long)R_cap / BM + E) * (N / BN);
-  return launch(tmA, tmB, a, bound, sm_margin, as_stream(stream));
+  const long long mt_bound = (long long)R_cap / BM + E;
+  const long long bound = mt_bound * (N / BN);
+  const long long sf_items = mt_bound * a.KB + (long long)E * a.n_tiles_n * a.KB;
+  return launch(tmA, tmB, a, bound, sf_items, sm_margin, as_stream(stream));
 }
 
 extern "C" moe_status_t moe_grouped_wgrad(const uint8_t* Aq, const uint8_t* As, const uint8_t* Bq, const uint8_t* Bs,
                                           const int32_t* counts, const int32_t* offsets, int E, int M, int N,
-                                          int R_cap, void* D, int out_f32, int sm_margin, int32_t* status,
-                                          moe_stream_t stream) {
+                                          int R_cap, void* D, int out_f32, void* ws, size_t ws_bytes, int sm_margin,
+                                          int32_t* status, moe_stream_t stream) {
   using namespace gmx;
-  if (!Aq || !As || !Bq || !Bs || !counts || !offsets || !D) return MOE_ERR_ARG;
+  if (!Aq || !As || !Bq || !Bs || !counts || !offsets || !D || !ws) return MOE_ERR_ARG;
   if (E <= 0 || E > E_MAX || M <= 0 || (M % BM) || N <= 0 || (N % BN) || R_cap <= 0 || (R_cap % BM))
     return MOE_ERR_ARG;
-  if (!aligned16(Aq) || !aligned16(Bq) || !aligned16(D) || sm_margin < 0) return MOE_ERR_ARG;
+  if (!aligned16(Aq) || !aligned16(Bq) || !aligned16(D) || (reinterpret_cast<uintptr_t>(As) & 3) ||
+      (reinterpret_cast<uintptr_t>(Bs) & 3) || (reinterpret_cast<uintptr_t>(ws) & 255) || sm_margin < 0)
+    return MOE_ERR_ARG;
+  size_t a_bytes, b_bytes;
+  wgrad_ws_parts(E, M, N, R_cap, &a_bytes, &b_bytes);
+  if (ws_bytes < a_bytes + b_bytes) return MOE_ERR_ARG;
   CUtensorMap tmA, tmB;
   {
     const uint64_t dims[2] = {(uint64_t)R_cap, (uint64_t)M};
@@ -553,12 +612,17 @@ extern "C" moe_status_t moe_grouped_wgrad(const uint8_t* Aq, const uint8_t* As, 
   a.kgrouped = 1;
   a.n_tiles_n = N / BN;
   a.m_tiles = M / BM;
+  a.KB = 0;
+  a.KG = R_cap / BK + E;
   a.As = As;
   a.Bs = Bs;
+  a.sfa_t = static_cast<uint8_t*>(ws);
+  a.sfb_t = static_cast<uint8_t*>(ws) + a_bytes;
   a.out = D;
   a.out_f32 = out_f32 ? 1 : 0;
   a.status = status;
   a.wait_ns = g_wait_limit_ns.load();
   const long long bound = (long long)E * (M / BM) * (N / BN);
-  return launch(tmA, tmB, a, bound, sm_margin, as_stream(stream));
+  const long long sf_items = (long long)(M / BM + N / BN) * a.KG;
+  return launch(tmA, tmB, a, bound, sf_items, sm_margin, as_stream(stream));
 }

@@ -74,6 +74,14 @@ class MoeLayer:
         self.dy_qc, self.dy_sc = z(H, R_cap, dt=u8), z(H, R_cap // 32, dt=u8)
         self.dW1 = z(E, N1, H)
         self.dW2 = z(E, F, H)
+        # scale re-tiling workspaces of the block-scaled GEMMs (one per call
+        # site, so that no two calls of one step share one)
+        lib = self.lib
+        ws = lambda n: z(max(n, 256), dt=u8)
+        self.ws_fc2 = ws(lib.moe_grouped_fc2_workspace_size(E, F, H, R_cap))
+        self.ws_dx = ws(lib.moe_grouped_fc2_workspace_size(E, N1, H, R_cap))
+        self.ws_wg1 = ws(lib.moe_grouped_wgrad_workspace_size(E, N1, H, R_cap))
+        self.ws_wg2 = ws(lib.moe_grouped_wgrad_workspace_size(E, F, H, R_cap))
         self.fc1_out = L.ActOut(self.a_q.data_ptr(), self.a_s.data_ptr(), self.a_qc.data_ptr(),
                                 self.a_sc.data_ptr(), None, None, self.pre.data_ptr())
         self.bwd_out = L.ActOut(self.d_q.data_ptr(), self.d_s.data_ptr(), self.d_qc.data_ptr(),
@@ -96,7 +104,7 @@ class MoeLayer:
                 _p(self.W2), E, F, H, 1, None, None, 0, _p(self.W2q), _p(self.W2s), s)),
             ("fc2", lambda: lib.moe_grouped_fc2_fwd(
                 _p(self.a_q), _p(self.a_s), _p(self.W2q), _p(self.W2s), _p(self.counts), _p(self.offsets), E, F,
-                H, R, _p(self.y_perm), self.sm_margin, st, s)),
+                H, R, _p(self.y_perm), _p(self.ws_fc2), self.ws_fc2.numel(), self.sm_margin, st, s)),
             ("combine", lambda: lib.moe_unpermute_combine(
                 _p(self.y_perm), _p(self.row_of), _p(topk_prob), T, H, k, _p(self.out), st, s)),
         ]
@@ -113,17 +121,17 @@ class MoeLayer:
                 _p(self.W1p), E, N1, H, 1, None, None, 0, _p(self.W1q), _p(self.W1s), s)),
             ("dx", lambda: lib.moe_grouped_fc2_fwd(
                 _p(self.d_q), _p(self.d_s), _p(self.W1q), _p(self.W1s), _p(self.counts), _p(self.offsets), E, N1,
-                H, R, _p(self.dX_perm), self.sm_margin, st, s)),
+                H, R, _p(self.dX_perm), _p(self.ws_dx), self.ws_dx.numel(), self.sm_margin, st, s)),
             ("quant_x_col", lambda: lib.moe_quantize_mxfp8(
                 _p(self.x_perm), 1, R, H, 1, _p(self.counts), _p(self.offsets), E, _p(self.x_qc), _p(self.x_sc), s)),
             ("quant_dy_col", lambda: lib.moe_quantize_mxfp8(
                 _p(dY_perm), 1, R, H, 1, _p(self.counts), _p(self.offsets), E, _p(self.dy_qc), _p(self.dy_sc), s)),
             ("wgrad_w1", lambda: lib.moe_grouped_wgrad(
                 _p(self.d_qc), _p(self.d_sc), _p(self.x_qc), _p(self.x_sc), _p(self.counts), _p(self.offsets), E,
-                N1, H, R, _p(self.dW1), 0, self.sm_margin, st, s)),
+                N1, H, R, _p(self.dW1), 0, _p(self.ws_wg1), self.ws_wg1.numel(), self.sm_margin, st, s)),
             ("wgrad_w2", lambda: lib.moe_grouped_wgrad(
                 _p(self.a_qc), _p(self.a_sc), _p(self.dy_qc), _p(self.dy_sc), _p(self.counts), _p(self.offsets),
-                E, F, H, R, _p(self.dW2), 0, self.sm_margin, st, s)),
+                E, F, H, R, _p(self.dW2), 0, _p(self.ws_wg2), self.ws_wg2.numel(), self.sm_margin, st, s)),
         ]
 
     def step_calls(self, x, topk_idx, topk_prob, dY_perm):

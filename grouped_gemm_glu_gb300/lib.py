@@ -45,8 +45,10 @@ _SIGS = {
     "moe_grouped_fc1_glu_quant_fwd": [P, P, P, P, P, P, I, I, I, I, C.POINTER(GluParams), I, C.POINTER(ActOut), I, P, P],
     "moe_grouped_dglu_quant_bwd": [P, P, P, P, P, P, I, I, I, I, C.POINTER(GluParams), I, C.POINTER(ActOut), I, P, P],
     "moe_quantize_mxfp8": [P, I, I, I, I, P, P, I, P, P, P],
-    "moe_grouped_fc2_fwd": [P, P, P, P, P, P, I, I, I, I, P, I, P, P],
-    "moe_grouped_wgrad": [P, P, P, P, P, P, I, I, I, I, P, I, I, P, P],
+    "moe_grouped_fc2_workspace_size": ([I, I, I, I], SZ),
+    "moe_grouped_fc2_fwd": [P, P, P, P, P, P, I, I, I, I, P, P, SZ, I, P, P],
+    "moe_grouped_wgrad_workspace_size": ([I, I, I, I], SZ),
+    "moe_grouped_wgrad": [P, P, P, P, P, P, I, I, I, I, P, I, P, SZ, I, P, P],
     "moe_unpermute_combine": [P, P, P, I, I, I, P, P, P],
     "moe_nvfp4_cast": [P, P, P, P, I, I, I, P, P, P, P],
     "moe_glu_act": [P, P, P, I, I, I, C.POINTER(GluParams), P, P],

@@ -168,8 +168,10 @@ def fc2_fwd(Aq, As, Wq, Ws, counts, offsets, sm_margin: int = 0, status=None, ou
     E, N, _ = Wq.shape
     y = out if out is not None else torch.empty(R_cap, N, dtype=torch.bfloat16, device=dev)
     st = status if status is not None else new_status(dev)
+    ws_bytes = lib.moe_grouped_fc2_workspace_size(E, K, N, R_cap)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     L.check(lib.moe_grouped_fc2_fwd(_p(Aq), _p(As), _p(Wq), _p(Ws), _p(counts), _p(offsets), E, K, N, R_cap,
-                                    _p(y), sm_margin, _p(st), _s()), "moe_grouped_fc2_fwd")
+                                    _p(y), _p(ws), ws_bytes, sm_margin, _p(st), _s()), "moe_grouped_fc2_fwd")
     return y
 
 
@@ -185,8 +187,11 @@ def wgrad(Aq_col, As_col, Bq_col, Bs_col, counts, offsets, out_f32: bool = False
     D = out if out is not None else torch.empty(E, M, N, dtype=torch.float32 if out_f32 else torch.bfloat16,
                                                 device=dev)
     st = status if status is not None else new_status(dev)
+    ws_bytes = lib.moe_grouped_wgrad_workspace_size(E, M, N, R_cap)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     L.check(lib.moe_grouped_wgrad(_p(Aq_col), _p(As_col), _p(Bq_col), _p(Bs_col), _p(counts), _p(offsets), E, M,
-                                  N, R_cap, _p(D), int(out_f32), sm_margin, _p(st), _s()), "moe_grouped_wgrad")
+                                  N, R_cap, _p(D), int(out_f32), _p(ws), ws_bytes, sm_margin, _p(st), _s()),
+            "moe_grouped_wgrad")
     return D
 
 

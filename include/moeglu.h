@@ -189,18 +189,27 @@ MOE_API moe_status_t moe_quantize_mxfp8(const moe_bf16* src, int G, int R, int C
                                 const int32_t* counts, const int32_t* offsets, int E,
                                 uint8_t* q, uint8_t* s, moe_stream_t stream);
 
+/* Bytes of device workspace moe_grouped_fc2_fwd needs (the scales of the
+ * visited tiles, rewritten in the order the tensor cores read them). */
+MOE_API size_t moe_grouped_fc2_workspace_size(int E, int K, int N, int R_cap);
+
 /* GroupGemm (+ bf16 out), block-scaled MXFP8 ([MoE-Fusion] GroupGemm +
  * Quantize family; [MegaMoE] §2.3: C ~ (A_q/s_A)(B_q/s_B)).
  * y[rows of e] = dequant(Aq,As)[rows] . dequant(Wq[e],Ws[e])^T, fp32
  * accumulate, bf16 out; pad rows 0.  Serves FC2 (K = F, N = H) and the
  * data-gradient GEMM dX = dFC1 . W1p (K = N1, N = H).
  * Aq [R_cap][K], As [R_cap][K/32], Wq [E][N][K], Ws [E][N][K/32].
+ * ws: moe_grouped_fc2_workspace_size() bytes, 256-byte aligned.
  * K % 128 == 0, N % 128 == 0. */
 MOE_API moe_status_t moe_grouped_fc2_fwd(const uint8_t* Aq, const uint8_t* As,
                                  const uint8_t* Wq, const uint8_t* Ws,
                                  const int32_t* counts, const int32_t* offsets,
                                  int E, int K, int N, int R_cap,
-                                 moe_bf16* y, int sm_margin, int32_t* status, moe_stream_t stream);
+                                 moe_bf16* y, void* ws, size_t ws_bytes,
+                                 int sm_margin, int32_t* status, moe_stream_t stream);
+
+/* Bytes of device workspace moe_grouped_wgrad needs. */
+MOE_API size_t moe_grouped_wgrad_workspace_size(int E, int M, int N, int R_cap);
 
 /* Weight-gradient grouped GEMM, contraction over each expert's rows
  * (variable K = the expert's padded row count).  Inputs are the
@@ -208,13 +217,15 @@ MOE_API moe_status_t moe_grouped_fc2_fwd(const uint8_t* Aq, const uint8_t* As,
  * Bq [N][R_cap], Bs [N][R_cap/32].  D[e] = A[:, seg e] . B[:, seg e]^T,
  * written as f32 (out_f32 != 0) or bf16 into D [E][M][N].
  * dW1p = wgrad(dFC1 col, x col); dW2 = wgrad(a col, dY col).
+ * ws: moe_grouped_wgrad_workspace_size() bytes, 256-byte aligned.
+ * Pad rows of each segment must hold zero codes (the quantizers write them).
  * M % 128 == 0, N % 128 == 0. */
 MOE_API moe_status_t moe_grouped_wgrad(const uint8_t* Aq, const uint8_t* As,
                                const uint8_t* Bq, const uint8_t* Bs,
                                const int32_t* counts, const int32_t* offsets,
                                int E, int M, int N, int R_cap,
-                               void* D, int out_f32, int sm_margin, int32_t* status,
-                               moe_stream_t stream);
+                               void* D, int out_f32, void* ws, size_t ws_bytes,
+                               int sm_margin, int32_t* status, moe_stream_t stream);
 
 /* Unpermute + combine ([MegaMoE] §2.1: y = sum_{i in topk} p_i E_i(x)).
  * out[t] = bf16( sum_j topk_prob[t][j] * y_perm[row_of[t*k+j]] ) over
