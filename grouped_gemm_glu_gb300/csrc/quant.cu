@@ -88,13 +88,18 @@ __global__ void __launch_bounds__(256) k_quant_rows(const uint16_t* __restrict__
   }
 }
 
-// Column-wise (transposed).  A CTA owns a tile of 32 rows (one MX block
-// along R) x 256 columns: it reads the tile with coalesced 16-byte loads
-// into shared memory (rows padded by 16 bytes so column reads are free of
-// bank conflicts), then thread c quantises column c's 32 values and writes
-// its 32 codes (one full 32-byte sector) to q[c][r0 .. r0+32).
-constexpr int QC_COLS = 256;
-constexpr int QC_ROW_BYTES = QC_COLS * 2 + 16;
+// Column-wise (transposed).  A CTA owns a tile of 128 rows (four MX blocks
+// along R) x 64 columns:
+//   1. coalesced 16-byte loads of the 128 x 64 bf16 tile into shared memory
+//      (8 lanes per 128-byte row);
+//   2. thread (column c, block b) quantises the 32 values of column c in
+//      rows 32b..32b+31 (consecutive lanes read consecutive columns: no bank
+//      conflicts) and writes its 32 codes into a [64][128]-byte code tile;
+//   3. each column's 128 codes leave as one full 128-byte line (8 lanes x 16
+//      bytes, 4 columns per warp instruction); its 4 scales as one word.
+constexpr int QC_ROWS = 128, QC_COLS = 64;
+constexpr int QC_IN_ROW = QC_COLS * 2 + 16;  // padded bytes per staged input row
+constexpr int QC_CODE_ROW = QC_ROWS + 16;    // padded bytes per staged code column
 
 __global__ void __launch_bounds__(256) k_quant_cols(const uint16_t* __restrict__ src, int G, int R, int Cc,
                                                     const int32_t* __restrict__ counts,
@@ -102,48 +107,89 @@ __global__ void __launch_bounds__(256) k_quant_cols(const uint16_t* __restrict__
                                                     uint8_t* __restrict__ q, uint8_t* __restrict__ s) {
   __shared__ int32_t s_off[QE_MAX + 1];
   __shared__ int32_t s_cnt[QE_MAX];
-  __shared__ __align__(16) uint8_t tile[32 * QC_ROW_BYTES];
+  __shared__ __align__(16) uint8_t tin[QC_ROWS * QC_IN_ROW];
+  __shared__ __align__(16) uint8_t tcode[QC_COLS * QC_CODE_ROW];
+  __shared__ uint8_t tscale[QC_COLS * 4];
+  __shared__ int real_rows[4];
   if (E > 0) load_seg(counts, offsets, E, s_off, s_cnt);
   const int col_tiles = (Cc + QC_COLS - 1) / QC_COLS;
-  const int row_blocks = R / 32;
-  const size_t total = (size_t)G * row_blocks * col_tiles;
-  const int t = threadIdx.x;
-  for (size_t i = blockIdx.x; i < total; i += gridDim.x) {
+  // grouped rows: only the tiles that hold rows < offsets[E]
+  const int rows_used = E > 0 ? max(0, min(R, s_off[E])) : R;
+  const int row_tiles = (rows_used + QC_ROWS - 1) / QC_ROWS;
+  const size_t total = (size_t)G * row_tiles * col_tiles;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int nblk = R / 32;
+  const int ch = t & 7;
+  // real rows of 32-row block rb (-1: past R or past offsets[E])
+  auto block_real = [&](int rb) -> int {
+    int real = rb < R ? 32 : -1;
+    if (E > 0 && real >= 0) real = block_real_rows(rb, s_off, s_cnt, E);
+    return real;
+  };
+  auto tile_coords = [&](size_t i, int& g, int& r0, int& c0) {
     const int ct = (int)(i % col_tiles);
     const size_t rest = i / col_tiles;
-    const int rbk = (int)(rest % row_blocks);
-    const int g = (int)(rest / row_blocks);
-    const int r0 = rbk * 32;
-    int real = 32;
-    if (E > 0) {
-      real = block_real_rows(r0, s_off, s_cnt, E);
-      if (real < 0) continue;  // uniform over the CTA
-    }
-    const int c0 = ct * QC_COLS;
-    // load: 32 rows x 32 chunks of 16 bytes; thread t covers chunk t%32 of rows t/32, t/32+8, ...
-    const int ch = t & 31;
+    r0 = (int)(rest % row_tiles) * QC_ROWS;
+    g = (int)(rest / row_tiles);
+    c0 = ct * QC_COLS;
+  };
+  // this thread's 4 chunks of a tile: rows t/8 + 32k, 16-byte chunk t%8
+  auto load_tile = [&](size_t i, uint4* v) {
+    int g, r0, c0;
+    tile_coords(i, g, r0, c0);
     const bool ch_ok = c0 + ch * 8 < Cc;
 #pragma unroll
-    for (int rr = 0; rr < 4; ++rr) {
-      const int r = (t >> 5) + rr * 8;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (ch_ok && r < real)
-        v = __ldg(reinterpret_cast<const uint4*>(src + ((size_t)g * R + r0 + r) * Cc + c0 + ch * 8));
-      *reinterpret_cast<uint4*>(tile + r * QC_ROW_BYTES + ch * 16) = v;
+    for (int k = 0; k < 4; ++k) {
+      const int rr = (t >> 3) + 32 * k;
+      v[k] = make_uint4(0, 0, 0, 0);
+      if (ch_ok && (rr & 31) < block_real(r0 + 32 * k))
+        v[k] = __ldg(reinterpret_cast<const uint4*>(src + ((size_t)g * R + r0 + rr) * Cc + c0 + ch * 8));
     }
+  };
+  uint4 nxt[4];
+  size_t i = blockIdx.x;
+  if (i < total) load_tile(i, nxt);
+  for (; i < total; i += gridDim.x) {
+    int g, r0, c0;
+    tile_coords(i, g, r0, c0);
+    if (t < 4) real_rows[t] = block_real(r0 + 32 * t);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4*>(tin + ((t >> 3) + 32 * k) * QC_IN_ROW + ch * 16) = nxt[k];
     __syncthreads();
-    const int c = c0 + t;
-    if (c < Cc) {
+    // prefetch the next tile while this one is quantised and stored
+    if (i + gridDim.x < total) load_tile(i + gridDim.x, nxt);
+    // quantise: warp w -> block b = w/2, columns (w%2)*32 + lane
+    {
+      const int b = warp >> 1;
+      const int cl = (warp & 1) * 32 + lane;
       float v[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        v[j] = __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t*>(tile + j * QC_ROW_BYTES + t * 2)) << 16);
+        v[j] = __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t*>(tin + (32 * b + j) * QC_IN_ROW + cl * 2))
+                               << 16);
       uint32_t codes[8];
       const uint32_t sb = mx_quant_block32(v, codes);
-      uint4* dq = reinterpret_cast<uint4*>(q + ((size_t)g * Cc + c) * R + r0);
-      dq[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-      dq[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-      s[((size_t)g * Cc + c) * (R / 32) + rbk] = (uint8_t)sb;
+      uint4* dc = reinterpret_cast<uint4*>(tcode + cl * QC_CODE_ROW + 32 * b);
+      dc[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+      dc[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+      tscale[cl * 4 + b] = (uint8_t)sb;
+    }
+    __syncthreads();
+    // store: lane group of 8 -> one column's 128 bytes; 4 columns per warp pass
+    {
+      const int sub = lane >> 3, part = lane & 7;
+      const bool full = r0 + QC_ROWS <= R;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int cl = warp * 8 + k * 4 + sub;
+        const int c = c0 + cl;
+        if (c < Cc) {
+          const uint4 val = *reinterpret_cast<const uint4*>(tcode + cl * QC_CODE_ROW + part * 16);
+          uint8_t* dst = q + ((size_t)g * Cc + c) * R + r0 + part * 16;
+          if (full || r0 + part * 16 < R) *reinterpret_cast<uint4*>(dst) = val;
+          if (part < 4 && real_rows[part] >= 0) s[((size_t)g * Cc + c) * nblk + (r0 >> 5) + part] = tscale[cl * 4 + part];
+        }
+      }
     }
     __syncthreads();
   }
@@ -240,7 +286,7 @@ extern "C" moe_status_t moe_quantize_mxfp8(const moe_bf16* src, int G, int R, in
     k_quant_rows<<<grid_for((size_t)G * R * (Cc / 32), 256), 256, 0, st>>>(src, G, R, Cc, counts, offsets, E, q, s);
   } else {
     if ((R % 32) || (Cc % 8)) return MOE_ERR_ARG;
-    const size_t tiles = (size_t)G * (R / 32) * ((Cc + QC_COLS - 1) / QC_COLS);
+    const size_t tiles = (size_t)G * ((R + QC_ROWS - 1) / QC_ROWS) * ((Cc + QC_COLS - 1) / QC_COLS);
     k_quant_cols<<<grid_for(tiles, 1), 256, 0, st>>>(src, G, R, Cc, counts, offsets, E, q, s);
   }
   count_launch();

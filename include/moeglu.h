@@ -183,8 +183,8 @@ MOE_API moe_status_t moe_grouped_dglu_quant_bwd(const moe_bf16* dY_perm, const m
  * col == 0: q [G][R][C], s [G][R][C/32] (blocks along C).
  * col != 0: q [G][C][R], s [G][C][R/32] (blocks of 32 rows; transposed).
  * counts/offsets (G == 1 only, may be NULL): rows of the permuted layout
- * outside [offsets[e], offsets[e]+counts[e]) are treated as zero and rows
- * >= offsets[E] are not written. */
+ * outside [offsets[e], offsets[e]+counts[e]) are treated as zero; results
+ * for rows >= offsets[E] are unspecified (their scales are not written). */
 MOE_API moe_status_t moe_quantize_mxfp8(const moe_bf16* src, int G, int R, int C, int col,
                                 const int32_t* counts, const int32_t* offsets, int E,
                                 uint8_t* q, uint8_t* s, moe_stream_t stream);
