@@ -207,13 +207,16 @@ def run_oracle_timed(inp, w, steps, warmup, budget_s):
 
 # ---------------------------------------------------------------------------
 
-def profile_traffic(kernel_name):
-    """DRAM bytes per launch from a committed ncu summary, if the summary was
-    taken on the current kernel source (else None)."""
-    p = os.path.join(ROOT, "profiles", f"{kernel_name}_traffic.json")
+def profile_traffic(call_name):
+    """DRAM bytes (read + write) per launch of one step call, from the
+    committed ncu launch list of this workload, if that capture was taken on
+    the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic_dsv3.json")
     if not os.path.exists(p):
         return None
-    d = json.load(open(p))
+    d = json.load(open(p)).get("calls", {}).get(call_name)
+    if not d:
+        return None
     h = hashlib.sha256()
     for f in d.get("sources", []):
         fp = os.path.join(ROOT, f)
@@ -396,7 +399,7 @@ def main():
     else:
         roof = {"bound": "hbm", "achieved": round(by / ms / 1e6, 1), "peak": peaks["hbm"], "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    tr = profile_traffic(dom)
+    tr = profile_traffic(dom) if w.E == base.E and w.name == WORKLOAD and not args.experts else None
     roof["traffic"] = tr
     roof["kernel"] = dom
     roof["peak_source"] = f"of {peaks['src']} ({'bf16 sustained' if dt == 'bf16' else 'fp8 = 2 x bf16 sustained' if dt else 'HBM copy'})"
