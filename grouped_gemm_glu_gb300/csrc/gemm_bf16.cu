@@ -32,9 +32,11 @@ namespace moeglu {
 namespace g16 {
 
 constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int EPI_WARPS = 4;
+// 8 epilogue warps: warp w reads TMEM lane quarter w % 4 and handles half
+// w / 4 of the tile's accumulator columns
+constexpr int EPI_WARPS = 8;
 constexpr int THREADS = (EPI_WARPS + 2) * 32;
-constexpr int PRODUCER_WARP = 4, MMA_WARP = 5;
+constexpr int PRODUCER_WARP = 8, MMA_WARP = 9;
 constexpr int A_TILE = BM * BK * 2;
 constexpr int B_TILE = BN * BK * 2;
 constexpr int STAGE_BYTES = A_TILE + B_TILE;
@@ -183,7 +185,7 @@ __device__ __forceinline__ void store_bf16x32(uint16_t* p, const float* v, bool 
 }
 
 template <int MODE>
-__device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& ti, uint32_t tacc, int q, int lane,
+__device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& ti, uint32_t tacc, int q, int h, int lane,
                                               uint8_t* scratch, uint32_t& amax_bits) {
   if (q * 32 >= ti.rows_pad) return;  // no row of this warp lies in the padded segment
   const int r_local = q * 32 + lane;
@@ -195,7 +197,7 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& ti, uin
 
   if (MODE == FWD_GLU) {
 #pragma unroll 1
-    for (int j = 0; j < BN / 64; ++j) {
+    for (int j = h * (BN / 128); j < (h + 1) * (BN / 128); ++j) {
       const int f0 = ti.n_idx * (BN / 2) + j * 32;
       if (f0 >= a.F) break;
       const int p0 = ti.n_idx * BN + j * 64;
@@ -224,7 +226,7 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& ti, uin
     }
   } else if (MODE == FWD_ELT || MODE == FWD_PRE) {
 #pragma unroll 1
-    for (int j = 0; j < BN / 32; ++j) {
+    for (int j = h * (BN / 64); j < (h + 1) * (BN / 64); ++j) {
       const int c0 = ti.n_idx * BN + j * 32;
       if (c0 >= a.N_gemm) break;
       float v[32];
@@ -245,7 +247,7 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& ti, uin
     }
   } else if (MODE == BWD_GLU) {
 #pragma unroll 1
-    for (int j = 0; j < BN / 32; ++j) {
+    for (int j = h * (BN / 64); j < (h + 1) * (BN / 64); ++j) {
       const int f0 = ti.n_idx * BN + j * 32;
       if (f0 >= a.F) break;
       const int p0 = (f0 / 32) * 64;
@@ -270,7 +272,7 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& ti, uin
     }
   } else {  // BWD_ELT
 #pragma unroll 1
-    for (int j = 0; j < BN / 32; ++j) {
+    for (int j = h * (BN / 64); j < (h + 1) * (BN / 64); ++j) {
       const int f0 = ti.n_idx * BN + j * 32;
       if (f0 >= a.F) break;
       float d[32], x[32];
@@ -441,8 +443,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     // epilogue warps 0..3: warp q reads TMEM lanes 32q..32q+31
-    const int q = warp;
-    uint8_t* scratch = scratch_all + q * SCRATCH_PER_WARP;
+    const int q = warp & 3, h = warp >> 2;
+    uint8_t* scratch = scratch_all + warp * SCRATCH_PER_WARP;
     uint32_t amax_bits = 0;
     int lt = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
@@ -455,7 +457,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const Tile ti = decode_tile(t, pref, E, a.n_tiles_n, a.counts, a.offsets, a.R_cap);
       const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
-      epilogue_tile<MODE>(a, ti, tacc, q, lane, scratch, amax_bits);
+      epilogue_tile<MODE>(a, ti, tacc, q, h, lane, scratch, amax_bits);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty + buf);
@@ -473,8 +475,264 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// CTA-pair variant (clusters of 2, tcgen05 cta_group::2).  The pair computes
+// a 256 x 256 tile: each CTA holds 128 rows of A and 128 of the 256 B rows
+// in its own shared memory (32 KB per stage, 6 stages) and receives its 128
+// accumulator rows in its own tensor memory.  The even CTA issues the MMAs
+// (M = 256) and its commits are multicast to both CTAs; both CTAs' TMA loads
+// complete on the even CTA's stage barrier; the odd CTA's epilogue releases
+// accumulators through the even CTA's barrier.  Per SM this fetches 32 KB
+// per 128x256x64 step instead of 48 KB.
+// ---------------------------------------------------------------------------
+namespace pair {
+constexpr int STAGES = 6;
+constexpr int B_HALF = (BN / 2) * BK * 2;
+constexpr int STAGE_BYTES = A_TILE + B_HALF;
+constexpr int OFF_SCRATCH = STAGES * STAGE_BYTES;
+constexpr int OFF_PREF = OFF_SCRATCH + EPI_WARPS * SCRATCH_PER_WARP;
+constexpr int OFF_BARS = OFF_PREF + (E_MAX + 2) * 4;
+constexpr int NUM_BARS = 2 * STAGES + 5;
+constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
+constexpr int SMEM_BYTES = 1024 + OFF_MISC + 64;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+}  // namespace pair
+
+// Tile t of the pair sequence: expert e, N tile, 256-row pair tile mp; this
+// CTA's half starts 128 * rank rows further.
+__device__ __forceinline__ Tile decode_pair(int t, const int32_t* pref, int E, int n_tiles_n, const int32_t* counts,
+                                            const int32_t* offsets, int R_cap, int rank) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pref[mid] * n_tiles_n <= t) lo = mid; else hi = mid - 1;
+  }
+  Tile ti;
+  ti.e = lo;
+  const int mt = pref[lo + 1] - pref[lo];
+  const int local = t - pref[lo] * n_tiles_n;
+  ti.n_idx = local / mt;
+  ti.m_idx = local - ti.n_idx * mt;
+  const int cnt = __ldg(counts + lo);
+  const int base = ti.m_idx * 2 * BM + rank * BM;
+  ti.row0 = __ldg(offsets + lo) + base;
+  ti.rows_valid = max(0, min(BM, cnt - base));
+  ti.rows_pad = max(0, min(BM, ((cnt + 31) & ~31) - base));
+  ti.rows_pad = ti.row0 < 0 ? 0 : max(0, min(ti.rows_pad, R_cap - ti.row0));
+  ti.rows_valid = min(ti.rows_valid, ti.rows_pad);
+  return ti;
+}
+
+template <int MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    k_grouped_bf16_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const Args a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* tiles = smem;
+  uint8_t* scratch_all = smem + pair::OFF_SCRATCH;
+  int32_t* pref = reinterpret_cast<int32_t*>(smem + pair::OFF_PREF);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + pair::OFF_BARS);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + pair::STAGES;
+  uint64_t* acc_full = bars + 2 * pair::STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* mma_done = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + pair::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + pair::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = a.E;
+  const uint32_t rank = cluster_ctarank();
+  const int cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+
+  if (warp == PRODUCER_WARP && lane == 0) {
+    for (int s = 0; s < pair::STAGES; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full + b, 1);
+      mbar_init(acc_empty + b, 2 * EPI_WARPS);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_async_shared();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc_pair(tmem_slot, TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  // 256-row pair tiles per expert -> exclusive prefix pref[0..E]
+  for (int e = threadIdx.x; e < E; e += THREADS) pref[e + 1] = (__ldg(a.counts + e) + 2 * BM - 1) / (2 * BM);
+  if (threadIdx.x == 0) pref[0] = 0;
+  __syncthreads();
+  if (warp == 0) {
+    const int per = (E + 31) / 32;
+    const int beg = 1 + lane * per, end = min(E + 1, beg + per);
+    int sum = 0;
+    for (int i = beg; i < end; ++i) sum += pref[i];
+    int incl = sum;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    int run = incl - sum;
+    for (int i = beg; i < end; ++i) {
+      run += pref[i];
+      pref[i] = run;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers and tensor memory exist before any cross-CTA use
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const bool over = __ldg(a.offsets + E) > a.R_cap;
+  if (over && threadIdx.x == 0) set_status(a.status, MOE_ERR_CAPACITY);
+  const int total = over ? 0 : pref[E] * a.n_tiles_n;
+  const int num_kb = a.K / BK;
+  WaitGuard guard{abort_flag, a.status, a.wait_ns};
+
+  if (warp == PRODUCER_WARP) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int t = cl; t < total; t += ncl) {
+        const Tile ti = decode_pair(t, pref, E, a.n_tiles_n, a.counts, a.offsets, a.R_cap, (int)rank);
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(empty + stage, phase ^ 1u, guard)) {
+            ok = false;
+            break;
+          }
+          uint8_t* a_dst = tiles + stage * pair::STAGE_BYTES;
+          const uint32_t bar_lead = mapa_shared(smem_u32(full + stage), 0);
+          if (rank == 0) mbar_arrive_expect_tx(full + stage, 2 * pair::STAGE_BYTES);
+          tma_load_2d_pair(a_dst, &tmA, bar_lead, kb * BK, ti.row0);
+          tma_load_3d_pair(a_dst + A_TILE, &tmB, bar_lead, kb * BK, ti.n_idx * BN + (int)rank * (BN / 2), ti.e);
+          if (++stage == pair::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == MMA_WARP) {
+    if (lane == 0 && rank == 0) {
+      const uint32_t idesc = idesc_bf16_f32(2 * BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int lt = 0;
+      for (int t = cl; t < total; t += ncl, ++lt) {
+        const int buf = lt & 1;
+        const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
+        if (!mbar_wait(acc_empty + buf, aph ^ 1u, guard)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(full + stage, phase, guard)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(tiles + stage * pair::STAGE_BYTES);
+          const uint32_t b_addr = a_addr + A_TILE;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            umma_bf16_pair(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32), sdesc_kmajor_sw128(b_addr + k * 32), idesc,
+                           (kb | k) != 0 ? 1u : 0u);
+          }
+          tc_commit_pair_mc(empty + stage, 0x3);
+          if (++stage == pair::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair_mc(acc_full + buf, 0x3);
+      }
+      tc_commit_pair_mc(mma_done, 0x1);
+      volatile int never = 0;
+      WaitGuard drain{&never, a.status, 100000000ull};
+      mbar_wait(mma_done, 0, drain);
+    }
+  } else {
+    const int q = warp & 3, h = warp >> 2;
+    uint8_t* scratch = scratch_all + warp * SCRATCH_PER_WARP;
+    uint32_t amax_bits = 0;
+    int lt = 0;
+    for (int t = cl; t < total; t += ncl, ++lt) {
+      const int buf = lt & 1;
+      const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(acc_full + buf, aph, guard) ? 1 : 0;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const Tile ti = decode_pair(t, pref, E, a.n_tiles_n, a.counts, a.offsets, a.R_cap, (int)rank);
+      const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
+      epilogue_tile<MODE>(a, ti, tacc, q, h, lane, scratch, amax_bits);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(acc_empty + buf), 0));
+    }
+    if (a.out_mode == MOE_OUT_NVFP4 && a.amax != nullptr) {
+      const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, amax_bits);
+      if (lane == 0 && m != 0) atomicMax(reinterpret_cast<int*>(a.amax), (int)m);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still touch its memory
+  if (warp == MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
+template <int MODE>
+static moe_status_t launch_pair(const void* A, const void* B, const Args& args, int sm_margin, cudaStream_t stream) {
+  CUtensorMap tmA, tmB;
+  {
+    const uint64_t dims[2] = {(uint64_t)args.K, (uint64_t)args.R_cap};
+    const uint64_t strides[1] = {(uint64_t)args.K * 2};
+    const uint32_t box[2] = {BK, BM};
+    if (!encode_tmap(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+      return MOE_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)args.K, (uint64_t)args.N_gemm, (uint64_t)args.E};
+    const uint64_t strides[2] = {(uint64_t)args.K * 2, (uint64_t)args.N_gemm * args.K * 2};
+    const uint32_t box[3] = {BK, BN / 2, 1};
+    if (!encode_tmap(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, B, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+      return MOE_ERR_CUDA;
+  }
+  const void* kfn = (const void*)k_grouped_bf16_pair<MODE>;
+  if (!set_smem_limit(kfn, pair::SMEM_BYTES)) return MOE_ERR_CUDA;
+  int clusters = max_active_pairs(kfn, THREADS, pair::SMEM_BYTES);
+  if (clusters <= 0) return MOE_ERR_CUDA;
+  const int by_margin = (sm_count() - sm_margin) / 2;
+  if (clusters > by_margin) clusters = by_margin;
+  const long long tiles_bound = ((long long)args.R_cap / (2 * BM) + args.E) * args.n_tiles_n;
+  if (clusters > tiles_bound) clusters = (int)tiles_bound;
+  if (clusters < 1) clusters = 1;
+  k_grouped_bf16_pair<MODE><<<2 * clusters, THREADS, pair::SMEM_BYTES, stream>>>(tmA, tmB, args);
+  count_launch();
+  return launch_status();
+}
+
 template <int MODE>
 static moe_status_t launch(const void* A, const void* B, const Args& args, int sm_margin, cudaStream_t stream) {
+  if (g_cta_pairs.load()) return launch_pair<MODE>(A, B, args, sm_margin, stream);
   CUtensorMap tmA, tmB;
   {
     const uint64_t dims[2] = {(uint64_t)args.K, (uint64_t)args.R_cap};

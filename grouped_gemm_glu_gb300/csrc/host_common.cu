@@ -1,5 +1,6 @@
 // Host helpers of libmoeglu (see host_common.h) and the small entry points
 // that launch nothing: status read-back, wait limit, launch counter.
+#include <map>
 #include <mutex>
 #include <set>
 #include <tuple>
@@ -10,6 +11,33 @@ namespace moeglu {
 
 std::atomic<uint64_t> g_launches{0};
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+std::atomic<int> g_cta_pairs{1};
+
+int max_active_pairs(const void* kernel, int threads, int smem_bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  auto key = std::make_pair(kernel, dev);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * 256, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) return 0;
+  cache[key] = n;
+  return n;
+}
 
 int sm_count() {
   static int cached[64] = {0};
@@ -87,3 +115,5 @@ extern "C" moe_status_t moe_get_status(const int32_t* status, int32_t* host_out,
 extern "C" void moe_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : 1); }
 
 extern "C" uint64_t moe_launch_count(void) { return g_launches.load(); }
+
+extern "C" void moe_set_cta_pairs(int enable) { g_cta_pairs.store(enable ? 1 : 0); }

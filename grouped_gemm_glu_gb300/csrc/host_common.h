@@ -16,6 +16,7 @@ namespace moeglu {
 
 extern std::atomic<uint64_t> g_launches;  // kernels launched by this library
 extern std::atomic<uint64_t> g_wait_limit_ns;
+extern std::atomic<int> g_cta_pairs;  // bf16 GEMMs on CTA pairs (cta_group::2)
 
 inline void count_launch(int n = 1) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
@@ -23,6 +24,10 @@ inline cudaStream_t as_stream(moe_stream_t s) { return reinterpret_cast<cudaStre
 
 // Number of SMs of the current device (cached per device).
 int sm_count();
+
+// Clusters of 2 CTAs of `kernel` that fit on the device at once (cached per
+// kernel and device); 0 on failure.
+int max_active_pairs(const void* kernel, int threads, int smem_bytes);
 
 // Opts a kernel into `bytes` of dynamic shared memory (once per kernel and
 // device; returns false on failure).

@@ -285,6 +285,12 @@ MOE_API moe_status_t moe_get_status(const int32_t* status, int32_t* host_out, mo
  * after it a wait gives up, sets MOE_ERR_TIMEOUT and the kernel returns. */
 MOE_API void moe_set_wait_limit_ns(uint64_t ns);
 
+/* Tile configuration of the bf16 grouped GEMMs (FC1 forward, dGLU
+ * backward): enable != 0 (default) runs them on CTA pairs (256 x 256 tiles,
+ * tcgen05 cta_group::2, 32 KB per SM per pipeline stage); 0 runs one CTA per
+ * 128 x 256 tile.  Both compute the same results.  Process-wide. */
+MOE_API void moe_set_cta_pairs(int enable);
+
 /* Cumulative number of kernels this library has launched in this process
  * (launch accounting for benchmarks). */
 MOE_API uint64_t moe_launch_count(void);
