@@ -262,6 +262,44 @@ __global__ void __launch_bounds__(256) k_glu_act(const uint16_t* __restrict__ pr
   }
 }
 
+// Unfused backward activation: da [R][F] bf16 (the data-gradient GEMM's
+// output) and the saved pre-activation [R][N1] bf16 -> dFC1 [R][N1] bf16 in
+// packed column order.  One thread per 32 columns of da of a row < offsets[E].
+__global__ void __launch_bounds__(256) k_dglu_act(const uint16_t* __restrict__ da, const uint16_t* __restrict__ pre,
+                                                  const int32_t* __restrict__ offsets, int E, int F, int N1,
+                                                  GluParams prm, uint16_t* __restrict__ d) {
+  const int R = __ldg(offsets + E);
+  const int nb = F / 32;
+  const bool gated = N1 == 2 * F;
+  const size_t total = (size_t)R * nb;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t r = i / nb;
+    const int b = (int)(i - r * nb);
+    const uint16_t* pr = pre + r * N1;
+    const uint16_t* dr = da + r * F + (size_t)b * 32;
+    const int pu = gated ? b * 64 : b * 32;
+    float du[32], dg[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float u = __uint_as_float((uint32_t)__ldg(pr + pu + j) << 16);
+      const float g = gated ? __uint_as_float((uint32_t)__ldg(pr + pu + 32 + j) << 16) : 0.0f;
+      const float dy = __uint_as_float((uint32_t)__ldg(dr + j) << 16);
+      act_bwd(prm, u, g, dy, du[j], dg[j]);
+    }
+    uint4* o = reinterpret_cast<uint4*>(d + r * N1 + pu);
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+      o[w] = make_uint4(pack_bf16x2(du[8 * w], du[8 * w + 1]), pack_bf16x2(du[8 * w + 2], du[8 * w + 3]),
+                        pack_bf16x2(du[8 * w + 4], du[8 * w + 5]), pack_bf16x2(du[8 * w + 6], du[8 * w + 7]));
+    if (gated) {
+#pragma unroll
+      for (int w = 0; w < 4; ++w)
+        o[4 + w] = make_uint4(pack_bf16x2(dg[8 * w], dg[8 * w + 1]), pack_bf16x2(dg[8 * w + 2], dg[8 * w + 3]),
+                              pack_bf16x2(dg[8 * w + 4], dg[8 * w + 5]), pack_bf16x2(dg[8 * w + 6], dg[8 * w + 7]));
+    }
+  }
+}
+
 static int grid_for(size_t items, int per_block) {
   const size_t g = (items + per_block - 1) / per_block;
   const size_t cap = (size_t)sm_count() * 16;
@@ -323,6 +361,29 @@ extern "C" moe_status_t moe_glu_act(const moe_bf16* pre, const int32_t* counts, 
   g.up_hi = params->up_hi;
   const int N1 = act == MOE_ACT_SRELU ? F : 2 * F;
   k_glu_act<<<grid_for((size_t)R_cap * (F / 32), 256), 256, 0, as_stream(stream)>>>(pre, offsets, E, F, N1, g, y);
+  count_launch();
+  return launch_status();
+}
+
+extern "C" moe_status_t moe_dglu_act(const moe_bf16* da, const moe_bf16* pre, const int32_t* counts,
+                                     const int32_t* offsets, int E, int F, int R_cap, const moe_glu_params_t* params,
+                                     moe_bf16* dfc1, moe_stream_t stream) {
+  (void)counts;
+  if (!da || !pre || !offsets || !params || !dfc1 || E <= 0 || F <= 0 || (F % 32) || R_cap <= 0) return MOE_ERR_ARG;
+  if (!aligned16(dfc1)) return MOE_ERR_ARG;
+  const int act = params->act;
+  if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SREGLU) return MOE_ERR_ARG;
+  GluParams g;
+  g.act = act;
+  g.alpha = params->alpha;
+  g.up_offset = params->up_offset;
+  g.gate_lo = params->gate_lo;
+  g.gate_hi = params->gate_hi;
+  g.up_lo = params->up_lo;
+  g.up_hi = params->up_hi;
+  const int N1 = act == MOE_ACT_SRELU ? F : 2 * F;
+  k_dglu_act<<<grid_for((size_t)R_cap * (F / 32), 256), 256, 0, as_stream(stream)>>>(da, pre, offsets, E, F, N1, g,
+                                                                                    dfc1);
   count_launch();
   return launch_status();
 }

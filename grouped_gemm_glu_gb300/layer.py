@@ -134,6 +134,59 @@ class MoeLayer:
                 E, F, H, R, _p(self.dW2), 0, _p(self.ws_wg2), self.ws_wg2.numel(), self.sm_margin, st, s)),
         ]
 
+    # ---- unfused path (the ablation baseline): the same tcgen05 GEMM writing
+    # bf16, then a separate activation kernel and separate quantize kernels
+    def _unfused_buffers(self):
+        if getattr(self, "_u", None) is None:
+            z = lambda *sh, dt=torch.bfloat16: torch.empty(*sh, dtype=dt, device=self.dev)
+            E, N1, H, F, R = self.E, self.N1, self.H, self.F, self.R_cap
+            u8 = torch.uint8
+            self._u = {
+                "pre": z(R, N1), "y": z(R, F), "a_q": z(R, F, dt=u8), "a_s": z(R, F // 32, dt=u8),
+                "a_qc": z(F, R, dt=u8), "a_sc": z(F, R // 32, dt=u8), "da": z(R, F), "d": z(R, N1),
+                "d_q": z(R, N1, dt=u8), "d_s": z(R, N1 // 32, dt=u8), "d_qc": z(N1, R, dt=u8),
+                "d_sc": z(N1, R // 32, dt=u8),
+            }
+            self._u_none = L.glu_params("none")
+            self._u_fwd_out = L.ActOut(None, None, None, None, None, None, self._u["pre"].data_ptr())
+            self._u_bwd_out = L.ActOut(None, None, None, None, None, None, self._u["da"].data_ptr())
+        return self._u
+
+    def forward_unfused_calls(self):
+        """GEMM (+bias) -> bf16 pre; activation -> bf16 y; MXFP8 rows; MXFP8 columns."""
+        u = self._unfused_buffers()
+        lib, s = self.lib, _s()
+        E, N1, H, F, R = self.E, self.N1, self.H, self.F, self.R_cap
+        st, cnt, off = _p(self.status), _p(self.counts), _p(self.offsets)
+        return [
+            ("gemm", lambda: lib.moe_grouped_fc1_glu_quant_fwd(
+                _p(self.x_perm), _p(self.W1p), _p(self.b1p), None, cnt, off, E, H, N1, R, C.byref(self._u_none),
+                L.OUT_BF16, C.byref(self._u_fwd_out), self.sm_margin, st, s)),
+            ("act", lambda: lib.moe_glu_act(_p(u["pre"]), cnt, off, E, F, R, C.byref(self.params), _p(u["y"]), s)),
+            ("quant_rows", lambda: lib.moe_quantize_mxfp8(_p(u["y"]), 1, R, F, 0, cnt, off, E, _p(u["a_q"]),
+                                                          _p(u["a_s"]), s)),
+            ("quant_cols", lambda: lib.moe_quantize_mxfp8(_p(u["y"]), 1, R, F, 1, cnt, off, E, _p(u["a_qc"]),
+                                                          _p(u["a_sc"]), s)),
+        ]
+
+    def backward_unfused_calls(self, dY_perm):
+        """GEMM dY . W2^T -> bf16 da; dActivation -> bf16 dFC1; MXFP8 rows; columns."""
+        u = self._unfused_buffers()
+        lib, s = self.lib, _s()
+        E, N1, H, F, R = self.E, self.N1, self.H, self.F, self.R_cap
+        st, cnt, off = _p(self.status), _p(self.counts), _p(self.offsets)
+        return [
+            ("gemm", lambda: lib.moe_grouped_fc1_glu_quant_fwd(
+                _p(dY_perm), _p(self.W2), None, None, cnt, off, E, H, F, R, C.byref(self._u_none), L.OUT_BF16,
+                C.byref(self._u_bwd_out), self.sm_margin, st, s)),
+            ("dact", lambda: lib.moe_dglu_act(_p(u["da"]), _p(self.pre), cnt, off, E, F, R, C.byref(self.params),
+                                              _p(u["d"]), s)),
+            ("quant_rows", lambda: lib.moe_quantize_mxfp8(_p(u["d"]), 1, R, N1, 0, cnt, off, E, _p(u["d_q"]),
+                                                          _p(u["d_s"]), s)),
+            ("quant_cols", lambda: lib.moe_quantize_mxfp8(_p(u["d"]), 1, R, N1, 1, cnt, off, E, _p(u["d_qc"]),
+                                                          _p(u["d_sc"]), s)),
+        ]
+
     def step_calls(self, x, topk_idx, topk_prob, dY_perm):
         return self.forward_calls(x, topk_idx, topk_prob) + self.backward_calls(dY_perm)
 

@@ -52,6 +52,7 @@ _SIGS = {
     "moe_unpermute_combine": [P, P, P, I, I, I, P, P, P],
     "moe_nvfp4_cast": [P, P, P, P, I, I, I, P, P, P, P],
     "moe_glu_act": [P, P, P, I, I, I, C.POINTER(GluParams), P, P],
+    "moe_dglu_act": [P, P, P, P, I, I, I, C.POINTER(GluParams), P, P],
     "moe_route_permute_noalloc": [P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P, P],
     "moe_route_noalloc_max_scratch_bytes": ([], SZ),
     "moe_get_status": [P, P, P],

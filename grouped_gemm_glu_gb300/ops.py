@@ -226,3 +226,14 @@ def glu_act(pre, counts, offsets, F: int, params: L.GluParams):
     L.check(lib.moe_glu_act(_p(pre), _p(counts), _p(offsets), counts.shape[0], F, R_cap, C.byref(params), _p(y),
                             _s()), "moe_glu_act")
     return y
+
+
+def dglu_act(da, pre, counts, offsets, F: int, params: L.GluParams):
+    """Unfused backward activation: da [R, F] and pre [R, N1] -> dFC1 [R, N1]."""
+    lib = L.load()
+    dev = _dev(da)
+    R_cap, N1 = pre.shape
+    d = torch.empty(R_cap, N1, dtype=torch.bfloat16, device=dev)
+    L.check(lib.moe_dglu_act(_p(da), _p(pre), _p(counts), _p(offsets), counts.shape[0], F, R_cap, C.byref(params),
+                             _p(d), _s()), "moe_dglu_act")
+    return d

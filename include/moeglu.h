@@ -277,6 +277,14 @@ MOE_API moe_status_t moe_route_permute_noalloc(const moe_bf16* x, const int32_t*
 /* Size in bytes of the fixed scratch array used by moe_route_permute_noalloc. */
 MOE_API size_t moe_route_noalloc_max_scratch_bytes(void);
 
+/* Standalone backward activation of the unfused path: da [R][F] bf16 (the
+ * data-gradient GEMM output, computed e.g. by moe_grouped_fc1_glu_quant_fwd
+ * with MOE_ACT_NONE on dY_perm and W2) and the saved pre [R][N1] bf16 ->
+ * dFC1 [R][N1] bf16 in packed column order (rows >= offsets[E] untouched). */
+MOE_API moe_status_t moe_dglu_act(const moe_bf16* da, const moe_bf16* pre, const int32_t* counts,
+                                  const int32_t* offsets, int E, int F, int R_cap,
+                                  const moe_glu_params_t* params, moe_bf16* dfc1, moe_stream_t stream);
+
 /* Copies the device status word to *host_out (synchronises `stream`; not
  * for use inside a graph capture). */
 MOE_API moe_status_t moe_get_status(const int32_t* status, int32_t* host_out, moe_stream_t stream);

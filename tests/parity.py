@@ -20,6 +20,8 @@
 """
 from __future__ import annotations
 
+import math
+
 import numpy as np
 import torch
 
@@ -53,11 +55,11 @@ def assert_bf16_close(gpu, ref, what="", rtol=2e-2, atol=1e-2):
                           f"at {np.unravel_index(np.argmax(err - lim), err.shape)}"
 
 
-def _near_pow2(a: np.ndarray) -> np.ndarray:
+def _near_pow2(a: np.ndarray, band: float = REL_BAND) -> np.ndarray:
     a = np.asarray(a, dtype=np.float64)
     with np.errstate(divide="ignore", invalid="ignore"):
-        l2 = np.log2(a)
-        return (a > 0) & (np.abs(a - np.exp2(np.round(l2))) <= REL_BAND * a)
+        p2 = np.exp2(np.round(np.log2(a)))
+        return (a > 0) & (np.abs(a - p2) <= band * p2)
 
 
 def e4m3_step(x_scaled: np.ndarray) -> np.ndarray:
@@ -68,9 +70,11 @@ def e4m3_step(x_scaled: np.ndarray) -> np.ndarray:
     return np.exp2(e - 3)
 
 
-def assert_mx_close(q_gpu, s_gpu, q_ref, s_ref, v_ref, what="", frac=0.999):
+def assert_mx_close(q_gpu, s_gpu, q_ref, s_ref, v_ref, what="", frac=0.999, rel_band=REL_BAND):
     """q [..., N] codes, s [..., N/32] scales, v_ref the oracle's float32
-    values that were quantised (used for the amax band)."""
+    values that were quantised (used for the amax band).  rel_band widens
+    the power-of-two band when both sides round to bf16 before quantising
+    (one bf16 step, 2^-7 relative)."""
     qg, sg = np.asarray(q_gpu), np.asarray(s_gpu).astype(np.int64)
     qr, sr = np.asarray(q_ref), np.asarray(s_ref).astype(np.int64)
     assert qg.shape == qr.shape and sg.shape == sr.shape, (what, qg.shape, qr.shape, sg.shape, sr.shape)
@@ -78,11 +82,14 @@ def assert_mx_close(q_gpu, s_gpu, q_ref, s_ref, v_ref, what="", frac=0.999):
     amax = np.abs(v).max(-1)
     diff = sg != sr
     if diff.any():
-        ok = (np.abs(sg - sr) == 1) & _near_pow2(amax)
+        ok = (np.abs(sg - sr) == 1) & _near_pow2(amax, rel_band)
         assert np.all(ok[diff]), f"{what}: scale mismatch off the power-of-two band: " \
                                  f"{np.sum(diff & ~ok)} blocks, e.g. gpu {sg[diff & ~ok][:4]} ref {sr[diff & ~ok][:4]} " \
                                  f"amax {amax[diff & ~ok][:4]}"
-        assert diff.mean() <= 1e-3, f"{what}: {diff.sum()} of {diff.size} scales differ"
+        # a block maximum falls in the band with probability ~ band / ln 2 (log-uniform
+        # mantissas): 1.4e-3 for the accumulation band, 1.1e-2 for one bf16 step
+        cap = max(1e-3, rel_band / math.log(2.0))
+        assert diff.mean() <= cap, f"{what}: {diff.sum()} of {diff.size} scales differ"
     finite = (sr != 255)[..., None]
     dg = O.mx_dequantize(qg, sg.astype(np.uint8)).reshape(v.shape)
     dr = O.mx_dequantize(qr, sr.astype(np.uint8)).reshape(v.shape)

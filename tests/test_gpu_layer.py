@@ -89,3 +89,45 @@ def test_layer_graph_replay_new_routing():
     torch.cuda.synchronize()
     for k in ("out", "dX_perm", "dW1", "dW2"):
         assert torch.equal(getattr(layer, k), got[k]), k
+
+
+def test_unfused_path_matches_oracle():
+    """The ablation baseline (bf16 GEMM -> activation -> quantize kernels,
+    forward and backward) against the oracle with the same rounding points:
+    the unfused path rounds the GEMM output to bf16, applies the activation
+    to that, rounds again to bf16 and quantises the bf16 tensor."""
+    from parity import assert_mx_close
+    w = synth.WORKLOADS["tiny"]
+    inp = synth.make_inputs(w, seed=24)
+    layer, g = _layer(w, inp)
+    layer.step(g["x"], g["topk_idx"], g["topk_prob"], g["dY"])
+    layer.run(layer.forward_unfused_calls())
+    layer.run(layer.backward_unfused_calls(g["dY"]))
+    torch.cuda.synchronize()
+    assert ops.read_status(layer.status) == 0
+    u = layer._u
+    prm = O.ActParams(O.ACT_SWIGLU)
+    rt = O.route(inp["topk_idx"].numpy(), 0, w.E)
+    R = rt.R_pad
+    real = rt.tok_of >= 0
+    fo = O.fc1_glu_fwd(O.permute(np_(inp["x"]), rt), O.repack_fc1(np_(inp["W1"])), None, rt, prm)
+    assert_bf16_close(np_(u["pre"])[:R], fo.pre_bf16, "unfused pre")
+    y = O.act_fwd(*O.unpack_glu_cols(fo.pre_bf16), prm)
+    y[~real] = 0
+    yb = O.bf16_round(y).astype(np.float32)
+    assert_bf16_close(np_(u["y"])[:R], yb, "unfused y")
+    band = 2.0 ** -7   # the bf16 roundings before the quantiser can move a block max by one bf16 step
+    q, s_ = O.mx_quantize_rows(yb)
+    assert_mx_close(np_(u["a_q"])[:R], np_(u["a_s"])[:R], q, s_, yb, "unfused a rows", rel_band=band)
+    qc, sc = O.mx_quantize_cols(yb)
+    assert_mx_close(np_(u["a_qc"])[:, :R], np_(u["a_sc"])[:, :R // 32], qc, sc, yb.T, "unfused a cols", rel_band=band)
+    dY = np_(inp["dY"])[:R].copy()
+    da = O.bf16_round(O.grouped_gemm_rows(dY, np_(inp["W2"]), rt))
+    assert_bf16_close(np_(u["da"])[:R], da, "unfused da")
+    du, dg = O.act_bwd(*O.unpack_glu_cols(fo.pre_bf16), da, prm)
+    d = O.pack_glu_cols(du, dg)
+    d[~real] = 0
+    db = O.bf16_round(d).astype(np.float32)
+    assert_bf16_close(np_(u["d"])[:R], db, "unfused dFC1")
+    q, s_ = O.mx_quantize_rows(db)
+    assert_mx_close(np_(u["d_q"])[:R], np_(u["d_s"])[:R], q, s_, db, "unfused dFC1 rows", rel_band=band)
