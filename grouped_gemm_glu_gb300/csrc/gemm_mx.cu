@@ -14,16 +14,20 @@
 //                 (128-row tile, 128-element k-block) 512 contiguous bytes,
 //                 byte 16*l + 4*j + i = scale of row 32*j + l, k sub-block i
 //                 (a gather done by thousands of warps in parallel)
-//   k_grouped_mx  persistent GEMM, 6 warps, one CTA per SM:
-//     warps 0-3  epilogue (thread = accumulator row): one wait for all 128
-//                columns, frees the accumulator, then bf16 / fp32 rows staged
-//                in shared memory and stored as full 128-byte lines
-//     warp  4    TMA producer: A and B tiles of 128 x 128 bytes (128-byte
-//                swizzle) and the two 512-byte scale blocks (1-D bulk
-//                copies), all completing on the stage's mbarrier
-//     warp  5    TMEM owner + MMA issuer: tcgen05.cp of the scale blocks into
-//                tensor memory, then 4 MMAs of K = 32 (M = N = 128) selecting
-//                scale byte k of each 32-bit column
+//   k_grouped_mx  persistent GEMM, 10 warps, one CTA per SM, 128 x 256 tiles:
+//     warps 0-7  epilogue: warp w reads TMEM lane quarter w % 4 and columns
+//                128 * (w / 4) .. +128 with one wait, releases the
+//                accumulator, then stages 8 rows at a time in shared memory
+//                and stores full 128-byte lines (bf16 / fp32)
+//     warp  8    TMA producer: A (128 x 128 bytes) and B (256 x 128 bytes)
+//                tiles with the 128-byte swizzle, and the scale blocks (512 +
+//                1024 bytes, 1-D bulk copies), all completing on the stage's
+//                mbarrier; 4 stages
+//     warp  9    TMEM owner + MMA issuer: tcgen05.cp of the scale blocks into
+//                tensor memory, then 4 MMAs of K = 32 (M = 128, N = 256)
+//                selecting scale byte k of each 32-bit column
+// The 256-wide tile halves the shared-memory traffic per FLOP of a 128-wide
+// one (each stage is written once by TMA and read once by the tensor core).
 // Every wait is bounded (MOE_ERR_TIMEOUT + early exit, never a trap).
 #include "common.cuh"
 #include "host_common.h"
@@ -31,20 +35,23 @@
 namespace moeglu {
 namespace gmx {
 
-constexpr int BM = 128, BN = 128, BK = 128, STAGES = 5;
-constexpr int EPI_WARPS = 4;
-constexpr int PRODUCER_WARP = 4, MMA_WARP = 5;
-constexpr int THREADS = 6 * 32;
+constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
+constexpr int EPI_WARPS = 8;
+constexpr int PRODUCER_WARP = 8, MMA_WARP = 9;
+constexpr int THREADS = 10 * 32;
 constexpr int A_TILE = BM * BK;
 constexpr int B_TILE = BN * BK;
 constexpr int STAGE_BYTES = A_TILE + B_TILE;
-constexpr int SF_BLOCK = 512;             // one (128-row tile, k-block) of scales
-constexpr int SF_STAGE = 2 * SF_BLOCK;    // A then B
+constexpr int SF_BLOCK = 512;             // one (128-row group, k-block) of scales
+constexpr int SFB_BYTES = 2 * SF_BLOCK;   // the B tile's two 128-row groups
+constexpr int SF_STAGE = SF_BLOCK + SFB_BYTES;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t SFA_COL = 2 * BN, SFB_COL = 2 * BN + 4;
+// accumulator: columns 0..255 (one buffer); scales of A: 4 columns; of B: 8
+constexpr uint32_t SFA_COL = BN, SFB_COL = BN + 4;
 constexpr int E_MAX = 1024;
 constexpr int EPI_ROW_BYTES = 256 + 16;   // staged output row (64 words + pad)
-constexpr int EPI_WARP_BYTES = 32 * EPI_ROW_BYTES;
+constexpr int EPI_ROWS = 8;               // rows staged per pass
+constexpr int EPI_WARP_BYTES = EPI_ROWS * EPI_ROW_BYTES;
 constexpr int OFF_SF = STAGES * STAGE_BYTES;
 constexpr int OFF_EPI = OFF_SF + STAGES * SF_STAGE;
 constexpr int OFF_PREF = OFF_EPI + EPI_WARPS * EPI_WARP_BYTES;
@@ -151,7 +158,7 @@ __device__ __forceinline__ Tile decode(int t, const int32_t* pref, const Args& a
     ti.kseg = a.K;
     ti.num_kb = a.K / BK;
     ti.sfa = (size_t)(pref[lo] + m_idx) * a.KB * SF_BLOCK;
-    ti.sfb = ((size_t)lo * a.n_tiles_n + n_idx) * a.KB * SF_BLOCK;
+    ti.sfb = ((size_t)lo * a.n_tiles_n + n_idx) * a.KB * SFB_BYTES;
   } else {
     const int per_e = a.m_tiles * a.n_tiles_n;
     ti.e = t / per_e;
@@ -166,14 +173,16 @@ __device__ __forceinline__ Tile decode(int t, const int32_t* pref, const Args& a
     ti.kseg = (o0 < 0 || o1 > a.R_cap || o1 < o0) ? 0 : o1 - o0;
     ti.num_kb = (ti.kseg + BK - 1) / BK;
     ti.sfa = ((size_t)m_idx * a.KG + pref[ti.e]) * SF_BLOCK;
-    ti.sfb = ((size_t)n_idx * a.KG + pref[ti.e]) * SF_BLOCK;
+    ti.sfb = ((size_t)n_idx * a.KG + pref[ti.e]) * SFB_BYTES;
   }
   return ti;
 }
 
 // ---------------------------------------------------------------------------
-// Scale re-tiling.  One warp per 512-byte block; lane l gathers the 4 scale
-// bytes of rows 32j + l (j = 0..3) and writes its 16 bytes.
+// Scale re-tiling.  One warp per 512-byte block (128 rows of A, or one of
+// the two 128-row halves of a 256-row B tile); lane l gathers the 4 scale
+// bytes of rows 32j + l (j = 0..3) and writes its 16 bytes.  Rows past the
+// operand's end read as 0.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t load4_unaligned(const uint8_t* row, int kbyte, int ks) {
   // bytes row[kbyte .. kbyte+3]; bytes at or past ks read as 0.  ks % 4 == 0.
@@ -189,16 +198,17 @@ __global__ void __launch_bounds__(256) k_sf_tile(const Args a) {
   if (__ldg(a.offsets + a.E) > a.R_cap) return;
   const int lane = threadIdx.x & 31;
   const int warps = blockDim.x >> 5;
+  const int bgroups = a.n_tiles_n * 2;  // 128-row groups of B (the last may pass N)
   size_t nA, nB;
   int ktot = 0;
   if (!a.kgrouped) {
     const int mt_cap = a.R_cap / BM + a.E;
     nA = (size_t)min(pref[a.E], mt_cap) * a.KB;
-    nB = (size_t)a.E * a.n_tiles_n * a.KB;
+    nB = (size_t)a.E * bgroups * a.KB;
   } else {
     ktot = min(pref[a.E], a.KG);
     nA = (size_t)a.m_tiles * ktot;
-    nB = (size_t)a.n_tiles_n * ktot;
+    nB = (size_t)bgroups * ktot;
   }
   const size_t total = nA + nB;
   for (size_t it = (size_t)blockIdx.x * warps + (threadIdx.x >> 5); it < total; it += (size_t)gridDim.x * warps) {
@@ -221,13 +231,14 @@ __global__ void __launch_bounds__(256) k_sf_tile(const Args a) {
         const size_t jb = it - nA;
         const int kb = (int)(jb % a.KB);
         const size_t rest = jb / a.KB;
-        const int nt = (int)(rest % a.n_tiles_n), e = (int)(rest / a.n_tiles_n);
+        const int g = (int)(rest % bgroups), e = (int)(rest / bgroups);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const int n = nt * BN + 32 * j + lane;
-          v[j] = __ldg(reinterpret_cast<const uint32_t*>(a.Bs + ((size_t)e * a.N + n) * ks + kb * 4));
+          const int n = g * 128 + 32 * j + lane;
+          v[j] = n < a.N ? __ldg(reinterpret_cast<const uint32_t*>(a.Bs + ((size_t)e * a.N + n) * ks + kb * 4)) : 0u;
         }
-        dst = a.sfb_t + jb * SF_BLOCK;
+        // [expert][n tile][k-block][half of the tile][512 bytes]
+        dst = a.sfb_t + ((((size_t)e * a.n_tiles_n + (g >> 1)) * a.KB + kb) * 2 + (g & 1)) * SF_BLOCK;
       }
     } else {
       const int ks = a.R_cap / 32;
@@ -237,52 +248,66 @@ __global__ void __launch_bounds__(256) k_sf_tile(const Args a) {
       const int e = find_group(pref, a.E, kg);
       const int kbyte = __ldg(a.offsets + e) / 32 + (kg - pref[e]) * 4;
       const uint8_t* base = isA ? a.As : a.Bs;
+      const int rows = isA ? a.M : a.N;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int r = rt * BM + 32 * j + lane;
-        v[j] = load4_unaligned(base + (size_t)r * ks, kbyte, ks);
+        const int r = rt * 128 + 32 * j + lane;
+        v[j] = r < rows ? load4_unaligned(base + (size_t)r * ks, kbyte, ks) : 0u;
       }
-      dst = (isA ? a.sfa_t : a.sfb_t) + ((size_t)rt * a.KG + kg) * SF_BLOCK;
+      // A: [m tile][k-block][512]; B: [n tile][k-block][half][512]
+      dst = isA ? a.sfa_t + ((size_t)rt * a.KG + kg) * SF_BLOCK
+                : a.sfb_t + (((size_t)(rt >> 1) * a.KG + kg) * 2 + (rt & 1)) * SF_BLOCK;
     }
     reinterpret_cast<uint4*>(dst)[lane] = make_uint4(v[0], v[1], v[2], v[3]);
   }
 }
 
-// Epilogue pass: stages 32 rows x 256 bytes of this warp's accumulator rows
-// (fp32: columns P..P+63; bf16: all 128) in shared memory and stores them as
-// full 128-byte lines, 2 rows per instruction.
+// Epilogue pass over this warp's 32 accumulator rows and its 128 columns
+// 128 * h .. (v[] holds them): fp32 goes out in two passes of 64 columns
+// (P = 0, 64), bf16 in one pass of 128.  Rows are staged 8 at a time in
+// shared memory (256 bytes each) and stored two rows per instruction as full
+// 128-byte lines; columns at or past N are not stored.
 template <bool F32, int P>
-__device__ __forceinline__ void store_pass(const Args& a, const Tile& ti, const float* v, uint8_t* stg, int q,
+__device__ __forceinline__ void store_pass(const Args& a, const Tile& ti, const float* v, uint8_t* stg, int q, int h,
                                            int lane) {
-  if (F32) {
-    float4* d = reinterpret_cast<float4*>(stg + lane * EPI_ROW_BYTES);
-#pragma unroll
-    for (int w = 0; w < 16; ++w) d[w] = make_float4(v[P + 4 * w], v[P + 4 * w + 1], v[P + 4 * w + 2], v[P + 4 * w + 3]);
-  } else {
-    uint4* d = reinterpret_cast<uint4*>(stg + lane * EPI_ROW_BYTES);
-#pragma unroll
-    for (int w = 0; w < 16; ++w)
-      d[w] = make_uint4(pack_bf16x2(v[8 * w], v[8 * w + 1]), pack_bf16x2(v[8 * w + 2], v[8 * w + 3]),
-                        pack_bf16x2(v[8 * w + 4], v[8 * w + 5]), pack_bf16x2(v[8 * w + 6], v[8 * w + 7]));
-  }
-  __syncwarp();
   const int es = F32 ? 4 : 2;
   const int half = lane >> 4, ch = lane & 15;
-#pragma unroll 4
-  for (int rr = 0; rr < 32; rr += 2) {
-    const int row = rr + half;
-    const int r_local = q * 32 + row;
-    if (r_local < ti.rows_pad) {
-      const uint4 val = *reinterpret_cast<const uint4*>(stg + row * EPI_ROW_BYTES + ch * 16);
-      uint8_t* g;
-      if (!a.kgrouped)
-        g = reinterpret_cast<uint8_t*>(a.out) + ((size_t)(ti.m0 + r_local) * a.N + ti.n0 + P) * es;
-      else
-        g = reinterpret_cast<uint8_t*>(a.out) + (((size_t)ti.e * a.M + ti.m0 + r_local) * a.N + ti.n0 + P) * es;
-      *reinterpret_cast<uint4*>(g + ch * 16) = val;
+  const int col0 = ti.n0 + h * 128 + P;             // first column of this pass
+  const bool ch_ok = col0 + ch * (16 / es) < a.N;  // this lane's 16-byte chunk exists
+#pragma unroll
+  for (int g = 0; g < 32 / EPI_ROWS; ++g) {
+    if ((lane >> 3) == g) {
+      const int srow = lane & 7;
+      if (F32) {
+        float4* d = reinterpret_cast<float4*>(stg + srow * EPI_ROW_BYTES);
+#pragma unroll
+        for (int w = 0; w < 16; ++w)
+          d[w] = make_float4(v[P + 4 * w], v[P + 4 * w + 1], v[P + 4 * w + 2], v[P + 4 * w + 3]);
+      } else {
+        uint4* d = reinterpret_cast<uint4*>(stg + srow * EPI_ROW_BYTES);
+#pragma unroll
+        for (int w = 0; w < 16; ++w)
+          d[w] = make_uint4(pack_bf16x2(v[8 * w], v[8 * w + 1]), pack_bf16x2(v[8 * w + 2], v[8 * w + 3]),
+                            pack_bf16x2(v[8 * w + 4], v[8 * w + 5]), pack_bf16x2(v[8 * w + 6], v[8 * w + 7]));
+      }
     }
+    __syncwarp();
+#pragma unroll
+    for (int rr = 0; rr < EPI_ROWS; rr += 2) {
+      const int srow = rr + half;
+      const int r_local = q * 32 + g * EPI_ROWS + srow;
+      if (r_local < ti.rows_pad && ch_ok) {
+        const uint4 val = *reinterpret_cast<const uint4*>(stg + srow * EPI_ROW_BYTES + ch * 16);
+        uint8_t* gp;
+        if (!a.kgrouped)
+          gp = reinterpret_cast<uint8_t*>(a.out) + ((size_t)(ti.m0 + r_local) * a.N + col0) * es;
+        else
+          gp = reinterpret_cast<uint8_t*>(a.out) + (((size_t)ti.e * a.M + ti.m0 + r_local) * a.N + col0) * es;
+        *reinterpret_cast<uint4*>(gp + ch * 16) = val;
+      }
+    }
+    __syncwarp();
   }
-  __syncwarp();
 }
 
 // ---------------------------------------------------------------------------
@@ -362,7 +387,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             tma_load_2d(dst + A_TILE, &tmB, full + stage, ti.kseg0 + kb * BK, ti.n0);
           }
           bulk_load(sdst, a.sfa_t + ti.sfa + (size_t)kb * SF_BLOCK, SF_BLOCK, full + stage);
-          bulk_load(sdst + SF_BLOCK, a.sfb_t + ti.sfb + (size_t)kb * SF_BLOCK, SF_BLOCK, full + stage);
+          bulk_load(sdst + SF_BLOCK, a.sfb_t + ti.sfb + (size_t)kb * SFB_BYTES, SFB_BYTES, full + stage);
           issued |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -387,11 +412,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       int lt = 0;
       for (int t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
         const Tile ti = decode(t, pref, a);
-        const int buf = lt & 1;
-        const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
+        const int buf = 0;  // one accumulator: the epilogue frees it as soon as it has read it
+        const uint32_t aph = (uint32_t)lt & 1u;
         if (!mbar_wait(acc_empty + buf, aph ^ 1u, guard)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+        const uint32_t d_tmem = tmem_base;
         bool ok = true;
         for (int kb = 0; kb < ti.num_kb; ++kb) {
           if (!mbar_wait(full + stage, phase, guard)) {
@@ -404,6 +429,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t sf_addr = smem_u32(sf + stage * SF_STAGE);
           tc_cp_32x128b_x4(tmem_base + SFA_COL, sdesc_noswizzle(sf_addr, 128));
           tc_cp_32x128b_x4(tmem_base + SFB_COL, sdesc_noswizzle(sf_addr + SF_BLOCK, 128));
+          tc_cp_32x128b_x4(tmem_base + SFB_COL + 4, sdesc_noswizzle(sf_addr + 2 * SF_BLOCK, 128));
           const int nsub = min(4, (ti.kseg - kb * BK) / 32);
           for (int k = 0; k < nsub; ++k) {
             umma_mxf8(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32), sdesc_kmajor_sw128(b_addr + k * 32),
@@ -425,23 +451,24 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_wait(mma_done, 0, drain);
     }
   } else {
-    const int q = warp;
-    uint8_t* stg = epi_all + q * EPI_WARP_BYTES;
+    const int q = warp & 3, h = warp >> 2;
+    uint8_t* stg = epi_all + warp * EPI_WARP_BYTES;
     const int out_es = (a.kgrouped && a.out_f32) ? 4 : 2;  // output element size
     int lt = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
-      const int buf = lt & 1;
-      const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
+      const int buf = 0;
+      const uint32_t aph = (uint32_t)lt & 1u;
       int ok = 1;
       if (lane == 0) ok = mbar_wait(acc_full + buf, aph, guard) ? 1 : 0;
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
       tc_fence_after();
       const Tile ti = decode(t, pref, a);
-      const bool live = q * 32 < ti.rows_pad;
+      const bool live = q * 32 < ti.rows_pad && ti.n0 + h * 128 < a.N;
       const bool real = q * 32 + lane < ti.rows_valid;
-      float v[BN];
-      if (live && ti.num_kb > 0) tmem_ld128(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN), v);
+      float v[128];
+      if (live && ti.num_kb > 0)
+        tmem_ld128(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * 128), v);
       // the accumulator is in registers: hand the buffer back to the MMA
       tc_fence_before();
       __syncwarp();
@@ -449,13 +476,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!live) continue;
       if (ti.num_kb == 0 || !real) {
 #pragma unroll
-        for (int i = 0; i < BN; ++i) v[i] = 0.0f;
+        for (int i = 0; i < 128; ++i) v[i] = 0.0f;
       }
       if (out_es == 4) {
-        store_pass<true, 0>(a, ti, v, stg, q, lane);
-        store_pass<true, 64>(a, ti, v, stg, q, lane);
+        store_pass<true, 0>(a, ti, v, stg, q, h, lane);
+        store_pass<true, 64>(a, ti, v, stg, q, h, lane);
       } else {
-        store_pass<false, 0>(a, ti, v, stg, q, lane);
+        store_pass<false, 0>(a, ti, v, stg, q, h, lane);
       }
     }
   }
@@ -485,16 +512,18 @@ static moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const
 
 static size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
 
+static int n_tiles(int N) { return (N + BN - 1) / BN; }
+
 static void fc2_ws_parts(int E, int K, int N, int R_cap, size_t* a_bytes, size_t* b_bytes) {
   const size_t KB = (size_t)K / BK;
   *a_bytes = align_up(((size_t)R_cap / BM + E) * KB * SF_BLOCK);
-  *b_bytes = align_up((size_t)E * (N / BN) * KB * SF_BLOCK);
+  *b_bytes = align_up((size_t)E * n_tiles(N) * KB * SFB_BYTES);
 }
 
 static void wgrad_ws_parts(int E, int M, int N, int R_cap, size_t* a_bytes, size_t* b_bytes) {
   const size_t KG = (size_t)R_cap / BK + E;
   *a_bytes = align_up((size_t)(M / BM) * KG * SF_BLOCK);
-  *b_bytes = align_up((size_t)(N / BN) * KG * SF_BLOCK);
+  *b_bytes = align_up((size_t)n_tiles(N) * KG * SFB_BYTES);
 }
 
 }  // namespace gmx
@@ -522,7 +551,7 @@ extern "C" moe_status_t moe_grouped_fc2_fwd(const uint8_t* Aq, const uint8_t* As
                                             int sm_margin, int32_t* status, moe_stream_t stream) {
   using namespace gmx;
   if (!Aq || !As || !Wq || !Ws || !counts || !offsets || !y || !ws) return MOE_ERR_ARG;
-  if (E <= 0 || E > E_MAX || K <= 0 || (K % BK) || N <= 0 || (N % BN) || R_cap <= 0 || (R_cap % BM))
+  if (E <= 0 || E > E_MAX || K <= 0 || (K % BK) || N <= 0 || (N % 128) || R_cap <= 0 || (R_cap % BM))
     return MOE_ERR_ARG;
   if (!aligned16(Aq) || !aligned16(Wq) || !aligned16(y) || (reinterpret_cast<uintptr_t>(As) & 3) ||
       (reinterpret_cast<uintptr_t>(Ws) & 3) || (reinterpret_cast<uintptr_t>(ws) & 255) || sm_margin < 0)
@@ -554,7 +583,7 @@ extern "C" moe_status_t moe_grouped_fc2_fwd(const uint8_t* Aq, const uint8_t* As
   a.K = K;
   a.R_cap = R_cap;
   a.kgrouped = 0;
-  a.n_tiles_n = N / BN;
+  a.n_tiles_n = n_tiles(N);
   a.m_tiles = 0;
   a.KB = K / BK;
   a.KG = 0;
@@ -567,8 +596,8 @@ extern "C" moe_status_t moe_grouped_fc2_fwd(const uint8_t* Aq, const uint8_t* As
   a.status = status;
   a.wait_ns = g_wait_limit_ns.load();
   const long long mt_bound = (long long)R_cap / BM + E;
-  const long long bound = mt_bound * (N / BN);
-  const long long sf_items = mt_bound * a.KB + (long long)E * a.n_tiles_n * a.KB;
+  const long long bound = mt_bound * a.n_tiles_n;
+  const long long sf_items = mt_bound * a.KB + (long long)E * 2 * a.n_tiles_n * a.KB;
   return launch(tmA, tmB, a, bound, sf_items, sm_margin, as_stream(stream));
 }
 
@@ -578,7 +607,7 @@ extern "C" moe_status_t moe_grouped_wgrad(const uint8_t* Aq, const uint8_t* As, 
                                           int32_t* status, moe_stream_t stream) {
   using namespace gmx;
   if (!Aq || !As || !Bq || !Bs || !counts || !offsets || !D || !ws) return MOE_ERR_ARG;
-  if (E <= 0 || E > E_MAX || M <= 0 || (M % BM) || N <= 0 || (N % BN) || R_cap <= 0 || (R_cap % BM))
+  if (E <= 0 || E > E_MAX || M <= 0 || (M % BM) || N <= 0 || (N % 128) || R_cap <= 0 || (R_cap % BM))
     return MOE_ERR_ARG;
   if (!aligned16(Aq) || !aligned16(Bq) || !aligned16(D) || (reinterpret_cast<uintptr_t>(As) & 3) ||
       (reinterpret_cast<uintptr_t>(Bs) & 3) || (reinterpret_cast<uintptr_t>(ws) & 255) || sm_margin < 0)
@@ -610,7 +639,7 @@ extern "C" moe_status_t moe_grouped_wgrad(const uint8_t* Aq, const uint8_t* As, 
   a.K = 0;
   a.R_cap = R_cap;
   a.kgrouped = 1;
-  a.n_tiles_n = N / BN;
+  a.n_tiles_n = n_tiles(N);
   a.m_tiles = M / BM;
   a.KB = 0;
   a.KG = R_cap / BK + E;
@@ -622,7 +651,7 @@ extern "C" moe_status_t moe_grouped_wgrad(const uint8_t* Aq, const uint8_t* As, 
   a.out_f32 = out_f32 ? 1 : 0;
   a.status = status;
   a.wait_ns = g_wait_limit_ns.load();
-  const long long bound = (long long)E * (M / BM) * (N / BN);
-  const long long sf_items = (long long)(M / BM + N / BN) * a.KG;
+  const long long bound = (long long)E * (M / BM) * a.n_tiles_n;
+  const long long sf_items = (long long)(M / BM + 2 * a.n_tiles_n) * a.KG;
   return launch(tmA, tmB, a, bound, sf_items, sm_margin, as_stream(stream));
 }
