@@ -39,6 +39,21 @@ int max_active_pairs(const void* kernel, int threads, int smem_bytes) {
   return n;
 }
 
+int max_active_blocks(const void* kernel, int threads, int smem_bytes) {
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, int, int, int>, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_tuple(kernel, dev, threads, smem_bytes);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem_bytes) != cudaSuccess) return 0;
+  cache[key] = n;
+  return n;
+}
+
 int sm_count() {
   static int cached[64] = {0};
   int dev = 0;

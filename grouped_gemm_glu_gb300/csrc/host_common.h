@@ -29,6 +29,10 @@ int sm_count();
 // kernel and device); 0 on failure.
 int max_active_pairs(const void* kernel, int threads, int smem_bytes);
 
+// CTAs of `kernel` resident per SM at `threads` threads and `smem_bytes` of
+// dynamic shared memory (cached; 0 on failure).
+int max_active_blocks(const void* kernel, int threads, int smem_bytes);
+
 // Opts a kernel into `bytes` of dynamic shared memory (once per kernel and
 // device; returns false on failure).
 bool set_smem_limit(const void* kernel, int bytes);

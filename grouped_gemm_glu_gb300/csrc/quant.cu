@@ -39,134 +39,171 @@ __device__ __forceinline__ void load_seg(const int32_t* counts, const int32_t* o
   __syncthreads();
 }
 
-// Row-wise: one thread per 32-element block.  rows >= offsets[E] untouched,
-// rows of an expert past its count are quantised as zeros.
+// Row-wise.  The blocks of src [G][R][C] are contiguous runs of 32 elements,
+// so the tensor is streamed flat: a warp task is QR_TASK consecutive blocks;
+// in each of its QR_TASK / 8 loads a lane holds 8 elements (16 bytes) of
+// block 8u + lane / 4, the 4 lanes of a block combine their amax with two
+// shuffles, and every load and store instruction of the warp covers
+// contiguous memory (512 bytes in, 256 bytes of codes out).  Rows >=
+// offsets[E] are untouched; rows of an expert past its count quantise as 0.
+constexpr int QR_TASK = 64;
+constexpr int QR_LOADS = QR_TASK / 8;
+
 __global__ void __launch_bounds__(256) k_quant_rows(const uint16_t* __restrict__ src, int G, int R, int Cc,
                                                     const int32_t* __restrict__ counts,
                                                     const int32_t* __restrict__ offsets, int E,
                                                     uint8_t* __restrict__ q, uint8_t* __restrict__ s) {
-  __shared__ int32_t s_off[QE_MAX + 1];
-  __shared__ int32_t s_cnt[QE_MAX];
+  extern __shared__ int32_t seg[];  // s_off [E + 1], s_cnt [E]
+  int32_t* s_off = seg;
+  int32_t* s_cnt = seg + E + 1;
   if (E > 0) load_seg(counts, offsets, E, s_off, s_cnt);
+  const int lane = threadIdx.x & 31, quarter = lane & 3;
   const int nb = Cc / 32;
-  const size_t total = (size_t)G * R * nb;
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
-    const size_t rowg = i / nb;  // g*R + r
-    const int b = (int)(i - rowg * nb);
-    const int r = (int)(rowg % R);
-    bool zero = false;
-    if (E > 0) {
-      const int real = block_real_rows(r & ~31, s_off, s_cnt, E);
-      if (real < 0) continue;
-      zero = (r & 31) >= real;
+  const size_t nblocks = (size_t)G * R * nb;
+  const size_t tasks = (nblocks + QR_TASK - 1) / QR_TASK;
+  const size_t nwarps = ((size_t)gridDim.x * blockDim.x) >> 5;
+  for (size_t task = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; task < tasks; task += nwarps) {
+    uint4 x[QR_LOADS];
+    bool keep[QR_LOADS];
+#pragma unroll
+    for (int u = 0; u < QR_LOADS; ++u) {
+      const size_t blk = task * QR_TASK + 8 * u + (lane >> 2);
+      keep[u] = blk < nblocks;
+      bool zero = false;
+      if (E > 0 && keep[u]) {
+        const int r = (int)(blk / nb);
+        const int real = block_real_rows(r & ~31, s_off, s_cnt, E);
+        keep[u] = real >= 0;
+        zero = (r & 31) >= real;
+      }
+      x[u] = make_uint4(0, 0, 0, 0);
+      if (keep[u] && !zero) x[u] = __ldg(reinterpret_cast<const uint4*>(src + blk * 32 + quarter * 8));
     }
-    float v[32];
-    if (zero) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = 0.0f;
-    } else {
-      const uint4* p = reinterpret_cast<const uint4*>(src + rowg * Cc + (size_t)b * 32);
+    for (int u = 0; u < QR_LOADS; ++u) {
+      const float v[8] = {bf16_lo(x[u].x), bf16_hi(x[u].x), bf16_lo(x[u].y), bf16_hi(x[u].y),
+                          bf16_lo(x[u].z), bf16_hi(x[u].z), bf16_lo(x[u].w), bf16_hi(x[u].w)};
+      uint32_t m = 0;
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const uint4 x = __ldg(p + w);
-        v[8 * w + 0] = bf16_lo(x.x);
-        v[8 * w + 1] = bf16_hi(x.x);
-        v[8 * w + 2] = bf16_lo(x.y);
-        v[8 * w + 3] = bf16_hi(x.y);
-        v[8 * w + 4] = bf16_lo(x.z);
-        v[8 * w + 5] = bf16_hi(x.z);
-        v[8 * w + 6] = bf16_lo(x.w);
-        v[8 * w + 7] = bf16_hi(x.w);
+      for (int i = 0; i < 8; ++i) m = max(m, abs_bits(v[i]));
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+      const uint32_t sb = e8m0_from_amax_bits(m);
+      uint2 c = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+      if (sb != 0xFFu) {
+        const float inv = mx_inv_scale(sb);
+        c.x = e4m3x2(v[0] * inv, v[1] * inv) | (e4m3x2(v[2] * inv, v[3] * inv) << 16);
+        c.y = e4m3x2(v[4] * inv, v[5] * inv) | (e4m3x2(v[6] * inv, v[7] * inv) << 16);
+      }
+      if (keep[u]) {
+        const size_t blk = task * QR_TASK + 8 * u + (lane >> 2);
+        *reinterpret_cast<uint2*>(q + blk * 32 + quarter * 8) = c;
+        if (quarter == 0) s[blk] = (uint8_t)sb;
       }
     }
-    uint32_t codes[8];
-    const uint32_t sb = mx_quant_block32(v, codes);
-    uint4* dq = reinterpret_cast<uint4*>(q + rowg * Cc + (size_t)b * 32);
-    dq[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-    dq[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-    s[rowg * nb + b] = (uint8_t)sb;
   }
 }
 
-// Column-wise (transposed).  A CTA owns a tile of 128 rows (four MX blocks
-// along R) x 64 columns:
-//   1. coalesced 16-byte loads of the 128 x 64 bf16 tile into shared memory
-//      (8 lanes per 128-byte row);
-//   2. thread (column c, block b) quantises the 32 values of column c in
-//      rows 32b..32b+31 (consecutive lanes read consecutive columns: no bank
-//      conflicts) and writes its 32 codes into a [64][128]-byte code tile;
+// Column-wise (transposed).  A CTA streams tiles of 128 rows (four MX blocks
+// along R) x 64 columns through a ring of QC_STAGES shared-memory buffers
+// filled by TMA (thread 0 issues; completion on one mbarrier per buffer):
+//   1. thread (column c, block b) reads the 32 values of column c in rows
+//      32b..32b+31 of the staged tile (consecutive lanes read consecutive
+//      columns: no bank conflicts), quantises them and writes its 32 codes
+//      into a [64][128]-byte code tile;
+//   2. the buffer is refilled with the tile QC_STAGES steps ahead;
 //   3. each column's 128 codes leave as one full 128-byte line (8 lanes x 16
-//      bytes, 4 columns per warp instruction); its 4 scales as one word.
-constexpr int QC_ROWS = 128, QC_COLS = 64;
-constexpr int QC_IN_ROW = QC_COLS * 2 + 16;  // padded bytes per staged input row
-constexpr int QC_CODE_ROW = QC_ROWS + 16;    // padded bytes per staged code column
+//      bytes, 4 columns per warp instruction), its 4 scales as bytes.
+// Rows past R or columns past C arrive as zeros from TMA and are not stored.
+constexpr int QC_ROWS = 128, QC_COLS = 64, QC_STAGES = 3;
+constexpr int QC_TILE = QC_ROWS * QC_COLS * 2;  // bytes of one staged bf16 tile (128-byte rows)
+constexpr int QC_CODE_ROW = QC_ROWS + 16;       // padded bytes per staged code column
+constexpr int QC_OFF_CODE = QC_STAGES * QC_TILE;
+constexpr int QC_OFF_SCALE = QC_OFF_CODE + QC_COLS * QC_CODE_ROW;
+constexpr int QC_OFF_BARS = QC_OFF_SCALE + QC_COLS * 4;
+constexpr int QC_OFF_MISC = QC_OFF_BARS + QC_STAGES * 8;  // real_rows[2][4], abort flag
+constexpr int QC_OFF_SEG = QC_OFF_MISC + 48;
+constexpr int QC_SMEM_BASE = QC_OFF_SEG;                  // + (2E + 1) ints of expert map
 
-__global__ void __launch_bounds__(256) k_quant_cols(const uint16_t* __restrict__ src, int G, int R, int Cc,
+__global__ void __launch_bounds__(256) k_quant_cols(const __grid_constant__ CUtensorMap tm, int G, int R, int Cc,
                                                     const int32_t* __restrict__ counts,
                                                     const int32_t* __restrict__ offsets, int E,
-                                                    uint8_t* __restrict__ q, uint8_t* __restrict__ s) {
-  __shared__ int32_t s_off[QE_MAX + 1];
-  __shared__ int32_t s_cnt[QE_MAX];
-  __shared__ __align__(16) uint8_t tin[QC_ROWS * QC_IN_ROW];
-  __shared__ __align__(16) uint8_t tcode[QC_COLS * QC_CODE_ROW];
-  __shared__ uint8_t tscale[QC_COLS * 4];
-  __shared__ int real_rows[4];
-  if (E > 0) load_seg(counts, offsets, E, s_off, s_cnt);
+                                                    uint8_t* __restrict__ q, uint8_t* __restrict__ s,
+                                                    int32_t* status, uint64_t wait_ns) {
+  extern __shared__ __align__(128) uint8_t qsm[];
+  uint8_t* tin = qsm;
+  uint8_t* tcode = qsm + QC_OFF_CODE;
+  uint8_t* tscale = qsm + QC_OFF_SCALE;
+  uint64_t* full = reinterpret_cast<uint64_t*>(qsm + QC_OFF_BARS);
+  int* real_rows = reinterpret_cast<int*>(qsm + QC_OFF_MISC);  // [2][4]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(qsm + QC_OFF_MISC + 32);
+  int32_t* s_off = reinterpret_cast<int32_t*>(qsm + QC_OFF_SEG);
+  int32_t* s_cnt = s_off + E + 1;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  if (t == 0) {
+    for (int st = 0; st < QC_STAGES; ++st) mbar_init(full + st, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tm);
+  }
+  if (E > 0) load_seg(counts, offsets, E, s_off, s_cnt);  // (ends with a barrier)
+  __syncthreads();
   const int col_tiles = (Cc + QC_COLS - 1) / QC_COLS;
   // grouped rows: only the tiles that hold rows < offsets[E]
   const int rows_used = E > 0 ? max(0, min(R, s_off[E])) : R;
   const int row_tiles = (rows_used + QC_ROWS - 1) / QC_ROWS;
-  const size_t total = (size_t)G * row_tiles * col_tiles;
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int total = G * row_tiles * col_tiles;
   const int nblk = R / 32;
-  const int ch = t & 7;
-  // real rows of 32-row block rb (-1: past R or past offsets[E])
-  auto block_real = [&](int rb) -> int {
+  auto block_real = [&](int rb) -> int {  // real rows of the 32-row block at rb; -1: none stored
     int real = rb < R ? 32 : -1;
     if (E > 0 && real >= 0) real = block_real_rows(rb, s_off, s_cnt, E);
     return real;
   };
-  auto tile_coords = [&](size_t i, int& g, int& r0, int& c0) {
-    const int ct = (int)(i % col_tiles);
-    const size_t rest = i / col_tiles;
-    r0 = (int)(rest % row_tiles) * QC_ROWS;
-    g = (int)(rest / row_tiles);
+  auto coords = [&](int i, int& g, int& r0, int& c0) {
+    const int ct = i % col_tiles;
+    const int rest = i / col_tiles;
+    r0 = (rest % row_tiles) * QC_ROWS;
+    g = rest / row_tiles;
     c0 = ct * QC_COLS;
   };
-  // this thread's 4 chunks of a tile: rows t/8 + 32k, 16-byte chunk t%8
-  auto load_tile = [&](size_t i, uint4* v) {
+  auto issue = [&](int i, int st) {
     int g, r0, c0;
-    tile_coords(i, g, r0, c0);
-    const bool ch_ok = c0 + ch * 8 < Cc;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int rr = (t >> 3) + 32 * k;
-      v[k] = make_uint4(0, 0, 0, 0);
-      if (ch_ok && (rr & 31) < block_real(r0 + 32 * k))
-        v[k] = __ldg(reinterpret_cast<const uint4*>(src + ((size_t)g * R + r0 + rr) * Cc + c0 + ch * 8));
-    }
+    coords(i, g, r0, c0);
+    mbar_arrive_expect_tx(full + st, QC_TILE);
+    tma_load_3d(tin + st * QC_TILE, &tm, full + st, c0, r0, g);
   };
-  uint4 nxt[4];
-  size_t i = blockIdx.x;
-  if (i < total) load_tile(i, nxt);
-  for (; i < total; i += gridDim.x) {
-    int g, r0, c0;
-    tile_coords(i, g, r0, c0);
-    if (t < 4) real_rows[t] = block_real(r0 + 32 * t);
+  // step j of this CTA handles tile blockIdx.x + j * gridDim.x in buffer j % QC_STAGES;
+  // its load is issued at step j - QC_STAGES (steps 0..QC_STAGES-1: here)
+  if (t == 0) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4*>(tin + ((t >> 3) + 32 * k) * QC_IN_ROW + ch * 16) = nxt[k];
-    __syncthreads();
-    // prefetch the next tile while this one is quantised and stored
-    if (i + gridDim.x < total) load_tile(i + gridDim.x, nxt);
-    // quantise: warp w -> block b = w/2, columns (w%2)*32 + lane
+    for (int st = 0; st < QC_STAGES; ++st) {
+      const int i = blockIdx.x + st * gridDim.x;
+      if (i < total) issue(i, st);
+    }
+  }
+  WaitGuard guard{abort_flag, status, wait_ns};
+  int k = 0;
+  for (int i = blockIdx.x; i < total; i += gridDim.x, ++k) {
+    const int st = k % QC_STAGES;
+    const uint32_t ph = (uint32_t)(k / QC_STAGES) & 1u;
+    int g, r0, c0;
+    coords(i, g, r0, c0);
+    int* rr = real_rows + 4 * (k & 1);
+    if (t < 4) rr[t] = block_real(r0 + 32 * t);
+    const bool ok = mbar_wait(full + st, ph, guard);
+    if (__syncthreads_or(ok ? 0 : 1)) break;
+    // 1. quantise: warp w -> block b = w / 2, column (w % 2) * 32 + lane
     {
       const int b = warp >> 1;
       const int cl = (warp & 1) * 32 + lane;
+      const int real = rr[b];
+      const uint8_t* src = tin + st * QC_TILE + (32 * b) * (QC_COLS * 2) + cl * 2;
       float v[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        v[j] = __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t*>(tin + (32 * b + j) * QC_IN_ROW + cl * 2))
-                               << 16);
+        v[j] = j < real ? __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t*>(src + j * QC_COLS * 2))
+                                          << 16)
+                        : 0.0f;
       uint32_t codes[8];
       const uint32_t sb = mx_quant_block32(v, codes);
       uint4* dc = reinterpret_cast<uint4*>(tcode + cl * QC_CODE_ROW + 32 * b);
@@ -175,23 +212,35 @@ __global__ void __launch_bounds__(256) k_quant_cols(const uint16_t* __restrict__
       tscale[cl * 4 + b] = (uint8_t)sb;
     }
     __syncthreads();
-    // store: lane group of 8 -> one column's 128 bytes; 4 columns per warp pass
+    // 2. the buffer is free again: fetch the tile QC_STAGES steps ahead
+    if (t == 0) {
+      const int nxt = i + QC_STAGES * gridDim.x;
+      if (nxt < total) issue(nxt, st);
+    }
+    // 3. store: lane group of 8 -> one column's 128 bytes; 4 columns per warp pass
     {
       const int sub = lane >> 3, part = lane & 7;
-      const bool full = r0 + QC_ROWS <= R;
+      const bool whole = r0 + QC_ROWS <= R;
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int cl = warp * 8 + k * 4 + sub;
+      for (int h = 0; h < 2; ++h) {
+        const int cl = warp * 8 + h * 4 + sub;
         const int c = c0 + cl;
         if (c < Cc) {
           const uint4 val = *reinterpret_cast<const uint4*>(tcode + cl * QC_CODE_ROW + part * 16);
           uint8_t* dst = q + ((size_t)g * Cc + c) * R + r0 + part * 16;
-          if (full || r0 + part * 16 < R) *reinterpret_cast<uint4*>(dst) = val;
-          if (part < 4 && real_rows[part] >= 0) s[((size_t)g * Cc + c) * nblk + (r0 >> 5) + part] = tscale[cl * 4 + part];
+          if (whole || r0 + part * 16 < R) *reinterpret_cast<uint4*>(dst) = val;
+          if (part < 4 && rr[part] >= 0) s[((size_t)g * Cc + c) * nblk + (r0 >> 5) + part] = tscale[cl * 4 + part];
         }
       }
     }
-    __syncthreads();
+  }
+  // after a timeout at step k: the loads of steps k .. k + QC_STAGES - 1 were
+  // issued and not consumed; let them land before the CTA exits
+  if (t == 0 && *abort_flag) {
+    volatile int never = 0;
+    WaitGuard drain{&never, status, 100000000ull};
+    for (int j = k; j < k + QC_STAGES; ++j)
+      if (blockIdx.x + j * gridDim.x < total) mbar_wait(full + j % QC_STAGES, (uint32_t)(j / QC_STAGES) & 1u, drain);
   }
 }
 
@@ -311,7 +360,7 @@ static int grid_for(size_t items, int per_block) {
 using namespace moeglu;
 
 extern "C" moe_status_t moe_quantize_mxfp8(const moe_bf16* src, int G, int R, int Cc, int col, const int32_t* counts,
-                                           const int32_t* offsets, int E, uint8_t* q, uint8_t* s,
+                                           const int32_t* offsets, int E, uint8_t* q, uint8_t* s, int32_t* status,
                                            moe_stream_t stream) {
   if (!src || !q || !s || G <= 0 || R <= 0 || Cc <= 0) return MOE_ERR_ARG;
   if ((counts == nullptr) != (offsets == nullptr)) return MOE_ERR_ARG;
@@ -319,13 +368,33 @@ extern "C" moe_status_t moe_quantize_mxfp8(const moe_bf16* src, int G, int R, in
   if (!counts) E = 0;
   if (!aligned16(src) || !aligned16(q)) return MOE_ERR_ARG;
   cudaStream_t st = as_stream(stream);
+  const int sms = sm_count();
   if (!col) {
     if (Cc % 32) return MOE_ERR_ARG;
-    k_quant_rows<<<grid_for((size_t)G * R * (Cc / 32), 256), 256, 0, st>>>(src, G, R, Cc, counts, offsets, E, q, s);
+    const int smem = E > 0 ? (2 * E + 1) * 4 : 0;
+    const size_t tasks = ((size_t)G * R * (Cc / 32) + QR_TASK - 1) / QR_TASK;
+    const int occ = max(1, max_active_blocks((const void*)k_quant_rows, 256, 2 * QE_MAX * 4 + 4));
+    size_t grid = (tasks + 7) / 8;
+    if (grid > (size_t)sms * occ) grid = (size_t)sms * occ;
+    k_quant_rows<<<(int)(grid < 1 ? 1 : grid), 256, smem, st>>>(src, G, R, Cc, counts, offsets, E, q, s);
   } else {
     if ((R % 32) || (Cc % 8)) return MOE_ERR_ARG;
     const size_t tiles = (size_t)G * ((R + QC_ROWS - 1) / QC_ROWS) * ((Cc + QC_COLS - 1) / QC_COLS);
-    k_quant_cols<<<grid_for(tiles, 1), 256, 0, st>>>(src, G, R, Cc, counts, offsets, E, q, s);
+    if (tiles > (size_t)INT32_MAX) return MOE_ERR_ARG;
+    CUtensorMap tm;
+    const uint64_t dims[3] = {(uint64_t)Cc, (uint64_t)R, (uint64_t)G};
+    const uint64_t strides[2] = {(uint64_t)Cc * 2, (uint64_t)R * Cc * 2};
+    const uint32_t box[3] = {QC_COLS, QC_ROWS, 1};
+    if (!encode_tmap(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, src, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return MOE_ERR_CUDA;
+    const int smem = QC_SMEM_BASE + (2 * E + 1) * 4;
+    const int smem_max = QC_SMEM_BASE + (2 * QE_MAX + 1) * 4;
+    if (!set_smem_limit((const void*)k_quant_cols, smem_max)) return MOE_ERR_CUDA;
+    const int occ = max(1, max_active_blocks((const void*)k_quant_cols, 256, smem_max));
+    size_t grid = tiles;
+    if (grid > (size_t)sms * occ) grid = (size_t)sms * occ;
+    k_quant_cols<<<(int)(grid < 1 ? 1 : grid), 256, smem, st>>>(tm, G, R, Cc, counts, offsets, E, q, s, status,
+                                                               g_wait_limit_ns.load());
   }
   count_launch();
   return launch_status();

@@ -101,7 +101,7 @@ class MoeLayer:
                 _p(self.x_perm), _p(self.W1p), _p(self.b1p), None, _p(self.counts), _p(self.offsets), E, H, F, R,
                 C.byref(self.params), L.OUT_MXFP8, C.byref(self.fc1_out), self.sm_margin, st, s)),
             ("quant_w2", lambda: lib.moe_quantize_mxfp8(
-                _p(self.W2), E, F, H, 1, None, None, 0, _p(self.W2q), _p(self.W2s), s)),
+                _p(self.W2), E, F, H, 1, None, None, 0, _p(self.W2q), _p(self.W2s), st, s)),
             ("fc2", lambda: lib.moe_grouped_fc2_fwd(
                 _p(self.a_q), _p(self.a_s), _p(self.W2q), _p(self.W2s), _p(self.counts), _p(self.offsets), E, F,
                 H, R, _p(self.y_perm), _p(self.ws_fc2), self.ws_fc2.numel(), self.sm_margin, st, s)),
@@ -118,14 +118,14 @@ class MoeLayer:
                 _p(dY_perm), _p(self.W2), _p(self.pre), None, _p(self.counts), _p(self.offsets), E, H, F, R,
                 C.byref(self.params), L.OUT_MXFP8, C.byref(self.bwd_out), self.sm_margin, st, s)),
             ("quant_w1", lambda: lib.moe_quantize_mxfp8(
-                _p(self.W1p), E, N1, H, 1, None, None, 0, _p(self.W1q), _p(self.W1s), s)),
+                _p(self.W1p), E, N1, H, 1, None, None, 0, _p(self.W1q), _p(self.W1s), st, s)),
             ("dx", lambda: lib.moe_grouped_fc2_fwd(
                 _p(self.d_q), _p(self.d_s), _p(self.W1q), _p(self.W1s), _p(self.counts), _p(self.offsets), E, N1,
                 H, R, _p(self.dX_perm), _p(self.ws_dx), self.ws_dx.numel(), self.sm_margin, st, s)),
             ("quant_x_col", lambda: lib.moe_quantize_mxfp8(
-                _p(self.x_perm), 1, R, H, 1, _p(self.counts), _p(self.offsets), E, _p(self.x_qc), _p(self.x_sc), s)),
+                _p(self.x_perm), 1, R, H, 1, _p(self.counts), _p(self.offsets), E, _p(self.x_qc), _p(self.x_sc), st, s)),
             ("quant_dy_col", lambda: lib.moe_quantize_mxfp8(
-                _p(dY_perm), 1, R, H, 1, _p(self.counts), _p(self.offsets), E, _p(self.dy_qc), _p(self.dy_sc), s)),
+                _p(dY_perm), 1, R, H, 1, _p(self.counts), _p(self.offsets), E, _p(self.dy_qc), _p(self.dy_sc), st, s)),
             ("wgrad_w1", lambda: lib.moe_grouped_wgrad(
                 _p(self.d_qc), _p(self.d_sc), _p(self.x_qc), _p(self.x_sc), _p(self.counts), _p(self.offsets), E,
                 N1, H, R, _p(self.dW1), 0, _p(self.ws_wg1), self.ws_wg1.numel(), self.sm_margin, st, s)),
@@ -164,9 +164,9 @@ class MoeLayer:
                 L.OUT_BF16, C.byref(self._u_fwd_out), self.sm_margin, st, s)),
             ("act", lambda: lib.moe_glu_act(_p(u["pre"]), cnt, off, E, F, R, C.byref(self.params), _p(u["y"]), s)),
             ("quant_rows", lambda: lib.moe_quantize_mxfp8(_p(u["y"]), 1, R, F, 0, cnt, off, E, _p(u["a_q"]),
-                                                          _p(u["a_s"]), s)),
+                                                          _p(u["a_s"]), st, s)),
             ("quant_cols", lambda: lib.moe_quantize_mxfp8(_p(u["y"]), 1, R, F, 1, cnt, off, E, _p(u["a_qc"]),
-                                                          _p(u["a_sc"]), s)),
+                                                          _p(u["a_sc"]), st, s)),
         ]
 
     def backward_unfused_calls(self, dY_perm):
@@ -182,9 +182,9 @@ class MoeLayer:
             ("dact", lambda: lib.moe_dglu_act(_p(u["da"]), _p(self.pre), cnt, off, E, F, R, C.byref(self.params),
                                               _p(u["d"]), s)),
             ("quant_rows", lambda: lib.moe_quantize_mxfp8(_p(u["d"]), 1, R, N1, 0, cnt, off, E, _p(u["d_q"]),
-                                                          _p(u["d_s"]), s)),
+                                                          _p(u["d_s"]), st, s)),
             ("quant_cols", lambda: lib.moe_quantize_mxfp8(_p(u["d"]), 1, R, N1, 1, cnt, off, E, _p(u["d_qc"]),
-                                                          _p(u["d_sc"]), s)),
+                                                          _p(u["d_sc"]), st, s)),
         ]
 
     def step_calls(self, x, topk_idx, topk_prob, dY_perm):

@@ -44,7 +44,7 @@ _SIGS = {
     "moe_route_permute": [P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P, SZ, P, P],
     "moe_grouped_fc1_glu_quant_fwd": [P, P, P, P, P, P, I, I, I, I, C.POINTER(GluParams), I, C.POINTER(ActOut), I, P, P],
     "moe_grouped_dglu_quant_bwd": [P, P, P, P, P, P, I, I, I, I, C.POINTER(GluParams), I, C.POINTER(ActOut), I, P, P],
-    "moe_quantize_mxfp8": [P, I, I, I, I, P, P, I, P, P, P],
+    "moe_quantize_mxfp8": [P, I, I, I, I, P, P, I, P, P, P, P],
     "moe_grouped_fc2_workspace_size": ([I, I, I, I], SZ),
     "moe_grouped_fc2_fwd": [P, P, P, P, P, P, I, I, I, I, P, P, SZ, I, P, P],
     "moe_grouped_wgrad_workspace_size": ([I, I, I, I], SZ),

@@ -138,7 +138,7 @@ def dglu_bwd(dY_perm, W2, pre, counts, offsets, F: int, params: L.GluParams, out
     return o
 
 
-def quantize_mxfp8(src, col: bool = False, counts=None, offsets=None, out=None):
+def quantize_mxfp8(src, col: bool = False, counts=None, offsets=None, out=None, status=None):
     """src [R, C] or [G, R, C] bf16 -> (q, s); col=True gives the transposed
     column-wise copy."""
     lib = L.load()
@@ -152,8 +152,8 @@ def quantize_mxfp8(src, col: bool = False, counts=None, offsets=None, out=None):
         q = torch.empty(G, R, Cc, dtype=torch.uint8, device=dev) if out is None else out[0]
         s = torch.empty(G, R, Cc // 32, dtype=torch.uint8, device=dev) if out is None else out[1]
     E = 0 if counts is None else counts.shape[0]
-    L.check(lib.moe_quantize_mxfp8(_p(s3), G, R, Cc, int(col), _p(counts), _p(offsets), E, _p(q), _p(s), _s()),
-            "moe_quantize_mxfp8")
+    L.check(lib.moe_quantize_mxfp8(_p(s3), G, R, Cc, int(col), _p(counts), _p(offsets), E, _p(q), _p(s),
+                                   _p(status), _s()), "moe_quantize_mxfp8")
     if src.dim() == 2 and out is None:
         return q[0], s[0]
     return q, s

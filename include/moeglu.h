@@ -179,15 +179,19 @@ MOE_API moe_status_t moe_grouped_dglu_quant_bwd(const moe_bf16* dY_perm, const m
                                         int32_t* status, moe_stream_t stream);
 
 /* MXFP8 quantisation of a bf16 tensor (the standalone quantize/transpose
- * kernel of the unfused path, and the weight cast).  src [G][R][C] bf16.
- * col == 0: q [G][R][C], s [G][R][C/32] (blocks along C).
- * col != 0: q [G][C][R], s [G][C][R/32] (blocks of 32 rows; transposed).
+ * kernel of the unfused path, and the weight cast).  src [G][R][C] bf16,
+ * 16-byte aligned.
+ * col == 0: q [G][R][C], s [G][R][C/32] (blocks along C); C % 32 == 0.
+ * col != 0: q [G][C][R], s [G][C][R/32] (blocks of 32 rows; transposed);
+ *           R % 32 == 0, C % 8 == 0; the tiles are staged by TMA.
  * counts/offsets (G == 1 only, may be NULL): rows of the permuted layout
  * outside [offsets[e], offsets[e]+counts[e]) are treated as zero; results
- * for rows >= offsets[E] are unspecified (their scales are not written). */
+ * for rows >= offsets[E] are unspecified (their scales are not written).
+ * status (nullable): device word that receives MOE_ERR_TIMEOUT if a staged
+ * tile never arrives (the column kernel then stops early). */
 MOE_API moe_status_t moe_quantize_mxfp8(const moe_bf16* src, int G, int R, int C, int col,
                                 const int32_t* counts, const int32_t* offsets, int E,
-                                uint8_t* q, uint8_t* s, moe_stream_t stream);
+                                uint8_t* q, uint8_t* s, int32_t* status, moe_stream_t stream);
 
 /* Bytes of device workspace moe_grouped_fc2_fwd needs (the scales of the
  * visited tiles, rewritten in the order the tensor cores read them). */

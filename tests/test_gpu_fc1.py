@@ -211,6 +211,24 @@ def test_quantize_kernels_bit_exact():
     assert_exact(np_(qc), qcr, "cols q")
 
 
+def test_quantize_kernels_ragged_shapes():
+    """Flat row streaming with a partial last warp task (672 blocks) and column
+    tiles cut by C = 200 (not a multiple of the 64-column tile) and R = 96."""
+    rng = np.random.default_rng(14)
+    src = synth._bf16(rng.standard_normal((1, 96, 224), dtype=np.float32) * 5)
+    q, s = ops.quantize_mxfp8(src.to(DEV), col=False)
+    qr, sr = O.mx_quantize_rows(np_(src))
+    assert_exact(np_(q), qr, "rows q")
+    assert_exact(np_(s), sr, "rows s")
+    src = synth._bf16(rng.standard_normal((2, 96, 200), dtype=np.float32))
+    st = ops.new_status(DEV)
+    qc, sc = ops.quantize_mxfp8(src.to(DEV), col=True, status=st)
+    qcr, scr = O.mx_quantize_rows(np.transpose(np_(src), (0, 2, 1)))
+    assert ops.read_status(st) == 0
+    assert_exact(np_(sc), scr, "cols s")
+    assert_exact(np_(qc), qcr, "cols q")
+
+
 def test_quantize_grouped_rows_masks_pad():
     counts = [5, 0, 40, 64]
     ids = np.concatenate([np.full(c, e) for e, c in enumerate(counts)]).astype(np.int32)
