@@ -311,6 +311,45 @@ def unpermute_combine(y_perm, row_of, topk_prob) -> np.ndarray:
     return out
 
 
+def combine_bwd(dout, y_perm, row_of, topk_prob, R_rows: int) -> tuple[np.ndarray, np.ndarray]:
+    """Gradient of the combine of [MegaMoE] §2.1 (out[t] = sum_j p[t,j] *
+    y_perm[row_of[t*k+j]]) for an upstream gradient dout [T, H]; the chain
+    rule on that sum, written out:
+      dY_perm[row_of[t*k+j]] = p[t,j] * dout[t]          (float64 [R_rows, H];
+                                                          rows no assignment
+                                                          maps to stay 0)
+      dprob[t, j]            = <dout[t], y_perm[row_of[t*k+j]]>  (0 if dropped)
+    """
+    g = np.asarray(dout, dtype=np.float64)
+    y = np.asarray(y_perm, dtype=np.float64)
+    p = np.asarray(topk_prob, dtype=np.float64)
+    T, k = p.shape
+    r = np.asarray(row_of, dtype=np.int64).reshape(T, k)
+    dY = np.zeros((R_rows, g.shape[1]))
+    dprob = np.zeros((T, k))
+    for t in range(T):
+        for j in range(k):
+            row = r[t, j]
+            if row < 0:
+                continue
+            dY[row] = p[t, j] * g[t]
+            dprob[t, j] = float(np.dot(g[t], y[row]))
+    return dY, dprob
+
+
+def permute_bwd(dx_perm, row_of, T: int, k: int) -> np.ndarray:
+    """Gradient of the permute (x_perm[row_of[t*k+j]] = x[t]): every token
+    collects the gradients of the rows it was copied to, summed in j order.
+    float64 [T, H]; 0 for a token with no local assignment."""
+    d = np.asarray(dx_perm, dtype=np.float64)
+    r = np.asarray(row_of, dtype=np.int64).reshape(T, k)
+    dx = np.zeros((T, d.shape[1]))
+    for j in range(k):
+        ok = r[:, j] >= 0
+        dx[ok] += d[r[ok, j]]
+    return dx
+
+
 # ---------------------------------------------------------------------------
 # FC1 weight repack.  [MoE-Fusion], "Optimizing GLU via fused GEMM epilogues"
 # (Fig. 2): the weights are repacked into input and gate columns so one
