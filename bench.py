@@ -65,6 +65,7 @@ def kernel_model(name, w, R, Rp):
         "quant_w2": (0, E * F * H * 2 + E * F * H * (1 + 1 / 32), None),
         "fc2": (2 * R * F * H, E * H * F * (1 + 1 / 32) + R * F * (1 + 1 / 32) + R * H * 2, "fp8"),
         "combine": (0, R * H * 2 + T * H * 2, None),
+        "combine_bwd": (0, T * H * 2 + R * H * 2 + Rp * H * 2 + T * k * 8, None),
         "dglu_quant": (2 * R * H * F, E * F * H * 2 + R * H * 2 + R * N1 * 2 + 2 * R * N1 * (1 + 1 / 32), "bf16"),
         "quant_w1": (0, E * N1 * H * 2 + E * N1 * H * (1 + 1 / 32), None),
         "dx": (2 * R * N1 * H, E * H * N1 * (1 + 1 / 32) + R * N1 * (1 + 1 / 32) + R * H * 2, "fp8"),
@@ -72,6 +73,7 @@ def kernel_model(name, w, R, Rp):
         "quant_dy_col": (0, R * H * 2 + R * H * (1 + 1 / 32), None),
         "wgrad_w1": (2 * R * N1 * H, (N1 + H) * R * (1 + 1 / 32) + E * N1 * H * 2, "fp8"),
         "wgrad_w2": (2 * R * F * H, (F + H) * R * (1 + 1 / 32) + E * F * H * 2, "fp8"),
+        "permute_bwd": (0, R * H * 2 + T * H * 2 + T * k * 4, None),
     }
     return m[name]
 
@@ -149,12 +151,13 @@ def oracle_sample_step(inp, w, E_s, f_s=None):
     W2d = np.stack([O.mx_dequantize(q, s) for q, s in W2q])
     y = O.bf16_round(O.grouped_gemm_rows(O.mx_dequantize(aq, asc), W2d, rt))
     O.unpermute_combine(y, rt.row_of, inp["topk_prob"].numpy())
-    dY = f64(inp["dY"][:Rp])
-    dY[rt.tok_of < 0] = 0
+    dY, _ = O.combine_bwd(f64(inp["dOut"]), y, rt.row_of, inp["topk_prob"].numpy(), Rp)
+    dY = O.bf16_round(dY)
     d = O.dglu_bwd(dY, W2, fo.pre_bf16, rt, prm)
     dq, ds = O.mx_quantize_rows(d)
     W1q = np.stack([O.mx_dequantize(*O.mx_quantize_cols(W1p[e])) for e in range(E_s)])
-    O.grouped_gemm_rows(O.mx_dequantize(dq, ds), W1q, rt)
+    dX = O.bf16_round(O.grouped_gemm_rows(O.mx_dequantize(dq, ds), W1q, rt))
+    O.permute_bwd(dX, rt.row_of, w.T, w.k)
     xqc = O.mx_dequantize(*O.mx_quantize_cols(xp))
     dyqc = O.mx_dequantize(*O.mx_quantize_cols(dY))
     O.grouped_wgrad(O.mx_dequantize(*O.mx_quantize_cols(d)), xqc, rt)
@@ -284,14 +287,14 @@ def main():
     w = synth.scaled(base, expert_begin=shard.shard_expert_begin(rank, base.E, base.n_experts))
     R_cap = w.capped_R(CAPACITY_FACTOR)
     inp = synth.make_inputs(w, seed=0, R_cap=R_cap)
-    host = {k: inp[k].pin_memory() for k in ("x", "topk_idx", "topk_prob", "dY")}
+    host = {k: inp[k].pin_memory() for k in ("x", "topk_idx", "topk_prob", "dOut")}
     g = {k: v.to(dev) for k, v in inp.items() if v is not None}
     params = L.glu_params(w.act)
     layer = MoeLayer(g["W1"], g["W2"], w.T, w.k, R_cap, params, expert_begin=w.expert_begin,
                      sm_margin=args.sm_margin)
-    X, I, P, DY = g["x"], g["topk_idx"], g["topk_prob"], g["dY"]
+    X, I, P, DO = g["x"], g["topk_idx"], g["topk_prob"], g["dOut"]
     for _ in range(args.warmup):
-        layer.step(X, I, P, DY)
+        layer.step(X, I, P, DO)
     torch.cuda.synchronize()
     st = ops.read_status(layer.status)
     if st:
@@ -300,7 +303,7 @@ def main():
     R = int(counts.sum())
     Rp = int(layer.offsets[-1].item())
 
-    graph = layer.capture(X, I, P, DY)
+    graph = layer.capture(X, I, P, DO)
     for _ in range(args.warmup):
         graph.replay()
     torch.cuda.synchronize()
@@ -324,7 +327,7 @@ def main():
     ms_graph = e0.elapsed_time(e1) / args.steps
 
     # -- timed region 2: eager, an event between kernels
-    calls = layer.step_calls(X, I, P, DY)
+    calls = layer.step_calls(X, I, P, DO)
     names = [n for n, _ in calls]
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(args.steps)]
     launches0 = lib.moe_launch_count()
@@ -352,7 +355,7 @@ def main():
         X.copy_(host["x"], non_blocking=True)
         I.copy_(host["topk_idx"], non_blocking=True)
         P.copy_(host["topk_prob"], non_blocking=True)
-        DY.copy_(host["dY"], non_blocking=True)
+        DO.copy_(host["dOut"], non_blocking=True)
         graph.replay()
         out_host.copy_(layer.out, non_blocking=True)
     e1.record()
@@ -370,8 +373,8 @@ def main():
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / n
 
-    by_name = dict(layer.step_calls(X, I, P, DY))
-    ufwd, ubwd = layer.forward_unfused_calls(), layer.backward_unfused_calls(DY)
+    by_name = dict(layer.step_calls(X, I, P, DO))
+    ufwd, ubwd = layer.forward_unfused_calls(), layer.backward_unfused_calls(layer.dY_perm)
     for calls in ([("fc1_glu_quant", by_name["fc1_glu_quant"])], ufwd, [("dglu_quant", by_name["dglu_quant"])], ubwd):
         layer.run(calls)  # warm-up
     na = max(3, min(args.steps, 20))

@@ -16,6 +16,9 @@
 //                   prob_perm
 //   k_permute_gather one warp per permuted row: 16-byte copies of x rows,
 //                   zero fill of pad rows
+//   k_unpermute_combine  weighted sum of each token's rows (the combine), or
+//                   the plain sum (permute backward)
+//   k_combine_bwd   one warp per permuted row: dY_perm and dprob
 #include <mutex>
 
 #include "common.cuh"
@@ -218,7 +221,7 @@ __global__ void __launch_bounds__(256) k_unpermute_combine(const uint4* __restri
     for (int j = 0; j < k; ++j) {
       const int32_t r = __ldg(row_of + (size_t)t * k + j);
       if (r < 0) continue;
-      const float p = __ldg(prob + (size_t)t * k + j);
+      const float p = prob ? __ldg(prob + (size_t)t * k + j) : 1.0f;  // no weights: permute backward
       const uint4 w = __ldg(y + (size_t)r * H8 + v);
       acc[0] = fmaf(p, bf16_lo(w.x), acc[0]);
       acc[1] = fmaf(p, bf16_hi(w.x), acc[1]);
@@ -231,6 +234,60 @@ __global__ void __launch_bounds__(256) k_unpermute_combine(const uint4* __restri
     }
     out[i] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
                         pack_bf16x2(acc[6], acc[7]));
+  }
+}
+
+// Combine backward (the chain rule on the combine above): one warp per
+// permuted row r < offsets[E].  Real row (t = tok_of[r] >= 0):
+//   dY_perm[r] = bf16(prob_perm[r] * dOut[t])
+//   dprob[t*k + j] = <dOut[t], y_perm[r]> for the slot j with row_of = r
+//                    (fp32: each lane adds its 16-byte chunks in order, then
+//                    a butterfly over the warp, so the order is fixed)
+// Pad rows get a zero dY_perm row; slots with row_of < 0 get dprob = 0.
+__global__ void __launch_bounds__(256) k_combine_bwd(const uint4* __restrict__ dout, const uint4* __restrict__ y_perm,
+                                                     const int32_t* __restrict__ row_of,
+                                                     const int32_t* __restrict__ tok_of,
+                                                     const float* __restrict__ prob_perm,
+                                                     const int32_t* __restrict__ offsets, int E, int T, int k,
+                                                     int H8, int R_cap, uint4* __restrict__ dY,
+                                                     float* __restrict__ dprob, int32_t* status) {
+  const size_t nthreads = (size_t)gridDim.x * blockDim.x;
+  const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (size_t i = tid; i < (size_t)T * k; i += nthreads)
+    if (__ldg(row_of + i) < 0) dprob[i] = 0.0f;
+  int R = __ldg(offsets + E);
+  if (R > R_cap) {
+    if (tid == 0) set_status(status, MOE_ERR_CAPACITY);
+    return;
+  }
+  const int lane = threadIdx.x & 31;
+  const size_t nwarps = nthreads >> 5;
+  for (size_t r = tid >> 5; r < (size_t)R; r += nwarps) {
+    const int t = __ldg(tok_of + r);
+    uint4* dst = dY + r * H8;
+    if (t < 0) {
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      for (int v = lane; v < H8; v += 32) dst[v] = z;
+      continue;
+    }
+    const float p = __ldg(prob_perm + r);
+    const uint4* g = dout + (size_t)t * H8;
+    const uint4* y = y_perm + r * H8;
+    float dot = 0.0f;
+    for (int v = lane; v < H8; v += 32) {
+      const uint4 a = __ldg(g + v), b = __ldg(y + v);
+      const float ga[8] = {bf16_lo(a.x), bf16_hi(a.x), bf16_lo(a.y), bf16_hi(a.y),
+                           bf16_lo(a.z), bf16_hi(a.z), bf16_lo(a.w), bf16_hi(a.w)};
+      const float yb[8] = {bf16_lo(b.x), bf16_hi(b.x), bf16_lo(b.y), bf16_hi(b.y),
+                           bf16_lo(b.z), bf16_hi(b.z), bf16_lo(b.w), bf16_hi(b.w)};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dot = fmaf(ga[i], yb[i], dot);
+      dst[v] = make_uint4(pack_bf16x2(p * ga[0], p * ga[1]), pack_bf16x2(p * ga[2], p * ga[3]),
+                          pack_bf16x2(p * ga[4], p * ga[5]), pack_bf16x2(p * ga[6], p * ga[7]));
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, d);
+    if (lane < k && __ldg(row_of + (size_t)t * k + lane) == (int32_t)r) dprob[(size_t)t * k + lane] = dot;
   }
 }
 
@@ -310,6 +367,39 @@ extern "C" moe_status_t moe_unpermute_combine(const moe_bf16* y_perm, const int3
   if (grid > cap) grid = cap;
   k_unpermute_combine<<<grid, 256, 0, as_stream(stream)>>>(reinterpret_cast<const uint4*>(y_perm), row_of,
                                                            topk_prob, T, H / 8, k, reinterpret_cast<uint4*>(out));
+  count_launch();
+  return launch_status();
+}
+
+extern "C" moe_status_t moe_combine_bwd(const moe_bf16* dout, const moe_bf16* y_perm, const int32_t* row_of,
+                                        const int32_t* tok_of, const float* prob_perm, const int32_t* offsets,
+                                        int T, int H, int k, int E, int R_cap, moe_bf16* dY_perm, float* dprob,
+                                        int32_t* status, moe_stream_t stream) {
+  if (!dout || !y_perm || !row_of || !tok_of || !prob_perm || !offsets || !dY_perm || !dprob) return MOE_ERR_ARG;
+  if (T <= 0 || H <= 0 || (H & 7) || k <= 0 || k > 32 || E <= 0 || E > ROUTE_E_MAX || R_cap <= 0) return MOE_ERR_ARG;
+  if (!aligned16(dout) || !aligned16(y_perm) || !aligned16(dY_perm)) return MOE_ERR_ARG;
+  int grid = sm_count() * 8;
+  if (grid < 1) grid = 1;
+  k_combine_bwd<<<grid, 256, 0, as_stream(stream)>>>(reinterpret_cast<const uint4*>(dout),
+                                                     reinterpret_cast<const uint4*>(y_perm), row_of, tok_of,
+                                                     prob_perm, offsets, E, T, k, H / 8, R_cap,
+                                                     reinterpret_cast<uint4*>(dY_perm), dprob, status);
+  count_launch();
+  return launch_status();
+}
+
+extern "C" moe_status_t moe_permute_bwd(const moe_bf16* dx_perm, const int32_t* row_of, int T, int H, int k,
+                                        moe_bf16* dx, int32_t* status, moe_stream_t stream) {
+  (void)status;
+  if (!dx_perm || !row_of || !dx) return MOE_ERR_ARG;
+  if (T <= 0 || H <= 0 || (H & 7) || k <= 0) return MOE_ERR_ARG;
+  if (!aligned16(dx_perm) || !aligned16(dx)) return MOE_ERR_ARG;
+  const size_t items = (size_t)T * (H / 8);
+  int grid = (int)((items + 255) / 256);
+  const int cap = sm_count() * 8;
+  if (grid > cap) grid = cap;
+  k_unpermute_combine<<<grid, 256, 0, as_stream(stream)>>>(reinterpret_cast<const uint4*>(dx_perm), row_of, nullptr,
+                                                           T, H / 8, k, reinterpret_cast<uint4*>(dx));
   count_launch();
   return launch_status();
 }

@@ -4,10 +4,13 @@ the host, so the whole step captures into one CUDA graph.
 
 Forward:  route+permute -> FC1 GroupGemm+Activation+Quantize/Transpose
           -> MXFP8 cast of W2 -> FC2 block-scaled GroupGemm -> unpermute+combine
-Backward: FC2-data-grad GroupGemm+dActivation+Quantize/Transpose (dFC1)
-          -> MXFP8 cast of W1p (transposed) -> dX = dFC1 . W1p
+Backward: (from dOut, the gradient at the layer output)
+          combine backward (dY_perm = p * dOut[tok], dprob = <dOut, y_perm>)
+          -> FC2-data-grad GroupGemm+dActivation+Quantize/Transpose (dFC1)
+          -> MXFP8 cast of W1p (transposed) -> dX_perm = dFC1 . W1p
           -> column-wise MXFP8 of x_perm and dY_perm
           -> weight gradients dW1p = dFC1^T x, dW2 = a^T dY (per expert)
+          -> permute backward (dx[t] = sum of its rows of dX_perm)
 
 Weight layouts: W1 [E][2F][H] (rows: input | gate; repacked once into W1p),
 W2 [E][F][H] (y = a . W2[e]); gradients come out in the same layouts
@@ -69,7 +72,10 @@ class MoeLayer:
         self.d_q, self.d_s = z(R_cap, N1, dt=u8), z(R_cap, N1 // 32, dt=u8)
         self.d_qc, self.d_sc = z(N1, R_cap, dt=u8), z(N1, R_cap // 32, dt=u8)
         self.W1q, self.W1s = z(E, H, N1, dt=u8), z(E, H, N1 // 32, dt=u8)
+        self.dY_perm = z(R_cap, H)
+        self.dprob = z(T, k, dt=torch.float32)
         self.dX_perm = z(R_cap, H)
+        self.dx = z(T, H)
         self.x_qc, self.x_sc = z(H, R_cap, dt=u8), z(H, R_cap // 32, dt=u8)
         self.dy_qc, self.dy_sc = z(H, R_cap, dt=u8), z(H, R_cap // 32, dt=u8)
         self.dW1 = z(E, N1, H)
@@ -109,11 +115,15 @@ class MoeLayer:
                 _p(self.y_perm), _p(self.row_of), _p(topk_prob), T, H, k, _p(self.out), st, s)),
         ]
 
-    def backward_calls(self, dY_perm):
+    def backward_calls(self, dOut):
         lib, s = self.lib, _s()
-        E, N1, H, F, R = self.E, self.N1, self.H, self.F, self.R_cap
+        E, N1, H, F, T, k, R = self.E, self.N1, self.H, self.F, self.T, self.k, self.R_cap
         st = _p(self.status)
+        dY_perm = self.dY_perm
         return [
+            ("combine_bwd", lambda: lib.moe_combine_bwd(
+                _p(dOut), _p(self.y_perm), _p(self.row_of), _p(self.tok_of), _p(self.prob_perm), _p(self.offsets),
+                T, H, k, E, R, _p(dY_perm), _p(self.dprob), st, s)),
             ("dglu_quant", lambda: lib.moe_grouped_dglu_quant_bwd(
                 _p(dY_perm), _p(self.W2), _p(self.pre), None, _p(self.counts), _p(self.offsets), E, H, F, R,
                 C.byref(self.params), L.OUT_MXFP8, C.byref(self.bwd_out), self.sm_margin, st, s)),
@@ -132,6 +142,8 @@ class MoeLayer:
             ("wgrad_w2", lambda: lib.moe_grouped_wgrad(
                 _p(self.a_qc), _p(self.a_sc), _p(self.dy_qc), _p(self.dy_sc), _p(self.counts), _p(self.offsets),
                 E, F, H, R, _p(self.dW2), 0, _p(self.ws_wg2), self.ws_wg2.numel(), self.sm_margin, st, s)),
+            ("permute_bwd", lambda: lib.moe_permute_bwd(
+                _p(self.dX_perm), _p(self.row_of), T, H, k, _p(self.dx), st, s)),
         ]
 
     # ---- unfused path (the ablation baseline): the same tcgen05 GEMM writing
@@ -187,8 +199,8 @@ class MoeLayer:
                                                           _p(u["d_sc"]), st, s)),
         ]
 
-    def step_calls(self, x, topk_idx, topk_prob, dY_perm):
-        return self.forward_calls(x, topk_idx, topk_prob) + self.backward_calls(dY_perm)
+    def step_calls(self, x, topk_idx, topk_prob, dOut):
+        return self.forward_calls(x, topk_idx, topk_prob) + self.backward_calls(dOut)
 
     def run(self, calls, events=None):
         """Issues the calls on the current stream; optional events[i] are
@@ -200,13 +212,13 @@ class MoeLayer:
         if events is not None:
             events[len(calls)].record()
 
-    def step(self, x, topk_idx, topk_prob, dY_perm):
-        self.run(self.step_calls(x, topk_idx, topk_prob, dY_perm))
+    def step(self, x, topk_idx, topk_prob, dOut):
+        self.run(self.step_calls(x, topk_idx, topk_prob, dOut))
 
-    def capture(self, x, topk_idx, topk_prob, dY_perm) -> torch.cuda.CUDAGraph:
+    def capture(self, x, topk_idx, topk_prob, dOut) -> torch.cuda.CUDAGraph:
         """Captures one forward + backward step into a CUDA graph (global
         capture mode: any host synchronisation inside would fail it)."""
-        calls = self.step_calls(x, topk_idx, topk_prob, dY_perm)
+        calls = self.step_calls(x, topk_idx, topk_prob, dOut)
         g = torch.cuda.CUDAGraph()
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
@@ -214,6 +226,6 @@ class MoeLayer:
             self.run(calls)  # warm-up outside capture (sets kernel attributes)
             torch.cuda.synchronize()
             with torch.cuda.graph(g, stream=s, capture_error_mode="global"):
-                self.run(self.step_calls(x, topk_idx, topk_prob, dY_perm))
+                self.run(self.step_calls(x, topk_idx, topk_prob, dOut))
         torch.cuda.current_stream().wait_stream(s)
         return g

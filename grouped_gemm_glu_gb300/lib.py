@@ -50,6 +50,8 @@ _SIGS = {
     "moe_grouped_wgrad_workspace_size": ([I, I, I, I], SZ),
     "moe_grouped_wgrad": [P, P, P, P, P, P, I, I, I, I, P, I, P, SZ, I, P, P],
     "moe_unpermute_combine": [P, P, P, I, I, I, P, P, P],
+    "moe_combine_bwd": [P, P, P, P, P, P, I, I, I, I, I, P, P, P, P],
+    "moe_permute_bwd": [P, P, I, I, I, P, P, P],
     "moe_nvfp4_cast": [P, P, P, P, I, I, I, P, P, P, P],
     "moe_glu_act": [P, P, P, I, I, I, C.POINTER(GluParams), P, P],
     "moe_dglu_act": [P, P, P, P, I, I, I, C.POINTER(GluParams), P, P],

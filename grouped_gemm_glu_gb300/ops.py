@@ -206,6 +206,33 @@ def unpermute_combine(y_perm, row_of, topk_prob, status=None, out=None):
     return o
 
 
+def combine_bwd(dout, y_perm, route: dict, k: int, status=None, out=None):
+    """Gradient of the combine for dout [T, H]: (dY_perm [R_cap, H] bf16,
+    dprob [T, k] f32); route = the dict of route_permute."""
+    lib = L.load()
+    dev = _dev(dout)
+    T, H = dout.shape
+    R_cap = y_perm.shape[0]
+    E = route["counts"].shape[0]
+    dY = out[0] if out is not None else torch.empty(R_cap, H, dtype=torch.bfloat16, device=dev)
+    dprob = out[1] if out is not None else torch.empty(T, k, dtype=torch.float32, device=dev)
+    st = status if status is not None else route.get("status")
+    L.check(lib.moe_combine_bwd(_p(dout), _p(y_perm), _p(route["row_of"]), _p(route["tok_of"]),
+                                _p(route["prob_perm"]), _p(route["offsets"]), T, H, k, E, R_cap, _p(dY),
+                                _p(dprob), _p(st), _s()), "moe_combine_bwd")
+    return dY, dprob
+
+
+def permute_bwd(dx_perm, row_of, T: int, k: int, status=None, out=None):
+    """Gradient of the permute: dx [T, H] bf16 from dx_perm [R_cap, H]."""
+    lib = L.load()
+    dev = _dev(dx_perm)
+    H = dx_perm.shape[1]
+    o = out if out is not None else torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    L.check(lib.moe_permute_bwd(_p(dx_perm), _p(row_of), T, H, k, _p(o), _p(status), _s()), "moe_permute_bwd")
+    return o
+
+
 def nvfp4_cast(y, amax, counts, offsets):
     lib = L.load()
     dev = _dev(y)

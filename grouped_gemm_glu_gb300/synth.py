@@ -154,9 +154,10 @@ def make_inputs(w: Workload, seed: int = 0, R_cap: int | None = None) -> dict:
     x bf16 [T, H]; topk_idx int32 [T, k]; topk_prob f32 [T, k];
     W1 bf16 [E, N1, H] in logical order (rows [0, F) input, [F, 2F) gate);
     b1 bf16 [E, N1] or None; W2 bf16 [E, F, H] (y = a @ W2_e);
-    dY bf16 [R_cap, H] (gradient arriving at the FC2 output, per permuted
-    row; rows that turn out to be padding are ignored by the path)."""
-    ss = np.random.SeedSequence(seed).spawn(6)
+    dY bf16 [R_cap, H] (a gradient at the FC2 output, per permuted row, for
+    calls that start there; rows that turn out to be padding are ignored);
+    dOut bf16 [T, H] (the gradient arriving at the layer output)."""
+    ss = np.random.SeedSequence(seed).spawn(7)
     sd = 1.0 / np.sqrt(w.H)
     out = {}
     out["x"] = _bf16(_normal(ss[0], (w.T, w.H)))
@@ -167,6 +168,7 @@ def make_inputs(w: Workload, seed: int = 0, R_cap: int | None = None) -> dict:
     out["W2"] = _bf16(_normal(ss[3], (w.E, w.F, w.H), sd))
     out["b1"] = _bf16(_normal(ss[4], (w.E, w.N1), 0.02)) if w.bias else None
     out["dY"] = _bf16(_normal(ss[5], (R_cap or w.R_cap, w.H)))
+    out["dOut"] = _bf16(_normal(ss[6], (w.T, w.H)))
     return out
 
 

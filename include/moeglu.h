@@ -238,6 +238,29 @@ MOE_API moe_status_t moe_unpermute_combine(const moe_bf16* y_perm, const int32_t
                                    const float* topk_prob, int T, int H, int k,
                                    moe_bf16* out, int32_t* status, moe_stream_t stream);
 
+/* Combine backward: the chain rule on the combine above ([MegaMoE] §2.1),
+ * for the gradient dout [T][H] bf16 arriving at the layer output.  For every
+ * permuted row r < offsets[E] with t = tok_of[r] >= 0:
+ *   dY_perm[r] = bf16(prob_perm[r] * dout[t])                 [R_cap][H]
+ *   dprob[t*k + j] = <dout[t], y_perm[r]>  (fp32) for the slot with
+ *                    row_of[t*k + j] == r                       [T*k] f32
+ * Pad rows (tok_of < 0) of dY_perm are written as 0, slots with row_of < 0
+ * get dprob 0, rows >= offsets[E] are untouched.  row_of / tok_of /
+ * prob_perm / offsets as written by moe_route_permute.  H % 8 == 0,
+ * 1 <= k <= 32, 16-byte aligned bf16 buffers.  offsets[E] > R_cap records
+ * MOE_ERR_CAPACITY in status and writes nothing else. */
+MOE_API moe_status_t moe_combine_bwd(const moe_bf16* dout, const moe_bf16* y_perm, const int32_t* row_of,
+                             const int32_t* tok_of, const float* prob_perm, const int32_t* offsets,
+                             int T, int H, int k, int E, int R_cap, moe_bf16* dY_perm, float* dprob,
+                             int32_t* status, moe_stream_t stream);
+
+/* Permute backward: dx[t] = bf16( sum_j dx_perm[row_of[t*k+j]] ) over the
+ * slots with row_of >= 0, summed in fp32 in j order (the gradient of the
+ * gather x_perm[row] = x[tok_of[row]]); 0 for a token with no local
+ * assignment.  dx_perm [R_cap][H], dx [T][H] bf16, H % 8 == 0. */
+MOE_API moe_status_t moe_permute_bwd(const moe_bf16* dx_perm, const int32_t* row_of, int T, int H, int k,
+                             moe_bf16* dx, int32_t* status, moe_stream_t stream);
+
 /* NVFP4 cast of the forward's bf16 output ([MoE-Fusion], "Fusing MXFP8 and
  * NVFP4 quantisation": the fused kernel emits BF16 + per-tensor amax).
  * s_g = 2688 / amax (1 if amax == 0) written to *s_global; per 16

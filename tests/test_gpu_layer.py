@@ -29,8 +29,8 @@ def oracle_chain(inp, w):
     W2d = np.stack([O.mx_dequantize(*O.mx_quantize_cols(W2[e])) for e in range(w.E)])
     y = O.bf16_round(O.grouped_gemm_rows(a, W2d, rt))
     out = O.bf16_round(O.unpermute_combine(y, rt.row_of, inp["topk_prob"].numpy()))
-    dY = f64(inp["dY"])[:Rp].copy()
-    dY[rt.tok_of < 0] = 0
+    dY, dprob = O.combine_bwd(f64(inp["dOut"]), y, rt.row_of, inp["topk_prob"].numpy(), Rp)
+    dY = O.bf16_round(dY)
     d = O.dglu_bwd(dY, W2, fo.pre_bf16, rt, prm)
     W1q = np.stack([O.mx_dequantize(*O.mx_quantize_cols(W1p[e])) for e in range(w.E)])
     dX = O.bf16_round(O.grouped_gemm_rows(O.mx_dequantize(*O.mx_quantize_rows(d)), W1q, rt))
@@ -38,7 +38,8 @@ def oracle_chain(inp, w):
                                        O.mx_dequantize(*O.mx_quantize_cols(xp)), rt))
     dW2 = O.bf16_round(O.grouped_wgrad(O.mx_dequantize(*O.mx_quantize_cols(fo.y)),
                                        O.mx_dequantize(*O.mx_quantize_cols(dY)), rt))
-    return rt, out, dX, dW1, dW2
+    dx = O.bf16_round(O.permute_bwd(dX, rt.row_of, w.T, w.k))
+    return rt, out, dX, dW1, dW2, dprob, dx
 
 
 def _layer(w, inp):
@@ -48,11 +49,13 @@ def _layer(w, inp):
 
 
 def _check(layer, inp, w):
-    rt, out, dX, dW1, dW2 = oracle_chain(inp, w)
+    rt, out, dX, dW1, dW2, dprob, dx = oracle_chain(inp, w)
     Rp = rt.R_pad
     assert_chain_close(np_(layer.out), out, "layer output")
     real = rt.tok_of >= 0
+    assert_chain_close(np_(layer.dprob), dprob, "dprob")
     assert_chain_close(np_(layer.dX_perm)[:Rp][real], dX[real], "dX_perm")
+    assert_chain_close(np_(layer.dx), dx, "dx")
     assert_chain_close(np_(layer.dW1), dW1, "dW1 (packed rows)")
     assert_chain_close(np_(layer.dW2), dW2, "dW2")
 
@@ -61,7 +64,7 @@ def test_layer_step_matches_oracle():
     w = synth.WORKLOADS["tiny"]
     inp = synth.make_inputs(w, seed=21)
     layer, g = _layer(w, inp)
-    layer.step(g["x"], g["topk_idx"], g["topk_prob"], g["dY"])
+    layer.step(g["x"], g["topk_idx"], g["topk_prob"], g["dOut"])
     torch.cuda.synchronize()
     assert ops.read_status(layer.status) == 0
     _check(layer, inp, w)
@@ -71,23 +74,23 @@ def test_layer_graph_replay_new_routing():
     w = synth.WORKLOADS["tiny"]
     inp = synth.make_inputs(w, seed=22)
     layer, g = _layer(w, inp)
-    graph = layer.capture(g["x"], g["topk_idx"], g["topk_prob"], g["dY"])
+    graph = layer.capture(g["x"], g["topk_idx"], g["topk_prob"], g["dOut"])
     # new batch: different tokens, routing and counts, copied into the captured buffers
     new = synth.make_inputs(synth.scaled(w), seed=23)
     new["W1"], new["W2"] = inp["W1"], inp["W2"]
-    for k in ("x", "topk_idx", "topk_prob", "dY"):
+    for k in ("x", "topk_idx", "topk_prob", "dOut"):
         g[k].copy_(new[k].to(DEV))
     graph.replay()
     torch.cuda.synchronize()
     assert ops.read_status(layer.status) == 0
-    got = {k: getattr(layer, k).clone() for k in ("out", "dX_perm", "dW1", "dW2", "counts")}
+    got = {k: getattr(layer, k).clone() for k in ("out", "dprob", "dX_perm", "dx", "dW1", "dW2", "counts")}
     assert not torch.equal(got["counts"].cpu(), torch.from_numpy(O.route(inp["topk_idx"].numpy(), 0, w.E)
                                                                  .counts.astype(np.int32)))
     _check(layer, new, w)
     # eager step on the same inputs gives identical bits (deterministic kernels)
-    layer.step(g["x"], g["topk_idx"], g["topk_prob"], g["dY"])
+    layer.step(g["x"], g["topk_idx"], g["topk_prob"], g["dOut"])
     torch.cuda.synchronize()
-    for k in ("out", "dX_perm", "dW1", "dW2"):
+    for k in ("out", "dprob", "dX_perm", "dx", "dW1", "dW2"):
         assert torch.equal(getattr(layer, k), got[k]), k
 
 
@@ -100,7 +103,7 @@ def test_unfused_path_matches_oracle():
     w = synth.WORKLOADS["tiny"]
     inp = synth.make_inputs(w, seed=24)
     layer, g = _layer(w, inp)
-    layer.step(g["x"], g["topk_idx"], g["topk_prob"], g["dY"])
+    layer.step(g["x"], g["topk_idx"], g["topk_prob"], g["dOut"])
     layer.run(layer.forward_unfused_calls())
     layer.run(layer.backward_unfused_calls(g["dY"]))
     torch.cuda.synchronize()

@@ -18,7 +18,7 @@ def test_header_declares_the_hot_path(lib):
     names = L.header_symbols()
     for n in ("moe_route_permute", "moe_grouped_fc1_glu_quant_fwd", "moe_grouped_fc2_fwd",
               "moe_grouped_dglu_quant_bwd", "moe_unpermute_combine", "moe_grouped_wgrad", "moe_quantize_mxfp8",
-              "moe_nvfp4_cast", "moe_repack_fc1"):
+              "moe_nvfp4_cast", "moe_repack_fc1", "moe_combine_bwd", "moe_permute_bwd"):
         assert n in names
 
 
@@ -37,6 +37,9 @@ def test_workspace_size_is_host_only(lib):
 def test_argument_validation_needs_no_device(lib):
     # a null pointer is rejected on the host before anything is launched
     assert lib.moe_unpermute_combine(None, None, None, 1, 8, 1, None, None, None) == L.MOE_ERR_ARG
+    assert lib.moe_combine_bwd(None, None, None, None, None, None, 1, 8, 1, 1, 128, None, None, None,
+                               None) == L.MOE_ERR_ARG
+    assert lib.moe_permute_bwd(None, None, 1, 8, 1, None, None, None) == L.MOE_ERR_ARG
     prm = L.glu_params("swiglu")
     out = L.ActOut()
     assert lib.moe_grouped_fc1_glu_quant_fwd(None, None, None, None, None, None, 4, 256, 512, 1152,
