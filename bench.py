@@ -432,7 +432,10 @@ def main():
     tr = profile_traffic(dom) if w.E == base.E and w.name == WORKLOAD and not args.experts else None
     roof["traffic"] = tr
     roof["kernel"] = dom
-    roof["peak_source"] = f"of {peaks['src']} ({'bf16 sustained' if dt == 'bf16' else 'fp8 = 2 x bf16 sustained' if dt else 'HBM copy'})"
+    if roof["bound"] == "hbm":
+        roof["peak_source"] = f"of {peaks['src']} (HBM copy)"
+    else:
+        roof["peak_source"] = f"of {peaks['src']} ({'bf16 sustained' if dt == 'bf16' else 'fp8 = 2 x bf16 sustained'})"
     roof["algorithmic"] = {"flops": fl, "bytes": by}
 
     fused = {}
