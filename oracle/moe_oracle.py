@@ -586,6 +586,35 @@ def dglu_bwd(dY_perm, W2, pre_bf16, rt: Routing, prm: ActParams, G: int = 32,
     return _zero_pad_rows(d, rt).astype(np.float32)
 
 
+def dglu_row_prob_grad(dY_perm, W2, pre_bf16, rt: Routing, prm: ActParams, G: int = 32) -> np.ndarray:
+    """Gradient of the per-row "feature scaling" factor ([MoE-Fusion],
+    "clamping and scaling"; reading: the router probability p multiplied into
+    the FC1 output, a = p * act(pre)): dL/dp[r] = sum_c da[r, c] * act(pre)[r, c]
+    with da = dY_perm @ W2_e^T, the activation taken on the saved bf16 pre.
+    float64 [R_pad]; pad rows 0."""
+    da = grouped_gemm_rows(dY_perm, W2, rt)
+    pre = np.asarray(pre_bf16, dtype=np.float64)
+    if GATED[prm.act]:
+        u, g = unpack_glu_cols(pre, G)
+        act = act_fwd(u, g, prm)
+    else:
+        act = act_fwd(pre, None, prm)
+    out = np.sum(da * act, axis=1)
+    out[rt.tok_of < 0] = 0.0
+    return out
+
+
+def rows_to_slots(row_values, row_of, T: int, k: int) -> np.ndarray:
+    """[T, k]: the value of the row each (token, slot) was routed to; 0 for
+    dropped slots."""
+    v = np.asarray(row_values, dtype=np.float64)
+    r = np.asarray(row_of, dtype=np.int64).reshape(T, k)
+    out = np.zeros((T, k))
+    ok = r >= 0
+    out[ok] = v[r[ok]]
+    return out
+
+
 def grouped_wgrad(A_col, B_col, rt: Routing) -> np.ndarray:
     """Weight gradient per expert, contraction over that expert's padded row
     segment: D_e = A_col[:, seg_e] @ B_col[:, seg_e]^T.  A_col [M, R_pad],

@@ -176,3 +176,47 @@ def test_wgrad_triple_loop():
             for n in range(H):
                 ref = sum(A[m, r] * B[n, r] for r in range(rt.R_pad) if rt.expert_of_row[r] == e)
                 assert abs(D[e, m, n] - ref) < 1e-12
+
+
+@pytest.mark.parametrize("act", [O.ACT_SWIGLU, O.ACT_GEGLU])
+def test_feature_scaling_gradients_against_finite_differences(act):
+    """Feature scaling: a = p * act(pre) per row, L = sum(dY * (a @ W2_e)).
+    dglu_bwd(row_scale=p) must be dL/dpre and dglu_row_prob_grad must be
+    dL/dp; the forward with row_scale must be p * act(pre); rows_to_slots
+    maps a row value to every (token, slot) routed there."""
+    rng, rt, x, W1, b1, W2, dY, F, G = _toy(act, seed=21)
+    prm = O.ActParams(act)
+    xp = O.permute(x, rt)
+    W1p = O.repack_fc1(W1, G)
+    pre = O.grouped_gemm_rows(xp, W1p, rt)
+    pre[rt.tok_of < 0] = 0
+    p = rng.uniform(0.1, 1.0, size=rt.R_pad)
+    p[rt.tok_of < 0] = 0
+
+    def loss(P, pp):
+        u, g = O.unpack_glu_cols(P, G)
+        y = O.act_fwd(u, g, prm) * pp[:, None]
+        y[rt.tok_of < 0] = 0
+        return float(np.sum(dY * O.grouped_gemm_rows(y, np.transpose(W2, (0, 2, 1)), rt)))
+
+    dp = O.dglu_row_prob_grad(dY, W2, pre, rt, prm, G)
+    d = O.dglu_bwd(dY, W2, pre, rt, prm, G, row_scale=p).astype(np.float64)
+    h = 1e-6
+    for r in np.nonzero(rt.tok_of >= 0)[0]:
+        e = np.zeros_like(p); e[r] = h
+        fd = (loss(pre, p + e) - loss(pre, p - e)) / (2 * h)
+        assert abs(dp[r] - fd) <= 1e-6 * max(1.0, abs(fd)), (r, dp[r], fd)
+    for r in np.nonzero(rt.tok_of >= 0)[0][:3]:
+        for c in range(2 * F):
+            P1, P2 = pre.copy(), pre.copy()
+            P1[r, c] += h
+            P2[r, c] -= h
+            fd = (loss(P1, p) - loss(P2, p)) / (2 * h)
+            assert abs(d[r, c] - fd) <= 1e-4 * max(1.0, abs(fd)), (r, c)
+    assert np.all(dp[rt.tok_of < 0] == 0)
+    fo = O.fc1_glu_fwd(xp, W1p, None, rt, prm, G, row_scale=p)
+    u, g = O.unpack_glu_cols(pre, G)
+    assert np.allclose(fo.y, (O.act_fwd(u, g, prm) * p[:, None]).astype(np.float32), rtol=1e-6, atol=1e-7)
+    slots = O.rows_to_slots(dp, rt.row_of, rt.row_of.size, 1)
+    for i, r in enumerate(rt.row_of):
+        assert slots[i, 0] == (dp[r] if r >= 0 else 0.0)
