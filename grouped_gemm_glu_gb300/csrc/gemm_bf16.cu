@@ -51,7 +51,9 @@ constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
 constexpr int SMEM_BYTES = 1024 + OFF_MISC + 64;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
-enum Mode { FWD_GLU = 0, FWD_ELT = 1, FWD_PRE = 2, BWD_GLU = 3, BWD_ELT = 4 };
+// BWD_*_DOT: the backward modes that also write the feature-scale partials
+// (separate instantiations, so the plain backward carries no extra code)
+enum Mode { FWD_GLU = 0, FWD_ELT = 1, FWD_PRE = 2, BWD_GLU = 3, BWD_ELT = 4, BWD_GLU_DOT = 5, BWD_ELT_DOT = 6 };
 
 struct Args {
   const int32_t* counts;
@@ -69,6 +71,7 @@ struct Args {
   uint16_t* y;
   float* amax;
   uint16_t* pre_out;
+  float* row_dot;          // backward: [R_cap][2 * n_tiles_n] partials of da * act(pre), may be null
   int32_t* status;
   uint64_t wait_ns;
 };
@@ -245,7 +248,9 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& ti, uin
         emit_block(a, yv, c0, row, rb, row_ok, scratch, lane, amax_bits);
       }
     }
-  } else if (MODE == BWD_GLU) {
+  } else if (MODE == BWD_GLU || MODE == BWD_GLU_DOT) {
+    constexpr bool DOT = MODE == BWD_GLU_DOT;
+    float dot = 0.0f;  // this warp half's share of sum_c da * act(pre) (feature-scale gradient)
 #pragma unroll 1
     for (int j = h * (BN / 64); j < (h + 1) * (BN / 64); ++j) {
       const int f0 = ti.n_idx * BN + j * 32;
@@ -256,6 +261,10 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& ti, uin
       if (real) {
         load_bf16x32(a.pre_in + (size_t)row * a.N1 + p0, u);
         load_bf16x32(a.pre_in + (size_t)row * a.N1 + p0 + 32, g);
+        if (DOT) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) dot = fmaf(d[i], act_fwd(a.prm, u[i], g[i]), dot);
+        }
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           float du, dg;
@@ -270,7 +279,10 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& ti, uin
       emit_block(a, u, p0, row, rb, row_ok, scratch, lane, amax_bits);
       emit_block(a, g, p0 + 32, row, rb, row_ok, scratch, lane, amax_bits);
     }
-  } else {  // BWD_ELT
+    if (DOT) a.row_dot[(size_t)row * (2 * a.n_tiles_n) + ti.n_idx * 2 + h] = dot;
+  } else {  // BWD_ELT, BWD_ELT_DOT
+    constexpr bool DOT = MODE == BWD_ELT_DOT;
+    float dot = 0.0f;
 #pragma unroll 1
     for (int j = h * (BN / 64); j < (h + 1) * (BN / 64); ++j) {
       const int f0 = ti.n_idx * BN + j * 32;
@@ -279,6 +291,10 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& ti, uin
       tmem_ld32(tacc + j * 32, d);
       if (real) {
         load_bf16x32(a.pre_in + (size_t)row * a.N1 + f0, x);
+        if (DOT) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) dot = fmaf(d[i], act_fwd(a.prm, x[i], 0.0f), dot);
+        }
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           float du, dg;
@@ -291,6 +307,7 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& ti, uin
       }
       emit_block(a, x, f0, row, rb, row_ok, scratch, lane, amax_bits);
     }
+    if (DOT) a.row_dot[(size_t)row * (2 * a.n_tiles_n) + ti.n_idx * 2 + h] = dot;
   }
 }
 
@@ -889,8 +906,46 @@ extern "C" moe_status_t moe_grouped_dglu_quant_bwd(const moe_bf16* dY_perm, cons
   a.q_col = dfc1->q_col;
   a.s_col = dfc1->s_col;
   a.y = reinterpret_cast<uint16_t*>(dfc1->y);
+  a.row_dot = dfc1->row_dot;
   a.status = status;
   a.wait_ns = g_wait_limit_ns.load();
+  if (a.row_dot != nullptr) {
+    if (gated) return launch<BWD_GLU_DOT>(dY_perm, W2, a, sm_margin, as_stream(stream));
+    return launch<BWD_ELT_DOT>(dY_perm, W2, a, sm_margin, as_stream(stream));
+  }
   if (gated) return launch<BWD_GLU>(dY_perm, W2, a, sm_margin, as_stream(stream));
   return launch<BWD_ELT>(dY_perm, W2, a, sm_margin, as_stream(stream));
+}
+
+extern "C" int moe_dglu_row_dot_parts(int F) { return F > 0 ? 2 * ((F + g16::BN - 1) / g16::BN) : 0; }
+
+namespace moeglu {
+// One thread per routed slot: the row's partials added in slot order.
+__global__ void __launch_bounds__(256) k_feature_scale_grad(const float* __restrict__ row_dot, int parts,
+                                                            const int32_t* __restrict__ row_of, int n,
+                                                            float* __restrict__ dprob) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    const int r = __ldg(row_of + i);
+    float s = 0.0f;
+    if (r >= 0) {
+      const float* p = row_dot + (size_t)r * parts;
+      for (int q = 0; q < parts; ++q) s += __ldg(p + q);
+    }
+    dprob[i] = s;
+  }
+}
+}  // namespace moeglu
+
+extern "C" moe_status_t moe_feature_scale_grad(const float* row_dot, int parts, const int32_t* row_of, int T, int k,
+                                               float* dprob, moe_stream_t stream) {
+  if (!row_dot || !row_of || !dprob || parts <= 0 || T <= 0 || k <= 0) return MOE_ERR_ARG;
+  const long long n = (long long)T * k;
+  if (n > (1ll << 31) - 1) return MOE_ERR_ARG;
+  long long grid = (n + 255) / 256;
+  const long long cap = (long long)sm_count() * 8;
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  k_feature_scale_grad<<<(int)grid, 256, 0, as_stream(stream)>>>(row_dot, parts, row_of, (int)n, dprob);
+  count_launch();
+  return launch_status();
 }

@@ -27,7 +27,7 @@ class GluParams(C.Structure):
 
 class ActOut(C.Structure):
     _fields_ = [("q_row", C.c_void_p), ("s_row", C.c_void_p), ("q_col", C.c_void_p), ("s_col", C.c_void_p),
-                ("y", C.c_void_p), ("amax", C.c_void_p), ("pre", C.c_void_p)]
+                ("y", C.c_void_p), ("amax", C.c_void_p), ("pre", C.c_void_p), ("row_dot", C.c_void_p)]
 
 
 def glu_params(act: str = "swiglu", alpha: float = 1.0, up_offset: float = 0.0,
@@ -52,6 +52,8 @@ _SIGS = {
     "moe_unpermute_combine": [P, P, P, I, I, I, P, P, P],
     "moe_combine_bwd": [P, P, P, P, P, P, I, I, I, I, I, P, P, P, P],
     "moe_permute_bwd": [P, P, I, I, I, P, P, P],
+    "moe_dglu_row_dot_parts": ([I], I),
+    "moe_feature_scale_grad": [P, I, P, I, I, P, P],
     "moe_nvfp4_cast": [P, P, P, P, I, I, I, P, P, P, P],
     "moe_glu_act": [P, P, P, I, I, I, C.POINTER(GluParams), P, P],
     "moe_dglu_act": [P, P, P, P, I, I, I, C.POINTER(GluParams), P, P],

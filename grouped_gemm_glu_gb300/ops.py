@@ -112,8 +112,10 @@ def fc1_fwd(x_perm, W1p, counts, offsets, F: int, params: L.GluParams, out_mode:
 
 def dglu_bwd(dY_perm, W2, pre, counts, offsets, F: int, params: L.GluParams, out_mode: int = L.OUT_MXFP8,
              row_scale=None, with_col: bool = True, sm_margin: int = 0, status=None,
-             out: dict | None = None) -> dict:
-    """GroupGemm + dActivation + Quantize/Transpose.  dFC1 in packed order."""
+             out: dict | None = None, row_dot: bool = False) -> dict:
+    """GroupGemm + dActivation + Quantize/Transpose.  dFC1 in packed order;
+    row_dot=True also returns o["row_dot"], the per-row partials of the
+    feature-scale gradient (reduce with feature_scale_grad)."""
     lib = L.load()
     dev = _dev(dY_perm)
     R_cap, H = dY_perm.shape
@@ -128,8 +130,11 @@ def dglu_bwd(dY_perm, W2, pre, counts, offsets, F: int, params: L.GluParams, out
             o.setdefault("s_col", torch.empty(N1, R_cap // 32, dtype=torch.uint8, device=dev))
     else:
         o.setdefault("y", torch.empty(R_cap, N1, dtype=torch.bfloat16, device=dev))
+    if row_dot:
+        o.setdefault("row_dot", torch.empty(R_cap, lib.moe_dglu_row_dot_parts(F), dtype=torch.float32, device=dev))
     st = status if status is not None else new_status(dev)
     ao = _act_out(o.get("q_row"), o.get("s_row"), o.get("q_col"), o.get("s_col"), o.get("y"))
+    ao.row_dot = o["row_dot"].data_ptr() if "row_dot" in o else None
     L.check(lib.moe_grouped_dglu_quant_bwd(_p(dY_perm), _p(W2), _p(pre), _p(row_scale), _p(counts), _p(offsets),
                                            E, H, F, R_cap, C.byref(params), out_mode, C.byref(ao), sm_margin,
                                            _p(st), _s()),
@@ -221,6 +226,15 @@ def combine_bwd(dout, y_perm, route: dict, k: int, status=None, out=None):
                                 _p(route["prob_perm"]), _p(route["offsets"]), T, H, k, E, R_cap, _p(dY),
                                 _p(dprob), _p(st), _s()), "moe_combine_bwd")
     return dY, dprob
+
+
+def feature_scale_grad(row_dot, row_of, T: int, k: int, out=None):
+    """dprob [T, k] f32 from the dGLU epilogue's per-row partials."""
+    lib = L.load()
+    o = out if out is not None else torch.empty(T, k, dtype=torch.float32, device=row_dot.device)
+    L.check(lib.moe_feature_scale_grad(_p(row_dot), row_dot.shape[1], _p(row_of), T, k, _p(o), _s()),
+            "moe_feature_scale_grad")
+    return o
 
 
 def permute_bwd(dx_perm, row_of, T: int, k: int, status=None, out=None):

@@ -115,6 +115,9 @@ typedef struct {
   moe_bf16* y;       /* bf16 output   [R_cap][N]      (BF16 / NVFP4 modes) */
   float* amax;       /* one float: max |y| over all real rows (NVFP4 mode); caller zeroes it */
   moe_bf16* pre;     /* forward only: saved pre-activation [R_cap][N1] (bias added), for the backward */
+  float* row_dot;    /* backward only, may be NULL: per-row partial sums of da * act(pre) (the
+                      * gradient of a per-row feature scale), [R_cap][moe_dglu_row_dot_parts(F)]
+                      * f32; reduce them with moe_feature_scale_grad */
 } moe_act_out_t;
 
 /* ---------------------------------------------------------------------- */
@@ -169,7 +172,12 @@ MOE_API moe_status_t moe_grouped_fc1_glu_quant_fwd(const moe_bf16* x_perm, const
  * da = dY_perm[rows of e] . W2[e]^T with W2 [E][F][H] (the forward is
  * y = a . W2[e]); (du, dg) from the saved bf16 pre [R_cap][N1]; times
  * row_scale when non-NULL; written as dFC1 [R_cap][N1] in packed column
- * order per out_mode (MXFP8 row + column-wise, or bf16).  H % 64 == 0. */
+ * order per out_mode (MXFP8 row + column-wise, or bf16).  When
+ * dfc1->row_dot is non-NULL the epilogue also writes, for every row of the
+ * padded segments, partial sums of da * act(pre) over disjoint column
+ * ranges (fp32, each slot written once: deterministic), the ingredients of
+ * the feature-scale gradient ([MoE-Fusion] "clamping and scaling").
+ * H % 64 == 0. */
 MOE_API moe_status_t moe_grouped_dglu_quant_bwd(const moe_bf16* dY_perm, const moe_bf16* W2,
                                         const moe_bf16* pre, const float* row_scale,
                                         const int32_t* counts, const int32_t* offsets,
@@ -233,10 +241,22 @@ MOE_API moe_status_t moe_grouped_wgrad(const uint8_t* Aq, const uint8_t* As,
 
 /* Unpermute + combine ([MegaMoE] §2.1: y = sum_{i in topk} p_i E_i(x)).
  * out[t] = bf16( sum_j topk_prob[t][j] * y_perm[row_of[t*k+j]] ) over
- * j with row_of >= 0, summed in fp32 in j order; 0 when none is local. */
+ * j with row_of >= 0, summed in fp32 in j order; 0 when none is local.
+ * H % 8 == 0. */
 MOE_API moe_status_t moe_unpermute_combine(const moe_bf16* y_perm, const int32_t* row_of,
                                    const float* topk_prob, int T, int H, int k,
                                    moe_bf16* out, int32_t* status, moe_stream_t stream);
+
+/* Number of partial-sum slots per row that moe_grouped_dglu_quant_bwd writes
+ * to dfc1->row_dot for FFN width F (host arithmetic). */
+MOE_API int moe_dglu_row_dot_parts(int F);
+
+/* Feature-scale gradient per routed slot: dprob[t*k+j] = sum of the `parts`
+ * partials of row row_of[t*k+j] in row_dot (added in slot order, fp32;
+ * 0 for row_of < 0).  With a = p * act(pre) in the forward (row_scale =
+ * prob_perm), this is dL/dp for the slot's router probability. */
+MOE_API moe_status_t moe_feature_scale_grad(const float* row_dot, int parts, const int32_t* row_of,
+                                    int T, int k, float* dprob, moe_stream_t stream);
 
 /* Combine backward: the chain rule on the combine above ([MegaMoE] §2.1),
  * for the gradient dout [T][H] bf16 arriving at the layer output.  For every
