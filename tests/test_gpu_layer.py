@@ -134,3 +134,17 @@ def test_unfused_path_matches_oracle():
     assert_bf16_close(np_(u["d"])[:R], db, "unfused dFC1")
     q, s_ = O.mx_quantize_rows(db)
     assert_mx_close(np_(u["d_q"])[:R], np_(u["d_s"])[:R], q, s_, db, "unfused dFC1 rows", rel_band=band)
+
+
+def test_dense_mode_single_expert():
+    """Dense MLP / shared expert: one local expert that every token uses
+    (E = 1, top-1), through the same layer step and kernels."""
+    w = synth.Workload("dense", 640, 256, 1, 1, 1, 512, "swiglu", "mxfp8", "normal")
+    inp = synth.make_inputs(w, seed=25)
+    assert int((inp["topk_idx"] == 0).sum()) == w.T
+    layer, g = _layer(w, inp)
+    layer.step(g["x"], g["topk_idx"], g["topk_prob"], g["dOut"])
+    torch.cuda.synchronize()
+    assert ops.read_status(layer.status) == 0
+    assert int(layer.counts[0]) == w.T
+    _check(layer, inp, w)
