@@ -17,12 +17,15 @@
 //   k_grouped_mx  persistent GEMM, 10 warps, one CTA per SM, 128 x 256 tiles:
 //     warps 0-7  epilogue: warp w reads TMEM lane quarter w % 4 and columns
 //                128 * (w / 4) .. +128 with one wait, releases the
-//                accumulator, then stages 8 rows at a time in shared memory
-//                and stores full 128-byte lines (bf16 / fp32)
+//                accumulator, then either stages 8 rows at a time in shared
+//                memory and stores full 128-byte lines (FC2, dX), or (weight
+//                gradients) stages its whole 32 x 128 block in the 128-byte
+//                swizzled layout and writes it with two TMA stores that
+//                stream while the next tile computes (bf16 / fp32)
 //     warp  8    TMA producer: A (128 x 128 bytes) and B (256 x 128 bytes)
 //                tiles with the 128-byte swizzle, and the scale blocks (512 +
 //                1024 bytes, 1-D bulk copies), all completing on the stage's
-//                mbarrier; 4 stages
+//                mbarrier; 4 stages (3 for the weight gradients)
 //     warp  9    TMEM owner + MMA issuer: tcgen05.cp of the scale blocks into
 //                tensor memory, then 4 MMAs of K = 32 (M = 128, N = 256)
 //                selecting scale byte k of each 32-bit column
@@ -35,7 +38,7 @@
 namespace moeglu {
 namespace gmx {
 
-constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
+constexpr int BM = 128, BN = 256, BK = 128;
 constexpr int EPI_WARPS = 8;
 constexpr int PRODUCER_WARP = 8, MMA_WARP = 9;
 constexpr int THREADS = 10 * 32;
@@ -51,15 +54,27 @@ constexpr uint32_t SFA_COL = BN, SFB_COL = BN + 4;
 constexpr int E_MAX = 1024;
 constexpr int EPI_ROW_BYTES = 256 + 16;   // staged output row (64 words + pad)
 constexpr int EPI_ROWS = 8;               // rows staged per pass
-constexpr int EPI_WARP_BYTES = EPI_ROWS * EPI_ROW_BYTES;
-constexpr int OFF_SF = STAGES * STAGE_BYTES;
-constexpr int OFF_EPI = OFF_SF + STAGES * SF_STAGE;
-constexpr int OFF_PREF = OFF_EPI + EPI_WARPS * EPI_WARP_BYTES;
-constexpr int OFF_BARS = OFF_PREF + (E_MAX + 2) * 4;
-constexpr int NUM_BARS = 2 * STAGES + 5;
-constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
-constexpr int SMEM_BYTES = 1024 + OFF_MISC + 64;
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+constexpr int TS_SUB = 32 * 128;          // TMA-store staging: one 32-row x 128-byte swizzled sub-tile
+
+// Shared-memory layout of the two instantiations.  TS = false (FC2, dX): 4
+// stages, 8-row staged line stores.  TS = true (weight gradients, whose K per
+// tile is one expert's rows and whose output tile is the bulk of the
+// traffic): 3 stages and a whole 32 x 128-column block per epilogue warp
+// staged for two asynchronous TMA stores, so the stores stream while the
+// next tile's MMAs run.
+template <bool TS>
+struct Lay {
+  static constexpr int STAGES = TS ? 3 : 4;
+  static constexpr int EPI_WARP_BYTES = TS ? 2 * TS_SUB : EPI_ROWS * EPI_ROW_BYTES;
+  static constexpr int OFF_SF = STAGES * STAGE_BYTES;
+  static constexpr int OFF_EPI = (OFF_SF + STAGES * SF_STAGE + 1023) / 1024 * 1024;
+  static constexpr int OFF_PREF = OFF_EPI + EPI_WARPS * EPI_WARP_BYTES;
+  static constexpr int OFF_BARS = OFF_PREF + (E_MAX + 2) * 4;
+  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  static constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = 1024 + OFF_MISC + 64;
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
 
 struct Args {
   const int32_t* counts;
@@ -310,11 +325,52 @@ __device__ __forceinline__ void store_pass(const Args& a, const Tile& ti, const 
   }
 }
 
+// Weight-gradient epilogue pass: this warp's 32 rows x 128 bf16 columns (or
+// 64 fp32 columns starting at P) as two 32 x 128-byte sub-tiles in the
+// 128-byte swizzled layout (16-byte chunk c of row r at chunk c ^ (r % 8):
+// the lanes of a quarter-warp hit distinct banks), then two TMA stores of
+// D[e] issued by lane 0.  The buffer is reused only after the previous
+// stores have read it.  M % 128 == 0 and N % 128 == 0 keep every box inside
+// D[e].
+template <bool F32, int P>
+__device__ __forceinline__ void store_pass_tma(const CUtensorMap* tmO, const Tile& ti, const float* v, uint8_t* stg,
+                                               int q, int h, int lane) {
+  if (lane == 0) bulk_wait_read_all();
+  __syncwarp();
+  const int sw = lane & 7;
+#pragma unroll
+  for (int w = 0; w < 16; ++w) {
+    uint4* d = reinterpret_cast<uint4*>(stg + (w >> 3) * TS_SUB + lane * 128 + (((w & 7) ^ sw) << 4));
+    if (F32)
+      *d = make_uint4(__float_as_uint(v[P + 4 * w]), __float_as_uint(v[P + 4 * w + 1]),
+                      __float_as_uint(v[P + 4 * w + 2]), __float_as_uint(v[P + 4 * w + 3]));
+    else
+      *d = make_uint4(pack_bf16x2(v[8 * w], v[8 * w + 1]), pack_bf16x2(v[8 * w + 2], v[8 * w + 3]),
+                      pack_bf16x2(v[8 * w + 4], v[8 * w + 5]), pack_bf16x2(v[8 * w + 6], v[8 * w + 7]));
+  }
+  fence_async_shared();
+  __syncwarp();
+  if (lane == 0) {
+    constexpr int SUB_COLS = F32 ? 32 : 64;
+    const int col0 = ti.n0 + h * 128 + P;
+    const int row = ti.m0 + q * 32;
+    tma_store_3d(tmO, stg, col0, row, ti.e);
+    tma_store_3d(tmO, stg + TS_SUB, col0 + SUB_COLS, row, ti.e);
+    bulk_commit();
+  }
+}
+
 // ---------------------------------------------------------------------------
 // The GEMM
 // ---------------------------------------------------------------------------
+template <bool TS>
 __global__ void __launch_bounds__(THREADS, 1)
-    k_grouped_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Args a) {
+    k_grouped_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const __grid_constant__ CUtensorMap tmO, const Args a) {
+  using L = Lay<TS>;
+  constexpr int STAGES = L::STAGES;
+  constexpr int OFF_SF = L::OFF_SF, OFF_EPI = L::OFF_EPI, OFF_PREF = L::OFF_PREF, OFF_BARS = L::OFF_BARS,
+                OFF_MISC = L::OFF_MISC, EPI_WARP_BYTES = L::EPI_WARP_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* tiles = smem;
@@ -348,6 +404,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     fence_async_shared();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (TS) tma_prefetch_desc(&tmO);
   }
   if (warp == MMA_WARP) {
     tmem_alloc(tmem_slot, TMEM_COLS);
@@ -478,13 +535,21 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 128; ++i) v[i] = 0.0f;
       }
-      if (out_es == 4) {
+      if (TS) {
+        if (out_es == 4) {
+          store_pass_tma<true, 0>(&tmO, ti, v, stg, q, h, lane);
+          store_pass_tma<true, 64>(&tmO, ti, v, stg, q, h, lane);
+        } else {
+          store_pass_tma<false, 0>(&tmO, ti, v, stg, q, h, lane);
+        }
+      } else if (out_es == 4) {
         store_pass<true, 0>(a, ti, v, stg, q, h, lane);
         store_pass<true, 64>(a, ti, v, stg, q, h, lane);
       } else {
         store_pass<false, 0>(a, ti, v, stg, q, h, lane);
       }
     }
+    if (TS && lane == 0) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
@@ -494,9 +559,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-static moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const Args& a, long long tiles_bound,
-                           long long sf_items, int sm_margin, cudaStream_t stream) {
-  if (!set_smem_limit((const void*)k_grouped_mx, SMEM_BYTES)) return MOE_ERR_CUDA;
+static moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap* tmO, const Args& a,
+                           long long tiles_bound, long long sf_items, int sm_margin, cudaStream_t stream) {
+  const bool ts = tmO != nullptr;
+  const void* kfn = ts ? (const void*)k_grouped_mx<true> : (const void*)k_grouped_mx<false>;
+  const int smem = ts ? Lay<true>::SMEM_BYTES : Lay<false>::SMEM_BYTES;
+  if (!set_smem_limit(kfn, smem)) return MOE_ERR_CUDA;
   const int sms = sm_count();
   long long sgrid = (sf_items + 7) / 8;
   if (sgrid > (long long)sms * 8) sgrid = (long long)sms * 8;
@@ -505,7 +573,10 @@ static moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const
   int grid = sms - sm_margin;
   if (grid > tiles_bound) grid = (int)tiles_bound;
   if (grid < 1) grid = 1;
-  k_grouped_mx<<<grid, THREADS, SMEM_BYTES, stream>>>(tmA, tmB, a);
+  if (ts)
+    k_grouped_mx<true><<<grid, THREADS, smem, stream>>>(tmA, tmB, *tmO, a);
+  else
+    k_grouped_mx<false><<<grid, THREADS, smem, stream>>>(tmA, tmB, tmA, a);
   count_launch(2);
   return launch_status();
 }
@@ -598,7 +669,7 @@ extern "C" moe_status_t moe_grouped_fc2_fwd(const uint8_t* Aq, const uint8_t* As
   const long long mt_bound = (long long)R_cap / BM + E;
   const long long bound = mt_bound * a.n_tiles_n;
   const long long sf_items = mt_bound * a.KB + (long long)E * 2 * a.n_tiles_n * a.KB;
-  return launch(tmA, tmB, a, bound, sf_items, sm_margin, as_stream(stream));
+  return launch(tmA, tmB, nullptr, a, bound, sf_items, sm_margin, as_stream(stream));
 }
 
 extern "C" moe_status_t moe_grouped_wgrad(const uint8_t* Aq, const uint8_t* As, const uint8_t* Bq, const uint8_t* Bs,
@@ -651,7 +722,17 @@ extern "C" moe_status_t moe_grouped_wgrad(const uint8_t* Aq, const uint8_t* As, 
   a.out_f32 = out_f32 ? 1 : 0;
   a.status = status;
   a.wait_ns = g_wait_limit_ns.load();
+  CUtensorMap tmO;
+  {
+    const uint64_t es = out_f32 ? 4 : 2;
+    const uint64_t dims[3] = {(uint64_t)N, (uint64_t)M, (uint64_t)E};
+    const uint64_t strides[2] = {(uint64_t)N * es, (uint64_t)M * N * es};
+    const uint32_t box[3] = {out_f32 ? 32u : 64u, 32, 1};
+    if (!encode_tmap(&tmO, out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, D, dims,
+                     strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return MOE_ERR_CUDA;
+  }
   const long long bound = (long long)E * (M / BM) * a.n_tiles_n;
   const long long sf_items = (long long)(M / BM + 2 * a.n_tiles_n) * a.KG;
-  return launch(tmA, tmB, a, bound, sf_items, sm_margin, as_stream(stream));
+  return launch(tmA, tmB, &tmO, a, bound, sf_items, sm_margin, as_stream(stream));
 }
