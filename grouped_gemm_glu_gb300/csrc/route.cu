@@ -16,8 +16,9 @@
 //                   prob_perm
 //   k_permute_gather one warp per permuted row: 16-byte copies of x rows,
 //                   zero fill of pad rows
-//   k_unpermute_combine  weighted sum of each token's rows (the combine), or
-//                   the plain sum (permute backward)
+//   k_unpermute_combine(_vec)  weighted sum of each token's rows (the combine),
+//                   or the plain sum (permute backward); vector index loads
+//                   for k = 4, 8
 //   k_combine_bwd   one warp per permuted row: dY_perm and dprob
 #include <mutex>
 
@@ -237,6 +238,54 @@ __global__ void __launch_bounds__(256) k_unpermute_combine(const uint4* __restri
   }
 }
 
+// The same sum for k = 4 or 8 (one thread per (token, 16-byte chunk)): the
+// token's row indices and weights arrive as 16-byte vector loads instead of
+// one load per slot, and all k row loads are issued before the adds (same
+// arithmetic and order as above).
+template <int KV>
+__global__ void __launch_bounds__(256) k_unpermute_combine_vec(const uint4* __restrict__ y,
+                                                               const int32_t* __restrict__ row_of,
+                                                               const float* __restrict__ prob, int T, int H8,
+                                                               uint4* __restrict__ out) {
+  const size_t total = (size_t)T * H8;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / H8);
+    const int v = (int)(i - (size_t)t * H8);
+    int rj[KV];
+    float pj[KV];
+#pragma unroll
+    for (int q = 0; q < KV / 4; ++q) {
+      const int4 r4 = __ldg(reinterpret_cast<const int4*>(row_of + (size_t)t * KV) + q);
+      rj[4 * q] = r4.x, rj[4 * q + 1] = r4.y, rj[4 * q + 2] = r4.z, rj[4 * q + 3] = r4.w;
+      if (prob) {
+        const float4 p4 = __ldg(reinterpret_cast<const float4*>(prob + (size_t)t * KV) + q);
+        pj[4 * q] = p4.x, pj[4 * q + 1] = p4.y, pj[4 * q + 2] = p4.z, pj[4 * q + 3] = p4.w;
+      } else {
+        pj[4 * q] = pj[4 * q + 1] = pj[4 * q + 2] = pj[4 * q + 3] = 1.0f;  // permute backward
+      }
+    }
+    uint4 w[KV];
+#pragma unroll
+    for (int j = 0; j < KV; ++j) w[j] = rj[j] >= 0 ? __ldg(y + (size_t)rj[j] * H8 + v) : make_uint4(0, 0, 0, 0);
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+    for (int j = 0; j < KV; ++j) {
+      if (rj[j] < 0) continue;
+      const float p = pj[j];
+      acc[0] = fmaf(p, bf16_lo(w[j].x), acc[0]);
+      acc[1] = fmaf(p, bf16_hi(w[j].x), acc[1]);
+      acc[2] = fmaf(p, bf16_lo(w[j].y), acc[2]);
+      acc[3] = fmaf(p, bf16_hi(w[j].y), acc[3]);
+      acc[4] = fmaf(p, bf16_lo(w[j].z), acc[4]);
+      acc[5] = fmaf(p, bf16_hi(w[j].z), acc[5]);
+      acc[6] = fmaf(p, bf16_lo(w[j].w), acc[6]);
+      acc[7] = fmaf(p, bf16_hi(w[j].w), acc[7]);
+    }
+    out[i] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                        pack_bf16x2(acc[6], acc[7]));
+  }
+}
+
 // Combine backward (the chain rule on the combine above): one warp per
 // permuted row r < offsets[E].  Real row (t = tok_of[r] >= 0):
 //   dY_perm[r] = bf16(prob_perm[r] * dOut[t])
@@ -354,6 +403,23 @@ extern "C" moe_status_t moe_route_permute(const moe_bf16* x, const int32_t* topk
   return launch_status();
 }
 
+static void launch_combine(const uint4* y, const int32_t* row_of, const float* prob, int T, int H8, int k, uint4* out,
+                           cudaStream_t st) {
+  const size_t items = (size_t)T * H8;
+  size_t grid = (items + 255) / 256;
+  const size_t cap = (size_t)sm_count() * 8;
+  if (grid > cap) grid = cap;
+  // the vector loads of row_of / prob need 16-byte alignment (k = 4 or 8)
+  const bool vec_ok = (reinterpret_cast<uintptr_t>(row_of) & 15) == 0 &&
+                      (prob == nullptr || (reinterpret_cast<uintptr_t>(prob) & 15) == 0);
+  if (k == 8 && vec_ok)
+    k_unpermute_combine_vec<8><<<(int)grid, 256, 0, st>>>(y, row_of, prob, T, H8, out);
+  else if (k == 4 && vec_ok)
+    k_unpermute_combine_vec<4><<<(int)grid, 256, 0, st>>>(y, row_of, prob, T, H8, out);
+  else
+    k_unpermute_combine<<<(int)grid, 256, 0, st>>>(y, row_of, prob, T, H8, k, out);
+}
+
 extern "C" moe_status_t moe_unpermute_combine(const moe_bf16* y_perm, const int32_t* row_of, const float* topk_prob,
                                               int T, int H, int k, moe_bf16* out, int32_t* status,
                                               moe_stream_t stream) {
@@ -361,12 +427,8 @@ extern "C" moe_status_t moe_unpermute_combine(const moe_bf16* y_perm, const int3
   if (!y_perm || !row_of || !topk_prob || !out) return MOE_ERR_ARG;
   if (T <= 0 || H <= 0 || (H & 7) || k <= 0) return MOE_ERR_ARG;
   if (!aligned16(y_perm) || !aligned16(out)) return MOE_ERR_ARG;
-  const size_t items = (size_t)T * (H / 8);
-  int grid = (int)((items + 255) / 256);
-  const int cap = sm_count() * 8;
-  if (grid > cap) grid = cap;
-  k_unpermute_combine<<<grid, 256, 0, as_stream(stream)>>>(reinterpret_cast<const uint4*>(y_perm), row_of,
-                                                           topk_prob, T, H / 8, k, reinterpret_cast<uint4*>(out));
+  launch_combine(reinterpret_cast<const uint4*>(y_perm), row_of, topk_prob, T, H / 8, k,
+                 reinterpret_cast<uint4*>(out), as_stream(stream));
   count_launch();
   return launch_status();
 }
@@ -394,12 +456,8 @@ extern "C" moe_status_t moe_permute_bwd(const moe_bf16* dx_perm, const int32_t* 
   if (!dx_perm || !row_of || !dx) return MOE_ERR_ARG;
   if (T <= 0 || H <= 0 || (H & 7) || k <= 0) return MOE_ERR_ARG;
   if (!aligned16(dx_perm) || !aligned16(dx)) return MOE_ERR_ARG;
-  const size_t items = (size_t)T * (H / 8);
-  int grid = (int)((items + 255) / 256);
-  const int cap = sm_count() * 8;
-  if (grid > cap) grid = cap;
-  k_unpermute_combine<<<grid, 256, 0, as_stream(stream)>>>(reinterpret_cast<const uint4*>(dx_perm), row_of, nullptr,
-                                                           T, H / 8, k, reinterpret_cast<uint4*>(dx));
+  launch_combine(reinterpret_cast<const uint4*>(dx_perm), row_of, nullptr, T, H / 8, k, reinterpret_cast<uint4*>(dx),
+                 as_stream(stream));
   count_launch();
   return launch_status();
 }
