@@ -89,6 +89,16 @@ def test_dglu_tiny_full(out_mode):
     _dglu_case(synth.WORKLOADS["tiny"], out_mode=out_mode)
 
 
+def test_dglu_single_cta_kernel():
+    """The single-CTA variant of the bf16 GEMM (CTA pairs switched off)."""
+    lib = L.load()
+    lib.moe_set_cta_pairs(0)
+    try:
+        _dglu_case(synth.WORKLOADS["tiny"], out_mode=L.OUT_MXFP8)
+    finally:
+        lib.moe_set_cta_pairs(1)
+
+
 def test_dglu_edge_counts():
     counts = [0, 1, 31, 32, 33, 127, 128, 129, 255, 256, 257, 0]
     w = synth.Workload("edge", sum(counts), 128, len(counts), len(counts), 1, 96, "swiglu", "mxfp8", "normal")

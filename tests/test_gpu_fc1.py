@@ -151,6 +151,20 @@ def test_fc1_tiny_full(out_mode):
         assert_bf16_close(np_(o["y"])[:R], O.bf16_round(fo.y), "y")
 
 
+def test_fc1_single_cta_kernel():
+    """The single-CTA variant of the bf16 GEMM (CTA pairs switched off)."""
+    lib = L.load()
+    lib.moe_set_cta_pairs(0)
+    try:
+        case = Case(synth.WORKLOADS["tiny"])
+        o = run_fc1(case, L.OUT_MXFP8)
+        torch.cuda.synchronize()
+        assert ops.read_status(o["status"]) == 0
+        check_blocks(case, o, list(range(0, case.rt.R_pad, 32)), L.OUT_MXFP8)
+    finally:
+        lib.moe_set_cta_pairs(1)
+
+
 def test_fc1_edge_counts():
     """Experts with 0, 1, 31, 32, 33, 127, 128, 129, 255, 256, 257 rows."""
     counts = [0, 1, 31, 32, 33, 127, 128, 129, 255, 256, 257, 0]
