@@ -90,6 +90,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, const Wa
 // ---------------------------------------------------------------------------
 // TMA (bulk tensor copies global -> shared, completion on an mbarrier)
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
@@ -382,7 +385,10 @@ struct GluParams {
   float alpha, up_offset, gate_lo, gate_hi, up_lo, up_hi;
 };
 
-__device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + __expf(-z)); }
+// logistic function with the approximate divide (about 2 ulp): it feeds
+// bf16 / MXFP8 outputs, and an IEEE divide here is a large share of the
+// epilogue's instructions
+__device__ __forceinline__ float sigmoidf_(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
 __device__ __forceinline__ float phi_cdf(float z) { return 0.5f * (1.0f + erff(z * 0.70710678118654752f)); }
 __device__ __forceinline__ float phi_pdf(float z) { return 0.39894228040143268f * __expf(-0.5f * z * z); }
 

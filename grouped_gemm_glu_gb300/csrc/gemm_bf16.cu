@@ -251,11 +251,16 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& ti, uin
   } else if (MODE == BWD_GLU || MODE == BWD_GLU_DOT) {
     constexpr bool DOT = MODE == BWD_GLU_DOT;
     float dot = 0.0f;  // this warp half's share of sum_c da * act(pre) (feature-scale gradient)
+    // the saved pre-activations of the next 32-column block (128 contiguous
+    // bytes of the row, one L1 line) are prefetched while this one is processed
+    const int j_end = (h + 1) * (BN / 64);
 #pragma unroll 1
-    for (int j = h * (BN / 64); j < (h + 1) * (BN / 64); ++j) {
+    for (int j = h * (BN / 64); j < j_end; ++j) {
       const int f0 = ti.n_idx * BN + j * 32;
       if (f0 >= a.F) break;
       const int p0 = (f0 / 32) * 64;
+      if (real && j + 1 < j_end && f0 + 32 < a.F)
+        prefetch_l1(a.pre_in + (size_t)row * a.N1 + p0 + 64);
       float d[32], u[32], g[32];
       tmem_ld32(tacc + j * 32, d);
       if (real) {
@@ -504,6 +509,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 // ---------------------------------------------------------------------------
 namespace pair {
 constexpr int STAGES = 6;
+constexpr int THREADS = (EPI_WARPS + 2) * 32;
 constexpr int B_HALF = (BN / 2) * BK * 2;
 constexpr int STAGE_BYTES = A_TILE + B_HALF;
 constexpr int OFF_SCRATCH = STAGES * STAGE_BYTES;
@@ -541,9 +547,9 @@ __device__ __forceinline__ Tile decode_pair(int t, const int32_t* pref, int E, i
 }
 
 template <int MODE>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
-    k_grouped_bf16_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const Args a) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
+    k_grouped_bf16_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA32,
+                        const __grid_constant__ CUtensorMap tmB, const Args a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* tiles = smem;
@@ -577,6 +583,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     fence_barrier_init();
     fence_async_shared();
     tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmA32);
     tma_prefetch_desc(&tmB);
   }
   if (warp == MMA_WARP) {
@@ -584,7 +591,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     tmem_relinquish_pair();
   }
   // 256-row pair tiles per expert -> exclusive prefix pref[0..E]
-  for (int e = threadIdx.x; e < E; e += THREADS) pref[e + 1] = (__ldg(a.counts + e) + 2 * BM - 1) / (2 * BM);
+  for (int e = threadIdx.x; e < E; e += pair::THREADS) pref[e + 1] = (__ldg(a.counts + e) + 2 * BM - 1) / (2 * BM);
   if (threadIdx.x == 0) pref[0] = 0;
   __syncthreads();
   if (warp == 0) {
@@ -621,16 +628,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       uint32_t phase = 0;
       for (int t = cl; t < total; t += ncl) {
         const Tile ti = decode_pair(t, pref, E, a.n_tiles_n, a.counts, a.offsets, a.R_cap, (int)rank);
+        // Only the 32-row blocks of A inside the expert's padded segment are
+        // fetched: the rows past it (the second half of an expert's last pair
+        // tile, mostly) feed accumulator rows the epilogue never reads, so a
+        // thin tail tile costs little more than its weight bytes.  The
+        // leader's barrier expects both CTAs' bytes.
+        const int a_blk = (ti.rows_pad + 31) / 32;
+        uint32_t tx = 0;
+        if (rank == 0) {
+          const Tile tp = decode_pair(t, pref, E, a.n_tiles_n, a.counts, a.offsets, a.R_cap, 1);
+          tx = (uint32_t)(a_blk + (tp.rows_pad + 31) / 32) * (32 * BK * 2) + 2u * pair::B_HALF;
+        }
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(empty + stage, phase ^ 1u, guard)) {
+          const int s = stage;
+          if (!mbar_wait(empty + s, phase ^ 1u, guard)) {
             ok = false;
             break;
           }
-          uint8_t* a_dst = tiles + stage * pair::STAGE_BYTES;
-          const uint32_t bar_lead = mapa_shared(smem_u32(full + stage), 0);
-          if (rank == 0) mbar_arrive_expect_tx(full + stage, 2 * pair::STAGE_BYTES);
-          tma_load_2d_pair(a_dst, &tmA, bar_lead, kb * BK, ti.row0);
+          uint8_t* a_dst = tiles + s * pair::STAGE_BYTES;
+          const uint32_t bar_lead = mapa_shared(smem_u32(full + s), 0);
+          if (rank == 0) mbar_arrive_expect_tx(full + s, tx);
+          if (a_blk == BM / 32) {
+            tma_load_2d_pair(a_dst, &tmA, bar_lead, kb * BK, ti.row0);
+          } else {
+            for (int i = 0; i < a_blk; ++i)
+              tma_load_2d_pair(a_dst + i * (32 * BK * 2), &tmA32, bar_lead, kb * BK, ti.row0 + 32 * i);
+          }
           tma_load_3d_pair(a_dst + A_TILE, &tmB, bar_lead, kb * BK, ti.n_idx * BN + (int)rank * (BN / 2), ti.e);
           if (++stage == pair::STAGES) {
             stage = 0;
@@ -716,12 +740,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
 template <int MODE>
 static moe_status_t launch_pair(const void* A, const void* B, const Args& args, int sm_margin, cudaStream_t stream) {
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA, tmA32, tmB;
   {
     const uint64_t dims[2] = {(uint64_t)args.K, (uint64_t)args.R_cap};
     const uint64_t strides[1] = {(uint64_t)args.K * 2};
     const uint32_t box[2] = {BK, BM};
     if (!encode_tmap(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+      return MOE_ERR_CUDA;
+    const uint32_t box32[2] = {BK, 32};
+    if (!encode_tmap(&tmA32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, dims, strides, box32,
                      CU_TENSOR_MAP_SWIZZLE_128B))
       return MOE_ERR_CUDA;
   }
@@ -735,14 +763,14 @@ static moe_status_t launch_pair(const void* A, const void* B, const Args& args, 
   }
   const void* kfn = (const void*)k_grouped_bf16_pair<MODE>;
   if (!set_smem_limit(kfn, pair::SMEM_BYTES)) return MOE_ERR_CUDA;
-  int clusters = max_active_pairs(kfn, THREADS, pair::SMEM_BYTES);
+  int clusters = max_active_pairs(kfn, pair::THREADS, pair::SMEM_BYTES);
   if (clusters <= 0) return MOE_ERR_CUDA;
   const int by_margin = (sm_count() - sm_margin) / 2;
   if (clusters > by_margin) clusters = by_margin;
   const long long tiles_bound = ((long long)args.R_cap / (2 * BM) + args.E) * args.n_tiles_n;
   if (clusters > tiles_bound) clusters = (int)tiles_bound;
   if (clusters < 1) clusters = 1;
-  k_grouped_bf16_pair<MODE><<<2 * clusters, THREADS, pair::SMEM_BYTES, stream>>>(tmA, tmB, args);
+  k_grouped_bf16_pair<MODE><<<2 * clusters, pair::THREADS, pair::SMEM_BYTES, stream>>>(tmA, tmA32, tmB, args);
   count_launch();
   return launch_status();
 }
