@@ -121,27 +121,48 @@ __device__ __forceinline__ void emit_block(const Args& a, const float* y, int co
       a.s_row[(size_t)row * (N / 32) + col0 / 32] = (uint8_t)sb;
     }
     if (a.q_col != nullptr) {
-      uint32_t my_sb = 0;
+      // Column blocks (one column, the warp's 32 rows), eight columns at a
+      // time through the warp's 1 KB of shared memory: row r's eight floats
+      // go to slot s(r) (r with its low two bits rotated by r / 8) with the
+      // two 16-byte halves swapped when bit 2 of the slot is set, so both the
+      // row-wise 16-byte writes and the column reads below hit 32 distinct
+      // banks.  Lane l then takes column l % 8, rows 8 (l / 8) .. +7: amax
+      // over its eight values and the three other lanes of the column, then
+      // eight codes as one 8-byte store (the column's 32 codes are one sector).
+      float* sf = reinterpret_cast<float*>(scratch);
+      const uint32_t r_w = (uint32_t)lane;
+      const uint32_t slot_w = (r_w & ~3u) | ((r_w + (r_w >> 3)) & 3u);
+      const uint32_t half_w = (slot_w >> 2) & 1u;
+      const int cc = lane & 7, rg = lane >> 3;
 #pragma unroll
-      for (int i = 0; i < 32; i += 2) {
-        const uint32_t s0 = e8m0_from_amax_bits(__reduce_max_sync(0xFFFFFFFFu, abs_bits(y[i])));
-        const uint32_t s1 = e8m0_from_amax_bits(__reduce_max_sync(0xFFFFFFFFu, abs_bits(y[i + 1])));
-        if (lane == i) my_sb = s0;
-        if (lane == i + 1) my_sb = s1;
-        uint32_t c2 = e4m3x2(y[i] * mx_inv_scale(min(s0, 253u)), y[i + 1] * mx_inv_scale(min(s1, 253u)));
-        if (s0 == 0xFFu) c2 = (c2 & 0xFF00u) | 0x7Fu;
-        if (s1 == 0xFFu) c2 = (c2 & 0x00FFu) | 0x7F00u;
-        scratch[i * 32 + lane] = (uint8_t)(c2 & 0xFFu);
-        scratch[(i + 1) * 32 + lane] = (uint8_t)(c2 >> 8);
+      for (int c8 = 0; c8 < 4; ++c8) {
+        float4* dst = reinterpret_cast<float4*>(sf + slot_w * 8);
+        dst[half_w] = make_float4(y[8 * c8 + 0], y[8 * c8 + 1], y[8 * c8 + 2], y[8 * c8 + 3]);
+        dst[half_w ^ 1u] = make_float4(y[8 * c8 + 4], y[8 * c8 + 5], y[8 * c8 + 6], y[8 * c8 + 7]);
+        __syncwarp();
+        float v[8];
+        uint32_t m = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t r = (uint32_t)(8 * rg + i);
+          const uint32_t sr = (r & ~3u) | ((r + (r >> 3)) & 3u);
+          v[i] = sf[sr * 8 + ((uint32_t)cc ^ (((sr >> 2) & 1u) << 2))];
+          m = max(m, abs_bits(v[i]));
+        }
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
+        const uint32_t sb = e8m0_from_amax_bits(m);
+        uint32_t w0 = 0x7F7F7F7Fu, w1 = 0x7F7F7F7Fu;
+        if (sb != 0xFFu) {
+          const float inv = mx_inv_scale(sb);
+          w0 = e4m3x2(v[0] * inv, v[1] * inv) | (e4m3x2(v[2] * inv, v[3] * inv) << 16);
+          w1 = e4m3x2(v[4] * inv, v[5] * inv) | (e4m3x2(v[6] * inv, v[7] * inv) << 16);
+        }
+        const size_t col = (size_t)(col0 + 8 * c8 + cc);
+        *reinterpret_cast<uint2*>(a.q_col + col * a.R_cap + rb + 8 * rg) = make_uint2(w0, w1);
+        if (rg == 0) a.s_col[col * (a.R_cap / 32) + rb / 32] = (uint8_t)sb;
+        __syncwarp();
       }
-      __syncwarp();
-      const uint4* src = reinterpret_cast<const uint4*>(scratch + lane * 32);
-      const uint4 w0 = src[0], w1 = src[1];
-      uint4* dst = reinterpret_cast<uint4*>(a.q_col + (size_t)(col0 + lane) * a.R_cap + rb);
-      dst[0] = w0;
-      dst[1] = w1;
-      a.s_col[(size_t)(col0 + lane) * (a.R_cap / 32) + rb / 32] = (uint8_t)my_sb;
-      __syncwarp();
     }
   } else {
     if (row_ok) {
