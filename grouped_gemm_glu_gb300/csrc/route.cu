@@ -68,7 +68,20 @@ __global__ void __launch_bounds__(1024) k_route_scan(int32_t* __restrict__ chunk
   const int e = threadIdx.x;
   int32_t total = 0;
   if (e < E) {
-    for (int c = 0; c < n_chunks; ++c) {
+    // eight chunk counts loaded before they are rewritten (one memory round
+    // trip per eight chunks instead of one per chunk)
+    int c = 0;
+    for (; c + 8 <= n_chunks; c += 8) {
+      int32_t v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = chunk_counts[(size_t)(c + u) * E + e];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        chunk_counts[(size_t)(c + u) * E + e] = total;
+        total += v[u];
+      }
+    }
+    for (; c < n_chunks; ++c) {
       int32_t* p = chunk_counts + (size_t)c * E + e;
       const int32_t v = *p;
       *p = total;
@@ -119,15 +132,28 @@ __global__ void __launch_bounds__(ROUTE_THREADS) k_route_scatter(
   const int w0 = chunk0 + warp * ROUTE_WARP_SPAN;
   const bool over = *overflow != 0;
   for (int e = threadIdx.x; e < ROUTE_WARPS * E; e += ROUTE_THREADS) wbase[e] = 0;
-  __syncthreads();
-  // pass 1: per-warp histogram of its contiguous span
-  for (int i = 0; i < ROUTE_WARP_SPAN; i += 32) {
-    const int a = w0 + i + lane;
+  // the lane's expert ids and weights of the span, loaded once up front
+  constexpr int NI = ROUTE_WARP_SPAN / 32;
+  int eid[NI];
+  float pv[NI];
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const int a = w0 + 32 * i + lane;
+    eid[i] = -1;
+    pv[i] = 0.0f;
     if (a < n_assign) {
       const int e = __ldg(idx + a) - expert_begin;
-      if (e >= 0 && e < E) atomicAdd(&wbase[warp * E + e], 1);
+      if (e >= 0 && e < E) {
+        eid[i] = e;
+        pv[i] = __ldg(prob + a);
+      }
     }
   }
+  __syncthreads();
+  // pass 1: per-warp histogram of its contiguous span
+#pragma unroll
+  for (int i = 0; i < NI; ++i)
+    if (eid[i] >= 0) atomicAdd(&wbase[warp * E + eid[i]], 1);
   __syncthreads();
   // exclusive prefix over warps, plus the chunk's base within the expert
   for (int e = threadIdx.x; e < E; e += ROUTE_THREADS) {
@@ -141,20 +167,17 @@ __global__ void __launch_bounds__(ROUTE_THREADS) k_route_scatter(
   __syncthreads();
   // pass 2: stable rank, 32 consecutive assignments at a time
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int i = 0; i < ROUTE_WARP_SPAN; i += 32) {
-    const int a = w0 + i + lane;
-    int e = -1;
-    if (a < n_assign) {
-      e = __ldg(idx + a) - expert_begin;
-      if (e < 0 || e >= E) e = -1;
-    }
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const int a = w0 + 32 * i + lane;
+    const int e = eid[i];
     const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
     if (a < n_assign) {
       if (e >= 0 && !over) {
         const int32_t row = wbase[warp * E + e] + __popc(peers & lt_mask);
         row_of[a] = row;
         tok_of[row] = a / k;
-        prob_perm[row] = __ldg(prob + a);
+        prob_perm[row] = pv[i];
       } else {
         row_of[a] = -1;
       }
@@ -196,7 +219,15 @@ __global__ void __launch_bounds__(256) k_permute_gather(const uint4* __restrict_
     if (real) {
       const int t = tok_of[r];
       const uint4* src = x + (size_t)t * H8;
-      for (int v = lane; v < H8; v += 32) dst[v] = __ldg(src + v);
+      // four 16-byte loads in flight per lane before the stores
+      for (int v = lane; v < H8; v += 128) {
+        uint4 c[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) c[u] = v + 32 * u < H8 ? __ldg(src + v + 32 * u) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (v + 32 * u < H8) dst[v + 32 * u] = c[u];
+      }
     } else {
       const uint4 z = make_uint4(0, 0, 0, 0);
       for (int v = lane; v < H8; v += 32) dst[v] = z;
@@ -238,19 +269,22 @@ __global__ void __launch_bounds__(256) k_unpermute_combine(const uint4* __restri
   }
 }
 
-// The same sum for k = 4 or 8 (one thread per (token, 16-byte chunk)): the
-// token's row indices and weights arrive as 16-byte vector loads instead of
-// one load per slot, and all k row loads are issued before the adds (same
-// arithmetic and order as above).
-template <int KV>
+// The same sum for k = 4 or 8: one thread per (token, NV 16-byte chunks
+// spaced H8 / NV apart, so consecutive threads still touch consecutive
+// chunks).  The token's row indices and weights arrive as 16-byte vector
+// loads, and each slot's NV row loads are issued together: NV x 16 bytes in
+// flight per thread at a modest register count.  Same arithmetic and order
+// as above.
+template <int KV, int NV>
 __global__ void __launch_bounds__(256) k_unpermute_combine_vec(const uint4* __restrict__ y,
                                                                const int32_t* __restrict__ row_of,
                                                                const float* __restrict__ prob, int T, int H8,
                                                                uint4* __restrict__ out) {
-  const size_t total = (size_t)T * H8;
+  const int Q = (H8 + NV - 1) / NV;
+  const size_t total = (size_t)T * Q;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
-    const int t = (int)(i / H8);
-    const int v = (int)(i - (size_t)t * H8);
+    const int t = (int)(i / Q);
+    const int v0 = (int)(i - (size_t)t * Q);
     int rj[KV];
     float pj[KV];
 #pragma unroll
@@ -264,25 +298,41 @@ __global__ void __launch_bounds__(256) k_unpermute_combine_vec(const uint4* __re
         pj[4 * q] = pj[4 * q + 1] = pj[4 * q + 2] = pj[4 * q + 3] = 1.0f;  // permute backward
       }
     }
-    uint4 w[KV];
+    float acc[NV][8];
 #pragma unroll
-    for (int j = 0; j < KV; ++j) w[j] = rj[j] >= 0 ? __ldg(y + (size_t)rj[j] * H8 + v) : make_uint4(0, 0, 0, 0);
-    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int n = 0; n < NV; ++n)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[n][e] = 0.0f;
 #pragma unroll
     for (int j = 0; j < KV; ++j) {
       if (rj[j] < 0) continue;
+      const uint4* src = y + (size_t)rj[j] * H8;
+      uint4 w[NV];
+#pragma unroll
+      for (int n = 0; n < NV; ++n) {
+        const int v = v0 + n * Q;
+        w[n] = v < H8 ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+      }
       const float p = pj[j];
-      acc[0] = fmaf(p, bf16_lo(w[j].x), acc[0]);
-      acc[1] = fmaf(p, bf16_hi(w[j].x), acc[1]);
-      acc[2] = fmaf(p, bf16_lo(w[j].y), acc[2]);
-      acc[3] = fmaf(p, bf16_hi(w[j].y), acc[3]);
-      acc[4] = fmaf(p, bf16_lo(w[j].z), acc[4]);
-      acc[5] = fmaf(p, bf16_hi(w[j].z), acc[5]);
-      acc[6] = fmaf(p, bf16_lo(w[j].w), acc[6]);
-      acc[7] = fmaf(p, bf16_hi(w[j].w), acc[7]);
+#pragma unroll
+      for (int n = 0; n < NV; ++n) {
+        acc[n][0] = fmaf(p, bf16_lo(w[n].x), acc[n][0]);
+        acc[n][1] = fmaf(p, bf16_hi(w[n].x), acc[n][1]);
+        acc[n][2] = fmaf(p, bf16_lo(w[n].y), acc[n][2]);
+        acc[n][3] = fmaf(p, bf16_hi(w[n].y), acc[n][3]);
+        acc[n][4] = fmaf(p, bf16_lo(w[n].z), acc[n][4]);
+        acc[n][5] = fmaf(p, bf16_hi(w[n].z), acc[n][5]);
+        acc[n][6] = fmaf(p, bf16_lo(w[n].w), acc[n][6]);
+        acc[n][7] = fmaf(p, bf16_hi(w[n].w), acc[n][7]);
+      }
     }
-    out[i] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
-                        pack_bf16x2(acc[6], acc[7]));
+#pragma unroll
+    for (int n = 0; n < NV; ++n) {
+      const int v = v0 + n * Q;
+      if (v < H8)
+        out[(size_t)t * H8 + v] = make_uint4(pack_bf16x2(acc[n][0], acc[n][1]), pack_bf16x2(acc[n][2], acc[n][3]),
+                                             pack_bf16x2(acc[n][4], acc[n][5]), pack_bf16x2(acc[n][6], acc[n][7]));
+    }
   }
 }
 
@@ -405,19 +455,25 @@ extern "C" moe_status_t moe_route_permute(const moe_bf16* x, const int32_t* topk
 
 static void launch_combine(const uint4* y, const int32_t* row_of, const float* prob, int T, int H8, int k, uint4* out,
                            cudaStream_t st) {
-  const size_t items = (size_t)T * H8;
-  size_t grid = (items + 255) / 256;
+  constexpr int NV = 4;
   const size_t cap = (size_t)sm_count() * 8;
-  if (grid > cap) grid = cap;
   // the vector loads of row_of / prob need 16-byte alignment (k = 4 or 8)
   const bool vec_ok = (reinterpret_cast<uintptr_t>(row_of) & 15) == 0 &&
                       (prob == nullptr || (reinterpret_cast<uintptr_t>(prob) & 15) == 0);
-  if (k == 8 && vec_ok)
-    k_unpermute_combine_vec<8><<<(int)grid, 256, 0, st>>>(y, row_of, prob, T, H8, out);
-  else if (k == 4 && vec_ok)
-    k_unpermute_combine_vec<4><<<(int)grid, 256, 0, st>>>(y, row_of, prob, T, H8, out);
-  else
+  if ((k == 8 || k == 4) && vec_ok) {
+    const size_t items = (size_t)T * ((H8 + NV - 1) / NV);
+    size_t grid = (items + 255) / 256;
+    if (grid > cap) grid = cap;
+    if (k == 8)
+      k_unpermute_combine_vec<8, NV><<<(int)grid, 256, 0, st>>>(y, row_of, prob, T, H8, out);
+    else
+      k_unpermute_combine_vec<4, NV><<<(int)grid, 256, 0, st>>>(y, row_of, prob, T, H8, out);
+  } else {
+    const size_t items = (size_t)T * H8;
+    size_t grid = (items + 255) / 256;
+    if (grid > cap) grid = cap;
     k_unpermute_combine<<<(int)grid, 256, 0, st>>>(y, row_of, prob, T, H8, k, out);
+  }
 }
 
 extern "C" moe_status_t moe_unpermute_combine(const moe_bf16* y_perm, const int32_t* row_of, const float* topk_prob,
