@@ -383,6 +383,8 @@ __device__ __forceinline__ uint32_t mx_quant_block32(const float* v, uint32_t* c
 struct GluParams {
   int act;
   float alpha, up_offset, gate_lo, gate_hi, up_lo, up_hi;
+  int lean;  // SwiGLU with every clamp bound infinite: the epilogues take the short forms below
+  float nk;  // -alpha * log2(e), for the short forms
 };
 
 // logistic function with the approximate divide (about 2 ulp): it feeds
@@ -391,6 +393,28 @@ struct GluParams {
 __device__ __forceinline__ float sigmoidf_(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
 __device__ __forceinline__ float phi_cdf(float z) { return 0.5f * (1.0f + erff(z * 0.70710678118654752f)); }
 __device__ __forceinline__ float phi_pdf(float z) { return 0.39894228040143268f * __expf(-0.5f * z * z); }
+
+// Short SwiGLU forms for GluParams::lean (no clamps).  sigma(alpha g) =
+// 1 / (1 + 2^(nk g)) with nk = -alpha log2(e) folded on the host (exp(x) =
+// 2^(x log2 e)); 2^x is the hardware approximation (ex2.approx), the divide
+// the approximate one.  Backward uses d/dg [g sigma(alpha g)] =
+// sigma + alpha (g sigma)(1 - sigma).
+__device__ __forceinline__ float ex2_hw(float x) {
+  float y;
+  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float swiglu_fwd_lean(const GluParams& p, float u, float g) {
+  const float s = __fdividef(1.0f, 1.0f + ex2_hw(p.nk * g));
+  return (u + p.up_offset) * (g * s);
+}
+__device__ __forceinline__ void swiglu_bwd_lean(const GluParams& p, float u, float g, float dy, float& du,
+                                                float& dg) {
+  const float s = __fdividef(1.0f, 1.0f + ex2_hw(p.nk * g));
+  const float gs = g * s;
+  du = dy * gs;
+  dg = dy * (u + p.up_offset) * fmaf(p.alpha * gs, 1.0f - s, s);
+}
 
 // forward: y = act(u, g); sReLU uses u only
 __device__ __forceinline__ float act_fwd(const GluParams& p, float u, float g) {

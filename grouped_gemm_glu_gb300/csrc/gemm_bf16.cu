@@ -25,6 +25,8 @@
 //              (2 x 256 columns), tcgen05.commit frees smem stages and
 //              hands finished accumulators to the epilogue
 // Every wait is bounded (MOE_ERR_TIMEOUT + early exit, never a trap).
+#include <cmath>
+
 #include "common.cuh"
 #include "host_common.h"
 
@@ -245,7 +247,16 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& ti, uin
       }
       float yv[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) yv[i] = real ? act_fwd(a.prm, v[i], v[32 + i]) * rs : 0.0f;
+      for (int i = 0; i < 32; ++i) yv[i] = 0.0f;
+      if (real) {
+        if (a.prm.lean) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) yv[i] = swiglu_fwd_lean(a.prm, v[i], v[32 + i]) * rs;
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) yv[i] = act_fwd(a.prm, v[i], v[32 + i]) * rs;
+        }
+      }
       emit_block(a, yv, f0, row, rb, row_ok, scratch, lane, amax_bits);
     }
   } else if (MODE == FWD_ELT || MODE == FWD_PRE) {
@@ -291,12 +302,22 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& ti, uin
 #pragma unroll
           for (int i = 0; i < 32; ++i) dot = fmaf(d[i], act_fwd(a.prm, u[i], g[i]), dot);
         }
+        if (a.prm.lean) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float du, dg;
-          act_bwd(a.prm, u[i], g[i], d[i] * rs, du, dg);
-          u[i] = du;
-          g[i] = dg;
+          for (int i = 0; i < 32; ++i) {
+            float du, dg;
+            swiglu_bwd_lean(a.prm, u[i], g[i], d[i] * rs, du, dg);
+            u[i] = du;
+            g[i] = dg;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            float du, dg;
+            act_bwd(a.prm, u[i], g[i], d[i] * rs, du, dg);
+            u[i] = du;
+            g[i] = dg;
+          }
         }
       } else {
 #pragma unroll
@@ -837,6 +858,9 @@ static GluParams to_glu(const moe_glu_params_t* p) {
   g.gate_hi = p->gate_hi;
   g.up_lo = p->up_lo;
   g.up_hi = p->up_hi;
+  g.lean = (p->act == MOE_ACT_SWIGLU && std::isinf(p->gate_lo) && std::isinf(p->gate_hi) &&
+            std::isinf(p->up_lo) && std::isinf(p->up_hi)) ? 1 : 0;
+  g.nk = -p->alpha * 1.4426950408889634f;
   return g;
 }
 

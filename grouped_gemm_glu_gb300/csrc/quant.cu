@@ -428,6 +428,8 @@ extern "C" moe_status_t moe_glu_act(const moe_bf16* pre, const int32_t* counts, 
   g.gate_hi = params->gate_hi;
   g.up_lo = params->up_lo;
   g.up_hi = params->up_hi;
+  g.lean = 0;  // the unfused kernels keep the general forms
+  g.nk = 0.0f;
   const int N1 = act == MOE_ACT_SRELU ? F : 2 * F;
   k_glu_act<<<grid_for((size_t)R_cap * (F / 32), 256), 256, 0, as_stream(stream)>>>(pre, offsets, E, F, N1, g, y);
   count_launch();
@@ -450,6 +452,8 @@ extern "C" moe_status_t moe_dglu_act(const moe_bf16* da, const moe_bf16* pre, co
   g.gate_hi = params->gate_hi;
   g.up_lo = params->up_lo;
   g.up_hi = params->up_hi;
+  g.lean = 0;  // the unfused kernels keep the general forms
+  g.nk = 0.0f;
   const int N1 = act == MOE_ACT_SRELU ? F : 2 * F;
   k_dglu_act<<<grid_for((size_t)R_cap * (F / 32), 256), 256, 0, as_stream(stream)>>>(da, pre, offsets, E, F, N1, g,
                                                                                     dfc1);
