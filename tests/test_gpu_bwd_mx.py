@@ -1,6 +1,8 @@
 """GPU parity of the fused backward GroupGemm + dActivation + Quantize/Transpose
 and of the block-scaled MXFP8 grouped GEMMs (FC2 forward, data gradient,
 weight gradient) against the oracle, each fed the same synthetic inputs."""
+import sys
+
 import numpy as np
 import pytest
 import torch
@@ -87,6 +89,14 @@ def _dglu_case(w, rows=None, counts=None, seed=0, out_mode=L.OUT_MXFP8):
 @pytest.mark.parametrize("out_mode", [L.OUT_MXFP8, L.OUT_BF16])
 def test_dglu_tiny_full(out_mode):
     _dglu_case(synth.WORKLOADS["tiny"], out_mode=out_mode)
+
+
+def test_dglu_swiglu_alpha_offset_unclamped(monkeypatch):
+    """dSwiGLU with alpha = 1.702 and (up + 1) but no clamp: the epilogue's
+    short derivative form with non-default alpha and offset."""
+    monkeypatch.setattr(sys.modules[__name__], "_act", lambda w: (
+        L.glu_params("swiglu", alpha=1.702, up_offset=1.0), O.ActParams(O.ACT_SWIGLU, alpha=1.702, up_offset=1.0)))
+    _dglu_case(synth.WORKLOADS["tiny"], out_mode=L.OUT_MXFP8)
 
 
 def test_dglu_single_cta_kernel():

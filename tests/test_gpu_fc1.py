@@ -5,6 +5,8 @@ oracle.  Small workloads are compared in full; the full-size ones on sampled
 the oracle evaluates one by one."""
 import math
 
+import sys
+
 import numpy as np
 import pytest
 import torch
@@ -149,6 +151,18 @@ def test_fc1_tiny_full(out_mode):
         assert_mx_close(np_(o["q_col"])[:, :R], np_(o["s_col"])[:, :R // 32], qc, sc, fo.y.T, "col-wise")
     else:
         assert_bf16_close(np_(o["y"])[:R], O.bf16_round(fo.y), "y")
+
+
+def test_fc1_swiglu_alpha_offset_unclamped(monkeypatch):
+    """SwiGLU with alpha = 1.702 and (up + 1) but every clamp bound infinite:
+    the epilogue's short SwiGLU form with non-default alpha and offset."""
+    monkeypatch.setattr(sys.modules[__name__], "act_params", lambda w: (
+        L.glu_params("swiglu", alpha=1.702, up_offset=1.0), O.ActParams(O.ACT_SWIGLU, alpha=1.702, up_offset=1.0)))
+    case = Case(synth.WORKLOADS["tiny"])
+    o = run_fc1(case, L.OUT_MXFP8)
+    torch.cuda.synchronize()
+    assert ops.read_status(o["status"]) == 0
+    check_blocks(case, o, list(range(0, case.rt.R_pad, 32)), L.OUT_MXFP8)
 
 
 def test_fc1_single_cta_kernel():
