@@ -627,3 +627,54 @@ def grouped_wgrad(A_col, B_col, rt: Routing) -> np.ndarray:
         if r1 > r0:
             out[e] = A[:, r0:r1] @ B[:, r0:r1].T
     return out
+
+
+# ---------------------------------------------------------------------------
+# NVFP4 backward.  [MoE-Fusion], "Fusing MXFP8 and NVFP4 quantisation": for
+# NVFP4 the backward kernel also computes the amax of the transposed Hadamard
+# rotation of its output, which removes the separate pass over the tensor
+# that this per-tensor amax would otherwise need.
+# Readings (the page gives neither the size of the transform nor its signs):
+#  - the rotation acts along the rows of the output (the token dimension,
+#    which is the contraction dimension of the weight-gradient GEMM that reads
+#    the transposed tensor) on blocks of 16 consecutive rows; expert segments
+#    are padded to 32 rows, so no block straddles two experts;
+#  - it is the orthonormal random Hadamard transform H16 diag(s) / 4 with H16
+#    the 16 x 16 Sylvester-Hadamard matrix (H[i][j] = (-1)^popcount(i & j))
+#    and s 16 random signs drawn by the caller and passed in (bit i of
+#    `sign_mask` set: s_i = -1);
+#  - it is applied to the bf16 tensor the kernel writes (what a separate pass
+#    would read); pad rows are zero.
+# The amax does not depend on the row order of H16.
+# ---------------------------------------------------------------------------
+RHT_BLOCK = 16
+
+
+def hadamard16() -> np.ndarray:
+    """H16[i][j] = (-1)^popcount(i & j) (Sylvester order), float64."""
+    i = np.arange(RHT_BLOCK)
+    ones = np.array([[bin(int(a) & int(b)).count("1") for b in i] for a in i])
+    return np.where(ones % 2 == 0, 1.0, -1.0)
+
+
+def rht_signs(sign_mask: int) -> np.ndarray:
+    """The diagonal s of the rotation: -1 where bit i of the mask is set."""
+    return np.array([-1.0 if (int(sign_mask) >> i) & 1 else 1.0 for i in range(RHT_BLOCK)])
+
+
+def rht_transposed(y, sign_mask: int) -> np.ndarray:
+    """Z [R, C] with Z[16b:16b+16, c] = H16 diag(s) bf16(y)[16b:16b+16, c] / 4
+    for every 16-row block b and column c (R % 16 == 0), float64."""
+    Y = bf16_round(y)
+    R, C = Y.shape
+    if R % RHT_BLOCK:
+        raise ValueError("rows must be a multiple of 16")
+    M = hadamard16() * rht_signs(sign_mask)[None, :] / 4.0
+    Z = np.einsum("ij,bjc->bic", M, Y.reshape(R // RHT_BLOCK, RHT_BLOCK, C))
+    return Z.reshape(R, C)
+
+
+def rht_transposed_amax(y, sign_mask: int) -> float:
+    """Per-tensor amax of the rotated transposed output (0 for an empty tensor)."""
+    Z = rht_transposed(y, sign_mask)
+    return float(np.max(np.abs(Z))) if Z.size else 0.0
