@@ -74,6 +74,8 @@ struct Args {
   float* amax;
   uint16_t* pre_out;
   float* row_dot;          // backward: [R_cap][2 * n_tiles_n] partials of da * act(pre), may be null
+  float* rht_amax;         // backward NVFP4: amax of the transposed random Hadamard rotation, may be null
+  uint32_t rht_signs;      //   its 16 signs (bit i set: -1)
   int32_t* status;
   uint64_t wait_ns;
 };
@@ -105,13 +107,19 @@ __device__ __forceinline__ Tile decode_tile(int t, const int32_t* pref, int E, i
   return ti;
 }
 
+// Running per-thread maxima of the NVFP4 mode (float bits of |v|, v >= 0):
+// plain = max |y|, rht = max |rotated y| (backward, when requested).
+struct Amax {
+  uint32_t plain, rht;
+};
+
 // One 32-column block of activation results of one row -> its outputs.
 // y: 32 fp32 values (0 on pad rows).  col0: first output column (multiple
 // of 32).  row_ok: this thread's row lies inside the padded segment.
 // The column-wise MXFP8 path needs the whole warp (the warp's 32 rows are
 // one column block).
 __device__ __forceinline__ void emit_block(const Args& a, const float* y, int col0, int row, int rb, bool row_ok,
-                                           uint8_t* scratch, int lane, uint32_t& amax_bits) {
+                                           uint8_t* scratch, int lane, Amax& amax_bits) {
   const int N = a.out_N;
   if (a.out_mode == MOE_OUT_MXFP8) {
     uint32_t codes[8];
@@ -176,7 +184,24 @@ __device__ __forceinline__ void emit_block(const Args& a, const float* y, int co
     }
     if (a.out_mode == MOE_OUT_NVFP4) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) amax_bits = max(amax_bits, abs_bits(y[i]));
+      for (int i = 0; i < 32; ++i) amax_bits.plain = max(amax_bits.plain, abs_bits(y[i]));
+      if (a.rht_amax != nullptr) {
+        // Transposed random Hadamard rotation of the bf16 values written: the
+        // warp's rows are its lanes and a 16-row block is lanes 0-15 or 16-31,
+        // so H16 diag(s) per column is four xor-butterflies across the lanes
+        // (Sylvester order), then the 1/4 normalisation.
+        const float sg = ((a.rht_signs >> (lane & 15)) & 1u) ? -1.0f : 1.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float x = __bfloat162float(__float2bfloat16_rn(y[i])) * sg;
+#pragma unroll
+          for (int m = 1; m < 16; m <<= 1) {
+            const float o = __shfl_xor_sync(0xFFFFFFFFu, x, m);
+            x = (lane & m) ? (o - x) : (x + o);
+          }
+          amax_bits.rht = max(amax_bits.rht, abs_bits(x * 0.25f));
+        }
+      }
     }
   }
 }
@@ -212,7 +237,7 @@ __device__ __forceinline__ void store_bf16x32(uint16_t* p, const float* v, bool 
 
 template <int MODE>
 __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& ti, uint32_t tacc, int q, int h, int lane,
-                                              uint8_t* scratch, uint32_t& amax_bits) {
+                                              uint8_t* scratch, Amax& amax_bits) {
   if (q * 32 >= ti.rows_pad) return;  // no row of this warp lies in the padded segment
   const int r_local = q * 32 + lane;
   const bool real = r_local < ti.rows_valid;
@@ -509,7 +534,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // epilogue warps 0..3: warp q reads TMEM lanes 32q..32q+31
     const int q = warp & 3, h = warp >> 2;
     uint8_t* scratch = scratch_all + warp * SCRATCH_PER_WARP;
-    uint32_t amax_bits = 0;
+    Amax amax_bits{0u, 0u};
     int lt = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
       const int buf = lt & 1;
@@ -527,8 +552,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) mbar_arrive(acc_empty + buf);
     }
     if (a.out_mode == MOE_OUT_NVFP4 && a.amax != nullptr) {
-      const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, amax_bits);
+      const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, amax_bits.plain);
       if (lane == 0 && m != 0) atomicMax(reinterpret_cast<int*>(a.amax), (int)m);
+    }
+    if (a.out_mode == MOE_OUT_NVFP4 && a.rht_amax != nullptr) {
+      const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, amax_bits.rht);
+      if (lane == 0 && m != 0) atomicMax(reinterpret_cast<int*>(a.rht_amax), (int)m);
     }
   }
   tc_fence_before();
@@ -749,7 +778,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
   } else {
     const int q = warp & 3, h = warp >> 2;
     uint8_t* scratch = scratch_all + warp * SCRATCH_PER_WARP;
-    uint32_t amax_bits = 0;
+    Amax amax_bits{0u, 0u};
     int lt = 0;
     for (int t = cl; t < total; t += ncl, ++lt) {
       const int buf = lt & 1;
@@ -767,8 +796,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
       if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(acc_empty + buf), 0));
     }
     if (a.out_mode == MOE_OUT_NVFP4 && a.amax != nullptr) {
-      const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, amax_bits);
+      const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, amax_bits.plain);
       if (lane == 0 && m != 0) atomicMax(reinterpret_cast<int*>(a.amax), (int)m);
+    }
+    if (a.out_mode == MOE_OUT_NVFP4 && a.rht_amax != nullptr) {
+      const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, amax_bits.rht);
+      if (lane == 0 && m != 0) atomicMax(reinterpret_cast<int*>(a.rht_amax), (int)m);
     }
   }
   tc_fence_before();
@@ -929,6 +962,7 @@ extern "C" moe_status_t moe_grouped_fc1_glu_quant_fwd(const moe_bf16* x_perm, co
   a.s_col = out->s_col;
   a.y = reinterpret_cast<uint16_t*>(out->y);
   a.amax = out->amax;
+  if (out->rht_amax != nullptr) return MOE_ERR_ARG;  // the rotated amax belongs to the backward
   a.pre_out = reinterpret_cast<uint16_t*>(out->pre);
   a.out_N = F;
   if (gated) {
@@ -956,7 +990,6 @@ extern "C" moe_status_t moe_grouped_dglu_quant_bwd(const moe_bf16* dY_perm, cons
   if (sm_margin < 0) return MOE_ERR_ARG;
   const int act = params->act;
   if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SREGLU) return MOE_ERR_ARG;
-  if (out_mode == MOE_OUT_NVFP4) return MOE_ERR_UNSUPPORTED;
   if (!out_ok(out_mode, dfc1)) return MOE_ERR_ARG;
   const bool gated = act != MOE_ACT_SRELU;
   Args a{};
@@ -980,6 +1013,12 @@ extern "C" moe_status_t moe_grouped_dglu_quant_bwd(const moe_bf16* dY_perm, cons
   a.s_col = dfc1->s_col;
   a.y = reinterpret_cast<uint16_t*>(dfc1->y);
   a.row_dot = dfc1->row_dot;
+  // NVFP4 mode: max |dFC1| and, when asked for, the amax of its transposed
+  // random Hadamard rotation (what the NVFP4 cast of the transposed operand needs)
+  if ((dfc1->amax != nullptr || dfc1->rht_amax != nullptr) && out_mode != MOE_OUT_NVFP4) return MOE_ERR_ARG;
+  a.amax = dfc1->amax;
+  a.rht_amax = dfc1->rht_amax;
+  a.rht_signs = dfc1->rht_signs;
   a.status = status;
   a.wait_ns = g_wait_limit_ns.load();
   if (a.row_dot != nullptr) {

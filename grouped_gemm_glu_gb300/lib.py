@@ -27,7 +27,8 @@ class GluParams(C.Structure):
 
 class ActOut(C.Structure):
     _fields_ = [("q_row", C.c_void_p), ("s_row", C.c_void_p), ("q_col", C.c_void_p), ("s_col", C.c_void_p),
-                ("y", C.c_void_p), ("amax", C.c_void_p), ("pre", C.c_void_p), ("row_dot", C.c_void_p)]
+                ("y", C.c_void_p), ("amax", C.c_void_p), ("pre", C.c_void_p), ("row_dot", C.c_void_p),
+                ("rht_amax", C.c_void_p), ("rht_signs", C.c_uint32)]
 
 
 def glu_params(act: str = "swiglu", alpha: float = 1.0, up_offset: float = 0.0,

@@ -112,10 +112,12 @@ def fc1_fwd(x_perm, W1p, counts, offsets, F: int, params: L.GluParams, out_mode:
 
 def dglu_bwd(dY_perm, W2, pre, counts, offsets, F: int, params: L.GluParams, out_mode: int = L.OUT_MXFP8,
              row_scale=None, with_col: bool = True, sm_margin: int = 0, status=None,
-             out: dict | None = None, row_dot: bool = False) -> dict:
+             out: dict | None = None, row_dot: bool = False, rht_signs: int | None = None) -> dict:
     """GroupGemm + dActivation + Quantize/Transpose.  dFC1 in packed order;
     row_dot=True also returns o["row_dot"], the per-row partials of the
-    feature-scale gradient (reduce with feature_scale_grad)."""
+    feature-scale gradient (reduce with feature_scale_grad).  NVFP4 mode
+    returns y and amax (max |y|); with rht_signs (16-bit mask) also
+    o["rht_amax"], the amax of y's transposed random Hadamard rotation."""
     lib = L.load()
     dev = _dev(dY_perm)
     R_cap, H = dY_perm.shape
@@ -130,11 +132,17 @@ def dglu_bwd(dY_perm, W2, pre, counts, offsets, F: int, params: L.GluParams, out
             o.setdefault("s_col", torch.empty(N1, R_cap // 32, dtype=torch.uint8, device=dev))
     else:
         o.setdefault("y", torch.empty(R_cap, N1, dtype=torch.bfloat16, device=dev))
+        if out_mode == L.OUT_NVFP4:
+            o.setdefault("amax", torch.zeros(1, dtype=torch.float32, device=dev))
+            if rht_signs is not None:
+                o.setdefault("rht_amax", torch.zeros(1, dtype=torch.float32, device=dev))
     if row_dot:
         o.setdefault("row_dot", torch.empty(R_cap, lib.moe_dglu_row_dot_parts(F), dtype=torch.float32, device=dev))
     st = status if status is not None else new_status(dev)
-    ao = _act_out(o.get("q_row"), o.get("s_row"), o.get("q_col"), o.get("s_col"), o.get("y"))
+    ao = _act_out(o.get("q_row"), o.get("s_row"), o.get("q_col"), o.get("s_col"), o.get("y"), o.get("amax"))
     ao.row_dot = o["row_dot"].data_ptr() if "row_dot" in o else None
+    if "rht_amax" in o:
+        ao.rht_amax, ao.rht_signs = o["rht_amax"].data_ptr(), int(rht_signs) & 0xFFFF
     L.check(lib.moe_grouped_dglu_quant_bwd(_p(dY_perm), _p(W2), _p(pre), _p(row_scale), _p(counts), _p(offsets),
                                            E, H, F, R_cap, C.byref(params), out_mode, C.byref(ao), sm_margin,
                                            _p(st), _s()),

@@ -118,6 +118,12 @@ typedef struct {
   float* row_dot;    /* backward only, may be NULL: per-row partial sums of da * act(pre) (the
                       * gradient of a per-row feature scale), [R_cap][moe_dglu_row_dot_parts(F)]
                       * f32; reduce them with moe_feature_scale_grad */
+  float* rht_amax;   /* backward NVFP4 mode only, may be NULL: one float, the amax of the
+                      * transposed random Hadamard rotation of y ([MoE-Fusion] "Fusing MXFP8 and
+                      * NVFP4 quantisation"): over every 16-row block of the padded segments and
+                      * every column, max |H16 diag(s) bf16(y)[block, c]| / 4, H16 the Sylvester
+                      * Hadamard matrix; caller zeroes it.  Must be NULL in the forward. */
+  uint32_t rht_signs;/*   the 16 signs s of that rotation: bit i set -> s_i = -1 (drawn by the caller) */
 } moe_act_out_t;
 
 /* ---------------------------------------------------------------------- */
@@ -172,7 +178,9 @@ MOE_API moe_status_t moe_grouped_fc1_glu_quant_fwd(const moe_bf16* x_perm, const
  * da = dY_perm[rows of e] . W2[e]^T with W2 [E][F][H] (the forward is
  * y = a . W2[e]); (du, dg) from the saved bf16 pre [R_cap][N1]; times
  * row_scale when non-NULL; written as dFC1 [R_cap][N1] in packed column
- * order per out_mode (MXFP8 row + column-wise, or bf16).  When
+ * order per out_mode (MXFP8 row + column-wise, or bf16; NVFP4: bf16 plus
+ * max |dFC1| and, with dfc1->rht_amax set, the amax of dFC1's transposed
+ * random Hadamard rotation, so that no separate pass computes it).  When
  * dfc1->row_dot is non-NULL the epilogue also writes, for every row of the
  * padded segments, partial sums of da * act(pre) over disjoint column
  * ranges (fp32, each slot written once: deterministic), the ingredients of

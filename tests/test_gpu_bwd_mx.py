@@ -1,6 +1,7 @@
 """GPU parity of the fused backward GroupGemm + dActivation + Quantize/Transpose
 and of the block-scaled MXFP8 grouped GEMMs (FC2 forward, data gradient,
 weight gradient) against the oracle, each fed the same synthetic inputs."""
+import math
 import sys
 
 import numpy as np
@@ -97,6 +98,40 @@ def test_dglu_swiglu_alpha_offset_unclamped(monkeypatch):
     monkeypatch.setattr(sys.modules[__name__], "_act", lambda w: (
         L.glu_params("swiglu", alpha=1.702, up_offset=1.0), O.ActParams(O.ACT_SWIGLU, alpha=1.702, up_offset=1.0)))
     _dglu_case(synth.WORKLOADS["tiny"], out_mode=L.OUT_MXFP8)
+
+
+@pytest.mark.parametrize("name", ["tiny", "skew_srelu"])
+def test_dglu_nvfp4_rotated_amax(name):
+    """NVFP4 backward ([MoE-Fusion] "Fusing MXFP8 and NVFP4 quantisation"):
+    the epilogue writes dFC1 in bf16, max |dFC1| and the amax of dFC1's
+    transposed random Hadamard rotation.  The rotated amax is checked on the
+    kernel's own bf16 output (the transform alone, fp32 sums) and against the
+    oracle's dFC1 (the whole path)."""
+    w = synth.WORKLOADS[name]
+    if name != "tiny":
+        w = synth.scaled(w, T=512, H=512)
+    rt, cnt, off = _routing(w, 0, None)
+    inp = synth.make_inputs(w, 0)
+    rng = np.random.default_rng(100)
+    pre = synth._bf16(rng.standard_normal((w.R_cap, w.N1), dtype=np.float32) * 2.0)
+    gp, op = _act(w)
+    mask = 0xB3C5
+    o = ops.dglu_bwd(inp["dY"].to(DEV), inp["W2"].to(DEV), pre.to(DEV), cnt, off, w.F, gp, L.OUT_NVFP4,
+                     rht_signs=mask)
+    torch.cuda.synchronize()
+    assert ops.read_status(o["status"]) == 0
+    R = rt.R_pad
+    y = np_(o["y"])[:R].astype(np.float64)
+    got = float(o["rht_amax"].item())
+    assert math.isclose(got, O.rht_transposed_amax(y, mask), rel_tol=1e-5)
+    d = O.dglu_bwd(np_(inp["dY"])[:R], np_(inp["W2"]), np_(pre)[:R], rt, op)
+    assert math.isclose(got, O.rht_transposed_amax(d, mask), rel_tol=2e-2)
+    assert math.isclose(float(o["amax"].item()), float(np.max(np.abs(d))), rel_tol=2e-2)
+    # a different sign draw gives a different rotation (the signs reach the kernel)
+    o2 = ops.dglu_bwd(inp["dY"].to(DEV), inp["W2"].to(DEV), pre.to(DEV), cnt, off, w.F, gp, L.OUT_NVFP4,
+                      rht_signs=0x0001)
+    torch.cuda.synchronize()
+    assert math.isclose(float(o2["rht_amax"].item()), O.rht_transposed_amax(y, 0x0001), rel_tol=1e-5)
 
 
 def test_dglu_single_cta_kernel():
