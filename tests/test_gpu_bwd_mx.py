@@ -168,6 +168,16 @@ def test_dglu_dsv3_full_size_sampled():
     _dglu_case(w, rows=blocks)
 
 
+def test_dglu_gptoss_full_size_sampled():
+    """GPT-OSS-shaped backward at full size (clamped SwiGLU derivative, F 2880
+    with a half-full last N tile); every expert's first and last 32-row block."""
+    w = synth.WORKLOADS["gptoss"]
+    rt, _, _ = _routing(w)
+    blocks = sorted({int(rt.offsets[e]) for e in range(w.E) if rt.counts[e]} |
+                    {int(rt.offsets[e + 1]) - 32 for e in range(w.E) if rt.counts[e]})
+    _dglu_case(w, rows=blocks)
+
+
 def _fc2_case(E, K, N, counts, seed, experts=None, n_cols=None):
     """Block-scaled grouped GEMM on random MXFP8 operands; the oracle
     dequantises (exact) and multiplies in float64.  experts / n_cols limit

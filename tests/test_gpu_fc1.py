@@ -210,6 +210,17 @@ def test_fc1_dsv3_full_size_sampled():
     check_blocks(case, o, sample_blocks(case.rt, 16, 2), L.OUT_MXFP8)
 
 
+def test_fc1_gptoss_full_size_sampled():
+    """GPT-OSS-shaped layer at full size (T 16384, H 2880, 32 experts, top-4,
+    F 2880: N1 = 5760, the last N tile half full), bias, gate clamp +-7,
+    alpha 1.702, (up + 1), uniform router logits; sampled 32-row blocks."""
+    case = Case(synth.WORKLOADS["gptoss"])
+    o = run_fc1(case, L.OUT_MXFP8)
+    torch.cuda.synchronize()
+    assert ops.read_status(o["status"]) == 0
+    check_blocks(case, o, sample_blocks(case.rt, 8, 5), L.OUT_MXFP8)
+
+
 @pytest.mark.parametrize("name", ["skew", "skew_srelu"])
 def test_fc1_skew_nvfp4_mode_sampled(name):
     case = Case(synth.WORKLOADS[name])
