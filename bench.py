@@ -290,9 +290,12 @@ def main():
     inp = synth.make_inputs(w, seed=0, R_cap=R_cap)
     host = {k: inp[k].pin_memory() for k in ("x", "topk_idx", "topk_prob", "dOut")}
     g = {k: v.to(dev) for k, v in inp.items() if v is not None}
-    params = L.glu_params(w.act)
-    layer = MoeLayer(g["W1"], g["W2"], w.T, w.k, R_cap, params, expert_begin=w.expert_begin,
-                     sm_margin=args.sm_margin)
+    if w.gpt_oss:   # GPT-OSS SwiGLU: gate clamp +-7, alpha 1.702, (up + 1), FC1 bias
+        params = L.glu_params("swiglu", alpha=1.702, up_offset=1.0, gate_lo=-7.0, gate_hi=7.0)
+    else:
+        params = L.glu_params(w.act)
+    layer = MoeLayer(g["W1"], g["W2"], w.T, w.k, R_cap, params, b1=g.get("b1"), expert_begin=w.expert_begin,
+                     sm_margin=args.sm_margin, gated=w.gated)
     X, I, P, DO = g["x"], g["topk_idx"], g["topk_prob"], g["dOut"]
     for _ in range(args.warmup):
         layer.step(X, I, P, DO)

@@ -171,7 +171,7 @@ __device__ __forceinline__ Tile decode(int t, const int32_t* pref, const Args& a
     ti.rows_valid = min(ti.rows_valid, ti.rows_pad);
     ti.kseg0 = 0;
     ti.kseg = a.K;
-    ti.num_kb = a.K / BK;
+    ti.num_kb = a.KB;  // the last k-block may be partial (K % 128 == 32, 64 or 96)
     ti.sfa = (size_t)(pref[lo] + m_idx) * a.KB * SF_BLOCK;
     ti.sfb = ((size_t)lo * a.n_tiles_n + n_idx) * a.KB * SFB_BYTES;
   } else {
@@ -182,7 +182,7 @@ __device__ __forceinline__ Tile decode(int t, const int32_t* pref, const Args& a
     const int n_idx = local - m_idx * a.n_tiles_n;
     ti.m0 = m_idx * BM;
     ti.n0 = n_idx * BN;
-    ti.rows_valid = ti.rows_pad = BM;
+    ti.rows_valid = ti.rows_pad = min(BM, a.M - ti.m0);  // the last M tile may be partial (M % 32 == 0)
     const int o0 = __ldg(a.offsets + ti.e), o1 = __ldg(a.offsets + ti.e + 1);
     ti.kseg0 = o0;
     ti.kseg = (o0 < 0 || o1 > a.R_cap || o1 < o0) ? 0 : o1 - o0;
@@ -205,6 +205,18 @@ __device__ __forceinline__ uint32_t load4_unaligned(const uint8_t* row, int kbyt
   const uint32_t lo = w0 < ks ? __ldg(reinterpret_cast<const uint32_t*>(row + w0)) : 0u;
   const uint32_t hi = (sh != 0 && w0 + 4 < ks) ? __ldg(reinterpret_cast<const uint32_t*>(row + w0 + 4)) : 0u;
   return sh == 0 ? lo : __funnelshift_r(lo, hi, sh);
+}
+
+// Scale bytes kbyte .. kbyte+3 of one row of ks bytes (kbyte % 4 == 0);
+// bytes at or past ks read as 0.  Rows of a K that is not a multiple of 128
+// are not 4-byte aligned, so they are read bytewise.
+__device__ __forceinline__ uint32_t load_scale4(const uint8_t* row, int kbyte, int ks) {
+  if ((ks & 3) == 0) return kbyte < ks ? __ldg(reinterpret_cast<const uint32_t*>(row + kbyte)) : 0u;
+  uint32_t v = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if (kbyte + i < ks) v |= (uint32_t)__ldg(row + kbyte + i) << (8 * i);
+  return v;
 }
 
 __global__ void __launch_bounds__(256) k_sf_tile(const Args a) {
@@ -238,8 +250,7 @@ __global__ void __launch_bounds__(256) k_sf_tile(const Args a) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int r = m0 + 32 * j + lane;
-          v[j] = (r >= 0 && r < a.R_cap) ? __ldg(reinterpret_cast<const uint32_t*>(a.As + (size_t)r * ks + kb * 4))
-                                         : 0u;
+          v[j] = (r >= 0 && r < a.R_cap) ? load_scale4(a.As + (size_t)r * ks, kb * 4, ks) : 0u;
         }
         dst = a.sfa_t + it * SF_BLOCK;
       } else {
@@ -250,7 +261,7 @@ __global__ void __launch_bounds__(256) k_sf_tile(const Args a) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int n = g * 128 + 32 * j + lane;
-          v[j] = n < a.N ? __ldg(reinterpret_cast<const uint32_t*>(a.Bs + ((size_t)e * a.N + n) * ks + kb * 4)) : 0u;
+          v[j] = n < a.N ? load_scale4(a.Bs + ((size_t)e * a.N + n) * ks, kb * 4, ks) : 0u;
         }
         // [expert][n tile][k-block][half of the tile][512 bytes]
         dst = a.sfb_t + ((((size_t)e * a.n_tiles_n + (g >> 1)) * a.KB + kb) * 2 + (g & 1)) * SF_BLOCK;
@@ -330,11 +341,11 @@ __device__ __forceinline__ void store_pass(const Args& a, const Tile& ti, const 
 // 128-byte swizzled layout (16-byte chunk c of row r at chunk c ^ (r % 8):
 // the lanes of a quarter-warp hit distinct banks), then two TMA stores of
 // D[e] issued by lane 0.  The buffer is reused only after the previous
-// stores have read it.  M % 128 == 0 and N % 128 == 0 keep every box inside
-// D[e].
+// stores have read it.  The tensor map clips boxes that reach past M or N
+// (M, N multiples of 32); boxes that start past N are not issued.
 template <bool F32, int P>
 __device__ __forceinline__ void store_pass_tma(const CUtensorMap* tmO, const Tile& ti, const float* v, uint8_t* stg,
-                                               int q, int h, int lane) {
+                                               int q, int h, int lane, int N) {
   if (lane == 0) bulk_wait_read_all();
   __syncwarp();
   const int sw = lane & 7;
@@ -354,8 +365,10 @@ __device__ __forceinline__ void store_pass_tma(const CUtensorMap* tmO, const Til
     constexpr int SUB_COLS = F32 ? 32 : 64;
     const int col0 = ti.n0 + h * 128 + P;
     const int row = ti.m0 + q * 32;
-    tma_store_3d(tmO, stg, col0, row, ti.e);
-    tma_store_3d(tmO, stg + TS_SUB, col0 + SUB_COLS, row, ti.e);
+    // boxes reaching past N or M are clipped by the tensor map; one that
+    // starts at or past N (N % 128 != 0) is not issued
+    if (col0 < N) tma_store_3d(tmO, stg, col0, row, ti.e);
+    if (col0 + SUB_COLS < N) tma_store_3d(tmO, stg + TS_SUB, col0 + SUB_COLS, row, ti.e);
     bulk_commit();
   }
 }
@@ -537,10 +550,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (TS) {
         if (out_es == 4) {
-          store_pass_tma<true, 0>(&tmO, ti, v, stg, q, h, lane);
-          store_pass_tma<true, 64>(&tmO, ti, v, stg, q, h, lane);
+          store_pass_tma<true, 0>(&tmO, ti, v, stg, q, h, lane, a.N);
+          store_pass_tma<true, 64>(&tmO, ti, v, stg, q, h, lane, a.N);
         } else {
-          store_pass_tma<false, 0>(&tmO, ti, v, stg, q, h, lane);
+          store_pass_tma<false, 0>(&tmO, ti, v, stg, q, h, lane, a.N);
         }
       } else if (out_es == 4) {
         store_pass<true, 0>(a, ti, v, stg, q, h, lane);
@@ -584,16 +597,18 @@ static moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const
 static size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
 
 static int n_tiles(int N) { return (N + BN - 1) / BN; }
+static int k_blocks(int K) { return (K + BK - 1) / BK; }
+static int m_tiles_of(int M) { return (M + BM - 1) / BM; }
 
 static void fc2_ws_parts(int E, int K, int N, int R_cap, size_t* a_bytes, size_t* b_bytes) {
-  const size_t KB = (size_t)K / BK;
+  const size_t KB = (size_t)k_blocks(K);
   *a_bytes = align_up(((size_t)R_cap / BM + E) * KB * SF_BLOCK);
   *b_bytes = align_up((size_t)E * n_tiles(N) * KB * SFB_BYTES);
 }
 
 static void wgrad_ws_parts(int E, int M, int N, int R_cap, size_t* a_bytes, size_t* b_bytes) {
   const size_t KG = (size_t)R_cap / BK + E;
-  *a_bytes = align_up((size_t)(M / BM) * KG * SF_BLOCK);
+  *a_bytes = align_up((size_t)m_tiles_of(M) * KG * SF_BLOCK);
   *b_bytes = align_up((size_t)n_tiles(N) * KG * SFB_BYTES);
 }
 
@@ -622,7 +637,7 @@ extern "C" moe_status_t moe_grouped_fc2_fwd(const uint8_t* Aq, const uint8_t* As
                                             int sm_margin, int32_t* status, moe_stream_t stream) {
   using namespace gmx;
   if (!Aq || !As || !Wq || !Ws || !counts || !offsets || !y || !ws) return MOE_ERR_ARG;
-  if (E <= 0 || E > E_MAX || K <= 0 || (K % BK) || N <= 0 || (N % 128) || R_cap <= 0 || (R_cap % BM))
+  if (E <= 0 || E > E_MAX || K <= 0 || (K % 32) || N <= 0 || (N % 32) || R_cap <= 0 || (R_cap % BM))
     return MOE_ERR_ARG;
   if (!aligned16(Aq) || !aligned16(Wq) || !aligned16(y) || (reinterpret_cast<uintptr_t>(As) & 3) ||
       (reinterpret_cast<uintptr_t>(Ws) & 3) || (reinterpret_cast<uintptr_t>(ws) & 255) || sm_margin < 0)
@@ -656,7 +671,7 @@ extern "C" moe_status_t moe_grouped_fc2_fwd(const uint8_t* Aq, const uint8_t* As
   a.kgrouped = 0;
   a.n_tiles_n = n_tiles(N);
   a.m_tiles = 0;
-  a.KB = K / BK;
+  a.KB = k_blocks(K);
   a.KG = 0;
   a.As = As;
   a.Bs = Ws;
@@ -678,7 +693,7 @@ extern "C" moe_status_t moe_grouped_wgrad(const uint8_t* Aq, const uint8_t* As, 
                                           int32_t* status, moe_stream_t stream) {
   using namespace gmx;
   if (!Aq || !As || !Bq || !Bs || !counts || !offsets || !D || !ws) return MOE_ERR_ARG;
-  if (E <= 0 || E > E_MAX || M <= 0 || (M % BM) || N <= 0 || (N % 128) || R_cap <= 0 || (R_cap % BM))
+  if (E <= 0 || E > E_MAX || M <= 0 || (M % 32) || N <= 0 || (N % 32) || R_cap <= 0 || (R_cap % BM))
     return MOE_ERR_ARG;
   if (!aligned16(Aq) || !aligned16(Bq) || !aligned16(D) || (reinterpret_cast<uintptr_t>(As) & 3) ||
       (reinterpret_cast<uintptr_t>(Bs) & 3) || (reinterpret_cast<uintptr_t>(ws) & 255) || sm_margin < 0)
@@ -711,7 +726,7 @@ extern "C" moe_status_t moe_grouped_wgrad(const uint8_t* Aq, const uint8_t* As, 
   a.R_cap = R_cap;
   a.kgrouped = 1;
   a.n_tiles_n = n_tiles(N);
-  a.m_tiles = M / BM;
+  a.m_tiles = m_tiles_of(M);
   a.KB = 0;
   a.KG = R_cap / BK + E;
   a.As = As;
@@ -732,7 +747,7 @@ extern "C" moe_status_t moe_grouped_wgrad(const uint8_t* Aq, const uint8_t* As, 
                      strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return MOE_ERR_CUDA;
   }
-  const long long bound = (long long)E * (M / BM) * a.n_tiles_n;
-  const long long sf_items = (long long)(M / BM + 2 * a.n_tiles_n) * a.KG;
+  const long long bound = (long long)E * a.m_tiles * a.n_tiles_n;
+  const long long sf_items = (long long)(a.m_tiles + 2 * a.n_tiles_n) * a.KG;
   return launch(tmA, tmB, &tmO, a, bound, sf_items, sm_margin, as_stream(stream));
 }

@@ -220,7 +220,8 @@ MOE_API size_t moe_grouped_fc2_workspace_size(int E, int K, int N, int R_cap);
  * data-gradient GEMM dX = dFC1 . W1p (K = N1, N = H).
  * Aq [R_cap][K], As [R_cap][K/32], Wq [E][N][K], Ws [E][N][K/32].
  * ws: moe_grouped_fc2_workspace_size() bytes, 256-byte aligned.
- * K % 128 == 0, N % 128 == 0. */
+ * K % 32 == 0, N % 32 == 0 (a partial last 128-wide k-block or 256-wide
+ * column tile is handled; e.g. the GPT-OSS shapes K = N = 2880). */
 MOE_API moe_status_t moe_grouped_fc2_fwd(const uint8_t* Aq, const uint8_t* As,
                                  const uint8_t* Wq, const uint8_t* Ws,
                                  const int32_t* counts, const int32_t* offsets,
@@ -239,7 +240,7 @@ MOE_API size_t moe_grouped_wgrad_workspace_size(int E, int M, int N, int R_cap);
  * dW1p = wgrad(dFC1 col, x col); dW2 = wgrad(a col, dY col).
  * ws: moe_grouped_wgrad_workspace_size() bytes, 256-byte aligned.
  * Pad rows of each segment must hold zero codes (the quantizers write them).
- * M % 128 == 0, N % 128 == 0. */
+ * M % 32 == 0, N % 32 == 0. */
 MOE_API moe_status_t moe_grouped_wgrad(const uint8_t* Aq, const uint8_t* As,
                                const uint8_t* Bq, const uint8_t* Bs,
                                const int32_t* counts, const int32_t* offsets,

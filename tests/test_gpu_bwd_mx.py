@@ -234,6 +234,36 @@ def test_wgrad_edge_counts(out_f32):
             assert np.all(got[e] == 0)
 
 
+@pytest.mark.parametrize("K,N", [(2880, 2880), (5760, 2880), (96, 160)])
+def test_fc2_partial_k_block_and_column_tile(K, N):
+    """K and N multiples of 32 but not of 128 / 256 (the GPT-OSS FC2 K = N =
+    2880, its dX K = 5760, N = 2880, and a small odd case): the last k-block
+    and the last column tile are partial."""
+    counts = [3, 40, 0, 129] if K > 200 else [1, 33, 0, 70, 5]
+    _fc2_case(len(counts), K, N, counts, seed=7, n_cols=min(N, 200))
+
+
+@pytest.mark.parametrize("M,N", [(2880, 2880), (5760, 2880), (96, 160)])
+def test_wgrad_partial_row_and_column_tiles(M, N):
+    """M and N multiples of 32 but not of 128 / 256 (GPT-OSS dW2 and dW1
+    shapes): the last row tile and column tile of every expert are partial."""
+    counts = [0, 1, 31, 33, 129, 0]
+    E = len(counts)
+    w = synth.Workload("wg", sum(counts), 64, E, E, 1, 64, "swiglu", "mxfp8", "normal")
+    rt, cnt, off = _routing(w, 9, counts)
+    R_cap = w.R_cap
+    Aq, As = synth.random_mxfp8(M, R_cap, 10)
+    Bq, Bs = synth.random_mxfp8(N, R_cap, 11)
+    D = ops.wgrad(Aq.to(DEV), As.to(DEV), Bq.to(DEV), Bs.to(DEV), cnt, off, out_f32=False)
+    torch.cuda.synchronize()
+    rows = np.sort(np.random.default_rng(12).choice(M, min(M, 96), replace=False))
+    ref = O.grouped_wgrad(O.mx_dequantize(Aq.numpy()[rows], As.numpy()[rows]),
+                          O.mx_dequantize(Bq.numpy(), Bs.numpy()), rt)
+    got = np_(D)
+    assert_bf16_close(got[:, rows], O.bf16_round(ref), "wgrad")
+    assert np.all(got[[0, 5]] == 0)
+
+
 def test_wgrad_dsv3_dw2_shape_sampled_experts():
     # dW2 of the DeepSeek-V3 shard: [E, F=2048, H=7168], K = rows of each expert
     w = synth.WORKLOADS["dsv3"]

@@ -15,16 +15,25 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 
+def _acts(w):
+    """(kernel parameters, oracle parameters) of the workload's activation."""
+    if w.gpt_oss:
+        return (L.glu_params("swiglu", alpha=1.702, up_offset=1.0, gate_lo=-7.0, gate_hi=7.0),
+                O.ActParams(O.ACT_SWIGLU, alpha=1.702, up_offset=1.0, gate_lo=-7.0, gate_hi=7.0))
+    return L.glu_params("swiglu"), O.ActParams(O.ACT_SWIGLU)
+
+
 def oracle_chain(inp, w):
     """float64 oracle of the whole step with the same MXFP8 casts."""
     f64 = lambda t: np_(t)
-    prm = O.ActParams(O.ACT_SWIGLU)
+    prm = _acts(w)[1]
     rt = O.route(inp["topk_idx"].numpy(), 0, w.E)
     Rp = rt.R_pad
     xp = O.permute(f64(inp["x"]), rt)
     W1p = O.repack_fc1(f64(inp["W1"]))
     W2 = f64(inp["W2"])
-    fo = O.fc1_glu_fwd(xp, W1p, None, rt, prm)
+    b1p = None if inp.get("b1") is None else O.repack_fc1(f64(inp["b1"])[..., None])[..., 0]
+    fo = O.fc1_glu_fwd(xp, W1p, b1p, rt, prm)
     a = O.mx_dequantize(*O.mx_quantize_rows(fo.y))
     W2d = np.stack([O.mx_dequantize(*O.mx_quantize_cols(W2[e])) for e in range(w.E)])
     y = O.bf16_round(O.grouped_gemm_rows(a, W2d, rt))
@@ -44,20 +53,39 @@ def oracle_chain(inp, w):
 
 def _layer(w, inp):
     g = {k: (v.to(DEV) if v is not None else None) for k, v in inp.items()}
-    layer = MoeLayer(g["W1"], g["W2"], w.T, w.k, w.R_cap, L.glu_params("swiglu"))
+    layer = MoeLayer(g["W1"], g["W2"], w.T, w.k, w.R_cap, _acts(w)[0], b1=g.get("b1"))
     return layer, g
 
 
-def _check(layer, inp, w):
+def _check_stagewise(layer, rt):
+    """The backward GEMMs against the oracle fed the layer's own quantized
+    operands (each GEMM on its exact inputs; no upstream rounding involved)."""
+    Rp = rt.R_pad
+    deq = lambda q, s_: O.mx_dequantize(np_(q), np_(s_))
+    dW2 = O.grouped_wgrad(deq(layer.a_qc, layer.a_sc)[:, :Rp], deq(layer.dy_qc, layer.dy_sc)[:, :Rp], rt)
+    assert_bf16_close(np_(layer.dW2), O.bf16_round(dW2), "dW2 on the layer's operands")
+    dW1 = O.grouped_wgrad(deq(layer.d_qc, layer.d_sc)[:, :Rp], deq(layer.x_qc, layer.x_sc)[:, :Rp], rt)
+    assert_bf16_close(np_(layer.dW1), O.bf16_round(dW1), "dW1 on the layer's operands")
+    W1q = np.stack([deq(layer.W1q[e], layer.W1s[e]) for e in range(rt.E)])
+    dX = O.grouped_gemm_rows(deq(layer.d_q, layer.d_s)[:Rp], W1q, rt)
+    real = rt.tok_of >= 0
+    assert_bf16_close(np_(layer.dX_perm)[:Rp][real], O.bf16_round(dX)[real], "dX on the layer's operands")
+
+
+def _check(layer, inp, w, dprob_frac=0.999, wgrad_chain_bound=0.02):
     rt, out, dX, dW1, dW2, dprob, dx = oracle_chain(inp, w)
     Rp = rt.R_pad
     assert_chain_close(np_(layer.out), out, "layer output")
     real = rt.tok_of >= 0
-    assert_chain_close(np_(layer.dprob), dprob, "dprob")
+    # dprob = <dOut, y_perm> over H: on the layer's own y_perm it is an fp32 dot
+    # (tight); against the oracle chain it inherits every upstream rounding
+    _, dprob_own = O.combine_bwd(np_(inp["dOut"]), np_(layer.y_perm)[:Rp], rt.row_of, inp["topk_prob"].numpy(), Rp)
+    assert np.allclose(np_(layer.dprob), dprob_own, rtol=1e-4, atol=1e-4), "dprob on the layer's y_perm"
+    assert_chain_close(np_(layer.dprob), dprob, "dprob", frac=dprob_frac)
     assert_chain_close(np_(layer.dX_perm)[:Rp][real], dX[real], "dX_perm")
     assert_chain_close(np_(layer.dx), dx, "dx")
-    assert_chain_close(np_(layer.dW1), dW1, "dW1 (packed rows)")
-    assert_chain_close(np_(layer.dW2), dW2, "dW2")
+    assert_chain_close(np_(layer.dW1), dW1, "dW1 (packed rows)", max_frac=wgrad_chain_bound)
+    assert_chain_close(np_(layer.dW2), dW2, "dW2", max_frac=wgrad_chain_bound)
 
 
 def test_layer_step_matches_oracle():
@@ -68,6 +96,30 @@ def test_layer_step_matches_oracle():
     torch.cuda.synchronize()
     assert ops.read_status(layer.status) == 0
     _check(layer, inp, w)
+
+
+def test_layer_step_gptoss_shapes():
+    """A whole step at the GPT-OSS-shaped layer's widths (H = F = 2880, not
+    multiples of 128: partial last k-blocks and column tiles in FC2, dX and
+    the weight gradients), with its bias, clamp, alpha and (up + 1).  Fewer
+    tokens and 4 experts (every token reaches all of them: 256 rows each, as
+    many as in the DeepSeek-V3 shard) so that the float64 oracle chain stays
+    quick while each weight-gradient element still sums 256 products."""
+    w = synth.scaled(synth.WORKLOADS["gptoss"], T=256, E=4, n_experts=4)
+    inp = synth.make_inputs(w, seed=23)
+    layer, g = _layer(w, inp)
+    layer.step(g["x"], g["topk_idx"], g["topk_prob"], g["dOut"])
+    torch.cuda.synchronize()
+    assert ops.read_status(layer.status) == 0
+    # Each GEMM is first checked on the layer's own quantized operands (tight).
+    # Against the float64 chain, dprob sums 2880 products whose y factors carry
+    # the chain's MXFP8 code flips (one E4M3 step on <= 0.1% of codes, allowed
+    # per element), and the weight gradients sum 256 products of operands
+    # re-quantized after two such stages, where a scale one step apart (allowed
+    # near a power of two) moves a whole 32-row block of codes together: the
+    # chain rule takes 99% for dprob and 5% of the max for dW1 / dW2.
+    _check_stagewise(layer, O.route(inp["topk_idx"].numpy(), 0, w.E))
+    _check(layer, inp, w, dprob_frac=0.99, wgrad_chain_bound=0.05)
 
 
 def test_layer_graph_replay_new_routing():
