@@ -383,7 +383,7 @@ __device__ __forceinline__ uint32_t mx_quant_block32(const float* v, uint32_t* c
 struct GluParams {
   int act;
   float alpha, up_offset, gate_lo, gate_hi, up_lo, up_hi;
-  int lean;  // SwiGLU with every clamp bound infinite: the epilogues take the short forms below
+  int lean;  // SwiGLU: the epilogues take the short forms below (1: no clamp bound finite, 2: clamped)
   float nk;  // -alpha * log2(e), for the short forms
 };
 
@@ -414,6 +414,24 @@ __device__ __forceinline__ void swiglu_bwd_lean(const GluParams& p, float u, flo
   const float gs = g * s;
   du = dy * gs;
   dg = dy * (u + p.up_offset) * fmaf(p.alpha * gs, 1.0f - s, s);
+}
+// The same with the clamps (GPT-OSS: gate clamped to [gate_lo, gate_hi]);
+// the derivative of a clamp is 1 on the closed interval and 0 outside.
+__device__ __forceinline__ float swiglu_fwd_lean_clamped(const GluParams& p, float u, float g) {
+  const float gc = fminf(fmaxf(g, p.gate_lo), p.gate_hi);
+  const float uc = fminf(fmaxf(u, p.up_lo), p.up_hi) + p.up_offset;
+  const float s = __fdividef(1.0f, 1.0f + ex2_hw(p.nk * gc));
+  return uc * (gc * s);
+}
+__device__ __forceinline__ void swiglu_bwd_lean_clamped(const GluParams& p, float u, float g, float dy, float& du,
+                                                        float& dg) {
+  const float gc = fminf(fmaxf(g, p.gate_lo), p.gate_hi);
+  const float uc = fminf(fmaxf(u, p.up_lo), p.up_hi) + p.up_offset;
+  const bool in_g = g >= p.gate_lo && g <= p.gate_hi, in_u = u >= p.up_lo && u <= p.up_hi;
+  const float s = __fdividef(1.0f, 1.0f + ex2_hw(p.nk * gc));
+  const float gs = gc * s;
+  du = in_u ? dy * gs : 0.0f;
+  dg = in_g ? dy * uc * fmaf(p.alpha * gs, 1.0f - s, s) : 0.0f;
 }
 
 // forward: y = act(u, g); sReLU uses u only

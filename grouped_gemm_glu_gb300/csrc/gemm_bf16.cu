@@ -55,7 +55,15 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // BWD_*_DOT: the backward modes that also write the feature-scale partials
 // (separate instantiations, so the plain backward carries no extra code)
-enum Mode { FWD_GLU = 0, FWD_ELT = 1, FWD_PRE = 2, BWD_GLU = 3, BWD_ELT = 4, BWD_GLU_DOT = 5, BWD_ELT_DOT = 6 };
+enum Mode { FWD_GLU = 0, FWD_ELT = 1, FWD_PRE = 2, BWD_GLU = 3, BWD_ELT = 4, BWD_GLU_DOT = 5, BWD_ELT_DOT = 6,
+            // SwiGLU with its short activation forms (GluParams::lean 1: no clamp, 2: clamped), each
+            // its own instantiation so that a kernel carries only the activation code it runs
+            FWD_GLU_L1 = 7, FWD_GLU_L2 = 8, BWD_GLU_L1 = 9, BWD_GLU_L2 = 10 };
+__host__ __device__ constexpr bool is_fwd_glu(int m) { return m == FWD_GLU || m == FWD_GLU_L1 || m == FWD_GLU_L2; }
+__host__ __device__ constexpr bool is_bwd_glu(int m) { return m == BWD_GLU || m == BWD_GLU_DOT || m == BWD_GLU_L1 || m == BWD_GLU_L2; }
+__host__ __device__ constexpr int lean_of(int m) {
+  return (m == FWD_GLU_L1 || m == BWD_GLU_L1) ? 1 : (m == FWD_GLU_L2 || m == BWD_GLU_L2) ? 2 : 0;
+}
 
 struct Args {
   const int32_t* counts;
@@ -246,7 +254,7 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& ti, uin
   const int rb = ti.row0 + q * 32;
   const float rs = (a.row_scale != nullptr && real) ? __ldg(a.row_scale + row) : 1.0f;
 
-  if (MODE == FWD_GLU) {
+  if (is_fwd_glu(MODE)) {
 #pragma unroll 1
     for (int j = h * (BN / 128); j < (h + 1) * (BN / 128); ++j) {
       const int f0 = ti.n_idx * (BN / 2) + j * 32;
@@ -274,9 +282,12 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& ti, uin
 #pragma unroll
       for (int i = 0; i < 32; ++i) yv[i] = 0.0f;
       if (real) {
-        if (a.prm.lean) {
+        if (lean_of(MODE) == 1) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) yv[i] = swiglu_fwd_lean(a.prm, v[i], v[32 + i]) * rs;
+        } else if (lean_of(MODE) == 2) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) yv[i] = swiglu_fwd_lean_clamped(a.prm, v[i], v[32 + i]) * rs;
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) yv[i] = act_fwd(a.prm, v[i], v[32 + i]) * rs;
@@ -305,7 +316,7 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& ti, uin
         emit_block(a, yv, c0, row, rb, row_ok, scratch, lane, amax_bits);
       }
     }
-  } else if (MODE == BWD_GLU || MODE == BWD_GLU_DOT) {
+  } else if (is_bwd_glu(MODE)) {
     constexpr bool DOT = MODE == BWD_GLU_DOT;
     float dot = 0.0f;  // this warp half's share of sum_c da * act(pre) (feature-scale gradient)
     // the saved pre-activations of the next 32-column block (128 contiguous
@@ -327,11 +338,19 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& ti, uin
 #pragma unroll
           for (int i = 0; i < 32; ++i) dot = fmaf(d[i], act_fwd(a.prm, u[i], g[i]), dot);
         }
-        if (a.prm.lean) {
+        if (lean_of(MODE) == 1) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             float du, dg;
             swiglu_bwd_lean(a.prm, u[i], g[i], d[i] * rs, du, dg);
+            u[i] = du;
+            g[i] = dg;
+          }
+        } else if (lean_of(MODE) == 2) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            float du, dg;
+            swiglu_bwd_lean_clamped(a.prm, u[i], g[i], d[i] * rs, du, dg);
             u[i] = du;
             g[i] = dg;
           }
@@ -891,8 +910,10 @@ static GluParams to_glu(const moe_glu_params_t* p) {
   g.gate_hi = p->gate_hi;
   g.up_lo = p->up_lo;
   g.up_hi = p->up_hi;
-  g.lean = (p->act == MOE_ACT_SWIGLU && std::isinf(p->gate_lo) && std::isinf(p->gate_hi) &&
-            std::isinf(p->up_lo) && std::isinf(p->up_hi)) ? 1 : 0;
+  if (p->act != MOE_ACT_SWIGLU)
+    g.lean = 0;
+  else
+    g.lean = (std::isinf(p->gate_lo) && std::isinf(p->gate_hi) && std::isinf(p->up_lo) && std::isinf(p->up_hi)) ? 1 : 2;
   g.nk = -p->alpha * 1.4426950408889634f;
   return g;
 }
@@ -969,6 +990,8 @@ extern "C" moe_status_t moe_grouped_fc1_glu_quant_fwd(const moe_bf16* x_perm, co
     a.N1 = 2 * F;
     a.N_gemm = 2 * F;
     a.n_tiles_n = (2 * F + BN - 1) / BN;
+    if (a.prm.lean == 1) return launch<FWD_GLU_L1>(x_perm, W1p, a, sm_margin, as_stream(stream));
+    if (a.prm.lean == 2) return launch<FWD_GLU_L2>(x_perm, W1p, a, sm_margin, as_stream(stream));
     return launch<FWD_GLU>(x_perm, W1p, a, sm_margin, as_stream(stream));
   }
   a.N1 = F;
@@ -1025,6 +1048,8 @@ extern "C" moe_status_t moe_grouped_dglu_quant_bwd(const moe_bf16* dY_perm, cons
     if (gated) return launch<BWD_GLU_DOT>(dY_perm, W2, a, sm_margin, as_stream(stream));
     return launch<BWD_ELT_DOT>(dY_perm, W2, a, sm_margin, as_stream(stream));
   }
+  if (gated && a.prm.lean == 1) return launch<BWD_GLU_L1>(dY_perm, W2, a, sm_margin, as_stream(stream));
+  if (gated && a.prm.lean == 2) return launch<BWD_GLU_L2>(dY_perm, W2, a, sm_margin, as_stream(stream));
   if (gated) return launch<BWD_GLU>(dY_perm, W2, a, sm_margin, as_stream(stream));
   return launch<BWD_ELT>(dY_perm, W2, a, sm_margin, as_stream(stream));
 }
