@@ -383,7 +383,7 @@ __device__ __forceinline__ uint32_t mx_quant_block32(const float* v, uint32_t* c
 struct GluParams {
   int act;
   float alpha, up_offset, gate_lo, gate_hi, up_lo, up_hi;
-  int lean;  // SwiGLU: the epilogues take the short forms below (1: no clamp bound finite, 2: clamped)
+  int lean;  // short forms below: SwiGLU 1 (no clamp bound finite) / 2 (clamped), GeGLU 3 (no clamp)
   float nk;  // -alpha * log2(e), for the short forms
 };
 
@@ -415,7 +415,19 @@ __device__ __forceinline__ void swiglu_bwd_lean(const GluParams& p, float u, flo
   du = dy * gs;
   dg = dy * (u + p.up_offset) * fmaf(p.alpha * gs, 1.0f - s, s);
 }
-// The same with the clamps (GPT-OSS: gate clamped to [gate_lo, gate_hi]);
+// GeGLU (exact erf) without clamps: y = (u + c) g Phi(g),
+// d/dg [g Phi(g)] = Phi(g) + g phi(g).
+__device__ __forceinline__ float phi_cdf(float z);
+__device__ __forceinline__ float phi_pdf(float z);
+__device__ __forceinline__ float geglu_fwd_lean(const GluParams& p, float u, float g) {
+  return (u + p.up_offset) * (g * phi_cdf(g));
+}
+__device__ __forceinline__ void geglu_bwd_lean(const GluParams& p, float u, float g, float dy, float& du, float& dg) {
+  const float c = phi_cdf(g);
+  du = dy * (g * c);
+  dg = dy * (u + p.up_offset) * fmaf(g, phi_pdf(g), c);
+}
+// SwiGLU with the clamps (GPT-OSS: gate clamped to [gate_lo, gate_hi]);
 // the derivative of a clamp is 1 on the closed interval and 0 outside.
 __device__ __forceinline__ float swiglu_fwd_lean_clamped(const GluParams& p, float u, float g) {
   const float gc = fminf(fmaxf(g, p.gate_lo), p.gate_hi);

@@ -58,11 +58,18 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 enum Mode { FWD_GLU = 0, FWD_ELT = 1, FWD_PRE = 2, BWD_GLU = 3, BWD_ELT = 4, BWD_GLU_DOT = 5, BWD_ELT_DOT = 6,
             // SwiGLU with its short activation forms (GluParams::lean 1: no clamp, 2: clamped), each
             // its own instantiation so that a kernel carries only the activation code it runs
-            FWD_GLU_L1 = 7, FWD_GLU_L2 = 8, BWD_GLU_L1 = 9, BWD_GLU_L2 = 10 };
-__host__ __device__ constexpr bool is_fwd_glu(int m) { return m == FWD_GLU || m == FWD_GLU_L1 || m == FWD_GLU_L2; }
-__host__ __device__ constexpr bool is_bwd_glu(int m) { return m == BWD_GLU || m == BWD_GLU_DOT || m == BWD_GLU_L1 || m == BWD_GLU_L2; }
+            FWD_GLU_L1 = 7, FWD_GLU_L2 = 8, BWD_GLU_L1 = 9, BWD_GLU_L2 = 10, FWD_GLU_L3 = 11, BWD_GLU_L3 = 12 };
+__host__ __device__ constexpr bool is_fwd_glu(int m) {
+  return m == FWD_GLU || m == FWD_GLU_L1 || m == FWD_GLU_L2 || m == FWD_GLU_L3;
+}
+__host__ __device__ constexpr bool is_bwd_glu(int m) {
+  return m == BWD_GLU || m == BWD_GLU_DOT || m == BWD_GLU_L1 || m == BWD_GLU_L2 || m == BWD_GLU_L3;
+}
 __host__ __device__ constexpr int lean_of(int m) {
-  return (m == FWD_GLU_L1 || m == BWD_GLU_L1) ? 1 : (m == FWD_GLU_L2 || m == BWD_GLU_L2) ? 2 : 0;
+  return (m == FWD_GLU_L1 || m == BWD_GLU_L1)   ? 1
+         : (m == FWD_GLU_L2 || m == BWD_GLU_L2) ? 2
+         : (m == FWD_GLU_L3 || m == BWD_GLU_L3) ? 3
+                                                : 0;
 }
 
 struct Args {
@@ -288,6 +295,9 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& ti, uin
         } else if (lean_of(MODE) == 2) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) yv[i] = swiglu_fwd_lean_clamped(a.prm, v[i], v[32 + i]) * rs;
+        } else if (lean_of(MODE) == 3) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) yv[i] = geglu_fwd_lean(a.prm, v[i], v[32 + i]) * rs;
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) yv[i] = act_fwd(a.prm, v[i], v[32 + i]) * rs;
@@ -351,6 +361,14 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& ti, uin
           for (int i = 0; i < 32; ++i) {
             float du, dg;
             swiglu_bwd_lean_clamped(a.prm, u[i], g[i], d[i] * rs, du, dg);
+            u[i] = du;
+            g[i] = dg;
+          }
+        } else if (lean_of(MODE) == 3) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            float du, dg;
+            geglu_bwd_lean(a.prm, u[i], g[i], d[i] * rs, du, dg);
             u[i] = du;
             g[i] = dg;
           }
@@ -910,10 +928,13 @@ static GluParams to_glu(const moe_glu_params_t* p) {
   g.gate_hi = p->gate_hi;
   g.up_lo = p->up_lo;
   g.up_hi = p->up_hi;
-  if (p->act != MOE_ACT_SWIGLU)
-    g.lean = 0;
+  const bool unclamped = std::isinf(p->gate_lo) && std::isinf(p->gate_hi) && std::isinf(p->up_lo) && std::isinf(p->up_hi);
+  if (p->act == MOE_ACT_SWIGLU)
+    g.lean = unclamped ? 1 : 2;
+  else if (p->act == MOE_ACT_GEGLU && unclamped)
+    g.lean = 3;
   else
-    g.lean = (std::isinf(p->gate_lo) && std::isinf(p->gate_hi) && std::isinf(p->up_lo) && std::isinf(p->up_hi)) ? 1 : 2;
+    g.lean = 0;
   g.nk = -p->alpha * 1.4426950408889634f;
   return g;
 }
@@ -992,6 +1013,7 @@ extern "C" moe_status_t moe_grouped_fc1_glu_quant_fwd(const moe_bf16* x_perm, co
     a.n_tiles_n = (2 * F + BN - 1) / BN;
     if (a.prm.lean == 1) return launch<FWD_GLU_L1>(x_perm, W1p, a, sm_margin, as_stream(stream));
     if (a.prm.lean == 2) return launch<FWD_GLU_L2>(x_perm, W1p, a, sm_margin, as_stream(stream));
+    if (a.prm.lean == 3) return launch<FWD_GLU_L3>(x_perm, W1p, a, sm_margin, as_stream(stream));
     return launch<FWD_GLU>(x_perm, W1p, a, sm_margin, as_stream(stream));
   }
   a.N1 = F;
@@ -1050,6 +1072,7 @@ extern "C" moe_status_t moe_grouped_dglu_quant_bwd(const moe_bf16* dY_perm, cons
   }
   if (gated && a.prm.lean == 1) return launch<BWD_GLU_L1>(dY_perm, W2, a, sm_margin, as_stream(stream));
   if (gated && a.prm.lean == 2) return launch<BWD_GLU_L2>(dY_perm, W2, a, sm_margin, as_stream(stream));
+  if (gated && a.prm.lean == 3) return launch<BWD_GLU_L3>(dY_perm, W2, a, sm_margin, as_stream(stream));
   if (gated) return launch<BWD_GLU>(dY_perm, W2, a, sm_margin, as_stream(stream));
   return launch<BWD_ELT>(dY_perm, W2, a, sm_margin, as_stream(stream));
 }

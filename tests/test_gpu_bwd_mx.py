@@ -155,6 +155,11 @@ def test_dglu_gptoss_tail():
     _dglu_case(w)
 
 
+def test_dglu_geglu_tiny():
+    """GeGLU (exact erf): the epilogue's short GeGLU derivative."""
+    _dglu_case(synth.scaled(synth.WORKLOADS["tiny"], act="geglu"), out_mode=L.OUT_MXFP8)
+
+
 def test_dglu_srelu():
     w = synth.scaled(synth.WORKLOADS["skew_srelu"], T=512, H=512)
     _dglu_case(w)

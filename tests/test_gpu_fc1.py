@@ -165,6 +165,15 @@ def test_fc1_swiglu_alpha_offset_unclamped(monkeypatch):
     check_blocks(case, o, list(range(0, case.rt.R_pad, 32)), L.OUT_MXFP8)
 
 
+def test_fc1_geglu_tiny_full():
+    """GeGLU (exact erf) forward: the epilogue's short GeGLU form, every block."""
+    case = Case(synth.scaled(synth.WORKLOADS["tiny"], act="geglu"))
+    o = run_fc1(case, L.OUT_MXFP8)
+    torch.cuda.synchronize()
+    assert ops.read_status(o["status"]) == 0
+    check_blocks(case, o, list(range(0, case.rt.R_pad, 32)), L.OUT_MXFP8)
+
+
 def test_fc1_single_cta_kernel():
     """The single-CTA variant of the bf16 GEMM (CTA pairs switched off)."""
     lib = L.load()
