@@ -105,17 +105,19 @@ __global__ void __launch_bounds__(256) k_quant_rows(const uint16_t* __restrict__
 }
 
 // Column-wise (transposed).  A CTA streams tiles of 128 rows (four MX blocks
-// along R) x 64 columns through a ring of QC_STAGES shared-memory buffers
+// along R) x 128 columns through a ring of QC_STAGES shared-memory buffers
 // filled by TMA (thread 0 issues; completion on one mbarrier per buffer):
-//   1. thread (column c, block b) reads the 32 values of column c in rows
-//      32b..32b+31 of the staged tile (consecutive lanes read consecutive
-//      columns: no bank conflicts), quantises them and writes its 32 codes
-//      into a [64][128]-byte code tile;
+//   1. thread (column pair c, c + 1, block b) reads the two columns in rows
+//      32b..32b+31 of the staged tile as one 32-bit word per row (consecutive
+//      lanes read consecutive words: no bank conflicts), takes both amaxes at
+//      once as a packed 16-bit max of the bf16 magnitudes (the float amax is
+//      that value shifted left by 16), quantises both columns and writes
+//      their 32 + 32 codes into a [128][128]-byte code tile;
 //   2. the buffer is refilled with the tile QC_STAGES steps ahead;
 //   3. each column's 128 codes leave as one full 128-byte line (8 lanes x 16
 //      bytes, 4 columns per warp instruction), its 4 scales as bytes.
 // Rows past R or columns past C arrive as zeros from TMA and are not stored.
-constexpr int QC_ROWS = 128, QC_COLS = 64, QC_STAGES = 3;
+constexpr int QC_ROWS = 128, QC_COLS = 128, QC_STAGES = 2;
 constexpr int QC_TILE = QC_ROWS * QC_COLS * 2;  // bytes of one staged bf16 tile (128-byte rows)
 constexpr int QC_CODE_ROW = QC_ROWS + 16;       // padded bytes per staged code column
 constexpr int QC_OFF_CODE = QC_STAGES * QC_TILE;
@@ -192,24 +194,47 @@ __global__ void __launch_bounds__(256) k_quant_cols(const __grid_constant__ CUte
     if (t < 4) rr[t] = block_real(r0 + 32 * t);
     const bool ok = mbar_wait(full + st, ph, guard);
     if (__syncthreads_or(ok ? 0 : 1)) break;
-    // 1. quantise: warp w -> block b = w / 2, column (w % 2) * 32 + lane
+    // 1. quantise: warp w -> block b = w / 2, columns 2p, 2p + 1 with
+    //    p = (w % 2) * 32 + lane
     {
       const int b = warp >> 1;
-      const int cl = (warp & 1) * 32 + lane;
+      const int p = (warp & 1) * 32 + lane;
       const int real = rr[b];
-      const uint8_t* src = tin + st * QC_TILE + (32 * b) * (QC_COLS * 2) + cl * 2;
-      float v[32];
+      const uint8_t* src = tin + st * QC_TILE + (32 * b) * (QC_COLS * 2) + p * 4;
+      uint32_t w[32];
+      uint32_t m = 0;
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        v[j] = j < real ? __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t*>(src + j * QC_COLS * 2))
-                                          << 16)
-                        : 0.0f;
-      uint32_t codes[8];
-      const uint32_t sb = mx_quant_block32(v, codes);
-      uint4* dc = reinterpret_cast<uint4*>(tcode + cl * QC_CODE_ROW + 32 * b);
-      dc[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-      dc[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-      tscale[cl * 4 + b] = (uint8_t)sb;
+      for (int j = 0; j < 32; ++j) {
+        w[j] = j < real ? *reinterpret_cast<const uint32_t*>(src + j * QC_COLS * 2) : 0u;
+        m = __vmaxu2(m, w[j] & 0x7FFF7FFFu);
+      }
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        // column 2p + half: the low (half 0) or high bf16 of each word
+        const uint32_t sb = e8m0_from_amax_bits(half ? (m & 0xFFFF0000u) : (m << 16));
+        uint32_t codes[8];
+        if (sb == 0xFFu) {
+#pragma unroll
+          for (int k8 = 0; k8 < 8; ++k8) codes[k8] = 0x7F7F7F7Fu;
+        } else {
+          const float inv = mx_inv_scale(sb);
+#pragma unroll
+          for (int k8 = 0; k8 < 8; ++k8) {
+            float v4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t x = w[4 * k8 + e];
+              v4[e] = __uint_as_float(half ? (x & 0xFFFF0000u) : (x << 16));
+            }
+            codes[k8] = e4m3x2(v4[0] * inv, v4[1] * inv) | (e4m3x2(v4[2] * inv, v4[3] * inv) << 16);
+          }
+        }
+        const int cl = 2 * p + half;
+        uint4* dc = reinterpret_cast<uint4*>(tcode + cl * QC_CODE_ROW + 32 * b);
+        dc[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+        dc[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+        tscale[cl * 4 + b] = (uint8_t)sb;
+      }
     }
     __syncthreads();
     // 2. the buffer is free again: fetch the tile QC_STAGES steps ahead
@@ -222,8 +247,8 @@ __global__ void __launch_bounds__(256) k_quant_cols(const __grid_constant__ CUte
       const int sub = lane >> 3, part = lane & 7;
       const bool whole = r0 + QC_ROWS <= R;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int cl = warp * 8 + h * 4 + sub;
+      for (int h = 0; h < QC_COLS / 32; ++h) {
+        const int cl = warp * (QC_COLS / 8) + h * 4 + sub;
         const int c = c0 + cl;
         if (c < Cc) {
           const uint4 val = *reinterpret_cast<const uint4*>(tcode + cl * QC_CODE_ROW + part * 16);
