@@ -45,6 +45,17 @@ bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const vo
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Which short activation form a parameter set takes (GluParams::lean):
+// 1 SwiGLU without clamps, 2 clamped SwiGLU, 3 GeGLU (exact erf) without
+// clamps, 0 the general forms.
+inline int glu_lean_kind(const moe_glu_params_t* p) {
+  const bool unclamped = __builtin_isinf(p->gate_lo) && __builtin_isinf(p->gate_hi) && __builtin_isinf(p->up_lo) &&
+                         __builtin_isinf(p->up_hi);
+  if (p->act == MOE_ACT_SWIGLU) return unclamped ? 1 : 2;
+  if (p->act == MOE_ACT_GEGLU && unclamped) return 3;
+  return 0;
+}
+
 inline moe_status_t launch_status() {
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;

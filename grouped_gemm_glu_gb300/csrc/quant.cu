@@ -305,8 +305,38 @@ __global__ void __launch_bounds__(256) k_nvfp4_cast(const uint16_t* __restrict__
   }
 }
 
+// Eight bf16 values of one 16-byte word, widened to fp32.
+__device__ __forceinline__ void unpack8(const uint4 w, float* v) {
+  v[0] = bf16_lo(w.x);
+  v[1] = bf16_hi(w.x);
+  v[2] = bf16_lo(w.y);
+  v[3] = bf16_hi(w.y);
+  v[4] = bf16_lo(w.z);
+  v[5] = bf16_hi(w.z);
+  v[6] = bf16_lo(w.w);
+  v[7] = bf16_hi(w.w);
+}
+
+// The activation forms the unfused kernels are instantiated for; LEAN follows
+// GluParams::lean, so the two paths evaluate the same expressions.
+template <int LEAN>
+__device__ __forceinline__ float glu_fwd_form(const GluParams& p, float u, float g) {
+  if constexpr (LEAN == 1) return swiglu_fwd_lean(p, u, g);
+  else if constexpr (LEAN == 2) return swiglu_fwd_lean_clamped(p, u, g);
+  else if constexpr (LEAN == 3) return geglu_fwd_lean(p, u, g);
+  else return act_fwd(p, u, g);
+}
+template <int LEAN>
+__device__ __forceinline__ void glu_bwd_form(const GluParams& p, float u, float g, float dy, float& du, float& dg) {
+  if constexpr (LEAN == 1) swiglu_bwd_lean(p, u, g, dy, du, dg);
+  else if constexpr (LEAN == 2) swiglu_bwd_lean_clamped(p, u, g, dy, du, dg);
+  else if constexpr (LEAN == 3) geglu_bwd_lean(p, u, g, dy, du, dg);
+  else act_bwd(p, u, g, dy, du, dg);
+}
+
 // Unfused activation: pre [R][N1] bf16 -> y [R][F] bf16, one thread per 32
-// output columns of a row < offsets[E].
+// output columns of a row < offsets[E], 16-byte loads and stores.
+template <int LEAN>
 __global__ void __launch_bounds__(256) k_glu_act(const uint16_t* __restrict__ pre, const int32_t* __restrict__ offsets,
                                                  int E, int F, int N1, GluParams prm, uint16_t* __restrict__ y) {
   const int R = __ldg(offsets + E);
@@ -316,20 +346,25 @@ __global__ void __launch_bounds__(256) k_glu_act(const uint16_t* __restrict__ pr
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
     const size_t r = i / nb;
     const int b = (int)(i - r * nb);
-    float u[32], g[32];
-    const uint16_t* pr = pre + r * N1;
-    const int pu = gated ? b * 64 : b * 32;
+    const uint4* pr = reinterpret_cast<const uint4*>(pre + r * N1 + (gated ? b * 64 : b * 32));
+    uint4 wu[4], wg[4];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      u[j] = __uint_as_float((uint32_t)__ldg(pr + pu + j) << 16);
-      g[j] = gated ? __uint_as_float((uint32_t)__ldg(pr + pu + 32 + j) << 16) : 0.0f;
+    for (int w = 0; w < 4; ++w) wu[w] = __ldg(pr + w);
+    if (gated) {
+#pragma unroll
+      for (int w = 0; w < 4; ++w) wg[w] = __ldg(pr + 4 + w);
+    } else {
+#pragma unroll
+      for (int w = 0; w < 4; ++w) wg[w] = make_uint4(0, 0, 0, 0);
     }
     uint4* d = reinterpret_cast<uint4*>(y + r * F + (size_t)b * 32);
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-      float o[8];
+      float u[8], g[8], o[8];
+      unpack8(wu[w], u);
+      unpack8(wg[w], g);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) o[j] = act_fwd(prm, u[8 * w + j], g[8 * w + j]);
+      for (int j = 0; j < 8; ++j) o[j] = glu_fwd_form<LEAN>(prm, u[j], g[j]);
       d[w] = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
                         pack_bf16x2(o[6], o[7]));
     }
@@ -339,6 +374,7 @@ __global__ void __launch_bounds__(256) k_glu_act(const uint16_t* __restrict__ pr
 // Unfused backward activation: da [R][F] bf16 (the data-gradient GEMM's
 // output) and the saved pre-activation [R][N1] bf16 -> dFC1 [R][N1] bf16 in
 // packed column order.  One thread per 32 columns of da of a row < offsets[E].
+template <int LEAN>
 __global__ void __launch_bounds__(256) k_dglu_act(const uint16_t* __restrict__ da, const uint16_t* __restrict__ pre,
                                                   const int32_t* __restrict__ offsets, int E, int F, int N1,
                                                   GluParams prm, uint16_t* __restrict__ d) {
@@ -349,27 +385,42 @@ __global__ void __launch_bounds__(256) k_dglu_act(const uint16_t* __restrict__ d
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
     const size_t r = i / nb;
     const int b = (int)(i - r * nb);
-    const uint16_t* pr = pre + r * N1;
-    const uint16_t* dr = da + r * F + (size_t)b * 32;
     const int pu = gated ? b * 64 : b * 32;
-    float du[32], dg[32];
+    const uint4* pr = reinterpret_cast<const uint4*>(pre + r * N1 + pu);
+    const uint4* dr = reinterpret_cast<const uint4*>(da + r * F + (size_t)b * 32);
+    uint4 wu[4], wg[4], wd[4];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const float u = __uint_as_float((uint32_t)__ldg(pr + pu + j) << 16);
-      const float g = gated ? __uint_as_float((uint32_t)__ldg(pr + pu + 32 + j) << 16) : 0.0f;
-      const float dy = __uint_as_float((uint32_t)__ldg(dr + j) << 16);
-      act_bwd(prm, u, g, dy, du[j], dg[j]);
+    for (int w = 0; w < 4; ++w) {
+      wu[w] = __ldg(pr + w);
+      wd[w] = __ldg(dr + w);
+    }
+    if (gated) {
+#pragma unroll
+      for (int w = 0; w < 4; ++w) wg[w] = __ldg(pr + 4 + w);
+    } else {
+#pragma unroll
+      for (int w = 0; w < 4; ++w) wg[w] = make_uint4(0, 0, 0, 0);
+    }
+    uint4 ou[4], og[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      float u[8], g[8], dy[8], du[8], dg[8];
+      unpack8(wu[w], u);
+      unpack8(wg[w], g);
+      unpack8(wd[w], dy);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) glu_bwd_form<LEAN>(prm, u[j], g[j], dy[j], du[j], dg[j]);
+      ou[w] = make_uint4(pack_bf16x2(du[0], du[1]), pack_bf16x2(du[2], du[3]), pack_bf16x2(du[4], du[5]),
+                         pack_bf16x2(du[6], du[7]));
+      og[w] = make_uint4(pack_bf16x2(dg[0], dg[1]), pack_bf16x2(dg[2], dg[3]), pack_bf16x2(dg[4], dg[5]),
+                         pack_bf16x2(dg[6], dg[7]));
     }
     uint4* o = reinterpret_cast<uint4*>(d + r * N1 + pu);
 #pragma unroll
-    for (int w = 0; w < 4; ++w)
-      o[w] = make_uint4(pack_bf16x2(du[8 * w], du[8 * w + 1]), pack_bf16x2(du[8 * w + 2], du[8 * w + 3]),
-                        pack_bf16x2(du[8 * w + 4], du[8 * w + 5]), pack_bf16x2(du[8 * w + 6], du[8 * w + 7]));
+    for (int w = 0; w < 4; ++w) o[w] = ou[w];
     if (gated) {
 #pragma unroll
-      for (int w = 0; w < 4; ++w)
-        o[4 + w] = make_uint4(pack_bf16x2(dg[8 * w], dg[8 * w + 1]), pack_bf16x2(dg[8 * w + 2], dg[8 * w + 3]),
-                              pack_bf16x2(dg[8 * w + 4], dg[8 * w + 5]), pack_bf16x2(dg[8 * w + 6], dg[8 * w + 7]));
+      for (int w = 0; w < 4; ++w) o[4 + w] = og[w];
     }
   }
 }
@@ -442,7 +493,7 @@ extern "C" moe_status_t moe_glu_act(const moe_bf16* pre, const int32_t* counts, 
                                     int R_cap, const moe_glu_params_t* params, moe_bf16* y, moe_stream_t stream) {
   (void)counts;
   if (!pre || !offsets || !params || !y || E <= 0 || F <= 0 || (F % 32) || R_cap <= 0) return MOE_ERR_ARG;
-  if (!aligned16(y)) return MOE_ERR_ARG;
+  if (!aligned16(y) || !aligned16(pre)) return MOE_ERR_ARG;
   const int act = params->act;
   if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SREGLU) return MOE_ERR_ARG;
   GluParams g;
@@ -453,10 +504,15 @@ extern "C" moe_status_t moe_glu_act(const moe_bf16* pre, const int32_t* counts, 
   g.gate_hi = params->gate_hi;
   g.up_lo = params->up_lo;
   g.up_hi = params->up_hi;
-  g.lean = 0;  // the unfused kernels keep the general forms
-  g.nk = 0.0f;
+  g.lean = glu_lean_kind(params);
+  g.nk = -params->alpha * 1.4426950408889634f;
   const int N1 = act == MOE_ACT_SRELU ? F : 2 * F;
-  k_glu_act<<<grid_for((size_t)R_cap * (F / 32), 256), 256, 0, as_stream(stream)>>>(pre, offsets, E, F, N1, g, y);
+  const int grid = grid_for((size_t)R_cap * (F / 32), 256);
+  cudaStream_t st = as_stream(stream);
+  if (g.lean == 1) k_glu_act<1><<<grid, 256, 0, st>>>(pre, offsets, E, F, N1, g, y);
+  else if (g.lean == 2) k_glu_act<2><<<grid, 256, 0, st>>>(pre, offsets, E, F, N1, g, y);
+  else if (g.lean == 3) k_glu_act<3><<<grid, 256, 0, st>>>(pre, offsets, E, F, N1, g, y);
+  else k_glu_act<0><<<grid, 256, 0, st>>>(pre, offsets, E, F, N1, g, y);
   count_launch();
   return launch_status();
 }
@@ -466,7 +522,7 @@ extern "C" moe_status_t moe_dglu_act(const moe_bf16* da, const moe_bf16* pre, co
                                      moe_bf16* dfc1, moe_stream_t stream) {
   (void)counts;
   if (!da || !pre || !offsets || !params || !dfc1 || E <= 0 || F <= 0 || (F % 32) || R_cap <= 0) return MOE_ERR_ARG;
-  if (!aligned16(dfc1)) return MOE_ERR_ARG;
+  if (!aligned16(dfc1) || !aligned16(pre) || !aligned16(da)) return MOE_ERR_ARG;
   const int act = params->act;
   if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SREGLU) return MOE_ERR_ARG;
   GluParams g;
@@ -477,11 +533,15 @@ extern "C" moe_status_t moe_dglu_act(const moe_bf16* da, const moe_bf16* pre, co
   g.gate_hi = params->gate_hi;
   g.up_lo = params->up_lo;
   g.up_hi = params->up_hi;
-  g.lean = 0;  // the unfused kernels keep the general forms
-  g.nk = 0.0f;
+  g.lean = glu_lean_kind(params);
+  g.nk = -params->alpha * 1.4426950408889634f;
   const int N1 = act == MOE_ACT_SRELU ? F : 2 * F;
-  k_dglu_act<<<grid_for((size_t)R_cap * (F / 32), 256), 256, 0, as_stream(stream)>>>(da, pre, offsets, E, F, N1, g,
-                                                                                    dfc1);
+  const int grid = grid_for((size_t)R_cap * (F / 32), 256);
+  cudaStream_t st = as_stream(stream);
+  if (g.lean == 1) k_dglu_act<1><<<grid, 256, 0, st>>>(da, pre, offsets, E, F, N1, g, dfc1);
+  else if (g.lean == 2) k_dglu_act<2><<<grid, 256, 0, st>>>(da, pre, offsets, E, F, N1, g, dfc1);
+  else if (g.lean == 3) k_dglu_act<3><<<grid, 256, 0, st>>>(da, pre, offsets, E, F, N1, g, dfc1);
+  else k_dglu_act<0><<<grid, 256, 0, st>>>(da, pre, offsets, E, F, N1, g, dfc1);
   count_launch();
   return launch_status();
 }

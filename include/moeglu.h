@@ -303,7 +303,9 @@ MOE_API moe_status_t moe_nvfp4_cast(const moe_bf16* y, const float* amax,
                             moe_stream_t stream);
 
 /* Standalone activation of the unfused path: pre [R][N1] bf16 -> y [R][F]
- * bf16 (rows >= offsets[E] untouched, pad rows 0). */
+ * bf16 (rows >= offsets[E] untouched, pad rows 0).  F % 32 == 0; pre and y
+ * 16-byte aligned, else MOE_ERR_ARG.  Evaluates the same activation forms
+ * as the fused epilogue of moe_grouped_fc1_glu_quant_fwd. */
 MOE_API moe_status_t moe_glu_act(const moe_bf16* pre, const int32_t* counts, const int32_t* offsets,
                          int E, int F, int R_cap, const moe_glu_params_t* params,
                          moe_bf16* y, moe_stream_t stream);
@@ -336,7 +338,9 @@ MOE_API size_t moe_route_noalloc_max_scratch_bytes(void);
 /* Standalone backward activation of the unfused path: da [R][F] bf16 (the
  * data-gradient GEMM output, computed e.g. by moe_grouped_fc1_glu_quant_fwd
  * with MOE_ACT_NONE on dY_perm and W2) and the saved pre [R][N1] bf16 ->
- * dFC1 [R][N1] bf16 in packed column order (rows >= offsets[E] untouched). */
+ * dFC1 [R][N1] bf16 in packed column order (rows >= offsets[E] untouched).
+ * F % 32 == 0; da, pre and dfc1 16-byte aligned, else MOE_ERR_ARG.
+ * Evaluates the same forms as the fused epilogue of moe_grouped_dglu_quant_bwd. */
 MOE_API moe_status_t moe_dglu_act(const moe_bf16* da, const moe_bf16* pre, const int32_t* counts,
                                   const int32_t* offsets, int E, int F, int R_cap,
                                   const moe_glu_params_t* params, moe_bf16* dfc1, moe_stream_t stream);

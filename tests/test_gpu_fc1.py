@@ -313,16 +313,57 @@ def test_nvfp4_cast_bit_exact():
     assert_exact(np_(q), qr, "nvfp4 codes")
 
 
-@pytest.mark.parametrize("act", ["swiglu", "geglu", "srelu"])
-def test_unfused_glu_act(act):
+# Every activation form the unfused kernels are instantiated for: plain
+# SwiGLU, clamped GPT-OSS SwiGLU with alpha and the +1 offset, GeGLU with an
+# offset on the linear half, the general forms (sReGLU), and sReLU without a
+# gate.
+UNFUSED_ACTS = {
+    "swiglu": ({}, O.ACT_SWIGLU),
+    "swiglu_oss": ({"alpha": 1.702, "up_offset": 1.0, "gate_lo": -7.0, "gate_hi": 7.0, "up_lo": -7.0, "up_hi": 7.0},
+                   O.ACT_SWIGLU),
+    "geglu": ({"up_offset": 0.5}, O.ACT_GEGLU),
+    "sreglu": ({}, O.ACT_SREGLU),
+    "srelu": ({}, O.ACT_SRELU),
+}
+
+
+def _unfused_params(name):
+    kw, oact = UNFUSED_ACTS[name]
+    act = {O.ACT_SWIGLU: "swiglu", O.ACT_GEGLU: "geglu", O.ACT_SREGLU: "sreglu", O.ACT_SRELU: "srelu"}[oact]
+    return L.glu_params(act, **kw), O.ActParams(oact, **kw)
+
+
+@pytest.mark.parametrize("name", list(UNFUSED_ACTS))
+def test_unfused_glu_act(name):
     rng = np.random.default_rng(14)
-    F, R = 128, 64
-    N1 = F if act == "srelu" else 2 * F
-    pre = synth._bf16(rng.standard_normal((R, N1), dtype=np.float32) * 2)
-    offsets = torch.tensor([0, 64], dtype=torch.int32, device=DEV)
-    counts = torch.tensor([64], dtype=torch.int32, device=DEV)
-    y = ops.glu_act(pre.to(DEV), counts, offsets, F, L.glu_params(act))
-    p = np_(pre)
-    prm = O.ActParams(ORACLE_ACT[act])
-    ref = O.act_fwd(p, None, prm) if act == "srelu" else O.act_fwd(*O.unpack_glu_cols(p), prm)
-    assert_bf16_close(np_(y), O.bf16_round(ref), "glu_act")
+    F, R = 128, 96
+    prm_c, prm = _unfused_params(name)
+    N1 = F if prm.act == O.ACT_SRELU else 2 * F
+    pre = synth._bf16(rng.standard_normal((R, N1), dtype=np.float32) * 4)
+    # rows past offsets[E] are not processed and stay as they were
+    offsets = torch.tensor([0, 32, 80], dtype=torch.int32, device=DEV)
+    counts = torch.tensor([32, 48], dtype=torch.int32, device=DEV)
+    y = ops.glu_act(pre.to(DEV), counts, offsets, F, prm_c)
+    p = np_(pre)[:80]
+    ref = O.act_fwd(p, None, prm) if prm.act == O.ACT_SRELU else O.act_fwd(*O.unpack_glu_cols(p), prm)
+    assert_bf16_close(np_(y)[:80], O.bf16_round(ref), "glu_act")
+
+
+@pytest.mark.parametrize("name", list(UNFUSED_ACTS))
+def test_unfused_dglu_act(name):
+    rng = np.random.default_rng(15)
+    F, R = 128, 96
+    prm_c, prm = _unfused_params(name)
+    N1 = F if prm.act == O.ACT_SRELU else 2 * F
+    pre = synth._bf16(rng.standard_normal((R, N1), dtype=np.float32) * 4)
+    da = synth._bf16(rng.standard_normal((R, F), dtype=np.float32))
+    offsets = torch.tensor([0, 32, 80], dtype=torch.int32, device=DEV)
+    counts = torch.tensor([32, 48], dtype=torch.int32, device=DEV)
+    d = ops.dglu_act(da.to(DEV), pre.to(DEV), counts, offsets, F, prm_c)
+    p, dy = np_(pre)[:80], np_(da)[:80]
+    if prm.act == O.ACT_SRELU:
+        ref, _ = O.act_bwd(p, None, dy, prm)
+    else:
+        du, dg = O.act_bwd(*O.unpack_glu_cols(p), dy, prm)
+        ref = O.pack_glu_cols(du, dg)
+    assert_bf16_close(np_(d)[:80], O.bf16_round(ref), "dglu_act")
