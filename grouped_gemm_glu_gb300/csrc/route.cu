@@ -604,3 +604,37 @@ extern "C" moe_status_t moe_route_permute_noalloc(const moe_bf16* x, const int32
   count_launch(4);
   return launch_status();
 }
+
+namespace moeglu {
+
+// Self-test of the bounded pipeline wait that every persistent GEMM uses:
+// one thread waits, through the same guard, for phase 0 of an mbarrier.  With
+// arrive != 0 the thread arrives first and the wait succeeds at once; with
+// arrive == 0 nothing ever arrives, so the wait must give up after the limit,
+// record MOE_ERR_TIMEOUT and return (no trap, the context stays usable).
+__global__ void k_wait_selftest(int arrive, uint64_t limit_ns, int32_t* status, uint64_t* waited_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (arrive) mbar_arrive(&bar);
+    WaitGuard g{&abort_flag, status, limit_ns};
+    const uint64_t t0 = globaltimer_ns();
+    mbar_wait(&bar, 0u, g);
+    *waited_ns = globaltimer_ns() - t0;
+  }
+}
+
+}  // namespace moeglu
+
+extern "C" moe_status_t moe_wait_selftest(int arrive, int32_t* status, uint64_t* waited_ns, moe_stream_t stream) {
+  if (!status || !waited_ns) return MOE_ERR_ARG;
+  k_wait_selftest<<<1, 32, 0, as_stream(stream)>>>(arrive, g_wait_limit_ns.load(), status, waited_ns);
+  count_launch();
+  return launch_status();
+}

@@ -62,6 +62,7 @@ _SIGS = {
     "moe_route_noalloc_max_scratch_bytes": ([], SZ),
     "moe_get_status": [P, P, P],
     "moe_set_wait_limit_ns": ([U64], None),
+    "moe_wait_selftest": [I, P, P, P],
     "moe_set_cta_pairs": ([I], None),
     "moe_launch_count": ([], U64),
 }

@@ -35,6 +35,14 @@ def read_status(status: torch.Tensor) -> int:
     return out.value
 
 
+def wait_selftest(arrive: bool, device="cuda") -> tuple[int, int]:
+    """Runs the bounded-wait self-test; returns (status word, ns waited)."""
+    status = new_status(device)
+    waited = torch.zeros(1, dtype=torch.int64, device=device)
+    L.check(L.load().moe_wait_selftest(1 if arrive else 0, _p(status), _p(waited), _s()), "moe_wait_selftest")
+    return read_status(status), int(waited.item())
+
+
 def repack_fc1(W1: torch.Tensor, inverse: bool = False) -> torch.Tensor:
     """[E, 2F, H] logical input|gate rows <-> packed rows (bf16)."""
     lib = L.load()

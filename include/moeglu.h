@@ -353,6 +353,17 @@ MOE_API moe_status_t moe_get_status(const int32_t* status, int32_t* host_out, mo
  * after it a wait gives up, sets MOE_ERR_TIMEOUT and the kernel returns. */
 MOE_API void moe_set_wait_limit_ns(uint64_t ns);
 
+/* Self-test of the bounded wait behind every pipeline wait of the
+ * persistent kernels (failure detection without a GPU fault).  One thread
+ * waits for an mbarrier phase through the same guard the GEMMs use, with the
+ * limit set by moe_set_wait_limit_ns.  arrive != 0: the barrier is arrived
+ * at first, the wait succeeds and *status is not touched.  arrive == 0:
+ * nothing arrives, the wait gives up after the limit and ORs MOE_ERR_TIMEOUT
+ * into *status; the kernel then returns normally.  *waited_ns (device
+ * uint64) receives the time the wait took.  status and waited_ns are device
+ * pointers; NULL returns MOE_ERR_ARG. */
+MOE_API moe_status_t moe_wait_selftest(int arrive, int32_t* status, uint64_t* waited_ns, moe_stream_t stream);
+
 /* Tile configuration of the bf16 grouped GEMMs (FC1 forward, dGLU
  * backward): enable != 0 (default) runs them on CTA pairs (256 x 256 tiles,
  * tcgen05 cta_group::2, 32 KB per SM per pipeline stage); 0 runs one CTA per
