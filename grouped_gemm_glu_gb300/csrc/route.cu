@@ -19,6 +19,7 @@
 //   k_unpermute_combine(_vec)  weighted sum of each token's rows (the combine),
 //                   or the plain sum (permute backward); vector index loads
 //                   for k = 4, 8
+//   k_combine_warp  the same sum for the other k <= 32, one warp per token
 //   k_combine_bwd   one warp per permuted row: dY_perm and dprob
 #include <mutex>
 
@@ -336,6 +337,68 @@ __global__ void __launch_bounds__(256) k_unpermute_combine_vec(const uint4* __re
   }
 }
 
+// The same sum for the other k <= 32, one warp per token.  For k = 4, 8 the
+// per-thread form above keeps a whole row's loads in flight at once and is
+// faster; for other k the generic kernel issues one 16-byte load per slot and
+// thread, and this one U per slot and lane.  Lanes j < k load the token's row
+// index and weight once; the warp then streams the rows of the live slots:
+// each lane sums U 16-byte chunks (32 apart, so a warp load is 512
+// contiguous bytes of a row) over the slots in ascending j, with the same
+// fmaf sequence as the kernels above.
+template <int U>
+__global__ void __launch_bounds__(256) k_combine_warp(const uint4* __restrict__ y, const int32_t* __restrict__ row_of,
+                                                      const float* __restrict__ prob, int T, int H8, int k,
+                                                      uint4* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += gridDim.x * wpb) {
+    int r = -1;
+    float p = 0.0f;
+    if (lane < k) {
+      r = __ldg(row_of + (size_t)t * k + lane);
+      p = prob ? __ldg(prob + (size_t)t * k + lane) : 1.0f;  // no weights: permute backward
+    }
+    const uint32_t live = __ballot_sync(0xFFFFFFFFu, r >= 0);
+    for (int v0 = lane; v0 < H8; v0 += 32 * U) {
+      float acc[U][8];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[u][e] = 0.0f;
+      for (uint32_t m = live; m != 0; m &= m - 1) {
+        const int j = __ffs(m) - 1;
+        const int rj = __shfl_sync(0xFFFFFFFFu, r, j);
+        const float pj = __shfl_sync(0xFFFFFFFFu, p, j);
+        const uint4* src = y + (size_t)rj * H8;
+        uint4 w[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int v = v0 + 32 * u;
+          w[u] = v < H8 ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          acc[u][0] = fmaf(pj, bf16_lo(w[u].x), acc[u][0]);
+          acc[u][1] = fmaf(pj, bf16_hi(w[u].x), acc[u][1]);
+          acc[u][2] = fmaf(pj, bf16_lo(w[u].y), acc[u][2]);
+          acc[u][3] = fmaf(pj, bf16_hi(w[u].y), acc[u][3]);
+          acc[u][4] = fmaf(pj, bf16_lo(w[u].z), acc[u][4]);
+          acc[u][5] = fmaf(pj, bf16_hi(w[u].z), acc[u][5]);
+          acc[u][6] = fmaf(pj, bf16_lo(w[u].w), acc[u][6]);
+          acc[u][7] = fmaf(pj, bf16_hi(w[u].w), acc[u][7]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + 32 * u;
+        if (v < H8)
+          out[(size_t)t * H8 + v] = make_uint4(pack_bf16x2(acc[u][0], acc[u][1]), pack_bf16x2(acc[u][2], acc[u][3]),
+                                               pack_bf16x2(acc[u][4], acc[u][5]), pack_bf16x2(acc[u][6], acc[u][7]));
+      }
+    }
+  }
+}
+
 // Combine backward (the chain rule on the combine above): one warp per
 // permuted row r < offsets[E].  Real row (t = tok_of[r] >= 0):
 //   dY_perm[r] = bf16(prob_perm[r] * dOut[t])
@@ -468,6 +531,10 @@ static void launch_combine(const uint4* y, const int32_t* row_of, const float* p
       k_unpermute_combine_vec<8, NV><<<(int)grid, 256, 0, st>>>(y, row_of, prob, T, H8, out);
     else
       k_unpermute_combine_vec<4, NV><<<(int)grid, 256, 0, st>>>(y, row_of, prob, T, H8, out);
+  } else if (k <= 32) {
+    size_t grid = ((size_t)T + 7) / 8;  // 8 tokens (warps) per CTA
+    if (grid > cap) grid = cap;
+    k_combine_warp<4><<<(int)grid, 256, 0, st>>>(y, row_of, prob, T, H8, k, out);
   } else {
     const size_t items = (size_t)T * H8;
     size_t grid = (items + 255) / 256;
