@@ -44,3 +44,17 @@ def test_argument_validation_needs_no_device(lib):
     out = L.ActOut()
     assert lib.moe_grouped_fc1_glu_quant_fwd(None, None, None, None, None, None, 4, 256, 512, 1152,
                                              ctypes.byref(prm), 1, ctypes.byref(out), 0, None, None) == L.MOE_ERR_ARG
+    assert lib.moe_wait_selftest(0, None, None, None) == L.MOE_ERR_ARG
+    assert lib.moe_quantize_mxfp8(None, 1, 32, 32, 0, None, None, 0, None, None, None, None) == L.MOE_ERR_ARG
+    assert lib.moe_grouped_fc2_fwd(None, None, None, None, None, None, 4, 512, 256, 1152, None, None, 0, 0, None,
+                                   None) == L.MOE_ERR_ARG
+    assert lib.moe_grouped_wgrad(None, None, None, None, None, None, 4, 512, 256, 1152, None, 0, None, 0, 0, None,
+                                 None) == L.MOE_ERR_ARG
+    # shape and alignment rules are host checks too (these addresses are never dereferenced)
+    a16, a8 = 0x10000, 0x10008
+    assert lib.moe_glu_act(a16, a16, a16, 1, 48, 64, ctypes.byref(prm), a16, None) == L.MOE_ERR_ARG  # F % 32
+    assert lib.moe_glu_act(a16, a16, a16, 1, 64, 64, ctypes.byref(prm), a8, None) == L.MOE_ERR_ARG  # y unaligned
+    assert lib.moe_glu_act(a8, a16, a16, 1, 64, 64, ctypes.byref(prm), a16, None) == L.MOE_ERR_ARG  # pre unaligned
+    assert lib.moe_dglu_act(a8, a16, a16, a16, 1, 64, 64, ctypes.byref(prm), a16, None) == L.MOE_ERR_ARG
+    assert lib.moe_nvfp4_cast(a16, a16, a16, a16, 1, 40, 64, a16, a16, a16, None) == L.MOE_ERR_ARG  # N % 16
+    assert lib.moe_repack_fc1(a16, a16, 1, 32, 64, 0, None) == L.MOE_ERR_ARG  # in place
