@@ -112,3 +112,24 @@ def test_permute_unpermute_round_trip_identity():
     g = ops.route_permute(x, idx.to(DEV), ones, E, ((T + 31 * E) + 127) // 128 * 128)
     out = ops.unpermute_combine(g["x_perm"], g["row_of"], ones)
     assert torch.equal(out, x)
+
+
+@pytest.mark.parametrize("k,H", [(3, 2880), (6, 4096), (12, 2880), (32, 256)])
+def test_combine_and_permute_bwd_warp_per_token_k(k, H):
+    """Top-k other than 4 and 8 runs the one-warp-per-token kernel: a row
+    width that is not a multiple of the warp's 128-chunk step (H = 2880), and
+    a shard that sees only some of each token's experts (dropped slots)."""
+    rng = np.random.default_rng(20 + k)
+    T, n_experts, E, begin = 1024, 64, 16, 8
+    idx = np.stack([rng.permutation(n_experts)[:k] for _ in range(T)]).astype(np.int32)
+    prob = rng.random((T, k), dtype=np.float32)
+    rt = O.route(idx, begin, E)
+    R = int(rt.R_pad)
+    y = synth._bf16(rng.standard_normal((R, H), dtype=np.float32))
+    row_of = torch.from_numpy(rt.row_of.astype(np.int32)).to(DEV)
+    out = ops.unpermute_combine(y.to(DEV), row_of, torch.from_numpy(prob).to(DEV))
+    ref = O.bf16_round(O.unpermute_combine(np_(y), rt.row_of, prob))
+    assert_bf16_close(np_(out), ref, f"combine k={k}")
+    dx = ops.permute_bwd(y.to(DEV), row_of, T, k)
+    ref = O.bf16_round(O.permute_bwd(np_(y), rt.row_of, T, k))
+    assert_bf16_close(np_(dx), ref, f"permute bwd k={k}")
