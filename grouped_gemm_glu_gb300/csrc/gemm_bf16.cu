@@ -12,18 +12,24 @@
 // the kernel's own tile scheduler.  [MegaMoE] §4.2: producer / consumer warp
 // specialisation over a multi-stage shared-memory ring; §5.3: tails masked.)
 //
-// CTA = 6 warps, one CTA per SM, persistent over tiles t = blockIdx.x +
-// i*gridDim.x (tiles ordered expert-major, then N, then M so that the CTAs
-// working at one time share weight tiles in L2):
-//   warps 0-3  epilogue: TMEM -> registers (thread = accumulator row),
-//              bias, activation, MXFP8 row + column quantisation, stores
-//   warp  4    TMA producer (one thread): A = activations [rows][K] box
-//              128x64, B = weights [E][N][K] box 256x64, 128-byte swizzle,
-//              STAGES-deep ring of full/empty mbarriers
-//   warp  5    TMEM owner + MMA issuer (one thread): tcgen05.mma kind::f16,
-//              M=128 N=256 K=16, accumulator double-buffered in TMEM
-//              (2 x 256 columns), tcgen05.commit frees smem stages and
-//              hands finished accumulators to the epilogue
+// Two variants share the warp roles and the epilogue.  CTA = 10 warps, one
+// CTA per SM, persistent over tiles (ordered expert-major, then N, then M so
+// that the CTAs working at one time share weight tiles in L2):
+//   warps 0-7  epilogue: warp w reads TMEM lane quarter w % 4 (one thread =
+//              one accumulator row) and column half w / 4 of the tile; bias,
+//              activation (or its derivative from the saved pre-activation),
+//              MXFP8 row + column quantisation (or bf16 / NVFP4), stores
+//   warp  8    TMA producer (one thread): 128-byte-swizzled boxes of A
+//              (activations [rows][K], 64 columns of K) and B (weights
+//              [E][N][K]) into a multi-stage ring of full/empty mbarriers
+//   warp  9    TMEM owner + MMA issuer (one thread): tcgen05.mma kind::f16,
+//              K = 16 per instruction, fp32 accumulators double-buffered in
+//              TMEM (2 x 256 of the 512 columns); tcgen05.commit frees smem
+//              stages and hands finished accumulators to the epilogue
+// Default (k_grouped_bf16_pair): clusters of 2 CTAs run 256 x 256 tiles with
+// tcgen05 cta_group::2 (M = 256 issued by the even CTA, each CTA holding 128
+// rows of A and half of B per stage, 6 stages); moe_set_cta_pairs(0) selects
+// k_grouped_bf16, one CTA per 128 x 256 tile with 4 stages.
 // Every wait is bounded (MOE_ERR_TIMEOUT + early exit, never a trap).
 #include <cmath>
 

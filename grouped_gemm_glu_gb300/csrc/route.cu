@@ -615,7 +615,11 @@ static __device__ __align__(256) int32_t g_route_scratch[ROUTE_STATIC_SCRATCH_BY
 
 // Device address of g_route_scratch, looked up once per device.  On the
 // host the name g_route_scratch is only a stand-in for the device symbol,
-// never a usable address, so the address must come from the runtime.
+// never a usable address, so the address must come from the runtime.  The
+// cached address belongs to the device's primary context as it was at the
+// look-up: after cudaDeviceReset the library's module is loaded afresh and
+// the cached address is stale (the caller must not use this entry point on a
+// device after resetting it).
 static int32_t* route_scratch_ptr() {
   static std::mutex mu;
   static int32_t* ptrs[64] = {nullptr};
@@ -650,26 +654,11 @@ extern "C" moe_status_t moe_route_permute_noalloc(const moe_bf16* x, const int32
   if (moe_route_workspace_size(T, k, E) > ROUTE_STATIC_SCRATCH_BYTES) return MOE_ERR_ARG;
   int32_t* scratch = route_scratch_ptr();
   if (!scratch) return MOE_ERR_CUDA;
-  cudaStream_t s = as_stream(stream);
-  const int n_assign = T * k;
-  const int n_chunks = route_chunks(T, k);
-  int32_t* chunk_counts = scratch;  // every entry is written by k_route_count before it is read
-  int32_t* overflow = chunk_counts + (size_t)n_chunks * E;  // written by k_route_scan before it is read
-  k_route_count<<<n_chunks, ROUTE_THREADS, 0, s>>>(topk_idx, n_assign, expert_begin, E, chunk_counts);
-  k_route_scan<<<1, 1024, 0, s>>>(chunk_counts, n_chunks, E, R_cap, counts, offsets, overflow, status);
-  const int scatter_smem = ROUTE_WARPS * E * (int)sizeof(int32_t);
-  if (scatter_smem > 48 * 1024 && !set_smem_limit((const void*)k_route_scatter, scatter_smem)) return MOE_ERR_CUDA;
-  k_route_scatter<<<n_chunks, ROUTE_THREADS, scatter_smem, s>>>(topk_idx, topk_prob, n_assign, k, expert_begin, E,
-                                                                 chunk_counts, offsets, overflow, row_of, tok_of,
-                                                                 prob_perm);
-  const int sms = sm_count();
-  int grid = (R_cap + 7) / 8;
-  if (grid > sms * 8) grid = sms * 8;
-  if (grid < 1) grid = 1;
-  k_permute_gather<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), H / 8, E, counts, offsets, overflow,
-                                        tok_of, prob_perm, reinterpret_cast<uint4*>(x_perm));
-  count_launch(4);
-  return launch_status();
+  // the same launch sequence as the workspace entry point, on the fixed
+  // array (every entry of it that a kernel reads is written first by an
+  // earlier kernel of the same call, so nothing needs clearing)
+  return moe_route_permute(x, topk_idx, topk_prob, T, H, k, expert_begin, E, R_cap, x_perm, row_of, tok_of, prob_perm,
+                           counts, offsets, scratch, ROUTE_STATIC_SCRATCH_BYTES, status, stream);
 }
 
 namespace moeglu {

@@ -225,7 +225,10 @@ class MoeLayer:
         with torch.cuda.stream(s):
             self.run(calls)  # warm-up outside capture (sets kernel attributes)
             torch.cuda.synchronize()
+            n0 = self.lib.moe_launch_count()
             with torch.cuda.graph(g, stream=s, capture_error_mode="global"):
                 self.run(self.step_calls(x, topk_idx, topk_prob, dOut))
+            # kernel launches recorded into the graph (one per library launch)
+            self.graph_launches = int(self.lib.moe_launch_count() - n0)
         torch.cuda.current_stream().wait_stream(s)
         return g

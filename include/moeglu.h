@@ -317,12 +317,16 @@ MOE_API moe_status_t moe_glu_act(const moe_bf16* pre, const int32_t* counts, con
  * a convenience of this library, not part of the method.
  * Same arguments, results and status semantics as moe_route_permute minus
  * ws/ws_bytes.  Its scratch is a fixed 1 MiB array inside the library
- * (moe_route_noalloc_max_scratch_bytes()), present on every GPU that loads
- * the library until the process exits; a routing whose scratch
+ * (moe_route_noalloc_max_scratch_bytes()).  The array comes into being on a
+ * GPU when the library's device code is first loaded there (with CUDA's lazy
+ * module loading: the first kernel launch or the address look-up below) and
+ * stays until the process exits; a routing whose scratch
  * (moe_route_workspace_size(T, k, E)) exceeds it returns MOE_ERR_ARG.
  * The first call on each device looks up that array's device address
- * (cudaGetSymbolAddress) with the device current; make that first call
- * before any stream capture.  All calls share the one array: calls that
+ * (cudaGetSymbolAddress) with the device current and keeps it; make that
+ * first call before any stream capture.  After cudaDeviceReset the kept
+ * address is stale: do not call this entry point on a device that has been
+ * reset in this process.  All calls share the one array: calls that
  * may run at the same time on the GPU (different streams, or several host
  * threads) race on it and must be serialised by the caller.  Nothing in the
  * array needs to start at zero: each call writes every entry it reads. */

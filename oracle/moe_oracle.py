@@ -290,6 +290,10 @@ def permute(x, rt: Routing) -> np.ndarray:
 
 
 def permute_probs(topk_prob, rt: Routing) -> np.ndarray:
+    """prob_perm[row] = p[t, j] for the assignment (t, j) placed at that row
+    (the router weight of [MegaMoE] §2.1 carried along with the permuted
+    row, so that a per-row factor can be applied to it); pad rows 0.
+    float64 [R_pad]."""
     p = np.asarray(topk_prob, dtype=np.float64).reshape(-1)
     out = np.zeros(rt.R_pad)
     real = rt.slot_of >= 0

@@ -165,22 +165,42 @@ def test_dglu_srelu():
     _dglu_case(w)
 
 
+def _sampled_blocks(rt, n_random, seed):
+    """Every expert's first and last 32-row block plus n_random blocks drawn
+    uniformly over the padded rows (interior blocks of the long segments)."""
+    blocks = {int(rt.offsets[e]) for e in range(rt.E) if rt.counts[e]} | \
+             {int(rt.offsets[e + 1]) - 32 for e in range(rt.E) if rt.counts[e]}
+    if rt.R_pad:
+        blocks |= {int(b) * 32 for b in np.random.default_rng(seed).integers(0, rt.R_pad // 32, n_random)}
+    return sorted(blocks)
+
+
 def test_dglu_dsv3_full_size_sampled():
+    """DeepSeek-V3 shard backward at full size: every expert's first and last
+    block and 16 random interior blocks."""
     w = synth.WORKLOADS["dsv3"]
     rt, _, _ = _routing(w)
-    blocks = sorted({int(rt.offsets[e]) for e in range(w.E) if rt.counts[e]} |
-                    {int(rt.offsets[e + 1]) - 32 for e in range(w.E) if rt.counts[e]})
-    _dglu_case(w, rows=blocks)
+    _dglu_case(w, rows=_sampled_blocks(rt, 16, 21))
+
+
+@pytest.mark.parametrize("name", ["skew", "skew_srelu"])
+def test_dglu_skew_full_size_sampled(name):
+    """Skewed 64-expert config at full size (T 32768, H 4096, F 1536, top-6,
+    Zipf routing: one expert holds ~97% of the tokens, 8 hold none): GeGLU
+    (gated, N1 = 2F) and sReLU (not gated, N1 = F) derivatives, MXFP8 row
+    and column outputs, on sampled blocks."""
+    w = synth.WORKLOADS[name]
+    rt, _, _ = _routing(w)
+    _dglu_case(w, rows=_sampled_blocks(rt, 12, 22))
 
 
 def test_dglu_gptoss_full_size_sampled():
     """GPT-OSS-shaped backward at full size (clamped SwiGLU derivative, F 2880
-    with a half-full last N tile); every expert's first and last 32-row block."""
+    with a half-full last N tile); every expert's first and last 32-row block
+    and random interior blocks."""
     w = synth.WORKLOADS["gptoss"]
     rt, _, _ = _routing(w)
-    blocks = sorted({int(rt.offsets[e]) for e in range(w.E) if rt.counts[e]} |
-                    {int(rt.offsets[e + 1]) - 32 for e in range(w.E) if rt.counts[e]})
-    _dglu_case(w, rows=blocks)
+    _dglu_case(w, rows=_sampled_blocks(rt, 8, 23))
 
 
 def _fc2_case(E, K, N, counts, seed, experts=None, n_cols=None):

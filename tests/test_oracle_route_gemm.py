@@ -44,6 +44,28 @@ def test_route_matches_brute_force(T, k, E, eb, nexp):
     assert (rt.tok_of >= 0).sum() == sum(counts)
 
 
+@pytest.mark.parametrize("T,k,E,eb,nexp", [(37, 2, 4, 0, 4), (50, 3, 5, 2, 9), (64, 4, 2, 1, 8)])
+def test_permute_probs_brute_force(T, k, E, eb, nexp):
+    """prob_perm walks the assignments in (t, j) order with the brute-force
+    routing: the row of (t, j) holds p[t, j]; every other row (pad rows,
+    rows of no kept assignment) holds 0.  Probabilities are distinct, so a
+    slot/token mix-up or a transposed index cannot pass."""
+    rng = np.random.default_rng(T * 7 + k)
+    idx = np.stack([rng.permutation(nexp)[:k] for _ in range(T)])
+    p = rng.permutation(T * k).reshape(T, k) / (T * k) + 0.5
+    rt = O.route(idx, eb, E)
+    _, offs, row_of = _brute_route(idx, eb, E, O.ALIGN)
+    got = O.permute_probs(p, rt)
+    assert got.shape == (offs[-1],)
+    ref = np.zeros(offs[-1])
+    for t in range(T):
+        for j in range(k):
+            r = row_of[t * k + j]
+            if r >= 0:
+                ref[r] = p[t, j]
+    assert np.array_equal(got, ref)
+
+
 def test_route_empty_expert_and_all_on_one():
     idx = np.zeros((40, 1), dtype=np.int64) + 2      # every token on expert 2
     rt = O.route(idx, 0, 4)
