@@ -391,7 +391,10 @@ struct GluParams {
 // bf16 / MXFP8 outputs, and an IEEE divide here is a large share of the
 // epilogue's instructions
 __device__ __forceinline__ float sigmoidf_(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
-__device__ __forceinline__ float phi_cdf(float z) { return 0.5f * (1.0f + erff(z * 0.70710678118654752f)); }
+// Normal CDF as erfc(-z / sqrt 2) / 2: the erfc form keeps its relative
+// precision in the negative tail, where 1 + erf(z / sqrt 2) cancels to 0 for
+// z below about -5.9 in single precision.
+__device__ __forceinline__ float phi_cdf(float z) { return 0.5f * erfcf(-z * 0.70710678118654752f); }
 __device__ __forceinline__ float phi_pdf(float z) { return 0.39894228040143268f * __expf(-0.5f * z * z); }
 
 // Short SwiGLU forms for GluParams::lean (no clamps).  sigma(alpha g) =

@@ -419,8 +419,11 @@ def _sigmoid(z):
 
 
 def _phi_cdf(z):
-    from scipy.special import erf
-    return 0.5 * (1.0 + erf(z / math.sqrt(2.0)))
+    """Standard normal CDF, Phi(z) = erfc(-z / sqrt 2) / 2 (the same function
+    as (1 + erf(z / sqrt 2)) / 2, written with erfc so that the negative tail
+    keeps full relative precision instead of cancelling against 1)."""
+    from scipy.special import erfc
+    return 0.5 * erfc(-np.asarray(z, dtype=np.float64) / math.sqrt(2.0))
 
 
 def _phi_pdf(z):

@@ -93,3 +93,19 @@ def test_gpt_oss_variant_special_values():
     assert np.allclose(O.act_fwd(u, big, GPT_OSS), O.act_fwd(u, np.full(2, 7.0), GPT_OSS))
     _, dg = O.act_bwd(u, big, np.ones(2), GPT_OSS)
     assert np.all(dg == 0)
+
+
+def test_phi_cdf_negative_tail_relative_precision():
+    """The normal CDF keeps its relative precision deep in the negative tail,
+    where (1 + erf) would cancel to 0: tabulated values of Phi and the
+    Mills-ratio asymptote Phi(z) ~ phi(z) / |z| (1 - 1/z^2 + 3/z^4)."""
+    assert math.isclose(float(O._phi_cdf(-10.0)), 7.619853024160527e-24, rel_tol=1e-12)
+    assert math.isclose(float(O._phi_cdf(-5.0)), 2.866515718791939e-07, rel_tol=1e-12)
+    for z in (-12.0, -20.0, -30.0):
+        pdf = math.exp(-0.5 * z * z) / math.sqrt(2 * math.pi)
+        approx = pdf / abs(z) * (1 - 1 / z ** 2 + 3 / z ** 4)
+        assert math.isclose(float(O._phi_cdf(z)), approx, rel_tol=15 / z ** 6)
+    # GeGLU of a deep-tail gate is tiny but not zero, and so is its derivative
+    prm = O.ActParams(O.ACT_GEGLU)
+    y = O.act_fwd(np.array([2.0]), np.array([-9.0]), prm)
+    assert y[0] < 0 and abs(y[0]) > 1e-18
