@@ -611,6 +611,29 @@ def dglu_row_prob_grad(dY_perm, W2, pre_bf16, rt: Routing, prm: ActParams, G: in
     return out
 
 
+def fc1_bias_grad(dfc1, rt: Routing) -> np.ndarray:
+    """Gradient of the FC1 bias ([MoE-Fusion], "clamping and scaling": the
+    GLU's bias vector b_e added to every row of expert e; the chain rule on
+    pre = x_perm W1p_e^T + b1p_e): dbias[e] = sum over the expert's rows of
+    dL/dpre = dFC1 (the values before any quantisation; pad rows hold 0).
+    dfc1 [R_pad, N1] -> float64 [E, N1], in dfc1's column order."""
+    d = np.asarray(dfc1, dtype=np.float64)
+    out = np.zeros((rt.E, d.shape[1]))
+    for e in range(rt.E):
+        r0, n = int(rt.offsets[e]), int(rt.counts[e])
+        out[e] = d[r0:r0 + n].sum(axis=0)
+    return out
+
+
+def grouped_gemm_quant_fwd(A, B, rt: Routing) -> np.ndarray:
+    """GroupGemm + Quantize ([MoE-Fusion], the first kernel of the fused
+    family: a grouped GEMM whose output is quantised in its epilogue).
+    y = A_e @ B_e^T per expert (pad rows 0) as handed to the quantiser: the
+    float32 value of the accumulator (quantise with mx_quantize_rows /
+    mx_quantize_cols; the bf16 output mode is bf16_round of the same y)."""
+    return grouped_gemm_rows(A, B, rt).astype(np.float32)
+
+
 def rows_to_slots(row_values, row_of, T: int, k: int) -> np.ndarray:
     """[T, k]: the value of the row each (token, slot) was routed to; 0 for
     dropped slots."""

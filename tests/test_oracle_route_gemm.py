@@ -242,3 +242,74 @@ def test_feature_scaling_gradients_against_finite_differences(act):
     slots = O.rows_to_slots(dp, rt.row_of, rt.row_of.size, 1)
     for i, r in enumerate(rt.row_of):
         assert slots[i, 0] == (dp[r] if r >= 0 else 0.0)
+
+
+@pytest.mark.parametrize("oss", [False, True])
+def test_fc1_bias_grad_against_finite_differences(oss):
+    """dL/db1p[e, c] for L = sum(dY * (act(x W1p^T + b1p_e) @ W2_e)): central
+    differences in one bias entry at a time against fc1_bias_grad of
+    dglu_bwd's dFC1 (plain SwiGLU, and the GPT-OSS form with the gate clamp,
+    alpha and the +1 offset, whose bias the gradient is for)."""
+    rng, rt, x, W1, b1, W2, dY, F, G = _toy(O.ACT_SWIGLU, seed=21)
+    prm = (O.ActParams(O.ACT_SWIGLU, alpha=1.702, up_offset=1.0, gate_lo=-7.0, gate_hi=7.0) if oss
+           else O.ActParams(O.ACT_SWIGLU))
+    xp = O.permute(x, rt)
+    W1p = O.repack_fc1(W1 * (4.0 if oss else 1.0), G)   # reach past the +-7 clamp for some rows
+    b1p = O.repack_fc1(b1[..., None], G)[..., 0]
+    W2t = np.transpose(W2, (0, 2, 1))
+
+    def pre_of(b):
+        pre = O.grouped_gemm_rows(xp, W1p, rt)
+        for e in range(rt.E):
+            r0, n = rt.offsets[e], rt.counts[e]
+            pre[r0:r0 + n] += b[e]
+        pre[rt.tok_of < 0] = 0
+        return pre
+
+    def loss(b):
+        u, g = O.unpack_glu_cols(pre_of(b), G)
+        y = O.act_fwd(u, g, prm)
+        y[rt.tok_of < 0] = 0
+        return float(np.sum(dY * O.grouped_gemm_rows(y, W2t, rt)))
+
+    pre = pre_of(b1p)
+    if oss:
+        _, g = O.unpack_glu_cols(pre, G)
+        assert (np.abs(g[rt.tok_of >= 0]) > 7).any()
+    db = O.fc1_bias_grad(O.dglu_bwd(dY, W2, pre, rt, prm, G), rt)
+    assert db.shape == b1p.shape
+    h = 1e-6
+    for e in range(rt.E):
+        for c in range(2 * F):
+            bp, bm = b1p.copy(), b1p.copy()
+            bp[e, c] += h
+            bm[e, c] -= h
+            fd = (loss(bp) - loss(bm)) / (2 * h)
+            assert abs(db[e, c] - fd) <= 1e-4 * max(1.0, abs(fd)), (e, c, db[e, c], fd)
+
+
+def test_grouped_gemm_quant_closed_form():
+    """GroupGemm + Quantize on operands whose product is a constant per expert
+    (A = 1, B_e = c_e / K): every row-wise block of expert e holds c_e, so its
+    codes and scale are the hand-worked MXFP8 values of c_e (1.0 -> scale 0x77
+    code 0x78; 448 -> 0x7F / 0x7E; 0.75 -> 0x76 / 0x7C), pad rows give scale 0
+    and code 0, and the column-wise copy of a block of 32 equal rows is the
+    same code."""
+    K, N = 64, 64
+    idx = np.repeat(np.arange(3), [40, 3, 33])[:, None]
+    rt = O.route(idx, 0, 3)
+    c = np.array([1.0, 448.0, 0.75])
+    A = np.ones((rt.R_pad, K))
+    A[rt.tok_of < 0] = 0
+    B = np.stack([np.full((N, K), ce / K) for ce in c])
+    y = O.grouped_gemm_quant_fwd(A, B, rt)
+    assert y.dtype == np.float32
+    q, s = O.mx_quantize_rows(y)
+    qc, sc = O.mx_quantize_cols(y)
+    expect = {0: (0x77, 0x78), 1: (0x7F, 0x7E), 2: (0x76, 0x7C)}
+    for e, (sb, code) in expect.items():
+        r0, n = int(rt.offsets[e]), int(rt.counts[e])
+        assert np.all(s[r0:r0 + n] == sb) and np.all(q[r0:r0 + n] == code)
+        assert np.all(s[r0 + n:int(rt.offsets[e + 1])] == 0) and np.all(q[r0 + n:int(rt.offsets[e + 1])] == 0)
+    # expert 0 rows 0..31 are all real: its first column block is 32 copies of 1.0
+    assert np.all(sc[:, 0] == 0x77) and np.all(qc[:, :32] == 0x78)
