@@ -34,6 +34,7 @@
 #include <cmath>
 
 #include "common.cuh"
+#include "epilogue.cuh"
 #include "host_common.h"
 
 namespace moeglu {
@@ -64,7 +65,10 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 enum Mode { FWD_GLU = 0, FWD_ELT = 1, FWD_PRE = 2, BWD_GLU = 3, BWD_ELT = 4, BWD_GLU_DOT = 5, BWD_ELT_DOT = 6,
             // SwiGLU with its short activation forms (GluParams::lean 1: no clamp, 2: clamped), each
             // its own instantiation so that a kernel carries only the activation code it runs
-            FWD_GLU_L1 = 7, FWD_GLU_L2 = 8, BWD_GLU_L1 = 9, BWD_GLU_L2 = 10, FWD_GLU_L3 = 11, BWD_GLU_L3 = 12 };
+            FWD_GLU_L1 = 7, FWD_GLU_L2 = 8, BWD_GLU_L1 = 9, BWD_GLU_L2 = 10, FWD_GLU_L3 = 11, BWD_GLU_L3 = 12,
+            // plain grouped GEMM whose fp32 result goes through the output stage
+            // (GroupGemm + Quantize with bf16 operands)
+            FWD_ID = 13 };
 __host__ __device__ constexpr bool is_fwd_glu(int m) {
   return m == FWD_GLU || m == FWD_GLU_L1 || m == FWD_GLU_L2 || m == FWD_GLU_L3;
 }
@@ -95,6 +99,7 @@ struct Args {
   float* amax;
   uint16_t* pre_out;
   float* row_dot;          // backward: [R_cap][2 * n_tiles_n] partials of da * act(pre), may be null
+  float* db_parts;         // backward: [R_cap / 32][N1] column sums of dFC1 per 32-row block (bias gradient), may be null
   float* rht_amax;         // backward NVFP4: amax of the transposed random Hadamard rotation, may be null
   uint32_t rht_signs;      //   its 16 signs (bit i set: -1)
   int32_t* status;
@@ -126,134 +131,6 @@ __device__ __forceinline__ Tile decode_tile(int t, const int32_t* pref, int E, i
   ti.rows_pad = ti.row0 < 0 ? 0 : max(0, min(ti.rows_pad, R_cap - ti.row0));
   ti.rows_valid = min(ti.rows_valid, ti.rows_pad);
   return ti;
-}
-
-// Running per-thread maxima of the NVFP4 mode (float bits of |v|, v >= 0):
-// plain = max |y|, rht = max |rotated y| (backward, when requested).
-struct Amax {
-  uint32_t plain, rht;
-};
-
-// One 32-column block of activation results of one row -> its outputs.
-// y: 32 fp32 values (0 on pad rows).  col0: first output column (multiple
-// of 32).  row_ok: this thread's row lies inside the padded segment.
-// The column-wise MXFP8 path needs the whole warp (the warp's 32 rows are
-// one column block).
-__device__ __forceinline__ void emit_block(const Args& a, const float* y, int col0, int row, int rb, bool row_ok,
-                                           uint8_t* scratch, int lane, Amax& amax_bits) {
-  const int N = a.out_N;
-  if (a.out_mode == MOE_OUT_MXFP8) {
-    uint32_t codes[8];
-    const uint32_t sb = mx_quant_block32(y, codes);
-    if (row_ok) {
-      uint4* dst = reinterpret_cast<uint4*>(a.q_row + (size_t)row * N + col0);
-      dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-      dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-      a.s_row[(size_t)row * (N / 32) + col0 / 32] = (uint8_t)sb;
-    }
-    if (a.q_col != nullptr) {
-      // Column blocks (one column, the warp's 32 rows), eight columns at a
-      // time through the warp's 1 KB of shared memory: row r's eight floats
-      // go to slot s(r) (r with its low two bits rotated by r / 8) with the
-      // two 16-byte halves swapped when bit 2 of the slot is set, so both the
-      // row-wise 16-byte writes and the column reads below hit 32 distinct
-      // banks.  Lane l then takes column l % 8, rows 8 (l / 8) .. +7: amax
-      // over its eight values and the three other lanes of the column, then
-      // eight codes as one 8-byte store (the column's 32 codes are one sector).
-      float* sf = reinterpret_cast<float*>(scratch);
-      const uint32_t r_w = (uint32_t)lane;
-      const uint32_t slot_w = (r_w & ~3u) | ((r_w + (r_w >> 3)) & 3u);
-      const uint32_t half_w = (slot_w >> 2) & 1u;
-      const int cc = lane & 7, rg = lane >> 3;
-#pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8) {
-        float4* dst = reinterpret_cast<float4*>(sf + slot_w * 8);
-        dst[half_w] = make_float4(y[8 * c8 + 0], y[8 * c8 + 1], y[8 * c8 + 2], y[8 * c8 + 3]);
-        dst[half_w ^ 1u] = make_float4(y[8 * c8 + 4], y[8 * c8 + 5], y[8 * c8 + 6], y[8 * c8 + 7]);
-        __syncwarp();
-        float v[8];
-        uint32_t m = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint32_t r = (uint32_t)(8 * rg + i);
-          const uint32_t sr = (r & ~3u) | ((r + (r >> 3)) & 3u);
-          v[i] = sf[sr * 8 + ((uint32_t)cc ^ (((sr >> 2) & 1u) << 2))];
-          m = max(m, abs_bits(v[i]));
-        }
-        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
-        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
-        const uint32_t sb = e8m0_from_amax_bits(m);
-        uint32_t w0 = 0x7F7F7F7Fu, w1 = 0x7F7F7F7Fu;
-        if (sb != 0xFFu) {
-          const float inv = mx_inv_scale(sb);
-          w0 = e4m3x2(v[0] * inv, v[1] * inv) | (e4m3x2(v[2] * inv, v[3] * inv) << 16);
-          w1 = e4m3x2(v[4] * inv, v[5] * inv) | (e4m3x2(v[6] * inv, v[7] * inv) << 16);
-        }
-        const size_t col = (size_t)(col0 + 8 * c8 + cc);
-        *reinterpret_cast<uint2*>(a.q_col + col * a.R_cap + rb + 8 * rg) = make_uint2(w0, w1);
-        if (rg == 0) a.s_col[col * (a.R_cap / 32) + rb / 32] = (uint8_t)sb;
-        __syncwarp();
-      }
-    }
-  } else {
-    if (row_ok) {
-      uint4* dst = reinterpret_cast<uint4*>(a.y + (size_t)row * N + col0);
-#pragma unroll
-      for (int w = 0; w < 4; ++w)
-        dst[w] = make_uint4(pack_bf16x2(y[8 * w], y[8 * w + 1]), pack_bf16x2(y[8 * w + 2], y[8 * w + 3]),
-                            pack_bf16x2(y[8 * w + 4], y[8 * w + 5]), pack_bf16x2(y[8 * w + 6], y[8 * w + 7]));
-    }
-    if (a.out_mode == MOE_OUT_NVFP4) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) amax_bits.plain = max(amax_bits.plain, abs_bits(y[i]));
-      if (a.rht_amax != nullptr) {
-        // Transposed random Hadamard rotation of the bf16 values written: the
-        // warp's rows are its lanes and a 16-row block is lanes 0-15 or 16-31,
-        // so H16 diag(s) per column is four xor-butterflies across the lanes
-        // (Sylvester order), then the 1/4 normalisation.
-        const float sg = ((a.rht_signs >> (lane & 15)) & 1u) ? -1.0f : 1.0f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float x = __bfloat162float(__float2bfloat16_rn(y[i])) * sg;
-#pragma unroll
-          for (int m = 1; m < 16; m <<= 1) {
-            const float o = __shfl_xor_sync(0xFFFFFFFFu, x, m);
-            x = (lane & m) ? (o - x) : (x + o);
-          }
-          amax_bits.rht = max(amax_bits.rht, abs_bits(x * 0.25f));
-        }
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ void load_bf16x32(const uint16_t* p, float* v) {
-  const uint4* s = reinterpret_cast<const uint4*>(p);
-#pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    const uint4 q = __ldg(s + w);
-    v[8 * w + 0] = bf16_lo(q.x);
-    v[8 * w + 1] = bf16_hi(q.x);
-    v[8 * w + 2] = bf16_lo(q.y);
-    v[8 * w + 3] = bf16_hi(q.y);
-    v[8 * w + 4] = bf16_lo(q.z);
-    v[8 * w + 5] = bf16_hi(q.z);
-    v[8 * w + 6] = bf16_lo(q.w);
-    v[8 * w + 7] = bf16_hi(q.w);
-  }
-}
-
-__device__ __forceinline__ void store_bf16x32(uint16_t* p, const float* v, bool zero) {
-  uint4* d = reinterpret_cast<uint4*>(p);
-#pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    if (zero) {
-      d[w] = make_uint4(0, 0, 0, 0);
-    } else {
-      d[w] = make_uint4(pack_bf16x2(v[8 * w], v[8 * w + 1]), pack_bf16x2(v[8 * w + 2], v[8 * w + 3]),
-                        pack_bf16x2(v[8 * w + 4], v[8 * w + 5]), pack_bf16x2(v[8 * w + 6], v[8 * w + 7]));
-    }
-  }
 }
 
 template <int MODE>
@@ -311,7 +188,7 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& ti, uin
       }
       emit_block(a, yv, f0, row, rb, row_ok, scratch, lane, amax_bits);
     }
-  } else if (MODE == FWD_ELT || MODE == FWD_PRE) {
+  } else if (MODE == FWD_ELT || MODE == FWD_PRE || MODE == FWD_ID) {
 #pragma unroll 1
     for (int j = h * (BN / 64); j < (h + 1) * (BN / 64); ++j) {
       const int c0 = ti.n_idx * BN + j * 32;
@@ -330,6 +207,12 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& ti, uin
 #pragma unroll
         for (int i = 0; i < 32; ++i) yv[i] = real ? act_fwd(a.prm, v[i], 0.0f) * rs : 0.0f;
         emit_block(a, yv, c0, row, rb, row_ok, scratch, lane, amax_bits);
+      } else if (MODE == FWD_ID) {
+        if (!real) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+        }
+        emit_block(a, v, c0, row, rb, row_ok, scratch, lane, amax_bits);
       }
     }
   } else if (is_bwd_glu(MODE)) {
@@ -391,6 +274,13 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& ti, uin
 #pragma unroll
         for (int i = 0; i < 32; ++i) u[i] = g[i] = 0.0f;
       }
+      if (a.db_parts != nullptr) {
+        // bias gradient: this block's column sums over the warp's 32 rows
+        // (pad rows hold 0), one coalesced line per 32 columns
+        float* dst = a.db_parts + (size_t)(rb / 32) * a.N1 + p0 + lane;
+        dst[0] = warp_column_sum32(u, lane);
+        dst[32] = warp_column_sum32(g, lane);
+      }
       emit_block(a, u, p0, row, rb, row_ok, scratch, lane, amax_bits);
       emit_block(a, g, p0 + 32, row, rb, row_ok, scratch, lane, amax_bits);
     }
@@ -420,6 +310,7 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& ti, uin
 #pragma unroll
         for (int i = 0; i < 32; ++i) x[i] = 0.0f;
       }
+      if (a.db_parts != nullptr) a.db_parts[(size_t)(rb / 32) * a.N1 + f0 + lane] = warp_column_sum32(x, lane);
       emit_block(a, x, f0, row, rb, row_ok, scratch, lane, amax_bits);
     }
     if (DOT) a.row_dot[(size_t)row * (2 * a.n_tiles_n) + ti.n_idx * 2 + h] = dot;
@@ -1028,11 +919,38 @@ extern "C" moe_status_t moe_grouped_fc1_glu_quant_fwd(const moe_bf16* x_perm, co
   return launch<FWD_ELT>(x_perm, W1p, a, sm_margin, as_stream(stream));
 }
 
+namespace moeglu {
+// Bias gradient from the dGLU epilogue's partials: dbias[e][c] = sum over the
+// expert's 32-row blocks, in block order, of parts[block][c] (fp32; 0 for an
+// expert without rows).  One thread per (expert, column); a routing that
+// overflowed R_cap (no GEMM tile ran) gives zeros.
+__global__ void __launch_bounds__(256) k_bias_grad(const float* __restrict__ parts, const int32_t* __restrict__ offsets,
+                                                   int E, int N1, int R_cap, float* __restrict__ dbias) {
+  const bool over = __ldg(offsets + E) > R_cap;
+  const long long n = (long long)E * N1;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const int e = (int)(i / N1), c = (int)(i - (long long)e * N1);
+    float s = 0.0f;
+    if (!over) {
+      const int b0 = __ldg(offsets + e) / 32, b1 = __ldg(offsets + e + 1) / 32;
+      for (int b = b0; b < b1; ++b) s += __ldg(parts + (size_t)b * N1 + c);
+    }
+    dbias[i] = s;
+  }
+}
+}  // namespace moeglu
+
+extern "C" size_t moe_grouped_dglu_workspace_size(int N1, int R_cap) {
+  if (N1 <= 0 || R_cap <= 0) return 0;
+  return ((size_t)(R_cap / 32) * N1 * sizeof(float) + 255) & ~(size_t)255;
+}
+
 extern "C" moe_status_t moe_grouped_dglu_quant_bwd(const moe_bf16* dY_perm, const moe_bf16* W2, const moe_bf16* pre,
                                                    const float* row_scale, const int32_t* counts,
                                                    const int32_t* offsets, int E, int H, int F, int R_cap,
                                                    const moe_glu_params_t* params, int out_mode,
-                                                   const moe_act_out_t* dfc1, int sm_margin, int32_t* status,
+                                                   const moe_act_out_t* dfc1, float* dbias, void* ws,
+                                                   size_t ws_bytes, int sm_margin, int32_t* status,
                                                    moe_stream_t stream) {
   using namespace g16;
   if (!dY_perm || !W2 || !pre || !counts || !offsets || !params || !dfc1) return MOE_ERR_ARG;
@@ -1072,15 +990,68 @@ extern "C" moe_status_t moe_grouped_dglu_quant_bwd(const moe_bf16* dY_perm, cons
   a.rht_signs = dfc1->rht_signs;
   a.status = status;
   a.wait_ns = g_wait_limit_ns.load();
-  if (a.row_dot != nullptr) {
-    if (gated) return launch<BWD_GLU_DOT>(dY_perm, W2, a, sm_margin, as_stream(stream));
-    return launch<BWD_ELT_DOT>(dY_perm, W2, a, sm_margin, as_stream(stream));
+  if (dbias != nullptr) {
+    // the epilogue writes one column-sum line per 32-row block into ws
+    if (!ws || ws_bytes < moe_grouped_dglu_workspace_size(a.N1, R_cap) || (reinterpret_cast<uintptr_t>(ws) & 15))
+      return MOE_ERR_ARG;
+    a.db_parts = static_cast<float*>(ws);
   }
-  if (gated && a.prm.lean == 1) return launch<BWD_GLU_L1>(dY_perm, W2, a, sm_margin, as_stream(stream));
-  if (gated && a.prm.lean == 2) return launch<BWD_GLU_L2>(dY_perm, W2, a, sm_margin, as_stream(stream));
-  if (gated && a.prm.lean == 3) return launch<BWD_GLU_L3>(dY_perm, W2, a, sm_margin, as_stream(stream));
-  if (gated) return launch<BWD_GLU>(dY_perm, W2, a, sm_margin, as_stream(stream));
-  return launch<BWD_ELT>(dY_perm, W2, a, sm_margin, as_stream(stream));
+  cudaStream_t st = as_stream(stream);
+  moe_status_t rc;
+  if (a.row_dot != nullptr)
+    rc = gated ? launch<BWD_GLU_DOT>(dY_perm, W2, a, sm_margin, st) : launch<BWD_ELT_DOT>(dY_perm, W2, a, sm_margin, st);
+  else if (gated && a.prm.lean == 1)
+    rc = launch<BWD_GLU_L1>(dY_perm, W2, a, sm_margin, st);
+  else if (gated && a.prm.lean == 2)
+    rc = launch<BWD_GLU_L2>(dY_perm, W2, a, sm_margin, st);
+  else if (gated && a.prm.lean == 3)
+    rc = launch<BWD_GLU_L3>(dY_perm, W2, a, sm_margin, st);
+  else
+    rc = gated ? launch<BWD_GLU>(dY_perm, W2, a, sm_margin, st) : launch<BWD_ELT>(dY_perm, W2, a, sm_margin, st);
+  if (rc != MOE_OK || dbias == nullptr) return rc;
+  const long long n = (long long)E * a.N1;
+  long long grid = (n + 255) / 256;
+  if (grid > (long long)sm_count() * 8) grid = (long long)sm_count() * 8;
+  k_bias_grad<<<(int)grid, 256, 0, st>>>(a.db_parts, offsets, E, a.N1, R_cap, dbias);
+  count_launch();
+  return launch_status();
+}
+
+// Plain grouped GEMM y[rows of e] = A[rows] . W[e]^T with bf16 operands
+// (A [R_cap][K], W [E][N][K]) through the fused output stage (bf16, MXFP8
+// row + column-wise, or bf16 + NVFP4 amax); the bf16 case of
+// moe_grouped_fc2_fwd.  Arguments are checked by the caller except the ones
+// this kernel adds (K % 64).
+moe_status_t moeglu::grouped_gemm_bf16_out(const void* A, const void* W, const int32_t* counts, const int32_t* offsets,
+                                           int E, int K, int N, int R_cap, int out_mode, const moe_act_out_t* out,
+                                           int sm_margin, int32_t* status, cudaStream_t stream) {
+  using namespace g16;
+  if (E > E_MAX || (K % BK) || (R_cap % BM)) return MOE_ERR_ARG;
+  if (!aligned16(A) || !aligned16(W)) return MOE_ERR_ARG;
+  if (!out_ok(out_mode, out) || out->rht_amax != nullptr || out->pre != nullptr || out->row_dot != nullptr)
+    return MOE_ERR_ARG;
+  Args a{};
+  a.counts = counts;
+  a.offsets = offsets;
+  a.E = E;
+  a.K = K;
+  a.F = N;
+  a.N1 = N;
+  a.N_gemm = N;
+  a.R_cap = R_cap;
+  a.n_tiles_n = (N + BN - 1) / BN;
+  a.out_N = N;
+  a.prm = GluParams{};
+  a.out_mode = out_mode;
+  a.q_row = out->q_row;
+  a.s_row = out->s_row;
+  a.q_col = out->q_col;
+  a.s_col = out->s_col;
+  a.y = reinterpret_cast<uint16_t*>(out->y);
+  a.amax = out->amax;
+  a.status = status;
+  a.wait_ns = g_wait_limit_ns.load();
+  return launch<FWD_ID>(A, W, a, sm_margin, stream);
 }
 
 extern "C" int moe_dglu_row_dot_parts(int F) { return F > 0 ? 2 * ((F + g16::BN - 1) / g16::BN) : 0; }

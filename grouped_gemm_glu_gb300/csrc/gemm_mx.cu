@@ -33,6 +33,7 @@
 // one (each stage is written once by TMA and read once by the tensor core).
 // Every wait is bounded (MOE_ERR_TIMEOUT + early exit, never a trap).
 #include "common.cuh"
+#include "epilogue.cuh"
 #include "host_common.h"
 
 namespace moeglu {
@@ -92,6 +93,18 @@ struct Args {
   int out_f32;
   int32_t* status;
   uint64_t wait_ns;
+  // M-grouped quantised outputs (GroupGemm + Quantize), read by emit_block:
+  // out_mode MOE_OUT_MXFP8 writes q_row/s_row (+ q_col/s_col), MOE_OUT_NVFP4
+  // writes y (bf16) and the amax; MOE_OUT_BF16 keeps the staged bf16 path
+  int out_mode, out_N;
+  uint8_t* q_row;
+  uint8_t* s_row;
+  uint8_t* q_col;
+  uint8_t* s_col;
+  uint16_t* y;
+  float* amax;
+  float* rht_amax;         // always null here (the rotated amax belongs to the dGLU backward)
+  uint32_t rht_signs;
 };
 
 // Prefix in shared memory: M-grouped -> 128-row tiles per expert (from
@@ -376,7 +389,7 @@ __device__ __forceinline__ void store_pass_tma(const CUtensorMap* tmO, const Til
 // ---------------------------------------------------------------------------
 // The GEMM
 // ---------------------------------------------------------------------------
-template <bool TS>
+template <bool TS, bool QUANT>
 __global__ void __launch_bounds__(THREADS, 1)
     k_grouped_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmO, const Args a) {
@@ -524,6 +537,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int q = warp & 3, h = warp >> 2;
     uint8_t* stg = epi_all + warp * EPI_WARP_BYTES;
     const int out_es = (a.kgrouped && a.out_f32) ? 4 : 2;  // output element size
+    Amax amax_bits{0u, 0u};
     int lt = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
       const int buf = 0;
@@ -536,6 +550,42 @@ __global__ void __launch_bounds__(THREADS, 1)
       const Tile ti = decode(t, pref, a);
       const bool live = q * 32 < ti.rows_pad && ti.n0 + h * 128 < a.N;
       const bool real = q * 32 + lane < ti.rows_valid;
+      if (QUANT) {
+        // GroupGemm + Quantize (M-grouped only): the thread's row, 32 columns
+        // at a time, as MXFP8 row-wise codes (+ the column-wise copy through
+        // the warp's staging buffer) or bf16 plus the NVFP4 amax.  The 128
+        // columns are drained in two halves of 64 (the epilogue warps have
+        // 168 registers), and the accumulator is released once the second
+        // half is in registers.
+        const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * 128);
+        const int r_local = q * 32 + lane;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          float v[64];
+          if (live) {
+            tmem_ld32(tbase + half * 64, v);
+            tmem_ld32(tbase + half * 64 + 32, v + 32);
+          }
+          if (half == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty + buf);
+          }
+          if (!live) continue;
+          if (!real) {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) v[i] = 0.0f;
+          }
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int col0 = ti.n0 + h * 128 + half * 64 + 32 * j;
+            if (col0 < a.N)
+              emit_block(a, v + 32 * j, col0, ti.m0 + r_local, ti.m0 + q * 32, r_local < ti.rows_pad, stg, lane,
+                         amax_bits);
+          }
+        }
+        continue;
+      }
       float v[128];
       if (live && ti.num_kb > 0)
         tmem_ld128(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * 128), v);
@@ -563,6 +613,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
     if (TS && lane == 0) bulk_wait_all();
+    if (QUANT && a.out_mode == MOE_OUT_NVFP4 && a.amax != nullptr) {
+      const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, amax_bits.plain);
+      if (lane == 0 && m != 0) atomicMax(reinterpret_cast<int*>(a.amax), (int)m);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -575,7 +629,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 static moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap* tmO, const Args& a,
                            long long tiles_bound, long long sf_items, int sm_margin, cudaStream_t stream) {
   const bool ts = tmO != nullptr;
-  const void* kfn = ts ? (const void*)k_grouped_mx<true> : (const void*)k_grouped_mx<false>;
+  const bool quant = !ts && a.out_mode != MOE_OUT_BF16;
+  const void* kfn = ts      ? (const void*)k_grouped_mx<true, false>
+                    : quant ? (const void*)k_grouped_mx<false, true>
+                            : (const void*)k_grouped_mx<false, false>;
   const int smem = ts ? Lay<true>::SMEM_BYTES : Lay<false>::SMEM_BYTES;
   if (!set_smem_limit(kfn, smem)) return MOE_ERR_CUDA;
   const int sms = sm_count();
@@ -587,9 +644,11 @@ static moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const
   if (grid > tiles_bound) grid = (int)tiles_bound;
   if (grid < 1) grid = 1;
   if (ts)
-    k_grouped_mx<true><<<grid, THREADS, smem, stream>>>(tmA, tmB, *tmO, a);
+    k_grouped_mx<true, false><<<grid, THREADS, smem, stream>>>(tmA, tmB, *tmO, a);
+  else if (quant)
+    k_grouped_mx<false, true><<<grid, THREADS, smem, stream>>>(tmA, tmB, tmA, a);
   else
-    k_grouped_mx<false><<<grid, THREADS, smem, stream>>>(tmA, tmB, tmA, a);
+    k_grouped_mx<false, false><<<grid, THREADS, smem, stream>>>(tmA, tmB, tmA, a);
   count_launch(2);
   return launch_status();
 }
@@ -631,17 +690,36 @@ extern "C" size_t moe_grouped_wgrad_workspace_size(int E, int M, int N, int R_ca
   return a + b;
 }
 
-extern "C" moe_status_t moe_grouped_fc2_fwd(const uint8_t* Aq, const uint8_t* As, const uint8_t* Wq,
-                                            const uint8_t* Ws, const int32_t* counts, const int32_t* offsets, int E,
-                                            int K, int N, int R_cap, moe_bf16* y, void* ws, size_t ws_bytes,
-                                            int sm_margin, int32_t* status, moe_stream_t stream) {
+extern "C" moe_status_t moe_grouped_fc2_fwd(const moe_in_t* A, const moe_in_t* W, const int32_t* counts,
+                                            const int32_t* offsets, int E, int K, int N, int R_cap, int out_mode,
+                                            const moe_act_out_t* out, void* ws, size_t ws_bytes, int sm_margin,
+                                            int32_t* status, moe_stream_t stream) {
   using namespace gmx;
-  if (!Aq || !As || !Wq || !Ws || !counts || !offsets || !y || !ws) return MOE_ERR_ARG;
+  if (!A || !W || !A->data || !W->data || !counts || !offsets || !out) return MOE_ERR_ARG;
   if (E <= 0 || E > E_MAX || K <= 0 || (K % 32) || N <= 0 || (N % 32) || R_cap <= 0 || (R_cap % BM))
     return MOE_ERR_ARG;
-  if (!aligned16(Aq) || !aligned16(Wq) || !aligned16(y) || (reinterpret_cast<uintptr_t>(As) & 3) ||
-      (reinterpret_cast<uintptr_t>(Ws) & 3) || (reinterpret_cast<uintptr_t>(ws) & 255) || sm_margin < 0)
+  if (sm_margin < 0 || A->dtype != W->dtype) return MOE_ERR_ARG;  // one operand type per MMA
+  if (out_mode != MOE_OUT_BF16 && out_mode != MOE_OUT_MXFP8 && out_mode != MOE_OUT_NVFP4) return MOE_ERR_ARG;
+  if (out->pre || out->row_dot || out->rht_amax) return MOE_ERR_ARG;
+  if (A->dtype == MOE_IN_BF16)
+    return grouped_gemm_bf16_out(A->data, W->data, counts, offsets, E, K, N, R_cap, out_mode, out, sm_margin, status,
+                                 as_stream(stream));
+  if (A->dtype != MOE_IN_MXFP8) return MOE_ERR_ARG;
+  const uint8_t* Aq = static_cast<const uint8_t*>(A->data);
+  const uint8_t* Wq = static_cast<const uint8_t*>(W->data);
+  const uint8_t* As = A->scale;
+  const uint8_t* Ws = W->scale;
+  if (!As || !Ws || !ws) return MOE_ERR_ARG;
+  if (!aligned16(Aq) || !aligned16(Wq) || (reinterpret_cast<uintptr_t>(As) & 3) ||
+      (reinterpret_cast<uintptr_t>(Ws) & 3) || (reinterpret_cast<uintptr_t>(ws) & 255))
     return MOE_ERR_ARG;
+  if (out_mode == MOE_OUT_MXFP8) {
+    if (!out->q_row || !out->s_row || (out->q_col == nullptr) != (out->s_col == nullptr)) return MOE_ERR_ARG;
+    if (!aligned16(out->q_row) || (out->q_col && !aligned16(out->q_col))) return MOE_ERR_ARG;
+  } else {
+    if (!out->y || !aligned16(out->y)) return MOE_ERR_ARG;
+    if (out_mode == MOE_OUT_NVFP4 && !out->amax) return MOE_ERR_ARG;
+  }
   size_t a_bytes, b_bytes;
   fc2_ws_parts(E, K, N, R_cap, &a_bytes, &b_bytes);
   if (ws_bytes < a_bytes + b_bytes) return MOE_ERR_ARG;
@@ -677,10 +755,18 @@ extern "C" moe_status_t moe_grouped_fc2_fwd(const uint8_t* Aq, const uint8_t* As
   a.Bs = Ws;
   a.sfa_t = static_cast<uint8_t*>(ws);
   a.sfb_t = static_cast<uint8_t*>(ws) + a_bytes;
-  a.out = y;
+  a.out = out->y;
   a.out_f32 = 0;
   a.status = status;
   a.wait_ns = g_wait_limit_ns.load();
+  a.out_mode = out_mode;
+  a.out_N = N;
+  a.q_row = out->q_row;
+  a.s_row = out->s_row;
+  a.q_col = out->q_col;
+  a.s_col = out->s_col;
+  a.y = reinterpret_cast<uint16_t*>(out->y);
+  a.amax = out->amax;
   const long long mt_bound = (long long)R_cap / BM + E;
   const long long bound = mt_bound * a.n_tiles_n;
   const long long sf_items = mt_bound * a.KB + (long long)E * 2 * a.n_tiles_n * a.KB;

@@ -9,7 +9,8 @@ Backward: (from dOut, the gradient at the layer output)
           -> FC2-data-grad GroupGemm+dActivation+Quantize/Transpose (dFC1)
           -> MXFP8 cast of W1p (transposed) -> dX_perm = dFC1 . W1p
           -> column-wise MXFP8 of x_perm and dY_perm
-          -> weight gradients dW1p = dFC1^T x, dW2 = a^T dY (per expert)
+          -> weight gradients dW1p = dFC1^T x, dW2 = a^T dY (per expert),
+             and the FC1 bias gradient db1 (per expert column sums of dFC1)
           -> permute backward (dx[t] = sum of its rows of dX_perm)
 
 Weight layouts: W1 [E][2F][H] (rows: input | gate; repacked once into W1p),
@@ -88,6 +89,19 @@ class MoeLayer:
         self.ws_dx = ws(lib.moe_grouped_fc2_workspace_size(E, N1, H, R_cap))
         self.ws_wg1 = ws(lib.moe_grouped_wgrad_workspace_size(E, N1, H, R_cap))
         self.ws_wg2 = ws(lib.moe_grouped_wgrad_workspace_size(E, F, H, R_cap))
+        # FC1 bias gradient (packed order, like b1p) when the layer has a bias
+        self.db1, self.ws_db, self.ws_db_bytes = None, None, 0
+        if self.b1p is not None:
+            self.db1 = z(E, N1, dt=torch.float32)
+            self.ws_db_bytes = lib.moe_grouped_dglu_workspace_size(N1, R_cap)
+            self.ws_db = z(self.ws_db_bytes, dt=u8)
+        # operands and outputs of the two block-scaled M-grouped GEMMs
+        self.fc2_a = L.in_operand(self.a_q.data_ptr(), self.a_s.data_ptr())
+        self.fc2_w = L.in_operand(self.W2q.data_ptr(), self.W2s.data_ptr())
+        self.fc2_out = L.ActOut(None, None, None, None, self.y_perm.data_ptr(), None, None)
+        self.dx_a = L.in_operand(self.d_q.data_ptr(), self.d_s.data_ptr())
+        self.dx_w = L.in_operand(self.W1q.data_ptr(), self.W1s.data_ptr())
+        self.dx_out = L.ActOut(None, None, None, None, self.dX_perm.data_ptr(), None, None)
         self.fc1_out = L.ActOut(self.a_q.data_ptr(), self.a_s.data_ptr(), self.a_qc.data_ptr(),
                                 self.a_sc.data_ptr(), None, None, self.pre.data_ptr())
         self.bwd_out = L.ActOut(self.d_q.data_ptr(), self.d_s.data_ptr(), self.d_qc.data_ptr(),
@@ -109,8 +123,8 @@ class MoeLayer:
             ("quant_w2", lambda: lib.moe_quantize_mxfp8(
                 _p(self.W2), E, F, H, 1, None, None, 0, _p(self.W2q), _p(self.W2s), st, s)),
             ("fc2", lambda: lib.moe_grouped_fc2_fwd(
-                _p(self.a_q), _p(self.a_s), _p(self.W2q), _p(self.W2s), _p(self.counts), _p(self.offsets), E, F,
-                H, R, _p(self.y_perm), _p(self.ws_fc2), self.ws_fc2.numel(), self.sm_margin, st, s)),
+                C.byref(self.fc2_a), C.byref(self.fc2_w), _p(self.counts), _p(self.offsets), E, F, H, R,
+                L.OUT_BF16, C.byref(self.fc2_out), _p(self.ws_fc2), self.ws_fc2.numel(), self.sm_margin, st, s)),
             ("combine", lambda: lib.moe_unpermute_combine(
                 _p(self.y_perm), _p(self.row_of), _p(topk_prob), T, H, k, _p(self.out), st, s)),
         ]
@@ -126,12 +140,13 @@ class MoeLayer:
                 T, H, k, E, R, _p(dY_perm), _p(self.dprob), st, s)),
             ("dglu_quant", lambda: lib.moe_grouped_dglu_quant_bwd(
                 _p(dY_perm), _p(self.W2), _p(self.pre), None, _p(self.counts), _p(self.offsets), E, H, F, R,
-                C.byref(self.params), L.OUT_MXFP8, C.byref(self.bwd_out), self.sm_margin, st, s)),
+                C.byref(self.params), L.OUT_MXFP8, C.byref(self.bwd_out), _p(self.db1), _p(self.ws_db),
+                self.ws_db_bytes, self.sm_margin, st, s)),
             ("quant_w1", lambda: lib.moe_quantize_mxfp8(
                 _p(self.W1p), E, N1, H, 1, None, None, 0, _p(self.W1q), _p(self.W1s), st, s)),
             ("dx", lambda: lib.moe_grouped_fc2_fwd(
-                _p(self.d_q), _p(self.d_s), _p(self.W1q), _p(self.W1s), _p(self.counts), _p(self.offsets), E, N1,
-                H, R, _p(self.dX_perm), _p(self.ws_dx), self.ws_dx.numel(), self.sm_margin, st, s)),
+                C.byref(self.dx_a), C.byref(self.dx_w), _p(self.counts), _p(self.offsets), E, N1, H, R,
+                L.OUT_BF16, C.byref(self.dx_out), _p(self.ws_dx), self.ws_dx.numel(), self.sm_margin, st, s)),
             ("quant_x_col", lambda: lib.moe_quantize_mxfp8(
                 _p(self.x_perm), 1, R, H, 1, _p(self.counts), _p(self.offsets), E, _p(self.x_qc), _p(self.x_sc), st, s)),
             ("quant_dy_col", lambda: lib.moe_quantize_mxfp8(

@@ -31,6 +31,18 @@ class ActOut(C.Structure):
                 ("rht_amax", C.c_void_p), ("rht_signs", C.c_uint32)]
 
 
+IN_BF16, IN_MXFP8 = 0, 1
+
+
+class InT(C.Structure):
+    _fields_ = [("dtype", C.c_int32), ("data", C.c_void_p), ("scale", C.c_void_p)]
+
+
+def in_operand(data_ptr: int, scale_ptr: int | None = None) -> InT:
+    """A GEMM operand: bf16 when scale_ptr is None, else MXFP8 codes + scales."""
+    return InT(IN_BF16 if scale_ptr is None else IN_MXFP8, data_ptr, scale_ptr)
+
+
 def glu_params(act: str = "swiglu", alpha: float = 1.0, up_offset: float = 0.0,
                gate_lo: float = -math.inf, gate_hi: float = math.inf,
                up_lo: float = -math.inf, up_hi: float = math.inf) -> GluParams:
@@ -44,10 +56,12 @@ _SIGS = {
     "moe_route_workspace_size": ([I, I, I], SZ),
     "moe_route_permute": [P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P, SZ, P, P],
     "moe_grouped_fc1_glu_quant_fwd": [P, P, P, P, P, P, I, I, I, I, C.POINTER(GluParams), I, C.POINTER(ActOut), I, P, P],
-    "moe_grouped_dglu_quant_bwd": [P, P, P, P, P, P, I, I, I, I, C.POINTER(GluParams), I, C.POINTER(ActOut), I, P, P],
+    "moe_grouped_dglu_quant_bwd": [P, P, P, P, P, P, I, I, I, I, C.POINTER(GluParams), I, C.POINTER(ActOut), P, P, SZ,
+                                   I, P, P],
+    "moe_grouped_dglu_workspace_size": ([I, I], SZ),
     "moe_quantize_mxfp8": [P, I, I, I, I, P, P, I, P, P, P, P],
     "moe_grouped_fc2_workspace_size": ([I, I, I, I], SZ),
-    "moe_grouped_fc2_fwd": [P, P, P, P, P, P, I, I, I, I, P, P, SZ, I, P, P],
+    "moe_grouped_fc2_fwd": [C.POINTER(InT), C.POINTER(InT), P, P, I, I, I, I, I, C.POINTER(ActOut), P, SZ, I, P, P],
     "moe_grouped_wgrad_workspace_size": ([I, I, I, I], SZ),
     "moe_grouped_wgrad": [P, P, P, P, P, P, I, I, I, I, P, I, P, SZ, I, P, P],
     "moe_unpermute_combine": [P, P, P, I, I, I, P, P, P],

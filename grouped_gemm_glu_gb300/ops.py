@@ -120,12 +120,15 @@ def fc1_fwd(x_perm, W1p, counts, offsets, F: int, params: L.GluParams, out_mode:
 
 def dglu_bwd(dY_perm, W2, pre, counts, offsets, F: int, params: L.GluParams, out_mode: int = L.OUT_MXFP8,
              row_scale=None, with_col: bool = True, sm_margin: int = 0, status=None,
-             out: dict | None = None, row_dot: bool = False, rht_signs: int | None = None) -> dict:
+             out: dict | None = None, row_dot: bool = False, rht_signs: int | None = None,
+             dbias: bool = False) -> dict:
     """GroupGemm + dActivation + Quantize/Transpose.  dFC1 in packed order;
     row_dot=True also returns o["row_dot"], the per-row partials of the
     feature-scale gradient (reduce with feature_scale_grad).  NVFP4 mode
     returns y and amax (max |y|); with rht_signs (16-bit mask) also
-    o["rht_amax"], the amax of y's transposed random Hadamard rotation."""
+    o["rht_amax"], the amax of y's transposed random Hadamard rotation.
+    dbias=True also returns o["dbias"] [E, N1] f32, the FC1 bias gradient
+    (packed column order)."""
     lib = L.load()
     dev = _dev(dY_perm)
     R_cap, H = dY_perm.shape
@@ -151,9 +154,14 @@ def dglu_bwd(dY_perm, W2, pre, counts, offsets, F: int, params: L.GluParams, out
     ao.row_dot = o["row_dot"].data_ptr() if "row_dot" in o else None
     if "rht_amax" in o:
         ao.rht_amax, ao.rht_signs = o["rht_amax"].data_ptr(), int(rht_signs) & 0xFFFF
+    ws_bytes, ws = 0, None
+    if dbias:
+        o.setdefault("dbias", torch.empty(E, N1, dtype=torch.float32, device=dev))
+        ws_bytes = lib.moe_grouped_dglu_workspace_size(N1, R_cap)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     L.check(lib.moe_grouped_dglu_quant_bwd(_p(dY_perm), _p(W2), _p(pre), _p(row_scale), _p(counts), _p(offsets),
-                                           E, H, F, R_cap, C.byref(params), out_mode, C.byref(ao), sm_margin,
-                                           _p(st), _s()),
+                                           E, H, F, R_cap, C.byref(params), out_mode, C.byref(ao), _p(o.get("dbias")),
+                                           _p(ws), ws_bytes, sm_margin, _p(st), _s()),
             "moe_grouped_dglu_quant_bwd")
     o["status"] = st
     return o
@@ -180,20 +188,41 @@ def quantize_mxfp8(src, col: bool = False, counts=None, offsets=None, out=None, 
     return q, s
 
 
-def fc2_fwd(Aq, As, Wq, Ws, counts, offsets, sm_margin: int = 0, status=None, out=None):
-    """y [R_cap, N] bf16 = block-scaled grouped GEMM of MXFP8 A [R_cap, K]
-    and per-expert MXFP8 W [E, N, K]."""
+def fc2_fwd(Aq, As, Wq, Ws, counts, offsets, sm_margin: int = 0, status=None, out=None,
+            out_mode: int = L.OUT_BF16, with_col: bool = True):
+    """GroupGemm (+ Quantize): y [R_cap, N] = A [R_cap, K] . W[e]^T per expert
+    with W [E, N, K].  MXFP8 operands (codes Aq/Wq with E8M0 scales As/Ws),
+    or bf16 operands when As and Ws are None.  out_mode OUT_BF16 returns the
+    bf16 tensor y; OUT_MXFP8 returns {q_row, s_row[, q_col, s_col]};
+    OUT_NVFP4 returns {y, amax}."""
     lib = L.load()
     dev = _dev(Aq)
     R_cap, K = Aq.shape
     E, N, _ = Wq.shape
-    y = out if out is not None else torch.empty(R_cap, N, dtype=torch.bfloat16, device=dev)
+    if (As is None) != (Ws is None):
+        raise ValueError("both operands bf16 (no scales) or both MXFP8")
+    o = {}
+    if out_mode == L.OUT_BF16:
+        o["y"] = out if out is not None else torch.empty(R_cap, N, dtype=torch.bfloat16, device=dev)
+    elif out_mode == L.OUT_MXFP8:
+        o["q_row"] = torch.empty(R_cap, N, dtype=torch.uint8, device=dev)
+        o["s_row"] = torch.empty(R_cap, N // 32, dtype=torch.uint8, device=dev)
+        if with_col:
+            o["q_col"] = torch.empty(N, R_cap, dtype=torch.uint8, device=dev)
+            o["s_col"] = torch.empty(N, R_cap // 32, dtype=torch.uint8, device=dev)
+    else:
+        o["y"] = torch.empty(R_cap, N, dtype=torch.bfloat16, device=dev)
+        o["amax"] = torch.zeros(1, dtype=torch.float32, device=dev)
     st = status if status is not None else new_status(dev)
-    ws_bytes = lib.moe_grouped_fc2_workspace_size(E, K, N, R_cap)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    L.check(lib.moe_grouped_fc2_fwd(_p(Aq), _p(As), _p(Wq), _p(Ws), _p(counts), _p(offsets), E, K, N, R_cap,
-                                    _p(y), _p(ws), ws_bytes, sm_margin, _p(st), _s()), "moe_grouped_fc2_fwd")
-    return y
+    a_in = L.in_operand(Aq.data_ptr(), None if As is None else As.data_ptr())
+    w_in = L.in_operand(Wq.data_ptr(), None if Ws is None else Ws.data_ptr())
+    ws_bytes = lib.moe_grouped_fc2_workspace_size(E, K, N, R_cap) if As is not None else 0
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    ao = _act_out(o.get("q_row"), o.get("s_row"), o.get("q_col"), o.get("s_col"), o.get("y"), o.get("amax"))
+    L.check(lib.moe_grouped_fc2_fwd(C.byref(a_in), C.byref(w_in), _p(counts), _p(offsets), E, K, N, R_cap, out_mode,
+                                    C.byref(ao), _p(ws), ws_bytes, sm_margin, _p(st), _s()), "moe_grouped_fc2_fwd")
+    o["status"] = st
+    return o["y"] if out_mode == L.OUT_BF16 else o
 
 
 def wgrad(Aq_col, As_col, Bq_col, Bs_col, counts, offsets, out_f32: bool = False, sm_margin: int = 0,

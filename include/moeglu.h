@@ -126,6 +126,18 @@ typedef struct {
   uint32_t rht_signs;/*   the 16 signs s of that rotation: bit i set -> s_i = -1 (drawn by the caller) */
 } moe_act_out_t;
 
+/* Operand of a grouped GEMM that takes either precision. */
+typedef enum {
+  MOE_IN_BF16 = 0,  /* bf16 values */
+  MOE_IN_MXFP8 = 1  /* E4M3 codes with E8M0 scales, one per 32 elements along K */
+} moe_in_dtype_t;
+
+typedef struct {
+  int32_t dtype;          /* moe_in_dtype_t */
+  const void* data;       /* the values (bf16) or codes (E4M3) */
+  const uint8_t* scale;   /* MOE_IN_MXFP8 only: the E8M0 scales */
+} moe_in_t;
+
 /* ---------------------------------------------------------------------- */
 
 /* FC1 weight repack ([MoE-Fusion], "Optimizing GLU via fused GEMM
@@ -185,14 +197,27 @@ MOE_API moe_status_t moe_grouped_fc1_glu_quant_fwd(const moe_bf16* x_perm, const
  * padded segments, partial sums of da * act(pre) over disjoint column
  * ranges (fp32, each slot written once: deterministic), the ingredients of
  * the feature-scale gradient ([MoE-Fusion] "clamping and scaling").
+ * dbias (nullable, f32 [E][N1], packed column order like b1p): the gradient
+ * of the FC1 bias ([MoE-Fusion] "clamping and scaling": the bias vector of
+ * the GLU), dbias[e][c] = sum over the expert's rows of dFC1[r][c] taken on
+ * the fp32 values before quantisation.  The epilogue writes one column-sum
+ * line per 32-row block into ws (moe_grouped_dglu_workspace_size(N1, R_cap)
+ * bytes, 16-byte aligned; unused and may be NULL when dbias is NULL) and a
+ * second kernel adds each expert's lines in block order (deterministic; 0
+ * for an expert without rows).
  * H % 64 == 0. */
 MOE_API moe_status_t moe_grouped_dglu_quant_bwd(const moe_bf16* dY_perm, const moe_bf16* W2,
                                         const moe_bf16* pre, const float* row_scale,
                                         const int32_t* counts, const int32_t* offsets,
                                         int E, int H, int F, int R_cap,
                                         const moe_glu_params_t* params, int out_mode,
-                                        const moe_act_out_t* dfc1, int sm_margin,
+                                        const moe_act_out_t* dfc1, float* dbias,
+                                        void* ws, size_t ws_bytes, int sm_margin,
                                         int32_t* status, moe_stream_t stream);
+
+/* Bytes of device workspace moe_grouped_dglu_quant_bwd needs for the bias
+ * gradient (N1 = 2F gated, F for sReLU). */
+MOE_API size_t moe_grouped_dglu_workspace_size(int N1, int R_cap);
 
 /* MXFP8 quantisation of a bf16 tensor (the standalone quantize/transpose
  * kernel of the unfused path, and the weight cast).  src [G][R][C] bf16,
@@ -209,24 +234,36 @@ MOE_API moe_status_t moe_quantize_mxfp8(const moe_bf16* src, int G, int R, int C
                                 const int32_t* counts, const int32_t* offsets, int E,
                                 uint8_t* q, uint8_t* s, int32_t* status, moe_stream_t stream);
 
-/* Bytes of device workspace moe_grouped_fc2_fwd needs (the scales of the
- * visited tiles, rewritten in the order the tensor cores read them). */
+/* Bytes of device workspace moe_grouped_fc2_fwd needs with MXFP8 operands
+ * (the scales of the visited tiles, rewritten in the order the tensor cores
+ * read them); bf16 operands need none. */
 MOE_API size_t moe_grouped_fc2_workspace_size(int E, int K, int N, int R_cap);
 
-/* GroupGemm (+ bf16 out), block-scaled MXFP8 ([MoE-Fusion] GroupGemm +
- * Quantize family; [MegaMoE] §2.3: C ~ (A_q/s_A)(B_q/s_B)).
- * y[rows of e] = dequant(Aq,As)[rows] . dequant(Wq[e],Ws[e])^T, fp32
- * accumulate, bf16 out; pad rows 0.  Serves FC2 (K = F, N = H) and the
- * data-gradient GEMM dX = dFC1 . W1p (K = N1, N = H).
- * Aq [R_cap][K], As [R_cap][K/32], Wq [E][N][K], Ws [E][N][K/32].
- * ws: moe_grouped_fc2_workspace_size() bytes, 256-byte aligned.
- * K % 32 == 0, N % 32 == 0 (a partial last 128-wide k-block or 256-wide
- * column tile is handled; e.g. the GPT-OSS shapes K = N = 2880). */
-MOE_API moe_status_t moe_grouped_fc2_fwd(const uint8_t* Aq, const uint8_t* As,
-                                 const uint8_t* Wq, const uint8_t* Ws,
+/* GroupGemm + Quantize ([MoE-Fusion] "Boosting MoE Training Throughput with
+ * Advanced Fusion Kernels": the first of the three fused kernels, a grouped
+ * GEMM whose epilogue quantises its output; [MegaMoE] §2.3: block-scaled
+ * FP8, C ~ (A_q/s_A)(B_q/s_B)).
+ * y[rows of e] = A[rows] . W[e]^T, fp32 accumulate, pad rows 0, written per
+ * out_mode from the fp32 accumulator: MOE_OUT_BF16 (out->y), MOE_OUT_MXFP8
+ * (out->q_row/s_row, plus the column-wise copy out->q_col/s_col when
+ * non-NULL: blocks of 32 rows of one column, as for the fused FC1), or
+ * MOE_OUT_NVFP4 (out->y bf16 and out->amax, caller zeroes it).
+ * out->pre, row_dot and rht_amax must be NULL.
+ * Serves FC2 (K = F, N = H) and the data-gradient GEMM dX = dFC1 . W1p
+ * (K = N1, N = H).
+ * Operands: A [R_cap][K], W [E][N][K] (K contiguous in both), the same
+ * dtype for both (the tensor cores take one operand type per MMA):
+ *   MOE_IN_MXFP8: E4M3 codes, scale = E8M0 [R_cap][K/32] / [E][N][K/32]
+ *                 (4-byte aligned); block-scaled MMA (kind::mxf8f6f4);
+ *                 ws = moe_grouped_fc2_workspace_size() bytes, 256-byte
+ *                 aligned.  K % 32 == 0, N % 32 == 0 (a partial last
+ *                 128-wide k-block or 256-wide column tile is handled).
+ *   MOE_IN_BF16:  bf16, scale unused; kind::f16 MMA; ws unused (may be
+ *                 NULL).  K % 64 == 0, N % 32 == 0. */
+MOE_API moe_status_t moe_grouped_fc2_fwd(const moe_in_t* A, const moe_in_t* W,
                                  const int32_t* counts, const int32_t* offsets,
-                                 int E, int K, int N, int R_cap,
-                                 moe_bf16* y, void* ws, size_t ws_bytes,
+                                 int E, int K, int N, int R_cap, int out_mode,
+                                 const moe_act_out_t* out, void* ws, size_t ws_bytes,
                                  int sm_margin, int32_t* status, moe_stream_t stream);
 
 /* Bytes of device workspace moe_grouped_wgrad needs. */

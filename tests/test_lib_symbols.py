@@ -46,8 +46,12 @@ def test_argument_validation_needs_no_device(lib):
                                              ctypes.byref(prm), 1, ctypes.byref(out), 0, None, None) == L.MOE_ERR_ARG
     assert lib.moe_wait_selftest(0, None, None, None) == L.MOE_ERR_ARG
     assert lib.moe_quantize_mxfp8(None, 1, 32, 32, 0, None, None, 0, None, None, None, None) == L.MOE_ERR_ARG
-    assert lib.moe_grouped_fc2_fwd(None, None, None, None, None, None, 4, 512, 256, 1152, None, None, 0, 0, None,
+    assert lib.moe_grouped_fc2_fwd(None, None, None, None, 4, 512, 256, 1152, 0, None, None, 0, 0, None,
                                    None) == L.MOE_ERR_ARG
+    # mixed operand types (one bf16, one MXFP8) are rejected: one type per MMA
+    a_bf, w_mx = L.in_operand(0x10000), L.in_operand(0x10000, 0x20000)
+    assert lib.moe_grouped_fc2_fwd(ctypes.byref(a_bf), ctypes.byref(w_mx), 0x10000, 0x10000, 4, 512, 256, 1152, 0,
+                                   ctypes.byref(out), None, 0, 0, None, None) == L.MOE_ERR_ARG
     assert lib.moe_grouped_wgrad(None, None, None, None, None, None, 4, 512, 256, 1152, None, 0, None, 0, 0, None,
                                  None) == L.MOE_ERR_ARG
     # shape and alignment rules are host checks too (these addresses are never dereferenced)
