@@ -143,6 +143,68 @@ __device__ __forceinline__ void store_bf16x32(uint16_t* p, const float* v, bool 
   }
 }
 
+// Transposed output stage, for tiles whose accumulator holds one output
+// column per thread and 32 consecutive rows rb .. rb+31 in c[0..31] (the
+// lanes of the warp are 32 consecutive columns, col - lane .. col - lane + 31).
+// Row-wise MXFP8 blocks are the warp's 32 columns of one row (amax by a warp
+// max), column-wise blocks are the thread's own 32 values.  The outputs are
+// the same as emit_block's for the same values (codes decided from fp32 with
+// the same scale rule); rows rb .. rb+31 must lie inside the padded segment.
+template <class Out>
+__device__ __forceinline__ void emit_block_t(const Out& a, const float* c, int col, int rb, int lane, Amax& amax_bits) {
+  const int N = a.out_N;
+  if (a.out_mode == MOE_OUT_MXFP8) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, abs_bits(c[j]));
+      const uint32_t sb = e8m0_from_amax_bits(m);
+      const uint32_t code = sb == 0xFFu ? 0x7Fu : (e4m3x2(c[j] * mx_inv_scale(sb), 0.0f) & 0xFFu);
+      a.q_row[(size_t)(rb + j) * N + col] = (uint8_t)code;
+      if (lane == 0) a.s_row[(size_t)(rb + j) * (N / 32) + (col - lane) / 32] = (uint8_t)sb;
+    }
+    if (a.q_col != nullptr) {
+      uint32_t codes[8];
+      const uint32_t sb = mx_quant_block32(c, codes);
+      uint4* dst = reinterpret_cast<uint4*>(a.q_col + (size_t)col * a.R_cap + rb);
+      dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+      dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+      a.s_col[(size_t)col * (a.R_cap / 32) + rb / 32] = (uint8_t)sb;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      a.y[(size_t)(rb + j) * N + col] = __bfloat16_as_ushort(__float2bfloat16_rn(c[j]));
+    if (a.out_mode == MOE_OUT_NVFP4) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) amax_bits.plain = max(amax_bits.plain, abs_bits(c[j]));
+      if (a.rht_amax != nullptr) {
+        // transposed random Hadamard rotation of the bf16 values written:
+        // the 16-row blocks are this thread's c[0..15] and c[16..31], so
+        // H16 diag(s) is an in-register butterfly (Sylvester order), then /4
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          float x[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            x[i] = __bfloat162float(__float2bfloat16_rn(c[16 * b + i])) * (((a.rht_signs >> i) & 1u) ? -1.0f : 1.0f);
+#pragma unroll
+          for (int m = 1; m < 16; m <<= 1) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              if (i & m) continue;
+              const float lo = x[i], hi = x[i + m];
+              x[i] = lo + hi;
+              x[i + m] = lo - hi;
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) amax_bits.rht = max(amax_bits.rht, abs_bits(x[i] * 0.25f));
+        }
+      }
+    }
+  }
+}
+
 // Column sums of a warp's 32 x 32 block (lane = row, x[c] = column c of the
 // lane's row): returns, in lane c, the sum over the 32 rows of column c.  A
 // reduce-scatter by halving (the lanes that differ in bit m swap the halves

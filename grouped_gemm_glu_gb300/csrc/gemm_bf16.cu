@@ -100,6 +100,7 @@ struct Args {
   uint16_t* pre_out;
   float* row_dot;          // backward: [R_cap][2 * n_tiles_n] partials of da * act(pre), may be null
   float* db_parts;         // backward: [R_cap / 32][N1] column sums of dFC1 per 32-row block (bias gradient), may be null
+  int swap_max;            // pair kernel: an expert's last pair tile with at most this many rows runs swapped (0: never)
   float* rht_amax;         // backward NVFP4: amax of the transposed random Hadamard rotation, may be null
   uint32_t rht_signs;      //   its 16 signs (bit i set: -1)
   int32_t* status;
@@ -108,6 +109,10 @@ struct Args {
 
 struct Tile {
   int e, m_idx, n_idx, row0, rows_valid, rows_pad;
+  // swapped tail tile (CTA-pair kernel): the expert's last pair tile holds at
+  // most Args::swap_max rows, so it is computed transposed, weights as the
+  // M = 256 operand and its nt (a multiple of 32) rows as N
+  int swap, nt, tail0, tail_valid;
 };
 
 __device__ __forceinline__ Tile decode_tile(int t, const int32_t* pref, int E, int n_tiles_n,
@@ -130,6 +135,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const int32_t* pref, int E, i
   // never touch rows at or past R_cap, whatever counts/offsets hold
   ti.rows_pad = ti.row0 < 0 ? 0 : max(0, min(ti.rows_pad, R_cap - ti.row0));
   ti.rows_valid = min(ti.rows_valid, ti.rows_pad);
+  ti.swap = ti.nt = ti.tail0 = ti.tail_valid = 0;
   return ti;
 }
 
@@ -529,7 +535,7 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 // Tile t of the pair sequence: expert e, N tile, 256-row pair tile mp; this
 // CTA's half starts 128 * rank rows further.
 __device__ __forceinline__ Tile decode_pair(int t, const int32_t* pref, int E, int n_tiles_n, const int32_t* counts,
-                                            const int32_t* offsets, int R_cap, int rank) {
+                                            const int32_t* offsets, int R_cap, int rank, int swap_max) {
   int lo = 0, hi = E - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -548,13 +554,170 @@ __device__ __forceinline__ Tile decode_pair(int t, const int32_t* pref, int E, i
   ti.rows_pad = max(0, min(BM, ((cnt + 31) & ~31) - base));
   ti.rows_pad = ti.row0 < 0 ? 0 : max(0, min(ti.rows_pad, R_cap - ti.row0));
   ti.rows_valid = min(ti.rows_valid, ti.rows_pad);
+  // the expert's last pair tile, when thin, runs swapped: its rows become
+  // the N operand (nt = rows rounded up to 32, inside the padded segment)
+  const int tail = cnt - ti.m_idx * 2 * BM;
+  ti.tail0 = __ldg(offsets + lo) + ti.m_idx * 2 * BM;
+  ti.tail_valid = max(0, min(tail, 2 * BM));
+  ti.nt = min((ti.tail_valid + 31) & ~31, ti.tail0 < 0 ? 0 : (R_cap - ti.tail0) & ~31);
+  ti.swap = (tail > 0 && tail <= swap_max && ti.nt >= 32) ? 1 : 0;
   return ti;
+}
+
+// Named barrier of the two epilogue warps (lane quarters q and q + 1 of one
+// column half) that share a swapped forward tile's input and gate columns.
+__device__ __forceinline__ void pair_warps_sync(int id) { asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory"); }
+
+// Epilogue of a swapped tail tile.  This CTA's accumulator lane i holds GEMM
+// column n_idx * BN + rank * BN/2 + i, and accumulator column j holds row
+// tail0 + j (j < nt).  Warp (q, h) takes the columns of lane quarter q and
+// the 32-row groups h, h + 2, ...; each thread then owns one column and 32
+// consecutive rows, emitted through the transposed output stage.  Forward
+// GLU: lane quarters 2i (input) and 2i + 1 (gate) hold the two halves of one
+// packed 64-column block, so the gate warp hands its values to the input
+// warp through their shared 2 KB of scratch.
+template <int MODE>
+__device__ __forceinline__ void epilogue_swapped(const Args& a, const Tile& ti, uint32_t tacc, int q, int h, int lane,
+                                                 int rank, uint8_t* pair_scratch, Amax& amax_bits) {
+  const int colbase = ti.n_idx * BN + rank * (BN / 2) + q * 32;  // first GEMM column of this warp
+  const int ngroups = ti.nt / 32;
+  if (colbase >= a.N_gemm) return;  // a multiple of 64 (gated) or 32: whole warp pairs drop out together
+  const int col = colbase + lane;
+  if (is_fwd_glu(MODE)) {
+    const bool gate_warp = (q & 1) != 0;
+    const int bar_id = 1 + h * 2 + (q >> 1);
+    const float bias = a.bias != nullptr ? bf16_lo(__ldg(a.bias + (size_t)ti.e * a.N1 + col)) : 0.0f;
+    float* xs = reinterpret_cast<float*>(pair_scratch);  // 16 rows x 32 lanes
+    const int f = (colbase / 64) * 32 + lane;           // output column (input warp)
+#pragma unroll 1
+    for (int tg = h; tg < ngroups; tg += 2) {
+      const int rb = ti.tail0 + tg * 32;
+      const int nvalid = min(32, ti.tail_valid - tg * 32);
+      float v[32];
+      tmem_ld32(tacc + tg * 32, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = j < nvalid ? v[j] + bias : 0.0f;
+      if (a.pre_out != nullptr) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          a.pre_out[(size_t)(rb + j) * a.N1 + col] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
+      }
+      float g[32];
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        pair_warps_sync(bar_id);  // the input warp has read the previous half
+        if (gate_warp) {
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) xs[jj * 32 + lane] = v[16 * hf + jj];
+        }
+        pair_warps_sync(bar_id);
+        if (!gate_warp) {
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) g[16 * hf + jj] = xs[jj * 32 + lane];
+        }
+      }
+      if (gate_warp) continue;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {  // the activation in place of the input half
+        const float rs = (a.row_scale != nullptr && j < nvalid) ? __ldg(a.row_scale + rb + j) : 1.0f;
+        float yy;
+        if (lean_of(MODE) == 1)
+          yy = swiglu_fwd_lean(a.prm, v[j], g[j]);
+        else if (lean_of(MODE) == 2)
+          yy = swiglu_fwd_lean_clamped(a.prm, v[j], g[j]);
+        else if (lean_of(MODE) == 3)
+          yy = geglu_fwd_lean(a.prm, v[j], g[j]);
+        else
+          yy = act_fwd(a.prm, v[j], g[j]);
+        v[j] = j < nvalid ? yy * rs : 0.0f;
+      }
+      emit_block_t(a, v, f, rb, lane, amax_bits);
+    }
+    // the scratch goes back to the two warps' own use only after the input
+    // warp has read the last half
+    pair_warps_sync(bar_id);
+  } else if (MODE == FWD_ELT || MODE == FWD_PRE || MODE == FWD_ID) {
+    const float bias = a.bias != nullptr ? bf16_lo(__ldg(a.bias + (size_t)ti.e * a.N1 + col)) : 0.0f;
+#pragma unroll 1
+    for (int tg = h; tg < ngroups; tg += 2) {
+      const int rb = ti.tail0 + tg * 32;
+      const int nvalid = min(32, ti.tail_valid - tg * 32);
+      float v[32];
+      tmem_ld32(tacc + tg * 32, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = j < nvalid ? v[j] + bias : 0.0f;
+      if (a.pre_out != nullptr) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          a.pre_out[(size_t)(rb + j) * a.N1 + col] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
+      }
+      if (MODE == FWD_ELT) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float rs = (a.row_scale != nullptr && j < nvalid) ? __ldg(a.row_scale + rb + j) : 1.0f;
+          v[j] = j < nvalid ? act_fwd(a.prm, v[j], 0.0f) * rs : 0.0f;
+        }
+      }
+      if (MODE != FWD_PRE) emit_block_t(a, v, col, rb, lane, amax_bits);
+    }
+  } else {  // backward (the DOT instantiations never run swapped)
+    const bool gated = is_bwd_glu(MODE);
+    const int pu = gated ? (colbase / 32) * 64 + lane : col;  // packed input column (or the column itself)
+#pragma unroll 1
+    for (int tg = h; tg < ngroups; tg += 2) {
+      const int rb = ti.tail0 + tg * 32;
+      const int nvalid = min(32, ti.tail_valid - tg * 32);
+      float u[32], g[32];  // u: da on load, then d(input) in place
+      tmem_ld32(tacc + tg * 32, u);
+      const uint16_t* pp = a.pre_in + (size_t)rb * a.N1 + pu;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float dj = u[j];
+        u[j] = g[j] = 0.0f;
+        if (j < nvalid) {
+          const float rs = a.row_scale != nullptr ? __ldg(a.row_scale + rb + j) : 1.0f;
+          const float dy = dj * rs;
+          const float uu = __uint_as_float((uint32_t)__ldg(pp + (size_t)j * a.N1) << 16);
+          float du, dg;
+          if (gated) {
+            const float gg = __uint_as_float((uint32_t)__ldg(pp + (size_t)j * a.N1 + 32) << 16);
+            if (lean_of(MODE) == 1)
+              swiglu_bwd_lean(a.prm, uu, gg, dy, du, dg);
+            else if (lean_of(MODE) == 2)
+              swiglu_bwd_lean_clamped(a.prm, uu, gg, dy, du, dg);
+            else if (lean_of(MODE) == 3)
+              geglu_bwd_lean(a.prm, uu, gg, dy, du, dg);
+            else
+              act_bwd(a.prm, uu, gg, dy, du, dg);
+          } else {
+            act_bwd(a.prm, uu, 0.0f, dy, du, dg);
+          }
+          u[j] = du;
+          g[j] = dg;
+        }
+      }
+      if (a.db_parts != nullptr) {
+        float su = 0.0f, sg = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          su += u[j];
+          sg += g[j];
+        }
+        float* dst = a.db_parts + (size_t)(rb / 32) * a.N1 + pu;
+        dst[0] = su;
+        if (gated) dst[32] = sg;
+      }
+      emit_block_t(a, u, pu, rb, lane, amax_bits);
+      if (gated) emit_block_t(a, g, pu + 32, rb, lane, amax_bits);
+    }
+  }
 }
 
 template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
     k_grouped_bf16_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA32,
-                        const __grid_constant__ CUtensorMap tmB, const Args a) {
+                        const __grid_constant__ CUtensorMap tmA16, const __grid_constant__ CUtensorMap tmB,
+                        const Args a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* tiles = smem;
@@ -589,6 +752,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
     fence_async_shared();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmA32);
+    tma_prefetch_desc(&tmA16);
     tma_prefetch_desc(&tmB);
   }
   if (warp == MMA_WARP) {
@@ -632,17 +796,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       for (int t = cl; t < total; t += ncl) {
-        const Tile ti = decode_pair(t, pref, E, a.n_tiles_n, a.counts, a.offsets, a.R_cap, (int)rank);
+        const Tile ti = decode_pair(t, pref, E, a.n_tiles_n, a.counts, a.offsets, a.R_cap, (int)rank, a.swap_max);
         // Only the 32-row blocks of A inside the expert's padded segment are
         // fetched: the rows past it (the second half of an expert's last pair
-        // tile, mostly) feed accumulator rows the epilogue never reads, so a
-        // thin tail tile costs little more than its weight bytes.  The
+        // tile, mostly) feed accumulator rows the epilogue never reads.  A
+        // swapped tile loads this CTA's 128 weight rows into the A slot and
+        // its half of the tile's nt rows (16-row boxes) into the B slot.  The
         // leader's barrier expects both CTAs' bytes.
         const int a_blk = (ti.rows_pad + 31) / 32;
         uint32_t tx = 0;
         if (rank == 0) {
-          const Tile tp = decode_pair(t, pref, E, a.n_tiles_n, a.counts, a.offsets, a.R_cap, 1);
-          tx = (uint32_t)(a_blk + (tp.rows_pad + 31) / 32) * (32 * BK * 2) + 2u * pair::B_HALF;
+          if (ti.swap) {
+            tx = 2u * pair::B_HALF + (uint32_t)ti.nt * (BK * 2);
+          } else {
+            const Tile tp = decode_pair(t, pref, E, a.n_tiles_n, a.counts, a.offsets, a.R_cap, 1, a.swap_max);
+            tx = (uint32_t)(a_blk + (tp.rows_pad + 31) / 32) * (32 * BK * 2) + 2u * pair::B_HALF;
+          }
         }
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
@@ -654,7 +823,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
           uint8_t* a_dst = tiles + s * pair::STAGE_BYTES;
           const uint32_t bar_lead = mapa_shared(smem_u32(full + s), 0);
           if (rank == 0) mbar_arrive_expect_tx(full + s, tx);
-          if (a_blk == BM / 32) {
+          if (ti.swap) {
+            tma_load_3d_pair(a_dst, &tmB, bar_lead, kb * BK, ti.n_idx * BN + (int)rank * (BN / 2), ti.e);
+            const int half = ti.nt / 2;
+            for (int i = 0; i < half / 16; ++i)
+              tma_load_2d_pair(a_dst + A_TILE + i * (16 * BK * 2), &tmA16, bar_lead, kb * BK,
+                               ti.tail0 + (int)rank * half + 16 * i);
+          } else if (a_blk == BM / 32) {
             tma_load_2d_pair(a_dst, &tmA, bar_lead, kb * BK, ti.row0);
           } else {
             for (int i = 0; i < a_blk; ++i)
@@ -678,6 +853,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
       for (int t = cl; t < total; t += ncl, ++lt) {
         const int buf = lt & 1;
         const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
+        // a swapped tile multiplies the weight rows (A slot) by its nt rows
+        // (B slot): M = 256, N = nt
+        const Tile ti = decode_pair(t, pref, E, a.n_tiles_n, a.counts, a.offsets, a.R_cap, 0, a.swap_max);
+        const uint32_t id_t = ti.swap ? idesc_bf16_f32(2 * BM, ti.nt) : idesc;
         if (!mbar_wait(acc_empty + buf, aph ^ 1u, guard)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
@@ -692,7 +871,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
           const uint32_t b_addr = a_addr + A_TILE;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
-            umma_bf16_pair(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32), sdesc_kmajor_sw128(b_addr + k * 32), idesc,
+            umma_bf16_pair(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32), sdesc_kmajor_sw128(b_addr + k * 32), id_t,
                            (kb | k) != 0 ? 1u : 0u);
           }
           tc_commit_pair_mc(empty + stage, 0x3);
@@ -722,9 +901,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const Tile ti = decode_pair(t, pref, E, a.n_tiles_n, a.counts, a.offsets, a.R_cap, (int)rank);
+      const Tile ti = decode_pair(t, pref, E, a.n_tiles_n, a.counts, a.offsets, a.R_cap, (int)rank, a.swap_max);
       const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
-      epilogue_tile<MODE>(a, ti, tacc, q, h, lane, scratch, amax_bits);
+      if (ti.swap)
+        epilogue_swapped<MODE>(a, ti, tacc, q, h, lane, (int)rank, scratch_all + (warp & ~1) * SCRATCH_PER_WARP,
+                               amax_bits);
+      else
+        epilogue_tile<MODE>(a, ti, tacc, q, h, lane, scratch, amax_bits);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(acc_empty + buf), 0));
@@ -749,7 +932,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
 
 template <int MODE>
 static moe_status_t launch_pair(const void* A, const void* B, const Args& args, int sm_margin, cudaStream_t stream) {
-  CUtensorMap tmA, tmA32, tmB;
+  CUtensorMap tmA, tmA32, tmA16, tmB;
   {
     const uint64_t dims[2] = {(uint64_t)args.K, (uint64_t)args.R_cap};
     const uint64_t strides[1] = {(uint64_t)args.K * 2};
@@ -759,6 +942,10 @@ static moe_status_t launch_pair(const void* A, const void* B, const Args& args, 
       return MOE_ERR_CUDA;
     const uint32_t box32[2] = {BK, 32};
     if (!encode_tmap(&tmA32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, dims, strides, box32,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+      return MOE_ERR_CUDA;
+    const uint32_t box16[2] = {BK, 16};
+    if (!encode_tmap(&tmA16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, dims, strides, box16,
                      CU_TENSOR_MAP_SWIZZLE_128B))
       return MOE_ERR_CUDA;
   }
@@ -779,7 +966,11 @@ static moe_status_t launch_pair(const void* A, const void* B, const Args& args, 
   const long long tiles_bound = ((long long)args.R_cap / (2 * BM) + args.E) * args.n_tiles_n;
   if (clusters > tiles_bound) clusters = (int)tiles_bound;
   if (clusters < 1) clusters = 1;
-  k_grouped_bf16_pair<MODE><<<2 * clusters, pair::THREADS, pair::SMEM_BYTES, stream>>>(tmA, tmA32, tmB, args);
+  // thin expert tails run swapped, except in the feature-scale modes (their
+  // per-row partials are laid out for the regular tile)
+  Args a2 = args;
+  a2.swap_max = (MODE == BWD_GLU_DOT || MODE == BWD_ELT_DOT) ? 0 : g_tail_swap_rows.load();
+  k_grouped_bf16_pair<MODE><<<2 * clusters, pair::THREADS, pair::SMEM_BYTES, stream>>>(tmA, tmA32, tmA16, tmB, a2);
   count_launch();
   return launch_status();
 }

@@ -12,6 +12,7 @@ namespace moeglu {
 std::atomic<uint64_t> g_launches{0};
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_cta_pairs{1};
+std::atomic<int> g_tail_swap_rows{64};
 
 int max_active_pairs(const void* kernel, int threads, int smem_bytes) {
   static std::mutex mu;
@@ -132,3 +133,9 @@ extern "C" void moe_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? 
 extern "C" uint64_t moe_launch_count(void) { return g_launches.load(); }
 
 extern "C" void moe_set_cta_pairs(int enable) { g_cta_pairs.store(enable ? 1 : 0); }
+
+extern "C" moe_status_t moe_set_tail_swap(int max_rows) {
+  if (max_rows < 0 || max_rows > 128 || (max_rows % 32)) return MOE_ERR_ARG;
+  g_tail_swap_rows.store(max_rows);
+  return MOE_OK;
+}

@@ -17,6 +17,7 @@ namespace moeglu {
 extern std::atomic<uint64_t> g_launches;  // kernels launched by this library
 extern std::atomic<uint64_t> g_wait_limit_ns;
 extern std::atomic<int> g_cta_pairs;  // bf16 GEMMs on CTA pairs (cta_group::2)
+extern std::atomic<int> g_tail_swap_rows;  // pair GEMMs: swapped tail tiles of at most this many rows
 
 inline void count_launch(int n = 1) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 

@@ -78,6 +78,7 @@ _SIGS = {
     "moe_set_wait_limit_ns": ([U64], None),
     "moe_wait_selftest": [I, P, P, P],
     "moe_set_cta_pairs": ([I], None),
+    "moe_set_tail_swap": [I],
     "moe_launch_count": ([], U64),
 }
 

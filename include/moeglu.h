@@ -411,6 +411,16 @@ MOE_API moe_status_t moe_wait_selftest(int arrive, int32_t* status, uint64_t* wa
  * 128 x 256 tile.  Both compute the same results.  Process-wide. */
 MOE_API void moe_set_cta_pairs(int enable);
 
+/* Tail tiles of the CTA-pair bf16 GEMMs (FC1 forward, dGLU backward, the
+ * bf16 case of moe_grouped_fc2_fwd): an expert whose last 256-row pair tile
+ * holds at most max_rows rows computes that tile transposed (the weights as
+ * the M = 256 operand, the tile's rows rounded up to 32 as N), so the
+ * tensor cores do not multiply the empty rows of a mostly empty tile.  The
+ * results are the same as the regular tile's (the bias-gradient partials
+ * add their 32 rows in another order).  max_rows in {0 (off), 32, 64, 96,
+ * 128}, default 64; anything else returns MOE_ERR_ARG.  Process-wide. */
+MOE_API moe_status_t moe_set_tail_swap(int max_rows);
+
 /* Cumulative number of kernels this library has launched in this process
  * (launch accounting for benchmarks). */
 MOE_API uint64_t moe_launch_count(void);
