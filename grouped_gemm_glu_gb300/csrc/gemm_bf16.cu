@@ -829,13 +829,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
             for (int i = 0; i < half / 16; ++i)
               tma_load_2d_pair(a_dst + A_TILE + i * (16 * BK * 2), &tmA16, bar_lead, kb * BK,
                                ti.tail0 + (int)rank * half + 16 * i);
-          } else if (a_blk == BM / 32) {
-            tma_load_2d_pair(a_dst, &tmA, bar_lead, kb * BK, ti.row0);
           } else {
-            for (int i = 0; i < a_blk; ++i)
-              tma_load_2d_pair(a_dst + i * (32 * BK * 2), &tmA32, bar_lead, kb * BK, ti.row0 + 32 * i);
+            if (a_blk == BM / 32) {
+              tma_load_2d_pair(a_dst, &tmA, bar_lead, kb * BK, ti.row0);
+            } else {
+              for (int i = 0; i < a_blk; ++i)
+                tma_load_2d_pair(a_dst + i * (32 * BK * 2), &tmA32, bar_lead, kb * BK, ti.row0 + 32 * i);
+            }
+            tma_load_3d_pair(a_dst + A_TILE, &tmB, bar_lead, kb * BK, ti.n_idx * BN + (int)rank * (BN / 2), ti.e);
           }
-          tma_load_3d_pair(a_dst + A_TILE, &tmB, bar_lead, kb * BK, ti.n_idx * BN + (int)rank * (BN / 2), ti.e);
           if (++stage == pair::STAGES) {
             stage = 0;
             phase ^= 1u;

@@ -105,6 +105,12 @@ struct Args {
   float* amax;
   float* rht_amax;         // always null here (the rotated amax belongs to the dGLU backward)
   uint32_t rht_signs;
+  // MXFP8-input FC1 (EPI_GLU*, EPI_ELT): N = N1 GEMM columns (packed when
+  // gated), out_N = F outputs
+  const uint16_t* bias;    // [E][N1] bf16 or null
+  const float* row_scale;  // [R_cap] or null
+  uint16_t* pre_out;       // [R_cap][N1] bf16 or null
+  GluParams prm;
 };
 
 // Prefix in shared memory: M-grouped -> 128-row tiles per expert (from
@@ -389,7 +395,14 @@ __device__ __forceinline__ void store_pass_tma(const CUtensorMap* tmO, const Til
 // ---------------------------------------------------------------------------
 // The GEMM
 // ---------------------------------------------------------------------------
-template <bool TS, bool QUANT>
+// Epilogue kinds of the M-grouped instantiations (TS = false): plain bf16
+// rows, the quantising output stage (GroupGemm + Quantize), and the fused
+// activation of the MXFP8-input FC1 (GroupGemm + Activation +
+// Quantize/Transpose) with the activation forms of the bf16 kernel.
+enum Epi { EPI_BF16 = 0, EPI_QUANT = 1, EPI_GLU = 2, EPI_GLU_L1 = 3, EPI_GLU_L2 = 4, EPI_GLU_L3 = 5, EPI_ELT = 6 };
+__host__ __device__ constexpr bool epi_glu(int k) { return k >= EPI_GLU && k <= EPI_GLU_L3; }
+
+template <bool TS, int EPI>
 __global__ void __launch_bounds__(THREADS, 1)
     k_grouped_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmO, const Args a) {
@@ -550,7 +563,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const Tile ti = decode(t, pref, a);
       const bool live = q * 32 < ti.rows_pad && ti.n0 + h * 128 < a.N;
       const bool real = q * 32 + lane < ti.rows_valid;
-      if (QUANT) {
+      if (EPI == EPI_QUANT) {
         // GroupGemm + Quantize (M-grouped only): the thread's row, 32 columns
         // at a time, as MXFP8 row-wise codes (+ the column-wise copy through
         // the warp's staging buffer) or bf16 plus the NVFP4 amax.  The 128
@@ -586,6 +599,75 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         continue;
       }
+      if (epi_glu(EPI) || EPI == EPI_ELT) {
+        // FC1 on MXFP8 operands: the warp's 128 accumulator columns are two
+        // packed 64-column blocks (32 input + 32 gate columns each; or 64
+        // plain columns without a gate), drained one block at a time; bias,
+        // saved bf16 pre-activation, activation (times the row scale), then
+        // the output stage on the fp32 results.  The accumulator is released
+        // once the second block is in registers.
+        const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * 128);
+        const int r_local = q * 32 + lane;
+        const int row = ti.m0 + r_local;
+        const bool row_ok = r_local < ti.rows_pad;
+        const float rs = (a.row_scale != nullptr && real) ? __ldg(a.row_scale + row) : 1.0f;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          float v[64];
+          if (live) {
+            tmem_ld32(tbase + half * 64, v);
+            tmem_ld32(tbase + half * 64 + 32, v + 32);
+          }
+          if (half == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty + buf);
+          }
+          const int p0 = ti.n0 + h * 128 + half * 64;  // first GEMM column of the block
+          if (!live || p0 >= a.N) continue;
+          if (a.bias != nullptr) {
+            float b[32];
+            const uint16_t* bp = a.bias + (size_t)ti.e * a.N + p0;
+            load_bf16x32(bp, b);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] += b[i];
+            load_bf16x32(bp + 32, b);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[32 + i] += b[i];
+          }
+          if (a.pre_out != nullptr && row_ok) {
+            uint16_t* pp = a.pre_out + (size_t)row * a.N + p0;
+            store_bf16x32(pp, v, !real);
+            store_bf16x32(pp + 32, v + 32, !real);
+          }
+          if (epi_glu(EPI)) {
+            float yv[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              float y;
+              if (EPI == EPI_GLU_L1)
+                y = swiglu_fwd_lean(a.prm, v[i], v[32 + i]);
+              else if (EPI == EPI_GLU_L2)
+                y = swiglu_fwd_lean_clamped(a.prm, v[i], v[32 + i]);
+              else if (EPI == EPI_GLU_L3)
+                y = geglu_fwd_lean(a.prm, v[i], v[32 + i]);
+              else
+                y = act_fwd(a.prm, v[i], v[32 + i]);
+              yv[i] = real ? y * rs : 0.0f;
+            }
+            emit_block(a, yv, p0 / 2, row, ti.m0 + q * 32, row_ok, stg, lane, amax_bits);
+          } else {
+#pragma unroll
+            for (int bk = 0; bk < 2; ++bk) {
+              float yv[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) yv[i] = real ? act_fwd(a.prm, v[32 * bk + i], 0.0f) * rs : 0.0f;
+              emit_block(a, yv, p0 + 32 * bk, row, ti.m0 + q * 32, row_ok, stg, lane, amax_bits);
+            }
+          }
+        }
+        continue;
+      }
       float v[128];
       if (live && ti.num_kb > 0)
         tmem_ld128(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * 128), v);
@@ -613,7 +695,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
     if (TS && lane == 0) bulk_wait_all();
-    if (QUANT && a.out_mode == MOE_OUT_NVFP4 && a.amax != nullptr) {
+    if (EPI != EPI_BF16 && a.out_mode == MOE_OUT_NVFP4 && a.amax != nullptr) {
       const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, amax_bits.plain);
       if (lane == 0 && m != 0) atomicMax(reinterpret_cast<int*>(a.amax), (int)m);
     }
@@ -626,13 +708,27 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+template <bool TS, int EPI>
+static void launch_kernel(int grid, int smem, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmO,
+                          const Args& a, cudaStream_t stream) {
+  k_grouped_mx<TS, EPI><<<grid, THREADS, smem, stream>>>(tmA, tmB, tmO, a);
+}
+
+// epi: the epilogue kind (Epi) of an M-grouped call; the weight gradient
+// (tmO != null) always takes the TMA-store epilogue
 static moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap* tmO, const Args& a,
-                           long long tiles_bound, long long sf_items, int sm_margin, cudaStream_t stream) {
+                           long long tiles_bound, long long sf_items, int sm_margin, cudaStream_t stream,
+                           int epi = -1) {
   const bool ts = tmO != nullptr;
-  const bool quant = !ts && a.out_mode != MOE_OUT_BF16;
-  const void* kfn = ts      ? (const void*)k_grouped_mx<true, false>
-                    : quant ? (const void*)k_grouped_mx<false, true>
-                            : (const void*)k_grouped_mx<false, false>;
+  if (epi < 0) epi = a.out_mode != MOE_OUT_BF16 ? EPI_QUANT : EPI_BF16;
+  const void* kfn = ts                  ? (const void*)k_grouped_mx<true, EPI_BF16>
+                    : epi == EPI_QUANT  ? (const void*)k_grouped_mx<false, EPI_QUANT>
+                    : epi == EPI_GLU    ? (const void*)k_grouped_mx<false, EPI_GLU>
+                    : epi == EPI_GLU_L1 ? (const void*)k_grouped_mx<false, EPI_GLU_L1>
+                    : epi == EPI_GLU_L2 ? (const void*)k_grouped_mx<false, EPI_GLU_L2>
+                    : epi == EPI_GLU_L3 ? (const void*)k_grouped_mx<false, EPI_GLU_L3>
+                    : epi == EPI_ELT    ? (const void*)k_grouped_mx<false, EPI_ELT>
+                                        : (const void*)k_grouped_mx<false, EPI_BF16>;
   const int smem = ts ? Lay<true>::SMEM_BYTES : Lay<false>::SMEM_BYTES;
   if (!set_smem_limit(kfn, smem)) return MOE_ERR_CUDA;
   const int sms = sm_count();
@@ -644,11 +740,21 @@ static moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const
   if (grid > tiles_bound) grid = (int)tiles_bound;
   if (grid < 1) grid = 1;
   if (ts)
-    k_grouped_mx<true, false><<<grid, THREADS, smem, stream>>>(tmA, tmB, *tmO, a);
-  else if (quant)
-    k_grouped_mx<false, true><<<grid, THREADS, smem, stream>>>(tmA, tmB, tmA, a);
+    launch_kernel<true, EPI_BF16>(grid, smem, tmA, tmB, *tmO, a, stream);
+  else if (epi == EPI_QUANT)
+    launch_kernel<false, EPI_QUANT>(grid, smem, tmA, tmB, tmA, a, stream);
+  else if (epi == EPI_GLU)
+    launch_kernel<false, EPI_GLU>(grid, smem, tmA, tmB, tmA, a, stream);
+  else if (epi == EPI_GLU_L1)
+    launch_kernel<false, EPI_GLU_L1>(grid, smem, tmA, tmB, tmA, a, stream);
+  else if (epi == EPI_GLU_L2)
+    launch_kernel<false, EPI_GLU_L2>(grid, smem, tmA, tmB, tmA, a, stream);
+  else if (epi == EPI_GLU_L3)
+    launch_kernel<false, EPI_GLU_L3>(grid, smem, tmA, tmB, tmA, a, stream);
+  else if (epi == EPI_ELT)
+    launch_kernel<false, EPI_ELT>(grid, smem, tmA, tmB, tmA, a, stream);
   else
-    k_grouped_mx<false, false><<<grid, THREADS, smem, stream>>>(tmA, tmB, tmA, a);
+    launch_kernel<false, EPI_BF16>(grid, smem, tmA, tmB, tmA, a, stream);
   count_launch(2);
   return launch_status();
 }
@@ -771,6 +877,91 @@ extern "C" moe_status_t moe_grouped_fc2_fwd(const moe_in_t* A, const moe_in_t* W
   const long long bound = mt_bound * a.n_tiles_n;
   const long long sf_items = mt_bound * a.KB + (long long)E * 2 * a.n_tiles_n * a.KB;
   return launch(tmA, tmB, nullptr, a, bound, sf_items, sm_margin, as_stream(stream));
+}
+
+extern "C" moe_status_t moe_grouped_fc1_glu_quant_fwd_mxfp8(
+    const uint8_t* xq, const uint8_t* xs, const uint8_t* W1q, const uint8_t* W1s, const moe_bf16* b1p,
+    const float* row_scale, const int32_t* counts, const int32_t* offsets, int E, int H, int F, int R_cap,
+    const moe_glu_params_t* params, int out_mode, const moe_act_out_t* out, void* ws, size_t ws_bytes, int sm_margin,
+    int32_t* status, moe_stream_t stream) {
+  using namespace gmx;
+  if (!xq || !xs || !W1q || !W1s || !counts || !offsets || !params || !out || !ws) return MOE_ERR_ARG;
+  if (E <= 0 || E > E_MAX || H <= 0 || (H % 32) || F <= 0 || (F % 32) || R_cap <= 0 || (R_cap % BM) || sm_margin < 0)
+    return MOE_ERR_ARG;
+  const int act = params->act;
+  if (act < MOE_ACT_SWIGLU || act > MOE_ACT_SREGLU) return MOE_ERR_ARG;
+  const bool gated = act != MOE_ACT_SRELU;
+  const int N1 = gated ? 2 * F : F;
+  if (!aligned16(xq) || !aligned16(W1q) || (reinterpret_cast<uintptr_t>(xs) & 3) ||
+      (reinterpret_cast<uintptr_t>(W1s) & 3) || (reinterpret_cast<uintptr_t>(ws) & 255) || (b1p && !aligned16(b1p)))
+    return MOE_ERR_ARG;
+  if (out->row_dot || out->rht_amax) return MOE_ERR_ARG;
+  if (out->pre && !aligned16(out->pre)) return MOE_ERR_ARG;
+  if (out_mode == MOE_OUT_MXFP8) {
+    if (!out->q_row || !out->s_row || (out->q_col == nullptr) != (out->s_col == nullptr)) return MOE_ERR_ARG;
+    if (!aligned16(out->q_row) || (out->q_col && !aligned16(out->q_col))) return MOE_ERR_ARG;
+  } else if (out_mode == MOE_OUT_BF16 || out_mode == MOE_OUT_NVFP4) {
+    if (!out->y || !aligned16(out->y)) return MOE_ERR_ARG;
+    if (out_mode == MOE_OUT_NVFP4 && !out->amax) return MOE_ERR_ARG;
+  } else {
+    return MOE_ERR_ARG;
+  }
+  size_t a_bytes, b_bytes;
+  fc2_ws_parts(E, H, N1, R_cap, &a_bytes, &b_bytes);
+  if (ws_bytes < a_bytes + b_bytes) return MOE_ERR_ARG;
+  CUtensorMap tmA, tmB;
+  {
+    const uint64_t dims[2] = {(uint64_t)H, (uint64_t)R_cap};
+    const uint64_t strides[1] = {(uint64_t)H};
+    const uint32_t box[2] = {BK, BM};
+    if (!encode_tmap(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, xq, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return MOE_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)H, (uint64_t)N1, (uint64_t)E};
+    const uint64_t strides[2] = {(uint64_t)H, (uint64_t)N1 * H};
+    const uint32_t box[3] = {BK, BN, 1};
+    if (!encode_tmap(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, W1q, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return MOE_ERR_CUDA;
+  }
+  Args a{};
+  a.counts = counts;
+  a.offsets = offsets;
+  a.E = E;
+  a.N = N1;
+  a.K = H;
+  a.R_cap = R_cap;
+  a.kgrouped = 0;
+  a.n_tiles_n = n_tiles(N1);
+  a.KB = k_blocks(H);
+  a.As = xs;
+  a.Bs = W1s;
+  a.sfa_t = static_cast<uint8_t*>(ws);
+  a.sfb_t = static_cast<uint8_t*>(ws) + a_bytes;
+  a.status = status;
+  a.wait_ns = g_wait_limit_ns.load();
+  a.out_mode = out_mode;
+  a.out_N = F;
+  a.q_row = out->q_row;
+  a.s_row = out->s_row;
+  a.q_col = out->q_col;
+  a.s_col = out->s_col;
+  a.y = reinterpret_cast<uint16_t*>(out->y);
+  a.amax = out->amax;
+  a.bias = reinterpret_cast<const uint16_t*>(b1p);
+  a.row_scale = row_scale;
+  a.pre_out = reinterpret_cast<uint16_t*>(out->pre);
+  a.prm = GluParams{params->act,    params->alpha, params->up_offset, params->gate_lo, params->gate_hi,
+                    params->up_lo,  params->up_hi, glu_lean_kind(params), -params->alpha * 1.4426950408889634f};
+  int epi = EPI_ELT;
+  if (gated) {
+    const int lean = glu_lean_kind(params);
+    epi = lean == 1 ? EPI_GLU_L1 : lean == 2 ? EPI_GLU_L2 : lean == 3 ? EPI_GLU_L3 : EPI_GLU;
+  }
+  const long long mt_bound = (long long)R_cap / BM + E;
+  const long long bound = mt_bound * a.n_tiles_n;
+  const long long sf_items = mt_bound * a.KB + (long long)E * 2 * a.n_tiles_n * a.KB;
+  return launch(tmA, tmB, nullptr, a, bound, sf_items, sm_margin, as_stream(stream), epi);
 }
 
 extern "C" moe_status_t moe_grouped_wgrad(const uint8_t* Aq, const uint8_t* As, const uint8_t* Bq, const uint8_t* Bs,

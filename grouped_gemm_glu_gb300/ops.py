@@ -118,6 +118,42 @@ def fc1_fwd(x_perm, W1p, counts, offsets, F: int, params: L.GluParams, out_mode:
     return o
 
 
+def fc1_fwd_mxfp8(xq, xs, W1q, W1s, counts, offsets, F: int, params: L.GluParams, out_mode: int = L.OUT_MXFP8,
+                  b1p=None, row_scale=None, save_pre: bool = True, with_col: bool = True, sm_margin: int = 0,
+                  status=None) -> dict:
+    """GroupGemm + Activation + Quantize/Transpose on MXFP8 operands: xq/xs
+    [R_cap, H] (+ /32) the row-wise MXFP8 of x_perm, W1q/W1s [E, N1, H]
+    (+ /32) the row-wise MXFP8 of the packed W1p.  Same outputs as fc1_fwd."""
+    lib = L.load()
+    dev = _dev(xq)
+    R_cap, H = xq.shape
+    E, N1, _ = W1q.shape
+    o = {}
+    if out_mode == L.OUT_MXFP8:
+        o["q_row"] = torch.empty(R_cap, F, dtype=torch.uint8, device=dev)
+        o["s_row"] = torch.empty(R_cap, F // 32, dtype=torch.uint8, device=dev)
+        if with_col:
+            o["q_col"] = torch.empty(F, R_cap, dtype=torch.uint8, device=dev)
+            o["s_col"] = torch.empty(F, R_cap // 32, dtype=torch.uint8, device=dev)
+    else:
+        o["y"] = torch.empty(R_cap, F, dtype=torch.bfloat16, device=dev)
+        if out_mode == L.OUT_NVFP4:
+            o["amax"] = torch.zeros(1, dtype=torch.float32, device=dev)
+    if save_pre:
+        o["pre"] = torch.empty(R_cap, N1, dtype=torch.bfloat16, device=dev)
+    st = status if status is not None else new_status(dev)
+    ws_bytes = lib.moe_grouped_fc2_workspace_size(E, H, N1, R_cap)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    ao = _act_out(o.get("q_row"), o.get("s_row"), o.get("q_col"), o.get("s_col"), o.get("y"), o.get("amax"),
+                  o.get("pre"))
+    L.check(lib.moe_grouped_fc1_glu_quant_fwd_mxfp8(_p(xq), _p(xs), _p(W1q), _p(W1s), _p(b1p), _p(row_scale),
+                                                    _p(counts), _p(offsets), E, H, F, R_cap, C.byref(params),
+                                                    out_mode, C.byref(ao), _p(ws), ws_bytes, sm_margin, _p(st),
+                                                    _s()), "moe_grouped_fc1_glu_quant_fwd_mxfp8")
+    o["status"] = st
+    return o
+
+
 def dglu_bwd(dY_perm, W2, pre, counts, offsets, F: int, params: L.GluParams, out_mode: int = L.OUT_MXFP8,
              row_scale=None, with_col: bool = True, sm_margin: int = 0, status=None,
              out: dict | None = None, row_dot: bool = False, rht_signs: int | None = None,

@@ -266,6 +266,29 @@ MOE_API moe_status_t moe_grouped_fc2_fwd(const moe_in_t* A, const moe_in_t* W,
                                  const moe_act_out_t* out, void* ws, size_t ws_bytes,
                                  int sm_margin, int32_t* status, moe_stream_t stream);
 
+/* GroupGemm + Activation + Quantize/Transpose on MXFP8 operands ([MoE-Fusion]
+ * "Boosting MoE Training Throughput with Advanced Fusion Kernels": the fused
+ * MLP kernels serve the dense and MoE paths in BF16 and MXFP8 recipes; the
+ * FC1 input x is quantised to MXFP8 before the GEMM).  The same epilogue as
+ * moe_grouped_fc1_glu_quant_fwd (bias, activation, row scale, saved bf16
+ * pre-activation, MXFP8 row + column-wise / bf16 / NVFP4 outputs) on the
+ * block-scaled product
+ *   pre[rows of e] = dequant(xq, xs)[rows] . dequant(W1q[e], W1s[e])^T + b1p[e]
+ * xq [R_cap][H] E4M3 with xs [R_cap][H/32] E8M0 (the row-wise MXFP8 of x_perm,
+ * e.g. moe_quantize_mxfp8 with col = 0 and the routing's counts/offsets);
+ * W1q [E][N1][H] with W1s [E][N1][H/32] (the row-wise MXFP8 of the packed W1p,
+ * blocks along H).  ws: moe_grouped_fc2_workspace_size(E, H, N1, R_cap)
+ * bytes, 256-byte aligned.  H % 32 == 0, F % 32 == 0; out->row_dot and
+ * out->rht_amax must be NULL. */
+MOE_API moe_status_t moe_grouped_fc1_glu_quant_fwd_mxfp8(const uint8_t* xq, const uint8_t* xs,
+                                                 const uint8_t* W1q, const uint8_t* W1s,
+                                                 const moe_bf16* b1p, const float* row_scale,
+                                                 const int32_t* counts, const int32_t* offsets,
+                                                 int E, int H, int F, int R_cap,
+                                                 const moe_glu_params_t* params, int out_mode,
+                                                 const moe_act_out_t* out, void* ws, size_t ws_bytes,
+                                                 int sm_margin, int32_t* status, moe_stream_t stream);
+
 /* Bytes of device workspace moe_grouped_wgrad needs. */
 MOE_API size_t moe_grouped_wgrad_workspace_size(int E, int M, int N, int R_cap);
 
