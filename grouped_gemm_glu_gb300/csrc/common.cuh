@@ -61,6 +61,18 @@ __device__ __forceinline__ uint32_t mbar_test(uint64_t* b, uint32_t parity) {
   return ok;
 }
 
+// try_wait with acquire semantics at cluster scope: for barriers that
+// another CTA of the cluster arrives on after writing data the waiter reads.
+__device__ __forceinline__ uint32_t mbar_test_cluster(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(b)), "r"(parity)
+      : "memory");
+  return ok;
+}
+
 // A wait that gives up.  Every pipeline wait in the persistent kernels goes
 // through this: after `limit_ns` (or once another role of the CTA has given
 // up) it records MOE_ERR_TIMEOUT in the status word, raises the CTA's abort
@@ -85,6 +97,28 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, const Wa
       }
     }
   }
+}
+
+// The bounded wait with cluster-scope acquire (see mbar_test_cluster).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* b, uint32_t parity, const WaitGuard& g) {
+  if (mbar_test_cluster(b, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test_cluster(b, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*g.abort) return false;
+      if (globaltimer_ns() - t0 > g.limit_ns) {
+        *g.abort = 1;
+        set_status(g.status, MOE_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// 32-bit store into the shared memory of a CTA of the cluster (cluster address).
+__device__ __forceinline__ void st_shared_cluster(uint32_t cluster_addr, int32_t v) {
+  asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
 // ---------------------------------------------------------------------------

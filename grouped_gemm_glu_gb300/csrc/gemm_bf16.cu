@@ -101,6 +101,7 @@ struct Args {
   float* row_dot;          // backward: [R_cap][2 * n_tiles_n] partials of da * act(pre), may be null
   float* db_parts;         // backward: [R_cap / 32][N1] column sums of dFC1 per 32-row block (bias gradient), may be null
   int swap_max;            // pair kernel: an expert's last pair tile with at most this many rows runs swapped (0: never)
+  int* sched;              // pair kernel: tile counter of the dynamic scheduler (zeroed before the launch), or null
   float* rht_amax;         // backward NVFP4: amax of the transposed random Hadamard rotation, may be null
   uint32_t rht_signs;      //   its 16 signs (bit i set: -1)
   int32_t* status;
@@ -526,10 +527,16 @@ constexpr int STAGE_BYTES = A_TILE + B_HALF;
 constexpr int OFF_SCRATCH = STAGES * STAGE_BYTES;
 constexpr int OFF_PREF = OFF_SCRATCH + EPI_WARPS * SCRATCH_PER_WARP;
 constexpr int OFF_BARS = OFF_PREF + (E_MAX + 2) * 4;
-constexpr int NUM_BARS = 2 * STAGES + 5;
+// tile queue: TQ slots of tile indices handed from the leader's producer to
+// every other role of both CTAs, with a full and an empty barrier per slot
+constexpr int TQ = 4;
+constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * TQ;
 constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
 constexpr int SMEM_BYTES = 1024 + OFF_MISC + 64;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+// consumers that release a queue slot: the leader's MMA thread and both
+// CTAs' epilogue warps and the peer's producer
+constexpr int TQ_CONSUMERS = 1 + 2 * EPI_WARPS + 1;
 }  // namespace pair
 
 // Tile t of the pair sequence: expert e, N tile, 256-row pair tile mp; this
@@ -729,8 +736,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
   uint64_t* acc_full = bars + 2 * pair::STAGES;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* mma_done = acc_empty + 2;
+  uint64_t* tq_full = mma_done + 1;
+  uint64_t* tq_empty = tq_full + pair::TQ;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + pair::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + pair::OFF_MISC + 4);
+  volatile int32_t* tq = reinterpret_cast<volatile int32_t*>(smem + pair::OFF_MISC + 16);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = a.E;
@@ -747,6 +757,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
       mbar_init(acc_empty + b, 2 * EPI_WARPS);
     }
     mbar_init(mma_done, 1);
+    for (int i = 0; i < pair::TQ; ++i) {
+      mbar_init(tq_full + i, 1);
+      mbar_init(tq_empty + i, pair::TQ_CONSUMERS);
+    }
     *abort_flag = 0;
     fence_barrier_init();
     fence_async_shared();
@@ -791,11 +805,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
   const int num_kb = a.K / BK;
   WaitGuard guard{abort_flag, a.status, a.wait_ns};
 
+  // Tile sequence of this cluster.  The leader's producer takes the next
+  // tile (the scheduler's atomic counter when a.sched is set: clusters that
+  // finish early take more tiles, whatever else shares the SMs; otherwise the
+  // static stride cl, cl + ncl, ...), publishes it in queue slot i % TQ of
+  // both CTAs and ends the sequence with -1.  Every other role reads the
+  // slots in order and releases each one on the leader.
+  auto tq_next = [&](int i, bool own_cta_release, int& t) -> bool {
+    const int slot = i % pair::TQ;
+    const uint32_t ph = (uint32_t)(i / pair::TQ) & 1u;
+    if (!mbar_wait_cluster(tq_full + slot, ph, guard)) return false;
+    t = tq[slot];
+    if (own_cta_release)
+      mbar_arrive(tq_empty + slot);
+    else
+      mbar_arrive_cluster(mapa_shared(smem_u32(tq_empty + slot), 0));
+    return true;
+  };
+
   if (warp == PRODUCER_WARP) {
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      for (int t = cl; t < total; t += ncl) {
+      for (int i = 0;; ++i) {
+        int t;
+        if (rank == 0) {
+          const int slot = i % pair::TQ;
+          if (!mbar_wait(tq_empty + slot, ((uint32_t)(i / pair::TQ) & 1u) ^ 1u, guard)) break;
+          t = a.sched != nullptr ? atomicAdd(a.sched, 1) : cl + i * ncl;
+          if (t >= total) t = -1;
+          tq[slot] = t;
+          st_shared_cluster(mapa_shared(smem_u32((const void*)(tq + slot)), 1), t);
+          mbar_arrive(tq_full + slot);
+          mbar_arrive_cluster(mapa_shared(smem_u32(tq_full + slot), 1));
+        } else if (!tq_next(i, false, t)) {
+          break;
+        }
+        if (t < 0) break;
         const Tile ti = decode_pair(t, pref, E, a.n_tiles_n, a.counts, a.offsets, a.R_cap, (int)rank, a.swap_max);
         // Only the 32-row blocks of A inside the expert's padded segment are
         // fetched: the rows past it (the second half of an expert's last pair
@@ -852,7 +898,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       int lt = 0;
-      for (int t = cl; t < total; t += ncl, ++lt) {
+      for (;; ++lt) {
+        int t;
+        if (!tq_next(lt, true, t) || t < 0) break;
         const int buf = lt & 1;
         const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
         // a swapped tile multiplies the weight rows (A slot) by its nt rows
@@ -895,10 +943,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
     uint8_t* scratch = scratch_all + warp * SCRATCH_PER_WARP;
     Amax amax_bits{0u, 0u};
     int lt = 0;
-    for (int t = cl; t < total; t += ncl, ++lt) {
+    for (;; ++lt) {
+      int t = -1, ok = 1;
+      if (lane == 0) ok = tq_next(lt, rank == 0, t) ? 1 : 0;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      t = __shfl_sync(0xFFFFFFFFu, t, 0);
+      if (!ok || t < 0) break;
       const int buf = lt & 1;
       const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
-      int ok = 1;
       if (lane == 0) ok = mbar_wait(acc_full + buf, aph, guard) ? 1 : 0;
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
@@ -972,6 +1024,7 @@ static moe_status_t launch_pair(const void* A, const void* B, const Args& args, 
   // per-row partials are laid out for the regular tile)
   Args a2 = args;
   a2.swap_max = (MODE == BWD_GLU_DOT || MODE == BWD_ELT_DOT) ? 0 : g_tail_swap_rows.load();
+  if (a2.sched != nullptr && cudaMemsetAsync(a2.sched, 0, sizeof(int), stream) != cudaSuccess) return MOE_ERR_CUDA;
   k_grouped_bf16_pair<MODE><<<2 * clusters, pair::THREADS, pair::SMEM_BYTES, stream>>>(tmA, tmA32, tmA16, tmB, a2);
   count_launch();
   return launch_status();
@@ -1047,12 +1100,26 @@ static bool out_ok(int out_mode, const moe_act_out_t* o) {
 
 using namespace moeglu;
 
+// Workspace of the bf16 grouped GEMMs: the dynamic scheduler's tile counter
+// in its first 256 bytes, then (backward with a bias gradient) one column-sum
+// line per 32-row block.
+static constexpr size_t SCHED_BYTES = 256;
+static constexpr size_t g16_sched_bytes() { return SCHED_BYTES; }
+
+extern "C" size_t moe_grouped_fc1_workspace_size(int E, int N1, int R_cap) {
+  (void)E;
+  (void)N1;
+  (void)R_cap;
+  return SCHED_BYTES;
+}
+
 extern "C" moe_status_t moe_grouped_fc1_glu_quant_fwd(const moe_bf16* x_perm, const moe_bf16* W1p,
                                                       const moe_bf16* b1p, const float* row_scale,
                                                       const int32_t* counts, const int32_t* offsets, int E, int H,
                                                       int F, int R_cap, const moe_glu_params_t* params,
-                                                      int out_mode, const moe_act_out_t* out, int sm_margin,
-                                                      int32_t* status, moe_stream_t stream) {
+                                                      int out_mode, const moe_act_out_t* out, void* ws,
+                                                      size_t ws_bytes, int sm_margin, int32_t* status,
+                                                      moe_stream_t stream) {
   using namespace g16;
   if (!x_perm || !W1p || !counts || !offsets || !params || !out) return MOE_ERR_ARG;
   if (E <= 0 || E > E_MAX || H <= 0 || (H % BK) || F <= 0 || (F % 32) || R_cap <= 0 || (R_cap % BM)) return MOE_ERR_ARG;
@@ -1075,6 +1142,10 @@ extern "C" moe_status_t moe_grouped_fc1_glu_quant_fwd(const moe_bf16* x_perm, co
   a.out_mode = out_mode;
   a.status = status;
   a.wait_ns = g_wait_limit_ns.load();
+  if (ws != nullptr) {
+    if (ws_bytes < SCHED_BYTES || (reinterpret_cast<uintptr_t>(ws) & 15)) return MOE_ERR_ARG;
+    a.sched = static_cast<int*>(ws);
+  }
   if (none) {
     // unfused path: the GEMM writes the bf16 pre-activation of all N1 = F columns given
     if (!out->pre || !aligned16(out->pre)) return MOE_ERR_ARG;
@@ -1134,8 +1205,8 @@ __global__ void __launch_bounds__(256) k_bias_grad(const float* __restrict__ par
 }  // namespace moeglu
 
 extern "C" size_t moe_grouped_dglu_workspace_size(int N1, int R_cap) {
-  if (N1 <= 0 || R_cap <= 0) return 0;
-  return ((size_t)(R_cap / 32) * N1 * sizeof(float) + 255) & ~(size_t)255;
+  if (N1 <= 0 || R_cap <= 0) return g16_sched_bytes();
+  return g16_sched_bytes() + (((size_t)(R_cap / 32) * N1 * sizeof(float) + 255) & ~(size_t)255);
 }
 
 extern "C" moe_status_t moe_grouped_dglu_quant_bwd(const moe_bf16* dY_perm, const moe_bf16* W2, const moe_bf16* pre,
@@ -1183,11 +1254,14 @@ extern "C" moe_status_t moe_grouped_dglu_quant_bwd(const moe_bf16* dY_perm, cons
   a.rht_signs = dfc1->rht_signs;
   a.status = status;
   a.wait_ns = g_wait_limit_ns.load();
+  if (ws != nullptr) {
+    // the scheduler's counter, then (bias gradient) one column-sum line per 32-row block
+    if (ws_bytes < g16_sched_bytes() || (reinterpret_cast<uintptr_t>(ws) & 15)) return MOE_ERR_ARG;
+    a.sched = static_cast<int*>(ws);
+  }
   if (dbias != nullptr) {
-    // the epilogue writes one column-sum line per 32-row block into ws
-    if (!ws || ws_bytes < moe_grouped_dglu_workspace_size(a.N1, R_cap) || (reinterpret_cast<uintptr_t>(ws) & 15))
-      return MOE_ERR_ARG;
-    a.db_parts = static_cast<float*>(ws);
+    if (!ws || ws_bytes < moe_grouped_dglu_workspace_size(a.N1, R_cap)) return MOE_ERR_ARG;
+    a.db_parts = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + g16_sched_bytes());
   }
   cudaStream_t st = as_stream(stream);
   moe_status_t rc;
@@ -1217,7 +1291,8 @@ extern "C" moe_status_t moe_grouped_dglu_quant_bwd(const moe_bf16* dY_perm, cons
 // this kernel adds (K % 64).
 moe_status_t moeglu::grouped_gemm_bf16_out(const void* A, const void* W, const int32_t* counts, const int32_t* offsets,
                                            int E, int K, int N, int R_cap, int out_mode, const moe_act_out_t* out,
-                                           int sm_margin, int32_t* status, cudaStream_t stream) {
+                                           void* ws, size_t ws_bytes, int sm_margin, int32_t* status,
+                                           cudaStream_t stream) {
   using namespace g16;
   if (E > E_MAX || (K % BK) || (R_cap % BM)) return MOE_ERR_ARG;
   if (!aligned16(A) || !aligned16(W)) return MOE_ERR_ARG;
@@ -1244,6 +1319,7 @@ moe_status_t moeglu::grouped_gemm_bf16_out(const void* A, const void* W, const i
   a.amax = out->amax;
   a.status = status;
   a.wait_ns = g_wait_limit_ns.load();
+  if (ws != nullptr && ws_bytes >= 256 && (reinterpret_cast<uintptr_t>(ws) & 15) == 0) a.sched = static_cast<int*>(ws);
   return launch<FWD_ID>(A, W, a, sm_margin, stream);
 }
 

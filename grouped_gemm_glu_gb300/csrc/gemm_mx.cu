@@ -808,8 +808,8 @@ extern "C" moe_status_t moe_grouped_fc2_fwd(const moe_in_t* A, const moe_in_t* W
   if (out_mode != MOE_OUT_BF16 && out_mode != MOE_OUT_MXFP8 && out_mode != MOE_OUT_NVFP4) return MOE_ERR_ARG;
   if (out->pre || out->row_dot || out->rht_amax) return MOE_ERR_ARG;
   if (A->dtype == MOE_IN_BF16)
-    return grouped_gemm_bf16_out(A->data, W->data, counts, offsets, E, K, N, R_cap, out_mode, out, sm_margin, status,
-                                 as_stream(stream));
+    return grouped_gemm_bf16_out(A->data, W->data, counts, offsets, E, K, N, R_cap, out_mode, out, ws, ws_bytes,
+                                 sm_margin, status, as_stream(stream));
   if (A->dtype != MOE_IN_MXFP8) return MOE_ERR_ARG;
   const uint8_t* Aq = static_cast<const uint8_t*>(A->data);
   const uint8_t* Wq = static_cast<const uint8_t*>(W->data);

@@ -12,7 +12,7 @@ namespace moeglu {
 std::atomic<uint64_t> g_launches{0};
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_cta_pairs{1};
-std::atomic<int> g_tail_swap_rows{64};
+std::atomic<int> g_tail_swap_rows{32};
 
 int max_active_pairs(const void* kernel, int threads, int smem_bytes) {
   static std::mutex mu;

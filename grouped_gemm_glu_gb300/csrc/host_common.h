@@ -60,8 +60,8 @@ inline int glu_lean_kind(const moe_glu_params_t* p) {
 // Plain grouped GEMM with bf16 operands through the fused output stage
 // (gemm_bf16.cu; the bf16 case of moe_grouped_fc2_fwd).
 moe_status_t grouped_gemm_bf16_out(const void* A, const void* W, const int32_t* counts, const int32_t* offsets, int E,
-                                   int K, int N, int R_cap, int out_mode, const moe_act_out_t* out, int sm_margin,
-                                   int32_t* status, cudaStream_t stream);
+                                   int K, int N, int R_cap, int out_mode, const moe_act_out_t* out, void* ws,
+                                   size_t ws_bytes, int sm_margin, int32_t* status, cudaStream_t stream);
 
 inline moe_status_t launch_status() {
   const cudaError_t e = cudaGetLastError();

@@ -29,7 +29,10 @@ from .ops import _p, _s
 
 class MoeLayer:
     def __init__(self, W1, W2, T: int, k: int, R_cap: int, params: L.GluParams, b1=None,
-                 expert_begin: int = 0, sm_margin: int = 0, gated: bool = True):
+                 expert_begin: int = 0, sm_margin: int = 0, gated: bool = True, dynamic: bool = True):
+        """dynamic: the bf16 grouped GEMMs take their tiles from the dynamic
+        scheduler (each call site has its own counter workspace); False runs
+        the static schedule."""
         self.lib = L.load()
         dev = W1.device
         self.dev = dev
@@ -89,11 +92,19 @@ class MoeLayer:
         self.ws_dx = ws(lib.moe_grouped_fc2_workspace_size(E, N1, H, R_cap))
         self.ws_wg1 = ws(lib.moe_grouped_wgrad_workspace_size(E, N1, H, R_cap))
         self.ws_wg2 = ws(lib.moe_grouped_wgrad_workspace_size(E, F, H, R_cap))
-        # FC1 bias gradient (packed order, like b1p) when the layer has a bias
+        # scheduler counters of the bf16 GEMMs, and the FC1 bias gradient
+        # (packed order, like b1p) with its partial sums when the layer has a bias
+        self.ws_fc1 = self.ws_fc1u = None
+        self.ws_fc1_bytes = 0
         self.db1, self.ws_db, self.ws_db_bytes = None, None, 0
+        if dynamic:
+            self.ws_fc1_bytes = lib.moe_grouped_fc1_workspace_size(E, N1, R_cap)
+            self.ws_fc1, self.ws_fc1u = z(self.ws_fc1_bytes, dt=u8), z(self.ws_fc1_bytes, dt=u8)
+            self.ws_db_bytes = lib.moe_grouped_dglu_workspace_size(0, 0)
         if self.b1p is not None:
             self.db1 = z(E, N1, dt=torch.float32)
             self.ws_db_bytes = lib.moe_grouped_dglu_workspace_size(N1, R_cap)
+        if self.ws_db_bytes:
             self.ws_db = z(self.ws_db_bytes, dt=u8)
         # operands and outputs of the two block-scaled M-grouped GEMMs
         self.fc2_a = L.in_operand(self.a_q.data_ptr(), self.a_s.data_ptr())
@@ -119,7 +130,8 @@ class MoeLayer:
                 _p(self.ws), self.ws_bytes, st, s)),
             ("fc1_glu_quant", lambda: lib.moe_grouped_fc1_glu_quant_fwd(
                 _p(self.x_perm), _p(self.W1p), _p(self.b1p), None, _p(self.counts), _p(self.offsets), E, H, F, R,
-                C.byref(self.params), L.OUT_MXFP8, C.byref(self.fc1_out), self.sm_margin, st, s)),
+                C.byref(self.params), L.OUT_MXFP8, C.byref(self.fc1_out), _p(self.ws_fc1), self.ws_fc1_bytes,
+                self.sm_margin, st, s)),
             ("quant_w2", lambda: lib.moe_quantize_mxfp8(
                 _p(self.W2), E, F, H, 1, None, None, 0, _p(self.W2q), _p(self.W2s), st, s)),
             ("fc2", lambda: lib.moe_grouped_fc2_fwd(
@@ -188,7 +200,7 @@ class MoeLayer:
         return [
             ("gemm", lambda: lib.moe_grouped_fc1_glu_quant_fwd(
                 _p(self.x_perm), _p(self.W1p), _p(self.b1p), None, cnt, off, E, H, N1, R, C.byref(self._u_none),
-                L.OUT_BF16, C.byref(self._u_fwd_out), self.sm_margin, st, s)),
+                L.OUT_BF16, C.byref(self._u_fwd_out), _p(self.ws_fc1u), self.ws_fc1_bytes, self.sm_margin, st, s)),
             ("act", lambda: lib.moe_glu_act(_p(u["pre"]), cnt, off, E, F, R, C.byref(self.params), _p(u["y"]), s)),
             ("quant_rows", lambda: lib.moe_quantize_mxfp8(_p(u["y"]), 1, R, F, 0, cnt, off, E, _p(u["a_q"]),
                                                           _p(u["a_s"]), st, s)),
@@ -205,7 +217,7 @@ class MoeLayer:
         return [
             ("gemm", lambda: lib.moe_grouped_fc1_glu_quant_fwd(
                 _p(dY_perm), _p(self.W2), None, None, cnt, off, E, H, F, R, C.byref(self._u_none), L.OUT_BF16,
-                C.byref(self._u_bwd_out), self.sm_margin, st, s)),
+                C.byref(self._u_bwd_out), _p(self.ws_fc1u), self.ws_fc1_bytes, self.sm_margin, st, s)),
             ("dact", lambda: lib.moe_dglu_act(_p(u["da"]), _p(self.pre), cnt, off, E, F, R, C.byref(self.params),
                                               _p(u["d"]), s)),
             ("quant_rows", lambda: lib.moe_quantize_mxfp8(_p(u["d"]), 1, R, N1, 0, cnt, off, E, _p(u["d_q"]),

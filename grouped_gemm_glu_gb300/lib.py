@@ -55,7 +55,9 @@ _SIGS = {
     "moe_repack_fc1": [P, P, I, I, I, I, P],
     "moe_route_workspace_size": ([I, I, I], SZ),
     "moe_route_permute": [P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P, SZ, P, P],
-    "moe_grouped_fc1_glu_quant_fwd": [P, P, P, P, P, P, I, I, I, I, C.POINTER(GluParams), I, C.POINTER(ActOut), I, P, P],
+    "moe_grouped_fc1_glu_quant_fwd": [P, P, P, P, P, P, I, I, I, I, C.POINTER(GluParams), I, C.POINTER(ActOut), P,
+                                      SZ, I, P, P],
+    "moe_grouped_fc1_workspace_size": ([I, I, I], SZ),
     "moe_grouped_dglu_quant_bwd": [P, P, P, P, P, P, I, I, I, I, C.POINTER(GluParams), I, C.POINTER(ActOut), P, P, SZ,
                                    I, P, P],
     "moe_grouped_dglu_workspace_size": ([I, I], SZ),

@@ -82,9 +82,10 @@ def _act_out(q_row=None, s_row=None, q_col=None, s_col=None, y=None, amax=None, 
 
 def fc1_fwd(x_perm, W1p, counts, offsets, F: int, params: L.GluParams, out_mode: int = L.OUT_MXFP8,
             b1p=None, row_scale=None, save_pre: bool = True, with_col: bool = True, sm_margin: int = 0,
-            status=None, out: dict | None = None) -> dict:
+            status=None, out: dict | None = None, dynamic: bool = True) -> dict:
     """GroupGemm + Activation + Quantize/Transpose.  Returns the output tensors
-    ({q_row, s_row, q_col, s_col} | {y[, amax]}, and pre when saved)."""
+    ({q_row, s_row, q_col, s_col} | {y[, amax]}, and pre when saved).
+    dynamic=False runs the static tile schedule (no workspace)."""
     lib = L.load()
     dev = _dev(x_perm)
     R_cap, H = x_perm.shape
@@ -110,9 +111,11 @@ def fc1_fwd(x_perm, W1p, counts, offsets, F: int, params: L.GluParams, out_mode:
     st = status if status is not None else new_status(dev)
     ao = _act_out(o.get("q_row"), o.get("s_row"), o.get("q_col"), o.get("s_col"), o.get("y"), o.get("amax"),
                   o.get("pre"))
+    ws_bytes = lib.moe_grouped_fc1_workspace_size(E, N1, R_cap) if dynamic else 0
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if dynamic else None
     L.check(lib.moe_grouped_fc1_glu_quant_fwd(_p(x_perm), _p(W1p), _p(b1p), _p(row_scale), _p(counts),
                                               _p(offsets), E, H, F, R_cap, C.byref(params), out_mode,
-                                              C.byref(ao), sm_margin, _p(st), _s()),
+                                              C.byref(ao), _p(ws), ws_bytes, sm_margin, _p(st), _s()),
             "moe_grouped_fc1_glu_quant_fwd")
     o["status"] = st
     return o
@@ -157,7 +160,7 @@ def fc1_fwd_mxfp8(xq, xs, W1q, W1s, counts, offsets, F: int, params: L.GluParams
 def dglu_bwd(dY_perm, W2, pre, counts, offsets, F: int, params: L.GluParams, out_mode: int = L.OUT_MXFP8,
              row_scale=None, with_col: bool = True, sm_margin: int = 0, status=None,
              out: dict | None = None, row_dot: bool = False, rht_signs: int | None = None,
-             dbias: bool = False) -> dict:
+             dbias: bool = False, dynamic: bool = True) -> dict:
     """GroupGemm + dActivation + Quantize/Transpose.  dFC1 in packed order;
     row_dot=True also returns o["row_dot"], the per-row partials of the
     feature-scale gradient (reduce with feature_scale_grad).  NVFP4 mode
@@ -193,7 +196,8 @@ def dglu_bwd(dY_perm, W2, pre, counts, offsets, F: int, params: L.GluParams, out
     ws_bytes, ws = 0, None
     if dbias:
         o.setdefault("dbias", torch.empty(E, N1, dtype=torch.float32, device=dev))
-        ws_bytes = lib.moe_grouped_dglu_workspace_size(N1, R_cap)
+    if dbias or dynamic:
+        ws_bytes = lib.moe_grouped_dglu_workspace_size(N1, R_cap) if dbias else lib.moe_grouped_dglu_workspace_size(0, 0)
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     L.check(lib.moe_grouped_dglu_quant_bwd(_p(dY_perm), _p(W2), _p(pre), _p(row_scale), _p(counts), _p(offsets),
                                            E, H, F, R_cap, C.byref(params), out_mode, C.byref(ao), _p(o.get("dbias")),

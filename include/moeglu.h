@@ -176,14 +176,24 @@ MOE_API moe_status_t moe_route_permute(const moe_bf16* x, const int32_t* topk_id
  * applies the activation, multiplies by row_scale[row] when non-NULL
  * (feature scaling), and writes per out_mode.  Pad rows are written as 0.
  * x_perm [R_cap][H], W1p [E][N1][H] (packed when gated), b1p [E][N1] or
- * NULL, row_scale [R_cap] f32 or NULL.  H % 64 == 0, F % 32 == 0. */
+ * NULL, row_scale [R_cap] f32 or NULL.  H % 64 == 0, F % 32 == 0.
+ * ws (nullable, moe_grouped_fc1_workspace_size() bytes, 16-byte aligned):
+ * the dynamic tile scheduler's counter; NULL runs the static schedule. */
 MOE_API moe_status_t moe_grouped_fc1_glu_quant_fwd(const moe_bf16* x_perm, const moe_bf16* W1p,
                                            const moe_bf16* b1p, const float* row_scale,
                                            const int32_t* counts, const int32_t* offsets,
                                            int E, int H, int F, int R_cap,
                                            const moe_glu_params_t* params, int out_mode,
-                                           const moe_act_out_t* out, int sm_margin,
-                                           int32_t* status, moe_stream_t stream);
+                                           const moe_act_out_t* out, void* ws, size_t ws_bytes,
+                                           int sm_margin, int32_t* status, moe_stream_t stream);
+
+/* Bytes of device workspace of moe_grouped_fc1_glu_quant_fwd: the counter of
+ * the dynamic tile scheduler ([MoE-Fusion]: dynamic scheduling, so that the
+ * grouped kernels share the GPU with concurrent work).  With ws the CTA
+ * pairs take tiles from an atomic counter (zeroed by the call itself, in
+ * stream order) instead of a fixed stride; results are the same either way.
+ * Calls that may run at the same time need separate workspaces. */
+MOE_API size_t moe_grouped_fc1_workspace_size(int E, int N1, int R_cap);
 
 /* GroupGemm + dActivation + Quantize/Transpose, backward ([MoE-Fusion]: the
  * epilogue reads the GEMM output, computes dSwiGLU, quantises and writes).
@@ -201,10 +211,12 @@ MOE_API moe_status_t moe_grouped_fc1_glu_quant_fwd(const moe_bf16* x_perm, const
  * of the FC1 bias ([MoE-Fusion] "clamping and scaling": the bias vector of
  * the GLU), dbias[e][c] = sum over the expert's rows of dFC1[r][c] taken on
  * the fp32 values before quantisation.  The epilogue writes one column-sum
- * line per 32-row block into ws (moe_grouped_dglu_workspace_size(N1, R_cap)
- * bytes, 16-byte aligned; unused and may be NULL when dbias is NULL) and a
- * second kernel adds each expert's lines in block order (deterministic; 0
- * for an expert without rows).
+ * line per 32-row block into ws and a second kernel adds each expert's lines
+ * in block order (deterministic; 0 for an expert without rows).
+ * ws (moe_grouped_dglu_workspace_size(N1, R_cap) bytes, 16-byte aligned;
+ * required with dbias, else nullable): its first 256 bytes are the dynamic
+ * tile scheduler's counter (as for the forward; NULL runs the static
+ * schedule), the rest the bias-gradient lines.
  * H % 64 == 0. */
 MOE_API moe_status_t moe_grouped_dglu_quant_bwd(const moe_bf16* dY_perm, const moe_bf16* W2,
                                         const moe_bf16* pre, const float* row_scale,
@@ -258,8 +270,10 @@ MOE_API size_t moe_grouped_fc2_workspace_size(int E, int K, int N, int R_cap);
  *                 ws = moe_grouped_fc2_workspace_size() bytes, 256-byte
  *                 aligned.  K % 32 == 0, N % 32 == 0 (a partial last
  *                 128-wide k-block or 256-wide column tile is handled).
- *   MOE_IN_BF16:  bf16, scale unused; kind::f16 MMA; ws unused (may be
- *                 NULL).  K % 64 == 0, N % 32 == 0. */
+ *   MOE_IN_BF16:  bf16, scale unused; kind::f16 MMA on CTA pairs; ws
+ *                 nullable: with >= 256 bytes (16-byte aligned) it holds the
+ *                 dynamic tile scheduler's counter, as for the fused FC1.
+ *                 K % 64 == 0, N % 32 == 0. */
 MOE_API moe_status_t moe_grouped_fc2_fwd(const moe_in_t* A, const moe_in_t* W,
                                  const int32_t* counts, const int32_t* offsets,
                                  int E, int K, int N, int R_cap, int out_mode,
@@ -441,7 +455,7 @@ MOE_API void moe_set_cta_pairs(int enable);
  * tensor cores do not multiply the empty rows of a mostly empty tile.  The
  * results are the same as the regular tile's (the bias-gradient partials
  * add their 32 rows in another order).  max_rows in {0 (off), 32, 64, 96,
- * 128}, default 64; anything else returns MOE_ERR_ARG.  Process-wide. */
+ * 128}, default 32; anything else returns MOE_ERR_ARG.  Process-wide. */
 MOE_API moe_status_t moe_set_tail_swap(int max_rows);
 
 /* Cumulative number of kernels this library has launched in this process

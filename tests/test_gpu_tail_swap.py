@@ -26,7 +26,7 @@ def swap(request):
     lib = L.load()
     assert lib.moe_set_tail_swap(request.param) == 0
     yield request.param
-    lib.moe_set_tail_swap(64)
+    lib.moe_set_tail_swap(32)
 
 
 def _edge_ids():
@@ -39,7 +39,7 @@ def test_threshold_validation():
     lib = L.load()
     for bad in (-32, 16, 160, 256):
         assert lib.moe_set_tail_swap(bad) == L.MOE_ERR_ARG
-    assert lib.moe_set_tail_swap(64) == 0
+    assert lib.moe_set_tail_swap(32) == 0
 
 
 @pytest.mark.parametrize("act", ["swiglu", "geglu", "srelu"])

@@ -43,7 +43,8 @@ def test_argument_validation_needs_no_device(lib):
     prm = L.glu_params("swiglu")
     out = L.ActOut()
     assert lib.moe_grouped_fc1_glu_quant_fwd(None, None, None, None, None, None, 4, 256, 512, 1152,
-                                             ctypes.byref(prm), 1, ctypes.byref(out), 0, None, None) == L.MOE_ERR_ARG
+                                             ctypes.byref(prm), 1, ctypes.byref(out), None, 0, 0, None,
+                                             None) == L.MOE_ERR_ARG
     assert lib.moe_wait_selftest(0, None, None, None) == L.MOE_ERR_ARG
     assert lib.moe_quantize_mxfp8(None, 1, 32, 32, 0, None, None, 0, None, None, None, None) == L.MOE_ERR_ARG
     assert lib.moe_grouped_fc2_fwd(None, None, None, None, 4, 512, 256, 1152, 0, None, None, 0, 0, None,
