@@ -18,10 +18,14 @@ DEV = "cuda:0"
 KEYS = ("q_row", "s_row", "q_col", "s_col", "y", "pre", "amax", "dbias")
 
 
-def _same(a, b, what):
+def _same(a, b, what, R):
+    """Outputs are defined on the rows of the padded segments (R = offsets[E])."""
+    view = {"q_row": lambda t: t[:R], "s_row": lambda t: t[:R], "y": lambda t: t[:R], "pre": lambda t: t[:R],
+            "q_col": lambda t: t[:, :R], "s_col": lambda t: t[:, :R // 32]}
     for k in KEYS:
         if k in a or k in b:
-            assert torch.equal(a[k], b[k]), f"{what}: {k} differs between schedules"
+            f = view.get(k, lambda t: t)
+            assert torch.equal(f(a[k]), f(b[k])), f"{what}: {k} differs between schedules"
 
 
 def _case(name):
@@ -46,7 +50,7 @@ def test_dynamic_matches_static(name, out_mode):
     fd = ops.fc1_fwd(*args, b1p=case.b1p, dynamic=True)
     torch.cuda.synchronize()
     assert ops.read_status(fd["status"]) == 0
-    _same(fs, fd, "FC1")
+    _same(fs, fd, "FC1", case.rt.R_pad)
     dY = case.inp["dY"].to(DEV)
     W2 = case.g["W2"]
     bs = ops.dglu_bwd(dY, W2, fs["pre"], case.r["counts"], case.r["offsets"], w.F, gp, out_mode, dbias=True,
@@ -55,7 +59,7 @@ def test_dynamic_matches_static(name, out_mode):
                       dynamic=True)
     torch.cuda.synchronize()
     assert ops.read_status(bd["status"]) == 0
-    _same(bs, bd, "dGLU")
+    _same(bs, bd, "dGLU", case.rt.R_pad)
 
 
 def test_dynamic_with_a_concurrent_kernel_and_sm_margin():
@@ -82,7 +86,7 @@ def test_dynamic_with_a_concurrent_kernel_and_sm_margin():
     torch.cuda.synchronize()
     for o in outs:
         assert ops.read_status(o["status"]) == 0
-        _same(ref, o, "FC1 next to a concurrent kernel")
+        _same(ref, o, "FC1 next to a concurrent kernel", case.rt.R_pad)
 
 
 def test_two_calls_in_flight_on_two_streams():
@@ -103,5 +107,5 @@ def test_two_calls_in_flight_on_two_streams():
     with torch.cuda.stream(s2):
         o2 = ops.fc1_fwd(*args, b1p=case.b1p, dynamic=True, sm_margin=76)
     torch.cuda.synchronize()
-    _same(ref, o1, "stream 1")
-    _same(ref, o2, "stream 2")
+    _same(ref, o1, "stream 1", case.rt.R_pad)
+    _same(ref, o2, "stream 2", case.rt.R_pad)
