@@ -431,6 +431,43 @@ def main():
                      "unfused": "gemm(bf16 da) -> dact -> mxfp8 rows -> mxfp8 cols"},
         "pages": "up to 1.3x forward, 2.1x backward over unfused paths (unit microbenchmarks; GB200 figure)",
     }
+    # -- the MXFP8-input FC1 (same fused epilogue on the block-scaled product
+    #    of the row-wise MXFP8 x_perm and W1p): its two casts and the GEMM,
+    #    each timed alone; not part of the step above, whose FC1 is bf16
+    import ctypes as C
+    from grouped_gemm_glu_gb300.ops import _p, _s
+    u8 = torch.uint8
+    E_, N1_, H_, F_ = w.E, w.N1, w.H, w.F
+    xq = torch.empty(R_cap, H_, dtype=u8, device=dev)
+    xs = torch.empty(R_cap, H_ // 32, dtype=u8, device=dev)
+    w1q = torch.empty(E_, N1_, H_, dtype=u8, device=dev)
+    w1s = torch.empty(E_, N1_, H_ // 32, dtype=u8, device=dev)
+    mx_ws_bytes = lib.moe_grouped_fc2_workspace_size(E_, H_, N1_, R_cap)
+    mx_ws = torch.empty(mx_ws_bytes, dtype=u8, device=dev)
+    mx_out = L.ActOut(layer.a_q.data_ptr(), layer.a_s.data_ptr(), layer.a_qc.data_ptr(), layer.a_sc.data_ptr(),
+                      None, None, layer.pre.data_ptr())
+    st_p, s_p = _p(layer.status), _s()
+    mx_calls = {
+        "quant_x_rows": [("quant_x_rows", lambda: lib.moe_quantize_mxfp8(
+            _p(layer.x_perm), 1, R_cap, H_, 0, _p(layer.counts), _p(layer.offsets), E_, _p(xq), _p(xs), st_p, s_p))],
+        "quant_w1_rows": [("quant_w1_rows", lambda: lib.moe_quantize_mxfp8(
+            _p(layer.W1p), E_, N1_, H_, 0, None, None, 0, _p(w1q), _p(w1s), st_p, s_p))],
+        "fc1_mxfp8": [("fc1_mxfp8", lambda: lib.moe_grouped_fc1_glu_quant_fwd_mxfp8(
+            _p(xq), _p(xs), _p(w1q), _p(w1s), _p(layer.b1p), None, _p(layer.counts), _p(layer.offsets), E_, H_, F_,
+            R_cap, C.byref(params), L.OUT_MXFP8, C.byref(mx_out), _p(mx_ws), mx_ws_bytes, args.sm_margin, st_p,
+            s_p))],
+    }
+    mx_ms = {}
+    for n_, c_ in mx_calls.items():
+        layer.run(c_)
+        mx_ms[n_] = timed(c_, na)
+    fl_mx = 2 * R * H_ * N1_
+    by_mx = (E_ * N1_ * H_ + R * H_) * (1 + 1 / 32) + R * N1_ * 2 + 2 * R * F_ * (1 + 1 / 32)
+    fc1_mx = {"casts": {"x rows ms": round(mx_ms["quant_x_rows"], 4), "W1 rows ms": round(mx_ms["quant_w1_rows"], 4)},
+              "ms": round(mx_ms["fc1_mxfp8"], 4), "TFLOP/s": round(fl_mx / mx_ms["fc1_mxfp8"] / 1e9, 1),
+              "frac_of_fp8_peak": round(fl_mx / mx_ms["fc1_mxfp8"] / 1e9 / (2 * load_peaks()["bf16"]), 4),
+              "frac_of_hbm_roof": round(by_mx / mx_ms["fc1_mxfp8"] / 1e6 / load_peaks()["hbm"], 4),
+              "note": "FC1 on MXFP8 x and W1 (fp8 = 2 x bf16 burst peak); the step's FC1 is the bf16 kernel"}
     clocks = sampler.stop()
     st = ops.read_status(layer.status)
     if st:
@@ -522,11 +559,13 @@ def main():
         "config": {"workload": workload_desc(w), "T": w.T, "H": w.H, "E_local": w.E, "experts": w.n_experts,
                    "top_k": w.k, "F": w.F, "R_cap": R_cap, "routed_rows": R, "padded_rows": Rp,
                    "capacity_factor": CAPACITY_FACTOR, "l2": "inputs larger than L2 (no flush)",
-                   "step": "one CUDA graph: " + " -> ".join(names), "parallelism": f"ep-shards x{world}"},
+                   "step": "one CUDA graph: " + " -> ".join(names), "parallelism": f"ep-shards x{world}",
+                   "bf16_gemm_schedule": "dynamic (atomic tile counter)", "tail_swap_max_rows": 32},
         "roofline": roof,
         "fused_kernels": fused,
         "kernels": kern,
         "ablation_fused_vs_unfused": ablation,
+        "fc1_mxfp8_variant": fc1_mx,
         "eager_ms_per_step": round(ms_eager, 4),
         # counted: the eager region's launches plus, for the two graph
         # regions, the kernel launches recorded into the captured step graph
