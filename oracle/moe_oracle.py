@@ -218,6 +218,27 @@ def nvfp4_dequantize(packed, sb_code, s_g) -> np.ndarray:
     return (vals * (e4m3_decode(sb_code) / float(s_g))[..., None]).reshape(q.shape)
 
 
+def nvfp4_quantize_cols(v, s_g) -> tuple[np.ndarray, np.ndarray]:
+    """Column-wise NVFP4 of v [R, N] (R % 16 == 0): blocks of 16 consecutive
+    rows of one column, under the per-tensor scale s_g.  Returned transposed,
+    the K-major layout a GEMM contracting over R reads: packed codes
+    [N, R/2] (element 2i in the low nibble) and E4M3 block scales [N, R/16]."""
+    return nvfp4_quantize_rows(np.asarray(v, dtype=np.float32).T, s_g)
+
+
+def grouped_gemm_nvfp4(Aq, As, sgA, Bq, Bs, sgB, rt: "Routing") -> np.ndarray:
+    """Grouped GEMM on NVFP4 operands ([MoE-Fusion], "Fusing MXFP8 and NVFP4
+    quantisation": the NVFP4 recipe, E2M1 values with an E4M3 scale per 16
+    elements and a per-tensor float32 scale).  Each operand is dequantised
+    (v = e2m1(q) * e4m3(s_b) / s_g, exact in float64) and multiplied:
+    y[rows of e] = A[rows] @ B[e]^T for the expert's count rows, pad rows 0.
+    Aq [R, K/2], As [R, K/16]; Bq [E, N, K/2], Bs [E, N, K/16]; returns the
+    float32 value handed to the output rounding."""
+    A = nvfp4_dequantize(np.asarray(Aq), np.asarray(As), sgA)
+    B = np.stack([nvfp4_dequantize(np.asarray(Bq[e]), np.asarray(Bs[e]), sgB) for e in range(rt.E)])
+    return grouped_gemm_rows(A, B, rt).astype(np.float32)
+
+
 def bf16_round(x) -> np.ndarray:
     """float -> nearest bfloat16 (ties to even), via float32 (the kernel's
     value is a float32), returned as float64."""

@@ -131,3 +131,40 @@ def test_nvfp4_error_bound_random():
     # the block scale itself is rounded (<= 1/16 relative), values may saturate by that much
     assert np.all(err <= 1.0 + 6 * 0.0625 + 1e-6)
     assert math.isclose(float(sg), 2688.0 / np.float32(amax), rel_tol=1e-6)
+
+
+def test_nvfp4_cols_hand_worked():
+    """Column-wise NVFP4 with amax_tensor 6: s_g = 448 * 6 / 6 = 448; column 0
+    holds 6, 3, 0, ... (block amax 6 -> s_b = E4M3(6 / 6 * 448) = 448, code
+    0x7E; elements E2M1(v * 448 / 448): 6 -> 7, 3 -> 5, 0 -> 0, so the first
+    byte is 7 | 5 << 4 = 0x57); column 1 holds -0.5 in row 15 only (block amax
+    0.5 -> s_b = E4M3(0.5 / 6 * 448) = E4M3(37.33) = 36 = 1.125 * 2^5 (code 0x61, the
+    nearer of 36 and 40), element
+    E2M1(-0.5 * 448 / 36) = E2M1(-6.22) = -6 saturated (code 0xF), the high
+    nibble of byte 7)."""
+    v = np.zeros((16, 2))
+    v[0, 0], v[1, 0] = 6.0, 3.0
+    v[15, 1] = -0.5
+    sg = O.nvfp4_global_scale(6.0)
+    assert float(sg) == 448.0
+    q, sb = O.nvfp4_quantize_cols(v, sg)
+    assert q.shape == (2, 8) and sb.shape == (2, 1)
+    assert sb[0, 0] == 0x7E and q[0, 0] == 0x57 and np.all(q[0, 1:] == 0)
+    assert sb[1, 0] == 0x61 and q[1, 7] == 0xF0 and np.all(q[1, :7] == 0)
+
+
+def test_grouped_gemm_nvfp4_closed_form():
+    """A = E2M1 1.0 (code 2) and B = 0.5 (code 1) everywhere, block scales 448
+    (0x7E) and per-tensor scales 448: both dequantise exactly (1.0 and 0.5),
+    so every real output is K * 0.5 and pad rows are 0."""
+    K, N = 64, 16
+    idx = np.repeat(np.arange(2), [5, 33])[:, None]
+    rt = O.route(idx, 0, 2)
+    Aq = np.full((rt.R_pad, K // 2), 0x22, dtype=np.uint8)
+    As = np.full((rt.R_pad, K // 16), 0x7E, dtype=np.uint8)
+    Bq = np.full((2, N, K // 2), 0x11, dtype=np.uint8)
+    Bs = np.full((2, N, K // 16), 0x7E, dtype=np.uint8)
+    y = O.grouped_gemm_nvfp4(Aq, As, 448.0, Bq, Bs, 448.0, rt)
+    real = rt.tok_of >= 0
+    assert y.dtype == np.float32
+    assert np.all(y[real] == K * 0.5) and np.all(y[~real] == 0)
