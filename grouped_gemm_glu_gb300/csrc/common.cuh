@@ -220,6 +220,19 @@ __device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
+// Block-scaled E2M1 x E2M1 MMA (NVFP4: packed 4-bit elements, K = 64 per
+// instruction) with one E4M3 scale per 16 elements of K: each row's four
+// scales of the instruction are the four bytes of its 32-bit scale column.
+__device__ __forceinline__ void umma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
 // Copies 32 rows x 16 bytes of shared memory into 4 tensor-memory columns of
 // each of the four 32-lane sub-partitions (the same data in each).
 __device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
@@ -244,6 +257,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
 }
 __host__ __device__ constexpr uint32_t idesc_mxf8_e8m0(int M, int N) {
   return ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
+}
+// kind::mxf4nvf4: E2M1 operands (format code 1 of that kind), E4M3 scales
+// (scale-format bit 23 clear), fp32 accumulate, both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_nvf4_e4m3(int M, int N) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 __device__ __forceinline__ uint32_t idesc_with_sf_ids(uint32_t idesc, uint32_t a_id, uint32_t b_id) {
   return idesc | (b_id << 4) | (a_id << 29);

@@ -52,6 +52,9 @@ constexpr int SF_STAGE = SF_BLOCK + SFB_BYTES;
 constexpr uint32_t TMEM_COLS = 512;
 // accumulator: columns 0..255 (one buffer); scales of A: 4 columns; of B: 8
 constexpr uint32_t SFA_COL = BN, SFB_COL = BN + 4;
+// NVFP4: the four MMAs of a k-block each read their own scale columns (4 for
+// the 128 rows of A, 8 for the 256 rows of B)
+constexpr uint32_t SFA4_COL = BN, SFB4_COL = BN + 16;
 constexpr int E_MAX = 1024;
 constexpr int EPI_ROW_BYTES = 256 + 16;   // staged output row (64 words + pad)
 constexpr int EPI_ROWS = 8;               // rows staged per pass
@@ -63,12 +66,16 @@ constexpr int TS_SUB = 32 * 128;          // TMA-store staging: one 32-row x 128
 // traffic): 3 stages and a whole 32 x 128-column block per epilogue warp
 // staged for two asynchronous TMA stores, so the stores stream while the
 // next tile's MMAs run.
-template <bool TS>
+// NV4 (NVFP4 operands): the same 128-byte k-blocks now hold 256 E2M1
+// elements and 16 E4M3 scales per row (four 512-byte scale blocks per
+// 128-row group, one per MMA), so a stage carries 4x the scales; 3 stages.
+template <bool TS, bool NV4 = false>
 struct Lay {
-  static constexpr int STAGES = TS ? 3 : 4;
+  static constexpr int STAGES = (TS || NV4) ? 3 : 4;
+  static constexpr int SF_ST = NV4 ? 4 * SF_STAGE : SF_STAGE;
   static constexpr int EPI_WARP_BYTES = TS ? 2 * TS_SUB : EPI_ROWS * EPI_ROW_BYTES;
   static constexpr int OFF_SF = STAGES * STAGE_BYTES;
-  static constexpr int OFF_EPI = (OFF_SF + STAGES * SF_STAGE + 1023) / 1024 * 1024;
+  static constexpr int OFF_EPI = (OFF_SF + STAGES * SF_ST + 1023) / 1024 * 1024;
   static constexpr int OFF_PREF = OFF_EPI + EPI_WARPS * EPI_WARP_BYTES;
   static constexpr int OFF_BARS = OFF_PREF + (E_MAX + 2) * 4;
   static constexpr int NUM_BARS = 2 * STAGES + 5;
@@ -111,6 +118,11 @@ struct Args {
   const float* row_scale;  // [R_cap] or null
   uint16_t* pre_out;       // [R_cap][N1] bf16 or null
   GluParams prm;
+  // M-grouped: real k-blocks per tile (KB counts 4-scale groups of the tiled
+  // scales: KB = KBr for MXFP8, 4 * KBr for NVFP4) and scale bytes per row
+  int KBr, sf_ks;
+  const float* sg_a;       // NVFP4: per-tensor scales of A and B (the product is divided by both)
+  const float* sg_b;
 };
 
 // Prefix in shared memory: M-grouped -> 128-row tiles per expert (from
@@ -190,7 +202,7 @@ __device__ __forceinline__ Tile decode(int t, const int32_t* pref, const Args& a
     ti.rows_valid = min(ti.rows_valid, ti.rows_pad);
     ti.kseg0 = 0;
     ti.kseg = a.K;
-    ti.num_kb = a.KB;  // the last k-block may be partial (K % 128 == 32, 64 or 96)
+    ti.num_kb = a.KBr;  // the last k-block may be partial (MXFP8: K % 128 == 32, 64 or 96)
     ti.sfa = (size_t)(pref[lo] + m_idx) * a.KB * SF_BLOCK;
     ti.sfb = ((size_t)lo * a.n_tiles_n + n_idx) * a.KB * SFB_BYTES;
   } else {
@@ -261,7 +273,7 @@ __global__ void __launch_bounds__(256) k_sf_tile(const Args a) {
     uint32_t v[4];
     uint8_t* dst;
     if (!a.kgrouped) {
-      const int ks = a.K / 32;
+      const int ks = a.sf_ks;
       if (it < nA) {
         const int mt = (int)(it / a.KB), kb = (int)(it % a.KB);
         const int e = find_group(pref, a.E, mt);
@@ -399,14 +411,20 @@ __device__ __forceinline__ void store_pass_tma(const CUtensorMap* tmO, const Til
 // rows, the quantising output stage (GroupGemm + Quantize), and the fused
 // activation of the MXFP8-input FC1 (GroupGemm + Activation +
 // Quantize/Transpose) with the activation forms of the bf16 kernel.
-enum Epi { EPI_BF16 = 0, EPI_QUANT = 1, EPI_GLU = 2, EPI_GLU_L1 = 3, EPI_GLU_L2 = 4, EPI_GLU_L3 = 5, EPI_ELT = 6 };
+enum Epi { EPI_BF16 = 0, EPI_QUANT = 1, EPI_GLU = 2, EPI_GLU_L1 = 3, EPI_GLU_L2 = 4, EPI_GLU_L3 = 5, EPI_ELT = 6,
+           // NVFP4 operands (kind::mxf4nvf4, E4M3 scales per 16 elements), bf16 rows divided by
+           // the two per-tensor scales
+           EPI_NV4 = 7 };
 __host__ __device__ constexpr bool epi_glu(int k) { return k >= EPI_GLU && k <= EPI_GLU_L3; }
 
 template <bool TS, int EPI>
 __global__ void __launch_bounds__(THREADS, 1)
     k_grouped_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmO, const Args a) {
-  using L = Lay<TS>;
+  constexpr bool NV4 = EPI == EPI_NV4;
+  using L = Lay<TS, NV4>;
+  constexpr int SF_ST = L::SF_ST;
+  constexpr int SF_MUL = NV4 ? 4 : 1;  // 512-byte scale blocks per 128-row group and k-block
   constexpr int STAGES = L::STAGES;
   constexpr int OFF_SF = L::OFF_SF, OFF_EPI = L::OFF_EPI, OFF_PREF = L::OFF_PREF, OFF_BARS = L::OFF_BARS,
                 OFF_MISC = L::OFF_MISC, EPI_WARP_BYTES = L::EPI_WARP_BYTES;
@@ -473,8 +491,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           uint8_t* dst = tiles + stage * STAGE_BYTES;
-          uint8_t* sdst = sf + stage * SF_STAGE;
-          mbar_arrive_expect_tx(full + stage, STAGE_BYTES + SF_STAGE);
+          uint8_t* sdst = sf + stage * SF_ST;
+          mbar_arrive_expect_tx(full + stage, STAGE_BYTES + SF_ST);
           if (!a.kgrouped) {
             tma_load_2d(dst, &tmA, full + stage, kb * BK, ti.m0);
             tma_load_3d(dst + A_TILE, &tmB, full + stage, kb * BK, ti.n0, ti.e);
@@ -482,8 +500,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             tma_load_2d(dst, &tmA, full + stage, ti.kseg0 + kb * BK, ti.m0);
             tma_load_2d(dst + A_TILE, &tmB, full + stage, ti.kseg0 + kb * BK, ti.n0);
           }
-          bulk_load(sdst, a.sfa_t + ti.sfa + (size_t)kb * SF_BLOCK, SF_BLOCK, full + stage);
-          bulk_load(sdst + SF_BLOCK, a.sfb_t + ti.sfb + (size_t)kb * SFB_BYTES, SFB_BYTES, full + stage);
+          bulk_load(sdst, a.sfa_t + ti.sfa + (size_t)kb * SF_MUL * SF_BLOCK, SF_MUL * SF_BLOCK, full + stage);
+          bulk_load(sdst + SF_MUL * SF_BLOCK, a.sfb_t + ti.sfb + (size_t)kb * SF_MUL * SFB_BYTES, SF_MUL * SFB_BYTES,
+                    full + stage);
           issued |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -502,7 +521,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp == MMA_WARP) {
     if (lane == 0) {
-      const uint32_t idesc = idesc_mxf8_e8m0(BM, BN);
+      const uint32_t idesc = NV4 ? idesc_nvf4_e4m3(BM, BN) : idesc_mxf8_e8m0(BM, BN);
       int stage = 0;
       uint32_t phase = 0;
       int lt = 0;
@@ -522,15 +541,34 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_fence_after();
           const uint32_t a_addr = smem_u32(tiles + stage * STAGE_BYTES);
           const uint32_t b_addr = a_addr + A_TILE;
-          const uint32_t sf_addr = smem_u32(sf + stage * SF_STAGE);
-          tc_cp_32x128b_x4(tmem_base + SFA_COL, sdesc_noswizzle(sf_addr, 128));
-          tc_cp_32x128b_x4(tmem_base + SFB_COL, sdesc_noswizzle(sf_addr + SF_BLOCK, 128));
-          tc_cp_32x128b_x4(tmem_base + SFB_COL + 4, sdesc_noswizzle(sf_addr + 2 * SF_BLOCK, 128));
-          const int nsub = min(4, (ti.kseg - kb * BK) / 32);
-          for (int k = 0; k < nsub; ++k) {
-            umma_mxf8(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32), sdesc_kmajor_sw128(b_addr + k * 32),
-                      idesc_with_sf_ids(idesc, (uint32_t)k, (uint32_t)k), tmem_base + SFA_COL, tmem_base + SFB_COL,
-                      (kb | k) != 0 ? 1u : 0u);
+          const uint32_t sf_addr = smem_u32(sf + stage * SF_ST);
+          if (NV4) {
+            // four MMAs of K = 64 E2M1 elements (32 bytes of the 128-byte
+            // rows), each with its own 4 scale bytes per row: MMA k's block
+            // of A scales goes to columns SFA4 + 4k, its two blocks of B
+            // scales to SFB4 + 8k (rows 0..127) and SFB4 + 8k + 4
+            const int nsub = min(4, (ti.kseg - kb * 2 * BK) / 64);
+            for (int k = 0; k < nsub; ++k) {
+              tc_cp_32x128b_x4(tmem_base + SFA4_COL + 4 * k, sdesc_noswizzle(sf_addr + k * SF_BLOCK, 128));
+              tc_cp_32x128b_x4(tmem_base + SFB4_COL + 8 * k,
+                               sdesc_noswizzle(sf_addr + 4 * SF_BLOCK + k * SFB_BYTES, 128));
+              tc_cp_32x128b_x4(tmem_base + SFB4_COL + 8 * k + 4,
+                               sdesc_noswizzle(sf_addr + 4 * SF_BLOCK + k * SFB_BYTES + SF_BLOCK, 128));
+            }
+            for (int k = 0; k < nsub; ++k) {
+              umma_nvf4(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32), sdesc_kmajor_sw128(b_addr + k * 32), idesc,
+                        tmem_base + SFA4_COL + 4 * k, tmem_base + SFB4_COL + 8 * k, (kb | k) != 0 ? 1u : 0u);
+            }
+          } else {
+            tc_cp_32x128b_x4(tmem_base + SFA_COL, sdesc_noswizzle(sf_addr, 128));
+            tc_cp_32x128b_x4(tmem_base + SFB_COL, sdesc_noswizzle(sf_addr + SF_BLOCK, 128));
+            tc_cp_32x128b_x4(tmem_base + SFB_COL + 4, sdesc_noswizzle(sf_addr + 2 * SF_BLOCK, 128));
+            const int nsub = min(4, (ti.kseg - kb * BK) / 32);
+            for (int k = 0; k < nsub; ++k) {
+              umma_mxf8(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32), sdesc_kmajor_sw128(b_addr + k * 32),
+                        idesc_with_sf_ids(idesc, (uint32_t)k, (uint32_t)k), tmem_base + SFA_COL,
+                        tmem_base + SFB_COL, (kb | k) != 0 ? 1u : 0u);
+            }
           }
           tc_commit(empty + stage);
           if (++stage == STAGES) {
@@ -680,6 +718,13 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 128; ++i) v[i] = 0.0f;
       }
+      if (NV4) {
+        // NVFP4 values are e2m1 * s_b / s_g: the MMA applied the block scales,
+        // the two per-tensor scales divide the product here
+        const float g = 1.0f / (__ldg(a.sg_a) * __ldg(a.sg_b));
+#pragma unroll
+        for (int i = 0; i < 128; ++i) v[i] *= g;
+      }
       if (TS) {
         if (out_es == 4) {
           store_pass_tma<true, 0>(&tmO, ti, v, stg, q, h, lane, a.N);
@@ -728,8 +773,9 @@ static moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const
                     : epi == EPI_GLU_L2 ? (const void*)k_grouped_mx<false, EPI_GLU_L2>
                     : epi == EPI_GLU_L3 ? (const void*)k_grouped_mx<false, EPI_GLU_L3>
                     : epi == EPI_ELT    ? (const void*)k_grouped_mx<false, EPI_ELT>
+                    : epi == EPI_NV4    ? (const void*)k_grouped_mx<false, EPI_NV4>
                                         : (const void*)k_grouped_mx<false, EPI_BF16>;
-  const int smem = ts ? Lay<true>::SMEM_BYTES : Lay<false>::SMEM_BYTES;
+  const int smem = ts ? Lay<true>::SMEM_BYTES : epi == EPI_NV4 ? Lay<false, true>::SMEM_BYTES : Lay<false>::SMEM_BYTES;
   if (!set_smem_limit(kfn, smem)) return MOE_ERR_CUDA;
   const int sms = sm_count();
   long long sgrid = (sf_items + 7) / 8;
@@ -753,6 +799,8 @@ static moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const
     launch_kernel<false, EPI_GLU_L3>(grid, smem, tmA, tmB, tmA, a, stream);
   else if (epi == EPI_ELT)
     launch_kernel<false, EPI_ELT>(grid, smem, tmA, tmB, tmA, a, stream);
+  else if (epi == EPI_NV4)
+    launch_kernel<false, EPI_NV4>(grid, smem, tmA, tmB, tmA, a, stream);
   else
     launch_kernel<false, EPI_BF16>(grid, smem, tmA, tmB, tmA, a, stream);
   count_launch(2);
@@ -765,8 +813,12 @@ static int n_tiles(int N) { return (N + BN - 1) / BN; }
 static int k_blocks(int K) { return (K + BK - 1) / BK; }
 static int m_tiles_of(int M) { return (M + BM - 1) / BM; }
 
-static void fc2_ws_parts(int E, int K, int N, int R_cap, size_t* a_bytes, size_t* b_bytes) {
-  const size_t KB = (size_t)k_blocks(K);
+// Tiled-scale workspace of an M-grouped call: MXFP8 has one 512-byte block per
+// (128-row group, 128-element k-block); NVFP4 four per 256-element k-block.
+static size_t sf_kblocks(int K, bool nv4) { return nv4 ? 4 * (size_t)((K + 255) / 256) : (size_t)k_blocks(K); }
+
+static void fc2_ws_parts(int E, int K, int N, int R_cap, size_t* a_bytes, size_t* b_bytes, bool nv4 = false) {
+  const size_t KB = sf_kblocks(K, nv4);
   *a_bytes = align_up(((size_t)R_cap / BM + E) * KB * SF_BLOCK);
   *b_bytes = align_up((size_t)E * n_tiles(N) * KB * SFB_BYTES);
 }
@@ -784,9 +836,10 @@ using namespace moeglu;
 
 extern "C" size_t moe_grouped_fc2_workspace_size(int E, int K, int N, int R_cap) {
   if (E <= 0 || K <= 0 || N <= 0 || R_cap <= 0) return 0;
-  size_t a, b;
+  size_t a, b, a4, b4;
   gmx::fc2_ws_parts(E, K, N, R_cap, &a, &b);
-  return a + b;
+  gmx::fc2_ws_parts(E, K, N, R_cap, &a4, &b4, true);
+  return a + b > a4 + b4 ? a + b : a4 + b4;  // enough for either block-scaled operand type
 }
 
 extern "C" size_t moe_grouped_wgrad_workspace_size(int E, int M, int N, int R_cap) {
@@ -810,6 +863,63 @@ extern "C" moe_status_t moe_grouped_fc2_fwd(const moe_in_t* A, const moe_in_t* W
   if (A->dtype == MOE_IN_BF16)
     return grouped_gemm_bf16_out(A->data, W->data, counts, offsets, E, K, N, R_cap, out_mode, out, ws, ws_bytes,
                                  sm_margin, status, as_stream(stream));
+  if (A->dtype == MOE_IN_NVFP4) {
+    // NVFP4 operands: packed E2M1 (K/2 bytes per row), E4M3 scales per 16
+    // elements (K/16 bytes per row), per-tensor scales; bf16 output only
+    const uint8_t* Aq4 = static_cast<const uint8_t*>(A->data);
+    const uint8_t* Wq4 = static_cast<const uint8_t*>(W->data);
+    if (!A->scale || !W->scale || !A->global_scale || !W->global_scale || !ws) return MOE_ERR_ARG;
+    if (K % 64) return MOE_ERR_ARG;
+    if (out_mode != MOE_OUT_BF16) return MOE_ERR_UNSUPPORTED;
+    if (!out->y || !aligned16(out->y) || !aligned16(Aq4) || !aligned16(Wq4) ||
+        (reinterpret_cast<uintptr_t>(A->scale) & 3) || (reinterpret_cast<uintptr_t>(W->scale) & 3) ||
+        (reinterpret_cast<uintptr_t>(ws) & 255))
+      return MOE_ERR_ARG;
+    size_t a4, b4;
+    fc2_ws_parts(E, K, N, R_cap, &a4, &b4, true);
+    if (ws_bytes < a4 + b4) return MOE_ERR_ARG;
+    CUtensorMap tA, tB;
+    {
+      const uint64_t dims[2] = {(uint64_t)K / 2, (uint64_t)R_cap};
+      const uint64_t strides[1] = {(uint64_t)K / 2};
+      const uint32_t box[2] = {BK, BM};
+      if (!encode_tmap(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, Aq4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+        return MOE_ERR_CUDA;
+    }
+    {
+      const uint64_t dims[3] = {(uint64_t)K / 2, (uint64_t)N, (uint64_t)E};
+      const uint64_t strides[2] = {(uint64_t)K / 2, (uint64_t)N * (K / 2)};
+      const uint32_t box[3] = {BK, BN, 1};
+      if (!encode_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, Wq4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+        return MOE_ERR_CUDA;
+    }
+    Args a{};
+    a.counts = counts;
+    a.offsets = offsets;
+    a.E = E;
+    a.N = N;
+    a.K = K;
+    a.R_cap = R_cap;
+    a.n_tiles_n = n_tiles(N);
+    a.KB = (int)sf_kblocks(K, true);
+    a.KBr = (K + 255) / 256;
+    a.sf_ks = K / 16;
+    a.As = A->scale;
+    a.Bs = W->scale;
+    a.sfa_t = static_cast<uint8_t*>(ws);
+    a.sfb_t = static_cast<uint8_t*>(ws) + a4;
+    a.out = out->y;
+    a.status = status;
+    a.wait_ns = g_wait_limit_ns.load();
+    a.out_mode = MOE_OUT_BF16;
+    a.out_N = N;
+    a.sg_a = A->global_scale;
+    a.sg_b = W->global_scale;
+    const long long mt_bound = (long long)R_cap / BM + E;
+    const long long bound = mt_bound * a.n_tiles_n;
+    const long long sf_items = mt_bound * a.KB + (long long)E * 2 * a.n_tiles_n * a.KB;
+    return launch(tA, tB, nullptr, a, bound, sf_items, sm_margin, as_stream(stream), EPI_NV4);
+  }
   if (A->dtype != MOE_IN_MXFP8) return MOE_ERR_ARG;
   const uint8_t* Aq = static_cast<const uint8_t*>(A->data);
   const uint8_t* Wq = static_cast<const uint8_t*>(W->data);
@@ -856,6 +966,8 @@ extern "C" moe_status_t moe_grouped_fc2_fwd(const moe_in_t* A, const moe_in_t* W
   a.n_tiles_n = n_tiles(N);
   a.m_tiles = 0;
   a.KB = k_blocks(K);
+  a.KBr = a.KB;
+  a.sf_ks = K / 32;
   a.KG = 0;
   a.As = As;
   a.Bs = Ws;
@@ -934,6 +1046,8 @@ extern "C" moe_status_t moe_grouped_fc1_glu_quant_fwd_mxfp8(
   a.kgrouped = 0;
   a.n_tiles_n = n_tiles(N1);
   a.KB = k_blocks(H);
+  a.KBr = a.KB;
+  a.sf_ks = H / 32;
   a.As = xs;
   a.Bs = W1s;
   a.sfa_t = static_cast<uint8_t*>(ws);

@@ -269,13 +269,79 @@ __global__ void __launch_bounds__(256) k_quant_cols(const __grid_constant__ CUte
   }
 }
 
+// One NVFP4 block of 16 values under the per-tensor scale sg: returns the
+// E4M3 block-scale byte and writes the 16 E2M1 codes (element 2i in the low
+// nibble of byte i) to w[0..1].  s_b = E4M3(fp32(amax_b / 6) * sg),
+// q = E2M1(fp32(v * fp32(sg / s_b))), each step one fp32 operation.
+__device__ __forceinline__ uint32_t nvfp4_block16(const float* v, float sg, uint32_t* w) {
+  float ab = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) ab = fmaxf(ab, fabsf(v[j]));
+  const float sbf = (ab / 6.0f) * sg;
+  const __nv_fp8_storage_t sc = __nv_cvt_float_to_fp8(sbf, __NV_SATFINITE, __NV_E4M3);
+  const float sbv = __half2float(__half(__nv_cvt_fp8_to_halfraw(sc, __NV_E4M3)));
+  const float inv = sbv > 0.0f ? sg / sbv : 0.0f;
+  w[0] = w[1] = 0;
+#pragma unroll
+  for (int j = 0; j < 16; j += 2) {
+    const uint32_t c2 =
+        (uint32_t)__nv_cvt_float2_to_fp4x2(make_float2(v[j] * inv, v[j + 1] * inv), __NV_E2M1, cudaRoundNearest);
+    w[j / 8] |= (c2 & 0xFFu) << (8 * ((j % 8) / 2));
+  }
+  return (uint32_t)sc;
+}
+
+__device__ __forceinline__ float nvfp4_global_scale(float am) {
+  return (am > 0.0f && am <= 3.402823466e38f) ? 2688.0f / am : 1.0f;
+}
+
+// Column-wise NVFP4 (the K-major copy of a weight whose contraction runs
+// along its rows): src [G][R][C] bf16 -> q [G][C][R/2], s [G][C][R/16], one
+// thread per (g, 16-row block, column); neighbouring threads take
+// neighbouring columns, so each of the 16 row loads is coalesced.
+__global__ void __launch_bounds__(256) k_nvfp4_cast_cols(const uint16_t* __restrict__ src, int G, int R, int C,
+                                                         const float* __restrict__ amax, uint8_t* __restrict__ q,
+                                                         uint8_t* __restrict__ s, float* __restrict__ s_global) {
+  const float sg = nvfp4_global_scale(*amax);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *s_global = sg;
+  const int nb = R / 16;
+  const size_t total = (size_t)G * nb * C;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const int c = (int)(i % C);
+    const size_t rest = i / C;
+    const int rb = (int)(rest % nb);
+    const int g = (int)(rest / nb);
+    const uint16_t* p = src + ((size_t)g * R + (size_t)rb * 16) * C + c;
+    float v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float((uint32_t)__ldg(p + (size_t)j * C) << 16);
+    uint32_t w[2];
+    const uint32_t sc = nvfp4_block16(v, sg, w);
+    const size_t col = (size_t)g * C + c;
+    *reinterpret_cast<uint2*>(q + col * (R / 2) + (size_t)rb * 8) = make_uint2(w[0], w[1]);
+    s[col * nb + rb] = (uint8_t)sc;
+  }
+}
+
+// max |x| over a bf16 tensor of n8 16-byte words (x 16-byte aligned) into
+// *amax as ordered float bits (the caller's call zeroes it first).
+__global__ void __launch_bounds__(256) k_amax_bf16(const uint4* __restrict__ x, size_t n8, float* __restrict__ amax) {
+  uint32_t m = 0;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+    const uint4 w = __ldg(x + i);
+    const uint32_t a = max(max(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu), max(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
+    m = max(m, max(a & 0xFFFFu, a >> 16));
+  }
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  if ((threadIdx.x & 31) == 0 && m != 0) atomicMax(reinterpret_cast<int*>(amax), (int)(m << 16));
+}
+
 // NVFP4: one thread per 16-element block of a row < offsets[E].
 __global__ void __launch_bounds__(256) k_nvfp4_cast(const uint16_t* __restrict__ y, const float* __restrict__ amax,
                                                     const int32_t* __restrict__ offsets, int E, int N,
                                                     uint8_t* __restrict__ q, uint8_t* __restrict__ s,
                                                     float* __restrict__ s_global) {
-  const float am = *amax;
-  const float sg = (am > 0.0f && am <= 3.402823466e38f) ? 2688.0f / am : 1.0f;
+  const float sg = nvfp4_global_scale(*amax);
   if (blockIdx.x == 0 && threadIdx.x == 0) *s_global = sg;
   const int R = __ldg(offsets + E);
   const int nb = N / 16;
@@ -286,20 +352,8 @@ __global__ void __launch_bounds__(256) k_nvfp4_cast(const uint16_t* __restrict__
     float v[16] = {bf16_lo(a.x), bf16_hi(a.x), bf16_lo(a.y), bf16_hi(a.y), bf16_lo(a.z), bf16_hi(a.z),
                    bf16_lo(a.w), bf16_hi(a.w), bf16_lo(b.x), bf16_hi(b.x), bf16_lo(b.y), bf16_hi(b.y),
                    bf16_lo(b.z), bf16_hi(b.z), bf16_lo(b.w), bf16_hi(b.w)};
-    float ab = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) ab = fmaxf(ab, fabsf(v[j]));
-    const float sbf = (ab / 6.0f) * sg;
-    const __nv_fp8_storage_t sc = __nv_cvt_float_to_fp8(sbf, __NV_SATFINITE, __NV_E4M3);
-    const float sbv = __half2float(__half(__nv_cvt_fp8_to_halfraw(sc, __NV_E4M3)));
-    const float inv = sbv > 0.0f ? sg / sbv : 0.0f;
-    uint32_t w[2] = {0, 0};
-#pragma unroll
-    for (int j = 0; j < 16; j += 2) {
-      const uint32_t c2 =
-          (uint32_t)__nv_cvt_float2_to_fp4x2(make_float2(v[j] * inv, v[j + 1] * inv), __NV_E2M1, cudaRoundNearest);
-      w[j / 8] |= (c2 & 0xFFu) << (8 * ((j % 8) / 2));
-    }
+    uint32_t w[2];
+    const uint32_t sc = nvfp4_block16(v, sg, w);
     *reinterpret_cast<uint2*>(q + i * 8) = make_uint2(w[0], w[1]);
     s[i] = (uint8_t)sc;
   }
@@ -485,6 +539,25 @@ extern "C" moe_status_t moe_nvfp4_cast(const moe_bf16* y, const float* amax, con
   if (!aligned16(y) || (reinterpret_cast<uintptr_t>(q) & 7)) return MOE_ERR_ARG;
   k_nvfp4_cast<<<grid_for((size_t)R_cap * (N / 16), 256), 256, 0, as_stream(stream)>>>(y, amax, offsets, E, N, q, s,
                                                                                       s_global);
+  count_launch();
+  return launch_status();
+}
+
+extern "C" moe_status_t moe_amax_bf16(const moe_bf16* x, size_t n, float* amax, moe_stream_t stream) {
+  if (!x || !amax || n == 0 || (n % 8) || !aligned16(x)) return MOE_ERR_ARG;
+  cudaStream_t st = as_stream(stream);
+  if (cudaMemsetAsync(amax, 0, sizeof(float), st) != cudaSuccess) return MOE_ERR_CUDA;
+  k_amax_bf16<<<grid_for(n / 8, 256), 256, 0, st>>>(reinterpret_cast<const uint4*>(x), n / 8, amax);
+  count_launch();
+  return launch_status();
+}
+
+extern "C" moe_status_t moe_nvfp4_cast_cols(const moe_bf16* src, int G, int R, int C, const float* amax, uint8_t* q,
+                                            uint8_t* s, float* s_global, moe_stream_t stream) {
+  if (!src || !amax || !q || !s || !s_global || G <= 0 || R <= 0 || (R % 16) || C <= 0) return MOE_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(q) & 7)) return MOE_ERR_ARG;
+  k_nvfp4_cast_cols<<<grid_for((size_t)G * (R / 16) * C, 256), 256, 0, as_stream(stream)>>>(
+      reinterpret_cast<const uint16_t*>(src), G, R, C, amax, q, s, s_global);
   count_launch();
   return launch_status();
 }

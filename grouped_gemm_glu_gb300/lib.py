@@ -31,16 +31,21 @@ class ActOut(C.Structure):
                 ("rht_amax", C.c_void_p), ("rht_signs", C.c_uint32)]
 
 
-IN_BF16, IN_MXFP8 = 0, 1
+IN_BF16, IN_MXFP8, IN_NVFP4 = 0, 1, 2
 
 
 class InT(C.Structure):
-    _fields_ = [("dtype", C.c_int32), ("data", C.c_void_p), ("scale", C.c_void_p)]
+    _fields_ = [("dtype", C.c_int32), ("data", C.c_void_p), ("scale", C.c_void_p), ("global_scale", C.c_void_p)]
 
 
-def in_operand(data_ptr: int, scale_ptr: int | None = None) -> InT:
-    """A GEMM operand: bf16 when scale_ptr is None, else MXFP8 codes + scales."""
-    return InT(IN_BF16 if scale_ptr is None else IN_MXFP8, data_ptr, scale_ptr)
+def in_operand(data_ptr: int, scale_ptr: int | None = None, global_scale_ptr: int | None = None) -> InT:
+    """A GEMM operand: bf16 when scale_ptr is None, MXFP8 codes + scales, or
+    NVFP4 codes + block scales + per-tensor scale when global_scale_ptr is set."""
+    if scale_ptr is None:
+        return InT(IN_BF16, data_ptr, None, None)
+    if global_scale_ptr is None:
+        return InT(IN_MXFP8, data_ptr, scale_ptr, None)
+    return InT(IN_NVFP4, data_ptr, scale_ptr, global_scale_ptr)
 
 
 def glu_params(act: str = "swiglu", alpha: float = 1.0, up_offset: float = 0.0,
@@ -75,6 +80,8 @@ _SIGS = {
     "moe_feature_scale_grad": [P, I, P, I, I, P, P],
     "moe_nvfp4_cast": [P, P, P, P, I, I, I, P, P, P, P],
     "moe_glu_act": [P, P, P, I, I, I, C.POINTER(GluParams), P, P],
+    "moe_amax_bf16": [P, SZ, P, P],
+    "moe_nvfp4_cast_cols": [P, I, I, I, P, P, P, P, P],
     "moe_dglu_act": [P, P, P, P, I, I, I, C.POINTER(GluParams), P, P],
     "moe_route_permute_noalloc": [P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P, P],
     "moe_route_noalloc_max_scratch_bytes": ([], SZ),

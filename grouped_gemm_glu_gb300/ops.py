@@ -265,6 +265,50 @@ def fc2_fwd(Aq, As, Wq, Ws, counts, offsets, sm_margin: int = 0, status=None, ou
     return o["y"] if out_mode == L.OUT_BF16 else o
 
 
+def fc2_fwd_nvfp4(Aq, As, sgA, Wq, Ws, sgW, counts, offsets, sm_margin: int = 0, status=None, out=None):
+    """GroupGemm on NVFP4 operands: y [R_cap, N] bf16 = A . W[e]^T with
+    A = packed E2M1 [R_cap, K/2] + E4M3 scales [R_cap, K/16] + per-tensor
+    scale sgA (device float [1]), W [E, N, K/2] + [E, N, K/16] + sgW."""
+    lib = L.load()
+    dev = _dev(Aq)
+    R_cap, K2 = Aq.shape
+    K = 2 * K2
+    E, N, _ = Wq.shape
+    y = out if out is not None else torch.empty(R_cap, N, dtype=torch.bfloat16, device=dev)
+    st = status if status is not None else new_status(dev)
+    a_in = L.in_operand(Aq.data_ptr(), As.data_ptr(), sgA.data_ptr())
+    w_in = L.in_operand(Wq.data_ptr(), Ws.data_ptr(), sgW.data_ptr())
+    ws_bytes = lib.moe_grouped_fc2_workspace_size(E, K, N, R_cap)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    ao = _act_out(y=y)
+    L.check(lib.moe_grouped_fc2_fwd(C.byref(a_in), C.byref(w_in), _p(counts), _p(offsets), E, K, N, R_cap,
+                                    L.OUT_BF16, C.byref(ao), _p(ws), ws_bytes, sm_margin, _p(st), _s()),
+            "moe_grouped_fc2_fwd (NVFP4)")
+    return y
+
+
+def amax_bf16(x):
+    """max |x| of a bf16 tensor as a device float [1]."""
+    lib = L.load()
+    a = torch.empty(1, dtype=torch.float32, device=_dev(x))
+    L.check(lib.moe_amax_bf16(_p(x), x.numel(), _p(a), _s()), "moe_amax_bf16")
+    return a
+
+
+def nvfp4_cast_cols(src, amax):
+    """Column-wise NVFP4 of src [G, R, C] (or [R, C]) bf16: (q [G, C, R/2],
+    s [G, C, R/16], s_global [1])."""
+    lib = L.load()
+    dev = _dev(src)
+    s3 = src if src.dim() == 3 else src.unsqueeze(0)
+    G, R, Cc = s3.shape
+    q = torch.empty(G, Cc, R // 2, dtype=torch.uint8, device=dev)
+    s = torch.empty(G, Cc, R // 16, dtype=torch.uint8, device=dev)
+    sg = torch.empty(1, dtype=torch.float32, device=dev)
+    L.check(lib.moe_nvfp4_cast_cols(_p(s3), G, R, Cc, _p(amax), _p(q), _p(s), _p(sg), _s()), "moe_nvfp4_cast_cols")
+    return q, s, sg
+
+
 def wgrad(Aq_col, As_col, Bq_col, Bs_col, counts, offsets, out_f32: bool = False, sm_margin: int = 0,
           status=None, out=None):
     """D [E, M, N] = per-expert contraction over the expert's rows of the

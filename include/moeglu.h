@@ -129,13 +129,17 @@ typedef struct {
 /* Operand of a grouped GEMM that takes either precision. */
 typedef enum {
   MOE_IN_BF16 = 0,  /* bf16 values */
-  MOE_IN_MXFP8 = 1  /* E4M3 codes with E8M0 scales, one per 32 elements along K */
+  MOE_IN_MXFP8 = 1, /* E4M3 codes with E8M0 scales, one per 32 elements along K */
+  MOE_IN_NVFP4 = 2  /* packed E2M1 codes (element 2i in the low nibble of byte i) with E4M3
+                       scales, one per 16 elements along K, and one fp32 per-tensor scale s_g:
+                       value = e2m1 * s_b / s_g (moe_nvfp4_cast, moe_nvfp4_cast_cols) */
 } moe_in_dtype_t;
 
 typedef struct {
-  int32_t dtype;          /* moe_in_dtype_t */
-  const void* data;       /* the values (bf16) or codes (E4M3) */
-  const uint8_t* scale;   /* MOE_IN_MXFP8 only: the E8M0 scales */
+  int32_t dtype;              /* moe_in_dtype_t */
+  const void* data;           /* the values (bf16) or codes (E4M3, packed E2M1) */
+  const uint8_t* scale;       /* MXFP8: the E8M0 scales; NVFP4: the E4M3 block scales */
+  const float* global_scale;  /* NVFP4 only: device pointer to s_g */
 } moe_in_t;
 
 /* ---------------------------------------------------------------------- */
@@ -246,9 +250,10 @@ MOE_API moe_status_t moe_quantize_mxfp8(const moe_bf16* src, int G, int R, int C
                                 const int32_t* counts, const int32_t* offsets, int E,
                                 uint8_t* q, uint8_t* s, int32_t* status, moe_stream_t stream);
 
-/* Bytes of device workspace moe_grouped_fc2_fwd needs with MXFP8 operands
- * (the scales of the visited tiles, rewritten in the order the tensor cores
- * read them); bf16 operands need none. */
+/* Bytes of device workspace moe_grouped_fc2_fwd needs with block-scaled
+ * (MXFP8 or NVFP4) operands: the scales of the visited tiles, rewritten in the
+ * order the tensor cores read them (enough for either type); bf16 operands
+ * need none. */
 MOE_API size_t moe_grouped_fc2_workspace_size(int E, int K, int N, int R_cap);
 
 /* GroupGemm + Quantize ([MoE-Fusion] "Boosting MoE Training Throughput with
@@ -270,6 +275,14 @@ MOE_API size_t moe_grouped_fc2_workspace_size(int E, int K, int N, int R_cap);
  *                 ws = moe_grouped_fc2_workspace_size() bytes, 256-byte
  *                 aligned.  K % 32 == 0, N % 32 == 0 (a partial last
  *                 128-wide k-block or 256-wide column tile is handled).
+ *   MOE_IN_NVFP4: packed E2M1 A [R_cap][K/2], W [E][N][K/2], E4M3 block
+ *                 scales [R_cap][K/16] / [E][N][K/16] (4-byte aligned) and
+ *                 the per-tensor scales; block-scaled MMA (kind::mxf4nvf4,
+ *                 16-element blocks); the product is divided by both s_g in
+ *                 the epilogue.  ws as for MXFP8.  K % 64 == 0, N % 32 == 0;
+ *                 out_mode must be MOE_OUT_BF16 (else MOE_ERR_UNSUPPORTED).
+ *                 ([MoE-Fusion] "Fusing MXFP8 and NVFP4 quantisation": the
+ *                 consumer of the forward's NVFP4 cast.)
  *   MOE_IN_BF16:  bf16, scale unused; kind::f16 MMA on CTA pairs; ws
  *                 nullable: with >= 256 bytes (16-byte aligned) it holds the
  *                 dynamic tile scheduler's counter, as for the fused FC1.
@@ -375,6 +388,21 @@ MOE_API moe_status_t moe_nvfp4_cast(const moe_bf16* y, const float* amax,
                             const int32_t* counts, const int32_t* offsets, int E,
                             int N, int R_cap, uint8_t* q, uint8_t* s, float* s_global,
                             moe_stream_t stream);
+
+/* max |x| over n bf16 values (n % 8 == 0, x 16-byte aligned) into *amax
+ * (device float; overwritten): the per-tensor amax an NVFP4 weight cast
+ * needs. */
+MOE_API moe_status_t moe_amax_bf16(const moe_bf16* x, size_t n, float* amax, moe_stream_t stream);
+
+/* Column-wise (transposed) NVFP4 cast of a weight whose contraction runs
+ * along its rows ([MoE-Fusion] "Fusing MXFP8 and NVFP4 quantisation"; e.g.
+ * W2 [E][F][H] for an NVFP4 FC2, K = F): src [G][R][C] bf16 -> q [G][C][R/2]
+ * (element 2i in the low nibble), s [G][C][R/16] E4M3, with the same
+ * two-level rule as moe_nvfp4_cast under s_g = 2688 / amax (1 if 0 or not
+ * finite), written to *s_global.  amax: device float (moe_amax_bf16).
+ * R % 16 == 0, q 8-byte aligned. */
+MOE_API moe_status_t moe_nvfp4_cast_cols(const moe_bf16* src, int G, int R, int C, const float* amax,
+                                         uint8_t* q, uint8_t* s, float* s_global, moe_stream_t stream);
 
 /* Standalone activation of the unfused path: pre [R][N1] bf16 -> y [R][F]
  * bf16 (rows >= offsets[E] untouched, pad rows 0).  F % 32 == 0; pre and y
