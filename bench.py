@@ -49,10 +49,17 @@ def load_peaks():
     return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sus": 1700.0, "src": "fallback"}
 
 
+SHAPE = {"dsv3": "DeepSeek-V3-shaped expert-parallel shard", "gptoss": "GPT-OSS-shaped layer",
+         "skew": "skewed-routing 64-expert layer", "skew_srelu": "skewed-routing 64-expert layer",
+         "tiny": "tiny MoE MLP"}
+
+
 def workload_desc(w):
-    return (f"{w.name}: DeepSeek-V3-shaped expert-parallel shard, T={w.T} H={w.H} experts "
+    fwd = ("NVFP4 forward (FC1 bf16 + amax -> E2M1/E4M3 casts -> block-scaled NVFP4 FC2), MXFP8 backward"
+           if w.out == "nvfp4" else "MXFP8 E4M3/E8M0 outputs + transposed copies")
+    return (f"{w.name}: {SHAPE.get(w.name, w.name)}, T={w.T} H={w.H} experts "
             f"{w.expert_begin}..{w.expert_begin + w.E - 1} of {w.n_experts}, top-{w.k}, F={w.F}, {w.act}, "
-            f"MXFP8 E4M3/E8M0 outputs + transposed copies; forward + backward")
+            f"{fwd}; forward + backward")
 
 
 def kernel_model(name, w, R, Rp):
@@ -75,8 +82,20 @@ def kernel_model(name, w, R, Rp):
         "wgrad_w1": (2 * R * N1 * H, (N1 + H) * R * (1 + 1 / 32) + E * N1 * H * 2, "fp8"),
         "wgrad_w2": (2 * R * F * H, (F + H) * R * (1 + 1 / 32) + E * F * H * 2, "fp8"),
         "permute_bwd": (0, R * H * 2 + T * H * 2 + T * k * 4, None),
+        # NVFP4 forward: FC1 writes bf16 y + amax; casts to E2M1 + E4M3 per 16; FP4 FC2
+        "fc1_glu_nvfp4": (2 * R * H * N1, E * N1 * H * 2 + R * H * 2 + R * N1 * 2 + R * F * 2, "bf16"),
+        "quant_a_nvfp4": (0, R * F * 2 + R * F * (1 / 2 + 1 / 16), None),
+        "amax_w2": (0, E * F * H * 2, None),
+        "quant_w2_nvfp4": (0, E * F * H * 2 + E * F * H * (1 / 2 + 1 / 16), None),
+        "fc2_nvfp4": (2 * R * F * H, E * H * F * (1 / 2 + 1 / 16) + R * F * (1 / 2 + 1 / 16) + R * H * 2, "fp4"),
+        "quant_a_col": (0, R * F * 2 + R * F * (1 + 1 / 32), None),
     }
     return m[name]
+
+
+# dense tensor peak of an arithmetic type: the measured bf16 figure times the
+# nominal dense ratio (fp8 2x, fp4 6x bf16)
+PEAK_RATIO = {"bf16": 1.0, "fp8": 2.0, "fp4": 6.0}
 
 
 class ClockSampler:
@@ -295,7 +314,7 @@ def main():
     else:
         params = L.glu_params(w.act)
     layer = MoeLayer(g["W1"], g["W2"], w.T, w.k, R_cap, params, b1=g.get("b1"), expert_begin=w.expert_begin,
-                     sm_margin=args.sm_margin, gated=w.gated)
+                     sm_margin=args.sm_margin, gated=w.gated, nvfp4_fwd=w.out == "nvfp4")
     X, I, P, DO = g["x"], g["topk_idx"], g["topk_prob"], g["dOut"]
     for _ in range(args.warmup):
         layer.step(X, I, P, DO)
@@ -417,10 +436,11 @@ def main():
 
     by_name = dict(layer.step_calls(X, I, P, DO))
     ufwd, ubwd = layer.forward_unfused_calls(), layer.backward_unfused_calls(layer.dY_perm)
-    for calls in ([("fc1_glu_quant", by_name["fc1_glu_quant"])], ufwd, [("dglu_quant", by_name["dglu_quant"])], ubwd):
+    fused_fc1 = [("fc1_glu_quant", layer.fc1_mxfp8_call())]
+    for calls in (fused_fc1, ufwd, [("dglu_quant", by_name["dglu_quant"])], ubwd):
         layer.run(calls)  # warm-up
     na = max(3, min(args.steps, 20))
-    f_ms = timed([("fc1_glu_quant", by_name["fc1_glu_quant"])], na)
+    f_ms = timed(fused_fc1, na)
     uf_ms = timed(ufwd, na)
     b_ms = timed([("dglu_quant", by_name["dglu_quant"])], na)
     ub_ms = timed(ubwd, na)
@@ -485,8 +505,8 @@ def main():
             # kernels timed one by one inside a short region run at the
             # burst clocks: the burst peak applies (fp8 = 2 x bf16, the
             # nominal dense ratio); the sustained figure is kept beside it
-            peak = peaks["bf16"] if dt == "bf16" else 2 * peaks["bf16"]
-            peak_sus = peaks["bf16_sus"] if dt == "bf16" else 2 * peaks["bf16_sus"]
+            peak = PEAK_RATIO[dt] * peaks["bf16"]
+            peak_sus = PEAK_RATIO[dt] * peaks["bf16_sus"]
             ent["TFLOP/s"] = round(fl / ms / 1e9, 1)
             ent["frac_of_tensor_peak"] = round(fl / ms / 1e9 / peak, 4)
             ent["frac_of_sustained_tensor_peak"] = round(fl / ms / 1e9 / peak_sus, 4)
@@ -505,7 +525,7 @@ def main():
     dom = max(names, key=lambda n: per_kernel[n])
     fl, by, dt = kernel_model(dom, w, R, Rp)
     ms = per_kernel[dom]
-    peak_t = (peaks["bf16"] if dt == "bf16" else 2 * peaks["bf16"]) if fl else None
+    peak_t = PEAK_RATIO[dt] * peaks["bf16"] if fl else None
     t_tensor = fl / (peak_t * 1e12) if fl else 0.0
     t_hbm = by / (peaks["hbm"] * 1e9)
     if fl and t_tensor >= t_hbm:
@@ -519,7 +539,7 @@ def main():
     if roof["bound"] == "hbm":
         roof["peak_source"] = f"of {peaks['src']} (HBM copy)"
     else:
-        roof["peak_source"] = f"of {peaks['src']} ({'bf16 burst' if dt == 'bf16' else 'fp8 = 2 x bf16 burst'})"
+        roof["peak_source"] = f"of {peaks['src']} ({dt} = {PEAK_RATIO[dt]:g} x bf16 burst)"
     roof["algorithmic"] = {"flops": fl, "bytes": by}
 
     # the metric's own quantity: TFLOP/s of the fused forward
@@ -529,7 +549,7 @@ def main():
     # short region), then both together
     fused = {}
     fl_sum = ms_sum = 0.0
-    for n in ("fc1_glu_quant", "dglu_quant"):
+    for n in ("fc1_glu_nvfp4" if w.out == "nvfp4" else "fc1_glu_quant", "dglu_quant"):
         fl_n, by_n, _ = kernel_model(n, w, R, Rp)
         tf = fl_n / per_kernel[n] / 1e9
         fused[n] = {"ms": round(per_kernel[n], 4), "TFLOP/s": round(tf, 1),

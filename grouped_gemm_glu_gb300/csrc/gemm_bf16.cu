@@ -1032,6 +1032,12 @@ static moe_status_t launch_pair(const void* A, const void* B, const Args& args, 
 
 template <int MODE>
 static moe_status_t launch(const void* A, const void* B, const Args& args, int sm_margin, cudaStream_t stream) {
+  // the NVFP4 amaxes are maxima over this call's tiles: they start from zero
+  // (memset nodes in stream order, so a captured step needs no other kernel)
+  if (args.out_mode == MOE_OUT_NVFP4) {
+    if (args.amax && cudaMemsetAsync(args.amax, 0, sizeof(float), stream) != cudaSuccess) return MOE_ERR_CUDA;
+    if (args.rht_amax && cudaMemsetAsync(args.rht_amax, 0, sizeof(float), stream) != cudaSuccess) return MOE_ERR_CUDA;
+  }
   if (g_cta_pairs.load()) return launch_pair<MODE>(A, B, args, sm_margin, stream);
   CUtensorMap tmA, tmB;
   {

@@ -766,6 +766,9 @@ static moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const
                            int epi = -1) {
   const bool ts = tmO != nullptr;
   if (epi < 0) epi = a.out_mode != MOE_OUT_BF16 ? EPI_QUANT : EPI_BF16;
+  if (!ts && a.out_mode == MOE_OUT_NVFP4 && a.amax &&
+      cudaMemsetAsync(a.amax, 0, sizeof(float), stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
   const void* kfn = ts                  ? (const void*)k_grouped_mx<true, EPI_BF16>
                     : epi == EPI_QUANT  ? (const void*)k_grouped_mx<false, EPI_QUANT>
                     : epi == EPI_GLU    ? (const void*)k_grouped_mx<false, EPI_GLU>

@@ -29,10 +29,14 @@ from .ops import _p, _s
 
 class MoeLayer:
     def __init__(self, W1, W2, T: int, k: int, R_cap: int, params: L.GluParams, b1=None,
-                 expert_begin: int = 0, sm_margin: int = 0, gated: bool = True, dynamic: bool = True):
+                 expert_begin: int = 0, sm_margin: int = 0, gated: bool = True, dynamic: bool = True,
+                 nvfp4_fwd: bool = False):
         """dynamic: the bf16 grouped GEMMs take their tiles from the dynamic
         scheduler (each call site has its own counter workspace); False runs
-        the static schedule."""
+        the static schedule.  nvfp4_fwd: the forward runs the NVFP4 recipe
+        (FC1 epilogue in NVFP4 mode -> NVFP4 cast of its output and of W2 ->
+        NVFP4 FC2); the backward stays MXFP8 (the FC2 weight gradient then
+        reads a column-wise MXFP8 cast of the bf16 FC1 output)."""
         self.lib = L.load()
         dev = W1.device
         self.dev = dev
@@ -106,6 +110,17 @@ class MoeLayer:
             self.ws_db_bytes = lib.moe_grouped_dglu_workspace_size(N1, R_cap)
         if self.ws_db_bytes:
             self.ws_db = z(self.ws_db_bytes, dt=u8)
+        self.nvfp4_fwd = nvfp4_fwd
+        if nvfp4_fwd:
+            f32 = torch.float32
+            self.a_y, self.a_amax = z(R_cap, F), z(1, dt=f32)
+            self.a_q4, self.a_s4, self.a_sg = z(R_cap, F // 2, dt=u8), z(R_cap, F // 16, dt=u8), z(1, dt=f32)
+            self.w2_amax = z(1, dt=f32)
+            self.W2q4, self.W2s4, self.w2_sg = z(E, H, F // 2, dt=u8), z(E, H, F // 16, dt=u8), z(1, dt=f32)
+            self.fc1_out4 = L.ActOut(None, None, None, None, self.a_y.data_ptr(), self.a_amax.data_ptr(),
+                                     self.pre.data_ptr())
+            self.fc2_a4 = L.in_operand(self.a_q4.data_ptr(), self.a_s4.data_ptr(), self.a_sg.data_ptr())
+            self.fc2_w4 = L.in_operand(self.W2q4.data_ptr(), self.W2s4.data_ptr(), self.w2_sg.data_ptr())
         # operands and outputs of the two block-scaled M-grouped GEMMs
         self.fc2_a = L.in_operand(self.a_q.data_ptr(), self.a_s.data_ptr())
         self.fc2_w = L.in_operand(self.W2q.data_ptr(), self.W2s.data_ptr())
@@ -123,19 +138,55 @@ class MoeLayer:
         lib, s = self.lib, _s()
         E, N1, H, F, T, k, R = self.E, self.N1, self.H, self.F, self.T, self.k, self.R_cap
         st = _p(self.status)
+        if self.nvfp4_fwd:
+            return self._forward_calls_nvfp4(x, topk_idx, topk_prob)
         return [
             ("route_permute", lambda: lib.moe_route_permute(
                 _p(x), _p(topk_idx), _p(topk_prob), T, H, k, self.expert_begin, E, R, _p(self.x_perm),
                 _p(self.row_of), _p(self.tok_of), _p(self.prob_perm), _p(self.counts), _p(self.offsets),
                 _p(self.ws), self.ws_bytes, st, s)),
-            ("fc1_glu_quant", lambda: lib.moe_grouped_fc1_glu_quant_fwd(
-                _p(self.x_perm), _p(self.W1p), _p(self.b1p), None, _p(self.counts), _p(self.offsets), E, H, F, R,
-                C.byref(self.params), L.OUT_MXFP8, C.byref(self.fc1_out), _p(self.ws_fc1), self.ws_fc1_bytes,
-                self.sm_margin, st, s)),
+            ("fc1_glu_quant", self.fc1_mxfp8_call()),
             ("quant_w2", lambda: lib.moe_quantize_mxfp8(
                 _p(self.W2), E, F, H, 1, None, None, 0, _p(self.W2q), _p(self.W2s), st, s)),
             ("fc2", lambda: lib.moe_grouped_fc2_fwd(
                 C.byref(self.fc2_a), C.byref(self.fc2_w), _p(self.counts), _p(self.offsets), E, F, H, R,
+                L.OUT_BF16, C.byref(self.fc2_out), _p(self.ws_fc2), self.ws_fc2.numel(), self.sm_margin, st, s)),
+            ("combine", lambda: lib.moe_unpermute_combine(
+                _p(self.y_perm), _p(self.row_of), _p(topk_prob), T, H, k, _p(self.out), st, s)),
+        ]
+
+    def fc1_mxfp8_call(self):
+        """The fused FC1 with MXFP8 row + column outputs (the MXFP8 forward's
+        FC1 call; also the fused side of the forward ablation)."""
+        lib, s = self.lib, _s()
+        E, H, F, R = self.E, self.H, self.F, self.R_cap
+        st = _p(self.status)
+        return lambda: lib.moe_grouped_fc1_glu_quant_fwd(
+            _p(self.x_perm), _p(self.W1p), _p(self.b1p), None, _p(self.counts), _p(self.offsets), E, H, F, R,
+            C.byref(self.params), L.OUT_MXFP8, C.byref(self.fc1_out), _p(self.ws_fc1), self.ws_fc1_bytes,
+            self.sm_margin, st, s)
+
+    def _forward_calls_nvfp4(self, x, topk_idx, topk_prob):
+        lib, s = self.lib, _s()
+        E, N1, H, F, T, k, R = self.E, self.N1, self.H, self.F, self.T, self.k, self.R_cap
+        st = _p(self.status)
+        return [
+            ("route_permute", lambda: lib.moe_route_permute(
+                _p(x), _p(topk_idx), _p(topk_prob), T, H, k, self.expert_begin, E, R, _p(self.x_perm),
+                _p(self.row_of), _p(self.tok_of), _p(self.prob_perm), _p(self.counts), _p(self.offsets),
+                _p(self.ws), self.ws_bytes, st, s)),
+            ("fc1_glu_nvfp4", lambda: lib.moe_grouped_fc1_glu_quant_fwd(
+                _p(self.x_perm), _p(self.W1p), _p(self.b1p), None, _p(self.counts), _p(self.offsets), E, H, F, R,
+                C.byref(self.params), L.OUT_NVFP4, C.byref(self.fc1_out4), _p(self.ws_fc1), self.ws_fc1_bytes,
+                self.sm_margin, st, s)),
+            ("quant_a_nvfp4", lambda: lib.moe_nvfp4_cast(
+                _p(self.a_y), _p(self.a_amax), _p(self.counts), _p(self.offsets), E, F, R, _p(self.a_q4),
+                _p(self.a_s4), _p(self.a_sg), s)),
+            ("amax_w2", lambda: lib.moe_amax_bf16(_p(self.W2), self.W2.numel(), _p(self.w2_amax), s)),
+            ("quant_w2_nvfp4", lambda: lib.moe_nvfp4_cast_cols(
+                _p(self.W2), E, F, H, _p(self.w2_amax), _p(self.W2q4), _p(self.W2s4), _p(self.w2_sg), s)),
+            ("fc2_nvfp4", lambda: lib.moe_grouped_fc2_fwd(
+                C.byref(self.fc2_a4), C.byref(self.fc2_w4), _p(self.counts), _p(self.offsets), E, F, H, R,
                 L.OUT_BF16, C.byref(self.fc2_out), _p(self.ws_fc2), self.ws_fc2.numel(), self.sm_margin, st, s)),
             ("combine", lambda: lib.moe_unpermute_combine(
                 _p(self.y_perm), _p(self.row_of), _p(topk_prob), T, H, k, _p(self.out), st, s)),
@@ -166,6 +217,9 @@ class MoeLayer:
             ("wgrad_w1", lambda: lib.moe_grouped_wgrad(
                 _p(self.d_qc), _p(self.d_sc), _p(self.x_qc), _p(self.x_sc), _p(self.counts), _p(self.offsets), E,
                 N1, H, R, _p(self.dW1), 0, _p(self.ws_wg1), self.ws_wg1.numel(), self.sm_margin, st, s)),
+            *([("quant_a_col", lambda: lib.moe_quantize_mxfp8(
+                _p(self.a_y), 1, R, F, 1, _p(self.counts), _p(self.offsets), E, _p(self.a_qc), _p(self.a_sc), st,
+                s))] if self.nvfp4_fwd else []),
             ("wgrad_w2", lambda: lib.moe_grouped_wgrad(
                 _p(self.a_qc), _p(self.a_sc), _p(self.dy_qc), _p(self.dy_sc), _p(self.counts), _p(self.offsets),
                 E, F, H, R, _p(self.dW2), 0, _p(self.ws_wg2), self.ws_wg2.numel(), self.sm_margin, st, s)),

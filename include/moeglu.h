@@ -113,7 +113,7 @@ typedef struct {
   uint8_t* q_col;    /* transposed    [N][R_cap]      (column-wise blocks of 32 rows) */
   uint8_t* s_col;    /*               [N][R_cap/32]   */
   moe_bf16* y;       /* bf16 output   [R_cap][N]      (BF16 / NVFP4 modes) */
-  float* amax;       /* one float: max |y| over all real rows (NVFP4 mode); caller zeroes it */
+  float* amax;       /* one float: max |y| over all real rows (NVFP4 mode; the call zeroes it first) */
   moe_bf16* pre;     /* forward only: saved pre-activation [R_cap][N1] (bias added), for the backward */
   float* row_dot;    /* backward only, may be NULL: per-row partial sums of da * act(pre) (the
                       * gradient of a per-row feature scale), [R_cap][moe_dglu_row_dot_parts(F)]
@@ -122,7 +122,7 @@ typedef struct {
                       * transposed random Hadamard rotation of y ([MoE-Fusion] "Fusing MXFP8 and
                       * NVFP4 quantisation"): over every 16-row block of the padded segments and
                       * every column, max |H16 diag(s) bf16(y)[block, c]| / 4, H16 the Sylvester
-                      * Hadamard matrix; caller zeroes it.  Must be NULL in the forward. */
+                      * Hadamard matrix; the call zeroes it first.  Must be NULL in the forward. */
   uint32_t rht_signs;/*   the 16 signs s of that rotation: bit i set -> s_i = -1 (drawn by the caller) */
 } moe_act_out_t;
 
@@ -264,7 +264,7 @@ MOE_API size_t moe_grouped_fc2_workspace_size(int E, int K, int N, int R_cap);
  * out_mode from the fp32 accumulator: MOE_OUT_BF16 (out->y), MOE_OUT_MXFP8
  * (out->q_row/s_row, plus the column-wise copy out->q_col/s_col when
  * non-NULL: blocks of 32 rows of one column, as for the fused FC1), or
- * MOE_OUT_NVFP4 (out->y bf16 and out->amax, caller zeroes it).
+ * MOE_OUT_NVFP4 (out->y bf16 and out->amax, which the call zeroes first).
  * out->pre, row_dot and rht_amax must be NULL.
  * Serves FC2 (K = F, N = H) and the data-gradient GEMM dX = dFC1 . W1p
  * (K = N1, N = H).

@@ -107,3 +107,46 @@ def test_nvfp4_forward_chain(act):
     sw = np.stack([O.nvfp4_quantize_cols(W2[e], sw_ref)[1] for e in range(w.E)])
     ref = O.grouped_gemm_nvfp4(qa, sa, sa_ref, qw, sw, sw_ref, rt)
     assert_chain_close(np_(y)[: rt.R_pad], O.bf16_round(ref), f"nvfp4 chain {act}")
+
+
+def test_layer_nvfp4_forward_step_and_graph():
+    """MoeLayer with the NVFP4 forward on the skewed config (small T and H):
+    the layer output against the oracle's NVFP4 chain, the FC2 weight gradient
+    on the layer's own operands (the MXFP8 column cast of the bf16 FC1
+    output), and one captured graph replaying to the eager results."""
+    from grouped_gemm_glu_gb300.layer import MoeLayer
+    w = synth.scaled(synth.WORKLOADS["skew"], T=1024, H=512)
+    inp = synth.make_inputs(w, 3)
+    g = {k: (v.to(DEV) if v is not None else None) for k, v in inp.items()}
+    layer = MoeLayer(g["W1"], g["W2"], w.T, w.k, w.R_cap, L.glu_params("geglu"), nvfp4_fwd=True)
+    args = (g["x"], g["topk_idx"], g["topk_prob"], g["dOut"])
+    layer.step(*args)
+    torch.cuda.synchronize()
+    assert ops.read_status(layer.status) == 0
+    rt = O.route(inp["topk_idx"].numpy(), 0, w.E)
+    Rp = rt.R_pad
+    fo = O.fc1_glu_fwd(O.permute(np_(inp["x"]), rt), O.repack_fc1(np_(inp["W1"])), None, rt, O.ActParams(O.ACT_GEGLU))
+    sa = O.nvfp4_global_scale(fo.amax)
+    qa, sba = O.nvfp4_quantize_rows(O.bf16_round(fo.y), sa)
+    W2 = np_(inp["W2"])
+    sw = O.nvfp4_global_scale(float(np.max(np.abs(W2))))
+    cols = [O.nvfp4_quantize_cols(W2[e], sw) for e in range(w.E)]
+    y = O.bf16_round(O.grouped_gemm_nvfp4(qa, sba, sa, np.stack([c[0] for c in cols]),
+                                          np.stack([c[1] for c in cols]), sw, rt))
+    out = O.bf16_round(O.unpermute_combine(y, rt.row_of, inp["topk_prob"].numpy()))
+    assert_chain_close(np_(layer.out), out, "NVFP4 layer output")
+    deq = lambda q, s_: O.mx_dequantize(np_(q), np_(s_))
+    qc, sc = O.mx_quantize_cols(np_(layer.a_y)[:Rp])   # the layer's bf16 FC1 output, cast by the oracle
+    assert_exact(np_(layer.a_qc)[:, :Rp], qc, "column cast of the bf16 FC1 output")
+    assert_exact(np_(layer.a_sc)[:, :Rp // 32], sc, "its scales")
+    dW2 = O.grouped_wgrad(deq(layer.a_qc, layer.a_sc)[:, :Rp], deq(layer.dy_qc, layer.dy_sc)[:, :Rp], rt)
+    assert_bf16_close(np_(layer.dW2), O.bf16_round(dW2), "dW2 on the layer's operands")
+    eager = {k: getattr(layer, k).clone() for k in ("out", "dx", "dW1", "dW2", "dprob")}
+    graph = layer.capture(*args)
+    for t in eager:
+        getattr(layer, t).zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert ops.read_status(layer.status) == 0
+    for t, v in eager.items():
+        assert torch.equal(getattr(layer, t), v), f"graph replay differs from eager: {t}"
