@@ -563,11 +563,19 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_cp_32x128b_x4(tmem_base + SFA_COL, sdesc_noswizzle(sf_addr, 128));
             tc_cp_32x128b_x4(tmem_base + SFB_COL, sdesc_noswizzle(sf_addr + SF_BLOCK, 128));
             tc_cp_32x128b_x4(tmem_base + SFB_COL + 4, sdesc_noswizzle(sf_addr + 2 * SF_BLOCK, 128));
+            // descriptors of the stage computed once; a step of 32 bytes along
+            // K is +2 in the descriptor's 16-byte address field
             const int nsub = min(4, (ti.kseg - kb * BK) / 32);
-            for (int k = 0; k < nsub; ++k) {
-              umma_mxf8(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32), sdesc_kmajor_sw128(b_addr + k * 32),
-                        idesc_with_sf_ids(idesc, (uint32_t)k, (uint32_t)k), tmem_base + SFA_COL,
-                        tmem_base + SFB_COL, (kb | k) != 0 ? 1u : 0u);
+            const uint64_t ad = sdesc_kmajor_sw128(a_addr), bd = sdesc_kmajor_sw128(b_addr);
+            if (nsub == 4) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                umma_mxf8(d_tmem, ad + 2 * k, bd + 2 * k, idesc_with_sf_ids(idesc, (uint32_t)k, (uint32_t)k),
+                          tmem_base + SFA_COL, tmem_base + SFB_COL, (kb | k) != 0 ? 1u : 0u);
+            } else {
+              for (int k = 0; k < nsub; ++k)
+                umma_mxf8(d_tmem, ad + 2 * k, bd + 2 * k, idesc_with_sf_ids(idesc, (uint32_t)k, (uint32_t)k),
+                          tmem_base + SFA_COL, tmem_base + SFB_COL, (kb | k) != 0 ? 1u : 0u);
             }
           }
           tc_commit(empty + stage);
