@@ -296,30 +296,43 @@ __device__ __forceinline__ float nvfp4_global_scale(float am) {
 }
 
 // Column-wise NVFP4 (the K-major copy of a weight whose contraction runs
-// along its rows): src [G][R][C] bf16 -> q [G][C][R/2], s [G][C][R/16], one
-// thread per (g, 16-row block, column); neighbouring threads take
-// neighbouring columns, so each of the 16 row loads is coalesced.
+// along its rows): src [G][R][C] bf16 -> q [G][C][R/2], s [G][C][R/16].  One
+// thread per (g, BPT consecutive 16-row blocks, column); neighbouring threads
+// take neighbouring columns, so each row load is coalesced, and with BPT = 4
+// a thread's codes are one whole 32-byte sector of its output row.
+template <int BPT>
 __global__ void __launch_bounds__(256) k_nvfp4_cast_cols(const uint16_t* __restrict__ src, int G, int R, int C,
                                                          const float* __restrict__ amax, uint8_t* __restrict__ q,
                                                          uint8_t* __restrict__ s, float* __restrict__ s_global) {
   const float sg = nvfp4_global_scale(*amax);
   if (blockIdx.x == 0 && threadIdx.x == 0) *s_global = sg;
-  const int nb = R / 16;
-  const size_t total = (size_t)G * nb * C;
+  const int nb = R / 16, ng = nb / BPT;
+  const size_t total = (size_t)G * ng * C;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
     const int c = (int)(i % C);
     const size_t rest = i / C;
-    const int rb = (int)(rest % nb);
-    const int g = (int)(rest / nb);
-    const uint16_t* p = src + ((size_t)g * R + (size_t)rb * 16) * C + c;
-    float v[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float((uint32_t)__ldg(p + (size_t)j * C) << 16);
-    uint32_t w[2];
-    const uint32_t sc = nvfp4_block16(v, sg, w);
+    const int rg = (int)(rest % ng);
+    const int g = (int)(rest / ng);
     const size_t col = (size_t)g * C + c;
-    *reinterpret_cast<uint2*>(q + col * (R / 2) + (size_t)rb * 8) = make_uint2(w[0], w[1]);
-    s[col * nb + rb] = (uint8_t)sc;
+    uint32_t w[2 * BPT];
+    uint32_t sc4 = 0;
+#pragma unroll
+    for (int b = 0; b < BPT; ++b) {
+      const uint16_t* p = src + ((size_t)g * R + (size_t)(rg * BPT + b) * 16) * C + c;
+      float v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = __uint_as_float((uint32_t)__ldg(p + (size_t)j * C) << 16);
+      sc4 |= nvfp4_block16(v, sg, w + 2 * b) << (8 * b);
+    }
+    uint8_t* qd = q + col * (R / 2) + (size_t)rg * BPT * 8;
+    if (BPT == 4) {
+      reinterpret_cast<uint4*>(qd)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      reinterpret_cast<uint4*>(qd)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      *reinterpret_cast<uint32_t*>(s + col * nb + (size_t)rg * 4) = sc4;
+    } else {
+      *reinterpret_cast<uint2*>(qd) = make_uint2(w[0], w[1]);
+      s[col * nb + rg] = (uint8_t)sc4;
+    }
   }
 }
 
@@ -556,8 +569,15 @@ extern "C" moe_status_t moe_nvfp4_cast_cols(const moe_bf16* src, int G, int R, i
                                             uint8_t* s, float* s_global, moe_stream_t stream) {
   if (!src || !amax || !q || !s || !s_global || G <= 0 || R <= 0 || (R % 16) || C <= 0) return MOE_ERR_ARG;
   if ((reinterpret_cast<uintptr_t>(q) & 7)) return MOE_ERR_ARG;
-  k_nvfp4_cast_cols<<<grid_for((size_t)G * (R / 16) * C, 256), 256, 0, as_stream(stream)>>>(
-      reinterpret_cast<const uint16_t*>(src), G, R, C, amax, q, s, s_global);
+  // four blocks per thread (32-byte code stores, 4-byte scale stores) when
+  // the rows come in 64s and the outputs are aligned for it
+  const bool wide = (R % 64) == 0 && (reinterpret_cast<uintptr_t>(q) & 15) == 0 && (reinterpret_cast<uintptr_t>(s) & 3) == 0;
+  if (wide)
+    k_nvfp4_cast_cols<4><<<grid_for((size_t)G * (R / 64) * C, 256), 256, 0, as_stream(stream)>>>(
+        reinterpret_cast<const uint16_t*>(src), G, R, C, amax, q, s, s_global);
+  else
+    k_nvfp4_cast_cols<1><<<grid_for((size_t)G * (R / 16) * C, 256), 256, 0, as_stream(stream)>>>(
+        reinterpret_cast<const uint16_t*>(src), G, R, C, amax, q, s, s_global);
   count_launch();
   return launch_status();
 }

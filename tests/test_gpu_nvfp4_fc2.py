@@ -54,12 +54,13 @@ def test_nvfp4_fc2_edge_counts(K, N):
     assert_bf16_close(np_(y)[: rt.R_pad], O.bf16_round(ref), f"nvfp4 fc2 K={K} N={N}")
 
 
-def test_nvfp4_weight_cast_and_amax_bit_exact():
+@pytest.mark.parametrize("R", [64, 48, 1536])
+def test_nvfp4_weight_cast_and_amax_bit_exact(R):
     """The column-wise NVFP4 cast of a bf16 weight [E, F, H] and its per-tensor
     amax against the oracle on the same bf16 values: codes, scales and s_g
-    bit-exact."""
+    bit-exact (R a multiple of 64: four blocks per thread; R = 48: one)."""
     rng = np.random.default_rng(4)
-    W = synth._bf16(rng.standard_normal((3, 64, 96), dtype=np.float32) * np.exp2(rng.integers(-4, 4, (3, 1, 96))))
+    W = synth._bf16(rng.standard_normal((3, R, 96), dtype=np.float32) * np.exp2(rng.integers(-4, 4, (3, 1, 96))))
     Wd = W.to(DEV)
     am = ops.amax_bf16(Wd)
     q, s, sg = ops.nvfp4_cast_cols(Wd, am)
