@@ -725,6 +725,26 @@ def rht_transposed(y, sign_mask: int) -> np.ndarray:
     return Z.reshape(R, C)
 
 
+def nvfp4_rht_cast_cols(y, sign_mask: int, s_g) -> tuple[np.ndarray, np.ndarray]:
+    """NVFP4 operand of the weight-gradient GEMM ([MoE-Fusion], "Fusing MXFP8
+    and NVFP4 quantisation": the backward's NVFP4 operands are the transposed
+    tensors after a random Hadamard rotation): y [R, C] is rotated along its
+    rows (rht_transposed: 16-row blocks, H16 diag(s) / 4 on the bf16 values)
+    and cast column-wise to NVFP4 under s_g, whose blocks of 16 rows are the
+    rotation's blocks.  Returns codes [C, R/2] and scales [C, R/16]."""
+    return nvfp4_quantize_cols(rht_transposed(y, sign_mask), s_g)
+
+
+def grouped_wgrad_nvfp4(Aq, As, sgA, Bq, Bs, sgB, rt: "Routing") -> np.ndarray:
+    """Weight gradient on column-wise NVFP4 operands: each operand [M, R/2] /
+    [M, R/16] is dequantised (e2m1 * s_b / s_g) and D_e = A[:, seg_e] @
+    B[:, seg_e]^T over the expert's padded row segment (grouped_wgrad).
+    float64 [E, M, N]."""
+    A = nvfp4_dequantize(np.asarray(Aq), np.asarray(As), sgA)
+    B = nvfp4_dequantize(np.asarray(Bq), np.asarray(Bs), sgB)
+    return grouped_wgrad(A, B, rt)
+
+
 def rht_transposed_amax(y, sign_mask: int) -> float:
     """Per-tensor amax of the rotated transposed output (0 for an empty tensor)."""
     Z = rht_transposed(y, sign_mask)
