@@ -71,7 +71,7 @@ constexpr int TS_SUB = 32 * 128;          // TMA-store staging: one 32-row x 128
 // 128-row group, one per MMA), so a stage carries 4x the scales; 3 stages.
 template <bool TS, bool NV4 = false>
 struct Lay {
-  static constexpr int STAGES = (TS || NV4) ? 3 : 4;
+  static constexpr int STAGES = TS ? (NV4 ? 2 : 3) : (NV4 ? 3 : 4);
   static constexpr int SF_ST = NV4 ? 4 * SF_STAGE : SF_STAGE;
   static constexpr int EPI_WARP_BYTES = TS ? 2 * TS_SUB : EPI_ROWS * EPI_ROW_BYTES;
   static constexpr int OFF_SF = STAGES * STAGE_BYTES;
@@ -121,6 +121,7 @@ struct Args {
   // M-grouped: real k-blocks per tile (KB counts 4-scale groups of the tiled
   // scales: KB = KBr for MXFP8, 4 * KBr for NVFP4) and scale bytes per row
   int KBr, sf_ks;
+  int nv4;                 // NVFP4 operands (the EPI_NV4 instantiations)
   const float* sg_a;       // NVFP4: per-tensor scales of A and B (the product is divided by both)
   const float* sg_b;
 };
@@ -136,7 +137,9 @@ __device__ __forceinline__ void build_prefix(const Args& a, int32_t* pref, int n
       v = (__ldg(a.counts + e) + BM - 1) / BM;
     } else {
       const int seg = __ldg(a.offsets + e + 1) - __ldg(a.offsets + e);
-      v = seg > 0 ? (seg + BK - 1) / BK : 0;
+      // 4-scale groups of the tiled scales: one per 128-row k-block (MXFP8),
+      // four per 256-row k-block (NVFP4)
+      v = seg > 0 ? (a.nv4 ? 4 * ((seg + 2 * BK - 1) / (2 * BK)) : (seg + BK - 1) / BK) : 0;
     }
     pref[e + 1] = max(v, 0);
   }
@@ -217,7 +220,7 @@ __device__ __forceinline__ Tile decode(int t, const int32_t* pref, const Args& a
     const int o0 = __ldg(a.offsets + ti.e), o1 = __ldg(a.offsets + ti.e + 1);
     ti.kseg0 = o0;
     ti.kseg = (o0 < 0 || o1 > a.R_cap || o1 < o0) ? 0 : o1 - o0;
-    ti.num_kb = (ti.kseg + BK - 1) / BK;
+    ti.num_kb = a.nv4 ? (ti.kseg + 2 * BK - 1) / (2 * BK) : (ti.kseg + BK - 1) / BK;
     ti.sfa = ((size_t)m_idx * a.KG + pref[ti.e]) * SF_BLOCK;
     ti.sfb = ((size_t)n_idx * a.KG + pref[ti.e]) * SFB_BYTES;
   }
@@ -298,18 +301,26 @@ __global__ void __launch_bounds__(256) k_sf_tile(const Args a) {
         dst = a.sfb_t + ((((size_t)e * a.n_tiles_n + (g >> 1)) * a.KB + kb) * 2 + (g & 1)) * SF_BLOCK;
       }
     } else {
-      const int ks = a.R_cap / 32;
+      const int ks = a.sf_ks;  // scale bytes per operand row: R_cap / 32 (MXFP8) or R_cap / 16 (NVFP4)
+      const int rpb = a.nv4 ? 16 : 32;  // rows per scale byte
       const bool isA = it < nA;
       const size_t jb = isA ? it : it - nA;
       const int rt = (int)(jb / ktot), kg = (int)(jb % ktot);
       const int e = find_group(pref, a.E, kg);
-      const int kbyte = __ldg(a.offsets + e) / 32 + (kg - pref[e]) * 4;
+      const int kbyte = __ldg(a.offsets + e) / rpb + (kg - pref[e]) * 4;
+      // bytes past the expert's segment are zero, so a partial last MMA adds
+      // nothing from the next expert's rows
+      const int kend = __ldg(a.offsets + e + 1) / rpb;
       const uint8_t* base = isA ? a.As : a.Bs;
       const int rows = isA ? a.M : a.N;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int r = rt * 128 + 32 * j + lane;
-        v[j] = r < rows ? load4_unaligned(base + (size_t)r * ks, kbyte, ks) : 0u;
+        uint32_t w4 = r < rows ? load4_unaligned(base + (size_t)r * ks, kbyte, ks) : 0u;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (kbyte + i >= kend) w4 &= ~(0xFFu << (8 * i));
+        v[j] = w4;
       }
       // A: [m tile][k-block][512]; B: [n tile][k-block][half][512]
       dst = isA ? a.sfa_t + ((size_t)rt * a.KG + kg) * SF_BLOCK
@@ -497,8 +508,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             tma_load_2d(dst, &tmA, full + stage, kb * BK, ti.m0);
             tma_load_3d(dst + A_TILE, &tmB, full + stage, kb * BK, ti.n0, ti.e);
           } else {
-            tma_load_2d(dst, &tmA, full + stage, ti.kseg0 + kb * BK, ti.m0);
-            tma_load_2d(dst + A_TILE, &tmB, full + stage, ti.kseg0 + kb * BK, ti.n0);
+            // the contraction runs along the operands' rows of tokens: one byte
+            // per token (MXFP8) or per two tokens (packed NVFP4)
+            const int kx = NV4 ? ti.kseg0 / 2 + kb * BK : ti.kseg0 + kb * BK;
+            tma_load_2d(dst, &tmA, full + stage, kx, ti.m0);
+            tma_load_2d(dst + A_TILE, &tmB, full + stage, kx, ti.n0);
           }
           bulk_load(sdst, a.sfa_t + ti.sfa + (size_t)kb * SF_MUL * SF_BLOCK, SF_MUL * SF_BLOCK, full + stage);
           bulk_load(sdst + SF_MUL * SF_BLOCK, a.sfb_t + ti.sfb + (size_t)kb * SF_MUL * SFB_BYTES, SF_MUL * SFB_BYTES,
@@ -547,7 +561,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             // rows), each with its own 4 scale bytes per row: MMA k's block
             // of A scales goes to columns SFA4 + 4k, its two blocks of B
             // scales to SFB4 + 8k (rows 0..127) and SFB4 + 8k + 4
-            const int nsub = min(4, (ti.kseg - kb * 2 * BK) / 64);
+            // MMAs of 64 elements; a weight gradient's last one may cover 32
+            // rows of its segment (the scales of the rest are zero)
+            const int nsub = min(4, (ti.kseg - kb * 2 * BK + 63) / 64);
             for (int k = 0; k < nsub; ++k) {
               tc_cp_32x128b_x4(tmem_base + SFA4_COL + 4 * k, sdesc_noswizzle(sf_addr + k * SF_BLOCK, 128));
               tc_cp_32x128b_x4(tmem_base + SFB4_COL + 8 * k,
@@ -773,11 +789,12 @@ static moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const
                            long long tiles_bound, long long sf_items, int sm_margin, cudaStream_t stream,
                            int epi = -1) {
   const bool ts = tmO != nullptr;
-  if (epi < 0) epi = a.out_mode != MOE_OUT_BF16 ? EPI_QUANT : EPI_BF16;
+  if (epi < 0) epi = (!ts && a.out_mode != MOE_OUT_BF16) ? EPI_QUANT : EPI_BF16;
   if (!ts && a.out_mode == MOE_OUT_NVFP4 && a.amax &&
       cudaMemsetAsync(a.amax, 0, sizeof(float), stream) != cudaSuccess)
     return MOE_ERR_CUDA;
-  const void* kfn = ts                  ? (const void*)k_grouped_mx<true, EPI_BF16>
+  const void* kfn = ts ? (epi == EPI_NV4 ? (const void*)k_grouped_mx<true, EPI_NV4>
+                                         : (const void*)k_grouped_mx<true, EPI_BF16>)
                     : epi == EPI_QUANT  ? (const void*)k_grouped_mx<false, EPI_QUANT>
                     : epi == EPI_GLU    ? (const void*)k_grouped_mx<false, EPI_GLU>
                     : epi == EPI_GLU_L1 ? (const void*)k_grouped_mx<false, EPI_GLU_L1>
@@ -786,7 +803,8 @@ static moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const
                     : epi == EPI_ELT    ? (const void*)k_grouped_mx<false, EPI_ELT>
                     : epi == EPI_NV4    ? (const void*)k_grouped_mx<false, EPI_NV4>
                                         : (const void*)k_grouped_mx<false, EPI_BF16>;
-  const int smem = ts ? Lay<true>::SMEM_BYTES : epi == EPI_NV4 ? Lay<false, true>::SMEM_BYTES : Lay<false>::SMEM_BYTES;
+  const int smem = ts ? (epi == EPI_NV4 ? Lay<true, true>::SMEM_BYTES : Lay<true>::SMEM_BYTES)
+                      : (epi == EPI_NV4 ? Lay<false, true>::SMEM_BYTES : Lay<false>::SMEM_BYTES);
   if (!set_smem_limit(kfn, smem)) return MOE_ERR_CUDA;
   const int sms = sm_count();
   long long sgrid = (sf_items + 7) / 8;
@@ -796,7 +814,9 @@ static moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const
   int grid = sms - sm_margin;
   if (grid > tiles_bound) grid = (int)tiles_bound;
   if (grid < 1) grid = 1;
-  if (ts)
+  if (ts && epi == EPI_NV4)
+    launch_kernel<true, EPI_NV4>(grid, smem, tmA, tmB, *tmO, a, stream);
+  else if (ts)
     launch_kernel<true, EPI_BF16>(grid, smem, tmA, tmB, *tmO, a, stream);
   else if (epi == EPI_QUANT)
     launch_kernel<false, EPI_QUANT>(grid, smem, tmA, tmB, tmA, a, stream);
@@ -834,8 +854,15 @@ static void fc2_ws_parts(int E, int K, int N, int R_cap, size_t* a_bytes, size_t
   *b_bytes = align_up((size_t)E * n_tiles(N) * KB * SFB_BYTES);
 }
 
-static void wgrad_ws_parts(int E, int M, int N, int R_cap, size_t* a_bytes, size_t* b_bytes) {
-  const size_t KG = (size_t)R_cap / BK + E;
+// 4-scale groups a weight gradient's tiled scales hold per row tile (the
+// stride of the group axis): MXFP8 one per 128 rows of each segment, NVFP4
+// four per 256 rows
+static size_t wgrad_kg(int E, int R_cap, bool nv4) {
+  return nv4 ? (size_t)R_cap / 64 + 4 * (size_t)E : (size_t)R_cap / BK + E;
+}
+
+static void wgrad_ws_parts(int E, int M, int N, int R_cap, size_t* a_bytes, size_t* b_bytes, bool nv4 = false) {
+  const size_t KG = wgrad_kg(E, R_cap, nv4);
   *a_bytes = align_up((size_t)m_tiles_of(M) * KG * SF_BLOCK);
   *b_bytes = align_up((size_t)n_tiles(N) * KG * SFB_BYTES);
 }
@@ -855,9 +882,10 @@ extern "C" size_t moe_grouped_fc2_workspace_size(int E, int K, int N, int R_cap)
 
 extern "C" size_t moe_grouped_wgrad_workspace_size(int E, int M, int N, int R_cap) {
   if (E <= 0 || M <= 0 || N <= 0 || R_cap <= 0) return 0;
-  size_t a, b;
+  size_t a, b, a4, b4;
   gmx::wgrad_ws_parts(E, M, N, R_cap, &a, &b);
-  return a + b;
+  gmx::wgrad_ws_parts(E, M, N, R_cap, &a4, &b4, true);
+  return a + b > a4 + b4 ? a + b : a4 + b4;  // enough for MXFP8 or NVFP4 operands
 }
 
 extern "C" moe_status_t moe_grouped_fc2_fwd(const moe_in_t* A, const moe_in_t* W, const int32_t* counts,
@@ -914,6 +942,7 @@ extern "C" moe_status_t moe_grouped_fc2_fwd(const moe_in_t* A, const moe_in_t* W
     a.n_tiles_n = n_tiles(N);
     a.KB = (int)sf_kblocks(K, true);
     a.KBr = (K + 255) / 256;
+    a.nv4 = 1;
     a.sf_ks = K / 16;
     a.As = A->scale;
     a.Bs = W->scale;
@@ -1131,6 +1160,7 @@ extern "C" moe_status_t moe_grouped_wgrad(const uint8_t* Aq, const uint8_t* As, 
   a.m_tiles = m_tiles_of(M);
   a.KB = 0;
   a.KG = R_cap / BK + E;
+  a.sf_ks = R_cap / 32;
   a.As = As;
   a.Bs = Bs;
   a.sfa_t = static_cast<uint8_t*>(ws);
@@ -1152,4 +1182,71 @@ extern "C" moe_status_t moe_grouped_wgrad(const uint8_t* Aq, const uint8_t* As, 
   const long long bound = (long long)E * a.m_tiles * a.n_tiles_n;
   const long long sf_items = (long long)(a.m_tiles + 2 * a.n_tiles_n) * a.KG;
   return launch(tmA, tmB, &tmO, a, bound, sf_items, sm_margin, as_stream(stream));
+}
+
+extern "C" moe_status_t moe_grouped_wgrad_nvfp4(const uint8_t* Aq, const uint8_t* As, const float* sgA,
+                                                const uint8_t* Bq, const uint8_t* Bs, const float* sgB,
+                                                const int32_t* counts, const int32_t* offsets, int E, int M, int N,
+                                                int R_cap, void* D, int out_f32, void* ws, size_t ws_bytes,
+                                                int sm_margin, int32_t* status, moe_stream_t stream) {
+  using namespace gmx;
+  if (!Aq || !As || !sgA || !Bq || !Bs || !sgB || !counts || !offsets || !D || !ws) return MOE_ERR_ARG;
+  if (E <= 0 || E > E_MAX || M <= 0 || (M % 32) || N <= 0 || (N % 32) || R_cap <= 0 || (R_cap % BM))
+    return MOE_ERR_ARG;
+  if (!aligned16(Aq) || !aligned16(Bq) || !aligned16(D) || (reinterpret_cast<uintptr_t>(As) & 3) ||
+      (reinterpret_cast<uintptr_t>(Bs) & 3) || (reinterpret_cast<uintptr_t>(ws) & 255) || sm_margin < 0)
+    return MOE_ERR_ARG;
+  size_t a_bytes, b_bytes;
+  wgrad_ws_parts(E, M, N, R_cap, &a_bytes, &b_bytes, true);
+  if (ws_bytes < a_bytes + b_bytes) return MOE_ERR_ARG;
+  CUtensorMap tmA, tmB, tmO;
+  {
+    const uint64_t dims[2] = {(uint64_t)R_cap / 2, (uint64_t)M};
+    const uint64_t strides[1] = {(uint64_t)R_cap / 2};
+    const uint32_t box[2] = {BK, BM};
+    if (!encode_tmap(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, Aq, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return MOE_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)R_cap / 2, (uint64_t)N};
+    const uint64_t strides[1] = {(uint64_t)R_cap / 2};
+    const uint32_t box[2] = {BK, BN};
+    if (!encode_tmap(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, Bq, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return MOE_ERR_CUDA;
+  }
+  {
+    const uint64_t es = out_f32 ? 4 : 2;
+    const uint64_t dims[3] = {(uint64_t)N, (uint64_t)M, (uint64_t)E};
+    const uint64_t strides[2] = {(uint64_t)N * es, (uint64_t)M * N * es};
+    const uint32_t box[3] = {out_f32 ? 32u : 64u, 32, 1};
+    if (!encode_tmap(&tmO, out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, D, dims,
+                     strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return MOE_ERR_CUDA;
+  }
+  Args a{};
+  a.counts = counts;
+  a.offsets = offsets;
+  a.E = E;
+  a.M = M;
+  a.N = N;
+  a.R_cap = R_cap;
+  a.kgrouped = 1;
+  a.n_tiles_n = n_tiles(N);
+  a.m_tiles = m_tiles_of(M);
+  a.KG = (int)wgrad_kg(E, R_cap, true);
+  a.sf_ks = R_cap / 16;
+  a.nv4 = 1;
+  a.As = As;
+  a.Bs = Bs;
+  a.sfa_t = static_cast<uint8_t*>(ws);
+  a.sfb_t = static_cast<uint8_t*>(ws) + a_bytes;
+  a.out = D;
+  a.out_f32 = out_f32 ? 1 : 0;
+  a.status = status;
+  a.wait_ns = g_wait_limit_ns.load();
+  a.sg_a = sgA;
+  a.sg_b = sgB;
+  const long long bound = (long long)E * a.m_tiles * a.n_tiles_n;
+  const long long sf_items = (long long)(a.m_tiles + 2 * a.n_tiles_n) * a.KG;
+  return launch(tmA, tmB, &tmO, a, bound, sf_items, sm_margin, as_stream(stream), EPI_NV4);
 }

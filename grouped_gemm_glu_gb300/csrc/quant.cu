@@ -336,6 +336,102 @@ __global__ void __launch_bounds__(256) k_nvfp4_cast_cols(const uint16_t* __restr
   }
 }
 
+// Transposed random Hadamard rotation of one 16-row block of one column, in
+// place: v <- H16 diag(s) v / 4 (s_i = -1 where bit i of signs is set;
+// Sylvester order), on fp32 values of bf16 inputs.  The same butterfly as
+// the dGLU epilogue's rotated amax.
+__device__ __forceinline__ void rht16(float* v, uint32_t signs) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    if ((signs >> i) & 1u) v[i] = -v[i];
+#pragma unroll
+  for (int m = 1; m < 16; m <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i & m) continue;
+      const float lo = v[i], hi = v[i + m];
+      v[i] = lo + hi;
+      v[i + m] = lo - hi;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] *= 0.25f;
+}
+
+// Rows [16 b, 16 b + 16) of column c of src [R][C] bf16 as fp32.
+__device__ __forceinline__ void load_col16(const uint16_t* __restrict__ src, int C, int b, int c, float* v) {
+  const uint16_t* p = src + (size_t)b * 16 * C + c;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float((uint32_t)__ldg(p + (size_t)j * C) << 16);
+}
+
+// NVFP4 operand of the weight gradient: the rows of src [R_cap][C] (an
+// activation or its gradient in the permuted layout) below offsets[E],
+// rotated in 16-row blocks and cast column-wise: q [C][R_cap/2],
+// s [C][R_cap/16] under s_g = 2688 / amax (amax = the rotated amax).  One
+// thread per (4 consecutive 16-row blocks, column); blocks at or past
+// offsets[E] are not written.
+__global__ void __launch_bounds__(256) k_nvfp4_rht_cast_cols(const uint16_t* __restrict__ src, int R_cap, int C,
+                                                             const int32_t* __restrict__ offsets, int E,
+                                                             const float* __restrict__ amax, uint32_t signs,
+                                                             uint8_t* __restrict__ q, uint8_t* __restrict__ s,
+                                                             float* __restrict__ s_global) {
+  const float sg = nvfp4_global_scale(*amax);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *s_global = sg;
+  const int R = min(__ldg(offsets + E), R_cap);
+  const int nb = (R + 15) / 16, ng = (nb + 3) / 4;
+  const size_t total = (size_t)ng * C;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const int c = (int)(i % C);
+    const int rg = (int)(i / C);
+    uint32_t w[8];
+    uint32_t sc4 = 0;
+    const int nblk = min(4, nb - rg * 4);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      w[2 * b] = w[2 * b + 1] = 0;
+      if (b < nblk) {
+        float v[16];
+        load_col16(src, C, rg * 4 + b, c, v);
+        rht16(v, signs);
+        sc4 |= nvfp4_block16(v, sg, w + 2 * b) << (8 * b);
+      }
+    }
+    uint8_t* qd = q + (size_t)c * (R_cap / 2) + (size_t)rg * 32;
+    uint8_t* sd = s + (size_t)c * (R_cap / 16) + (size_t)rg * 4;
+    if (nblk == 4) {
+      reinterpret_cast<uint4*>(qd)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      reinterpret_cast<uint4*>(qd)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      *reinterpret_cast<uint32_t*>(sd) = sc4;
+    } else {
+      for (int b = 0; b < nblk; ++b) {
+        *reinterpret_cast<uint2*>(qd + 8 * b) = make_uint2(w[2 * b], w[2 * b + 1]);
+        sd[b] = (uint8_t)(sc4 >> (8 * b));
+      }
+    }
+  }
+}
+
+// max |rotated value| over the 16-row blocks below offsets[E] of every column
+// (the per-tensor amax of k_nvfp4_rht_cast_cols' input), as ordered float bits.
+__global__ void __launch_bounds__(256) k_rht_amax_cols(const uint16_t* __restrict__ src, int R_cap, int C,
+                                                       const int32_t* __restrict__ offsets, int E, uint32_t signs,
+                                                       float* __restrict__ amax) {
+  const int R = min(__ldg(offsets + E), R_cap);
+  const int nb = (R + 15) / 16;
+  const size_t total = (size_t)nb * C;
+  uint32_t m = 0;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    float v[16];
+    load_col16(src, C, (int)(i / C), (int)(i % C), v);
+    rht16(v, signs);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) m = max(m, __float_as_uint(v[j]) & 0x7FFFFFFFu);
+  }
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  if ((threadIdx.x & 31) == 0 && m != 0) atomicMax(reinterpret_cast<int*>(amax), (int)m);
+}
+
 // max |x| over a bf16 tensor of n8 16-byte words (x 16-byte aligned) into
 // *amax as ordered float bits (the caller's call zeroes it first).
 __global__ void __launch_bounds__(256) k_amax_bf16(const uint4* __restrict__ x, size_t n8, float* __restrict__ amax) {
@@ -578,6 +674,29 @@ extern "C" moe_status_t moe_nvfp4_cast_cols(const moe_bf16* src, int G, int R, i
   else
     k_nvfp4_cast_cols<1><<<grid_for((size_t)G * (R / 16) * C, 256), 256, 0, as_stream(stream)>>>(
         reinterpret_cast<const uint16_t*>(src), G, R, C, amax, q, s, s_global);
+  count_launch();
+  return launch_status();
+}
+
+extern "C" moe_status_t moe_rht_amax_cols(const moe_bf16* src, int R_cap, int C, const int32_t* offsets, int E,
+                                          uint32_t signs, float* amax, moe_stream_t stream) {
+  if (!src || !offsets || !amax || R_cap <= 0 || (R_cap % 128) || C <= 0 || E <= 0) return MOE_ERR_ARG;
+  cudaStream_t st = as_stream(stream);
+  if (cudaMemsetAsync(amax, 0, sizeof(float), st) != cudaSuccess) return MOE_ERR_CUDA;
+  k_rht_amax_cols<<<grid_for((size_t)(R_cap / 16) * C, 256), 256, 0, st>>>(
+      reinterpret_cast<const uint16_t*>(src), R_cap, C, offsets, E, signs & 0xFFFFu, amax);
+  count_launch();
+  return launch_status();
+}
+
+extern "C" moe_status_t moe_nvfp4_rht_cast_cols(const moe_bf16* src, int R_cap, int C, const int32_t* offsets, int E,
+                                                const float* amax, uint32_t signs, uint8_t* q, uint8_t* s,
+                                                float* s_global, moe_stream_t stream) {
+  if (!src || !offsets || !amax || !q || !s || !s_global || R_cap <= 0 || (R_cap % 128) || C <= 0 || E <= 0)
+    return MOE_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(s) & 3)) return MOE_ERR_ARG;
+  k_nvfp4_rht_cast_cols<<<grid_for((size_t)(R_cap / 64) * C, 256), 256, 0, as_stream(stream)>>>(
+      reinterpret_cast<const uint16_t*>(src), R_cap, C, offsets, E, amax, signs & 0xFFFFu, q, s, s_global);
   count_launch();
   return launch_status();
 }

@@ -329,6 +329,50 @@ def wgrad(Aq_col, As_col, Bq_col, Bs_col, counts, offsets, out_f32: bool = False
     return D
 
 
+def rht_amax_cols(src, offsets, signs: int):
+    """max |rotated value| of src [R_cap, C] (16-row Hadamard blocks below
+    offsets[E]) as a device float [1]."""
+    lib = L.load()
+    R_cap, Cc = src.shape
+    a = torch.empty(1, dtype=torch.float32, device=_dev(src))
+    L.check(lib.moe_rht_amax_cols(_p(src), R_cap, Cc, _p(offsets), offsets.shape[0] - 1, int(signs) & 0xFFFF, _p(a),
+                                  _s()), "moe_rht_amax_cols")
+    return a
+
+
+def nvfp4_rht_cast_cols(src, offsets, amax, signs: int):
+    """Rotated column-wise NVFP4 of src [R_cap, C]: (q [C, R_cap/2],
+    s [C, R_cap/16], s_global [1])."""
+    lib = L.load()
+    dev = _dev(src)
+    R_cap, Cc = src.shape
+    q = torch.empty(Cc, R_cap // 2, dtype=torch.uint8, device=dev)
+    s = torch.empty(Cc, R_cap // 16, dtype=torch.uint8, device=dev)
+    sg = torch.empty(1, dtype=torch.float32, device=dev)
+    L.check(lib.moe_nvfp4_rht_cast_cols(_p(src), R_cap, Cc, _p(offsets), offsets.shape[0] - 1, _p(amax),
+                                        int(signs) & 0xFFFF, _p(q), _p(s), _p(sg), _s()), "moe_nvfp4_rht_cast_cols")
+    return q, s, sg
+
+
+def wgrad_nvfp4(Aq, As, sgA, Bq, Bs, sgB, counts, offsets, out_f32: bool = False, sm_margin: int = 0, status=None):
+    """D [E, M, N] = per-expert contraction over the expert's rows of the
+    column-wise NVFP4 operands A [M, R_cap/2] and B [N, R_cap/2]."""
+    lib = L.load()
+    dev = _dev(Aq)
+    M, R2 = Aq.shape
+    R_cap = 2 * R2
+    N = Bq.shape[0]
+    E = counts.shape[0]
+    D = torch.empty(E, M, N, dtype=torch.float32 if out_f32 else torch.bfloat16, device=dev)
+    st = status if status is not None else new_status(dev)
+    ws_bytes = lib.moe_grouped_wgrad_workspace_size(E, M, N, R_cap)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    L.check(lib.moe_grouped_wgrad_nvfp4(_p(Aq), _p(As), _p(sgA), _p(Bq), _p(Bs), _p(sgB), _p(counts), _p(offsets), E,
+                                        M, N, R_cap, _p(D), int(out_f32), _p(ws), ws_bytes, sm_margin, _p(st), _s()),
+            "moe_grouped_wgrad_nvfp4")
+    return D
+
+
 def unpermute_combine(y_perm, row_of, topk_prob, status=None, out=None):
     lib = L.load()
     dev = _dev(y_perm)

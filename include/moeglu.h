@@ -316,7 +316,7 @@ MOE_API moe_status_t moe_grouped_fc1_glu_quant_fwd_mxfp8(const uint8_t* xq, cons
                                                  const moe_act_out_t* out, void* ws, size_t ws_bytes,
                                                  int sm_margin, int32_t* status, moe_stream_t stream);
 
-/* Bytes of device workspace moe_grouped_wgrad needs. */
+/* Bytes of device workspace moe_grouped_wgrad (and moe_grouped_wgrad_nvfp4) needs. */
 MOE_API size_t moe_grouped_wgrad_workspace_size(int E, int M, int N, int R_cap);
 
 /* Weight-gradient grouped GEMM, contraction over each expert's rows
@@ -334,6 +334,24 @@ MOE_API moe_status_t moe_grouped_wgrad(const uint8_t* Aq, const uint8_t* As,
                                int E, int M, int N, int R_cap,
                                void* D, int out_f32, void* ws, size_t ws_bytes,
                                int sm_margin, int32_t* status, moe_stream_t stream);
+
+/* Weight-gradient grouped GEMM on NVFP4 operands (kind::mxf4nvf4, E4M3
+ * scales per 16 rows): the NVFP4 form of moe_grouped_wgrad.  Aq [M][R_cap/2],
+ * As [M][R_cap/16], Bq [N][R_cap/2], Bs [N][R_cap/16] as written by
+ * moe_nvfp4_rht_cast_cols (rotated along the rows, which leaves the product
+ * unchanged), sgA / sgB their per-tensor scales (device floats).
+ * D[e] = dequant(A)[:, seg e] . dequant(B)[:, seg e]^T over the expert's
+ * padded row segment (contraction in MMAs of 64 rows; a segment's last MMA
+ * may cover 32 of its rows, the rest weighted 0), written as f32
+ * (out_f32 != 0) or bf16 into D [E][M][N]; 0 for an expert without rows.
+ * ws: moe_grouped_wgrad_workspace_size() bytes, 256-byte aligned.
+ * M % 32 == 0, N % 32 == 0. */
+MOE_API moe_status_t moe_grouped_wgrad_nvfp4(const uint8_t* Aq, const uint8_t* As, const float* sgA,
+                                     const uint8_t* Bq, const uint8_t* Bs, const float* sgB,
+                                     const int32_t* counts, const int32_t* offsets,
+                                     int E, int M, int N, int R_cap,
+                                     void* D, int out_f32, void* ws, size_t ws_bytes,
+                                     int sm_margin, int32_t* status, moe_stream_t stream);
 
 /* Unpermute + combine ([MegaMoE] §2.1: y = sum_{i in topk} p_i E_i(x)).
  * out[t] = bf16( sum_j topk_prob[t][j] * y_perm[row_of[t*k+j]] ) over
@@ -403,6 +421,27 @@ MOE_API moe_status_t moe_amax_bf16(const moe_bf16* x, size_t n, float* amax, moe
  * R % 16 == 0, q 8-byte aligned. */
 MOE_API moe_status_t moe_nvfp4_cast_cols(const moe_bf16* src, int G, int R, int C, const float* amax,
                                          uint8_t* q, uint8_t* s, float* s_global, moe_stream_t stream);
+
+/* NVFP4 backward operands ([MoE-Fusion] "Fusing MXFP8 and NVFP4
+ * quantisation": the weight-gradient GEMM reads the transposed tensors after
+ * a random Hadamard rotation, whose per-tensor amax the dGLU epilogue writes
+ * for dFC1).  For src [R_cap][C] bf16 in the permuted layout (dFC1, x_perm;
+ * rows >= offsets[E] are not read) every 16-row block of every column is
+ * rotated, z = H16 diag(s) v / 4 (H16 the Sylvester Hadamard matrix, bit i of
+ * signs set -> s_i = -1, the same rotation as moe_act_out_t.rht_amax), and:
+ *   moe_rht_amax_cols   writes max |z| to *amax (device float, overwritten);
+ *   moe_nvfp4_rht_cast_cols casts z column-wise to NVFP4 under
+ *       s_g = 2688 / amax (amax = that rotated amax), written to *s_global:
+ *       q [C][R_cap/2] (element 2i in the low nibble), s [C][R_cap/16] E4M3;
+ *       blocks at or past offsets[E] are not written.
+ * The rotation is orthonormal, so rotating both operands of the weight
+ * gradient along its contracted rows leaves the product unchanged.
+ * R_cap % 128 == 0; q 16-byte and s 4-byte aligned. */
+MOE_API moe_status_t moe_rht_amax_cols(const moe_bf16* src, int R_cap, int C, const int32_t* offsets, int E,
+                                       uint32_t signs, float* amax, moe_stream_t stream);
+MOE_API moe_status_t moe_nvfp4_rht_cast_cols(const moe_bf16* src, int R_cap, int C, const int32_t* offsets, int E,
+                                             const float* amax, uint32_t signs, uint8_t* q, uint8_t* s,
+                                             float* s_global, moe_stream_t stream);
 
 /* Standalone activation of the unfused path: pre [R][N1] bf16 -> y [R][F]
  * bf16 (rows >= offsets[E] untouched, pad rows 0).  F % 32 == 0; pre and y
