@@ -44,6 +44,11 @@ def _rot_operand(rt, R_cap, cols, seed):
     return vb, qf, sf, sg
 
 
+def _zero_codes_as_one(q):
+    lo, hi = q & 0xF, q >> 4
+    return (np.where(lo == 8, 0, lo) | (np.where(hi == 8, 0, hi) << 4)).astype(np.uint8)
+
+
 @pytest.mark.parametrize("M,N", [(256, 384), (96, 160), (2880, 288)])
 def test_nvfp4_wgrad_edge_counts(M, N):
     counts = [0, 1, 31, 33, 129, 300, 0]
@@ -78,7 +83,11 @@ def test_rotated_cast_and_amax():
     assert math.isclose(float(am.item()), O.rht_transposed_amax(v[:R], SIGNS), rel_tol=1e-6)
     assert math.isclose(float(sg.item()), float(sg_ref), rel_tol=1e-6)
     qg, sgc = np_(q)[:, : R // 2], np_(s)[:, : R // 16]
-    assert (qg == q_ref[:, : R // 2]).mean() >= 0.999 and (sgc == s_ref[:, : R // 16]).mean() >= 0.999
+    # a rotated value that is exactly zero (blocks of pad rows) comes out as +0 or -0
+    # depending on the order of the sums (fp32 butterfly vs float64): E2M1 codes 0x0 and
+    # 0x8 both mean 0, so the two zero codes are identified before comparing
+    assert (_zero_codes_as_one(qg) == _zero_codes_as_one(q_ref[:, : R // 2])).mean() >= 0.999
+    assert (sgc == s_ref[:, : R // 16]).mean() >= 0.999
     dg = O.nvfp4_dequantize(qg, sgc, float(sg.item()))
     dr = O.nvfp4_dequantize(q_ref[:, : R // 2], s_ref[:, : R // 16], sg_ref)
     blk = np.repeat(np.maximum(O.e4m3_decode(sgc), O.e4m3_decode(s_ref[:, : R // 16])), 16, axis=1) / float(sg_ref)
