@@ -122,4 +122,11 @@ def test_nvfp4_dw1_chain():
     qa, sb_a = O.nvfp4_rht_cast_cols(d, SIGNS, sa)
     qx, sb_x = O.nvfp4_rht_cast_cols(xp, SIGNS, sx)
     ref = O.bf16_round(O.grouped_wgrad_nvfp4(qa, sb_a, sa, qx, sb_x, sx, rt))
-    assert_chain_close(np_(D), ref, "NVFP4 dW1")
+    # The GEMM and the casts are checked tightly above.  Along the chain both sides
+    # round their own dFC1 to bf16; where the two differ by one step, the rotation
+    # spreads it over 16 values and an E2M1 code may flip.  One flip moves one
+    # product term by up to the 4 <-> 6 step of E2M1, a third of its block's
+    # largest magnitude: about 1/sqrt(K) ~ 4% of an output that sums K ~ 500
+    # tokens (the hottest expert of this batch).  So: the bf16 rule on 99.9% of
+    # the elements and every element within 5% of the output's largest magnitude.
+    assert_chain_close(np_(D), ref, "NVFP4 dW1", max_frac=0.05)
