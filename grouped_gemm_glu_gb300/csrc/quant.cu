@@ -438,8 +438,10 @@ __global__ void __launch_bounds__(256) k_amax_bf16(const uint4* __restrict__ x, 
   uint32_t m = 0;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
     const uint4 w = __ldg(x + i);
-    const uint32_t a = max(max(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu), max(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
-    m = max(m, max(a & 0xFFFFu, a >> 16));
+    // magnitudes of the eight bf16 values, each half of a word on its own
+    const uint32_t wv[4] = {w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu, w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) m = max(m, max(wv[h] & 0xFFFFu, wv[h] >> 16));
   }
   m = __reduce_max_sync(0xFFFFFFFFu, m);
   if ((threadIdx.x & 31) == 0 && m != 0) atomicMax(reinterpret_cast<int*>(amax), (int)(m << 16));
