@@ -55,7 +55,8 @@ SHAPE = {"dsv3": "DeepSeek-V3-shaped expert-parallel shard", "gptoss": "GPT-OSS-
 
 
 def workload_desc(w):
-    fwd = ("NVFP4 forward (FC1 bf16 + amax -> E2M1/E4M3 casts -> block-scaled NVFP4 FC2), MXFP8 backward"
+    fwd = ("NVFP4 (forward: FC1 bf16 + amax -> E2M1/E4M3 casts -> block-scaled NVFP4 FC2; backward: dGLU "
+           "bf16 + amax + rotated amax -> NVFP4 dX, random-Hadamard-rotated NVFP4 weight gradients)"
            if w.out == "nvfp4" else "MXFP8 E4M3/E8M0 outputs + transposed copies")
     return (f"{w.name}: {SHAPE.get(w.name, w.name)}, T={w.T} H={w.H} experts "
             f"{w.expert_begin}..{w.expert_begin + w.E - 1} of {w.n_experts}, top-{w.k}, F={w.F}, {w.act}, "
@@ -66,6 +67,7 @@ def kernel_model(name, w, R, Rp):
     """Algorithmic FLOPs, minimal HBM bytes and the arithmetic type of one
     launch of each step kernel (R real rows, Rp padded rows)."""
     E, H, F, N1, T, k = w.E, w.H, w.F, w.N1, w.T, w.k
+    nv = 1 / 2 + 1 / 16  # bytes per NVFP4 element: E2M1 code + E4M3 scale per 16
     m = {
         "route_permute": (0, T * k * 8 + 2 * R * H * 2 + (Rp - R) * H * 2, None),
         "fc1_glu_quant": (2 * R * H * N1, E * N1 * H * 2 + R * H * 2 + R * N1 * 2 + 2 * R * F * (1 + 1 / 32),
@@ -88,7 +90,23 @@ def kernel_model(name, w, R, Rp):
         "amax_w2": (0, E * F * H * 2, None),
         "quant_w2_nvfp4": (0, E * F * H * 2 + E * F * H * (1 / 2 + 1 / 16), None),
         "fc2_nvfp4": (2 * R * F * H, E * H * F * (1 / 2 + 1 / 16) + R * F * (1 / 2 + 1 / 16) + R * H * 2, "fp4"),
-        "quant_a_col": (0, R * F * 2 + R * F * (1 + 1 / 32), None),
+        # NVFP4 backward: dGLU writes bf16 dFC1 + its amax and rotated amax; NVFP4 rows of dFC1
+        # and W1 (along 2F) for dX; rotated column-wise NVFP4 casts (with their amax passes)
+        # of dFC1, x, a and dY for the weight gradients
+        "dglu_nvfp4": (2 * R * H * F, E * F * H * 2 + R * H * 2 + R * N1 * 2 + R * N1 * 2, "bf16"),
+        "quant_d_nvfp4": (0, R * N1 * 2 + R * N1 * nv, None),
+        "amax_w1": (0, E * N1 * H * 2, None),
+        "quant_w1_nvfp4": (0, E * N1 * H * 2 + E * N1 * H * nv, None),
+        "dx_nvfp4": (2 * R * N1 * H, E * H * N1 * nv + R * N1 * nv + R * H * 2, "fp4"),
+        "quant_d_rht": (0, R * N1 * 2 + R * N1 * nv, None),
+        "rht_amax_x": (0, R * H * 2, None),
+        "quant_x_rht": (0, R * H * 2 + R * H * nv, None),
+        "wgrad_w1_nvfp4": (2 * R * N1 * H, (N1 + H) * R * nv + E * N1 * H * 2, "fp4"),
+        "rht_amax_a": (0, R * F * 2, None),
+        "quant_a_rht": (0, R * F * 2 + R * F * nv, None),
+        "rht_amax_dy": (0, R * H * 2, None),
+        "quant_dy_rht": (0, R * H * 2 + R * H * nv, None),
+        "wgrad_w2_nvfp4": (2 * R * F * H, (F + H) * R * nv + E * F * H * 2, "fp4"),
     }
     return m[name]
 
@@ -314,7 +332,7 @@ def main():
     else:
         params = L.glu_params(w.act)
     layer = MoeLayer(g["W1"], g["W2"], w.T, w.k, R_cap, params, b1=g.get("b1"), expert_begin=w.expert_begin,
-                     sm_margin=args.sm_margin, gated=w.gated, nvfp4_fwd=w.out == "nvfp4")
+                     sm_margin=args.sm_margin, gated=w.gated, nvfp4=w.out == "nvfp4")
     X, I, P, DO = g["x"], g["topk_idx"], g["topk_prob"], g["dOut"]
     for _ in range(args.warmup):
         layer.step(X, I, P, DO)
@@ -434,15 +452,15 @@ def main():
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / n
 
-    by_name = dict(layer.step_calls(X, I, P, DO))
     ufwd, ubwd = layer.forward_unfused_calls(), layer.backward_unfused_calls(layer.dY_perm)
     fused_fc1 = [("fc1_glu_quant", layer.fc1_mxfp8_call())]
-    for calls in (fused_fc1, ufwd, [("dglu_quant", by_name["dglu_quant"])], ubwd):
+    fused_dglu = [("dglu_quant", layer.dglu_mxfp8_call())]
+    for calls in (fused_fc1, ufwd, fused_dglu, ubwd):
         layer.run(calls)  # warm-up
     na = max(3, min(args.steps, 20))
     f_ms = timed(fused_fc1, na)
     uf_ms = timed(ufwd, na)
-    b_ms = timed([("dglu_quant", by_name["dglu_quant"])], na)
+    b_ms = timed(fused_dglu, na)
     ub_ms = timed(ubwd, na)
     ablation = {
         "forward": {"fused_ms": round(f_ms, 4), "unfused_ms": round(uf_ms, 4), "speedup": round(uf_ms / f_ms, 3),
@@ -549,7 +567,7 @@ def main():
     # short region), then both together
     fused = {}
     fl_sum = ms_sum = 0.0
-    for n in ("fc1_glu_nvfp4" if w.out == "nvfp4" else "fc1_glu_quant", "dglu_quant"):
+    for n in (("fc1_glu_nvfp4", "dglu_nvfp4") if w.out == "nvfp4" else ("fc1_glu_quant", "dglu_quant")):
         fl_n, by_n, _ = kernel_model(n, w, R, Rp)
         tf = fl_n / per_kernel[n] / 1e9
         fused[n] = {"ms": round(per_kernel[n], 4), "TFLOP/s": round(tf, 1),
@@ -574,7 +592,7 @@ def main():
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16+mxfp8",
+        "dtype": "bf16+nvfp4" if w.out == "nvfp4" else "bf16+mxfp8",
         "data": "synthetic (seeded; random-init weights N(0,1/H), x N(0,1), router logits N(0,1))",
         "config": {"workload": workload_desc(w), "T": w.T, "H": w.H, "E_local": w.E, "experts": w.n_experts,
                    "top_k": w.k, "F": w.F, "R_cap": R_cap, "routed_rows": R, "padded_rows": Rp,

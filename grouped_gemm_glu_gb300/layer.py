@@ -30,13 +30,17 @@ from .ops import _p, _s
 class MoeLayer:
     def __init__(self, W1, W2, T: int, k: int, R_cap: int, params: L.GluParams, b1=None,
                  expert_begin: int = 0, sm_margin: int = 0, gated: bool = True, dynamic: bool = True,
-                 nvfp4_fwd: bool = False):
+                 nvfp4: bool = False, rht_signs: int = 0x6A5D):
         """dynamic: the bf16 grouped GEMMs take their tiles from the dynamic
         scheduler (each call site has its own counter workspace); False runs
-        the static schedule.  nvfp4_fwd: the forward runs the NVFP4 recipe
-        (FC1 epilogue in NVFP4 mode -> NVFP4 cast of its output and of W2 ->
-        NVFP4 FC2); the backward stays MXFP8 (the FC2 weight gradient then
-        reads a column-wise MXFP8 cast of the bf16 FC1 output)."""
+        the static schedule.  nvfp4: the step runs the NVFP4 recipe.  Forward:
+        FC1 epilogue in NVFP4 mode (bf16 + amax) -> NVFP4 casts of its output
+        and of W2 -> NVFP4 FC2.  Backward: the dGLU epilogue in NVFP4 mode (bf16
+        dFC1, its amax and the amax of its transposed random Hadamard rotation
+        with the 16 signs rht_signs) -> NVFP4 dFC1 and W1 (along 2F) -> NVFP4
+        dX; the weight gradients on the rotated column-wise NVFP4 casts of
+        dFC1, x, the FC1 output and dY (the same signs on both operands of a
+        product, so the rotation cancels)."""
         self.lib = L.load()
         dev = W1.device
         self.dev = dev
@@ -110,8 +114,8 @@ class MoeLayer:
             self.ws_db_bytes = lib.moe_grouped_dglu_workspace_size(N1, R_cap)
         if self.ws_db_bytes:
             self.ws_db = z(self.ws_db_bytes, dt=u8)
-        self.nvfp4_fwd = nvfp4_fwd
-        if nvfp4_fwd:
+        self.nvfp4 = nvfp4
+        if nvfp4:
             f32 = torch.float32
             self.a_y, self.a_amax = z(R_cap, F), z(1, dt=f32)
             self.a_q4, self.a_s4, self.a_sg = z(R_cap, F // 2, dt=u8), z(R_cap, F // 16, dt=u8), z(1, dt=f32)
@@ -121,6 +125,23 @@ class MoeLayer:
                                      self.pre.data_ptr())
             self.fc2_a4 = L.in_operand(self.a_q4.data_ptr(), self.a_s4.data_ptr(), self.a_sg.data_ptr())
             self.fc2_w4 = L.in_operand(self.W2q4.data_ptr(), self.W2s4.data_ptr(), self.w2_sg.data_ptr())
+            # backward: bf16 dFC1 with its amaxes; NVFP4 rows of dFC1 and W1 (along 2F) for dX;
+            # rotated column-wise NVFP4 of dFC1, x, a and dY for the weight gradients
+            self.rht_signs = int(rht_signs) & 0xFFFF
+            one = lambda: z(1, dt=f32)
+            self.d_y, self.d_amax, self.d_rht = z(R_cap, N1), one(), one()
+            self.d_q4, self.d_s4, self.d_sg = z(R_cap, N1 // 2, dt=u8), z(R_cap, N1 // 16, dt=u8), one()
+            self.w1_amax, self.w1_sg = one(), one()
+            self.W1q4, self.W1s4 = z(E, H, N1 // 2, dt=u8), z(E, H, N1 // 16, dt=u8)
+            rot = lambda C_: (z(C_, R_cap // 2, dt=u8), z(C_, R_cap // 16, dt=u8), one(), one())
+            self.d_rq, self.d_rs, self.d_rsg, _ = rot(N1)
+            self.x_rq, self.x_rs, self.x_rsg, self.x_ramax = rot(H)
+            self.dy_rq, self.dy_rs, self.dy_rsg, self.dy_ramax = rot(H)
+            self.a_rq, self.a_rs, self.a_rsg, self.a_ramax = rot(F)
+            self.bwd_out4 = L.ActOut(None, None, None, None, self.d_y.data_ptr(), self.d_amax.data_ptr(), None,
+                                     None, self.d_rht.data_ptr(), self.rht_signs)
+            self.dx_a4 = L.in_operand(self.d_q4.data_ptr(), self.d_s4.data_ptr(), self.d_sg.data_ptr())
+            self.dx_w4 = L.in_operand(self.W1q4.data_ptr(), self.W1s4.data_ptr(), self.w1_sg.data_ptr())
         # operands and outputs of the two block-scaled M-grouped GEMMs
         self.fc2_a = L.in_operand(self.a_q.data_ptr(), self.a_s.data_ptr())
         self.fc2_w = L.in_operand(self.W2q.data_ptr(), self.W2s.data_ptr())
@@ -138,7 +159,7 @@ class MoeLayer:
         lib, s = self.lib, _s()
         E, N1, H, F, T, k, R = self.E, self.N1, self.H, self.F, self.T, self.k, self.R_cap
         st = _p(self.status)
-        if self.nvfp4_fwd:
+        if self.nvfp4:
             return self._forward_calls_nvfp4(x, topk_idx, topk_prob)
         return [
             ("route_permute", lambda: lib.moe_route_permute(
@@ -165,6 +186,16 @@ class MoeLayer:
             _p(self.x_perm), _p(self.W1p), _p(self.b1p), None, _p(self.counts), _p(self.offsets), E, H, F, R,
             C.byref(self.params), L.OUT_MXFP8, C.byref(self.fc1_out), _p(self.ws_fc1), self.ws_fc1_bytes,
             self.sm_margin, st, s)
+
+    def dglu_mxfp8_call(self):
+        """The fused dGLU with MXFP8 row + column outputs (the MXFP8 backward's
+        dGLU call; also the fused side of the backward ablation)."""
+        lib, s = self.lib, _s()
+        E, H, F, R = self.E, self.H, self.F, self.R_cap
+        return lambda: lib.moe_grouped_dglu_quant_bwd(
+            _p(self.dY_perm), _p(self.W2), _p(self.pre), None, _p(self.counts), _p(self.offsets), E, H, F, R,
+            C.byref(self.params), L.OUT_MXFP8, C.byref(self.bwd_out), _p(self.db1), _p(self.ws_db),
+            self.ws_db_bytes, self.sm_margin, _p(self.status), s)
 
     def _forward_calls_nvfp4(self, x, topk_idx, topk_prob):
         lib, s = self.lib, _s()
@@ -197,14 +228,13 @@ class MoeLayer:
         E, N1, H, F, T, k, R = self.E, self.N1, self.H, self.F, self.T, self.k, self.R_cap
         st = _p(self.status)
         dY_perm = self.dY_perm
+        if self.nvfp4:
+            return self._backward_calls_nvfp4(dOut)
         return [
             ("combine_bwd", lambda: lib.moe_combine_bwd(
                 _p(dOut), _p(self.y_perm), _p(self.row_of), _p(self.tok_of), _p(self.prob_perm), _p(self.offsets),
                 T, H, k, E, R, _p(dY_perm), _p(self.dprob), st, s)),
-            ("dglu_quant", lambda: lib.moe_grouped_dglu_quant_bwd(
-                _p(dY_perm), _p(self.W2), _p(self.pre), None, _p(self.counts), _p(self.offsets), E, H, F, R,
-                C.byref(self.params), L.OUT_MXFP8, C.byref(self.bwd_out), _p(self.db1), _p(self.ws_db),
-                self.ws_db_bytes, self.sm_margin, st, s)),
+            ("dglu_quant", self.dglu_mxfp8_call()),
             ("quant_w1", lambda: lib.moe_quantize_mxfp8(
                 _p(self.W1p), E, N1, H, 1, None, None, 0, _p(self.W1q), _p(self.W1s), st, s)),
             ("dx", lambda: lib.moe_grouped_fc2_fwd(
@@ -217,12 +247,54 @@ class MoeLayer:
             ("wgrad_w1", lambda: lib.moe_grouped_wgrad(
                 _p(self.d_qc), _p(self.d_sc), _p(self.x_qc), _p(self.x_sc), _p(self.counts), _p(self.offsets), E,
                 N1, H, R, _p(self.dW1), 0, _p(self.ws_wg1), self.ws_wg1.numel(), self.sm_margin, st, s)),
-            *([("quant_a_col", lambda: lib.moe_quantize_mxfp8(
-                _p(self.a_y), 1, R, F, 1, _p(self.counts), _p(self.offsets), E, _p(self.a_qc), _p(self.a_sc), st,
-                s))] if self.nvfp4_fwd else []),
             ("wgrad_w2", lambda: lib.moe_grouped_wgrad(
                 _p(self.a_qc), _p(self.a_sc), _p(self.dy_qc), _p(self.dy_sc), _p(self.counts), _p(self.offsets),
                 E, F, H, R, _p(self.dW2), 0, _p(self.ws_wg2), self.ws_wg2.numel(), self.sm_margin, st, s)),
+            ("permute_bwd", lambda: lib.moe_permute_bwd(
+                _p(self.dX_perm), _p(self.row_of), T, H, k, _p(self.dx), st, s)),
+        ]
+
+    def _backward_calls_nvfp4(self, dOut):
+        lib, s = self.lib, _s()
+        E, N1, H, F, T, k, R = self.E, self.N1, self.H, self.F, self.T, self.k, self.R_cap
+        st, cnt, off = _p(self.status), _p(self.counts), _p(self.offsets)
+        sig = self.rht_signs
+
+        def rot_cast(name, src, C_, ramax, q, sc, sg, amax_call=True):
+            calls = []
+            if amax_call:
+                calls.append((f"rht_amax_{name}", lambda: lib.moe_rht_amax_cols(_p(src), R, C_, off, E, sig, _p(ramax),
+                                                                                 s)))
+            calls.append((f"quant_{name}_rht", lambda: lib.moe_nvfp4_rht_cast_cols(_p(src), R, C_, off, E, _p(ramax),
+                                                                                    sig, _p(q), _p(sc), _p(sg), s)))
+            return calls
+
+        return [
+            ("combine_bwd", lambda: lib.moe_combine_bwd(
+                _p(dOut), _p(self.y_perm), _p(self.row_of), _p(self.tok_of), _p(self.prob_perm), off,
+                T, H, k, E, R, _p(self.dY_perm), _p(self.dprob), st, s)),
+            ("dglu_nvfp4", lambda: lib.moe_grouped_dglu_quant_bwd(
+                _p(self.dY_perm), _p(self.W2), _p(self.pre), None, cnt, off, E, H, F, R, C.byref(self.params),
+                L.OUT_NVFP4, C.byref(self.bwd_out4), _p(self.db1), _p(self.ws_db), self.ws_db_bytes,
+                self.sm_margin, st, s)),
+            ("quant_d_nvfp4", lambda: lib.moe_nvfp4_cast(
+                _p(self.d_y), _p(self.d_amax), cnt, off, E, N1, R, _p(self.d_q4), _p(self.d_s4), _p(self.d_sg), s)),
+            ("amax_w1", lambda: lib.moe_amax_bf16(_p(self.W1p), self.W1p.numel(), _p(self.w1_amax), s)),
+            ("quant_w1_nvfp4", lambda: lib.moe_nvfp4_cast_cols(
+                _p(self.W1p), E, N1, H, _p(self.w1_amax), _p(self.W1q4), _p(self.W1s4), _p(self.w1_sg), s)),
+            ("dx_nvfp4", lambda: lib.moe_grouped_fc2_fwd(
+                C.byref(self.dx_a4), C.byref(self.dx_w4), cnt, off, E, N1, H, R, L.OUT_BF16, C.byref(self.dx_out),
+                _p(self.ws_dx), self.ws_dx.numel(), self.sm_margin, st, s)),
+            *rot_cast("d", self.d_y, N1, self.d_rht, self.d_rq, self.d_rs, self.d_rsg, amax_call=False),
+            *rot_cast("x", self.x_perm, H, self.x_ramax, self.x_rq, self.x_rs, self.x_rsg),
+            ("wgrad_w1_nvfp4", lambda: lib.moe_grouped_wgrad_nvfp4(
+                _p(self.d_rq), _p(self.d_rs), _p(self.d_rsg), _p(self.x_rq), _p(self.x_rs), _p(self.x_rsg), cnt, off,
+                E, N1, H, R, _p(self.dW1), 0, _p(self.ws_wg1), self.ws_wg1.numel(), self.sm_margin, st, s)),
+            *rot_cast("a", self.a_y, F, self.a_ramax, self.a_rq, self.a_rs, self.a_rsg),
+            *rot_cast("dy", self.dY_perm, H, self.dy_ramax, self.dy_rq, self.dy_rs, self.dy_rsg),
+            ("wgrad_w2_nvfp4", lambda: lib.moe_grouped_wgrad_nvfp4(
+                _p(self.a_rq), _p(self.a_rs), _p(self.a_rsg), _p(self.dy_rq), _p(self.dy_rs), _p(self.dy_rsg), cnt,
+                off, E, F, H, R, _p(self.dW2), 0, _p(self.ws_wg2), self.ws_wg2.numel(), self.sm_margin, st, s)),
             ("permute_bwd", lambda: lib.moe_permute_bwd(
                 _p(self.dX_perm), _p(self.row_of), T, H, k, _p(self.dx), st, s)),
         ]

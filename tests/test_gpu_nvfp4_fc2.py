@@ -110,23 +110,52 @@ def test_nvfp4_forward_chain(act):
     assert_chain_close(np_(y)[: rt.R_pad], O.bf16_round(ref), f"nvfp4 chain {act}")
 
 
-def test_layer_nvfp4_forward_step_and_graph():
-    """MoeLayer with the NVFP4 forward on the skewed config (small T and H):
-    the layer output against the oracle's NVFP4 chain, the FC2 weight gradient
-    on the layer's own operands (the MXFP8 column cast of the bf16 FC1
-    output), and one captured graph replaying to the eager results."""
+def _zero_codes_as_one(q):
+    """E2M1 codes 0x0 and 0x8 (+0, -0) both mean zero; map -0 to +0 in both nibbles."""
+    lo, hi = q & 0xF, q >> 4
+    return (np.where(lo == 8, 0, lo) | (np.where(hi == 8, 0, hi) << 4)).astype(np.uint8)
+
+
+def _assert_rot_cast(q, s, sg, v, signs, what):
+    """A rotated column-wise NVFP4 cast of the layer's bf16 tensor v [Rp, C]
+    against the oracle's cast of the same tensor under the same s_g: codes and
+    scales equal on >= 99.9% (a rotated value the fp32 butterfly and the
+    float64 oracle round differently may cross an E2M1 / E4M3 boundary), the
+    dequantised values within two E2M1 steps of their block everywhere."""
+    Rp = v.shape[0]
+    qr, sr = O.nvfp4_rht_cast_cols(v, signs, sg)
+    qg, sgc = np_(q)[:, : Rp // 2], np_(s)[:, : Rp // 16]
+    assert (_zero_codes_as_one(qg) == _zero_codes_as_one(qr)).mean() >= 0.999, what
+    assert (sgc == sr).mean() >= 0.999, what
+    dg, dr = O.nvfp4_dequantize(qg, sgc, sg), O.nvfp4_dequantize(qr, sr, sg)
+    blk = np.repeat(np.maximum(O.e4m3_decode(sgc), O.e4m3_decode(sr)), 16, axis=1) / float(sg)
+    assert np.all(np.abs(dg - dr) <= 2.0 * blk * (1 + 1e-6)), what
+
+
+SIGNS = 0x6A5D
+
+
+def test_layer_nvfp4_step_and_graph():
+    """MoeLayer in NVFP4 mode on the skewed config (small T and H).  Forward:
+    the layer output against the oracle's NVFP4 chain.  Backward: dFC1 and its
+    two amaxes against the oracle's dGLU on the layer's dY and saved pre; every
+    NVFP4 cast against the oracle's cast of the layer's own bf16 tensor; dX,
+    dW1 and dW2 against the oracle's GEMMs on the layer's own NVFP4 operands;
+    dx through the permute backward.  Then one captured graph replays to the
+    eager results."""
     from grouped_gemm_glu_gb300.layer import MoeLayer
     w = synth.scaled(synth.WORKLOADS["skew"], T=1024, H=512)
     inp = synth.make_inputs(w, 3)
     g = {k: (v.to(DEV) if v is not None else None) for k, v in inp.items()}
-    layer = MoeLayer(g["W1"], g["W2"], w.T, w.k, w.R_cap, L.glu_params("geglu"), nvfp4_fwd=True)
+    prm = O.ActParams(O.ACT_GEGLU)
+    layer = MoeLayer(g["W1"], g["W2"], w.T, w.k, w.R_cap, L.glu_params("geglu"), nvfp4=True, rht_signs=SIGNS)
     args = (g["x"], g["topk_idx"], g["topk_prob"], g["dOut"])
     layer.step(*args)
     torch.cuda.synchronize()
     assert ops.read_status(layer.status) == 0
     rt = O.route(inp["topk_idx"].numpy(), 0, w.E)
     Rp = rt.R_pad
-    fo = O.fc1_glu_fwd(O.permute(np_(inp["x"]), rt), O.repack_fc1(np_(inp["W1"])), None, rt, O.ActParams(O.ACT_GEGLU))
+    fo = O.fc1_glu_fwd(O.permute(np_(inp["x"]), rt), O.repack_fc1(np_(inp["W1"])), None, rt, prm)
     sa = O.nvfp4_global_scale(fo.amax)
     qa, sba = O.nvfp4_quantize_rows(O.bf16_round(fo.y), sa)
     W2 = np_(inp["W2"])
@@ -136,12 +165,48 @@ def test_layer_nvfp4_forward_step_and_graph():
                                           np.stack([c[1] for c in cols]), sw, rt))
     out = O.bf16_round(O.unpermute_combine(y, rt.row_of, inp["topk_prob"].numpy()))
     assert_chain_close(np_(layer.out), out, "NVFP4 layer output")
-    deq = lambda q, s_: O.mx_dequantize(np_(q), np_(s_))
-    qc, sc = O.mx_quantize_cols(np_(layer.a_y)[:Rp])   # the layer's bf16 FC1 output, cast by the oracle
-    assert_exact(np_(layer.a_qc)[:, :Rp], qc, "column cast of the bf16 FC1 output")
-    assert_exact(np_(layer.a_sc)[:, :Rp // 32], sc, "its scales")
-    dW2 = O.grouped_wgrad(deq(layer.a_qc, layer.a_sc)[:, :Rp], deq(layer.dy_qc, layer.dy_sc)[:, :Rp], rt)
-    assert_bf16_close(np_(layer.dW2), O.bf16_round(dW2), "dW2 on the layer's operands")
+
+    # dFC1 from the layer's own dY and saved pre; its amax and rotated amax (fp32, before bf16)
+    d_ref = O.dglu_bwd(np_(layer.dY_perm)[:Rp], W2, np_(layer.pre)[:Rp], rt, prm)
+    d = np_(layer.d_y)[:Rp]
+    assert_bf16_close(d, O.bf16_round(d_ref), "dFC1")
+    assert abs(float(layer.d_amax.item()) / np.max(np.abs(d_ref)) - 1) < 1e-2
+    assert abs(float(layer.d_rht.item()) / O.rht_transposed_amax(d_ref, SIGNS) - 1) < 1e-2
+    # NVFP4 rows of dFC1 and W1 along 2F: the data gradient's operands
+    sd = O.nvfp4_global_scale(float(layer.d_amax.item()))
+    assert float(layer.d_sg.item()) == float(sd)
+    qd, sbd = O.nvfp4_quantize_rows(d, sd)
+    assert_exact(_zero_codes_as_one(np_(layer.d_q4)[:Rp]), _zero_codes_as_one(qd), "dFC1 NVFP4 codes")
+    assert_exact(np_(layer.d_s4)[:Rp], sbd, "dFC1 NVFP4 scales")
+    W1p = np_(layer.W1p)
+    s1 = O.nvfp4_global_scale(float(np.max(np.abs(W1p))))
+    assert float(layer.w1_sg.item()) == float(s1)
+    c1 = [O.nvfp4_quantize_cols(W1p[e], s1) for e in range(w.E)]
+    assert_exact(np_(layer.W1q4), np.stack([c[0] for c in c1]), "W1 NVFP4 codes (along 2F)")
+    assert_exact(np_(layer.W1s4), np.stack([c[1] for c in c1]), "W1 NVFP4 scales")
+    dX = O.grouped_gemm_nvfp4(np_(layer.d_q4)[:Rp], np_(layer.d_s4)[:Rp], float(layer.d_sg.item()),
+                              np_(layer.W1q4), np_(layer.W1s4), float(layer.w1_sg.item()), rt)
+    assert_bf16_close(np_(layer.dX_perm)[:Rp], O.bf16_round(dX), "NVFP4 dX on the layer's operands")
+    dx = O.permute_bwd(np_(layer.dX_perm)[:Rp], rt.row_of, w.T, w.k)
+    assert_bf16_close(np_(layer.dx), O.bf16_round(dx), "dx")
+
+    # rotated column-wise casts and the weight gradients
+    rot = {"d": (d, layer.d_rht), "x": (np_(layer.x_perm)[:Rp], layer.x_ramax),
+           "a": (np_(layer.a_y)[:Rp], layer.a_ramax), "dy": (np_(layer.dY_perm)[:Rp], layer.dy_ramax)}
+    for n, (v, am) in rot.items():
+        if n != "d":
+            assert abs(float(am.item()) / O.rht_transposed_amax(v, SIGNS) - 1) < 1e-6, n
+        sg = getattr(layer, f"{n}_rsg")
+        assert abs(float(sg.item()) / float(O.nvfp4_global_scale(float(am.item()))) - 1) < 1e-6, n
+        _assert_rot_cast(getattr(layer, f"{n}_rq"), getattr(layer, f"{n}_rs"), float(sg.item()), v, SIGNS,
+                         f"rotated cast of {n}")
+    op = lambda n: (np_(getattr(layer, f"{n}_rq"))[:, : Rp // 2], np_(getattr(layer, f"{n}_rs"))[:, : Rp // 16],
+                    float(getattr(layer, f"{n}_rsg").item()))
+    dW1 = O.grouped_wgrad_nvfp4(*op("d"), *op("x"), rt)
+    assert_bf16_close(np_(layer.dW1), O.bf16_round(dW1), "NVFP4 dW1 on the layer's operands")
+    dW2 = O.grouped_wgrad_nvfp4(*op("a"), *op("dy"), rt)
+    assert_bf16_close(np_(layer.dW2), O.bf16_round(dW2), "NVFP4 dW2 on the layer's operands")
+
     eager = {k: getattr(layer, k).clone() for k in ("out", "dx", "dW1", "dW2", "dprob")}
     graph = layer.capture(*args)
     for t in eager:
