@@ -269,25 +269,53 @@ __global__ void __launch_bounds__(256) k_quant_cols(const __grid_constant__ CUte
   }
 }
 
+// Eight fp32 values (a.x, a.y, b.x, ... d.y) to E2M1, round to nearest even
+// with saturation, packed element 2i in the low nibble of byte i: each
+// cvt...e2m1x2 puts its first source operand in the high nibble, and the
+// four bytes are joined by one vector move.
+__device__ __forceinline__ uint32_t e2m1x8(float2 a, float2 b, float2 c, float2 d) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q3, %8, %7;\n\t"
+      "mov.b32 %0, {q0, q1, q2, q3};\n\t}"
+      : "=r"(r)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y), "f"(d.x), "f"(d.y));
+  return r;
+}
+
 // One NVFP4 block of 16 values under the per-tensor scale sg: returns the
 // E4M3 block-scale byte and writes the 16 E2M1 codes (element 2i in the low
 // nibble of byte i) to w[0..1].  s_b = E4M3(fp32(amax_b / 6) * sg),
-// q = E2M1(fp32(v * fp32(sg / s_b))), each step one fp32 operation.
-__device__ __forceinline__ uint32_t nvfp4_block16(const float* v, float sg, uint32_t* w) {
+// q = E2M1(fp32(v * fp32(sg / s_b))), each step one fp32 operation.  The
+// block is pre * v[0..15] with pre a power of two (the 1/4 of the Hadamard
+// rotation): scaling by it is exact, so it is applied to the block amax and
+// to the quantisation multiplier instead of to each value.
+// inv_tab (optional): the multiplier of every scale code, inv_tab[c] =
+// fp32(sg / s_b(c)) * pre (0 where s_b(c) is 0 or NaN), made once per CTA by
+// nvfp4_inv_table; the same values as computed here, without a divide per block.
+__device__ __forceinline__ uint32_t nvfp4_block16(const float* v, float sg, uint32_t* w, float pre = 1.0f,
+                                                  const float* inv_tab = nullptr) {
   float ab = 0.0f;
 #pragma unroll
   for (int j = 0; j < 16; ++j) ab = fmaxf(ab, fabsf(v[j]));
+  ab *= pre;
   const float sbf = (ab / 6.0f) * sg;
   const __nv_fp8_storage_t sc = __nv_cvt_float_to_fp8(sbf, __NV_SATFINITE, __NV_E4M3);
-  const float sbv = __half2float(__half(__nv_cvt_fp8_to_halfraw(sc, __NV_E4M3)));
-  const float inv = sbv > 0.0f ? sg / sbv : 0.0f;
-  w[0] = w[1] = 0;
-#pragma unroll
-  for (int j = 0; j < 16; j += 2) {
-    const uint32_t c2 =
-        (uint32_t)__nv_cvt_float2_to_fp4x2(make_float2(v[j] * inv, v[j + 1] * inv), __NV_E2M1, cudaRoundNearest);
-    w[j / 8] |= (c2 & 0xFFu) << (8 * ((j % 8) / 2));
+  float inv;
+  if (inv_tab != nullptr) {
+    inv = inv_tab[sc & 0x7Fu];
+  } else {
+    const float sbv = __half2float(__half(__nv_cvt_fp8_to_halfraw(sc, __NV_E4M3)));
+    inv = (sbv > 0.0f ? sg / sbv : 0.0f) * pre;
   }
+  float2 x[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) x[k] = __fmul2_rn(make_float2(v[2 * k], v[2 * k + 1]), make_float2(inv, inv));
+  w[0] = e2m1x8(x[0], x[1], x[2], x[3]);
+  w[1] = e2m1x8(x[4], x[5], x[6], x[7]);
   return (uint32_t)sc;
 }
 
@@ -295,43 +323,88 @@ __device__ __forceinline__ float nvfp4_global_scale(float am) {
   return (am > 0.0f && am <= 3.402823466e38f) ? 2688.0f / am : 1.0f;
 }
 
+// The quantisation multiplier of each of the 128 non-negative E4M3 scale
+// codes (the block amax is never negative, so the sign bit stays clear):
+// tab[c] = fp32(sg / s_b(c)) * pre, 0 for s_b(c) = 0 and for the NaN code.
+// Filled by threads 0..127 of the CTA; the caller synchronises after.
+__device__ __forceinline__ void nvfp4_inv_table(float* tab, float sg, float pre) {
+  if (threadIdx.x < 128) {
+    const float sbv = __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)threadIdx.x, __NV_E4M3)));
+    tab[threadIdx.x] = (sbv > 0.0f ? sg / sbv : 0.0f) * pre;
+  }
+}
+
+// Rows [row0, row0 + 16) of CPT adjacent columns c, c + 1, ... of src [.][C]
+// bf16 as fp32.  CPT = 2 (c and C even, src 4-byte aligned): one 32-bit load
+// per row, so a warp's loads of one row cover 128 contiguous bytes.
+template <int CPT>
+__device__ __forceinline__ void load_cols16(const uint16_t* __restrict__ src, int C, size_t row0, int c,
+                                            float (&v)[CPT][16]) {
+  const uint16_t* p = src + row0 * C + c;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    if constexpr (CPT == 2) {
+      const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(p + (size_t)j * C));
+      v[0][j] = __uint_as_float(w << 16);
+      v[1][j] = __uint_as_float(w & 0xFFFF0000u);
+    } else {
+      v[0][j] = __uint_as_float((uint32_t)__ldg(p + (size_t)j * C) << 16);
+    }
+  }
+}
+
+// BPT blocks' codes (8 bytes each) and scales of one column at q_col / s_col
+// (the column's rows of q [.][R/2] and s [.][R/16], offset to the first block).
+template <int BPT>
+__device__ __forceinline__ void store_col_blocks(uint8_t* q_col, uint8_t* s_col, const uint32_t* w, uint32_t sc4,
+                                                 int nblk) {
+  if (BPT == 4 && nblk == 4) {
+    reinterpret_cast<uint4*>(q_col)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    reinterpret_cast<uint4*>(q_col)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    *reinterpret_cast<uint32_t*>(s_col) = sc4;
+  } else {
+    for (int b = 0; b < nblk; ++b) {
+      *reinterpret_cast<uint2*>(q_col + 8 * b) = make_uint2(w[2 * b], w[2 * b + 1]);
+      s_col[b] = (uint8_t)(sc4 >> (8 * b));
+    }
+  }
+}
+
 // Column-wise NVFP4 (the K-major copy of a weight whose contraction runs
 // along its rows): src [G][R][C] bf16 -> q [G][C][R/2], s [G][C][R/16].  One
-// thread per (g, BPT consecutive 16-row blocks, column); neighbouring threads
-// take neighbouring columns, so each row load is coalesced, and with BPT = 4
-// a thread's codes are one whole 32-byte sector of its output row.
-template <int BPT>
+// thread per (g, BPT consecutive 16-row blocks, CPT adjacent columns);
+// neighbouring threads take neighbouring columns, so each row load is
+// coalesced, and with BPT = 4 a thread's codes of a column are one whole
+// 32-byte sector of its output row.
+template <int BPT, int CPT>
 __global__ void __launch_bounds__(256) k_nvfp4_cast_cols(const uint16_t* __restrict__ src, int G, int R, int C,
                                                          const float* __restrict__ amax, uint8_t* __restrict__ q,
                                                          uint8_t* __restrict__ s, float* __restrict__ s_global) {
   const float sg = nvfp4_global_scale(*amax);
   if (blockIdx.x == 0 && threadIdx.x == 0) *s_global = sg;
-  const int nb = R / 16, ng = nb / BPT;
-  const size_t total = (size_t)G * ng * C;
+  const int nb = R / 16, ng = nb / BPT, ncp = C / CPT;
+  const size_t total = (size_t)G * ng * ncp;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
-    const int c = (int)(i % C);
-    const size_t rest = i / C;
+    const int c = (int)(i % ncp) * CPT;
+    const size_t rest = i / ncp;
     const int rg = (int)(rest % ng);
     const int g = (int)(rest / ng);
-    const size_t col = (size_t)g * C + c;
-    uint32_t w[2 * BPT];
-    uint32_t sc4 = 0;
+    uint32_t w[CPT][2 * BPT];
+    uint32_t sc4[CPT];
+#pragma unroll
+    for (int cc = 0; cc < CPT; ++cc) sc4[cc] = 0;
 #pragma unroll
     for (int b = 0; b < BPT; ++b) {
-      const uint16_t* p = src + ((size_t)g * R + (size_t)(rg * BPT + b) * 16) * C + c;
-      float v[16];
+      float v[CPT][16];
+      load_cols16<CPT>(src + (size_t)g * R * C, C, (size_t)(rg * BPT + b) * 16, c, v);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) v[j] = __uint_as_float((uint32_t)__ldg(p + (size_t)j * C) << 16);
-      sc4 |= nvfp4_block16(v, sg, w + 2 * b) << (8 * b);
+      for (int cc = 0; cc < CPT; ++cc) sc4[cc] |= nvfp4_block16(v[cc], sg, w[cc] + 2 * b) << (8 * b);
     }
-    uint8_t* qd = q + col * (R / 2) + (size_t)rg * BPT * 8;
-    if (BPT == 4) {
-      reinterpret_cast<uint4*>(qd)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      reinterpret_cast<uint4*>(qd)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-      *reinterpret_cast<uint32_t*>(s + col * nb + (size_t)rg * 4) = sc4;
-    } else {
-      *reinterpret_cast<uint2*>(qd) = make_uint2(w[0], w[1]);
-      s[col * nb + rg] = (uint8_t)sc4;
+#pragma unroll
+    for (int cc = 0; cc < CPT; ++cc) {
+      const size_t col = (size_t)g * C + c + cc;
+      store_col_blocks<BPT>(q + col * (R / 2) + (size_t)rg * BPT * 8, s + col * nb + (size_t)rg * BPT, w[cc],
+                            sc4[cc], BPT);
     }
   }
 }
@@ -340,10 +413,7 @@ __global__ void __launch_bounds__(256) k_nvfp4_cast_cols(const uint16_t* __restr
 // place: v <- H16 diag(s) v / 4 (s_i = -1 where bit i of signs is set;
 // Sylvester order), on fp32 values of bf16 inputs.  The same butterfly as
 // the dGLU epilogue's rotated amax.
-__device__ __forceinline__ void rht16(float* v, uint32_t signs) {
-#pragma unroll
-  for (int i = 0; i < 16; ++i)
-    if ((signs >> i) & 1u) v[i] = -v[i];
+__device__ __forceinline__ void hadamard16_unscaled(float* v) {  // v <- H16 v
 #pragma unroll
   for (int m = 1; m < 16; m <<= 1) {
 #pragma unroll
@@ -354,23 +424,41 @@ __device__ __forceinline__ void rht16(float* v, uint32_t signs) {
       v[i + m] = lo - hi;
     }
   }
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] *= 0.25f;
 }
 
-// Rows [16 b, 16 b + 16) of column c of src [R][C] bf16 as fp32.
-__device__ __forceinline__ void load_col16(const uint16_t* __restrict__ src, int C, int b, int c, float* v) {
-  const uint16_t* p = src + (size_t)b * 16 * C + c;
+// The same butterfly on two columns at once (v[j] = row j of both), with the
+// packed two-lane fp32 add; lo - hi as fma(hi, -1, lo), rounded once like
+// the subtraction.
+__device__ __forceinline__ void hadamard16_unscaled_x2(float2* v) {
+  const float2 neg1 = make_float2(-1.0f, -1.0f);
 #pragma unroll
-  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float((uint32_t)__ldg(p + (size_t)j * C) << 16);
+  for (int m = 1; m < 16; m <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i & m) continue;
+      const float2 lo = v[i], hi = v[i + m];
+      v[i] = __fadd2_rn(lo, hi);
+      v[i + m] = __ffma2_rn(hi, neg1, lo);
+    }
+  }
+}
+
+__device__ __forceinline__ void rht16(float* v, uint32_t signs) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    if ((signs >> i) & 1u) v[i] = -v[i];
+  hadamard16_unscaled(v);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] *= 0.25f;
 }
 
 // NVFP4 operand of the weight gradient: the rows of src [R_cap][C] (an
 // activation or its gradient in the permuted layout) below offsets[E],
 // rotated in 16-row blocks and cast column-wise: q [C][R_cap/2],
 // s [C][R_cap/16] under s_g = 2688 / amax (amax = the rotated amax).  One
-// thread per (4 consecutive 16-row blocks, column); blocks at or past
-// offsets[E] are not written.
+// thread per (4 consecutive 16-row blocks, CPT adjacent columns); blocks at
+// or past offsets[E] are not written.
+template <int CPT>
 __global__ void __launch_bounds__(256) k_nvfp4_rht_cast_cols(const uint16_t* __restrict__ src, int R_cap, int C,
                                                              const int32_t* __restrict__ offsets, int E,
                                                              const float* __restrict__ amax, uint32_t signs,
@@ -379,57 +467,242 @@ __global__ void __launch_bounds__(256) k_nvfp4_rht_cast_cols(const uint16_t* __r
   const float sg = nvfp4_global_scale(*amax);
   if (blockIdx.x == 0 && threadIdx.x == 0) *s_global = sg;
   const int R = min(__ldg(offsets + E), R_cap);
-  const int nb = (R + 15) / 16, ng = (nb + 3) / 4;
-  const size_t total = (size_t)ng * C;
+  const int nb = (R + 15) / 16, ng = (nb + 3) / 4, ncp = C / CPT;
+  const size_t total = (size_t)ng * ncp;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
-    const int c = (int)(i % C);
-    const int rg = (int)(i / C);
-    uint32_t w[8];
-    uint32_t sc4 = 0;
+    const int c = (int)(i % ncp) * CPT;
+    const int rg = (int)(i / ncp);
+    uint32_t w[CPT][8];
+    uint32_t sc4[CPT];
     const int nblk = min(4, nb - rg * 4);
 #pragma unroll
+    for (int cc = 0; cc < CPT; ++cc) sc4[cc] = 0;
+#pragma unroll
     for (int b = 0; b < 4; ++b) {
-      w[2 * b] = w[2 * b + 1] = 0;
       if (b < nblk) {
-        float v[16];
-        load_col16(src, C, rg * 4 + b, c, v);
-        rht16(v, signs);
-        sc4 |= nvfp4_block16(v, sg, w + 2 * b) << (8 * b);
+        float v[CPT][16];
+        load_cols16<CPT>(src, C, (size_t)(rg * 4 + b) * 16, c, v);
+#pragma unroll
+        for (int cc = 0; cc < CPT; ++cc) {
+          rht16(v[cc], signs);
+          sc4[cc] |= nvfp4_block16(v[cc], sg, w[cc] + 2 * b) << (8 * b);
+        }
+      } else {
+#pragma unroll
+        for (int cc = 0; cc < CPT; ++cc) w[cc][2 * b] = w[cc][2 * b + 1] = 0;
       }
     }
-    uint8_t* qd = q + (size_t)c * (R_cap / 2) + (size_t)rg * 32;
-    uint8_t* sd = s + (size_t)c * (R_cap / 16) + (size_t)rg * 4;
-    if (nblk == 4) {
-      reinterpret_cast<uint4*>(qd)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      reinterpret_cast<uint4*>(qd)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-      *reinterpret_cast<uint32_t*>(sd) = sc4;
-    } else {
-      for (int b = 0; b < nblk; ++b) {
-        *reinterpret_cast<uint2*>(qd + 8 * b) = make_uint2(w[2 * b], w[2 * b + 1]);
-        sd[b] = (uint8_t)(sc4 >> (8 * b));
-      }
-    }
+#pragma unroll
+    for (int cc = 0; cc < CPT; ++cc)
+      store_col_blocks<4>(q + (size_t)(c + cc) * (R_cap / 2) + (size_t)rg * 32,
+                          s + (size_t)(c + cc) * (R_cap / 16) + (size_t)rg * 4, w[cc], sc4[cc], nblk);
   }
 }
 
 // max |rotated value| over the 16-row blocks below offsets[E] of every column
-// (the per-tensor amax of k_nvfp4_rht_cast_cols' input), as ordered float bits.
+// (the per-tensor amax of k_nvfp4_rht_cast_cols' input), as ordered float
+// bits.  One thread per (16-row block, CPT adjacent columns).
+template <int CPT>
 __global__ void __launch_bounds__(256) k_rht_amax_cols(const uint16_t* __restrict__ src, int R_cap, int C,
                                                        const int32_t* __restrict__ offsets, int E, uint32_t signs,
                                                        float* __restrict__ amax) {
   const int R = min(__ldg(offsets + E), R_cap);
-  const int nb = (R + 15) / 16;
-  const size_t total = (size_t)nb * C;
+  const int nb = (R + 15) / 16, ncp = C / CPT;
+  const size_t total = (size_t)nb * ncp;
   uint32_t m = 0;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
-    float v[16];
-    load_col16(src, C, (int)(i / C), (int)(i % C), v);
-    rht16(v, signs);
+    float v[CPT][16];
+    load_cols16<CPT>(src, C, (size_t)(i / ncp) * 16, (int)(i % ncp) * CPT, v);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) m = max(m, __float_as_uint(v[j]) & 0x7FFFFFFFu);
+    for (int cc = 0; cc < CPT; ++cc) {
+      rht16(v[cc], signs);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) m = max(m, __float_as_uint(v[cc][j]) & 0x7FFFFFFFu);
+    }
   }
   m = __reduce_max_sync(0xFFFFFFFFu, m);
   if ((threadIdx.x & 31) == 0 && m != 0) atomicMax(reinterpret_cast<int*>(amax), (int)m);
+}
+
+// Column-wise NVFP4 through shared memory: the weight casts (NC_CAST) and
+// the rotated operands of the weight gradient (NC_RHT_CAST, and their
+// rotated amax, NC_RHT_AMAX).  A CTA streams tiles of 128 rows (eight 16-row
+// blocks) x NC_COLS columns of src [G][R][C] through a ring of NC_STAGES
+// buffers filled by TMA (thread 0 issues; one mbarrier per buffer); two
+// independent (block, pair) items per thread give the ALU-heavy rotation and
+// cast the instruction-level parallelism that hides their latencies:
+//   1. thread (column pair p, block b) reads its two columns in the 16 rows
+//      of a block as one 32-bit word per row (consecutive lanes read
+//      consecutive words: no bank conflicts), rotates both columns (rotated
+//      modes, both at once with packed two-lane fp32 adds) and casts them
+//      into a [NC_COLS][64]-byte code tile and a [NC_COLS][8] scale tile,
+//      or folds them into its amax (NC_RHT_AMAX);
+//   2. the buffer is refilled with the tile NC_STAGES steps ahead;
+//   3. each column's 64 code bytes leave as 4 x 16 bytes (8 columns per warp
+//      instruction) and its 8 scales as one 8-byte word.
+// Only the blocks below rows_valid (R, or offsets[E] for the permuted
+// operands: a multiple of 32) are read into a result or stored; columns
+// past C arrive as zeros from TMA and are not stored.  R % 128 == 0.
+enum { NC_CAST = 0, NC_RHT_CAST = 1, NC_RHT_AMAX = 2 };
+constexpr int NC_ROWS = 128, NC_COLS = 128, NC_STAGES = 3, NC_THREADS = 256, NC_CTAS_PER_SM = 2;
+constexpr int NC_PAIRS = NC_COLS / 2;                          // column pairs of a tile row
+constexpr int NC_ITEMS = (NC_ROWS / 16) * NC_PAIRS / NC_THREADS;  // (block, pair) items per thread
+constexpr int NC_WARPS = NC_THREADS / 32;
+constexpr int NC_TILE = NC_ROWS * NC_COLS * 2;   // bytes of one staged bf16 tile
+constexpr int NC_CODE_ROW = NC_ROWS / 2 + 16;    // padded bytes per staged code column
+constexpr int NC_OFF_CODE = NC_STAGES * NC_TILE;
+constexpr int NC_OFF_SCALE = NC_OFF_CODE + NC_COLS * NC_CODE_ROW;
+constexpr int NC_OFF_BARS = NC_OFF_SCALE + NC_COLS * 8;
+constexpr int NC_OFF_MISC = NC_OFF_BARS + NC_STAGES * 8;  // abort flag
+constexpr int NC_OFF_TAB = NC_OFF_MISC + 16;               // float [128]: nvfp4_inv_table
+constexpr int NC_SMEM = NC_OFF_TAB + 128 * 4;
+
+template <int MODE>
+__global__ void __launch_bounds__(NC_THREADS, NC_CTAS_PER_SM) k_nvfp4_cols_tma(const __grid_constant__ CUtensorMap tm, int G, int R, int C,
+                                                        const int32_t* __restrict__ offsets, int E,
+                                                        const float* __restrict__ amax, uint32_t signs,
+                                                        uint8_t* __restrict__ q, uint8_t* __restrict__ s,
+                                                        float* __restrict__ s_global, float* __restrict__ amax_out,
+                                                        int32_t* status, uint64_t wait_ns) {
+  extern __shared__ __align__(128) uint8_t nsm[];
+  uint8_t* tin = nsm;
+  uint8_t* tcode = nsm + NC_OFF_CODE;
+  uint8_t* tscale = nsm + NC_OFF_SCALE;
+  uint64_t* full = reinterpret_cast<uint64_t*>(nsm + NC_OFF_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(nsm + NC_OFF_MISC);
+  float* inv_tab = reinterpret_cast<float*>(nsm + NC_OFF_TAB);
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  constexpr float pre = MODE == NC_CAST ? 1.0f : 0.25f;
+  float sg = 1.0f;
+  if constexpr (MODE != NC_RHT_AMAX) {
+    sg = nvfp4_global_scale(*amax);
+    if (blockIdx.x == 0 && t == 0) *s_global = sg;
+    nvfp4_inv_table(inv_tab, sg, pre);
+  }
+  if (t == 0) {
+    for (int st = 0; st < NC_STAGES; ++st) mbar_init(full + st, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tm);
+  }
+  __syncthreads();
+  const int rows_valid = offsets ? max(0, min(__ldg(offsets + E), R)) : R;
+  const int col_tiles = (C + NC_COLS - 1) / NC_COLS;
+  const int row_tiles = (rows_valid + NC_ROWS - 1) / NC_ROWS;
+  const int total = G * row_tiles * col_tiles;
+  auto coords = [&](int i, int& g, int& r0, int& c0) {
+    c0 = (i % col_tiles) * NC_COLS;
+    const int rest = i / col_tiles;
+    r0 = (rest % row_tiles) * NC_ROWS;
+    g = rest / row_tiles;
+  };
+  auto issue = [&](int i, int st) {
+    int g, r0, c0;
+    coords(i, g, r0, c0);
+    mbar_arrive_expect_tx(full + st, NC_TILE);
+    tma_load_3d(tin + st * NC_TILE, &tm, full + st, c0, r0, g);
+  };
+  if (t == 0) {
+#pragma unroll
+    for (int st = 0; st < NC_STAGES; ++st) {
+      const int i = blockIdx.x + st * gridDim.x;
+      if (i < total) issue(i, st);
+    }
+  }
+  WaitGuard guard{abort_flag, status, wait_ns};
+  const int p = t % NC_PAIRS, bq = t / NC_PAIRS;  // column pair; blocks bq + (NC_THREADS / NC_PAIRS) h
+  // rotated modes: the sign of row j of a block flips both bf16 of the
+  // packed word (s_j = -1 -> XOR 0x80008000); the butterfly then runs
+  // without its 1/4, which is folded into the cast or the amax (exact)
+  uint32_t smask[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) smask[j] = (MODE != NC_CAST && ((signs >> j) & 1u)) ? 0x80008000u : 0u;
+  uint32_t m_abs = 0;
+  int k = 0;
+  for (int i = blockIdx.x; i < total; i += gridDim.x, ++k) {
+    const int st = k % NC_STAGES;
+    const uint32_t ph = (uint32_t)(k / NC_STAGES) & 1u;
+    int g, r0, c0;
+    coords(i, g, r0, c0);
+    const int nvalid = min(8, (rows_valid - r0 + 15) / 16);
+    const bool ok = mbar_wait(full + st, ph, guard);
+    if (__syncthreads_or(ok ? 0 : 1)) break;
+#pragma unroll
+    for (int h = 0; h < NC_ITEMS; ++h) {
+      const int b = bq + (NC_THREADS / NC_PAIRS) * h;
+      if (b < nvalid) {
+        const uint8_t* src = tin + st * NC_TILE + (16 * b) * (NC_COLS * 2) + p * 4;
+        float2 v2[16];  // row j of the block: (column 2p, column 2p + 1)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(src + j * NC_COLS * 2) ^ smask[j];
+          v2[j] = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+        }
+        if constexpr (MODE != NC_CAST) hadamard16_unscaled_x2(v2);
+        float v[2][16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          v[0][j] = v2[j].x;
+          v[1][j] = v2[j].y;
+        }
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          if constexpr (MODE == NC_RHT_AMAX) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) m_abs = max(m_abs, __float_as_uint(v[cc][j]) & 0x7FFFFFFFu);
+          } else {
+            uint32_t w2[2];
+            const uint32_t sc = nvfp4_block16(v[cc], sg, w2, pre, inv_tab);
+            const int cl = 2 * p + cc;
+            *reinterpret_cast<uint2*>(tcode + cl * NC_CODE_ROW + 8 * b) = make_uint2(w2[0], w2[1]);
+            tscale[cl * 8 + b] = (uint8_t)sc;
+          }
+        }
+      }
+    }
+    __syncthreads();
+    // 2. the buffer is free again: fetch the tile NC_STAGES steps ahead
+    if (t == 0) {
+      const int nxt = i + NC_STAGES * gridDim.x;
+      if (nxt < total) issue(nxt, st);
+    }
+    // 3. store: lane group of 4 -> one column's 64 code bytes; 8 columns per warp pass
+    if constexpr (MODE != NC_RHT_AMAX) {
+      const int sub = lane >> 2, part = lane & 3;
+#pragma unroll
+      for (int h2 = 0; h2 < NC_COLS / (8 * NC_WARPS); ++h2) {
+        const int cl = warp * (NC_COLS / NC_WARPS) + h2 * 8 + sub;
+        const int c = c0 + cl;
+        if (c < C) {
+          const size_t col = (size_t)g * C + c;
+          if (2 * part < nvalid)
+            *reinterpret_cast<uint4*>(q + col * (R / 2) + r0 / 2 + part * 16) =
+                *reinterpret_cast<const uint4*>(tcode + cl * NC_CODE_ROW + part * 16);
+          if (part == 0) {
+            uint8_t* sd = s + col * (R / 16) + r0 / 16;
+            if (nvalid == 8)
+              *reinterpret_cast<uint2*>(sd) = *reinterpret_cast<const uint2*>(tscale + cl * 8);
+            else
+              for (int b = 0; b < nvalid; ++b) sd[b] = tscale[cl * 8 + b];
+          }
+        }
+      }
+    }
+  }
+  if constexpr (MODE == NC_RHT_AMAX) {
+    m_abs = __reduce_max_sync(0xFFFFFFFFu, m_abs);
+    // the 1/4 of the rotation (exact; a NaN stays NaN, inf stays inf)
+    m_abs = __float_as_uint(__uint_as_float(m_abs) * 0.25f);
+    if (lane == 0 && m_abs != 0) atomicMax(reinterpret_cast<int*>(amax_out), (int)m_abs);
+  }
+  // after a timeout at step k: the loads of steps k .. k + NC_STAGES - 1 were
+  // issued and not consumed; let them land before the CTA exits
+  if (t == 0 && *abort_flag) {
+    volatile int never = 0;
+    WaitGuard drain{&never, status, 100000000ull};
+    for (int j = k; j < k + NC_STAGES; ++j)
+      if (blockIdx.x + j * gridDim.x < total) mbar_wait(full + j % NC_STAGES, (uint32_t)(j / NC_STAGES) & 1u, drain);
+  }
 }
 
 // max |x| over a bf16 tensor of n8 16-byte words (x 16-byte aligned) into
@@ -663,42 +936,95 @@ extern "C" moe_status_t moe_amax_bf16(const moe_bf16* x, size_t n, float* amax, 
   return launch_status();
 }
 
+template <int MODE>
+static moe_status_t launch_nvfp4_cols_tma(const moe_bf16* src, int G, int R, int C, const int32_t* offsets, int E,
+                                          const float* amax, uint32_t signs, uint8_t* q, uint8_t* s, float* s_global,
+                                          float* amax_out, int32_t* status, cudaStream_t st) {
+  const size_t tiles = (size_t)G * ((R + NC_ROWS - 1) / NC_ROWS) * ((C + NC_COLS - 1) / NC_COLS);
+  if (tiles > (size_t)INT32_MAX) return MOE_ERR_ARG;
+  CUtensorMap tm;
+  const uint64_t dims[3] = {(uint64_t)C, (uint64_t)R, (uint64_t)G};
+  const uint64_t strides[2] = {(uint64_t)C * 2, (uint64_t)R * C * 2};
+  const uint32_t box[3] = {NC_COLS, NC_ROWS, 1};
+  if (!encode_tmap(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, src, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return MOE_ERR_CUDA;
+  const void* fn = (const void*)k_nvfp4_cols_tma<MODE>;
+  if (!set_smem_limit(fn, NC_SMEM)) return MOE_ERR_CUDA;
+  const int occ = max(1, max_active_blocks(fn, NC_THREADS, NC_SMEM));
+  size_t grid = tiles;
+  if (grid > (size_t)sm_count() * occ) grid = (size_t)sm_count() * occ;
+  k_nvfp4_cols_tma<MODE><<<(int)(grid < 1 ? 1 : grid), NC_THREADS, NC_SMEM, st>>>(
+      tm, G, R, C, offsets, E, amax, signs, q, s, s_global, amax_out, status, g_wait_limit_ns.load());
+  count_launch();
+  return launch_status();
+}
+
+// The staged (TMA) form needs 16-byte rows and 128-row tiles; other shapes
+// take the direct kernels (two adjacent columns per thread when C is even).
+static bool nvfp4_cols_staged(const void* src, int R, int C) { return aligned16(src) && (C % 8) == 0 && (R % 128) == 0; }
+
 extern "C" moe_status_t moe_nvfp4_cast_cols(const moe_bf16* src, int G, int R, int C, const float* amax, uint8_t* q,
-                                            uint8_t* s, float* s_global, moe_stream_t stream) {
+                                            uint8_t* s, float* s_global, int32_t* status, moe_stream_t stream) {
   if (!src || !amax || !q || !s || !s_global || G <= 0 || R <= 0 || (R % 16) || C <= 0) return MOE_ERR_ARG;
   if ((reinterpret_cast<uintptr_t>(q) & 7)) return MOE_ERR_ARG;
+  cudaStream_t st = as_stream(stream);
+  if (nvfp4_cols_staged(src, R, C) && aligned16(q) && (reinterpret_cast<uintptr_t>(s) & 7) == 0)
+    return launch_nvfp4_cols_tma<NC_CAST>(src, G, R, C, nullptr, 0, amax, 0u, q, s, s_global, nullptr, status, st);
   // four blocks per thread (32-byte code stores, 4-byte scale stores) when
   // the rows come in 64s and the outputs are aligned for it
-  const bool wide = (R % 64) == 0 && (reinterpret_cast<uintptr_t>(q) & 15) == 0 && (reinterpret_cast<uintptr_t>(s) & 3) == 0;
-  if (wide)
-    k_nvfp4_cast_cols<4><<<grid_for((size_t)G * (R / 64) * C, 256), 256, 0, as_stream(stream)>>>(
-        reinterpret_cast<const uint16_t*>(src), G, R, C, amax, q, s, s_global);
+  const bool wide = (R % 64) == 0 && aligned16(q) && (reinterpret_cast<uintptr_t>(s) & 3) == 0;
+  // two adjacent columns per thread (32-bit row loads) when C is even
+  const bool pair = (C % 2) == 0 && (reinterpret_cast<uintptr_t>(src) & 3) == 0;
+  const uint16_t* src16 = reinterpret_cast<const uint16_t*>(src);
+  const size_t units = (size_t)G * (R / (wide ? 64 : 16)) * (C / (pair ? 2 : 1));
+  if (wide && pair)
+    k_nvfp4_cast_cols<4, 2><<<grid_for(units, 256), 256, 0, st>>>(src16, G, R, C, amax, q, s, s_global);
+  else if (wide)
+    k_nvfp4_cast_cols<4, 1><<<grid_for(units, 256), 256, 0, st>>>(src16, G, R, C, amax, q, s, s_global);
+  else if (pair)
+    k_nvfp4_cast_cols<1, 2><<<grid_for(units, 256), 256, 0, st>>>(src16, G, R, C, amax, q, s, s_global);
   else
-    k_nvfp4_cast_cols<1><<<grid_for((size_t)G * (R / 16) * C, 256), 256, 0, as_stream(stream)>>>(
-        reinterpret_cast<const uint16_t*>(src), G, R, C, amax, q, s, s_global);
+    k_nvfp4_cast_cols<1, 1><<<grid_for(units, 256), 256, 0, st>>>(src16, G, R, C, amax, q, s, s_global);
   count_launch();
   return launch_status();
 }
 
 extern "C" moe_status_t moe_rht_amax_cols(const moe_bf16* src, int R_cap, int C, const int32_t* offsets, int E,
-                                          uint32_t signs, float* amax, moe_stream_t stream) {
+                                          uint32_t signs, float* amax, int32_t* status, moe_stream_t stream) {
   if (!src || !offsets || !amax || R_cap <= 0 || (R_cap % 128) || C <= 0 || E <= 0) return MOE_ERR_ARG;
   cudaStream_t st = as_stream(stream);
   if (cudaMemsetAsync(amax, 0, sizeof(float), st) != cudaSuccess) return MOE_ERR_CUDA;
-  k_rht_amax_cols<<<grid_for((size_t)(R_cap / 16) * C, 256), 256, 0, st>>>(
-      reinterpret_cast<const uint16_t*>(src), R_cap, C, offsets, E, signs & 0xFFFFu, amax);
+  if (nvfp4_cols_staged(src, R_cap, C))
+    return launch_nvfp4_cols_tma<NC_RHT_AMAX>(src, 1, R_cap, C, offsets, E, nullptr, signs & 0xFFFFu, nullptr,
+                                              nullptr, nullptr, amax, status, st);
+  const uint16_t* src16 = reinterpret_cast<const uint16_t*>(src);
+  if ((C % 2) == 0 && (reinterpret_cast<uintptr_t>(src) & 3) == 0)
+    k_rht_amax_cols<2><<<grid_for((size_t)(R_cap / 16) * (C / 2), 256), 256, 0, st>>>(src16, R_cap, C, offsets, E,
+                                                                                      signs & 0xFFFFu, amax);
+  else
+    k_rht_amax_cols<1><<<grid_for((size_t)(R_cap / 16) * C, 256), 256, 0, st>>>(src16, R_cap, C, offsets, E,
+                                                                                signs & 0xFFFFu, amax);
   count_launch();
   return launch_status();
 }
 
 extern "C" moe_status_t moe_nvfp4_rht_cast_cols(const moe_bf16* src, int R_cap, int C, const int32_t* offsets, int E,
                                                 const float* amax, uint32_t signs, uint8_t* q, uint8_t* s,
-                                                float* s_global, moe_stream_t stream) {
+                                                float* s_global, int32_t* status, moe_stream_t stream) {
   if (!src || !offsets || !amax || !q || !s || !s_global || R_cap <= 0 || (R_cap % 128) || C <= 0 || E <= 0)
     return MOE_ERR_ARG;
   if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(s) & 3)) return MOE_ERR_ARG;
-  k_nvfp4_rht_cast_cols<<<grid_for((size_t)(R_cap / 64) * C, 256), 256, 0, as_stream(stream)>>>(
-      reinterpret_cast<const uint16_t*>(src), R_cap, C, offsets, E, amax, signs & 0xFFFFu, q, s, s_global);
+  cudaStream_t st = as_stream(stream);
+  if (nvfp4_cols_staged(src, R_cap, C) && (reinterpret_cast<uintptr_t>(s) & 7) == 0)
+    return launch_nvfp4_cols_tma<NC_RHT_CAST>(src, 1, R_cap, C, offsets, E, amax, signs & 0xFFFFu, q, s, s_global,
+                                              nullptr, status, st);
+  const uint16_t* src16 = reinterpret_cast<const uint16_t*>(src);
+  if ((C % 2) == 0 && (reinterpret_cast<uintptr_t>(src) & 3) == 0)
+    k_nvfp4_rht_cast_cols<2><<<grid_for((size_t)(R_cap / 64) * (C / 2), 256), 256, 0, st>>>(
+        src16, R_cap, C, offsets, E, amax, signs & 0xFFFFu, q, s, s_global);
+  else
+    k_nvfp4_rht_cast_cols<1><<<grid_for((size_t)(R_cap / 64) * C, 256), 256, 0, st>>>(
+        src16, R_cap, C, offsets, E, amax, signs & 0xFFFFu, q, s, s_global);
   count_launch();
   return launch_status();
 }

@@ -215,7 +215,7 @@ class MoeLayer:
                 _p(self.a_s4), _p(self.a_sg), s)),
             ("amax_w2", lambda: lib.moe_amax_bf16(_p(self.W2), self.W2.numel(), _p(self.w2_amax), s)),
             ("quant_w2_nvfp4", lambda: lib.moe_nvfp4_cast_cols(
-                _p(self.W2), E, F, H, _p(self.w2_amax), _p(self.W2q4), _p(self.W2s4), _p(self.w2_sg), s)),
+                _p(self.W2), E, F, H, _p(self.w2_amax), _p(self.W2q4), _p(self.W2s4), _p(self.w2_sg), st, s)),
             ("fc2_nvfp4", lambda: lib.moe_grouped_fc2_fwd(
                 C.byref(self.fc2_a4), C.byref(self.fc2_w4), _p(self.counts), _p(self.offsets), E, F, H, R,
                 L.OUT_BF16, C.byref(self.fc2_out), _p(self.ws_fc2), self.ws_fc2.numel(), self.sm_margin, st, s)),
@@ -264,9 +264,9 @@ class MoeLayer:
             calls = []
             if amax_call:
                 calls.append((f"rht_amax_{name}", lambda: lib.moe_rht_amax_cols(_p(src), R, C_, off, E, sig, _p(ramax),
-                                                                                 s)))
+                                                                                 st, s)))
             calls.append((f"quant_{name}_rht", lambda: lib.moe_nvfp4_rht_cast_cols(_p(src), R, C_, off, E, _p(ramax),
-                                                                                    sig, _p(q), _p(sc), _p(sg), s)))
+                                                                                    sig, _p(q), _p(sc), _p(sg), st, s)))
             return calls
 
         return [
@@ -281,7 +281,7 @@ class MoeLayer:
                 _p(self.d_y), _p(self.d_amax), cnt, off, E, N1, R, _p(self.d_q4), _p(self.d_s4), _p(self.d_sg), s)),
             ("amax_w1", lambda: lib.moe_amax_bf16(_p(self.W1p), self.W1p.numel(), _p(self.w1_amax), s)),
             ("quant_w1_nvfp4", lambda: lib.moe_nvfp4_cast_cols(
-                _p(self.W1p), E, N1, H, _p(self.w1_amax), _p(self.W1q4), _p(self.W1s4), _p(self.w1_sg), s)),
+                _p(self.W1p), E, N1, H, _p(self.w1_amax), _p(self.W1q4), _p(self.W1s4), _p(self.w1_sg), st, s)),
             ("dx_nvfp4", lambda: lib.moe_grouped_fc2_fwd(
                 C.byref(self.dx_a4), C.byref(self.dx_w4), cnt, off, E, N1, H, R, L.OUT_BF16, C.byref(self.dx_out),
                 _p(self.ws_dx), self.ws_dx.numel(), self.sm_margin, st, s)),

@@ -81,10 +81,10 @@ _SIGS = {
     "moe_nvfp4_cast": [P, P, P, P, I, I, I, P, P, P, P],
     "moe_glu_act": [P, P, P, I, I, I, C.POINTER(GluParams), P, P],
     "moe_amax_bf16": [P, SZ, P, P],
-    "moe_rht_amax_cols": [P, I, I, P, I, C.c_uint32, P, P],
-    "moe_nvfp4_rht_cast_cols": [P, I, I, P, I, P, C.c_uint32, P, P, P, P],
+    "moe_rht_amax_cols": [P, I, I, P, I, C.c_uint32, P, P, P],
+    "moe_nvfp4_rht_cast_cols": [P, I, I, P, I, P, C.c_uint32, P, P, P, P, P],
     "moe_grouped_wgrad_nvfp4": [P, P, P, P, P, P, P, P, I, I, I, I, P, I, P, SZ, I, P, P],
-    "moe_nvfp4_cast_cols": [P, I, I, I, P, P, P, P, P],
+    "moe_nvfp4_cast_cols": [P, I, I, I, P, P, P, P, P, P],
     "moe_dglu_act": [P, P, P, P, I, I, I, C.POINTER(GluParams), P, P],
     "moe_route_permute_noalloc": [P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P, P],
     "moe_route_noalloc_max_scratch_bytes": ([], SZ),

@@ -295,7 +295,7 @@ def amax_bf16(x):
     return a
 
 
-def nvfp4_cast_cols(src, amax):
+def nvfp4_cast_cols(src, amax, status=None):
     """Column-wise NVFP4 of src [G, R, C] (or [R, C]) bf16: (q [G, C, R/2],
     s [G, C, R/16], s_global [1])."""
     lib = L.load()
@@ -305,7 +305,8 @@ def nvfp4_cast_cols(src, amax):
     q = torch.empty(G, Cc, R // 2, dtype=torch.uint8, device=dev)
     s = torch.empty(G, Cc, R // 16, dtype=torch.uint8, device=dev)
     sg = torch.empty(1, dtype=torch.float32, device=dev)
-    L.check(lib.moe_nvfp4_cast_cols(_p(s3), G, R, Cc, _p(amax), _p(q), _p(s), _p(sg), _s()), "moe_nvfp4_cast_cols")
+    L.check(lib.moe_nvfp4_cast_cols(_p(s3), G, R, Cc, _p(amax), _p(q), _p(s), _p(sg), _p(status), _s()),
+            "moe_nvfp4_cast_cols")
     return q, s, sg
 
 
@@ -329,18 +330,18 @@ def wgrad(Aq_col, As_col, Bq_col, Bs_col, counts, offsets, out_f32: bool = False
     return D
 
 
-def rht_amax_cols(src, offsets, signs: int):
+def rht_amax_cols(src, offsets, signs: int, status=None):
     """max |rotated value| of src [R_cap, C] (16-row Hadamard blocks below
     offsets[E]) as a device float [1]."""
     lib = L.load()
     R_cap, Cc = src.shape
     a = torch.empty(1, dtype=torch.float32, device=_dev(src))
     L.check(lib.moe_rht_amax_cols(_p(src), R_cap, Cc, _p(offsets), offsets.shape[0] - 1, int(signs) & 0xFFFF, _p(a),
-                                  _s()), "moe_rht_amax_cols")
+                                  _p(status), _s()), "moe_rht_amax_cols")
     return a
 
 
-def nvfp4_rht_cast_cols(src, offsets, amax, signs: int):
+def nvfp4_rht_cast_cols(src, offsets, amax, signs: int, status=None):
     """Rotated column-wise NVFP4 of src [R_cap, C]: (q [C, R_cap/2],
     s [C, R_cap/16], s_global [1])."""
     lib = L.load()
@@ -350,7 +351,8 @@ def nvfp4_rht_cast_cols(src, offsets, amax, signs: int):
     s = torch.empty(Cc, R_cap // 16, dtype=torch.uint8, device=dev)
     sg = torch.empty(1, dtype=torch.float32, device=dev)
     L.check(lib.moe_nvfp4_rht_cast_cols(_p(src), R_cap, Cc, _p(offsets), offsets.shape[0] - 1, _p(amax),
-                                        int(signs) & 0xFFFF, _p(q), _p(s), _p(sg), _s()), "moe_nvfp4_rht_cast_cols")
+                                        int(signs) & 0xFFFF, _p(q), _p(s), _p(sg), _p(status), _s()),
+            "moe_nvfp4_rht_cast_cols")
     return q, s, sg
 
 

@@ -418,9 +418,14 @@ MOE_API moe_status_t moe_amax_bf16(const moe_bf16* x, size_t n, float* amax, moe
  * (element 2i in the low nibble), s [G][C][R/16] E4M3, with the same
  * two-level rule as moe_nvfp4_cast under s_g = 2688 / amax (1 if 0 or not
  * finite), written to *s_global.  amax: device float (moe_amax_bf16).
- * R % 16 == 0, q 8-byte aligned. */
+ * R % 16 == 0, q 8-byte aligned.  With src 16-byte aligned, C % 8 == 0,
+ * R % 128 == 0, q 16- and s 8-byte aligned the cast streams 128 x 128 tiles
+ * through shared memory by TMA; its pipeline waits are bounded and a wait
+ * that gives up ORs MOE_ERR_TIMEOUT into *status (device int32, may be
+ * NULL).  Other shapes take a direct kernel without waits. */
 MOE_API moe_status_t moe_nvfp4_cast_cols(const moe_bf16* src, int G, int R, int C, const float* amax,
-                                         uint8_t* q, uint8_t* s, float* s_global, moe_stream_t stream);
+                                         uint8_t* q, uint8_t* s, float* s_global, int32_t* status,
+                                         moe_stream_t stream);
 
 /* NVFP4 backward operands ([MoE-Fusion] "Fusing MXFP8 and NVFP4
  * quantisation": the weight-gradient GEMM reads the transposed tensors after
@@ -436,12 +441,16 @@ MOE_API moe_status_t moe_nvfp4_cast_cols(const moe_bf16* src, int G, int R, int 
  *       blocks at or past offsets[E] are not written.
  * The rotation is orthonormal, so rotating both operands of the weight
  * gradient along its contracted rows leaves the product unchanged.
- * R_cap % 128 == 0; q 16-byte and s 4-byte aligned. */
+ * R_cap % 128 == 0; q 16-byte and s 4-byte aligned.  With src 16-byte
+ * aligned, C % 8 == 0 (and s 8-byte aligned for the cast) both stream
+ * 128 x 128 tiles through shared memory by TMA, with bounded waits that OR
+ * MOE_ERR_TIMEOUT into *status (device int32, may be NULL) when they give
+ * up; other shapes take direct kernels. */
 MOE_API moe_status_t moe_rht_amax_cols(const moe_bf16* src, int R_cap, int C, const int32_t* offsets, int E,
-                                       uint32_t signs, float* amax, moe_stream_t stream);
+                                       uint32_t signs, float* amax, int32_t* status, moe_stream_t stream);
 MOE_API moe_status_t moe_nvfp4_rht_cast_cols(const moe_bf16* src, int R_cap, int C, const int32_t* offsets, int E,
                                              const float* amax, uint32_t signs, uint8_t* q, uint8_t* s,
-                                             float* s_global, moe_stream_t stream);
+                                             float* s_global, int32_t* status, moe_stream_t stream);
 
 /* Standalone activation of the unfused path: pre [R][N1] bf16 -> y [R][F]
  * bf16 (rows >= offsets[E] untouched, pad rows 0).  F % 32 == 0; pre and y

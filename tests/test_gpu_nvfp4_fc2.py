@@ -54,17 +54,22 @@ def test_nvfp4_fc2_edge_counts(K, N):
     assert_bf16_close(np_(y)[: rt.R_pad], O.bf16_round(ref), f"nvfp4 fc2 K={K} N={N}")
 
 
-@pytest.mark.parametrize("R", [64, 48, 1536])
-def test_nvfp4_weight_cast_and_amax_bit_exact(R):
+@pytest.mark.parametrize("R,C", [(64, 96), (48, 96), (1536, 96), (64, 45), (48, 45)])
+def test_nvfp4_weight_cast_and_amax_bit_exact(R, C):
     """The column-wise NVFP4 cast of a bf16 weight [E, F, H] and its per-tensor
     amax against the oracle on the same bf16 values: codes, scales and s_g
-    bit-exact (R a multiple of 64: four blocks per thread; R = 48: one)."""
+    bit-exact.  R = 1536, C = 96: 128 x 128 tiles staged through shared
+    memory (a partial column tile); otherwise the direct kernels: R a
+    multiple of 64 four blocks per thread, R = 48 one; C even two columns
+    per thread, C odd one."""
     rng = np.random.default_rng(4)
-    W = synth._bf16(rng.standard_normal((3, R, 96), dtype=np.float32) * np.exp2(rng.integers(-4, 4, (3, 1, 96))))
+    W = synth._bf16(rng.standard_normal((3, R, C), dtype=np.float32) * np.exp2(rng.integers(-4, 4, (3, 1, C))))
     Wd = W.to(DEV)
     am = ops.amax_bf16(Wd)
-    q, s, sg = ops.nvfp4_cast_cols(Wd, am)
+    st = ops.new_status(DEV)
+    q, s, sg = ops.nvfp4_cast_cols(Wd, am, status=st)
     torch.cuda.synchronize()
+    assert ops.read_status(st) == 0
     Wn = np_(W)
     assert float(am.item()) == float(np.max(np.abs(Wn)))
     sg_ref = O.nvfp4_global_scale(float(np.max(np.abs(Wn))))

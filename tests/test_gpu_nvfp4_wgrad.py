@@ -67,18 +67,24 @@ def test_nvfp4_wgrad_edge_counts(M, N):
     assert np.all(np_(D)[[0, 6]] == 0)
 
 
-def test_rotated_cast_and_amax():
+@pytest.mark.parametrize("C", [200, 46, 45])
+def test_rotated_cast_and_amax(C):
     """The rotated amax to fp32 rounding, and the rotated NVFP4 codes / scales:
     equal to the oracle's on >= 99.9% (a rotated value the two sides round
     differently in its last bit may cross an E2M1 or E4M3 boundary) and the
-    dequantised values within one E2M1 step everywhere."""
+    dequantised values within two E2M1 steps everywhere.  C = 200: tiles
+    staged through shared memory (a partial column tile, and a partial row
+    tile at offsets[E]); C = 46: the direct kernels on column pairs; C = 45:
+    one column per thread."""
     counts = [5, 40, 0, 300, 64]
     rt, R_cap, cnt, off = _routing(counts, 5)
-    v, q_ref, s_ref, sg_ref = _rot_operand(rt, R_cap, 200, 6)
+    v, q_ref, s_ref, sg_ref = _rot_operand(rt, R_cap, C, 6)
     vd = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16).to(DEV)
-    am = ops.rht_amax_cols(vd, off, SIGNS)
-    q, s, sg = ops.nvfp4_rht_cast_cols(vd, off, am, SIGNS)
+    st = ops.new_status(DEV)
+    am = ops.rht_amax_cols(vd, off, SIGNS, status=st)
+    q, s, sg = ops.nvfp4_rht_cast_cols(vd, off, am, SIGNS, status=st)
     torch.cuda.synchronize()
+    assert ops.read_status(st) == 0
     R = rt.R_pad
     assert math.isclose(float(am.item()), O.rht_transposed_amax(v[:R], SIGNS), rel_tol=1e-6)
     assert math.isclose(float(sg.item()), float(sg_ref), rel_tol=1e-6)
