@@ -81,6 +81,9 @@ def kernel_model(name, w, R, Rp):
         "dx": (2 * R * N1 * H, E * H * N1 * (1 + 1 / 32) + R * N1 * (1 + 1 / 32) + R * H * 2, "fp8"),
         "quant_x_col": (0, R * H * 2 + R * H * (1 + 1 / 32), None),
         "quant_dy_col": (0, R * H * 2 + R * H * (1 + 1 / 32), None),
+        # the gather / combine backward that also write the column-wise MXFP8 copy
+        "route_permute_qcol": (0, T * k * 8 + 2 * R * H * 2 + (Rp - R) * H * 2 + Rp * H * (1 + 1 / 32), None),
+        "combine_bwd_qcol": (0, T * H * 2 + R * H * 2 + Rp * H * 2 + T * k * 8 + Rp * H * (1 + 1 / 32), None),
         "wgrad_w1": (2 * R * N1 * H, (N1 + H) * R * (1 + 1 / 32) + E * N1 * H * 2, "fp8"),
         "wgrad_w2": (2 * R * F * H, (F + H) * R * (1 + 1 / 32) + E * F * H * 2, "fp8"),
         "permute_bwd": (0, R * H * 2 + T * H * 2 + T * k * 4, None),

@@ -21,6 +21,9 @@
 //                   for k = 4, 8
 //   k_combine_warp  the same sum for the other k <= 32, one warp per token
 //   k_combine_bwd   one warp per permuted row: dY_perm and dprob
+//   k_permute_gather_qcol / k_combine_bwd_qcol  the gather / the combine
+//                   backward by 32-row blocks, each block's rows also cast
+//                   column-wise to MXFP8 (the weight-gradient operands)
 #include <mutex>
 
 #include "common.cuh"
@@ -238,6 +241,212 @@ __global__ void __launch_bounds__(256) k_permute_gather(const uint4* __restrict_
       }
     }
   }
+}
+
+// Column-wise MXFP8 of the permuted rows, fused into the kernels that write
+// them (the weight gradient's operands x_perm and dY_perm; [MoE-Fusion]
+// "Fusing MXFP8 and NVFP4 quantisation": MXFP8 = row-wise output plus a
+// transposed copy).  A CTA of QF_THREADS owns one 32-row block (one MX block
+// along the rows, inside one expert's padded segment) and walks the columns
+// in chunks: warp w produces row w of the chunk (stored as by the plain
+// kernel, and staged in shared memory), then two threads per column
+// quantise the column's 32 values: codes to q_col [C][R_cap] (32 bytes at
+// row r0), the E8M0 scale to s_col [C][R_cap / 32].  The next chunk's loads
+// are in flight while a chunk is quantised.
+constexpr int QF_THREADS = 1024;  // 32 warps: one per row of the block
+// chunk widths: the gather 1024 columns (4 gathered 16-byte loads per lane
+// and chunk), the combine backward 512 (two input streams)
+template <int COLS>
+struct Qf {
+  static constexpr int V = COLS / 8 / 32;    // 16-byte vectors per lane and row of a chunk
+  static constexpr int ROW = COLS * 2 + 16;  // staged bytes per row (padded)
+  static constexpr int SMEM = 32 * ROW;
+};
+
+// Thread pair (c, h) of each group of 512 columns: rows 16h .. 16h + 15 of
+// column c of the staged chunk; the pair's two 16-byte code stores fill one
+// 32-byte sector, so a warp instruction writes 16 whole sectors.
+template <int COLS>
+__device__ __forceinline__ void qf_cast_chunk(const uint8_t* tile, int ncols, int c0, int R_cap, int r0,
+                                              uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col) {
+  using Q = Qf<COLS>;
+  const int h = threadIdx.x & 1;
+#pragma unroll 1
+  for (int cg = 0; cg < COLS; cg += QF_THREADS / 2) {
+    const int c = cg + (threadIdx.x >> 1);
+    uint32_t v[8];  // rows 16h + 2i (low half) and 16h + 2i + 1 (high half)
+    uint32_t m = 0;
+    if (c < ncols) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t lo = *reinterpret_cast<const uint16_t*>(tile + (16 * h + 2 * i) * Q::ROW + 2 * c);
+        const uint32_t hi = *reinterpret_cast<const uint16_t*>(tile + (16 * h + 2 * i + 1) * Q::ROW + 2 * c);
+        v[i] = lo | (hi << 16);
+        m = max(m, max(lo & 0x7FFFu, hi & 0x7FFFu));
+      }
+    }
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));  // amax of the column's 32 rows
+    if (c < ncols) {
+      const uint32_t sb = e8m0_from_amax_bits(m << 16);
+      uint32_t codes[4];
+      if (sb == 0xFFu) {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) codes[w] = 0x7F7F7F7Fu;
+      } else {
+        const float inv = mx_inv_scale(sb);
+#pragma unroll
+        for (int w = 0; w < 4; ++w)
+          codes[w] = e4m3x2(bf16_lo(v[2 * w]) * inv, bf16_hi(v[2 * w]) * inv) |
+                     (e4m3x2(bf16_lo(v[2 * w + 1]) * inv, bf16_hi(v[2 * w + 1]) * inv) << 16);
+      }
+      *reinterpret_cast<uint4*>(q_col + (size_t)(c0 + c) * R_cap + r0 + 16 * h) =
+          make_uint4(codes[0], codes[1], codes[2], codes[3]);
+      if (h == 0) s_col[(size_t)(c0 + c) * (R_cap / 32) + r0 / 32] = (uint8_t)sb;
+    }
+  }
+}
+
+// Real rows (0..32) of the 32-row block at r0 < offsets[E]: found by one
+// binary search over the offsets (each block lies inside one expert).
+__device__ __forceinline__ int block_real_rows_g(const int32_t* __restrict__ counts,
+                                                 const int32_t* __restrict__ offsets, int E, int r0) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(offsets + mid) <= r0) lo = mid; else hi = mid - 1;
+  }
+  return max(0, min(32, __ldg(offsets + lo) + __ldg(counts + lo) - r0));
+}
+
+// k_permute_gather with the column-wise MXFP8 of x_perm: one CTA per 32-row
+// block below offsets[E] (the same rows, zero fill, tok_of / prob_perm of
+// pad rows as k_permute_gather).
+__global__ void __launch_bounds__(QF_THREADS) k_permute_gather_qcol(
+    const uint4* __restrict__ x, int H, int E, const int32_t* __restrict__ counts,
+    const int32_t* __restrict__ offsets, const int32_t* __restrict__ overflow, int R_cap,
+    int32_t* __restrict__ tok_of, float* __restrict__ prob_perm, uint4* __restrict__ x_perm,
+    uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col) {
+  using Q = Qf<1024>;
+  extern __shared__ __align__(16) uint8_t qf_tile[];  // [32][Q::ROW]
+  __shared__ int s_real;
+  if (*overflow) return;
+  const int r0 = blockIdx.x * 32;
+  if (r0 >= __ldg(offsets + E)) return;
+  if (threadIdx.x == 0) s_real = block_real_rows_g(counts, offsets, E, r0);
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = r0 + warp;
+  const bool real = warp < s_real;
+  const int H8 = H / 8;
+  const uint4* src = x + (real ? (size_t)__ldg(tok_of + r) * H8 : 0);
+  uint4* dst = x_perm + (size_t)r * H8;
+  if (!real && lane == 0) {
+    tok_of[r] = -1;
+    prob_perm[r] = 0.0f;
+  }
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  uint4 a[Q::V];
+#pragma unroll
+  for (int u = 0; u < Q::V; ++u) {
+    const int v = lane + 32 * u;
+    a[u] = (real && v < H8) ? __ldg(src + v) : z;
+  }
+  for (int c0 = 0; c0 < H; c0 += 1024) {
+    const int ncols = min(1024, H - c0);
+#pragma unroll
+    for (int u = 0; u < Q::V; ++u) {
+      const int v = lane + 32 * u;
+      if (8 * v < ncols) {
+        dst[c0 / 8 + v] = a[u];
+        *reinterpret_cast<uint4*>(qf_tile + warp * Q::ROW + 16 * v) = a[u];
+      }
+    }
+    __syncthreads();
+    const int n0 = c0 + 1024;  // next chunk's loads, in flight during the cast
+#pragma unroll
+    for (int u = 0; u < Q::V; ++u) {
+      const int v = n0 / 8 + lane + 32 * u;
+      a[u] = (real && v < H8) ? __ldg(src + v) : z;
+    }
+    qf_cast_chunk<1024>(qf_tile, ncols, c0, R_cap, r0, q_col, s_col);
+    __syncthreads();
+  }
+}
+
+// k_combine_bwd with the column-wise MXFP8 of dY_perm: one CTA per 32-row
+// block below offsets[E], warp w on row r0 + w.  The same dY_perm rows, and
+// the same dprob: each lane takes the 16-byte chunks lane, lane + 32, ... of
+// the row in order (as k_combine_bwd), then the warp's butterfly.
+__global__ void __launch_bounds__(QF_THREADS) k_combine_bwd_qcol(
+    const uint4* __restrict__ dout, const uint4* __restrict__ y_perm, const int32_t* __restrict__ row_of,
+    const int32_t* __restrict__ tok_of, const float* __restrict__ prob_perm, const int32_t* __restrict__ offsets,
+    int E, int T, int k, int H, int R_cap, uint4* __restrict__ dY, float* __restrict__ dprob,
+    uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col, int32_t* status) {
+  using Q = Qf<512>;
+  extern __shared__ __align__(16) uint8_t qf_tile[];  // [32][Q::ROW]
+  const size_t nthreads = (size_t)gridDim.x * blockDim.x;
+  const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (size_t i = tid; i < (size_t)T * k; i += nthreads)
+    if (__ldg(row_of + i) < 0) dprob[i] = 0.0f;
+  const int R = __ldg(offsets + E);
+  if (R > R_cap) {
+    if (tid == 0) set_status(status, MOE_ERR_CAPACITY);
+    return;
+  }
+  const int r0 = blockIdx.x * 32;
+  if (r0 >= R) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = r0 + warp;
+  const int t = __ldg(tok_of + r);
+  const bool real = t >= 0;
+  const float p = real ? __ldg(prob_perm + r) : 0.0f;
+  const int H8 = H / 8;
+  const uint4* g = dout + (real ? (size_t)t * H8 : 0);
+  const uint4* y = y_perm + (size_t)r * H8;
+  uint4* dst = dY + (size_t)r * H8;
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  uint4 ga[Q::V], yb[Q::V];
+#pragma unroll
+  for (int u = 0; u < Q::V; ++u) {
+    const int v = lane + 32 * u;
+    ga[u] = (real && v < H8) ? __ldg(g + v) : z;
+    yb[u] = (real && v < H8) ? __ldg(y + v) : z;
+  }
+  float dot = 0.0f;
+  for (int c0 = 0; c0 < H; c0 += 512) {
+    const int ncols = min(512, H - c0);
+#pragma unroll
+    for (int u = 0; u < Q::V; ++u) {
+      const int v = lane + 32 * u;
+      if (8 * v < ncols) {
+        const uint4 a = ga[u], b = yb[u];
+        const float gv[8] = {bf16_lo(a.x), bf16_hi(a.x), bf16_lo(a.y), bf16_hi(a.y),
+                             bf16_lo(a.z), bf16_hi(a.z), bf16_lo(a.w), bf16_hi(a.w)};
+        const float yv[8] = {bf16_lo(b.x), bf16_hi(b.x), bf16_lo(b.y), bf16_hi(b.y),
+                             bf16_lo(b.z), bf16_hi(b.z), bf16_lo(b.w), bf16_hi(b.w)};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dot = fmaf(gv[i], yv[i], dot);
+        const uint4 o = real ? make_uint4(pack_bf16x2(p * gv[0], p * gv[1]), pack_bf16x2(p * gv[2], p * gv[3]),
+                                          pack_bf16x2(p * gv[4], p * gv[5]), pack_bf16x2(p * gv[6], p * gv[7]))
+                             : z;
+        dst[c0 / 8 + v] = o;
+        *reinterpret_cast<uint4*>(qf_tile + warp * Q::ROW + 16 * v) = o;
+      }
+    }
+    __syncthreads();
+    const int n0 = c0 + 512;
+#pragma unroll
+    for (int u = 0; u < Q::V; ++u) {
+      const int v = n0 / 8 + lane + 32 * u;
+      ga[u] = (real && v < H8) ? __ldg(g + v) : z;
+      yb[u] = (real && v < H8) ? __ldg(y + v) : z;
+    }
+    qf_cast_chunk<512>(qf_tile, ncols, c0, R_cap, r0, q_col, s_col);
+    __syncthreads();
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, d);
+  if (real && lane < k && __ldg(row_of + (size_t)t * k + lane) == (int32_t)r) dprob[(size_t)t * k + lane] = dot;
 }
 
 // out[t] = bf16(sum_j p[t][j] * y_perm[row_of[t*k+j]]) in fp32, j ascending.
@@ -484,10 +693,11 @@ extern "C" size_t moe_route_workspace_size(int T, int k, int E) {
 extern "C" moe_status_t moe_route_permute(const moe_bf16* x, const int32_t* topk_idx, const float* topk_prob, int T,
                                           int H, int k, int expert_begin, int E, int R_cap, moe_bf16* x_perm,
                                           int32_t* row_of, int32_t* tok_of, float* prob_perm, int32_t* counts,
-                                          int32_t* offsets, void* ws, size_t ws_bytes, int32_t* status,
-                                          moe_stream_t stream) {
+                                          int32_t* offsets, uint8_t* xq_col, uint8_t* xs_col, void* ws,
+                                          size_t ws_bytes, int32_t* status, moe_stream_t stream) {
   if (!x || !topk_idx || !topk_prob || !x_perm || !row_of || !tok_of || !prob_perm || !counts || !offsets || !ws)
     return MOE_ERR_ARG;
+  if ((xq_col == nullptr) != (xs_col == nullptr) || (xq_col && !aligned16(xq_col))) return MOE_ERR_ARG;
   if (T <= 0 || H <= 0 || (H & 7) || k <= 0 || k > 64 || E <= 0 || E > ROUTE_E_MAX || R_cap <= 0 || (R_cap & 31))
     return MOE_ERR_ARG;
   if ((int64_t)T * k > (int64_t)INT32_MAX / 2) return MOE_ERR_ARG;
@@ -505,13 +715,20 @@ extern "C" moe_status_t moe_route_permute(const moe_bf16* x, const int32_t* topk
   k_route_scatter<<<n_chunks, ROUTE_THREADS, scatter_smem, s>>>(topk_idx, topk_prob, n_assign, k, expert_begin, E,
                                                                  chunk_counts, offsets, overflow, row_of, tok_of,
                                                                  prob_perm);
-  const int sms = sm_count();
-  const int rows_bound = R_cap;
-  int grid = (rows_bound + 7) / 8;
-  if (grid > sms * 8) grid = sms * 8;
-  if (grid < 1) grid = 1;
-  k_permute_gather<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), H / 8, E, counts, offsets, overflow,
-                                        tok_of, prob_perm, reinterpret_cast<uint4*>(x_perm));
+  if (xq_col) {
+    if (!set_smem_limit((const void*)k_permute_gather_qcol, Qf<1024>::SMEM)) return MOE_ERR_CUDA;
+    k_permute_gather_qcol<<<R_cap / 32, QF_THREADS, Qf<1024>::SMEM, s>>>(
+        reinterpret_cast<const uint4*>(x), H, E, counts, offsets, overflow, R_cap, tok_of, prob_perm,
+        reinterpret_cast<uint4*>(x_perm), xq_col, xs_col);
+  } else {
+    const int sms = sm_count();
+    const int rows_bound = R_cap;
+    int grid = (rows_bound + 7) / 8;
+    if (grid > sms * 8) grid = sms * 8;
+    if (grid < 1) grid = 1;
+    k_permute_gather<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), H / 8, E, counts, offsets, overflow,
+                                          tok_of, prob_perm, reinterpret_cast<uint4*>(x_perm));
+  }
   count_launch(4);
   return launch_status();
 }
@@ -559,10 +776,19 @@ extern "C" moe_status_t moe_unpermute_combine(const moe_bf16* y_perm, const int3
 extern "C" moe_status_t moe_combine_bwd(const moe_bf16* dout, const moe_bf16* y_perm, const int32_t* row_of,
                                         const int32_t* tok_of, const float* prob_perm, const int32_t* offsets,
                                         int T, int H, int k, int E, int R_cap, moe_bf16* dY_perm, float* dprob,
-                                        int32_t* status, moe_stream_t stream) {
+                                        uint8_t* dyq_col, uint8_t* dys_col, int32_t* status, moe_stream_t stream) {
   if (!dout || !y_perm || !row_of || !tok_of || !prob_perm || !offsets || !dY_perm || !dprob) return MOE_ERR_ARG;
   if (T <= 0 || H <= 0 || (H & 7) || k <= 0 || k > 32 || E <= 0 || E > ROUTE_E_MAX || R_cap <= 0) return MOE_ERR_ARG;
   if (!aligned16(dout) || !aligned16(y_perm) || !aligned16(dY_perm)) return MOE_ERR_ARG;
+  if ((dyq_col == nullptr) != (dys_col == nullptr)) return MOE_ERR_ARG;
+  if (dyq_col) {
+    if ((R_cap & 31) || !aligned16(dyq_col)) return MOE_ERR_ARG;
+    k_combine_bwd_qcol<<<R_cap / 32, QF_THREADS, Qf<512>::SMEM, as_stream(stream)>>>(
+        reinterpret_cast<const uint4*>(dout), reinterpret_cast<const uint4*>(y_perm), row_of, tok_of, prob_perm,
+        offsets, E, T, k, H, R_cap, reinterpret_cast<uint4*>(dY_perm), dprob, dyq_col, dys_col, status);
+    count_launch();
+    return launch_status();
+  }
   int grid = sm_count() * 8;
   if (grid < 1) grid = 1;
   k_combine_bwd<<<grid, 256, 0, as_stream(stream)>>>(reinterpret_cast<const uint4*>(dout),
@@ -642,7 +868,8 @@ extern "C" moe_status_t moe_route_permute_noalloc(const moe_bf16* x, const int32
                                                   int T, int H, int k, int expert_begin, int E, int R_cap,
                                                   moe_bf16* x_perm, int32_t* row_of, int32_t* tok_of,
                                                   float* prob_perm, int32_t* counts, int32_t* offsets,
-                                                  int32_t* status, moe_stream_t stream) {
+                                                  uint8_t* xq_col, uint8_t* xs_col, int32_t* status,
+                                                  moe_stream_t stream) {
   using namespace moeglu;
   if (!x || !topk_idx || !topk_prob || !x_perm || !row_of || !tok_of || !prob_perm || !counts || !offsets)
     return MOE_ERR_ARG;
@@ -658,7 +885,7 @@ extern "C" moe_status_t moe_route_permute_noalloc(const moe_bf16* x, const int32
   // array (every entry of it that a kernel reads is written first by an
   // earlier kernel of the same call, so nothing needs clearing)
   return moe_route_permute(x, topk_idx, topk_prob, T, H, k, expert_begin, E, R_cap, x_perm, row_of, tok_of, prob_perm,
-                           counts, offsets, scratch, ROUTE_STATIC_SCRATCH_BYTES, status, stream);
+                           counts, offsets, xq_col, xs_col, scratch, ROUTE_STATIC_SCRATCH_BYTES, status, stream);
 }
 
 namespace moeglu {

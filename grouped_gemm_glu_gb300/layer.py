@@ -30,7 +30,7 @@ from .ops import _p, _s
 class MoeLayer:
     def __init__(self, W1, W2, T: int, k: int, R_cap: int, params: L.GluParams, b1=None,
                  expert_begin: int = 0, sm_margin: int = 0, gated: bool = True, dynamic: bool = True,
-                 nvfp4: bool = False, rht_signs: int = 0x6A5D):
+                 nvfp4: bool = False, rht_signs: int = 0x6A5D, fused_col_casts: bool = True):
         """dynamic: the bf16 grouped GEMMs take their tiles from the dynamic
         scheduler (each call site has its own counter workspace); False runs
         the static schedule.  nvfp4: the step runs the NVFP4 recipe.  Forward:
@@ -40,7 +40,10 @@ class MoeLayer:
         with the 16 signs rht_signs) -> NVFP4 dFC1 and W1 (along 2F) -> NVFP4
         dX; the weight gradients on the rotated column-wise NVFP4 casts of
         dFC1, x, the FC1 output and dY (the same signs on both operands of a
-        product, so the rotation cancels)."""
+        product, so the rotation cancels).  fused_col_casts (MXFP8 recipe):
+        the column-wise MXFP8 copies of x_perm and dY_perm that the weight
+        gradients read are made by the gather and by the combine backward
+        themselves; False runs them as separate quantize calls."""
         self.lib = L.load()
         dev = W1.device
         self.dev = dev
@@ -115,6 +118,7 @@ class MoeLayer:
         if self.ws_db_bytes:
             self.ws_db = z(self.ws_db_bytes, dt=u8)
         self.nvfp4 = nvfp4
+        self.fused_cols = fused_col_casts and not nvfp4
         if nvfp4:
             f32 = torch.float32
             self.a_y, self.a_amax = z(R_cap, F), z(1, dt=f32)
@@ -161,10 +165,11 @@ class MoeLayer:
         st = _p(self.status)
         if self.nvfp4:
             return self._forward_calls_nvfp4(x, topk_idx, topk_prob)
+        xq, xs = (_p(self.x_qc), _p(self.x_sc)) if self.fused_cols else (None, None)
         return [
-            ("route_permute", lambda: lib.moe_route_permute(
+            ("route_permute_qcol" if self.fused_cols else "route_permute", lambda: lib.moe_route_permute(
                 _p(x), _p(topk_idx), _p(topk_prob), T, H, k, self.expert_begin, E, R, _p(self.x_perm),
-                _p(self.row_of), _p(self.tok_of), _p(self.prob_perm), _p(self.counts), _p(self.offsets),
+                _p(self.row_of), _p(self.tok_of), _p(self.prob_perm), _p(self.counts), _p(self.offsets), xq, xs,
                 _p(self.ws), self.ws_bytes, st, s)),
             ("fc1_glu_quant", self.fc1_mxfp8_call()),
             ("quant_w2", lambda: lib.moe_quantize_mxfp8(
@@ -204,8 +209,8 @@ class MoeLayer:
         return [
             ("route_permute", lambda: lib.moe_route_permute(
                 _p(x), _p(topk_idx), _p(topk_prob), T, H, k, self.expert_begin, E, R, _p(self.x_perm),
-                _p(self.row_of), _p(self.tok_of), _p(self.prob_perm), _p(self.counts), _p(self.offsets),
-                _p(self.ws), self.ws_bytes, st, s)),
+                _p(self.row_of), _p(self.tok_of), _p(self.prob_perm), _p(self.counts), _p(self.offsets), None,
+                None, _p(self.ws), self.ws_bytes, st, s)),
             ("fc1_glu_nvfp4", lambda: lib.moe_grouped_fc1_glu_quant_fwd(
                 _p(self.x_perm), _p(self.W1p), _p(self.b1p), None, _p(self.counts), _p(self.offsets), E, H, F, R,
                 C.byref(self.params), L.OUT_NVFP4, C.byref(self.fc1_out4), _p(self.ws_fc1), self.ws_fc1_bytes,
@@ -230,20 +235,24 @@ class MoeLayer:
         dY_perm = self.dY_perm
         if self.nvfp4:
             return self._backward_calls_nvfp4(dOut)
+        dq, ds = (_p(self.dy_qc), _p(self.dy_sc)) if self.fused_cols else (None, None)
+        col_casts = [] if self.fused_cols else [
+            ("quant_x_col", lambda: lib.moe_quantize_mxfp8(
+                _p(self.x_perm), 1, R, H, 1, _p(self.counts), _p(self.offsets), E, _p(self.x_qc), _p(self.x_sc), st, s)),
+            ("quant_dy_col", lambda: lib.moe_quantize_mxfp8(
+                _p(dY_perm), 1, R, H, 1, _p(self.counts), _p(self.offsets), E, _p(self.dy_qc), _p(self.dy_sc), st, s)),
+        ]
         return [
-            ("combine_bwd", lambda: lib.moe_combine_bwd(
+            ("combine_bwd_qcol" if self.fused_cols else "combine_bwd", lambda: lib.moe_combine_bwd(
                 _p(dOut), _p(self.y_perm), _p(self.row_of), _p(self.tok_of), _p(self.prob_perm), _p(self.offsets),
-                T, H, k, E, R, _p(dY_perm), _p(self.dprob), st, s)),
+                T, H, k, E, R, _p(dY_perm), _p(self.dprob), dq, ds, st, s)),
             ("dglu_quant", self.dglu_mxfp8_call()),
             ("quant_w1", lambda: lib.moe_quantize_mxfp8(
                 _p(self.W1p), E, N1, H, 1, None, None, 0, _p(self.W1q), _p(self.W1s), st, s)),
             ("dx", lambda: lib.moe_grouped_fc2_fwd(
                 C.byref(self.dx_a), C.byref(self.dx_w), _p(self.counts), _p(self.offsets), E, N1, H, R,
                 L.OUT_BF16, C.byref(self.dx_out), _p(self.ws_dx), self.ws_dx.numel(), self.sm_margin, st, s)),
-            ("quant_x_col", lambda: lib.moe_quantize_mxfp8(
-                _p(self.x_perm), 1, R, H, 1, _p(self.counts), _p(self.offsets), E, _p(self.x_qc), _p(self.x_sc), st, s)),
-            ("quant_dy_col", lambda: lib.moe_quantize_mxfp8(
-                _p(dY_perm), 1, R, H, 1, _p(self.counts), _p(self.offsets), E, _p(self.dy_qc), _p(self.dy_sc), st, s)),
+            *col_casts,
             ("wgrad_w1", lambda: lib.moe_grouped_wgrad(
                 _p(self.d_qc), _p(self.d_sc), _p(self.x_qc), _p(self.x_sc), _p(self.counts), _p(self.offsets), E,
                 N1, H, R, _p(self.dW1), 0, _p(self.ws_wg1), self.ws_wg1.numel(), self.sm_margin, st, s)),
@@ -272,7 +281,7 @@ class MoeLayer:
         return [
             ("combine_bwd", lambda: lib.moe_combine_bwd(
                 _p(dOut), _p(self.y_perm), _p(self.row_of), _p(self.tok_of), _p(self.prob_perm), off,
-                T, H, k, E, R, _p(self.dY_perm), _p(self.dprob), st, s)),
+                T, H, k, E, R, _p(self.dY_perm), _p(self.dprob), None, None, st, s)),
             ("dglu_nvfp4", lambda: lib.moe_grouped_dglu_quant_bwd(
                 _p(self.dY_perm), _p(self.W2), _p(self.pre), None, cnt, off, E, H, F, R, C.byref(self.params),
                 L.OUT_NVFP4, C.byref(self.bwd_out4), _p(self.db1), _p(self.ws_db), self.ws_db_bytes,

@@ -59,7 +59,7 @@ P, I, U64, SZ, F32 = C.c_void_p, C.c_int, C.c_uint64, C.c_size_t, C.c_float
 _SIGS = {
     "moe_repack_fc1": [P, P, I, I, I, I, P],
     "moe_route_workspace_size": ([I, I, I], SZ),
-    "moe_route_permute": [P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P, SZ, P, P],
+    "moe_route_permute": [P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, SZ, P, P],
     "moe_grouped_fc1_glu_quant_fwd": [P, P, P, P, P, P, I, I, I, I, C.POINTER(GluParams), I, C.POINTER(ActOut), P,
                                       SZ, I, P, P],
     "moe_grouped_fc1_workspace_size": ([I, I, I], SZ),
@@ -74,7 +74,7 @@ _SIGS = {
     "moe_grouped_wgrad_workspace_size": ([I, I, I, I], SZ),
     "moe_grouped_wgrad": [P, P, P, P, P, P, I, I, I, I, P, I, P, SZ, I, P, P],
     "moe_unpermute_combine": [P, P, P, I, I, I, P, P, P],
-    "moe_combine_bwd": [P, P, P, P, P, P, I, I, I, I, I, P, P, P, P],
+    "moe_combine_bwd": [P, P, P, P, P, P, I, I, I, I, I, P, P, P, P, P, P],
     "moe_permute_bwd": [P, P, I, I, I, P, P, P],
     "moe_dglu_row_dot_parts": ([I], I),
     "moe_feature_scale_grad": [P, I, P, I, I, P, P],
@@ -86,7 +86,7 @@ _SIGS = {
     "moe_grouped_wgrad_nvfp4": [P, P, P, P, P, P, P, P, I, I, I, I, P, I, P, SZ, I, P, P],
     "moe_nvfp4_cast_cols": [P, I, I, I, P, P, P, P, P, P],
     "moe_dglu_act": [P, P, P, P, I, I, I, C.POINTER(GluParams), P, P],
-    "moe_route_permute_noalloc": [P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P, P],
+    "moe_route_permute_noalloc": [P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P],
     "moe_route_noalloc_max_scratch_bytes": ([], SZ),
     "moe_get_status": [P, P, P],
     "moe_set_wait_limit_ns": ([U64], None),

@@ -52,7 +52,10 @@ def repack_fc1(W1: torch.Tensor, inverse: bool = False) -> torch.Tensor:
     return out
 
 
-def route_permute(x, topk_idx, topk_prob, E: int, R_cap: int, expert_begin: int = 0, status=None) -> dict:
+def route_permute(x, topk_idx, topk_prob, E: int, R_cap: int, expert_begin: int = 0, status=None,
+                  with_col: bool = False) -> dict:
+    """Routing + gather; with_col also returns the column-wise MXFP8 copy of
+    x_perm made during the gather (x_qc [H, R_cap], x_sc [H, R_cap/32])."""
     lib = L.load()
     dev = _dev(x)
     T, H = x.shape
@@ -65,12 +68,16 @@ def route_permute(x, topk_idx, topk_prob, E: int, R_cap: int, expert_begin: int 
         "counts": torch.empty(E, dtype=torch.int32, device=dev),
         "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
     }
+    if with_col:
+        o["x_qc"] = torch.zeros(H, R_cap, dtype=torch.uint8, device=dev)
+        o["x_sc"] = torch.zeros(H, R_cap // 32, dtype=torch.uint8, device=dev)
     ws_bytes = lib.moe_route_workspace_size(T, k, E)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     st = status if status is not None else new_status(dev)
     L.check(lib.moe_route_permute(_p(x), _p(topk_idx), _p(topk_prob), T, H, k, expert_begin, E, R_cap,
                                   _p(o["x_perm"]), _p(o["row_of"]), _p(o["tok_of"]), _p(o["prob_perm"]),
-                                  _p(o["counts"]), _p(o["offsets"]), _p(ws), ws_bytes, _p(st), _s()),
+                                  _p(o["counts"]), _p(o["offsets"]), _p(o.get("x_qc")), _p(o.get("x_sc")), _p(ws),
+                                  ws_bytes, _p(st), _s()),
             "moe_route_permute")
     o["status"] = st
     return o
@@ -386,9 +393,10 @@ def unpermute_combine(y_perm, row_of, topk_prob, status=None, out=None):
     return o
 
 
-def combine_bwd(dout, y_perm, route: dict, k: int, status=None, out=None):
+def combine_bwd(dout, y_perm, route: dict, k: int, status=None, out=None, col=None):
     """Gradient of the combine for dout [T, H]: (dY_perm [R_cap, H] bf16,
-    dprob [T, k] f32); route = the dict of route_permute."""
+    dprob [T, k] f32); route = the dict of route_permute.  col = (q [H, R_cap],
+    s [H, R_cap/32]) uint8 tensors: also the column-wise MXFP8 of dY_perm."""
     lib = L.load()
     dev = _dev(dout)
     T, H = dout.shape
@@ -399,7 +407,8 @@ def combine_bwd(dout, y_perm, route: dict, k: int, status=None, out=None):
     st = status if status is not None else route.get("status")
     L.check(lib.moe_combine_bwd(_p(dout), _p(y_perm), _p(route["row_of"]), _p(route["tok_of"]),
                                 _p(route["prob_perm"]), _p(route["offsets"]), T, H, k, E, R_cap, _p(dY),
-                                _p(dprob), _p(st), _s()), "moe_combine_bwd")
+                                _p(dprob), _p(col[0] if col else None), _p(col[1] if col else None), _p(st),
+                                _s()), "moe_combine_bwd")
     return dY, dprob
 
 

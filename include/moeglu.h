@@ -167,11 +167,18 @@ MOE_API size_t moe_route_workspace_size(int T, int k, int E);
  *      expert in ascending t*k+j), tok_of [R_cap] (token of each row, -1
  *      on pad rows), prob_perm [R_cap] (0 on pad rows), x_perm [R_cap][H]
  *      (pad rows zero).  ws: moe_route_workspace_size() bytes.
- *      offsets[E] > R_cap sets MOE_ERR_CAPACITY in *status and writes no rows. */
+ *      offsets[E] > R_cap sets MOE_ERR_CAPACITY in *status and writes no rows.
+ * xq_col / xs_col (both or neither; xq_col 16-byte aligned): also the
+ *      column-wise MXFP8 copy of x_perm that the FC1 weight gradient reads
+ *      ([MoE-Fusion] "Fusing MXFP8 and NVFP4 quantisation": MXFP8 = row-wise
+ *      output plus a transposed copy), made while the rows are gathered:
+ *      xq_col [H][R_cap] E4M3 codes, xs_col [H][R_cap/32] E8M0 scales, one
+ *      block per 32 rows (the same values as moe_quantize_mxfp8 with col = 1
+ *      on x_perm and the counts); blocks at or past offsets[E] untouched. */
 MOE_API moe_status_t moe_route_permute(const moe_bf16* x, const int32_t* topk_idx, const float* topk_prob,
                                int T, int H, int k, int expert_begin, int E, int R_cap,
                                moe_bf16* x_perm, int32_t* row_of, int32_t* tok_of, float* prob_perm,
-                               int32_t* counts, int32_t* offsets,
+                               int32_t* counts, int32_t* offsets, uint8_t* xq_col, uint8_t* xs_col,
                                void* ws, size_t ws_bytes, int32_t* status, moe_stream_t stream);
 
 /* GroupGemm + Activation + Quantize/Transpose, forward ([MoE-Fusion]).
@@ -382,11 +389,15 @@ MOE_API moe_status_t moe_feature_scale_grad(const float* row_dot, int parts, con
  * get dprob 0, rows >= offsets[E] are untouched.  row_of / tok_of /
  * prob_perm / offsets as written by moe_route_permute.  H % 8 == 0,
  * 1 <= k <= 32, 16-byte aligned bf16 buffers.  offsets[E] > R_cap records
- * MOE_ERR_CAPACITY in status and writes nothing else. */
+ * MOE_ERR_CAPACITY in status and writes nothing else.
+ * dyq_col / dys_col (both or neither; dyq_col 16-byte aligned, R_cap % 32
+ * == 0): also the column-wise MXFP8 copy of dY_perm that the FC2 weight
+ * gradient reads, made while the rows are written: dyq_col [H][R_cap],
+ * dys_col [H][R_cap/32], as moe_quantize_mxfp8 with col = 1 on dY_perm. */
 MOE_API moe_status_t moe_combine_bwd(const moe_bf16* dout, const moe_bf16* y_perm, const int32_t* row_of,
                              const int32_t* tok_of, const float* prob_perm, const int32_t* offsets,
                              int T, int H, int k, int E, int R_cap, moe_bf16* dY_perm, float* dprob,
-                             int32_t* status, moe_stream_t stream);
+                             uint8_t* dyq_col, uint8_t* dys_col, int32_t* status, moe_stream_t stream);
 
 /* Permute backward: dx[t] = bf16( sum_j dx_perm[row_of[t*k+j]] ) over the
  * slots with row_of >= 0, summed in fp32 in j order (the gradient of the
@@ -484,7 +495,8 @@ MOE_API moe_status_t moe_route_permute_noalloc(const moe_bf16* x, const int32_t*
                                                int T, int H, int k, int expert_begin, int E, int R_cap,
                                                moe_bf16* x_perm, int32_t* row_of, int32_t* tok_of,
                                                float* prob_perm, int32_t* counts, int32_t* offsets,
-                                               int32_t* status, moe_stream_t stream);
+                                               uint8_t* xq_col, uint8_t* xs_col, int32_t* status,
+                                               moe_stream_t stream);
 
 /* Size in bytes of the fixed scratch array used by moe_route_permute_noalloc. */
 MOE_API size_t moe_route_noalloc_max_scratch_bytes(void);

@@ -38,7 +38,7 @@ def test_argument_validation_needs_no_device(lib):
     # a null pointer is rejected on the host before anything is launched
     assert lib.moe_unpermute_combine(None, None, None, 1, 8, 1, None, None, None) == L.MOE_ERR_ARG
     assert lib.moe_combine_bwd(None, None, None, None, None, None, 1, 8, 1, 1, 128, None, None, None,
-                               None) == L.MOE_ERR_ARG
+                               None, None, None) == L.MOE_ERR_ARG
     assert lib.moe_permute_bwd(None, None, 1, 8, 1, None, None, None) == L.MOE_ERR_ARG
     prm = L.glu_params("swiglu")
     out = L.ActOut()

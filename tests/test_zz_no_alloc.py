@@ -39,7 +39,8 @@ def _noalloc(x, idx, prob, E, R_cap, expert_begin=0):
     o = _outputs(T, H, k, E, R_cap)
     rc = lib.moe_route_permute_noalloc(P(x), P(idx), P(prob), T, H, k, expert_begin, E, R_cap, P(o["x_perm"]),
                                        P(o["row_of"]), P(o["tok_of"]), P(o["prob_perm"]), P(o["counts"]),
-                                       P(o["offsets"]), P(o["status"]), C.c_void_p(torch.cuda.current_stream().cuda_stream))
+                                       P(o["offsets"]), None, None, P(o["status"]),
+                                       C.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert rc == L.MOE_OK
     return o
 
@@ -89,5 +90,5 @@ def test_noalloc_rejects_routing_beyond_its_scratch():
     o = _outputs(T, 8, k, E, 128)
     rc = lib.moe_route_permute_noalloc(P(x), P(idx), P(prob), T, 8, k, 0, E, 128, P(o["x_perm"]), P(o["row_of"]),
                                        P(o["tok_of"]), P(o["prob_perm"]), P(o["counts"]), P(o["offsets"]),
-                                       P(o["status"]), None)
+                                       None, None, P(o["status"]), None)
     assert rc == L.MOE_ERR_ARG
