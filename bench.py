@@ -446,14 +446,16 @@ def main():
     ms_e2e = e0.elapsed_time(e1) / args.steps
     # -- ablation: fused kernels vs the unfused path (same GEMM writing bf16,
     #    separate activation and quantize kernels), per direction
-    def timed(calls, n):
+    def timed_on(lay, calls, n):
         torch.cuda.synchronize()
         e0.record()
         for _ in range(n):
-            layer.run(calls)
+            lay.run(calls)
         e1.record()
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / n
+
+    timed = lambda calls, n: timed_on(layer, calls, n)
 
     ufwd, ubwd = layer.forward_unfused_calls(), layer.backward_unfused_calls(layer.dY_perm)
     fused_fc1 = [("fc1_glu_quant", layer.fc1_mxfp8_call())]
@@ -477,38 +479,51 @@ def main():
     #    each timed alone; not part of the step above, whose FC1 is bf16
     import ctypes as C
     from grouped_gemm_glu_gb300.ops import _p, _s
-    u8 = torch.uint8
-    E_, N1_, H_, F_ = w.E, w.N1, w.H, w.F
-    xq = torch.empty(R_cap, H_, dtype=u8, device=dev)
-    xs = torch.empty(R_cap, H_ // 32, dtype=u8, device=dev)
-    w1q = torch.empty(E_, N1_, H_, dtype=u8, device=dev)
-    w1s = torch.empty(E_, N1_, H_ // 32, dtype=u8, device=dev)
-    mx_ws_bytes = lib.moe_grouped_fc2_workspace_size(E_, H_, N1_, R_cap)
-    mx_ws = torch.empty(mx_ws_bytes, dtype=u8, device=dev)
-    mx_out = L.ActOut(layer.a_q.data_ptr(), layer.a_s.data_ptr(), layer.a_qc.data_ptr(), layer.a_sc.data_ptr(),
-                      None, None, layer.pre.data_ptr())
-    st_p, s_p = _p(layer.status), _s()
-    mx_calls = {
-        "quant_x_rows": [("quant_x_rows", lambda: lib.moe_quantize_mxfp8(
-            _p(layer.x_perm), 1, R_cap, H_, 0, _p(layer.counts), _p(layer.offsets), E_, _p(xq), _p(xs), st_p, s_p))],
-        "quant_w1_rows": [("quant_w1_rows", lambda: lib.moe_quantize_mxfp8(
-            _p(layer.W1p), E_, N1_, H_, 0, None, None, 0, _p(w1q), _p(w1s), st_p, s_p))],
-        "fc1_mxfp8": [("fc1_mxfp8", lambda: lib.moe_grouped_fc1_glu_quant_fwd_mxfp8(
-            _p(xq), _p(xs), _p(w1q), _p(w1s), _p(layer.b1p), None, _p(layer.counts), _p(layer.offsets), E_, H_, F_,
-            R_cap, C.byref(params), L.OUT_MXFP8, C.byref(mx_out), _p(mx_ws), mx_ws_bytes, args.sm_margin, st_p,
-            s_p))],
-    }
-    mx_ms = {}
-    for n_, c_ in mx_calls.items():
-        layer.run(c_)
-        mx_ms[n_] = timed(c_, na)
-    fl_mx = 2 * R * H_ * N1_
-    by_mx = (E_ * N1_ * H_ + R * H_) * (1 + 1 / 32) + R * N1_ * 2 + 2 * R * F_ * (1 + 1 / 32)
-    fc1_mx = {"casts": {"x rows ms": round(mx_ms["quant_x_rows"], 4), "W1 rows ms": round(mx_ms["quant_w1_rows"], 4)},
-              "ms": round(mx_ms["fc1_mxfp8"], 4), "TFLOP/s": round(fl_mx / mx_ms["fc1_mxfp8"] / 1e9, 1),
-              "frac_of_fp8_peak": round(fl_mx / mx_ms["fc1_mxfp8"] / 1e9 / (2 * load_peaks()["bf16"]), 4),
-              "frac_of_hbm_roof": round(by_mx / mx_ms["fc1_mxfp8"] / 1e6 / load_peaks()["hbm"], 4),
-              "note": "FC1 on MXFP8 x and W1 (fp8 = 2 x bf16 burst peak); the step's FC1 is the bf16 kernel"}
+    # -- the MXFP8-input FC1 variant: the whole step with it (x_perm cast
+    #    row-wise after the gather, both MXFP8 copies of W1 from one read in
+    #    the forward, no W1 cast in the backward), as one graph, and its three
+    #    forward calls one by one
+    fc1_mx = None
+    if w.out != "nvfp4":
+        layer_mx = MoeLayer(g["W1"], g["W2"], w.T, w.k, R_cap, params, b1=g.get("b1"), expert_begin=w.expert_begin,
+                            sm_margin=args.sm_margin, gated=w.gated, fc1_mxfp8=True)
+        for _ in range(args.warmup):
+            layer_mx.step(X, I, P, DO)
+        graph_mx = layer_mx.capture(X, I, P, DO)
+        for _ in range(args.warmup):
+            graph_mx.replay()
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(args.steps):
+            graph_mx.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms_graph_mx = e0.elapsed_time(e1) / args.steps
+        by_name_mx = dict(layer_mx.step_calls(X, I, P, DO))
+        mx_ms = {}
+        for n_ in ("quant_x_rows", "quant_w1_dual", "fc1_mxfp8"):
+            c_ = [(n_, by_name_mx[n_])]
+            layer_mx.run(c_)
+            mx_ms[n_] = timed_on(layer_mx, c_, na)
+        st_mx = ops.read_status(layer_mx.status)
+        if st_mx:
+            raise SystemExit(f"device status {st_mx} in the MXFP8-FC1 step")
+        E_, N1_, H_, F_ = w.E, w.N1, w.H, w.F
+        fl_mx = 2 * R * H_ * N1_
+        by_mx = (E_ * N1_ * H_ + R * H_) * (1 + 1 / 32) + R * N1_ * 2 + 2 * R * F_ * (1 + 1 / 32)
+        by_dual = E_ * N1_ * H_ * 2 + 2 * E_ * N1_ * H_ * (1 + 1 / 32)
+        peaks_ = load_peaks()
+        fc1_mx = {"step_graph_ms": round(ms_graph_mx, 4),
+                  "step_graph_ms_bf16_fc1": round(ms_graph, 4),
+                  "x rows cast ms": round(mx_ms["quant_x_rows"], 4),
+                  "W1 dual cast ms": round(mx_ms["quant_w1_dual"], 4),
+                  "W1 dual cast frac_of_hbm_peak": round(by_dual / mx_ms["quant_w1_dual"] / 1e6 / peaks_["hbm"], 4),
+                  "fc1 ms": round(mx_ms["fc1_mxfp8"], 4), "fc1 TFLOP/s": round(fl_mx / mx_ms["fc1_mxfp8"] / 1e9, 1),
+                  "fc1 frac_of_fp8_peak": round(fl_mx / mx_ms["fc1_mxfp8"] / 1e9 / (2 * peaks_["bf16"]), 4),
+                  "fc1 frac_of_hbm_roof": round(by_mx / mx_ms["fc1_mxfp8"] / 1e6 / peaks_["hbm"], 4),
+                  "note": "layer with fc1_mxfp8=True: FC1 on MXFP8 x and W1 (fp8 = 2 x bf16 burst peak), W1's two "
+                          "MXFP8 copies in one pass; the headline step keeps the bf16 FC1"}
+        del graph_mx, layer_mx
     clocks = sampler.stop()
     st = ops.read_status(layer.status)
     if st:

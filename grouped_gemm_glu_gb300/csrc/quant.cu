@@ -127,10 +127,18 @@ constexpr int QC_OFF_MISC = QC_OFF_BARS + QC_STAGES * 8;  // real_rows[2][4], ab
 constexpr int QC_OFF_SEG = QC_OFF_MISC + 48;
 constexpr int QC_SMEM_BASE = QC_OFF_SEG;                  // + (2E + 1) ints of expert map
 
+// ROWS: the same pass also writes the row-wise copy (q_row [G][R][C],
+// s_row [G][R][C/32]) from the staged tile: four lanes per 32-element block,
+// 8 elements (one 16-byte shared-memory load) each, two rows per warp
+// instruction (512 contiguous bytes: no bank conflicts), 8-byte code stores
+// that join into whole 128-byte lines.  One read of a weight then feeds both
+// of its MXFP8 copies (along C for one GEMM, along R for another).
+template <bool ROWS>
 __global__ void __launch_bounds__(256) k_quant_cols(const __grid_constant__ CUtensorMap tm, int G, int R, int Cc,
                                                     const int32_t* __restrict__ counts,
                                                     const int32_t* __restrict__ offsets, int E,
                                                     uint8_t* __restrict__ q, uint8_t* __restrict__ s,
+                                                    uint8_t* __restrict__ q_row, uint8_t* __restrict__ s_row,
                                                     int32_t* status, uint64_t wait_ns) {
   extern __shared__ __align__(128) uint8_t qsm[];
   uint8_t* tin = qsm;
@@ -234,6 +242,33 @@ __global__ void __launch_bounds__(256) k_quant_cols(const __grid_constant__ CUte
         dc[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
         dc[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
         tscale[cl * 4 + b] = (uint8_t)sb;
+      }
+    }
+    // 1b. row-wise copy (ROWS): warp w, pass it -> rows 2 (8 it + w) + (lane / 16),
+    //     block (lane / 4) % 4, elements 8 (lane % 4) .. + 8 of it
+    if constexpr (ROWS) {
+      const int rsub = lane >> 4, blk = (lane >> 2) & 3, part = lane & 3;
+#pragma unroll 2
+      for (int it = 0; it < QC_ROWS / 16; ++it) {
+        const int lr = 2 * (8 * it + warp) + rsub;
+        const uint4 x = *reinterpret_cast<const uint4*>(tin + st * QC_TILE + lr * (QC_COLS * 2) + 64 * blk + 16 * part);
+        uint32_t m = __vmaxu2(__vmaxu2(x.x & 0x7FFF7FFFu, x.y & 0x7FFF7FFFu), __vmaxu2(x.z & 0x7FFF7FFFu, x.w & 0x7FFF7FFFu));
+        m = max(m & 0xFFFFu, m >> 16);
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+        const uint32_t sb = e8m0_from_amax_bits(m << 16);
+        uint2 c = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        if (sb != 0xFFu) {
+          const float inv = mx_inv_scale(sb);
+          c.x = e4m3x2(bf16_lo(x.x) * inv, bf16_hi(x.x) * inv) | (e4m3x2(bf16_lo(x.y) * inv, bf16_hi(x.y) * inv) << 16);
+          c.y = e4m3x2(bf16_lo(x.z) * inv, bf16_hi(x.z) * inv) | (e4m3x2(bf16_lo(x.w) * inv, bf16_hi(x.w) * inv) << 16);
+        }
+        const int row = r0 + lr, col = c0 + 32 * blk;
+        if (row < R && col < Cc) {
+          const size_t rr = (size_t)g * R + row;
+          *reinterpret_cast<uint2*>(q_row + rr * Cc + col + 8 * part) = c;
+          if (part == 0) s_row[rr * (Cc / 32) + col / 32] = (uint8_t)sb;
+        }
       }
     }
     __syncthreads();
@@ -903,13 +938,39 @@ extern "C" moe_status_t moe_quantize_mxfp8(const moe_bf16* src, int G, int R, in
       return MOE_ERR_CUDA;
     const int smem = QC_SMEM_BASE + (2 * E + 1) * 4;
     const int smem_max = QC_SMEM_BASE + (2 * QE_MAX + 1) * 4;
-    if (!set_smem_limit((const void*)k_quant_cols, smem_max)) return MOE_ERR_CUDA;
-    const int occ = max(1, max_active_blocks((const void*)k_quant_cols, 256, smem_max));
+    if (!set_smem_limit((const void*)k_quant_cols<false>, smem_max)) return MOE_ERR_CUDA;
+    const int occ = max(1, max_active_blocks((const void*)k_quant_cols<false>, 256, smem_max));
     size_t grid = tiles;
     if (grid > (size_t)sms * occ) grid = (size_t)sms * occ;
-    k_quant_cols<<<(int)(grid < 1 ? 1 : grid), 256, smem, st>>>(tm, G, R, Cc, counts, offsets, E, q, s, status,
-                                                               g_wait_limit_ns.load());
+    k_quant_cols<false><<<(int)(grid < 1 ? 1 : grid), 256, smem, st>>>(tm, G, R, Cc, counts, offsets, E, q, s,
+                                                                      nullptr, nullptr, status,
+                                                                      g_wait_limit_ns.load());
   }
+  count_launch();
+  return launch_status();
+}
+
+extern "C" moe_status_t moe_quantize_mxfp8_dual(const moe_bf16* src, int G, int R, int Cc, uint8_t* q_row,
+                                                uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, int32_t* status,
+                                                moe_stream_t stream) {
+  if (!src || !q_row || !s_row || !q_col || !s_col || G <= 0 || R <= 0 || Cc <= 0) return MOE_ERR_ARG;
+  if ((R % 32) || (Cc % 32) || !aligned16(src) || !aligned16(q_col) || (reinterpret_cast<uintptr_t>(q_row) & 7))
+    return MOE_ERR_ARG;
+  const size_t tiles = (size_t)G * ((R + QC_ROWS - 1) / QC_ROWS) * ((Cc + QC_COLS - 1) / QC_COLS);
+  if (tiles > (size_t)INT32_MAX) return MOE_ERR_ARG;
+  CUtensorMap tm;
+  const uint64_t dims[3] = {(uint64_t)Cc, (uint64_t)R, (uint64_t)G};
+  const uint64_t strides[2] = {(uint64_t)Cc * 2, (uint64_t)R * Cc * 2};
+  const uint32_t box[3] = {QC_COLS, QC_ROWS, 1};
+  if (!encode_tmap(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, src, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return MOE_ERR_CUDA;
+  const int smem = QC_SMEM_BASE + 4;
+  if (!set_smem_limit((const void*)k_quant_cols<true>, smem)) return MOE_ERR_CUDA;
+  const int occ = max(1, max_active_blocks((const void*)k_quant_cols<true>, 256, smem));
+  size_t grid = tiles;
+  if (grid > (size_t)sm_count() * occ) grid = (size_t)sm_count() * occ;
+  k_quant_cols<true><<<(int)(grid < 1 ? 1 : grid), 256, smem, as_stream(stream)>>>(
+      tm, G, R, Cc, nullptr, nullptr, 0, q_col, s_col, q_row, s_row, status, g_wait_limit_ns.load());
   count_launch();
   return launch_status();
 }

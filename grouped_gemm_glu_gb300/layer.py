@@ -30,7 +30,8 @@ from .ops import _p, _s
 class MoeLayer:
     def __init__(self, W1, W2, T: int, k: int, R_cap: int, params: L.GluParams, b1=None,
                  expert_begin: int = 0, sm_margin: int = 0, gated: bool = True, dynamic: bool = True,
-                 nvfp4: bool = False, rht_signs: int = 0x6A5D, fused_col_casts: bool = True):
+                 nvfp4: bool = False, rht_signs: int = 0x6A5D, fused_col_casts: bool = True,
+                 fc1_mxfp8: bool = False):
         """dynamic: the bf16 grouped GEMMs take their tiles from the dynamic
         scheduler (each call site has its own counter workspace); False runs
         the static schedule.  nvfp4: the step runs the NVFP4 recipe.  Forward:
@@ -43,7 +44,11 @@ class MoeLayer:
         product, so the rotation cancels).  fused_col_casts (MXFP8 recipe):
         the column-wise MXFP8 copies of x_perm and dY_perm that the weight
         gradients read are made by the gather and by the combine backward
-        themselves; False runs them as separate quantize calls."""
+        themselves; False runs them as separate quantize calls.  fc1_mxfp8
+        (MXFP8 recipe): FC1 contracts MXFP8 x_perm (row-wise cast after the
+        gather) with MXFP8 W1, whose two copies (along H for FC1, along 2F for
+        the data gradient) come from one read of W1 in the forward; the
+        backward then has no W1 cast of its own."""
         self.lib = L.load()
         dev = W1.device
         self.dev = dev
@@ -119,6 +124,11 @@ class MoeLayer:
             self.ws_db = z(self.ws_db_bytes, dt=u8)
         self.nvfp4 = nvfp4
         self.fused_cols = fused_col_casts and not nvfp4
+        self.fc1_mxfp8 = fc1_mxfp8 and not nvfp4
+        if self.fc1_mxfp8:
+            self.x_qr, self.x_sr = z(R_cap, H, dt=u8), z(R_cap, H // 32, dt=u8)
+            self.W1qr, self.W1sr = z(E, N1, H, dt=u8), z(E, N1, H // 32, dt=u8)
+            self.ws_fc1mx = ws(lib.moe_grouped_fc2_workspace_size(E, H, N1, R_cap))
         if nvfp4:
             f32 = torch.float32
             self.a_y, self.a_amax = z(R_cap, F), z(1, dt=f32)
@@ -166,12 +176,25 @@ class MoeLayer:
         if self.nvfp4:
             return self._forward_calls_nvfp4(x, topk_idx, topk_prob)
         xq, xs = (_p(self.x_qc), _p(self.x_sc)) if self.fused_cols else (None, None)
+        fc1 = [("fc1_glu_quant", self.fc1_mxfp8_call())]
+        if self.fc1_mxfp8:
+            fc1 = [
+                ("quant_x_rows", lambda: lib.moe_quantize_mxfp8(
+                    _p(self.x_perm), 1, R, H, 0, _p(self.counts), _p(self.offsets), E, _p(self.x_qr), _p(self.x_sr),
+                    st, s)),
+                ("quant_w1_dual", lambda: lib.moe_quantize_mxfp8_dual(
+                    _p(self.W1p), E, N1, H, _p(self.W1qr), _p(self.W1sr), _p(self.W1q), _p(self.W1s), st, s)),
+                ("fc1_mxfp8", lambda: lib.moe_grouped_fc1_glu_quant_fwd_mxfp8(
+                    _p(self.x_qr), _p(self.x_sr), _p(self.W1qr), _p(self.W1sr), _p(self.b1p), None, _p(self.counts),
+                    _p(self.offsets), E, H, F, R, C.byref(self.params), L.OUT_MXFP8, C.byref(self.fc1_out),
+                    _p(self.ws_fc1mx), self.ws_fc1mx.numel(), self.sm_margin, st, s)),
+            ]
         return [
             ("route_permute_qcol" if self.fused_cols else "route_permute", lambda: lib.moe_route_permute(
                 _p(x), _p(topk_idx), _p(topk_prob), T, H, k, self.expert_begin, E, R, _p(self.x_perm),
                 _p(self.row_of), _p(self.tok_of), _p(self.prob_perm), _p(self.counts), _p(self.offsets), xq, xs,
                 _p(self.ws), self.ws_bytes, st, s)),
-            ("fc1_glu_quant", self.fc1_mxfp8_call()),
+            *fc1,
             ("quant_w2", lambda: lib.moe_quantize_mxfp8(
                 _p(self.W2), E, F, H, 1, None, None, 0, _p(self.W2q), _p(self.W2s), st, s)),
             ("fc2", lambda: lib.moe_grouped_fc2_fwd(
@@ -247,8 +270,8 @@ class MoeLayer:
                 _p(dOut), _p(self.y_perm), _p(self.row_of), _p(self.tok_of), _p(self.prob_perm), _p(self.offsets),
                 T, H, k, E, R, _p(dY_perm), _p(self.dprob), dq, ds, st, s)),
             ("dglu_quant", self.dglu_mxfp8_call()),
-            ("quant_w1", lambda: lib.moe_quantize_mxfp8(
-                _p(self.W1p), E, N1, H, 1, None, None, 0, _p(self.W1q), _p(self.W1s), st, s)),
+            *([] if self.fc1_mxfp8 else [("quant_w1", lambda: lib.moe_quantize_mxfp8(
+                _p(self.W1p), E, N1, H, 1, None, None, 0, _p(self.W1q), _p(self.W1s), st, s))]),
             ("dx", lambda: lib.moe_grouped_fc2_fwd(
                 C.byref(self.dx_a), C.byref(self.dx_w), _p(self.counts), _p(self.offsets), E, N1, H, R,
                 L.OUT_BF16, C.byref(self.dx_out), _p(self.ws_dx), self.ws_dx.numel(), self.sm_margin, st, s)),

@@ -67,6 +67,7 @@ _SIGS = {
                                    I, P, P],
     "moe_grouped_dglu_workspace_size": ([I, I], SZ),
     "moe_quantize_mxfp8": [P, I, I, I, I, P, P, I, P, P, P, P],
+    "moe_quantize_mxfp8_dual": [P, I, I, I, P, P, P, P, P, P],
     "moe_grouped_fc1_glu_quant_fwd_mxfp8": [P, P, P, P, P, P, P, P, I, I, I, I, C.POINTER(GluParams), I,
                                             C.POINTER(ActOut), P, SZ, I, P, P],
     "moe_grouped_fc2_workspace_size": ([I, I, I, I], SZ),

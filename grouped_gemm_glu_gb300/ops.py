@@ -235,6 +235,22 @@ def quantize_mxfp8(src, col: bool = False, counts=None, offsets=None, out=None, 
     return q, s
 
 
+def quantize_mxfp8_dual(src, status=None):
+    """src [G, R, C] (or [R, C]) bf16 read once -> (q_row [G, R, C],
+    s_row [G, R, C/32], q_col [G, C, R], s_col [G, C, R/32])."""
+    lib = L.load()
+    dev = _dev(src)
+    s3 = src if src.dim() == 3 else src.unsqueeze(0)
+    G, R, Cc = s3.shape
+    qr = torch.empty(G, R, Cc, dtype=torch.uint8, device=dev)
+    sr = torch.empty(G, R, Cc // 32, dtype=torch.uint8, device=dev)
+    qc = torch.empty(G, Cc, R, dtype=torch.uint8, device=dev)
+    sc = torch.empty(G, Cc, R // 32, dtype=torch.uint8, device=dev)
+    L.check(lib.moe_quantize_mxfp8_dual(_p(s3), G, R, Cc, _p(qr), _p(sr), _p(qc), _p(sc), _p(status), _s()),
+            "moe_quantize_mxfp8_dual")
+    return qr, sr, qc, sc
+
+
 def fc2_fwd(Aq, As, Wq, Ws, counts, offsets, sm_margin: int = 0, status=None, out=None,
             out_mode: int = L.OUT_BF16, with_col: bool = True):
     """GroupGemm (+ Quantize): y [R_cap, N] = A [R_cap, K] . W[e]^T per expert

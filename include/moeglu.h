@@ -257,6 +257,19 @@ MOE_API moe_status_t moe_quantize_mxfp8(const moe_bf16* src, int G, int R, int C
                                 const int32_t* counts, const int32_t* offsets, int E,
                                 uint8_t* q, uint8_t* s, int32_t* status, moe_stream_t stream);
 
+/* Both MXFP8 copies of a weight in one pass ([MoE-Fusion] "Fusing MXFP8 and
+ * NVFP4 quantisation": a row-wise output plus a transposed copy): src
+ * [G][R][C] bf16 is read once and written as
+ *   q_row [G][R][C], s_row [G][R][C/32]  (blocks along C, as col == 0), and
+ *   q_col [G][C][R], s_col [G][C][R/32]  (blocks along R, as col != 0),
+ * the same bytes as the two moe_quantize_mxfp8 calls.  For W1p [E][2F][H]
+ * the first feeds an MXFP8-input FC1 (contraction over H), the second the
+ * data gradient (contraction over 2F).  R % 32 == 0, C % 32 == 0; src and
+ * q_col 16-byte, q_row 8-byte aligned.  status (nullable) as above. */
+MOE_API moe_status_t moe_quantize_mxfp8_dual(const moe_bf16* src, int G, int R, int C, uint8_t* q_row,
+                                             uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, int32_t* status,
+                                             moe_stream_t stream);
+
 /* Bytes of device workspace moe_grouped_fc2_fwd needs with block-scaled
  * (MXFP8 or NVFP4) operands: the scales of the visited tiles, rewritten in the
  * order the tensor cores read them (enough for either type); bf16 operands

@@ -11,7 +11,7 @@ import test_gpu_fc1 as F
 from grouped_gemm_glu_gb300 import lib as L
 from grouped_gemm_glu_gb300 import ops, synth
 from oracle import moe_oracle as O
-from parity import assert_bf16_close, assert_mx_close, np_
+from parity import assert_bf16_close, assert_exact, assert_mx_close, np_
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -116,3 +116,29 @@ def test_fc1_mxfp8_dsv3_full_size_sampled():
         acc["v"].append(y)
     cat = {k: np.concatenate(v) for k, v in acc.items()}
     assert_mx_close(cat["qg"], cat["sg"], cat["qr"], cat["sr"], cat["v"], "dsv3 mxfp8 FC1 row-wise")
+
+
+@pytest.mark.parametrize("G,R,C", [(3, 96, 160), (2, 256, 256), (1, 4096, 448)])
+def test_weight_dual_cast_bit_exact(G, R, C):
+    """Both MXFP8 copies of a weight from one read (row-wise along C for the
+    MXFP8-input FC1, column-wise along R for the data gradient): bit-exact
+    against the oracle's two casts, with partial tiles (R 96, C 160), a NaN
+    and an Inf (scale 0xFF, codes 0x7F for their blocks) and exponents spread
+    over 2^-8 .. 2^8 per column."""
+    rng = np.random.default_rng(G * R + C)
+    Wf = rng.standard_normal((G, R, C), dtype=np.float32) * np.exp2(rng.integers(-8, 8, (G, 1, C)))
+    Wf[0, 5, 7] = np.nan
+    Wf[G - 1, R - 1, C - 1] = np.inf
+    W = synth._bf16(Wf)
+    st = ops.new_status(DEV)
+    qr, sr, qc, sc = ops.quantize_mxfp8_dual(W.to(DEV), status=st)
+    torch.cuda.synchronize()
+    assert ops.read_status(st) == 0
+    Wn = np_(W)
+    for g in range(G):
+        q_ref, s_ref = O.mx_quantize_rows(Wn[g])
+        assert_exact(np_(qr[g]), q_ref, f"row codes {g}")
+        assert_exact(np_(sr[g]), s_ref, f"row scales {g}")
+        q_ref, s_ref = O.mx_quantize_cols(Wn[g])
+        assert_exact(np_(qc[g]), q_ref, f"column codes {g}")
+        assert_exact(np_(sc[g]), s_ref, f"column scales {g}")

@@ -9,7 +9,7 @@ from grouped_gemm_glu_gb300 import lib as L
 from grouped_gemm_glu_gb300 import ops, synth
 from grouped_gemm_glu_gb300.layer import MoeLayer
 from oracle import moe_oracle as O
-from parity import assert_bf16_close, assert_chain_close, np_
+from parity import assert_bf16_close, assert_chain_close, assert_exact, np_
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -200,3 +200,49 @@ def test_dense_mode_single_expert():
     assert ops.read_status(layer.status) == 0
     assert int(layer.counts[0]) == w.T
     _check(layer, inp, w)
+
+
+def test_layer_step_mxfp8_fc1():
+    """The layer with the MXFP8-input FC1: both MXFP8 copies of W1 from one
+    read (bit-exact against the oracle's two casts), the row-wise cast of
+    x_perm (bit-exact), FC1's saved pre-activations against the oracle FC1 on
+    the dequantised operands, the backward GEMMs on the layer's own operands,
+    and one captured graph replaying to the eager results."""
+    w = synth.WORKLOADS["tiny"]
+    inp = synth.make_inputs(w, seed=24)
+    g = {k: (v.to(DEV) if v is not None else None) for k, v in inp.items()}
+    kp, prm = _acts(w)
+    layer = MoeLayer(g["W1"], g["W2"], w.T, w.k, w.R_cap, kp, fc1_mxfp8=True)
+    args = (g["x"], g["topk_idx"], g["topk_prob"], g["dOut"])
+    layer.step(*args)
+    torch.cuda.synchronize()
+    assert ops.read_status(layer.status) == 0
+    names = [n for n, _ in layer.step_calls(*args)]
+    assert "quant_w1_dual" in names and "fc1_mxfp8" in names and "quant_w1" not in names
+    rt = O.route(inp["topk_idx"].numpy(), 0, w.E)
+    Rp = rt.R_pad
+    W1p = O.repack_fc1(np_(inp["W1"]))
+    for e in range(w.E):
+        q, s_ = O.mx_quantize_rows(W1p[e])
+        assert_exact(np_(layer.W1qr[e]), q, "W1 rows codes")
+        assert_exact(np_(layer.W1sr[e]), s_, "W1 rows scales")
+        q, s_ = O.mx_quantize_cols(W1p[e])
+        assert_exact(np_(layer.W1q[e]), q, "W1 columns codes")
+        assert_exact(np_(layer.W1s[e]), s_, "W1 columns scales")
+    xp = O.permute(np_(inp["x"]), rt)
+    xq, xs = O.mx_quantize_rows(xp)
+    assert_exact(np_(layer.x_qr)[:Rp], xq, "x_perm rows codes")
+    assert_exact(np_(layer.x_sr)[:Rp], xs, "x_perm rows scales")
+    fo = O.fc1_glu_fwd(O.mx_dequantize(xq, xs), np.stack([O.mx_dequantize(*O.mx_quantize_rows(W1p[e]))
+                                                          for e in range(w.E)]), None, rt, prm)
+    assert_bf16_close(np_(layer.pre)[:Rp], fo.pre_bf16, "FC1 pre-activations")
+    _check_stagewise(layer, rt)
+    eager = {k: getattr(layer, k).clone() for k in ("out", "dx", "dW1", "dW2", "dprob")}
+    graph = layer.capture(*args)
+    for t in eager:
+        getattr(layer, t).zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert ops.read_status(layer.status) == 0
+    for t, v in eager.items():
+        assert torch.equal(getattr(layer, t), v), f"graph replay differs from eager: {t}"

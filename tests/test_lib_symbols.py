@@ -37,6 +37,7 @@ def test_workspace_size_is_host_only(lib):
 def test_argument_validation_needs_no_device(lib):
     # a null pointer is rejected on the host before anything is launched
     assert lib.moe_unpermute_combine(None, None, None, 1, 8, 1, None, None, None) == L.MOE_ERR_ARG
+    assert lib.moe_quantize_mxfp8_dual(None, 1, 32, 32, None, None, None, None, None, None) == L.MOE_ERR_ARG
     assert lib.moe_combine_bwd(None, None, None, None, None, None, 1, 8, 1, 1, 128, None, None, None,
                                None, None, None) == L.MOE_ERR_ARG
     assert lib.moe_permute_bwd(None, None, 1, 8, 1, None, None, None) == L.MOE_ERR_ARG
