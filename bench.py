@@ -253,8 +253,9 @@ def run_oracle_timed(inp, w, steps, warmup, budget_s):
 
 def profile_traffic(call_name):
     """DRAM bytes (read + write) per launch of one step call, from the
-    committed ncu launch list of this workload, if that capture was taken on
-    the current kernel sources (else None)."""
+    committed ncu capture of that kernel (taken on the 8-expert shard and
+    scaled to this workload), if it was taken on the current kernel sources
+    (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic_dsv3.json")
     if not os.path.exists(p):
         return None
@@ -571,6 +572,9 @@ def main():
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
     tr = profile_traffic(dom) if w.E == base.E and w.name == WORKLOAD and not args.experts else None
     roof["traffic"] = tr
+    if tr is not None:
+        roof["traffic_source"] = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of this kernel on the 8-expert "
+                                  "shard, x 32/8 (profiles/traffic_dsv3.json)")
     roof["kernel"] = dom
     if roof["bound"] == "hbm":
         roof["peak_source"] = f"of {peaks['src']} (HBM copy)"
