@@ -89,6 +89,7 @@ struct Args {
   const int32_t* offsets;
   int E, M, N, K, R_cap;   // K: fixed contraction (M-grouped); M: rows of A (K-grouped)
   int kgrouped;            // 0: FC2 / dX, 1: weight gradient
+  int b_pretiled;          // M-grouped: Bs is already in the tensor-core order (sfb_t = Bs; nothing to re-tile)
   int n_tiles_n, m_tiles;  // tiles along N; along M (K-grouped)
   int KB;                  // M-grouped: k-blocks per row tile (K / 128)
   int KG;                  // K-grouped: stride of the k-block axis of the tiled scales
@@ -265,7 +266,7 @@ __global__ void __launch_bounds__(256) k_sf_tile(const Args a) {
   if (!a.kgrouped) {
     const int mt_cap = a.R_cap / BM + a.E;
     nA = (size_t)min(pref[a.E], mt_cap) * a.KB;
-    nB = (size_t)a.E * bgroups * a.KB;
+    nB = a.b_pretiled ? 0 : (size_t)a.E * bgroups * a.KB;
   } else {
     ktot = min(pref[a.E], a.KG);
     nA = (size_t)a.m_tiles * ktot;
@@ -896,7 +897,9 @@ extern "C" moe_status_t moe_grouped_fc2_fwd(const moe_in_t* A, const moe_in_t* W
   if (!A || !W || !A->data || !W->data || !counts || !offsets || !out) return MOE_ERR_ARG;
   if (E <= 0 || E > E_MAX || K <= 0 || (K % 32) || N <= 0 || (N % 32) || R_cap <= 0 || (R_cap % BM))
     return MOE_ERR_ARG;
-  if (sm_margin < 0 || A->dtype != W->dtype) return MOE_ERR_ARG;  // one operand type per MMA
+  // one operand type per MMA (an MXFP8 weight may carry pre-tiled scales)
+  const bool w_tiled = A->dtype == MOE_IN_MXFP8 && W->dtype == MOE_IN_MXFP8_TILED;
+  if (sm_margin < 0 || (A->dtype != W->dtype && !w_tiled)) return MOE_ERR_ARG;
   if (out_mode != MOE_OUT_BF16 && out_mode != MOE_OUT_MXFP8 && out_mode != MOE_OUT_NVFP4) return MOE_ERR_ARG;
   if (out->pre || out->row_dot || out->rht_amax) return MOE_ERR_ARG;
   if (A->dtype == MOE_IN_BF16)
@@ -969,6 +972,7 @@ extern "C" moe_status_t moe_grouped_fc2_fwd(const moe_in_t* A, const moe_in_t* W
   if (!aligned16(Aq) || !aligned16(Wq) || (reinterpret_cast<uintptr_t>(As) & 3) ||
       (reinterpret_cast<uintptr_t>(Ws) & 3) || (reinterpret_cast<uintptr_t>(ws) & 255))
     return MOE_ERR_ARG;
+  if (w_tiled && (reinterpret_cast<uintptr_t>(Ws) & 15)) return MOE_ERR_ARG;  // 16-byte bulk copies
   if (out_mode == MOE_OUT_MXFP8) {
     if (!out->q_row || !out->s_row || (out->q_col == nullptr) != (out->s_col == nullptr)) return MOE_ERR_ARG;
     if (!aligned16(out->q_row) || (out->q_col && !aligned16(out->q_col))) return MOE_ERR_ARG;
@@ -1012,7 +1016,8 @@ extern "C" moe_status_t moe_grouped_fc2_fwd(const moe_in_t* A, const moe_in_t* W
   a.As = As;
   a.Bs = Ws;
   a.sfa_t = static_cast<uint8_t*>(ws);
-  a.sfb_t = static_cast<uint8_t*>(ws) + a_bytes;
+  a.sfb_t = w_tiled ? const_cast<uint8_t*>(Ws) : static_cast<uint8_t*>(ws) + a_bytes;
+  a.b_pretiled = w_tiled ? 1 : 0;
   a.out = out->y;
   a.out_f32 = 0;
   a.status = status;
@@ -1027,7 +1032,7 @@ extern "C" moe_status_t moe_grouped_fc2_fwd(const moe_in_t* A, const moe_in_t* W
   a.amax = out->amax;
   const long long mt_bound = (long long)R_cap / BM + E;
   const long long bound = mt_bound * a.n_tiles_n;
-  const long long sf_items = mt_bound * a.KB + (long long)E * 2 * a.n_tiles_n * a.KB;
+  const long long sf_items = mt_bound * a.KB + (w_tiled ? 0 : (long long)E * 2 * a.n_tiles_n * a.KB);
   return launch(tmA, tmB, nullptr, a, bound, sf_items, sm_margin, as_stream(stream));
 }
 

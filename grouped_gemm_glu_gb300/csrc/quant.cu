@@ -133,13 +133,19 @@ constexpr int QC_SMEM_BASE = QC_OFF_SEG;                  // + (2E + 1) ints of 
 // instruction (512 contiguous bytes: no bank conflicts), 8-byte code stores
 // that join into whole 128-byte lines.  One read of a weight then feeds both
 // of its MXFP8 copies (along C for one GEMM, along R for another).
+// s_tiled: the scales leave in the order the block-scaled GEMM's tensor-core
+// copies read them when this tensor is its N x K weight operand (N = C, K =
+// R): [G][ceil(C/256)][ceil(R/128)][2][512 bytes], the 512 bytes of one
+// (128-row group of C, 128-element k-block of R) holding at byte
+// 16 l + 4 j + i the scale of row 32 j + l of the group, sub-block i.  A
+// staged tile is exactly one such block.
 template <bool ROWS>
 __global__ void __launch_bounds__(256) k_quant_cols(const __grid_constant__ CUtensorMap tm, int G, int R, int Cc,
                                                     const int32_t* __restrict__ counts,
                                                     const int32_t* __restrict__ offsets, int E,
                                                     uint8_t* __restrict__ q, uint8_t* __restrict__ s,
                                                     uint8_t* __restrict__ q_row, uint8_t* __restrict__ s_row,
-                                                    int32_t* status, uint64_t wait_ns) {
+                                                    int s_tiled, int32_t* status, uint64_t wait_ns) {
   extern __shared__ __align__(128) uint8_t qsm[];
   uint8_t* tin = qsm;
   uint8_t* tcode = qsm + QC_OFF_CODE;
@@ -289,8 +295,15 @@ __global__ void __launch_bounds__(256) k_quant_cols(const __grid_constant__ CUte
           const uint4 val = *reinterpret_cast<const uint4*>(tcode + cl * QC_CODE_ROW + part * 16);
           uint8_t* dst = q + ((size_t)g * Cc + c) * R + r0 + part * 16;
           if (whole || r0 + part * 16 < R) *reinterpret_cast<uint4*>(dst) = val;
-          if (part < 4 && rr[part] >= 0) s[((size_t)g * Cc + c) * nblk + (r0 >> 5) + part] = tscale[cl * 4 + part];
+          if (!s_tiled && part < 4 && rr[part] >= 0)
+            s[((size_t)g * Cc + c) * nblk + (r0 >> 5) + part] = tscale[cl * 4 + part];
         }
+      }
+      if (s_tiled && warp == 0) {  // the tile's 512-byte block: lane l writes bytes 16 l .. 16 l + 15
+        const int nt = (Cc + 255) / 256, kbs = (R + 127) / 128, gi = c0 / QC_COLS;
+        const uint32_t* ts = reinterpret_cast<const uint32_t*>(tscale);
+        uint8_t* dst = s + ((((size_t)g * nt + (gi >> 1)) * kbs + r0 / QC_ROWS) * 2 + (gi & 1)) * 512;
+        reinterpret_cast<uint4*>(dst)[lane] = make_uint4(ts[lane], ts[32 + lane], ts[64 + lane], ts[96 + lane]);
       }
     }
   }
@@ -928,6 +941,7 @@ extern "C" moe_status_t moe_quantize_mxfp8(const moe_bf16* src, int G, int R, in
     k_quant_rows<<<(int)(grid < 1 ? 1 : grid), 256, smem, st>>>(src, G, R, Cc, counts, offsets, E, q, s);
   } else {
     if ((R % 32) || (Cc % 8)) return MOE_ERR_ARG;
+    if (col == 2 && (E > 0 || (reinterpret_cast<uintptr_t>(s) & 15))) return MOE_ERR_ARG;  // weights only
     const size_t tiles = (size_t)G * ((R + QC_ROWS - 1) / QC_ROWS) * ((Cc + QC_COLS - 1) / QC_COLS);
     if (tiles > (size_t)INT32_MAX) return MOE_ERR_ARG;
     CUtensorMap tm;
@@ -943,11 +957,16 @@ extern "C" moe_status_t moe_quantize_mxfp8(const moe_bf16* src, int G, int R, in
     size_t grid = tiles;
     if (grid > (size_t)sms * occ) grid = (size_t)sms * occ;
     k_quant_cols<false><<<(int)(grid < 1 ? 1 : grid), 256, smem, st>>>(tm, G, R, Cc, counts, offsets, E, q, s,
-                                                                      nullptr, nullptr, status,
+                                                                      nullptr, nullptr, col == 2 ? 1 : 0, status,
                                                                       g_wait_limit_ns.load());
   }
   count_launch();
   return launch_status();
+}
+
+extern "C" size_t moe_mxfp8_tiled_scale_bytes(int G, int R, int C) {
+  if (G <= 0 || R <= 0 || C <= 0) return 0;
+  return (size_t)G * ((C + 255) / 256) * ((R + 127) / 128) * 1024;
 }
 
 extern "C" moe_status_t moe_quantize_mxfp8_dual(const moe_bf16* src, int G, int R, int Cc, uint8_t* q_row,
@@ -970,7 +989,7 @@ extern "C" moe_status_t moe_quantize_mxfp8_dual(const moe_bf16* src, int G, int 
   size_t grid = tiles;
   if (grid > (size_t)sm_count() * occ) grid = (size_t)sm_count() * occ;
   k_quant_cols<true><<<(int)(grid < 1 ? 1 : grid), 256, smem, as_stream(stream)>>>(
-      tm, G, R, Cc, nullptr, nullptr, 0, q_col, s_col, q_row, s_row, status, g_wait_limit_ns.load());
+      tm, G, R, Cc, nullptr, nullptr, 0, q_col, s_col, q_row, s_row, 0, status, g_wait_limit_ns.load());
   count_launch();
   return launch_status();
 }

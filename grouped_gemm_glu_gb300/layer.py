@@ -85,13 +85,16 @@ class MoeLayer:
         self.a_q, self.a_s = z(R_cap, F, dt=u8), z(R_cap, F // 32, dt=u8)
         self.a_qc, self.a_sc = z(F, R_cap, dt=u8), z(F, R_cap // 32, dt=u8)
         self.pre = z(R_cap, N1)
-        self.W2q, self.W2s = z(E, H, F, dt=u8), z(E, H, F // 32, dt=u8)
+        # weight copies for FC2 / dX (MXFP8, transposed), scales in the tensor-core order
+        self.W2q = z(E, H, F, dt=u8)
+        self.W2s = z(self.lib.moe_mxfp8_tiled_scale_bytes(E, F, H), dt=u8)
         self.y_perm = z(R_cap, H)
         self.out = z(T, H)
         # backward
         self.d_q, self.d_s = z(R_cap, N1, dt=u8), z(R_cap, N1 // 32, dt=u8)
         self.d_qc, self.d_sc = z(N1, R_cap, dt=u8), z(N1, R_cap // 32, dt=u8)
-        self.W1q, self.W1s = z(E, H, N1, dt=u8), z(E, H, N1 // 32, dt=u8)
+        self.W1q = z(E, H, N1, dt=u8)
+        self.W1s = z(self.lib.moe_mxfp8_tiled_scale_bytes(E, N1, H), dt=u8)
         self.dY_perm = z(R_cap, H)
         self.dprob = z(T, k, dt=torch.float32)
         self.dX_perm = z(R_cap, H)
@@ -128,6 +131,7 @@ class MoeLayer:
         if self.fc1_mxfp8:
             self.x_qr, self.x_sr = z(R_cap, H, dt=u8), z(R_cap, H // 32, dt=u8)
             self.W1qr, self.W1sr = z(E, N1, H, dt=u8), z(E, N1, H // 32, dt=u8)
+            self.W1s_p = z(E, H, N1 // 32, dt=u8)  # the dual cast's column scales (plain layout)
             self.ws_fc1mx = ws(lib.moe_grouped_fc2_workspace_size(E, H, N1, R_cap))
         if nvfp4:
             f32 = torch.float32
@@ -158,10 +162,11 @@ class MoeLayer:
             self.dx_w4 = L.in_operand(self.W1q4.data_ptr(), self.W1s4.data_ptr(), self.w1_sg.data_ptr())
         # operands and outputs of the two block-scaled M-grouped GEMMs
         self.fc2_a = L.in_operand(self.a_q.data_ptr(), self.a_s.data_ptr())
-        self.fc2_w = L.in_operand(self.W2q.data_ptr(), self.W2s.data_ptr())
+        self.fc2_w = L.in_operand(self.W2q.data_ptr(), self.W2s.data_ptr(), tiled=True)
         self.fc2_out = L.ActOut(None, None, None, None, self.y_perm.data_ptr(), None, None)
         self.dx_a = L.in_operand(self.d_q.data_ptr(), self.d_s.data_ptr())
-        self.dx_w = L.in_operand(self.W1q.data_ptr(), self.W1s.data_ptr())
+        self.dx_w = (L.in_operand(self.W1q.data_ptr(), self.W1s_p.data_ptr()) if self.fc1_mxfp8
+                     else L.in_operand(self.W1q.data_ptr(), self.W1s.data_ptr(), tiled=True))
         self.dx_out = L.ActOut(None, None, None, None, self.dX_perm.data_ptr(), None, None)
         self.fc1_out = L.ActOut(self.a_q.data_ptr(), self.a_s.data_ptr(), self.a_qc.data_ptr(),
                                 self.a_sc.data_ptr(), None, None, self.pre.data_ptr())
@@ -183,7 +188,7 @@ class MoeLayer:
                     _p(self.x_perm), 1, R, H, 0, _p(self.counts), _p(self.offsets), E, _p(self.x_qr), _p(self.x_sr),
                     st, s)),
                 ("quant_w1_dual", lambda: lib.moe_quantize_mxfp8_dual(
-                    _p(self.W1p), E, N1, H, _p(self.W1qr), _p(self.W1sr), _p(self.W1q), _p(self.W1s), st, s)),
+                    _p(self.W1p), E, N1, H, _p(self.W1qr), _p(self.W1sr), _p(self.W1q), _p(self.W1s_p), st, s)),
                 ("fc1_mxfp8", lambda: lib.moe_grouped_fc1_glu_quant_fwd_mxfp8(
                     _p(self.x_qr), _p(self.x_sr), _p(self.W1qr), _p(self.W1sr), _p(self.b1p), None, _p(self.counts),
                     _p(self.offsets), E, H, F, R, C.byref(self.params), L.OUT_MXFP8, C.byref(self.fc1_out),
@@ -196,7 +201,7 @@ class MoeLayer:
                 _p(self.ws), self.ws_bytes, st, s)),
             *fc1,
             ("quant_w2", lambda: lib.moe_quantize_mxfp8(
-                _p(self.W2), E, F, H, 1, None, None, 0, _p(self.W2q), _p(self.W2s), st, s)),
+                _p(self.W2), E, F, H, 2, None, None, 0, _p(self.W2q), _p(self.W2s), st, s)),
             ("fc2", lambda: lib.moe_grouped_fc2_fwd(
                 C.byref(self.fc2_a), C.byref(self.fc2_w), _p(self.counts), _p(self.offsets), E, F, H, R,
                 L.OUT_BF16, C.byref(self.fc2_out), _p(self.ws_fc2), self.ws_fc2.numel(), self.sm_margin, st, s)),
@@ -271,7 +276,7 @@ class MoeLayer:
                 T, H, k, E, R, _p(dY_perm), _p(self.dprob), dq, ds, st, s)),
             ("dglu_quant", self.dglu_mxfp8_call()),
             *([] if self.fc1_mxfp8 else [("quant_w1", lambda: lib.moe_quantize_mxfp8(
-                _p(self.W1p), E, N1, H, 1, None, None, 0, _p(self.W1q), _p(self.W1s), st, s))]),
+                _p(self.W1p), E, N1, H, 2, None, None, 0, _p(self.W1q), _p(self.W1s), st, s))]),
             ("dx", lambda: lib.moe_grouped_fc2_fwd(
                 C.byref(self.dx_a), C.byref(self.dx_w), _p(self.counts), _p(self.offsets), E, N1, H, R,
                 L.OUT_BF16, C.byref(self.dx_out), _p(self.ws_dx), self.ws_dx.numel(), self.sm_margin, st, s)),

@@ -31,20 +31,23 @@ class ActOut(C.Structure):
                 ("rht_amax", C.c_void_p), ("rht_signs", C.c_uint32)]
 
 
-IN_BF16, IN_MXFP8, IN_NVFP4 = 0, 1, 2
+IN_BF16, IN_MXFP8, IN_NVFP4, IN_MXFP8_TILED = 0, 1, 2, 3
 
 
 class InT(C.Structure):
     _fields_ = [("dtype", C.c_int32), ("data", C.c_void_p), ("scale", C.c_void_p), ("global_scale", C.c_void_p)]
 
 
-def in_operand(data_ptr: int, scale_ptr: int | None = None, global_scale_ptr: int | None = None) -> InT:
-    """A GEMM operand: bf16 when scale_ptr is None, MXFP8 codes + scales, or
-    NVFP4 codes + block scales + per-tensor scale when global_scale_ptr is set."""
+def in_operand(data_ptr: int, scale_ptr: int | None = None, global_scale_ptr: int | None = None,
+               tiled: bool = False) -> InT:
+    """A GEMM operand: bf16 when scale_ptr is None, MXFP8 codes + scales
+    (tiled: scales already in the tensor-core order, a weight cast with
+    col = 2), or NVFP4 codes + block scales + per-tensor scale when
+    global_scale_ptr is set."""
     if scale_ptr is None:
         return InT(IN_BF16, data_ptr, None, None)
     if global_scale_ptr is None:
-        return InT(IN_MXFP8, data_ptr, scale_ptr, None)
+        return InT(IN_MXFP8_TILED if tiled else IN_MXFP8, data_ptr, scale_ptr, None)
     return InT(IN_NVFP4, data_ptr, scale_ptr, global_scale_ptr)
 
 
@@ -68,6 +71,7 @@ _SIGS = {
     "moe_grouped_dglu_workspace_size": ([I, I], SZ),
     "moe_quantize_mxfp8": [P, I, I, I, I, P, P, I, P, P, P, P],
     "moe_quantize_mxfp8_dual": [P, I, I, I, P, P, P, P, P, P],
+    "moe_mxfp8_tiled_scale_bytes": ([I, I, I], SZ),
     "moe_grouped_fc1_glu_quant_fwd_mxfp8": [P, P, P, P, P, P, P, P, I, I, I, I, C.POINTER(GluParams), I,
                                             C.POINTER(ActOut), P, SZ, I, P, P],
     "moe_grouped_fc2_workspace_size": ([I, I, I, I], SZ),

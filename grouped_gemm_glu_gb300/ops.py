@@ -214,13 +214,21 @@ def dglu_bwd(dY_perm, W2, pre, counts, offsets, F: int, params: L.GluParams, out
     return o
 
 
-def quantize_mxfp8(src, col: bool = False, counts=None, offsets=None, out=None, status=None):
+def quantize_mxfp8(src, col: bool = False, counts=None, offsets=None, out=None, status=None, tiled: bool = False):
     """src [R, C] or [G, R, C] bf16 -> (q, s); col=True gives the transposed
-    column-wise copy."""
+    column-wise copy; tiled (with col) writes the scales in the tensor-core
+    order of a GEMM weight operand (flat uint8 [moe_mxfp8_tiled_scale_bytes])."""
     lib = L.load()
     dev = _dev(src)
     s3 = src if src.dim() == 3 else src.unsqueeze(0)
     G, R, Cc = s3.shape
+    if col and tiled:
+        q = torch.empty(G, Cc, R, dtype=torch.uint8, device=dev) if out is None else out[0]
+        s = (torch.empty(lib.moe_mxfp8_tiled_scale_bytes(G, R, Cc), dtype=torch.uint8, device=dev)
+             if out is None else out[1])
+        L.check(lib.moe_quantize_mxfp8(_p(s3), G, R, Cc, 2, None, None, 0, _p(q), _p(s), _p(status), _s()),
+                "moe_quantize_mxfp8")
+        return (q[0] if src.dim() == 2 and out is None else q), s
     if col:
         q = torch.empty(G, Cc, R, dtype=torch.uint8, device=dev) if out is None else out[0]
         s = torch.empty(G, Cc, R // 32, dtype=torch.uint8, device=dev) if out is None else out[1]
@@ -252,12 +260,13 @@ def quantize_mxfp8_dual(src, status=None):
 
 
 def fc2_fwd(Aq, As, Wq, Ws, counts, offsets, sm_margin: int = 0, status=None, out=None,
-            out_mode: int = L.OUT_BF16, with_col: bool = True):
+            out_mode: int = L.OUT_BF16, with_col: bool = True, w_tiled: bool = False):
     """GroupGemm (+ Quantize): y [R_cap, N] = A [R_cap, K] . W[e]^T per expert
     with W [E, N, K].  MXFP8 operands (codes Aq/Wq with E8M0 scales As/Ws),
     or bf16 operands when As and Ws are None.  out_mode OUT_BF16 returns the
     bf16 tensor y; OUT_MXFP8 returns {q_row, s_row[, q_col, s_col]};
-    OUT_NVFP4 returns {y, amax}."""
+    OUT_NVFP4 returns {y, amax}.  w_tiled: Ws is in the tensor-core order
+    (quantize_mxfp8(..., col=True, tiled=True))."""
     lib = L.load()
     dev = _dev(Aq)
     R_cap, K = Aq.shape
@@ -278,7 +287,7 @@ def fc2_fwd(Aq, As, Wq, Ws, counts, offsets, sm_margin: int = 0, status=None, ou
         o["amax"] = torch.zeros(1, dtype=torch.float32, device=dev)
     st = status if status is not None else new_status(dev)
     a_in = L.in_operand(Aq.data_ptr(), None if As is None else As.data_ptr())
-    w_in = L.in_operand(Wq.data_ptr(), None if Ws is None else Ws.data_ptr())
+    w_in = L.in_operand(Wq.data_ptr(), None if Ws is None else Ws.data_ptr(), tiled=w_tiled)
     ws_bytes = lib.moe_grouped_fc2_workspace_size(E, K, N, R_cap) if As is not None else 0
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     ao = _act_out(o.get("q_row"), o.get("s_row"), o.get("q_col"), o.get("s_col"), o.get("y"), o.get("amax"))

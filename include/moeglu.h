@@ -128,11 +128,15 @@ typedef struct {
 
 /* Operand of a grouped GEMM that takes either precision. */
 typedef enum {
-  MOE_IN_BF16 = 0,  /* bf16 values */
-  MOE_IN_MXFP8 = 1, /* E4M3 codes with E8M0 scales, one per 32 elements along K */
-  MOE_IN_NVFP4 = 2  /* packed E2M1 codes (element 2i in the low nibble of byte i) with E4M3
-                       scales, one per 16 elements along K, and one fp32 per-tensor scale s_g:
-                       value = e2m1 * s_b / s_g (moe_nvfp4_cast, moe_nvfp4_cast_cols) */
+  MOE_IN_BF16 = 0,        /* bf16 values */
+  MOE_IN_MXFP8 = 1,       /* E4M3 codes with E8M0 scales, one per 32 elements along K */
+  MOE_IN_NVFP4 = 2,       /* packed E2M1 codes (element 2i in the low nibble of byte i) with E4M3
+                             scales, one per 16 elements along K, and one fp32 per-tensor scale
+                             s_g: value = e2m1 * s_b / s_g (moe_nvfp4_cast, moe_nvfp4_cast_cols) */
+  MOE_IN_MXFP8_TILED = 3  /* an MXFP8 weight (the W operand of moe_grouped_fc2_fwd, next to an
+                             MXFP8 A) whose scales are already in the order the tensor cores copy
+                             them, as written by moe_quantize_mxfp8 with col = 2: the call skips
+                             their re-tiling.  Scales 16-byte aligned. */
 } moe_in_dtype_t;
 
 typedef struct {
@@ -246,8 +250,16 @@ MOE_API size_t moe_grouped_dglu_workspace_size(int N1, int R_cap);
  * kernel of the unfused path, and the weight cast).  src [G][R][C] bf16,
  * 16-byte aligned.
  * col == 0: q [G][R][C], s [G][R][C/32] (blocks along C); C % 32 == 0.
- * col != 0: q [G][C][R], s [G][C][R/32] (blocks of 32 rows; transposed);
+ * col == 1: q [G][C][R], s [G][C][R/32] (blocks of 32 rows; transposed);
  *           R % 32 == 0, C % 8 == 0; the tiles are staged by TMA.
+ * col == 2: as col == 1, with the scales written in the order the
+ *           block-scaled GEMM's tensor-core copies read them when the
+ *           result is its N x K weight (N = C, K = R; an MXFP8_TILED
+ *           operand of moe_grouped_fc2_fwd):
+ *           s [G][ceil(C/256)][ceil(R/128)][2][512] bytes, byte 16 l + 4 j + i
+ *           of the 512 of (128-row group g of C, k-block b of R) = the scale
+ *           of row 128 g + 32 j + l, rows 128 b + 32 i .. + 31 of R
+ *           (moe_mxfp8_tiled_scale_bytes); no counts; s 16-byte aligned.
  * counts/offsets (G == 1 only, may be NULL): rows of the permuted layout
  * outside [offsets[e], offsets[e]+counts[e]) are treated as zero; results
  * for rows >= offsets[E] are unspecified (their scales are not written).
@@ -256,6 +268,9 @@ MOE_API size_t moe_grouped_dglu_workspace_size(int N1, int R_cap);
 MOE_API moe_status_t moe_quantize_mxfp8(const moe_bf16* src, int G, int R, int C, int col,
                                 const int32_t* counts, const int32_t* offsets, int E,
                                 uint8_t* q, uint8_t* s, int32_t* status, moe_stream_t stream);
+
+/* Bytes of the col == 2 scale layout of moe_quantize_mxfp8 for src [G][R][C]. */
+MOE_API size_t moe_mxfp8_tiled_scale_bytes(int G, int R, int C);
 
 /* Both MXFP8 copies of a weight in one pass ([MoE-Fusion] "Fusing MXFP8 and
  * NVFP4 quantisation": a row-wise output plus a transposed copy): src

@@ -111,3 +111,14 @@ def assert_chain_close(gpu, ref, what="", frac=0.999, max_frac=0.02):
     assert ok.mean() >= frac, f"{what}: only {ok.mean():.5f} of elements within the bf16 rule"
     bound = max_frac * np.abs(r).max()
     assert err.max() <= bound, f"{what}: worst |d|={err.max():.4g} above {100 * max_frac:g}% of max |ref| ({bound:.4g})"
+
+
+def untile_weight_scales(s_tiled, G: int, R: int, C: int) -> np.ndarray:
+    """The plain column-wise scale layout [G][C][R/32] of scales written in
+    the tensor-core order (moe_quantize_mxfp8 with col = 2): the 512 bytes of
+    (128-row group of C, 128-element k-block of R) hold at byte 16 l + 4 j + i
+    the scale of row 32 j + l of the group, sub-block i of the k-block."""
+    nt, kbs = (C + 255) // 256, (R + 127) // 128
+    t = np.asarray(s_tiled, dtype=np.uint8).reshape(G, nt, kbs, 2, 32, 4, 4)   # g, ntile, kb, half, l, j, i
+    t = t.transpose(0, 1, 3, 5, 4, 2, 6).reshape(G, nt * 256, kbs * 4)          # g, c, sub-block
+    return t[:, :C, : R // 32]

@@ -10,7 +10,7 @@ import torch
 from grouped_gemm_glu_gb300 import lib as L
 from grouped_gemm_glu_gb300 import ops, synth
 from oracle import moe_oracle as O
-from parity import assert_bf16_close, assert_mx_close, np_
+from parity import assert_bf16_close, assert_exact, assert_mx_close, np_, untile_weight_scales
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -192,3 +192,33 @@ def test_dbias_gptoss_full_size_sampled_experts():
     """GPT-OSS-shaped backward at full size (T 16384, 32 experts of ~2048
     rows): the bias gradient of four experts, each summed over ~64 blocks."""
     _dbias_case(synth.WORKLOADS["gptoss"], experts=(0, 9, 22, 31))
+
+
+@pytest.mark.parametrize("E,K,N", [(3, 160, 384), (2, 4096, 2880), (4, 2048, 7168)])
+def test_tiled_weight_scales(E, K, N):
+    """A weight cast with its scales written in the tensor-core order
+    (moe_quantize_mxfp8 col = 2): the same codes as the plain column cast and
+    the same scales once un-permuted (K = 160: a partial last k-block; N =
+    384 and 2880: an odd number of 128-row groups); the FC2 on that operand
+    (MXFP8_TILED, no re-tiling of its scales) gives the same bits as on the
+    plain one."""
+    rng = np.random.default_rng(E * K + N)
+    Wsrc = synth._bf16(rng.standard_normal((E, K, N), dtype=np.float32)
+                       * np.exp2(rng.integers(-6, 6, (E, 1, N)))).to(DEV)   # [E][K][N]: cast along K
+    st = ops.new_status(DEV)
+    q_t, s_t = ops.quantize_mxfp8(Wsrc, col=True, tiled=True, status=st)
+    q_p, s_p = ops.quantize_mxfp8(Wsrc, col=True, status=st)
+    torch.cuda.synchronize()
+    assert ops.read_status(st) == 0
+    assert torch.equal(q_t, q_p)
+    assert_exact(untile_weight_scales(np_(s_t), E, K, N), np_(s_p), "un-permuted tiled scales")
+    counts = [0, 33, 300, 129][:E] + [0] * max(0, E - 4)
+    rt, R_cap, cnt, off = _routing(counts, 11)
+    Aq, As = synth.random_mxfp8(R_cap, K, 12)
+    Aq, As = Aq.to(DEV), As.to(DEV)
+    y_t = ops.fc2_fwd(Aq, As, q_t, s_t, cnt, off, status=st, w_tiled=True)
+    y_p = ops.fc2_fwd(Aq, As, q_p, s_p, cnt, off, status=st)
+    torch.cuda.synchronize()
+    assert ops.read_status(st) == 0
+    R = rt.R_pad
+    assert torch.equal(y_t[:R], y_p[:R]), "FC2 on tiled vs plain weight scales"

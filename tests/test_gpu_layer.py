@@ -9,7 +9,7 @@ from grouped_gemm_glu_gb300 import lib as L
 from grouped_gemm_glu_gb300 import ops, synth
 from grouped_gemm_glu_gb300.layer import MoeLayer
 from oracle import moe_oracle as O
-from parity import assert_bf16_close, assert_chain_close, assert_exact, np_
+from parity import assert_bf16_close, assert_chain_close, assert_exact, np_, untile_weight_scales
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -66,7 +66,9 @@ def _check_stagewise(layer, rt):
     assert_bf16_close(np_(layer.dW2), O.bf16_round(dW2), "dW2 on the layer's operands")
     dW1 = O.grouped_wgrad(deq(layer.d_qc, layer.d_sc)[:, :Rp], deq(layer.x_qc, layer.x_sc)[:, :Rp], rt)
     assert_bf16_close(np_(layer.dW1), O.bf16_round(dW1), "dW1 on the layer's operands")
-    W1q = np.stack([deq(layer.W1q[e], layer.W1s[e]) for e in range(rt.E)])
+    W1s = (np_(layer.W1s_p) if layer.fc1_mxfp8 else
+           untile_weight_scales(np_(layer.W1s), rt.E, layer.N1, layer.H))
+    W1q = np.stack([O.mx_dequantize(np_(layer.W1q[e]), W1s[e]) for e in range(rt.E)])
     dX = O.grouped_gemm_rows(deq(layer.d_q, layer.d_s)[:Rp], W1q, rt)
     real = rt.tok_of >= 0
     assert_bf16_close(np_(layer.dX_perm)[:Rp][real], O.bf16_round(dX)[real], "dX on the layer's operands")
@@ -228,7 +230,7 @@ def test_layer_step_mxfp8_fc1():
         assert_exact(np_(layer.W1sr[e]), s_, "W1 rows scales")
         q, s_ = O.mx_quantize_cols(W1p[e])
         assert_exact(np_(layer.W1q[e]), q, "W1 columns codes")
-        assert_exact(np_(layer.W1s[e]), s_, "W1 columns scales")
+        assert_exact(np_(layer.W1s_p[e]), s_, "W1 columns scales")
     xp = O.permute(np_(inp["x"]), rt)
     xq, xs = O.mx_quantize_rows(xp)
     assert_exact(np_(layer.x_qr)[:Rp], xq, "x_perm rows codes")
