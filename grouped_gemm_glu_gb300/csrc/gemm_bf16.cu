@@ -29,7 +29,11 @@
 // Default (k_grouped_bf16_pair): clusters of 2 CTAs run 256 x 256 tiles with
 // tcgen05 cta_group::2 (M = 256 issued by the even CTA, each CTA holding 128
 // rows of A and half of B per stage, 6 stages); moe_set_cta_pairs(0) selects
-// k_grouped_bf16, one CTA per 128 x 256 tile with 4 stages.
+// k_grouped_bf16, one CTA per 128 x 256 tile with 4 stages.  The pair
+// kernel takes its tiles from an atomic counter in the call's workspace (the
+// leader's producer hands each tile to both CTAs through a 4-slot queue) and
+// computes an expert's thin last tile transposed (weights as M = 256, the
+// rows as N).
 // Every wait is bounded (MOE_ERR_TIMEOUT + early exit, never a trap).
 #include <cmath>
 
