@@ -897,8 +897,9 @@ extern "C" moe_status_t moe_grouped_fc2_fwd(const moe_in_t* A, const moe_in_t* W
   if (!A || !W || !A->data || !W->data || !counts || !offsets || !out) return MOE_ERR_ARG;
   if (E <= 0 || E > E_MAX || K <= 0 || (K % 32) || N <= 0 || (N % 32) || R_cap <= 0 || (R_cap % BM))
     return MOE_ERR_ARG;
-  // one operand type per MMA (an MXFP8 weight may carry pre-tiled scales)
-  const bool w_tiled = A->dtype == MOE_IN_MXFP8 && W->dtype == MOE_IN_MXFP8_TILED;
+  // one operand type per MMA (an MXFP8 or NVFP4 weight may carry pre-tiled scales)
+  const bool w_tiled = (A->dtype == MOE_IN_MXFP8 && W->dtype == MOE_IN_MXFP8_TILED) ||
+                       (A->dtype == MOE_IN_NVFP4 && W->dtype == MOE_IN_NVFP4_TILED);
   if (sm_margin < 0 || (A->dtype != W->dtype && !w_tiled)) return MOE_ERR_ARG;
   if (out_mode != MOE_OUT_BF16 && out_mode != MOE_OUT_MXFP8 && out_mode != MOE_OUT_NVFP4) return MOE_ERR_ARG;
   if (out->pre || out->row_dot || out->rht_amax) return MOE_ERR_ARG;
@@ -917,6 +918,7 @@ extern "C" moe_status_t moe_grouped_fc2_fwd(const moe_in_t* A, const moe_in_t* W
         (reinterpret_cast<uintptr_t>(A->scale) & 3) || (reinterpret_cast<uintptr_t>(W->scale) & 3) ||
         (reinterpret_cast<uintptr_t>(ws) & 255))
       return MOE_ERR_ARG;
+    if (w_tiled && (reinterpret_cast<uintptr_t>(W->scale) & 15)) return MOE_ERR_ARG;  // 16-byte bulk copies
     size_t a4, b4;
     fc2_ws_parts(E, K, N, R_cap, &a4, &b4, true);
     if (ws_bytes < a4 + b4) return MOE_ERR_ARG;
@@ -950,7 +952,8 @@ extern "C" moe_status_t moe_grouped_fc2_fwd(const moe_in_t* A, const moe_in_t* W
     a.As = A->scale;
     a.Bs = W->scale;
     a.sfa_t = static_cast<uint8_t*>(ws);
-    a.sfb_t = static_cast<uint8_t*>(ws) + a4;
+    a.sfb_t = w_tiled ? const_cast<uint8_t*>(W->scale) : static_cast<uint8_t*>(ws) + a4;
+    a.b_pretiled = w_tiled ? 1 : 0;
     a.out = out->y;
     a.status = status;
     a.wait_ns = g_wait_limit_ns.load();
@@ -960,7 +963,7 @@ extern "C" moe_status_t moe_grouped_fc2_fwd(const moe_in_t* A, const moe_in_t* W
     a.sg_b = W->global_scale;
     const long long mt_bound = (long long)R_cap / BM + E;
     const long long bound = mt_bound * a.n_tiles_n;
-    const long long sf_items = mt_bound * a.KB + (long long)E * 2 * a.n_tiles_n * a.KB;
+    const long long sf_items = mt_bound * a.KB + (w_tiled ? 0 : (long long)E * 2 * a.n_tiles_n * a.KB);
     return launch(tA, tB, nullptr, a, bound, sf_items, sm_margin, as_stream(stream), EPI_NV4);
   }
   if (A->dtype != MOE_IN_MXFP8) return MOE_ERR_ARG;

@@ -587,7 +587,10 @@ __global__ void __launch_bounds__(256) k_rht_amax_cols(const uint16_t* __restric
 //      or folds them into its amax (NC_RHT_AMAX);
 //   2. the buffer is refilled with the tile NC_STAGES steps ahead;
 //   3. each column's 64 code bytes leave as 4 x 16 bytes (8 columns per warp
-//      instruction) and its 8 scales as one 8-byte word.
+//      instruction) and its 8 scales as one 8-byte word, or (s_tiled, weight
+//      casts) the tile's scales as two 512-byte blocks in the order the
+//      block-scaled GEMM's tensor-core copies read them, so that its call
+//      has no weight scales to re-tile.
 // Only the blocks below rows_valid (R, or offsets[E] for the permuted
 // operands: a multiple of 32) are read into a result or stored; columns
 // past C arrive as zeros from TMA and are not stored.  R % 128 == 0.
@@ -611,7 +614,7 @@ __global__ void __launch_bounds__(NC_THREADS, NC_CTAS_PER_SM) k_nvfp4_cols_tma(c
                                                         const float* __restrict__ amax, uint32_t signs,
                                                         uint8_t* __restrict__ q, uint8_t* __restrict__ s,
                                                         float* __restrict__ s_global, float* __restrict__ amax_out,
-                                                        int32_t* status, uint64_t wait_ns) {
+                                                        int s_tiled, int32_t* status, uint64_t wait_ns) {
   extern __shared__ __align__(128) uint8_t nsm[];
   uint8_t* tin = nsm;
   uint8_t* tcode = nsm + NC_OFF_CODE;
@@ -726,13 +729,38 @@ __global__ void __launch_bounds__(NC_THREADS, NC_CTAS_PER_SM) k_nvfp4_cols_tma(c
           if (2 * part < nvalid)
             *reinterpret_cast<uint4*>(q + col * (R / 2) + r0 / 2 + part * 16) =
                 *reinterpret_cast<const uint4*>(tcode + cl * NC_CODE_ROW + part * 16);
-          if (part == 0) {
+          if (part == 0 && !s_tiled) {
             uint8_t* sd = s + col * (R / 16) + r0 / 16;
             if (nvalid == 8)
               *reinterpret_cast<uint2*>(sd) = *reinterpret_cast<const uint2*>(tscale + cl * 8);
             else
               for (int b = 0; b < nvalid; ++b) sd[b] = tscale[cl * 8 + b];
           }
+        }
+      }
+      if (s_tiled && warp == 0) {
+        // the tile's scales in the block-scaled GEMM's order (rows R = K,
+        // all valid): one 512-byte block per 64-row group of R, lane l
+        // writing bytes 16 l .. 16 l + 15, byte 16 l + 4 j + i = the scale
+        // of column 32 j + l of the 128-column group, sub-block i (column
+        // cl's scales 4 q .. 4 q + 3 are 32-bit word 2 cl + q of tscale)
+        const int nt = (C + 255) / 256, kgs = 4 * ((R + 255) / 256), gi = c0 / NC_COLS;
+        const uint32_t* ts = reinterpret_cast<const uint32_t*>(tscale);
+        uint8_t* base = s + ((size_t)g * nt + (gi >> 1)) * kgs * 1024 + (gi & 1) * 512;
+        // groups past R in the last k-block of 256 and the missing half of a
+        // last 256-column tile hold zero scales (their codes are zero too)
+        const bool r_tail = r0 + NC_ROWS == R && (R % 256) != 0;
+        const bool c_tail = (gi & 1) == 0 && c0 + NC_COLS >= C;
+        const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (q >= 2 && !r_tail) break;
+          uint8_t* dst = base + (size_t)(r0 / 64 + q) * 1024;
+          const uint4 v = q < 2 ? make_uint4(ts[2 * lane + q], ts[2 * (32 + lane) + q], ts[2 * (64 + lane) + q],
+                                             ts[2 * (96 + lane) + q])
+                                : zero;
+          reinterpret_cast<uint4*>(dst)[lane] = v;
+          if (c_tail) reinterpret_cast<uint4*>(dst + 512)[lane] = zero;
         }
       }
     }
@@ -1019,7 +1047,7 @@ extern "C" moe_status_t moe_amax_bf16(const moe_bf16* x, size_t n, float* amax, 
 template <int MODE>
 static moe_status_t launch_nvfp4_cols_tma(const moe_bf16* src, int G, int R, int C, const int32_t* offsets, int E,
                                           const float* amax, uint32_t signs, uint8_t* q, uint8_t* s, float* s_global,
-                                          float* amax_out, int32_t* status, cudaStream_t st) {
+                                          float* amax_out, int32_t* status, cudaStream_t st, int s_tiled = 0) {
   const size_t tiles = (size_t)G * ((R + NC_ROWS - 1) / NC_ROWS) * ((C + NC_COLS - 1) / NC_COLS);
   if (tiles > (size_t)INT32_MAX) return MOE_ERR_ARG;
   CUtensorMap tm;
@@ -1034,7 +1062,7 @@ static moe_status_t launch_nvfp4_cols_tma(const moe_bf16* src, int G, int R, int
   size_t grid = tiles;
   if (grid > (size_t)sm_count() * occ) grid = (size_t)sm_count() * occ;
   k_nvfp4_cols_tma<MODE><<<(int)(grid < 1 ? 1 : grid), NC_THREADS, NC_SMEM, st>>>(
-      tm, G, R, C, offsets, E, amax, signs, q, s, s_global, amax_out, status, g_wait_limit_ns.load());
+      tm, G, R, C, offsets, E, amax, signs, q, s, s_global, amax_out, s_tiled, status, g_wait_limit_ns.load());
   count_launch();
   return launch_status();
 }
@@ -1067,6 +1095,20 @@ extern "C" moe_status_t moe_nvfp4_cast_cols(const moe_bf16* src, int G, int R, i
     k_nvfp4_cast_cols<1, 1><<<grid_for(units, 256), 256, 0, st>>>(src16, G, R, C, amax, q, s, s_global);
   count_launch();
   return launch_status();
+}
+
+extern "C" size_t moe_nvfp4_tiled_scale_bytes(int G, int R, int C) {
+  if (G <= 0 || R <= 0 || C <= 0) return 0;
+  return (size_t)G * ((C + 255) / 256) * ((R + 255) / 256) * 4096;
+}
+
+extern "C" moe_status_t moe_nvfp4_cast_cols_tiled(const moe_bf16* src, int G, int R, int C, const float* amax,
+                                                  uint8_t* q, uint8_t* s, float* s_global, int32_t* status,
+                                                  moe_stream_t stream) {
+  if (!src || !amax || !q || !s || !s_global || G <= 0 || R <= 0 || C <= 0) return MOE_ERR_ARG;
+  if (!nvfp4_cols_staged(src, R, C) || !aligned16(q) || !aligned16(s)) return MOE_ERR_ARG;
+  return launch_nvfp4_cols_tma<NC_CAST>(src, G, R, C, nullptr, 0, amax, 0u, q, s, s_global, nullptr, status,
+                                        as_stream(stream), 1);
 }
 
 extern "C" moe_status_t moe_rht_amax_cols(const moe_bf16* src, int R_cap, int C, const int32_t* offsets, int E,

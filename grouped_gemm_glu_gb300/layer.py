@@ -138,11 +138,18 @@ class MoeLayer:
             self.a_y, self.a_amax = z(R_cap, F), z(1, dt=f32)
             self.a_q4, self.a_s4, self.a_sg = z(R_cap, F // 2, dt=u8), z(R_cap, F // 16, dt=u8), z(1, dt=f32)
             self.w2_amax = z(1, dt=f32)
-            self.W2q4, self.W2s4, self.w2_sg = z(E, H, F // 2, dt=u8), z(E, H, F // 16, dt=u8), z(1, dt=f32)
+            # weight casts write their scales in the tensor-core order when the
+            # staged cast takes the shapes (F % 128 == 0, H % 8 == 0)
+            self.w4_tiled = F % 128 == 0 and H % 8 == 0
+            w4s = (lambda R_, C_: z(lib.moe_nvfp4_tiled_scale_bytes(E, R_, C_), dt=u8)) if self.w4_tiled else \
+                (lambda R_, C_: z(E, C_, R_ // 16, dt=u8))
+            self.cast_w4 = lib.moe_nvfp4_cast_cols_tiled if self.w4_tiled else lib.moe_nvfp4_cast_cols
+            self.W2q4, self.W2s4, self.w2_sg = z(E, H, F // 2, dt=u8), w4s(F, H), z(1, dt=f32)
             self.fc1_out4 = L.ActOut(None, None, None, None, self.a_y.data_ptr(), self.a_amax.data_ptr(),
                                      self.pre.data_ptr())
             self.fc2_a4 = L.in_operand(self.a_q4.data_ptr(), self.a_s4.data_ptr(), self.a_sg.data_ptr())
-            self.fc2_w4 = L.in_operand(self.W2q4.data_ptr(), self.W2s4.data_ptr(), self.w2_sg.data_ptr())
+            self.fc2_w4 = L.in_operand(self.W2q4.data_ptr(), self.W2s4.data_ptr(), self.w2_sg.data_ptr(),
+                                       tiled=self.w4_tiled)
             # backward: bf16 dFC1 with its amaxes; NVFP4 rows of dFC1 and W1 (along 2F) for dX;
             # rotated column-wise NVFP4 of dFC1, x, a and dY for the weight gradients
             self.rht_signs = int(rht_signs) & 0xFFFF
@@ -150,7 +157,7 @@ class MoeLayer:
             self.d_y, self.d_amax, self.d_rht = z(R_cap, N1), one(), one()
             self.d_q4, self.d_s4, self.d_sg = z(R_cap, N1 // 2, dt=u8), z(R_cap, N1 // 16, dt=u8), one()
             self.w1_amax, self.w1_sg = one(), one()
-            self.W1q4, self.W1s4 = z(E, H, N1 // 2, dt=u8), z(E, H, N1 // 16, dt=u8)
+            self.W1q4, self.W1s4 = z(E, H, N1 // 2, dt=u8), w4s(N1, H)
             rot = lambda C_: (z(C_, R_cap // 2, dt=u8), z(C_, R_cap // 16, dt=u8), one(), one())
             self.d_rq, self.d_rs, self.d_rsg, _ = rot(N1)
             self.x_rq, self.x_rs, self.x_rsg, self.x_ramax = rot(H)
@@ -159,7 +166,8 @@ class MoeLayer:
             self.bwd_out4 = L.ActOut(None, None, None, None, self.d_y.data_ptr(), self.d_amax.data_ptr(), None,
                                      None, self.d_rht.data_ptr(), self.rht_signs)
             self.dx_a4 = L.in_operand(self.d_q4.data_ptr(), self.d_s4.data_ptr(), self.d_sg.data_ptr())
-            self.dx_w4 = L.in_operand(self.W1q4.data_ptr(), self.W1s4.data_ptr(), self.w1_sg.data_ptr())
+            self.dx_w4 = L.in_operand(self.W1q4.data_ptr(), self.W1s4.data_ptr(), self.w1_sg.data_ptr(),
+                                      tiled=self.w4_tiled)
         # operands and outputs of the two block-scaled M-grouped GEMMs
         self.fc2_a = L.in_operand(self.a_q.data_ptr(), self.a_s.data_ptr())
         self.fc2_w = L.in_operand(self.W2q.data_ptr(), self.W2s.data_ptr(), tiled=True)
@@ -247,7 +255,7 @@ class MoeLayer:
                 _p(self.a_y), _p(self.a_amax), _p(self.counts), _p(self.offsets), E, F, R, _p(self.a_q4),
                 _p(self.a_s4), _p(self.a_sg), s)),
             ("amax_w2", lambda: lib.moe_amax_bf16(_p(self.W2), self.W2.numel(), _p(self.w2_amax), s)),
-            ("quant_w2_nvfp4", lambda: lib.moe_nvfp4_cast_cols(
+            ("quant_w2_nvfp4", lambda: self.cast_w4(
                 _p(self.W2), E, F, H, _p(self.w2_amax), _p(self.W2q4), _p(self.W2s4), _p(self.w2_sg), st, s)),
             ("fc2_nvfp4", lambda: lib.moe_grouped_fc2_fwd(
                 C.byref(self.fc2_a4), C.byref(self.fc2_w4), _p(self.counts), _p(self.offsets), E, F, H, R,
@@ -317,7 +325,7 @@ class MoeLayer:
             ("quant_d_nvfp4", lambda: lib.moe_nvfp4_cast(
                 _p(self.d_y), _p(self.d_amax), cnt, off, E, N1, R, _p(self.d_q4), _p(self.d_s4), _p(self.d_sg), s)),
             ("amax_w1", lambda: lib.moe_amax_bf16(_p(self.W1p), self.W1p.numel(), _p(self.w1_amax), s)),
-            ("quant_w1_nvfp4", lambda: lib.moe_nvfp4_cast_cols(
+            ("quant_w1_nvfp4", lambda: self.cast_w4(
                 _p(self.W1p), E, N1, H, _p(self.w1_amax), _p(self.W1q4), _p(self.W1s4), _p(self.w1_sg), st, s)),
             ("dx_nvfp4", lambda: lib.moe_grouped_fc2_fwd(
                 C.byref(self.dx_a4), C.byref(self.dx_w4), cnt, off, E, N1, H, R, L.OUT_BF16, C.byref(self.dx_out),

@@ -31,7 +31,7 @@ class ActOut(C.Structure):
                 ("rht_amax", C.c_void_p), ("rht_signs", C.c_uint32)]
 
 
-IN_BF16, IN_MXFP8, IN_NVFP4, IN_MXFP8_TILED = 0, 1, 2, 3
+IN_BF16, IN_MXFP8, IN_NVFP4, IN_MXFP8_TILED, IN_NVFP4_TILED = 0, 1, 2, 3, 4
 
 
 class InT(C.Structure):
@@ -43,12 +43,12 @@ def in_operand(data_ptr: int, scale_ptr: int | None = None, global_scale_ptr: in
     """A GEMM operand: bf16 when scale_ptr is None, MXFP8 codes + scales
     (tiled: scales already in the tensor-core order, a weight cast with
     col = 2), or NVFP4 codes + block scales + per-tensor scale when
-    global_scale_ptr is set."""
+    global_scale_ptr is set (tiled: a weight from moe_nvfp4_cast_cols_tiled)."""
     if scale_ptr is None:
         return InT(IN_BF16, data_ptr, None, None)
     if global_scale_ptr is None:
         return InT(IN_MXFP8_TILED if tiled else IN_MXFP8, data_ptr, scale_ptr, None)
-    return InT(IN_NVFP4, data_ptr, scale_ptr, global_scale_ptr)
+    return InT(IN_NVFP4_TILED if tiled else IN_NVFP4, data_ptr, scale_ptr, global_scale_ptr)
 
 
 def glu_params(act: str = "swiglu", alpha: float = 1.0, up_offset: float = 0.0,
@@ -90,6 +90,8 @@ _SIGS = {
     "moe_nvfp4_rht_cast_cols": [P, I, I, P, I, P, C.c_uint32, P, P, P, P, P],
     "moe_grouped_wgrad_nvfp4": [P, P, P, P, P, P, P, P, I, I, I, I, P, I, P, SZ, I, P, P],
     "moe_nvfp4_cast_cols": [P, I, I, I, P, P, P, P, P, P],
+    "moe_nvfp4_cast_cols_tiled": [P, I, I, I, P, P, P, P, P, P],
+    "moe_nvfp4_tiled_scale_bytes": ([I, I, I], SZ),
     "moe_dglu_act": [P, P, P, P, I, I, I, C.POINTER(GluParams), P, P],
     "moe_route_permute_noalloc": [P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P],
     "moe_route_noalloc_max_scratch_bytes": ([], SZ),

@@ -297,10 +297,12 @@ def fc2_fwd(Aq, As, Wq, Ws, counts, offsets, sm_margin: int = 0, status=None, ou
     return o["y"] if out_mode == L.OUT_BF16 else o
 
 
-def fc2_fwd_nvfp4(Aq, As, sgA, Wq, Ws, sgW, counts, offsets, sm_margin: int = 0, status=None, out=None):
+def fc2_fwd_nvfp4(Aq, As, sgA, Wq, Ws, sgW, counts, offsets, sm_margin: int = 0, status=None, out=None,
+                  w_tiled: bool = False):
     """GroupGemm on NVFP4 operands: y [R_cap, N] bf16 = A . W[e]^T with
     A = packed E2M1 [R_cap, K/2] + E4M3 scales [R_cap, K/16] + per-tensor
-    scale sgA (device float [1]), W [E, N, K/2] + [E, N, K/16] + sgW."""
+    scale sgA (device float [1]), W [E, N, K/2] + [E, N, K/16] + sgW
+    (w_tiled: Ws in the tensor-core order, nvfp4_cast_cols(..., tiled=True))."""
     lib = L.load()
     dev = _dev(Aq)
     R_cap, K2 = Aq.shape
@@ -309,7 +311,7 @@ def fc2_fwd_nvfp4(Aq, As, sgA, Wq, Ws, sgW, counts, offsets, sm_margin: int = 0,
     y = out if out is not None else torch.empty(R_cap, N, dtype=torch.bfloat16, device=dev)
     st = status if status is not None else new_status(dev)
     a_in = L.in_operand(Aq.data_ptr(), As.data_ptr(), sgA.data_ptr())
-    w_in = L.in_operand(Wq.data_ptr(), Ws.data_ptr(), sgW.data_ptr())
+    w_in = L.in_operand(Wq.data_ptr(), Ws.data_ptr(), sgW.data_ptr(), tiled=w_tiled)
     ws_bytes = lib.moe_grouped_fc2_workspace_size(E, K, N, R_cap)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     ao = _act_out(y=y)
@@ -327,18 +329,25 @@ def amax_bf16(x):
     return a
 
 
-def nvfp4_cast_cols(src, amax, status=None):
+def nvfp4_cast_cols(src, amax, status=None, tiled: bool = False, out=None):
     """Column-wise NVFP4 of src [G, R, C] (or [R, C]) bf16: (q [G, C, R/2],
-    s [G, C, R/16], s_global [1])."""
+    s [G, C, R/16], s_global [1]); tiled: s in the tensor-core order of a
+    GEMM weight operand (flat uint8 [moe_nvfp4_tiled_scale_bytes]).  out:
+    optional (q, s, s_global) to write into."""
     lib = L.load()
     dev = _dev(src)
     s3 = src if src.dim() == 3 else src.unsqueeze(0)
     G, R, Cc = s3.shape
-    q = torch.empty(G, Cc, R // 2, dtype=torch.uint8, device=dev)
-    s = torch.empty(G, Cc, R // 16, dtype=torch.uint8, device=dev)
-    sg = torch.empty(1, dtype=torch.float32, device=dev)
-    L.check(lib.moe_nvfp4_cast_cols(_p(s3), G, R, Cc, _p(amax), _p(q), _p(s), _p(sg), _p(status), _s()),
-            "moe_nvfp4_cast_cols")
+    if out is not None:
+        q, s, sg = out
+    else:
+        q = torch.empty(G, Cc, R // 2, dtype=torch.uint8, device=dev)
+        s = (torch.empty(lib.moe_nvfp4_tiled_scale_bytes(G, R, Cc), dtype=torch.uint8, device=dev) if tiled
+             else torch.empty(G, Cc, R // 16, dtype=torch.uint8, device=dev))
+        sg = torch.empty(1, dtype=torch.float32, device=dev)
+    fn = lib.moe_nvfp4_cast_cols_tiled if tiled else lib.moe_nvfp4_cast_cols
+    L.check(fn(_p(s3), G, R, Cc, _p(amax), _p(q), _p(s), _p(sg), _p(status), _s()),
+            "moe_nvfp4_cast_cols_tiled" if tiled else "moe_nvfp4_cast_cols")
     return q, s, sg
 
 

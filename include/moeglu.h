@@ -133,10 +133,12 @@ typedef enum {
   MOE_IN_NVFP4 = 2,       /* packed E2M1 codes (element 2i in the low nibble of byte i) with E4M3
                              scales, one per 16 elements along K, and one fp32 per-tensor scale
                              s_g: value = e2m1 * s_b / s_g (moe_nvfp4_cast, moe_nvfp4_cast_cols) */
-  MOE_IN_MXFP8_TILED = 3  /* an MXFP8 weight (the W operand of moe_grouped_fc2_fwd, next to an
+  MOE_IN_MXFP8_TILED = 3, /* an MXFP8 weight (the W operand of moe_grouped_fc2_fwd, next to an
                              MXFP8 A) whose scales are already in the order the tensor cores copy
                              them, as written by moe_quantize_mxfp8 with col = 2: the call skips
                              their re-tiling.  Scales 16-byte aligned. */
+  MOE_IN_NVFP4_TILED = 4  /* the same for an NVFP4 weight next to an NVFP4 A: scales as written by
+                             moe_nvfp4_cast_cols_tiled.  Scales 16-byte aligned. */
 } moe_in_dtype_t;
 
 typedef struct {
@@ -304,7 +306,9 @@ MOE_API size_t moe_grouped_fc2_workspace_size(int E, int K, int N, int R_cap);
  * Serves FC2 (K = F, N = H) and the data-gradient GEMM dX = dFC1 . W1p
  * (K = N1, N = H).
  * Operands: A [R_cap][K], W [E][N][K] (K contiguous in both), the same
- * dtype for both (the tensor cores take one operand type per MMA):
+ * dtype for both (the tensor cores take one operand type per MMA; a W of
+ * MOE_IN_MXFP8_TILED / MOE_IN_NVFP4_TILED counts as MXFP8 / NVFP4 and
+ * carries its scales in the tensor-core order):
  *   MOE_IN_MXFP8: E4M3 codes, scale = E8M0 [R_cap][K/32] / [E][N][K/32]
  *                 (4-byte aligned); block-scaled MMA (kind::mxf8f6f4);
  *                 ws = moe_grouped_fc2_workspace_size() bytes, 256-byte
@@ -465,6 +469,23 @@ MOE_API moe_status_t moe_amax_bf16(const moe_bf16* x, size_t n, float* amax, moe
 MOE_API moe_status_t moe_nvfp4_cast_cols(const moe_bf16* src, int G, int R, int C, const float* amax,
                                          uint8_t* q, uint8_t* s, float* s_global, int32_t* status,
                                          moe_stream_t stream);
+
+/* moe_nvfp4_cast_cols with the scales written in the order the block-scaled
+ * GEMM's tensor-core copies read them when the result is its N x K weight
+ * operand (N = C, K = R; W of moe_grouped_fc2_fwd as MOE_IN_NVFP4_TILED), so
+ * that the GEMM call re-tiles no weight scales:
+ * s [G][ceil(C/256)][4 ceil(R/256)][2][512 bytes]; the 512 bytes of (256-
+ * column tile n, 64-row group k of R, 128-column half h) hold at byte
+ * 16 l + 4 j + i the scale of column 256 n + 128 h + 32 j + l, rows
+ * 64 k + 16 i .. + 15 of R.  Groups past R and columns past C hold zero
+ * scales.  Codes and scale values equal moe_nvfp4_cast_cols's.  Staged form
+ * only: src and q 16-byte aligned, s 16-byte aligned, C % 8 == 0,
+ * R % 128 == 0, else MOE_ERR_ARG.  s holds moe_nvfp4_tiled_scale_bytes(G, R,
+ * C) bytes. */
+MOE_API moe_status_t moe_nvfp4_cast_cols_tiled(const moe_bf16* src, int G, int R, int C, const float* amax,
+                                               uint8_t* q, uint8_t* s, float* s_global, int32_t* status,
+                                               moe_stream_t stream);
+MOE_API size_t moe_nvfp4_tiled_scale_bytes(int G, int R, int C);
 
 /* NVFP4 backward operands ([MoE-Fusion] "Fusing MXFP8 and NVFP4
  * quantisation": the weight-gradient GEMM reads the transposed tensors after

@@ -122,3 +122,25 @@ def untile_weight_scales(s_tiled, G: int, R: int, C: int) -> np.ndarray:
     t = np.asarray(s_tiled, dtype=np.uint8).reshape(G, nt, kbs, 2, 32, 4, 4)   # g, ntile, kb, half, l, j, i
     t = t.transpose(0, 1, 3, 5, 4, 2, 6).reshape(G, nt * 256, kbs * 4)          # g, c, sub-block
     return t[:, :C, : R // 32]
+
+
+def untile_nvfp4_weight_scales(s_tiled, G: int, R: int, C: int) -> np.ndarray:
+    """The plain column-wise NVFP4 scale layout [G][C][R/16] of scales written
+    in the tensor-core order (moe_nvfp4_cast_cols_tiled): the 512 bytes of
+    (256-column tile, 64-row group of R, 128-column half) hold at byte
+    16 l + 4 j + i the scale of column 32 j + l of the half, 16-row sub-block
+    i of the group."""
+    nt, kgs = (C + 255) // 256, 4 * ((R + 255) // 256)
+    t = np.asarray(s_tiled, dtype=np.uint8).reshape(G, nt, kgs, 2, 32, 4, 4)   # g, ntile, group, half, l, j, i
+    t = t.transpose(0, 1, 3, 5, 4, 2, 6).reshape(G, nt * 256, kgs * 4)          # g, c, sub-block
+    return t[:, :C, : R // 16]
+
+
+def nvfp4_tiled_pad(s_tiled, G: int, R: int, C: int) -> np.ndarray:
+    """The scale bytes of a tiled NVFP4 weight layout that lie past R or C
+    (groups after the last row, columns after the last one), which the cast
+    writes as zeros."""
+    nt, kgs = (C + 255) // 256, 4 * ((R + 255) // 256)
+    t = np.asarray(s_tiled, dtype=np.uint8).reshape(G, nt, kgs, 2, 32, 4, 4)
+    t = t.transpose(0, 1, 3, 5, 4, 2, 6).reshape(G, nt * 256, kgs * 4)
+    return np.concatenate([t[:, C:, :].ravel(), t[:, :C, R // 16:].ravel()])

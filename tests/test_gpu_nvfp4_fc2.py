@@ -10,7 +10,8 @@ import torch
 from grouped_gemm_glu_gb300 import lib as L
 from grouped_gemm_glu_gb300 import ops, synth
 from oracle import moe_oracle as O
-from parity import assert_bf16_close, assert_chain_close, assert_exact, np_
+from parity import (assert_bf16_close, assert_chain_close, assert_exact, np_, nvfp4_tiled_pad,
+                    untile_nvfp4_weight_scales)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -78,6 +79,62 @@ def test_nvfp4_weight_cast_and_amax_bit_exact(R, C):
         qr, sr = O.nvfp4_quantize_cols(Wn[e], sg_ref)
         assert_exact(np_(q[e]), qr, f"codes expert {e}")
         assert_exact(np_(s[e]), sr, f"scales expert {e}")
+
+
+@pytest.mark.parametrize("R,C", [(1536, 512), (384, 264), (640, 392)])
+def test_nvfp4_tiled_weight_scales(R, C):
+    """moe_nvfp4_cast_cols_tiled: the same codes and (after un-permuting the
+    tensor-core order) the same scales as the plain cast, bit for bit, with
+    zero scales past R and C in a buffer that started as 0xAA.  R = 384 and
+    640 end in half a 256-row k-block; C = 264 ends in the first half of a
+    256-column tile (its second half is written as zeros), C = 392 inside a
+    second half."""
+    E = 3
+    rng = np.random.default_rng(R + C)
+    W = synth._bf16(rng.standard_normal((E, R, C), dtype=np.float32) * np.exp2(rng.integers(-4, 4, (E, 1, C))))
+    Wd = W.to(DEV)
+    am = ops.amax_bf16(Wd)
+    q0, s0, sg0 = ops.nvfp4_cast_cols(Wd, am)
+    lib = L.load()
+    q = torch.full((E, C, R // 2), 0xAA, dtype=torch.uint8, device=DEV)
+    s = torch.full((lib.moe_nvfp4_tiled_scale_bytes(E, R, C),), 0xAA, dtype=torch.uint8, device=DEV)
+    sg = torch.zeros(1, dtype=torch.float32, device=DEV)
+    st = ops.new_status(DEV)
+    ops.nvfp4_cast_cols(Wd, am, status=st, tiled=True, out=(q, s, sg))
+    torch.cuda.synchronize()
+    assert ops.read_status(st) == 0
+    assert float(sg.item()) == float(sg0.item())
+    assert torch.equal(q, q0), "codes"
+    assert_exact(untile_nvfp4_weight_scales(np_(s), E, R, C), np_(s0), "scales")
+    assert not nvfp4_tiled_pad(np_(s), E, R, C).any(), "pad scales"
+
+
+@pytest.mark.parametrize("K,N", [(1536, 512), (384, 288)])
+def test_nvfp4_fc2_tiled_weight_bit_identical(K, N):
+    """FC2 on an NVFP4 weight cast with tiled scales (MOE_IN_NVFP4_TILED, no
+    weight-scale re-tiling in the call) returns the same bits as on the plain
+    cast of the same weight.  K = 384 ends in half a k-block, N = 288 in a
+    partial column tile whose missing half holds zero scales."""
+    counts = [0, 1, 33, 128, 129, 300]
+    E = len(counts)
+    rt, R_cap, cnt, off = _routing(counts, 5)
+    Aq, As, sgA = _nvfp4_operand(R_cap, K, 6)
+    rng = np.random.default_rng(7)
+    W = synth._bf16(rng.standard_normal((E, K, N), dtype=np.float32) / np.sqrt(K)).to(DEV)  # [E][K][N]
+    am = ops.amax_bf16(W)
+    wq, ws, sgw = ops.nvfp4_cast_cols(W, am)
+    wq_t, ws_t, sgw_t = ops.nvfp4_cast_cols(W, am, tiled=True)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    sga = torch.tensor([float(sgA)], device=DEV)
+    st = ops.new_status(DEV)
+    y0 = ops.fc2_fwd_nvfp4(t(Aq), t(As), sga, wq, ws, sgw, cnt, off, status=st)
+    y1 = ops.fc2_fwd_nvfp4(t(Aq), t(As), sga, wq_t, ws_t, sgw_t, cnt, off, status=st, w_tiled=True)
+    torch.cuda.synchronize()
+    assert ops.read_status(st) == 0
+    Rp = rt.R_pad
+    assert torch.equal(y0[:Rp].view(torch.int16), y1[:Rp].view(torch.int16))
+    ref = O.grouped_gemm_nvfp4(Aq[:Rp], As[:Rp], sgA, np_(wq), np_(ws), float(sgw.item()), rt)
+    assert_bf16_close(np_(y1)[:Rp], O.bf16_round(ref), f"nvfp4 fc2 tiled weight K={K} N={N}")
 
 
 @pytest.mark.parametrize("act", ["geglu", "srelu"])
@@ -188,9 +245,12 @@ def test_layer_nvfp4_step_and_graph():
     assert float(layer.w1_sg.item()) == float(s1)
     c1 = [O.nvfp4_quantize_cols(W1p[e], s1) for e in range(w.E)]
     assert_exact(np_(layer.W1q4), np.stack([c[0] for c in c1]), "W1 NVFP4 codes (along 2F)")
-    assert_exact(np_(layer.W1s4), np.stack([c[1] for c in c1]), "W1 NVFP4 scales")
+    W1s4 = np_(layer.W1s4)
+    if layer.w4_tiled:  # scales in the tensor-core order: un-permute them
+        W1s4 = untile_nvfp4_weight_scales(W1s4, w.E, W1p.shape[1], W1p.shape[2])
+    assert_exact(W1s4, np.stack([c[1] for c in c1]), "W1 NVFP4 scales")
     dX = O.grouped_gemm_nvfp4(np_(layer.d_q4)[:Rp], np_(layer.d_s4)[:Rp], float(layer.d_sg.item()),
-                              np_(layer.W1q4), np_(layer.W1s4), float(layer.w1_sg.item()), rt)
+                              np_(layer.W1q4), W1s4, float(layer.w1_sg.item()), rt)
     assert_bf16_close(np_(layer.dX_perm)[:Rp], O.bf16_round(dX), "NVFP4 dX on the layer's operands")
     dx = O.permute_bwd(np_(layer.dX_perm)[:Rp], rt.row_of, w.T, w.k)
     assert_bf16_close(np_(layer.dx), O.bf16_round(dx), "dx")
