@@ -587,7 +587,7 @@ __global__ void __launch_bounds__(256) k_rht_amax_cols(const uint16_t* __restric
 //      or folds them into its amax (NC_RHT_AMAX);
 //   2. the buffer is refilled with the tile NC_STAGES steps ahead;
 //   3. each column's 64 code bytes leave as 4 x 16 bytes (8 columns per warp
-//      instruction) and its 8 scales as one 8-byte word, or (s_tiled, weight
+//      instruction) and its 8 scales as one 8-byte word, or (TILED, weight
 //      casts) the tile's scales as two 512-byte blocks in the order the
 //      block-scaled GEMM's tensor-core copies read them, so that its call
 //      has no weight scales to re-tile.
@@ -608,13 +608,13 @@ constexpr int NC_OFF_MISC = NC_OFF_BARS + NC_STAGES * 8;  // abort flag
 constexpr int NC_OFF_TAB = NC_OFF_MISC + 16;               // float [128]: nvfp4_inv_table
 constexpr int NC_SMEM = NC_OFF_TAB + 128 * 4;
 
-template <int MODE>
+template <int MODE, bool TILED = false>
 __global__ void __launch_bounds__(NC_THREADS, NC_CTAS_PER_SM) k_nvfp4_cols_tma(const __grid_constant__ CUtensorMap tm, int G, int R, int C,
                                                         const int32_t* __restrict__ offsets, int E,
                                                         const float* __restrict__ amax, uint32_t signs,
                                                         uint8_t* __restrict__ q, uint8_t* __restrict__ s,
                                                         float* __restrict__ s_global, float* __restrict__ amax_out,
-                                                        int s_tiled, int32_t* status, uint64_t wait_ns) {
+                                                        int32_t* status, uint64_t wait_ns) {
   extern __shared__ __align__(128) uint8_t nsm[];
   uint8_t* tin = nsm;
   uint8_t* tcode = nsm + NC_OFF_CODE;
@@ -729,7 +729,7 @@ __global__ void __launch_bounds__(NC_THREADS, NC_CTAS_PER_SM) k_nvfp4_cols_tma(c
           if (2 * part < nvalid)
             *reinterpret_cast<uint4*>(q + col * (R / 2) + r0 / 2 + part * 16) =
                 *reinterpret_cast<const uint4*>(tcode + cl * NC_CODE_ROW + part * 16);
-          if (part == 0 && !s_tiled) {
+          if (part == 0 && !TILED) {
             uint8_t* sd = s + col * (R / 16) + r0 / 16;
             if (nvalid == 8)
               *reinterpret_cast<uint2*>(sd) = *reinterpret_cast<const uint2*>(tscale + cl * 8);
@@ -738,7 +738,7 @@ __global__ void __launch_bounds__(NC_THREADS, NC_CTAS_PER_SM) k_nvfp4_cols_tma(c
           }
         }
       }
-      if (s_tiled && warp == 0) {
+      if (TILED && warp == 0) {
         // the tile's scales in the block-scaled GEMM's order (rows R = K,
         // all valid): one 512-byte block per 64-row group of R, lane l
         // writing bytes 16 l .. 16 l + 15, byte 16 l + 4 j + i = the scale
@@ -783,7 +783,7 @@ __global__ void __launch_bounds__(NC_THREADS, NC_CTAS_PER_SM) k_nvfp4_cols_tma(c
 
 // max |x| over a bf16 tensor of n8 16-byte words (x 16-byte aligned) into
 // *amax as ordered float bits (the caller's call zeroes it first).
-__global__ void __launch_bounds__(256) k_amax_bf16(const uint4* __restrict__ x, size_t n8, float* __restrict__ amax) {
+__global__ void __launch_bounds__(256, 1) k_amax_bf16(const uint4* __restrict__ x, size_t n8, float* __restrict__ amax) {
   uint32_t m = 0;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
     const uint4 w = __ldg(x + i);
@@ -1044,10 +1044,10 @@ extern "C" moe_status_t moe_amax_bf16(const moe_bf16* x, size_t n, float* amax, 
   return launch_status();
 }
 
-template <int MODE>
+template <int MODE, bool TILED = false>
 static moe_status_t launch_nvfp4_cols_tma(const moe_bf16* src, int G, int R, int C, const int32_t* offsets, int E,
                                           const float* amax, uint32_t signs, uint8_t* q, uint8_t* s, float* s_global,
-                                          float* amax_out, int32_t* status, cudaStream_t st, int s_tiled = 0) {
+                                          float* amax_out, int32_t* status, cudaStream_t st) {
   const size_t tiles = (size_t)G * ((R + NC_ROWS - 1) / NC_ROWS) * ((C + NC_COLS - 1) / NC_COLS);
   if (tiles > (size_t)INT32_MAX) return MOE_ERR_ARG;
   CUtensorMap tm;
@@ -1056,13 +1056,13 @@ static moe_status_t launch_nvfp4_cols_tma(const moe_bf16* src, int G, int R, int
   const uint32_t box[3] = {NC_COLS, NC_ROWS, 1};
   if (!encode_tmap(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, src, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
     return MOE_ERR_CUDA;
-  const void* fn = (const void*)k_nvfp4_cols_tma<MODE>;
+  const void* fn = (const void*)k_nvfp4_cols_tma<MODE, TILED>;
   if (!set_smem_limit(fn, NC_SMEM)) return MOE_ERR_CUDA;
   const int occ = max(1, max_active_blocks(fn, NC_THREADS, NC_SMEM));
   size_t grid = tiles;
   if (grid > (size_t)sm_count() * occ) grid = (size_t)sm_count() * occ;
-  k_nvfp4_cols_tma<MODE><<<(int)(grid < 1 ? 1 : grid), NC_THREADS, NC_SMEM, st>>>(
-      tm, G, R, C, offsets, E, amax, signs, q, s, s_global, amax_out, s_tiled, status, g_wait_limit_ns.load());
+  k_nvfp4_cols_tma<MODE, TILED><<<(int)(grid < 1 ? 1 : grid), NC_THREADS, NC_SMEM, st>>>(
+      tm, G, R, C, offsets, E, amax, signs, q, s, s_global, amax_out, status, g_wait_limit_ns.load());
   count_launch();
   return launch_status();
 }
@@ -1107,8 +1107,8 @@ extern "C" moe_status_t moe_nvfp4_cast_cols_tiled(const moe_bf16* src, int G, in
                                                   moe_stream_t stream) {
   if (!src || !amax || !q || !s || !s_global || G <= 0 || R <= 0 || C <= 0) return MOE_ERR_ARG;
   if (!nvfp4_cols_staged(src, R, C) || !aligned16(q) || !aligned16(s)) return MOE_ERR_ARG;
-  return launch_nvfp4_cols_tma<NC_CAST>(src, G, R, C, nullptr, 0, amax, 0u, q, s, s_global, nullptr, status,
-                                        as_stream(stream), 1);
+  return launch_nvfp4_cols_tma<NC_CAST, true>(src, G, R, C, nullptr, 0, amax, 0u, q, s, s_global, nullptr, status,
+                                              as_stream(stream));
 }
 
 extern "C" moe_status_t moe_rht_amax_cols(const moe_bf16* src, int R_cap, int C, const int32_t* offsets, int E,

@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS) k_route_scatter(
 
 // One warp per permuted row r < offsets[E]: a real row copies x[tok_of[r]],
 // a pad row is zero-filled and gets tok_of = -1, prob_perm = 0.
-__global__ void __launch_bounds__(256) k_permute_gather(const uint4* __restrict__ x, int H8, int E,
+__global__ void __launch_bounds__(256, 1) k_permute_gather(const uint4* __restrict__ x, int H8, int E,
                                                         const int32_t* __restrict__ counts,
                                                         const int32_t* __restrict__ offsets,
                                                         const int32_t* __restrict__ overflow,
@@ -452,7 +452,7 @@ __global__ void __launch_bounds__(QF_THREADS) k_combine_bwd_qcol(
 // out[t] = bf16(sum_j p[t][j] * y_perm[row_of[t*k+j]]) in fp32, j ascending.
 // Work items are (token, 8-element vector) pairs, consecutive threads on
 // consecutive vectors of one row.
-__global__ void __launch_bounds__(256) k_unpermute_combine(const uint4* __restrict__ y, const int32_t* __restrict__ row_of,
+__global__ void __launch_bounds__(256, 1) k_unpermute_combine(const uint4* __restrict__ y, const int32_t* __restrict__ row_of,
                                                            const float* __restrict__ prob, int T, int H8, int k,
                                                            uint4* __restrict__ out) {
   const size_t total = (size_t)T * H8;
@@ -484,9 +484,12 @@ __global__ void __launch_bounds__(256) k_unpermute_combine(const uint4* __restri
 // chunks).  The token's row indices and weights arrive as 16-byte vector
 // loads, and each slot's NV row loads are issued together: NV x 16 bytes in
 // flight per thread at a modest register count.  Same arithmetic and order
-// as above.
-template <int KV, int NV>
-__global__ void __launch_bounds__(256) k_unpermute_combine_vec(const uint4* __restrict__ y,
+// as above.  WP: with weights (combine); without (permute backward, every
+// weight 1) is its own instantiation, since a run-time test of prob in the
+// loop cost 20% (the row loads were scheduled less eagerly).  The bound of
+// one CTA per SM leaves ptxas free to schedule the loads for latency.
+template <int KV, int NV, bool WP>
+__global__ void __launch_bounds__(256, 1) k_unpermute_combine_vec(const uint4* __restrict__ y,
                                                                const int32_t* __restrict__ row_of,
                                                                const float* __restrict__ prob, int T, int H8,
                                                                uint4* __restrict__ out) {
@@ -501,7 +504,7 @@ __global__ void __launch_bounds__(256) k_unpermute_combine_vec(const uint4* __re
     for (int q = 0; q < KV / 4; ++q) {
       const int4 r4 = __ldg(reinterpret_cast<const int4*>(row_of + (size_t)t * KV) + q);
       rj[4 * q] = r4.x, rj[4 * q + 1] = r4.y, rj[4 * q + 2] = r4.z, rj[4 * q + 3] = r4.w;
-      if (prob) {
+      if constexpr (WP) {
         const float4 p4 = __ldg(reinterpret_cast<const float4*>(prob + (size_t)t * KV) + q);
         pj[4 * q] = p4.x, pj[4 * q + 1] = p4.y, pj[4 * q + 2] = p4.z, pj[4 * q + 3] = p4.w;
       } else {
@@ -555,7 +558,7 @@ __global__ void __launch_bounds__(256) k_unpermute_combine_vec(const uint4* __re
 // contiguous bytes of a row) over the slots in ascending j, with the same
 // fmaf sequence as the kernels above.
 template <int U>
-__global__ void __launch_bounds__(256) k_combine_warp(const uint4* __restrict__ y, const int32_t* __restrict__ row_of,
+__global__ void __launch_bounds__(256, 1) k_combine_warp(const uint4* __restrict__ y, const int32_t* __restrict__ row_of,
                                                       const float* __restrict__ prob, int T, int H8, int k,
                                                       uint4* __restrict__ out) {
   const int lane = threadIdx.x & 31;
@@ -615,7 +618,7 @@ __global__ void __launch_bounds__(256) k_combine_warp(const uint4* __restrict__ 
 //                    (fp32: each lane adds its 16-byte chunks in order, then
 //                    a butterfly over the warp, so the order is fixed)
 // Pad rows get a zero dY_perm row; slots with row_of < 0 get dprob = 0.
-__global__ void __launch_bounds__(256) k_combine_bwd(const uint4* __restrict__ dout, const uint4* __restrict__ y_perm,
+__global__ void __launch_bounds__(256, 1) k_combine_bwd(const uint4* __restrict__ dout, const uint4* __restrict__ y_perm,
                                                      const int32_t* __restrict__ row_of,
                                                      const int32_t* __restrict__ tok_of,
                                                      const float* __restrict__ prob_perm,
@@ -744,10 +747,14 @@ static void launch_combine(const uint4* y, const int32_t* row_of, const float* p
     const size_t items = (size_t)T * ((H8 + NV - 1) / NV);
     size_t grid = (items + 255) / 256;
     if (grid > cap) grid = cap;
-    if (k == 8)
-      k_unpermute_combine_vec<8, NV><<<(int)grid, 256, 0, st>>>(y, row_of, prob, T, H8, out);
+    if (k == 8 && prob)
+      k_unpermute_combine_vec<8, NV, true><<<(int)grid, 256, 0, st>>>(y, row_of, prob, T, H8, out);
+    else if (k == 8)
+      k_unpermute_combine_vec<8, NV, false><<<(int)grid, 256, 0, st>>>(y, row_of, nullptr, T, H8, out);
+    else if (prob)
+      k_unpermute_combine_vec<4, NV, true><<<(int)grid, 256, 0, st>>>(y, row_of, prob, T, H8, out);
     else
-      k_unpermute_combine_vec<4, NV><<<(int)grid, 256, 0, st>>>(y, row_of, prob, T, H8, out);
+      k_unpermute_combine_vec<4, NV, false><<<(int)grid, 256, 0, st>>>(y, row_of, nullptr, T, H8, out);
   } else if (k <= 32) {
     size_t grid = ((size_t)T + 7) / 8;  // 8 tokens (warps) per CTA
     if (grid > cap) grid = cap;
