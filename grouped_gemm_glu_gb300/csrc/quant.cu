@@ -49,7 +49,7 @@ __device__ __forceinline__ void load_seg(const int32_t* counts, const int32_t* o
 constexpr int QR_TASK = 64;
 constexpr int QR_LOADS = QR_TASK / 8;
 
-__global__ void __launch_bounds__(256) k_quant_rows(const uint16_t* __restrict__ src, int G, int R, int Cc,
+__global__ void __launch_bounds__(256, 1) k_quant_rows(const uint16_t* __restrict__ src, int G, int R, int Cc,
                                                     const int32_t* __restrict__ counts,
                                                     const int32_t* __restrict__ offsets, int E,
                                                     uint8_t* __restrict__ q, uint8_t* __restrict__ s) {
