@@ -197,8 +197,12 @@ def _assert_rot_cast(q, s, sg, v, signs, what):
 SIGNS = 0x6A5D
 
 
-def test_layer_nvfp4_step_and_graph():
-    """MoeLayer in NVFP4 mode on the skewed config (small T and H).  Forward:
+@pytest.mark.parametrize("F", [1536, 1600])
+def test_layer_nvfp4_step_and_graph(F):
+    """MoeLayer in NVFP4 mode on the skewed config (small T and H; F = 1536
+    casts the weights with their scales in the tensor-core order, F = 1600 (F
+    % 128 = 64) with the plain scale layout and the direct column cast of W2,
+    a k-block of 256 ending half full).  Forward:
     the layer output against the oracle's NVFP4 chain.  Backward: dFC1 and its
     two amaxes against the oracle's dGLU on the layer's dY and saved pre; every
     NVFP4 cast against the oracle's cast of the layer's own bf16 tensor; dX,
@@ -206,7 +210,7 @@ def test_layer_nvfp4_step_and_graph():
     dx through the permute backward.  Then one captured graph replays to the
     eager results."""
     from grouped_gemm_glu_gb300.layer import MoeLayer
-    w = synth.scaled(synth.WORKLOADS["skew"], T=1024, H=512)
+    w = synth.scaled(synth.WORKLOADS["skew"], T=1024, H=512, F=F)
     inp = synth.make_inputs(w, 3)
     g = {k: (v.to(DEV) if v is not None else None) for k, v in inp.items()}
     prm = O.ActParams(O.ACT_GEGLU)
@@ -215,6 +219,7 @@ def test_layer_nvfp4_step_and_graph():
     layer.step(*args)
     torch.cuda.synchronize()
     assert ops.read_status(layer.status) == 0
+    assert layer.w4_tiled == (F % 128 == 0)
     rt = O.route(inp["topk_idx"].numpy(), 0, w.E)
     Rp = rt.R_pad
     fo = O.fc1_glu_fwd(O.permute(np_(inp["x"]), rt), O.repack_fc1(np_(inp["W1"])), None, rt, prm)
